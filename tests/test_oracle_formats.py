@@ -1,0 +1,92 @@
+"""Pins of the oracle's weight-format decoding against definitions and library conversions."""
+import numpy as np
+import pytest
+import torch
+
+from oracle.formats import bf16_bits_to_f64, blockscale_dequant, e4m3_codes_to_f64, parse_blob
+from workloads import Shape, f32_to_bf16_bits, f32_to_e4m3_codes, make_blob
+
+
+def test_bf16_closed_form_values():
+    bits = np.array([0x3F80, 0xC000, 0x0000, 0x8000, 0x7F80, 0x0001, 0x3F81], np.uint16)
+    v = bf16_bits_to_f64(bits)
+    assert v[0] == 1.0 and v[1] == -2.0 and v[2] == 0.0
+    assert np.signbit(v[3]) and v[3] == 0.0
+    assert np.isinf(v[4])
+    assert v[5] == 2.0 ** -133          # smallest subnormal
+    assert v[6] == 1.0 + 2.0 ** -7      # one ulp above 1
+
+
+def test_bf16_matches_torch_all_finite_codes():
+    codes = np.arange(1 << 16, dtype=np.uint16)
+    ours = bf16_bits_to_f64(codes)
+    t = torch.from_numpy(codes.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    fin = np.isfinite(t)
+    assert np.array_equal(ours[fin], t[fin])
+    assert np.array_equal(np.isnan(ours), np.isnan(t))
+
+
+def test_e4m3_closed_form_values():
+    v = e4m3_codes_to_f64(np.array([0x38, 0x7E, 0x01, 0x08, 0xB8, 0x7F, 0xFF, 0x00, 0x30], np.uint8))
+    assert v[0] == 1.0
+    assert v[1] == 448.0                 # max finite
+    assert v[2] == 2.0 ** -9             # smallest subnormal
+    assert v[3] == 2.0 ** -6             # smallest normal
+    assert v[4] == -1.0
+    assert np.isnan(v[5]) and np.isnan(v[6])
+    assert v[7] == 0.0
+    assert v[8] == 0.5
+
+
+def test_e4m3_matches_torch_all_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    ours = e4m3_codes_to_f64(codes)
+    t = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(ours), np.isnan(t))
+    fin = ~np.isnan(t)
+    assert np.array_equal(ours[fin], t[fin])
+
+
+def test_generator_e4m3_encoder_matches_torch_rounding():
+    g = np.random.default_rng(5)
+    a = np.concatenate([g.standard_normal(200000).astype(np.float32) * 50,
+                        g.standard_normal(20000).astype(np.float32) * 0.01,
+                        np.array([448, -448, 0.0, 2 ** -10, 3 * 2 ** -10, 1.0625, 1.1875], np.float32)])
+    ours = f32_to_e4m3_codes(a)
+    t = torch.from_numpy(a).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    inr = np.abs(a) <= 448
+    assert np.array_equal(ours[inr], t[inr])
+
+
+def test_generator_bf16_rounding_matches_torch():
+    a = np.random.default_rng(6).standard_normal(100000).astype(np.float32)
+    ours = f32_to_bf16_bits(a)
+    t = torch.from_numpy(a).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, t)
+
+
+def test_blockscale_indexing_is_row_block_major():
+    # all codes = 1.0; scale of block (rb, cb) = 10*rb + cb + 1 -> dequant shows the grid
+    codes = np.full((256, 384), 0x38, np.uint8)
+    scales = np.array([[10 * rb + cb + 1 for cb in range(3)] for rb in range(2)], np.float32)
+    d = blockscale_dequant(codes, scales)
+    assert d[0, 0] == 1 and d[127, 127] == 1
+    assert d[0, 128] == 2 and d[0, 383] == 3
+    assert d[128, 0] == 11 and d[255, 383] == 13
+
+
+@pytest.mark.parametrize("wdtype", ["f32", "bf16", "fp8"])
+def test_parse_blob_roundtrip(wdtype):
+    sh = Shape(L=1, E=1, k=1, H=256, I=128, wdtype=wdtype, adtype="f32")
+    blob = make_blob(sh, 7, 0)
+    wg, wu, wd = parse_blob(blob, wdtype, sh.H, sh.I)
+    assert wg.shape == (128, 256) and wu.shape == (128, 256) and wd.shape == (256, 128)
+    # regenerate the float32 draws the generator quantised and compare within the format's step
+    from workloads import _rng
+    g = _rng(7, 0xB10B, 0)
+    gu = g.standard_normal((256, 256), dtype=np.float32) * np.float32(0.02)
+    d = g.standard_normal((256, 128), dtype=np.float32) * np.float32(0.02)
+    rel = {"f32": 0.0, "bf16": 2 ** -8, "fp8": 2 ** -3}[wdtype]
+    assert np.allclose(wg, gu[:128], rtol=rel, atol=1e-3 * (wdtype == "fp8"))
+    assert np.allclose(wu, gu[128:], rtol=rel, atol=1e-3 * (wdtype == "fp8"))
+    assert np.allclose(wd, d, rtol=rel, atol=1e-3 * (wdtype == "fp8"))
