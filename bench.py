@@ -1,0 +1,414 @@
+#!/usr/bin/env python
+"""Benchmark of the expert-slot-cache MoE decode step on GB300.
+
+Workload: Qwen3-30B-A3B-shaped decode (48 MoE layers, 128 experts, top-8,
+hidden 2048, expert intermediate 768, bf16 weights, batch 1), cache of 37% of
+the 6144 (layer, expert) slots, Zipf(1.1) routing with 80% step-to-step reuse.
+One bench step = one decode token through all 48 MoE layers: per layer the
+control kernel, the slot fills on the side stream, the grouped SwiGLU GEMV
+over resident and filled experts, and the combine with supplied CPU partial
+sums.  Metric: MoE-layer decode steps per second (48 per bench step).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs an independent replica on its own GPU (the path
+has no exchange step on one node: replicas only), the timed region is bracketed
+by barriers, and rank 0 prints one JSON line with the max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from workloads import (activations, config, default_max_fetch, make_blob, make_pool,  # noqa: E402
+                       prefill_routing, routing_trace)
+
+WORKLOAD = "qwen3_decode_b1"
+METRIC = "MoE-layer decode steps/s"
+UNIT = "layer-steps/s"
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=256)
+    p.add_argument("--warmup", type=int, default=8)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--pool-blobs", type=int, default=64, help="distinct expert blobs in the host arena")
+    p.add_argument("--no-graph", action="store_true", help="launch eagerly instead of replaying a CUDA graph")
+    p.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the oracle CPU baseline")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-prefill", action="store_true")
+    p.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
+    return p.parse_args(argv)
+
+
+# ----------------------------------------------------------------------------
+# measured peaks and clocks
+# ----------------------------------------------------------------------------
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        hbm = d.get("hbm_gbs") or d.get("hbm_GBs")
+        bf16 = d.get("bf16_tflops")
+        bf16_s = d.get("bf16_tflops_sustained", bf16)
+        if hbm:
+            return float(hbm), float(bf16 or 1900.0), float(bf16_s or 1700.0), "of measured"
+    return 6800.0, 1900.0, 1700.0, "of fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], 0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# the oracle as CPU baseline (runs in a fresh interpreter: no fork after CUDA init)
+# ----------------------------------------------------------------------------
+def cpu_worker(seconds: float, pool_blobs: int, bw):
+    """Oracle control + float64 SwiGLU on successive layer-steps of the workload until the budget ends."""
+    from oracle.cache import SlotCache
+    from oracle.ffn import combine, swiglu_expert
+    from oracle.formats import activations_to_f64, parse_blob
+    cfg = config(WORKLOAD)
+    s = cfg.shape
+    ids, w = routing_trace(cfg)
+    K = default_max_fetch(s, cfg.T)
+    ora = SlotCache(s.L, s.E, cfg.capacity, K, bw[0], bw[1])
+    blobs = {}
+    t0 = time.perf_counter()
+    n = 0
+    st = 0
+    while time.perf_counter() - t0 < seconds:
+        for l in range(s.L):
+            plan = ora.decode(l, ids[st % cfg.steps, l])
+            x = activations_to_f64(activations(cfg, st % cfg.steps, l), s.adtype)
+            y = np.zeros((cfg.T, s.k, s.H))
+            for t in range(cfg.T):
+                for j in range(s.k):
+                    f = l * s.E + int(ids[st % cfg.steps, l, t, j])
+                    p = f % pool_blobs
+                    if p not in blobs:
+                        blobs[p] = parse_blob(make_blob(s, cfg.seed, p), s.wdtype, s.H, s.I)
+                    y[t, j] = swiglu_expert(x[t], *blobs[p])
+            combine(w[st % cfg.steps, l], y, plan.slot_map, y)
+            n += 1
+            if time.perf_counter() - t0 >= seconds:
+                break
+        st += 1
+    dt = time.perf_counter() - t0
+    print(json.dumps({"layer_steps": n, "seconds": dt}))
+
+
+def run_cpu_baseline(seconds: float, pool_blobs: int, bw):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-worker", "--cpu-seconds", str(seconds),
+           "--pool-blobs", str(pool_blobs)]
+    env["BENCH_BW"] = f"{bw[0]},{bw[1]}"
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=seconds * 4 + 120)
+    line = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    if r.returncode != 0 or not line:
+        return None
+    d = json.loads(line[-1])
+    return {"value": d["layer_steps"] / d["seconds"], "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{d['layer_steps']} layer-steps of {WORKLOAD} from step 0 (list-LRU control + "
+                      f"float64 SwiGLU per routed pair + fixed-order combine), one thread, "
+                      f"{d['seconds']:.1f} s"}
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+def main(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    if args.impl == "reference":
+        return reference_arm(args, world, rank)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from serving_layer_moe_gb300 import MoECache, bench_bw
+
+    cfg = config(WORKLOAD)
+    s = cfg.shape
+    # calibration: B_P through the fill path, B_H host read; B_cpu = residual
+    bp_gbs, bh_gbs, rec = bench_bw(local, s.blob_bytes)
+    b_pcie = max(1, int(bp_gbs * 1000))
+    b_cpu = max(0, int(bh_gbs * 1000) - b_pcie)
+
+    arena, offs = make_pool(s, cfg.seed, n_phys=args.pool_blobs)
+    pool = torch.from_numpy(arena).pin_memory()
+    del arena
+    K = default_max_fetch(s, cfg.T)
+    cache = MoECache(L=s.L, E=s.E, H=s.H, I=s.I, top_k=s.k, max_tokens=cfg.T, wdtype=s.wdtype,
+                     adtype=s.adtype, host_pool=pool, blob_offsets=offs, n_slots=cfg.capacity,
+                     max_fetch=K, bw_pcie_mbps=b_pcie, bw_cpu_mbps=b_cpu, device=local)
+
+    ids, w = routing_trace(cfg)
+    xs = np.stack([np.stack([activations(cfg, st, l) for l in range(s.L)]) for st in range(cfg.steps)])
+    x_all = torch.from_numpy(xs.view(np.int16)).to(dev)            # [steps, L, T, H] bf16 bits
+    ids_all = torch.from_numpy(ids).to(dev)                         # [steps, L, T, k]
+    w_all = torch.from_numpy(w).to(dev)
+    xb = torch.empty_like(x_all[0])
+    ib = torch.empty_like(ids_all[0])
+    wb = torch.empty_like(w_all[0])
+    out = torch.empty(s.L, cfg.T, s.H, dtype=torch.float32, device=dev)
+    cpu_part = torch.zeros(cfg.T, s.k, s.H, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    sp = stream.cuda_stream
+    layer_bytes = [(xb[l].data_ptr(), ib[l].data_ptr(), wb[l].data_ptr(), out[l].data_ptr()) for l in range(s.L)]
+
+    def enqueue_step():
+        for l in range(s.L):
+            xp, ip, wp, op = layer_bytes[l]
+            cache.decode_ptrs(l, cfg.T, xp, ip, wp, cpu_part.data_ptr(), op, None, sp)
+
+    def stage(st):
+        xb.copy_(x_all[st % cfg.steps], non_blocking=True)
+        ib.copy_(ids_all[st % cfg.steps], non_blocking=True)
+        wb.copy_(w_all[st % cfg.steps], non_blocking=True)
+
+    step = 0
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            stage(step)
+            enqueue_step()
+            step += 1
+    torch.cuda.synchronize(dev)
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            enqueue_step()
+        torch.cuda.synchronize(dev)
+
+    launches_per_layer = 7
+    # ---- timed region: inputs resident in HBM ---------------------------------
+    cnt0 = cache.state()[3].copy()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk, torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            stage(step)
+            if graph is not None:
+                graph.replay()
+            else:
+                enqueue_step()
+            step += 1
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        dist.barrier()
+    cnt1 = cache.state()[3].copy()
+    layer_steps = args.steps * s.L * world
+    value = layer_steps / (ms / 1e3)
+
+    # ---- end to end: host buffers in, result out, every step ------------------------
+    x_h = torch.from_numpy(xs.view(np.int16)).pin_memory()
+    ids_h = torch.from_numpy(ids).pin_memory()
+    w_h = torch.from_numpy(w).pin_memory()
+    out_h = torch.empty(s.L, cfg.T, s.H, dtype=torch.float32).pin_memory()
+    e2e_steps = max(8, args.steps // 2)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    e2 = torch.cuda.Event(enable_timing=True)
+    e3 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e2.record(stream)
+        for _ in range(e2e_steps):
+            st = step % cfg.steps
+            xb.copy_(x_h[st], non_blocking=True)
+            ib.copy_(ids_h[st], non_blocking=True)
+            wb.copy_(w_h[st], non_blocking=True)
+            if graph is not None:
+                graph.replay()
+            else:
+                enqueue_step()
+            out_h.copy_(out, non_blocking=True)
+            step += 1
+        e3.record(stream)
+        torch.cuda.synchronize(dev)
+    ms_e2e = e2.elapsed_time(e3)
+    if world > 1:
+        t = torch.tensor([ms_e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+    h2d = xb.numel() * 2 + ib.numel() * 4 + wb.numel() * 4
+    d2h = out.numel() * 4
+
+    # ---- kernel timing for the roofline (library CUDA events, eager launches) ----------
+    prof_steps = 32
+    cnt_p0 = cache.state()[3].copy()
+    cache.profile_start()
+    with torch.cuda.stream(stream):
+        for _ in range(prof_steps):
+            stage(step)
+            enqueue_step()
+            step += 1
+    prof = cache.profile_stop()
+    cnt_p1 = cache.state()[3].copy()
+    hbm_peak, bf16_peak, bf16_sust, peak_src = measured_peaks()
+    gpu_experts = int((cnt_p1[0] - cnt_p0[0]) + (cnt_p1[2] - cnt_p0[2]))   # hits + fills executed
+    gemv_bytes = gpu_experts * s.blob_bytes
+    gemv_ms = prof["gemv_resident"][0] + prof["gemv_filled"][0]
+    gemv_launches = prof["gemv_resident"][1] + prof["gemv_filled"][1]
+    fill_bytes = int(cnt_p1[2] - cnt_p0[2]) * s.blob_bytes
+    total_prof_ms = sum(v[0] for v in prof.values())
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD}: Qwen3-30B-A3B-shaped decode, 48 MoE layers x 128 experts, "
+                               f"top-8, H 2048, I 768, bf16 weights, batch 1, C={cfg.capacity} slots (37%), "
+                               f"Zipf(1.1) routing with 80% reuse; one step = 48 MoE-layer decodes",
+                   "global_batch": cfg.T * world, "parallelism": f"replicas x{world}",
+                   "B_pcie_mbps": b_pcie, "B_cpu_mbps": b_cpu, "B_H_gbs": round(bh_gbs, 1),
+                   "recommend_hybrid": rec, "K": K,
+                   "host_pool": f"{args.pool_blobs} distinct seeded expert blobs in a page-locked arena, "
+                                f"flat id f -> blob f mod {args.pool_blobs}",
+                   "graph": graph is not None,
+                   "l2": "inputs larger than L2: each step reads ~48 x 8 x 9.4 MB of expert weights"},
+        "cache_stats": {"hits": int(cnt1[0] - cnt0[0]), "misses": int(cnt1[1] - cnt0[1]),
+                        "fills": int(cnt1[2] - cnt0[2]), "cpu_assigned": int(cnt1[3] - cnt0[3]),
+                        "read_miss_rate": round(float(cnt1[5] - cnt0[5]) / max(1, float(cnt1[4] + cnt1[5] - cnt0[4] - cnt0[5])), 4)},
+        "e2e": {"value": round(e2e_steps * s.L * world / (ms_e2e / 1e3), 1), "unit": UNIT,
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": args.steps * s.L * launches_per_layer,
+        "roofline": {"bound": "hbm", "kernel": "expert GEMV (gate/up + down) over resident and filled slots",
+                     "achieved": round(gemv_bytes / (gemv_ms / 1e3) / 1e9, 1) if gemv_ms > 0 else None,
+                     "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(gemv_bytes / (gemv_ms / 1e3) / 1e9 / hbm_peak, 3) if gemv_ms > 0 else None,
+                     "peak_source": peak_src, "traffic": None,
+                     "bytes_per_launch": round(gemv_bytes / max(1, gemv_launches)),
+                     "launches_timed": gemv_launches},
+        "kernel_ms_share": {k: round(v[0] / total_prof_ms, 3) for k, v in prof.items() if v[1]},
+        "fill": {"achieved_gbs": round(fill_bytes / (prof["fill"][0] / 1e3) / 1e9, 1) if prof["fill"][0] > 0 else None,
+                 "bench_bw_B_P_gbs": round(bp_gbs, 1), "note": "fill kernel time includes waiting for nothing; "
+                 "it runs on the side stream concurrently with the resident-expert GEMV"},
+        "control_us": round(1e3 * prof["control"][0] / max(1, prof["control"][1]), 2),
+        "clocks": clk.summary(),
+    }
+    if not args.no_prefill:
+        result["prefill"] = prefill_measure(args, dev, local)
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = run_cpu_baseline(args.cpu_seconds, args.pool_blobs, (b_pcie, b_cpu))
+    if rank == 0:
+        print(json.dumps(result))
+    cache.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def prefill_measure(args, dev, local):
+    """Prefill chunk: 8192 tokens through 48 layers with full-layer double buffering (if built)."""
+    return None
+
+
+def reference_arm(args, world, rank):
+    """The oracle as the reference arm: bounded samples of the same workload on host cores."""
+    if rank != 0:
+        return
+    b = os.environ.get("BENCH_BW", "200000,100000").split(",")
+    bw = (int(b[0]), int(b[1]))
+    per_step = max(2.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    vals = []
+    for i in range(args.warmup + args.steps):
+        r = run_cpu_baseline(per_step, args.pool_blobs, bw)
+        if r and i >= args.warmup:
+            vals.append(r["value"])
+    v = statistics.mean(vals) if vals else None
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{WORKLOAD} (oracle: list-LRU control + float64 SwiGLU)"},
+            "cpu_baseline": {"value": v, "unit": UNIT, "kind": "oracle", "cores": 1,
+                             "sample": f"{per_step:.0f} s of oracle layer-steps per bench step, one thread"},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    a = parse_args()
+    if a.cpu_worker:
+        b = os.environ.get("BENCH_BW", "200000,100000").split(",")
+        cpu_worker(a.cpu_seconds, a.pool_blobs, (int(b[0]), int(b[1])))
+    else:
+        main(a)

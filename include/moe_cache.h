@@ -1,0 +1,231 @@
+/*
+ * moe_cache.h -- C ABI of libmoecache.so: one MoE layer over a global cache of
+ * complete (layer, expert) slots in GPU memory, for one GB300 (sm_103a).
+ *
+ * What the library computes (FreeToken, as described on four web pages):
+ *
+ *  - The complete routed-expert pool lives in host memory and is the source of
+ *    truth; the GPU memory set aside for experts is ONE least-recently-used
+ *    cache of complete (layer, expert) slots, every bank indexed by the flat
+ *    id f = layer * E + expert.  (snackonai deep dive "FreeToken, or why your
+ *    laptop was never the bottleneck", sections "What It Actually Does" and
+ *    "The Architecture, Unpacked".)
+ *  - Per decode layer one device-side control kernel dedups the routed
+ *    experts, classifies them against the residency table, derives the miss
+ *    split q, surfaces the K least-recently-used victim slots in one pass and
+ *    rewrites expert ids into slot ids or a CPU flag, with no host sync.
+ *    (same page, "The Architecture, Unpacked", decision three; ai.thesatyajit
+ *    article "FreeToken: a 753B model on one GPU ...", section "Residency that
+ *    follows the router", last paragraph.)
+ *  - The split: q* = round(m * B_pcie / (B_pcie + B_cpu)) with B_cpu the
+ *    residual host bandwidth B_H - B_P, rounded half to even, then
+ *    max(1, min(q*, m)) when m > 0, then capped by K and by the evictable
+ *    slots.  (snackonai, "The split policy itself"; thesatyajit, "Decode: the
+ *    one equation".)
+ *  - Hits and filled experts run as grouped SwiGLU work on the GPU; fills
+ *    copy complete experts host -> GPU on a side stream; the combine merges
+ *    the GPU partial sums with caller-supplied partial sums of CPU-assigned
+ *    experts, weighted by the router gates, in fixed top-k order.
+ *    (snackonai, "The split policy itself", closing note; "What It Actually
+ *    Does": the partial sums merge exactly.)
+ *  - Prefill: two full-layer buffers out of the same slot pool; while layer l
+ *    computes, a transfer stream loads all experts of layer l+1; on-demand
+ *    loading when two layers do not fit.  (thesatyajit, "Prefill: hide the
+ *    pool behind the wire"; snackonai, decision two.)
+ *  - Resize: rebuild the cache for a new slot count without touching the
+ *    host pool.  (snackonai, "Resizing the cache without a restart";
+ *    thesatyajit, "Elastic memory, because the machine is not yours".)
+ *  - Calibration: measure B_P (host -> GPU expert transfer) and B_H (host
+ *    expert read) and recommend the hybrid backend iff B_H > 2 * B_P.
+ *    (snackonai, "Calibration decides the backend, not the GPU".)
+ *
+ * Conventions for every call:
+ *  - Device pointers ("_dev") are caller-owned device memory of the cache's
+ *    device; host pointers ("_host") are caller-owned host memory.  The
+ *    library owns the slot pool, its tables, streams and events.
+ *  - Returns a moe_status; on failure moe_last_error() gives a message
+ *    (thread-local, valid until the next call on the same thread).
+ *  - A decode or prefill call only enqueues work on the caller's stream (a
+ *    cudaStream_t passed as void*, NULL = legacy default stream) and never
+ *    blocks the host.  Every other call synchronises the library's streams.
+ *  - Range violations the GPU detects (an expert id outside [0, E), a
+ *    CPU-assigned pair with no CPU partial sums) set an error word; the next
+ *    call on the cache returns MOE_EDEVICE and clears it.  The affected
+ *    outputs are left defined (id -> CPU flag, missing partial -> 0).
+ *  - Not thread-safe per cache: one caller thread at a time.
+ */
+#ifndef MOE_CACHE_H
+#define MOE_CACHE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct moe_cache moe_cache;   /* opaque; created and freed by the library */
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_EINVAL = 1,     /* a bad argument (shape, pointer, layer, T, config) */
+  MOE_ENOMEM = 2,     /* device or pinned host allocation failed */
+  MOE_ECUDA = 3,      /* a CUDA runtime error (message has the CUDA error string) */
+  MOE_ECAPACITY = 4,  /* the slot pool cannot hold what the call needs */
+  MOE_EBUSY = 5,      /* reserved: a safe-point call while work is in flight */
+  MOE_EDEVICE = 6     /* the GPU flagged a range violation in an earlier call */
+} moe_status;
+
+typedef enum moe_dtype {
+  MOE_F32 = 0,            /* IEEE binary32 */
+  MOE_BF16 = 1,           /* bfloat16 */
+  MOE_FP8E4M3_B128 = 2    /* OCP e4m3 codes with one fp32 scale per 128x128 block */
+} moe_dtype;
+
+/*
+ * Expert blob ("bank layout"), S bytes, one per flat id, 16-byte aligned:
+ *   W_gu [2I, H] row-major in wdtype (rows 0..I-1 gate, rows I..2I-1 up),
+ *   W_d  [H, I]  row-major in wdtype,
+ *   MOE_FP8E4M3_B128 only: s_gu [2I/128, H/128] fp32, s_d [H/128, I/128] fp32.
+ * S = 3*I*H*sizeof(w) (+ 4*(2I*H + H*I)/16384 for fp8).  H and I must be
+ * multiples of 128 (fp8) or 8 (f32, bf16).
+ */
+typedef struct moe_config {
+  int32_t n_layers;       /* L */
+  int32_t n_experts;      /* E routed experts per layer (1..4096) */
+  int32_t hidden;         /* H */
+  int32_t inter;          /* I, SwiGLU intermediate size */
+  int32_t top_k;          /* k (1..E) */
+  int32_t max_tokens;     /* largest T of a decode call (1..1024) */
+  int32_t max_fetch;      /* K: fills per layer per call; < 0 = min(E, max_tokens * k) */
+  int32_t wdtype;         /* moe_dtype of the expert weights */
+  int32_t adtype;         /* activations: MOE_F32 or MOE_BF16 (prefill needs MOE_BF16 + bf16 weights) */
+  int32_t n_shared;       /* 0, or 1 always-resident shared expert per layer (gate 1.0) */
+  uint32_t bw_pcie_mbps;  /* B_pcie in MB/s (> 0 unless bw_cpu_mbps > 0) */
+  uint32_t bw_cpu_mbps;   /* B_cpu = B_H - B_P in MB/s; 0 = offload mode (every miss fills, up to K) */
+  int32_t device;         /* CUDA device ordinal */
+  int32_t max_prefill_tokens; /* largest T of a prefill call; 0 = prefill disabled */
+} moe_config;
+
+/*
+ * Create a cache of n_slots slots on cfg->device.
+ *   host_pool       caller-owned host memory holding the expert blobs; the
+ *                   caller keeps it alive and unchanged until destroy.  If it
+ *                   is not page-locked already the library registers it
+ *                   (mapped, read-only) and unregisters it at destroy.
+ *   host_pool_bytes its size.
+ *   blob_offsets    L*E byte offsets (host array, copied), blob f at
+ *                   host_pool + blob_offsets[f]; each a multiple of 16 and
+ *                   offset + S <= host_pool_bytes.  NULL = dense, f * S.
+ *   shared_host     n_shared == 1: L shared-expert blobs back to back (host,
+ *                   copied to GPU memory at create); otherwise NULL.
+ *   n_slots         C >= 1 and < 2^20.  Slots start empty (cold start).
+ * Errors: MOE_EINVAL (config), MOE_ENOMEM, MOE_ECUDA.
+ */
+moe_status moe_cache_create(const moe_config* cfg, const void* host_pool, uint64_t host_pool_bytes,
+                            const uint64_t* blob_offsets, const void* shared_host, uint64_t n_slots,
+                            moe_cache** out);
+
+/* Free everything the cache owns (synchronises its streams first).  NULL is a no-op. */
+moe_status moe_cache_destroy(moe_cache* cache);
+
+/*
+ * Safe-point rebuild for n_slots slots: keeps the min(n_slots, resident) most
+ * recently used experts, packed into slots 0.. in ascending old-slot order
+ * with their recency; the other slots start empty.  Synchronises the device.
+ * Errors: MOE_EINVAL (n_slots == 0 or >= 2^20), MOE_ENOMEM (old pool is kept).
+ */
+moe_status moe_cache_resize(moe_cache* cache, uint64_t n_slots);
+
+/*
+ * One MoE layer of decode for T tokens (0 <= T <= max_tokens), enqueued on `stream`.
+ *   x_dev        [T, H] in adtype
+ *   topk_ids_dev [T, k] int32 routed expert ids of this layer (0..E-1, distinct per token)
+ *   topk_w_dev   [T, k] fp32 router gates
+ *   cpu_part_dev [T, k, H] fp32 unweighted outputs of the CPU-assigned pairs, read
+ *                only where the slot map says CPU; may be NULL when no pair can be
+ *                CPU-assigned (offload mode with K >= k*T and enough slots)
+ *   out_dev      [T, H] fp32: sum_j w[t,j] * y[t,j] in j order (+ shared expert)
+ *   slot_map_dev [T, k] int32 out, may be NULL: the slot each pair ran from, -1 = CPU
+ * Errors: MOE_EINVAL, MOE_EDEVICE (earlier violation), MOE_ECUDA.
+ */
+moe_status moe_layer_decode(moe_cache* cache, int32_t layer, int32_t T, const void* x_dev,
+                            const int32_t* topk_ids_dev, const float* topk_w_dev,
+                            const float* cpu_part_dev, float* out_dev, int32_t* slot_map_dev,
+                            void* stream);
+
+/*
+ * One MoE layer of a prefill chunk of T tokens (1 <= T <= max_prefill_tokens), bf16
+ * activations and bf16 weights.  Full-layer mode (C >= 2E): makes layer `layer`
+ * resident, starts loading all of layer+1 on the transfer stream, runs the grouped
+ * GEMM on `stream`, and marks the layer's E experts used.  C < 2E: loads the routed
+ * experts of the layer on demand, at most C at a time.
+ *   x_dev [T, H] bf16, topk_ids_dev / topk_w_dev [T, k], out_dev [T, H] fp32 (overwritten).
+ * Errors: MOE_EINVAL, MOE_EDEVICE, MOE_ECUDA.
+ */
+moe_status moe_layer_prefill(moe_cache* cache, int32_t layer, int32_t T, const void* x_dev,
+                             const int32_t* topk_ids_dev, const float* topk_w_dev, float* out_dev,
+                             void* stream);
+
+/*
+ * Copy the residency state to host arrays (synchronises the device); any pointer may be NULL.
+ *   slot_to_expert_host [C] int32 (-1 = empty), stamps_host [C] uint64 (0 = empty; a
+ *   larger stamp = more recently used), expert_to_slot_host [L*E] int32 (-1 = not resident),
+ *   counters_host [8] uint64: unique hits, unique misses, fills, CPU-assigned, pair reads
+ *   that hit, pair reads that missed, decode calls, experts loaded by prefill;
+ *   clock_host: the last stamp handed out.
+ */
+moe_status moe_cache_get_state(moe_cache* cache, int32_t* slot_to_expert_host, uint64_t* stamps_host,
+                               int32_t* expert_to_slot_host, uint64_t* counters_host,
+                               uint64_t* clock_host);
+
+/*
+ * The last decode call's plan (synchronises the device); any pointer may be NULL.
+ *   scalars_host [8] int32: layer, unique u, hits h, misses m, fills q, CPU-assigned,
+ *                GPU experts run (h + q + shared), 0.
+ *   victims_host [K] int32: the K least-recently-used evictable slots in eviction
+ *                order (key (stamp, slot) ascending, this call's hits excluded), -1 padded.
+ *   fills_host   [2K] int32: (flat id, slot) of the q fills, in fill order.
+ *   y_host       [T, k, H] fp32: the GPU partial sum of each GPU-run pair (unweighted),
+ *                undefined for CPU-assigned pairs.
+ */
+moe_status moe_cache_get_plan(moe_cache* cache, int32_t* scalars_host, int32_t* victims_host,
+                              int32_t* fills_host, float* y_host);
+
+/*
+ * Sizes of a cache: info_host[8] uint64: slot bytes S, slots C, K, L*E,
+ * device bytes held, host pool bytes, 0, 0.
+ */
+moe_status moe_cache_info(moe_cache* cache, uint64_t* info_host);
+
+/*
+ * Kernel timing.  enable = 1: start recording a CUDA event pair around every kernel
+ * group the cache launches (events are created on demand, so do not start profiling
+ * while a stream is being captured).  enable = 0: stop, synchronise, and return per
+ * kind the summed milliseconds and the number of timed groups since the start, kinds
+ * 0 control, 1 fill, 2 GEMV of resident experts, 3 GEMV of filled experts, 4 combine,
+ * 5 prefill control, 6 prefill load, 7 prefill grouped GEMM.  ms_host[8] and
+ * launches_host[8] may be NULL.
+ */
+moe_status moe_cache_profile(moe_cache* cache, int32_t enable, double* ms_host, uint64_t* launches_host);
+
+/*
+ * Calibrate on `device` with expert-sized blobs of expert_bytes (rounded up to 16).
+ *   b_pcie_gbs         B_P: host -> GPU expert transfer, GB/s (1e9 B/s), through the
+ *                      library's own fill path (SM copy from page-locked host memory)
+ *   b_host_gbs         B_H: host-side expert read bandwidth, GB/s (all host threads
+ *                      streaming the pool, the bytes an in-place CPU expert reads)
+ *   recommend_hybrid   1 iff B_H > 2.0 * B_P, else 0
+ * Any output may be NULL.  Allocates and frees its own buffers.  Synchronises.
+ */
+moe_status bench_bw(int32_t device, uint64_t expert_bytes, double* b_pcie_gbs, double* b_host_gbs,
+                    int32_t* recommend_hybrid);
+
+/* The message of the last failed call on this thread ("" if none). */
+const char* moe_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_CACHE_H */

@@ -1,0 +1,104 @@
+// The cache object shared by the translation units of libmoecache.so.
+#pragma once
+
+#include "internal.cuh"
+
+#include <cuda.h>
+
+#include <vector>
+
+// set the thread's last error message and return `st`
+moe_status fail(moe_status st, const char* fmt, ...);
+
+#define CK(call)                                                                      \
+  do {                                                                                \
+    cudaError_t e_ = (call);                                                          \
+    if (e_ != cudaSuccess)                                                            \
+      return fail(e_ == cudaErrorMemoryAllocation ? MOE_ENOMEM : MOE_ECUDA, "%s: %s", \
+                  #call, cudaGetErrorString(e_));                                     \
+  } while (0)
+
+using namespace moe;
+
+struct DeviceGuard {
+  int prev = -1;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != dev) cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+// ---------------------------------------------------------------------------
+// the cache object
+// ---------------------------------------------------------------------------
+struct moe_cache {
+  moe_config cfg{};
+  Shape sh{};
+  int K = 0;
+  uint64_t C = 0;
+  int sms = 0;
+  int gemv_grid = 0;
+  int fill_ctas = 0;
+  // host pool
+  const uint8_t* host_pool = nullptr;
+  const uint8_t* host_pool_dev = nullptr;
+  uint64_t host_bytes = 0;
+  bool registered_here = false;
+  // device memory
+  uint8_t* slots = nullptr;
+  uint8_t* shared = nullptr;
+  uint64_t* offsets = nullptr;
+  CacheTables tab{};
+  DecodeBufs b{};
+  void* work = nullptr;            // one allocation behind DecodeBufs
+  uint64_t dev_bytes = 0;
+  int last_T = 0;
+  // error word (page-locked, mapped)
+  uint32_t* err_host = nullptr;
+  uint32_t* err_dev = nullptr;
+  // streams / events
+  cudaStream_t fill_stream = nullptr;
+  cudaEvent_t ev_ctrl = nullptr, ev_fill = nullptr;
+  // prefill state (prefill.cu)
+  void* prefill = nullptr;
+  // kernel timing (moe_cache_profile)
+  bool profiling = false;
+  std::vector<cudaEvent_t> prof_events;     // pairs, created outside any capture
+  std::vector<int> prof_kind;               // kind of each pair
+  size_t prof_used = 0;
+};
+
+// Record a start/stop event pair around a kernel group of `kind` when profiling.
+struct ProfScope {
+  moe_cache* c;
+  cudaStream_t s;
+  size_t idx = (size_t)-1;
+  ProfScope(moe_cache* c_, cudaStream_t s_, int kind) : c(c_), s(s_) {
+    if (!c->profiling) return;
+    if (c->prof_used * 2 + 2 > c->prof_events.size()) {
+      for (int i = 0; i < 256; ++i) {
+        cudaEvent_t e;
+        if (cudaEventCreate(&e) != cudaSuccess) { c->profiling = false; return; }
+        c->prof_events.push_back(e);
+      }
+      c->prof_kind.resize(c->prof_events.size() / 2);
+    }
+    idx = c->prof_used++;
+    c->prof_kind[idx] = kind;
+    cudaEventRecord(c->prof_events[2 * idx], s);
+  }
+  ~ProfScope() {
+    if (idx != (size_t)-1) cudaEventRecord(c->prof_events[2 * idx + 1], s);
+  }
+};
+
+namespace moe {
+// prefill.cu
+moe_status prefill_init(moe_cache* c);
+void prefill_free(moe_cache* c);
+}  // namespace moe
+

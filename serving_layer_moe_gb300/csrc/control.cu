@@ -1,0 +1,402 @@
+// Routing-control kernel of one decode MoE layer (one CTA, no host sync).
+//
+// Follows the snackonai deep dive "FreeToken, or why your laptop was never the
+// bottleneck", section "The Architecture, Unpacked" (decision three: one
+// kernel per MoE layer dedups the routed experts, classifies them against the
+// residency table, derives q, picks victims and rewrites logical ids into
+// physical slot ids or a CPU flag; victim selection is one pass that surfaces
+// the K least recently used slots) and section "The split policy itself"
+// (q* = round(m B_P / B_H), clamp max(1, min(q, m)), the first q misses fill).
+// Recency follows ai.thesatyajit.com "FreeToken: a 753B model on one GPU ...",
+// section "Residency that follows the router": a hit refreshes recency, a
+// fill admits, an eviction removes the least recently demanded entry.
+//
+// Readings (the pages leave these open):
+//   * B_H = B_pcie + B_cpu, so q* = round_half_even(m B_pcie / (B_pcie + B_cpu))
+//     in exact integer arithmetic; the clamp applies when m > 0; q is then
+//     capped by K and by the evictable slots V = C - hits.
+//   * Misses fill in ascending flat id; the i-th fill takes the i-th victim.
+//   * LRU key of a slot = (stamp, slot); an empty slot has stamp 0; slots that
+//     hold one of this call's hits are not evictable.  Victims = the K
+//     smallest keys, ascending.
+//   * After the rewrite every expert that runs on the GPU (hits, fills) is
+//     stamped in ascending flat id with the next values of one global clock;
+//     CPU-assigned experts are not touched.
+//
+// Design for one SM: the routed set is a bitmap over E experts in shared
+// memory (dedup = atomicOr, order = popcount prefix); hit/miss ranks come from
+// warp ballots; the K smallest of C 64-bit keys come from an MSB radix select
+// with 8-bit digits (a 256-bin shared histogram per digit, only the digits the
+// current clock can reach), after which the K survivors are ranked by
+// comparison.  Cost is a few passes over the stamp array regardless of how
+// many misses occurred.
+#include "internal.cuh"
+
+namespace moe {
+
+namespace {
+
+struct CtrlArgs {
+  int layer, T, k, E, C, K, n_shared;
+  uint32_t bp, bc;
+  uint64_t S;
+  const int32_t* ids;
+  CacheTables tab;
+  DecodeBufs b;
+  int32_t* slot_map_out;
+  const uint8_t* slots_base;
+  const uint8_t* shared_blob;   // this layer's shared expert, or null
+  uint32_t* err;
+  int umax;                     // min(E, T*k)
+};
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// round_half_even(m * bp / (bp + bc)) on integers (bp + bc > 0)
+__device__ __forceinline__ uint32_t q_star(uint32_t m, uint32_t bp, uint32_t bc) {
+  const uint64_t num = (uint64_t)m * bp;
+  const uint64_t den = (uint64_t)bp + bc;
+  uint64_t q = num / den;
+  const uint64_t r = num - q * den;
+  if (2 * r > den) q += 1;
+  else if (2 * r == den) q += (q & 1);
+  return (uint32_t)q;
+}
+
+// shared scalars of the control CTA
+struct CtrlScalars {
+  int bad, u, h, m, q, keff, ngpu, ntouch, ncand, digit, kth, read_hits, read_misses;
+  unsigned long long clock0;
+};
+
+__global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ CtrlScalars sc;
+  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31;
+  const int NW = (a.E + 31) >> 5;
+  const int P = a.T * a.k;
+  const int U = a.umax;
+
+  // shared layout
+  uint32_t* ebits = reinterpret_cast<uint32_t*>(smem);       // [NW]
+  uint32_t* ebase = ebits + NW;                                // [NW + 1]
+  int32_t* uniq_e = reinterpret_cast<int32_t*>(ebase + NW + 1);// [U]
+  int32_t* uniq_slot = uniq_e + U;                             // [U]
+  int32_t* uniq_rank = uniq_slot + U;                          // [U] hit rank or miss rank
+  int32_t* uniq_cls = uniq_rank + U;                           // [U] 0 hit, 1 fill, 2 cpu
+  int32_t* miss_list = uniq_cls + U;                           // [U] unique index by miss rank
+  int32_t* gcnt = miss_list + U;                               // [U + 2] pairs per GPU expert
+  uint32_t* hist = reinterpret_cast<uint32_t*>(gcnt + U + 2);  // [256]
+  unsigned long long* cand = reinterpret_cast<unsigned long long*>(
+      (reinterpret_cast<uintptr_t>(hist + 256) + 7) & ~uintptr_t(7));  // [K]
+
+  const int32_t* e2s = a.tab.e2s;
+  int32_t* s2e = a.tab.s2e;
+  uint64_t* stamp = a.tab.stamp;
+  const int fbase = a.layer * a.E;
+
+  // ---- 1. dedup: routed-expert bitmap ------------------------------------
+  for (int i = tid; i < NW; i += nt) ebits[i] = 0u;
+  if (tid == 0) {
+    sc.bad = 0; sc.ncand = 0; sc.read_hits = 0; sc.read_misses = 0;
+    sc.clock0 = (unsigned long long)*a.tab.clock;
+  }
+  for (int i = tid; i < U + 2; i += nt) gcnt[i] = 0;
+  __syncthreads();
+  for (int p = tid; p < P; p += nt) {
+    const int e = a.ids[p];
+    if ((unsigned)e >= (unsigned)a.E) atomicOr(&sc.bad, 1);
+    else atomicOr(&ebits[e >> 5], 1u << (e & 31));
+  }
+  __syncthreads();
+  if (tid < 32) {  // exclusive popcount prefix over the bitmap words
+    int running = 0;
+    for (int w0 = 0; w0 < NW; w0 += 32) {
+      const int w = w0 + lane;
+      const int c = (w < NW) ? __popc(ebits[w]) : 0;
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (w < NW) ebase[w] = running + incl - c;
+      running += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) { ebase[NW] = running; sc.u = running; }
+  }
+  __syncthreads();
+  const int u = sc.u;
+  for (int e = tid; e < a.E; e += nt) {
+    const uint32_t wbits = ebits[e >> 5];
+    if (wbits & (1u << (e & 31))) {
+      const int idx = ebase[e >> 5] + __popc(wbits & ((1u << (e & 31)) - 1u));
+      uniq_e[idx] = e;
+    }
+  }
+  __syncthreads();
+
+  // ---- 2. classify against the residency table ----------------------------
+  for (int i = tid; i < u; i += nt) uniq_slot[i] = e2s[fbase + uniq_e[i]];
+  __syncthreads();
+  if (tid < 32) {  // hit / miss ranks in ascending flat id
+    int hb = 0, mb = 0;
+    for (int c0 = 0; c0 < u; c0 += 32) {
+      const int i = c0 + lane;
+      const bool valid = i < u;
+      const bool hit = valid && uniq_slot[i] >= 0;
+      const bool miss = valid && !hit;
+      const uint32_t bh = __ballot_sync(0xffffffffu, hit);
+      const uint32_t bm = __ballot_sync(0xffffffffu, miss);
+      if (hit) { uniq_rank[i] = hb + __popc(bh & lanemask_lt()); uniq_cls[i] = 0; }
+      if (miss) {
+        const int r = mb + __popc(bm & lanemask_lt());
+        uniq_rank[i] = r;
+        miss_list[r] = i;
+        uniq_cls[i] = 2;
+      }
+      hb += __popc(bh);
+      mb += __popc(bm);
+    }
+    if (lane == 0) {
+      sc.h = hb;
+      sc.m = mb;
+      // ---- 3. the split q ----------------------------------------------------
+      const int V = a.C - hb;  // slots this call may evict
+      int q = 0;
+      if (mb > 0) {
+        q = (int)q_star((uint32_t)mb, a.bp, a.bc);
+        q = max(1, min(q, mb));
+        q = min(q, min(a.K, V));
+        q = max(q, 0);
+      }
+      sc.q = q;
+      sc.keff = max(0, min(a.K, V));
+    }
+  }
+  __syncthreads();
+  const int h = sc.h, m = sc.m, q = sc.q, keff = sc.keff;
+
+  // ---- 4. the K least-recently-used evictable slots, one radix select -------
+  // key(s) = (stamp << 20) | s, or all-ones when s holds one of this call's hits
+  auto key_of = [&](int s) -> unsigned long long {
+    const int f = s2e[s];
+    if (f >= fbase && f < fbase + a.E) {
+      const int e = f - fbase;
+      if (ebits[e >> 5] & (1u << (e & 31))) return ~0ull;
+    }
+    return ((unsigned long long)stamp[s] << kSlotBits) | (unsigned long long)s;
+  };
+  if (keff > 0) {
+    const unsigned long long maxkey = (sc.clock0 << kSlotBits) | (kMaxSlots - 1);
+    const int top = 63 - __clzll((long long)maxkey);
+    unsigned long long prefix = 0ull, maskhi = 0ull;
+    int kth = keff;  // 1-based rank still to find below the current prefix
+    for (int shift = (top / 8) * 8; shift >= 0; shift -= 8) {
+      for (int i = tid; i < 256; i += nt) hist[i] = 0u;
+      __syncthreads();
+      for (int s = tid; s < a.C; s += nt) {
+        const unsigned long long key = key_of(s);
+        if ((key & maskhi) == prefix) atomicAdd(&hist[(key >> shift) & 255ull], 1u);
+      }
+      __syncthreads();
+      if (tid < 32) {
+        int c = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) c += (int)hist[lane * 8 + j];
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        const int excl = incl - c;
+        const bool here = (excl < kth) && (kth <= incl);
+        if (here) {
+          int run = excl, d = lane * 8;
+          for (int j = 0; j < 8; ++j) {
+            const int hj = (int)hist[lane * 8 + j];
+            if (run + hj >= kth) { d = lane * 8 + j; break; }
+            run += hj;
+          }
+          sc.digit = d;
+          sc.kth = kth - run;
+        }
+      }
+      __syncthreads();
+      prefix |= (unsigned long long)sc.digit << shift;
+      maskhi |= 255ull << shift;
+      kth = sc.kth;
+      __syncthreads();
+    }
+    // prefix is now the keff-th smallest key; keys are unique, so exactly keff are <= it
+    for (int s = tid; s < a.C; s += nt) {
+      const unsigned long long key = key_of(s);
+      if (key <= prefix) {
+        const int i = atomicAdd(&sc.ncand, 1);
+        if (i < keff) cand[i] = key;
+      }
+    }
+    __syncthreads();
+    for (int i = tid; i < keff; i += nt) {
+      const unsigned long long ki = cand[i];
+      int r = 0;
+      for (int j = 0; j < keff; ++j) r += (cand[j] < ki);
+      a.b.victims[r] = (int32_t)(ki & (kMaxSlots - 1));
+    }
+  }
+  for (int i = keff + tid; i < a.K; i += nt) a.b.victims[i] = -1;
+  __syncthreads();  // victims visible to the block (global writes, same CTA)
+
+  // ---- 5. rewrite: fills take victims in order, the rest go to the CPU ------
+  for (int r = tid; r < m; r += nt) {
+    const int i = miss_list[r];
+    const int f = fbase + uniq_e[i];
+    if (r < q) {
+      const int v = a.b.victims[r];
+      const int old = s2e[v];
+      if (old >= 0) a.tab.e2s[old] = -1;
+      s2e[v] = f;
+      a.tab.e2s[f] = v;
+      uniq_slot[i] = v;
+      uniq_cls[i] = 1;
+      a.b.fills[2 * r] = f;
+      a.b.fills[2 * r + 1] = v;
+    } else {
+      a.b.cpu[r - q] = f;
+    }
+  }
+  __syncthreads();
+
+  // ---- 6. recency: stamp GPU-run experts in ascending flat id ---------------
+  if (tid < 32) {
+    int tb = 0;
+    for (int c0 = 0; c0 < u; c0 += 32) {
+      const int i = c0 + lane;
+      const bool touched = (i < u) && uniq_cls[i] < 2;
+      const uint32_t bt = __ballot_sync(0xffffffffu, touched);
+      if (touched) stamp[uniq_slot[i]] = sc.clock0 + (unsigned long long)(tb + __popc(bt & lanemask_lt())) + 1ull;
+      tb += __popc(bt);
+    }
+    if (lane == 0) {
+      sc.ntouch = tb;
+      *a.tab.clock = sc.clock0 + (unsigned long long)tb;
+      if (((sc.clock0 + tb) >> (64 - kSlotBits)) != 0ull) atomicOr(&sc.bad, 2);
+    }
+  }
+  // GPU expert index of each unique: hits 0..h-1, shared expert h, fills after
+  const int ns = a.n_shared;
+  const int nfirst = h + ns;
+  for (int i = tid; i < u; i += nt) {
+    const int cls = uniq_cls[i];
+    int g = -1;
+    if (cls == 0) g = uniq_rank[i];
+    else if (cls == 1) g = nfirst + uniq_rank[i];
+    uniq_rank[i] = g;  // reuse: GPU expert index (or -1)
+    if (g >= 0) a.b.gpu_w[g] = a.slots_base + (size_t)uniq_slot[i] * a.S;
+  }
+  if (ns && tid == 0) a.b.gpu_w[h] = a.shared_blob;
+  __syncthreads();
+
+  // ---- 7. slot map and pair lists ---------------------------------------------
+  int my_hits = 0, my_misses = 0;
+  for (int p = tid; p < P; p += nt) {
+    const int e = a.ids[p];
+    int slot = -1;
+    if ((unsigned)e < (unsigned)a.E) {
+      const uint32_t wbits = ebits[e >> 5];
+      const int i = ebase[e >> 5] + __popc(wbits & ((1u << (e & 31)) - 1u));
+      const int cls = uniq_cls[i];
+      if (cls == 0) ++my_hits; else ++my_misses;
+      if (cls < 2) {
+        slot = uniq_slot[i];
+        atomicAdd(&gcnt[uniq_rank[i]], 1);
+      }
+    } else {
+      ++my_misses;
+    }
+    a.b.slot_map[p] = slot;
+    if (a.slot_map_out) a.slot_map_out[p] = slot;
+  }
+  if (my_hits) atomicAdd(&sc.read_hits, my_hits);
+  if (my_misses) atomicAdd(&sc.read_misses, my_misses);
+  const int ngpu = nfirst + q;
+  if (ns && tid == 0) gcnt[h] = a.T;
+  __syncthreads();
+  if (tid < 32) {  // exclusive scan of pair counts -> offsets (gcnt becomes write cursors)
+    int running = 0;
+    for (int c0 = 0; c0 < ngpu; c0 += 32) {
+      const int g = c0 + lane;
+      const int c = g < ngpu ? gcnt[g] : 0;
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (g < ngpu) { a.b.gpu_off[g] = running + incl - c; gcnt[g] = running + incl - c; }
+      running += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) a.b.gpu_off[ngpu] = running;
+  }
+  __syncthreads();
+  for (int p = tid; p < P; p += nt) {
+    const int slot = a.b.slot_map[p];
+    if (slot >= 0) {
+      const int e = a.ids[p];
+      const uint32_t wbits = ebits[e >> 5];
+      const int i = ebase[e >> 5] + __popc(wbits & ((1u << (e & 31)) - 1u));
+      const int pos = atomicAdd(&gcnt[uniq_rank[i]], 1);
+      a.b.gpu_pairs[pos] = p;
+    }
+  }
+  if (ns) {
+    for (int t = tid; t < a.T; t += nt) a.b.gpu_pairs[gcnt[h] + t] = P + t;  // shared pairs after routed ones
+  }
+
+  // ---- 8. plan scalars, counters, error word ------------------------------------
+  __syncthreads();
+  if (tid == 0) {
+    int32_t* pl = a.b.plan;
+    pl[P_LAYER] = a.layer; pl[P_U] = u; pl[P_H] = h; pl[P_M] = m; pl[P_Q] = q;
+    pl[P_NCPU] = m - q; pl[P_NGPU] = ngpu; pl[P_NFIRST] = nfirst;
+    uint64_t* c = a.tab.counters;
+    c[0] += (uint64_t)h; c[1] += (uint64_t)m; c[2] += (uint64_t)q; c[3] += (uint64_t)(m - q);
+    c[4] += (uint64_t)sc.read_hits; c[5] += (uint64_t)sc.read_misses; c[6] += 1ull;
+    uint32_t e = 0;
+    if (sc.bad & 1) e |= kErrBadExpertId;
+    if (sc.bad & 2) e |= kErrClock;
+    if (e) atomicOr_system(a.err, e);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decode_control(const Shape& sh, int layer, int T, int C, int K, uint32_t bp,
+                                  uint32_t bc, const int32_t* ids, CacheTables tab, DecodeBufs b,
+                                  int32_t* slot_map_out, const uint8_t* slots_base,
+                                  const uint8_t* shared_base, uint32_t* err, cudaStream_t s) {
+  CtrlArgs a;
+  a.layer = layer; a.T = T; a.k = sh.k; a.E = sh.E; a.C = C; a.K = K; a.n_shared = sh.n_shared;
+  a.bp = bp; a.bc = bc; a.S = sh.S; a.ids = ids; a.tab = tab; a.b = b;
+  a.slot_map_out = slot_map_out; a.slots_base = slots_base;
+  a.shared_blob = sh.n_shared ? shared_base + (size_t)layer * sh.S : nullptr;
+  a.err = err;
+  a.umax = min(sh.E, T * sh.k);
+  const int NW = (sh.E + 31) / 32;
+  const size_t smem = (size_t)(2 * NW + 1) * 4 + (size_t)(6 * a.umax + 2) * 4 + 257 * 4 + 8 +
+                      (size_t)K * 8 + 16;
+  decode_control_kernel<<<1, kCtrlThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t setup_control_kernels() {
+  return cudaFuncSetAttribute(decode_control_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              200 * 1024);
+}
+
+}  // namespace moe

@@ -1,0 +1,415 @@
+// Decode-side expert work: the slot fill copy, the grouped SwiGLU GEMV over
+// resident slots, and the fixed-order combine.
+//
+// Follows the snackonai deep dive "FreeToken, or why your laptop was never the
+// bottleneck", section "The split policy itself" (closing note: the GPU miss
+// path runs its cache update, batched copy and grouped evaluation) and section
+// "What It Actually Does" (GPU and CPU partial sums merge exactly); the
+// dev.to summary "FreeToken runs frontier-scale MoE models ...", section "When
+// it misses": RAM -> link -> VRAM -> GPU execute.
+//
+// Expert (not written out on the pages; the SwiGLU of the Qwen3 / DeepSeek-V3
+// MoE families): h = silu(W_gate x) * (W_up x) in fp32, y = W_down h in fp32.
+//
+// GB300 design: decode is a matrix-vector product per expert (a handful of
+// tokens per expert), so it is bound by HBM bandwidth, not by tensor cores.
+// Each warp streams whole weight rows with 16-byte loads (coalesced: lane l
+// reads chunks l, l+32, ...), keeps several rows' loads in flight, and reduces
+// with shuffles.  Work is the flat list of (GPU expert, row) pairs the control
+// kernel published through device-resident counts, spread over a fixed grid of
+// a few CTAs per SM (152 SMs), so launches have fixed shapes and can be graph
+// captured.  The fill copy is an SM copy kernel reading page-locked host memory
+// over the host link (NVLink-C2C on a Grace host), because the fill list is
+// decided on the device and a copy-engine memcpy would need host-known
+// addresses.
+#include "internal.cuh"
+
+#include <cuda_fp8.h>
+
+namespace moe {
+
+namespace {
+
+constexpr int kGemvThreads = 512;
+constexpr int kChunksPerLane = 4;
+
+// ---- weight formats: one 16-byte chunk -> V floats ---------------------------
+template <int WT> struct WFmt;
+template <> struct WFmt<MOE_F32> {
+  static constexpr int V = 4, ES = 4;
+  __device__ static void unpack(const uint4& w, float* f) {
+    f[0] = __uint_as_float(w.x); f[1] = __uint_as_float(w.y);
+    f[2] = __uint_as_float(w.z); f[3] = __uint_as_float(w.w);
+  }
+};
+template <> struct WFmt<MOE_BF16> {
+  static constexpr int V = 8, ES = 2;
+  __device__ static void unpack(const uint4& w, float* f) {
+    const uint32_t v[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(v[i] << 16);
+      f[2 * i + 1] = __uint_as_float(v[i] & 0xffff0000u);
+    }
+  }
+};
+template <> struct WFmt<MOE_FP8E4M3_B128> {
+  static constexpr int V = 16, ES = 1;
+  __device__ static void unpack(const uint4& w, float* f) {
+    const uint32_t v[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(v[i] & 0xffffu), __NV_E4M3);
+      const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(v[i] >> 16), __NV_E4M3);
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+      f[4 * i] = a.x; f[4 * i + 1] = a.y; f[4 * i + 2] = b.x; f[4 * i + 3] = b.y;
+    }
+  }
+};
+
+// ---- activations: V consecutive values as floats --------------------------
+template <int AT, int V> __device__ __forceinline__ void load_act(const void* x, size_t off, float* f);
+template <int V> __device__ __forceinline__ void load_act_f32(const float* p, float* f) {
+#pragma unroll
+  for (int i = 0; i < V; i += 4) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(p + i));
+    f[i] = v.x; f[i + 1] = v.y; f[i + 2] = v.z; f[i + 3] = v.w;
+  }
+}
+template <> __device__ __forceinline__ void load_act<MOE_F32, 4>(const void* x, size_t off, float* f) {
+  load_act_f32<4>(reinterpret_cast<const float*>(x) + off, f);
+}
+template <> __device__ __forceinline__ void load_act<MOE_F32, 8>(const void* x, size_t off, float* f) {
+  load_act_f32<8>(reinterpret_cast<const float*>(x) + off, f);
+}
+template <> __device__ __forceinline__ void load_act<MOE_F32, 16>(const void* x, size_t off, float* f) {
+  load_act_f32<16>(reinterpret_cast<const float*>(x) + off, f);
+}
+template <int V> __device__ __forceinline__ void load_act_bf16(const uint16_t* p, float* f) {
+#pragma unroll
+  for (int i = 0; i < V; i += 8) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(p + i));
+    WFmt<MOE_BF16>::unpack(v, f + i);
+  }
+}
+template <> __device__ __forceinline__ void load_act<MOE_BF16, 8>(const void* x, size_t off, float* f) {
+  load_act_bf16<8>(reinterpret_cast<const uint16_t*>(x) + off, f);
+}
+template <> __device__ __forceinline__ void load_act<MOE_BF16, 16>(const void* x, size_t off, float* f) {
+  load_act_bf16<16>(reinterpret_cast<const uint16_t*>(x) + off, f);
+}
+template <> __device__ __forceinline__ void load_act<MOE_BF16, 4>(const void* x, size_t off, float* f) {
+  const uint2 v = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(x) + off));
+  f[0] = __uint_as_float(v.x << 16); f[1] = __uint_as_float(v.x & 0xffff0000u);
+  f[2] = __uint_as_float(v.y << 16); f[3] = __uint_as_float(v.y & 0xffff0000u);
+}
+
+// weights are read once per step: stream them past L1
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+
+struct GemvArgs {
+  int H, I, k, T, P;             // P = T * k (pair ids >= P are shared-expert rows)
+  int pass;                      // 0: hits + shared, 1: fills
+  const void* x;
+  DecodeBufs b;
+};
+
+__device__ __forceinline__ int token_of(int pid, int k, int P) { return pid < P ? pid / k : pid - P; }
+
+// ---- phase 1: h[pair, i] = silu(gate_i . x_t) * (up_i . x_t) ------------------
+template <int WT, int AT, int kTokGroup>
+__global__ void __launch_bounds__(kGemvThreads, kTokGroup == 1 ? 2 : 1) gate_up_kernel(GemvArgs a) {
+  using F = WFmt<WT>;
+  constexpr int V = F::V;
+  const int* plan = a.b.plan;
+  const int g0 = a.pass == 0 ? 0 : plan[P_NFIRST];
+  const int g1 = a.pass == 0 ? plan[P_NFIRST] : plan[P_NGPU];
+  const int H = a.H, I = a.I;
+  const long rows = (long)(g1 - g0) * I;
+  const int lane = threadIdx.x & 31;
+  const long nwarps = (long)gridDim.x * (blockDim.x >> 5);
+  const long wid = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int NCH = H / V;                       // 16-byte chunks per row
+  const size_t row_bytes = (size_t)H * F::ES;
+  const int HB = H / 128;                      // fp8 scale columns
+
+  for (long r = wid; r < rows; r += nwarps) {
+    const int g = g0 + (int)(r / I);
+    const int i = (int)(r % I);
+    const uint8_t* wb = a.b.gpu_w[g];
+    const uint4* gate = reinterpret_cast<const uint4*>(wb + (size_t)i * row_bytes);
+    const uint4* up = reinterpret_cast<const uint4*>(wb + (size_t)(I + i) * row_bytes);
+    const float* sgu = reinterpret_cast<const float*>(wb + 3ull * (size_t)I * row_bytes);
+    const int pb = a.b.gpu_off[g], pe = a.b.gpu_off[g + 1];
+    for (int tp = pb; tp < pe; tp += kTokGroup) {
+      const int nt = min(kTokGroup, pe - tp);
+      int tok[kTokGroup];
+#pragma unroll
+      for (int n = 0; n < kTokGroup; ++n) tok[n] = n < nt ? token_of(a.b.gpu_pairs[tp + n], a.k, a.P) : 0;
+      float ag[kTokGroup], au[kTokGroup];
+#pragma unroll
+      for (int n = 0; n < kTokGroup; ++n) { ag[n] = 0.f; au[n] = 0.f; }
+      for (int seg = 0; seg < NCH; seg += 32 * kChunksPerLane) {
+        uint4 wg[kChunksPerLane], wu[kChunksPerLane];
+#pragma unroll
+        for (int j = 0; j < kChunksPerLane; ++j) {
+          const int c = seg + j * 32 + lane;
+          if (c < NCH) { wg[j] = ld_stream(gate + c); wu[j] = ld_stream(up + c); }
+        }
+#pragma unroll
+        for (int j = 0; j < kChunksPerLane; ++j) {
+          const int c = seg + j * 32 + lane;
+          if (c < NCH) {
+            float fg[V], fu[V];
+            F::unpack(wg[j], fg);
+            F::unpack(wu[j], fu);
+            float scg = 1.f, scu = 1.f;
+            if (WT == MOE_FP8E4M3_B128) {
+              const int cb = (c * V) >> 7;
+              scg = __ldg(sgu + (size_t)(i >> 7) * HB + cb);
+              scu = __ldg(sgu + (size_t)((I + i) >> 7) * HB + cb);
+            }
+#pragma unroll
+            for (int n = 0; n < kTokGroup; ++n) {
+              if (n < nt) {
+                float xv[V];
+                load_act<AT, V>(a.x, (size_t)tok[n] * H + (size_t)c * V, xv);
+                float dg = 0.f, du = 0.f;
+#pragma unroll
+                for (int v = 0; v < V; ++v) { dg = fmaf(fg[v], xv[v], dg); du = fmaf(fu[v], xv[v], du); }
+                ag[n] = fmaf(dg, scg, ag[n]);
+                au[n] = fmaf(du, scu, au[n]);
+              }
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int n = 0; n < kTokGroup; ++n) {
+        if (n < nt) {
+          const float sg = warp_sum(ag[n]);
+          const float su = warp_sum(au[n]);
+          if (lane == 0) a.b.h[(size_t)a.b.gpu_pairs[tp + n] * I + i] = silu(sg) * su;
+        }
+      }
+    }
+  }
+}
+
+// ---- phase 2: y[pair, r] = down_r . h[pair] ------------------------------------
+template <int WT, int kTokGroup>
+__global__ void __launch_bounds__(kGemvThreads, kTokGroup == 1 ? 2 : 1) down_kernel(GemvArgs a) {
+  using F = WFmt<WT>;
+  constexpr int V = F::V;
+  const int* plan = a.b.plan;
+  const int g0 = a.pass == 0 ? 0 : plan[P_NFIRST];
+  const int g1 = a.pass == 0 ? plan[P_NFIRST] : plan[P_NGPU];
+  const int H = a.H, I = a.I;
+  const long rows = (long)(g1 - g0) * H;
+  const int lane = threadIdx.x & 31;
+  const long nwarps = (long)gridDim.x * (blockDim.x >> 5);
+  const long wid = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int NCH = I / V;
+  const size_t row_bytes = (size_t)I * F::ES;
+  const size_t down_off = 2ull * (size_t)I * (size_t)H * F::ES;
+  const size_t sd_off = 3ull * (size_t)I * (size_t)H * F::ES + 4ull * (size_t)(2 * I / 128) * (H / 128);
+  const int IB = I / 128;
+
+  for (long r = wid; r < rows; r += nwarps) {
+    const int g = g0 + (int)(r / H);
+    const int row = (int)(r % H);
+    const uint8_t* wb = a.b.gpu_w[g];
+    const uint4* wrow = reinterpret_cast<const uint4*>(wb + down_off + (size_t)row * row_bytes);
+    const float* sd = reinterpret_cast<const float*>(wb + sd_off);
+    const int pb = a.b.gpu_off[g], pe = a.b.gpu_off[g + 1];
+    for (int tp = pb; tp < pe; tp += kTokGroup) {
+      const int nt = min(kTokGroup, pe - tp);
+      int pid[kTokGroup];
+#pragma unroll
+      for (int n = 0; n < kTokGroup; ++n) pid[n] = n < nt ? a.b.gpu_pairs[tp + n] : 0;
+      float acc[kTokGroup];
+#pragma unroll
+      for (int n = 0; n < kTokGroup; ++n) acc[n] = 0.f;
+      for (int seg = 0; seg < NCH; seg += 32 * kChunksPerLane) {
+        uint4 w[kChunksPerLane];
+#pragma unroll
+        for (int j = 0; j < kChunksPerLane; ++j) {
+          const int c = seg + j * 32 + lane;
+          if (c < NCH) w[j] = ld_stream(wrow + c);
+        }
+#pragma unroll
+        for (int j = 0; j < kChunksPerLane; ++j) {
+          const int c = seg + j * 32 + lane;
+          if (c < NCH) {
+            float fw[V];
+            F::unpack(w[j], fw);
+            float sc = 1.f;
+            if (WT == MOE_FP8E4M3_B128) sc = __ldg(sd + (size_t)(row >> 7) * IB + ((c * V) >> 7));
+#pragma unroll
+            for (int n = 0; n < kTokGroup; ++n) {
+              if (n < nt) {
+                float hv[V];
+                load_act_f32<V>(a.b.h + (size_t)pid[n] * I + (size_t)c * V, hv);
+                float d = 0.f;
+#pragma unroll
+                for (int v = 0; v < V; ++v) d = fmaf(fw[v], hv[v], d);
+                acc[n] = fmaf(d, sc, acc[n]);
+              }
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int n = 0; n < kTokGroup; ++n) {
+        if (n < nt) {
+          const float s = warp_sum(acc[n]);
+          if (lane == 0) a.b.y[(size_t)pid[n] * H + row] = s;
+        }
+      }
+    }
+  }
+}
+
+// ---- combine: out[t] = sum_j w[t,j] * (slot >= 0 ? y : cpu_part) in j order (+ shared) --
+__global__ void combine_kernel(int T, int H, int k, int n_shared, const float* __restrict__ w,
+                               const int32_t* __restrict__ sm, const float* __restrict__ y,
+                               const float* __restrict__ cpu, float* __restrict__ out, uint32_t* err) {
+  const int H4 = H >> 2;
+  const long n = (long)T * H4;
+  const int P = T * k;
+  bool missing = false;
+  for (long idx = (long)blockIdx.x * blockDim.x + threadIdx.x; idx < n; idx += (long)gridDim.x * blockDim.x) {
+    const int t = (int)(idx / H4);
+    const int c = (int)(idx % H4) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < k; ++j) {
+      const int p = t * k + j;
+      const float wt = __ldg(w + p);
+      float4 v;
+      if (sm[p] >= 0) {
+        v = __ldg(reinterpret_cast<const float4*>(y + (size_t)p * H + c));
+      } else if (cpu != nullptr) {
+        v = __ldg(reinterpret_cast<const float4*>(cpu + (size_t)p * H + c));
+      } else {
+        v = make_float4(0.f, 0.f, 0.f, 0.f);
+        missing = true;
+      }
+      acc.x = fmaf(wt, v.x, acc.x); acc.y = fmaf(wt, v.y, acc.y);
+      acc.z = fmaf(wt, v.z, acc.z); acc.w = fmaf(wt, v.w, acc.w);
+    }
+    if (n_shared) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(y + (size_t)(P + t) * H + c));
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    *reinterpret_cast<float4*>(out + (size_t)t * H + c) = acc;
+  }
+  if (__any_sync(0xffffffffu, missing) && (threadIdx.x & 31) == 0) atomicOr_system(err, kErrMissingCpuPart);
+}
+
+// ---- blob copy: complete experts host pool -> slots ---------------------------------
+// list = (flat id, slot) pairs; the copy starts at pair *skip (if skip) and takes *count
+// pairs.  Every CTA copies its 1/gridDim share of every blob, so one launch spreads
+// any number of blobs over the whole grid with 16-byte loads, 4 in flight per thread.
+__global__ void __launch_bounds__(512) copy_blobs_kernel(const int32_t* __restrict__ count,
+                                                         const int32_t* __restrict__ skip,
+                                                         const int32_t* __restrict__ list,
+                                                         const uint8_t* __restrict__ host,
+                                                         const uint64_t* __restrict__ offs,
+                                                         uint8_t* __restrict__ slots, uint64_t S) {
+  constexpr int U = 4;
+  const int n = *count;
+  const int32_t* pairs = list + (skip ? 2 * (*skip) : 0);
+  const uint64_t n16 = S >> 4;
+  const uint64_t per = (n16 + gridDim.x - 1) / gridDim.x;
+  const uint64_t c0 = per * blockIdx.x;
+  const uint64_t c1 = min(n16, c0 + per);
+  for (int i = 0; i < n; ++i) {
+    const int f = pairs[2 * i];
+    const int s = pairs[2 * i + 1];
+    const uint4* src = reinterpret_cast<const uint4*>(host + offs[f]);
+    uint4* dst = reinterpret_cast<uint4*>(slots + (size_t)s * S);
+    uint64_t c = c0 + threadIdx.x;
+    for (; c + (U - 1) * blockDim.x < c1; c += U * blockDim.x) {
+      uint4 v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) v[u] = src[c + u * blockDim.x];
+#pragma unroll
+      for (int u = 0; u < U; ++u) __stcs(dst + c + u * blockDim.x, v[u]);
+    }
+    for (; c < c1; c += blockDim.x) __stcs(dst + c, src[c]);
+  }
+}
+
+template <int WT, int AT>
+cudaError_t launch_gemv_typed(const GemvArgs& a, int sms, cudaStream_t s) {
+  if (a.T == 1) {
+    gate_up_kernel<WT, AT, 1><<<2 * sms, kGemvThreads, 0, s>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    down_kernel<WT, 1><<<2 * sms, kGemvThreads, 0, s>>>(a);
+    return cudaGetLastError();
+  }
+  gate_up_kernel<WT, AT, 4><<<sms, kGemvThreads, 0, s>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  down_kernel<WT, 4><<<sms, kGemvThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int gemv_block_threads() { return kGemvThreads; }
+
+cudaError_t launch_fill(const Shape& sh, const int32_t* plan, const int32_t* fills,
+                        const uint8_t* host_pool_dev, const uint64_t* offsets, uint8_t* slots,
+                        int n_ctas, cudaStream_t s) {
+  return launch_copy_blobs(plan + P_Q, nullptr, fills, host_pool_dev, offsets, slots, sh.S, n_ctas, s);
+}
+
+cudaError_t launch_copy_blobs(const int32_t* count, const int32_t* skip, const int32_t* list,
+                              const uint8_t* host_pool_dev, const uint64_t* offsets, uint8_t* slots,
+                              uint64_t S, int n_ctas, cudaStream_t s) {
+  copy_blobs_kernel<<<n_ctas, 512, 0, s>>>(count, skip, list, host_pool_dev, offsets, slots, S);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_expert_gemv(const Shape& sh, int pass, int T, const void* x, DecodeBufs b,
+                               int sms, cudaStream_t s) {
+  GemvArgs a;
+  a.H = sh.H; a.I = sh.I; a.k = sh.k; a.T = T; a.P = T * sh.k; a.pass = pass; a.x = x; a.b = b;
+  if (sh.wdtype == MOE_F32 && sh.adtype == MOE_F32) return launch_gemv_typed<MOE_F32, MOE_F32>(a, sms, s);
+  if (sh.wdtype == MOE_F32 && sh.adtype == MOE_BF16) return launch_gemv_typed<MOE_F32, MOE_BF16>(a, sms, s);
+  if (sh.wdtype == MOE_BF16 && sh.adtype == MOE_F32) return launch_gemv_typed<MOE_BF16, MOE_F32>(a, sms, s);
+  if (sh.wdtype == MOE_BF16 && sh.adtype == MOE_BF16) return launch_gemv_typed<MOE_BF16, MOE_BF16>(a, sms, s);
+  if (sh.wdtype == MOE_FP8E4M3_B128 && sh.adtype == MOE_F32)
+    return launch_gemv_typed<MOE_FP8E4M3_B128, MOE_F32>(a, sms, s);
+  if (sh.wdtype == MOE_FP8E4M3_B128 && sh.adtype == MOE_BF16)
+    return launch_gemv_typed<MOE_FP8E4M3_B128, MOE_BF16>(a, sms, s);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_combine(const Shape& sh, int T, const float* w, const float* cpu_part,
+                           DecodeBufs b, float* out, uint32_t* err, cudaStream_t s) {
+  const long n = (long)T * (sh.H / 4);
+  const int threads = 256;
+  const long want = (n + threads - 1) / threads;
+  const int grid = (int)(want < 152L * 8 ? want : 152L * 8);
+  combine_kernel<<<grid, threads, 0, s>>>(T, sh.H, sh.k, sh.n_shared, w, b.slot_map, b.y, cpu_part, out, err);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

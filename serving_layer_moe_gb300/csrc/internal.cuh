@@ -1,0 +1,109 @@
+// Internal declarations of libmoecache.so (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#include "../../include/moe_cache.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// limits
+// ---------------------------------------------------------------------------
+constexpr int kMaxExperts = 4096;          // E: routed-expert bitmap of 128 words
+constexpr int kMaxDecodeTokens = 1024;
+constexpr int kSlotBits = 20;              // slot index field of an LRU key
+constexpr uint64_t kMaxSlots = 1ull << kSlotBits;
+constexpr int kCtrlThreads = 1024;
+
+// error word bits (device -> host through page-locked mapped memory)
+enum : uint32_t {
+  kErrBadExpertId = 1u,
+  kErrMissingCpuPart = 2u,
+  kErrCapacity = 4u,
+  kErrClock = 8u,
+  kErrTimeout = 16u,
+};
+
+// ---------------------------------------------------------------------------
+// plan scalars written by the decode control kernel, read by the GEMV / fill
+// ---------------------------------------------------------------------------
+enum PlanIdx : int {
+  P_LAYER = 0, P_U = 1, P_H = 2, P_M = 3, P_Q = 4, P_NCPU = 5, P_NGPU = 6,
+  P_NFIRST = 7,     // GPU experts in the first (resident) pass: hits + shared
+  P_COUNT = 8,
+};
+
+// kernel groups timed by moe_cache_profile
+enum ProfKind : int {
+  PROF_CONTROL = 0, PROF_FILL = 1, PROF_GEMV_RESIDENT = 2, PROF_GEMV_FILLED = 3, PROF_COMBINE = 4,
+  PROF_PREFILL_CONTROL = 5, PROF_PREFILL_LOAD = 6, PROF_PREFILL_GEMM = 7, PROF_KINDS = 8,
+};
+
+// Everything the decode kernels of one call need, by value.
+struct DecodeBufs {
+  int32_t* plan;          // [P_COUNT]
+  int32_t* victims;       // [K]
+  int32_t* fills;         // [2K]  (flat id, slot)
+  int32_t* cpu;           // [max unique]
+  int32_t* slot_map;      // [max_tokens * k]  internal copy
+  int32_t* gpu_off;       // [max_gpu + 1]  pair-list offsets per GPU expert
+  int32_t* gpu_pairs;     // [max_pairs]    pair ids grouped by GPU expert
+  const uint8_t** gpu_w;  // [max_gpu]      weight blob of each GPU expert
+  float* h;               // [max_pairs, I] SwiGLU activations
+  float* y;               // [max_pairs, H] expert outputs (unweighted)
+};
+
+struct CacheTables {
+  int32_t* e2s;           // [L*E]
+  int32_t* s2e;           // [C]
+  uint64_t* stamp;        // [C]
+  uint64_t* clock;        // [1]
+  uint64_t* counters;     // [8]
+};
+
+struct Shape {
+  int L, E, H, I, k;
+  int wdtype, adtype;
+  int n_shared;
+  uint64_t S;             // blob bytes
+};
+
+// ---------------------------------------------------------------------------
+// kernels (launch wrappers; all enqueue only)
+// ---------------------------------------------------------------------------
+// control.cu
+cudaError_t launch_decode_control(const Shape& sh, int layer, int T, int C, int K, uint32_t bp,
+                                  uint32_t bc, const int32_t* ids, CacheTables tab, DecodeBufs b,
+                                  int32_t* slot_map_out, const uint8_t* slots_base,
+                                  const uint8_t* shared_base, uint32_t* err, cudaStream_t s);
+
+cudaError_t setup_control_kernels();  // once per device, before the first launch
+
+// expert_gemv.cu
+cudaError_t launch_fill(const Shape& sh, const int32_t* plan, const int32_t* fills,
+                        const uint8_t* host_pool_dev, const uint64_t* offsets, uint8_t* slots,
+                        int n_ctas, cudaStream_t s);
+cudaError_t launch_copy_blobs(const int32_t* count, const int32_t* skip, const int32_t* list,
+                              const uint8_t* host_pool_dev, const uint64_t* offsets, uint8_t* slots,
+                              uint64_t S, int n_ctas, cudaStream_t s);
+cudaError_t launch_expert_gemv(const Shape& sh, int pass, int T, const void* x, DecodeBufs b,
+                               int sms, cudaStream_t s);
+cudaError_t launch_combine(const Shape& sh, int T, const float* w, const float* cpu_part,
+                           DecodeBufs b, float* out, uint32_t* err, cudaStream_t s);
+int gemv_block_threads();
+
+// blob geometry
+inline uint64_t blob_bytes(int wdtype, int H, int I) {
+  uint64_t HI = (uint64_t)H * (uint64_t)I;
+  if (wdtype == MOE_F32) return 12ull * HI;
+  if (wdtype == MOE_BF16) return 6ull * HI;
+  uint64_t ns = (uint64_t)(2 * I / 128) * (H / 128) + (uint64_t)(H / 128) * (I / 128);
+  return 3ull * HI + 4ull * ns;
+}
+
+}  // namespace moe

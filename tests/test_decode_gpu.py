@@ -1,0 +1,161 @@
+"""Decode parity on the GPU: libmoecache.so through its C ABI vs the CPU oracle.
+
+Control state (slot maps, q, victims, fills, residency tables, stamps, clock,
+counters) must be bit-exact; layer outputs within 2e-2 relative max error.
+"""
+import numpy as np
+import pytest
+
+from tests.harness import TOL, build_pool, make_cache, run_decode_parity, torch_act
+from workloads import activations, config, routing_trace
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import serving_layer_moe_gb300 as m
+    m.load_library()
+
+
+def _ok(res):
+    assert not res.mismatches, res.mismatches[:1]
+    assert res.max_err <= TOL, res.max_err
+
+
+def test_tiny_all_steps():
+    cfg = config("tiny")
+    res = run_decode_parity(cfg, cfg.bw_mbps, fp_every=1)
+    _ok(res)
+    assert res.fp_checked == 32 and res.cpu_pairs > 0 and res.fills > 0
+
+
+def test_tiny_registered_pageable_pool_and_offload_mode():
+    # pool handed over as pageable numpy memory (the library registers it); B_cpu = 0
+    cfg = config("tiny").with_(steps=12)
+    res = run_decode_parity(cfg, (1000, 0), fp_every=1, pinned=False)
+    _ok(res)
+
+
+def test_tiny_fetch_cap_and_cpu_heavy_split():
+    cfg = config("tiny").with_(steps=16, max_fetch=1)
+    res = run_decode_parity(cfg, (100, 900), fp_every=2)
+    _ok(res)
+    assert res.cpu_pairs > 0
+
+
+def test_tiny_zero_fetch_is_all_cpu():
+    cfg = config("tiny").with_(steps=4, max_fetch=0)
+    res = run_decode_parity(cfg, (1000, 1000), fp_every=1)
+    _ok(res)
+    assert res.fills == 0
+
+
+def test_qwen3_b1_full_trace():
+    cfg = config("qwen3_decode_b1")
+    res = run_decode_parity(cfg, (200000, 100000), n_phys=48, fp_every=997, state_every=16)
+    _ok(res)
+    assert res.calls == 256 * 48 and res.fp_checked >= 10
+
+
+def test_qwen3_b16_with_resize():
+    cfg = config("qwen3_decode_b16")
+    res = run_decode_parity(cfg, cfg.bw_mbps, n_phys=48, fp_every=1499, state_every=8, check_plan=True)
+    _ok(res)
+    assert res.calls == 256 * 48 and res.cpu_pairs > 0
+
+
+def test_dsv3_fp8_shared_expert():
+    cfg = config("dsv3_decode_slice")
+    res = run_decode_parity(cfg, (150000, 150000), n_phys=6, fp_every=97, fp_limit=6, state_every=4)
+    _ok(res)
+    assert res.fp_checked >= 5
+
+
+def test_ragged_T_and_empty_call():
+    import torch
+    cfg = config("qwen3_decode_b16").with_(steps=3)
+    s = cfg.shape
+    arena, offs, pool = build_pool(cfg, n_phys=16)
+    cache, K = make_cache(cfg, pool, offs, None, (1000, 0))
+    dev = torch.device("cuda", 0)
+    ids, w = routing_trace(cfg)
+    out = torch.full((16, s.H), 7.0, device=dev)
+    # T = 0 is a no-op
+    cache.decode(0, torch.empty(0, s.H, dtype=torch.int16, device=dev), torch.empty(0, s.k, dtype=torch.int32, device=dev),
+                 torch.empty(0, s.k, device=dev), out)
+    torch.cuda.synchronize()
+    assert float(out[0, 0]) == 7.0
+    # T = 3 of max 16
+    x = activations(cfg, 0, 0)[:3]
+    cache.decode(0, torch_act(x, dev), torch.from_numpy(ids[0, 0, :3].copy()).to(dev),
+                 torch.from_numpy(w[0, 0, :3].copy()).to(dev), out[:3])
+    torch.cuda.synchronize()
+    assert np.all(np.isfinite(out[:3].cpu().numpy()))
+    assert float(out[3, 0]) == 7.0
+    cache.close()
+
+
+def test_exact_merge_split_equals_all_gpu():
+    # The combine merges exactly: supplying, as CPU partial sums, the very fp32
+    # values the GPU computes for those experts gives a bit-identical output.
+    import torch
+    cfg = config("tiny").with_(steps=1)
+    s = cfg.shape
+    arena, offs, pool = build_pool(cfg)
+    dev = torch.device("cuda", 0)
+    ids, w = routing_trace(cfg)
+    x = torch_act(activations(cfg, 0, 0), dev)
+    i_d, w_d = torch.from_numpy(ids[0, 0]).to(dev), torch.from_numpy(w[0, 0]).to(dev)
+    big, _ = make_cache(cfg, pool, offs, None, (1000, 0), n_slots=8)      # everything fits
+    out_all = torch.empty(cfg.T, s.H, device=dev)
+    big.decode(0, x, i_d, w_d, out_all)
+    y_all = big.plan(T=cfg.T)["y"]
+    small, _ = make_cache(cfg.with_(max_fetch=1), pool, offs, None, (100, 900), n_slots=4)
+    sm = torch.empty(cfg.T, s.k, dtype=torch.int32, device=dev)
+    out_split = torch.empty(cfg.T, s.H, device=dev)
+    cpu = torch.from_numpy(y_all).to(dev)
+    small.decode(0, x, i_d, w_d, out_split, cpu_part=cpu, slot_map=sm)
+    torch.cuda.synchronize()
+    assert (sm < 0).any()
+    assert torch.equal(out_split, out_all)
+    big.close()
+    small.close()
+
+
+def test_device_errors_are_reported_on_the_next_call():
+    import torch
+    from serving_layer_moe_gb300 import MoEError
+    cfg = config("tiny").with_(steps=1)
+    s = cfg.shape
+    arena, offs, pool = build_pool(cfg)
+    cache, _ = make_cache(cfg.with_(max_fetch=1), pool, offs, None, (100, 900))
+    dev = torch.device("cuda", 0)
+    x = torch_act(activations(cfg, 0, 0), dev)
+    w = torch.full((cfg.T, s.k), 0.5, device=dev)
+    out = torch.empty(cfg.T, s.H, device=dev)
+    bad = torch.tensor([[0, 9]] * cfg.T, dtype=torch.int32, device=dev)        # 9 >= E
+    cache.decode(0, x, bad, w, out, cpu_part=torch.zeros(cfg.T, s.k, s.H, device=dev))
+    torch.cuda.synchronize()
+    good = torch.tensor([[0, 1], [2, 3], [4, 5], [6, 7]], dtype=torch.int32, device=dev)
+    with pytest.raises(MoEError) as ei:
+        cache.decode(0, x, good, w, out)
+    assert ei.value.status == 6
+    # CPU-assigned pairs but no CPU partial sums: flagged, outputs stay finite
+    cache.decode(0, x, good, w, out)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
+    with pytest.raises(MoEError) as ei:
+        cache.decode(0, x, good, w, out)
+    assert ei.value.status == 6
+    cache.close()
+
+
+def test_bench_bw_reports_two_bandwidths():
+    from serving_layer_moe_gb300 import bench_bw
+    bp, bh, rec = bench_bw(0, 9437184)
+    assert bp > 1.0 and bh > 1.0
+    assert rec == (bh > 2.0 * bp)

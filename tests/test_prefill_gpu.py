@@ -1,0 +1,175 @@
+"""Prefill parity on the GPU: full-layer double buffering and on-demand groups vs the oracle.
+
+Residency state after every layer must be bit-exact; outputs within 2e-2
+relative max error (h is stored as bf16 between the two GEMMs).
+"""
+import numpy as np
+import pytest
+
+from oracle.cache import SlotCache
+from oracle.ffn import ExpertStore, combine, pair_outputs, relative_max_error
+from tests.harness import TOL, torch_act
+from workloads import Config, Shape, activations, config, make_pool, prefill_routing, routing_trace
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def _make(cfg, C, n_phys=None, max_tokens=None):
+    import torch
+    from serving_layer_moe_gb300 import MoECache
+    s = cfg.shape
+    arena, offs = make_pool(s, cfg.seed, n_phys=n_phys)
+    pool = torch.from_numpy(arena).pin_memory()
+    cache = MoECache(L=s.L, E=s.E, H=s.H, I=s.I, top_k=s.k, max_tokens=max_tokens or 16, wdtype=s.wdtype,
+                     adtype=s.adtype, host_pool=pool, blob_offsets=offs, n_slots=C, bw_pcie_mbps=1000,
+                     bw_cpu_mbps=0, device=0, max_prefill_tokens=cfg.T)
+    store = ExpertStore(arena, offs, s.wdtype, s.H, s.I, s.blob_bytes, memo=2 * s.E + 4)
+    return cache, store
+
+
+def _check_state(cache, ora):
+    g = cache.state()
+    o = ora.state()
+    for name, a, b in zip(["s2e", "stamps", "e2s", "counters"], g[:4], o[:4]):
+        assert np.array_equal(a, b), name
+    assert g[4] == o[4]
+
+
+def _run_prefill(cfg, C, layers, n_phys=None, sample=None, seed=0):
+    import torch
+    s = cfg.shape
+    dev = torch.device("cuda", 0)
+    cache, store = _make(cfg, C, n_phys=n_phys)
+    ora = SlotCache(s.L, s.E, C, K=s.E, b_pcie=1000, b_cpu=0)
+    out = torch.empty(cfg.T, s.H, device=dev)
+    worst = 0.0
+    g = np.random.default_rng(seed)
+    for l in layers:
+        ids, w = prefill_routing(cfg, l)
+        x = activations(cfg, 0, l)
+        plan = ora.prefill(l, ids)
+        cache.prefill(l, torch_act(x, dev), torch.from_numpy(ids).to(dev), torch.from_numpy(w).to(dev), out)
+        torch.cuda.synchronize()
+        _check_state(cache, ora)
+        got = out.cpu().numpy()
+        assert np.all(np.isfinite(got))
+        toks = np.arange(cfg.T) if sample is None else np.sort(g.choice(cfg.T, size=sample, replace=False))
+        mask = np.zeros(ids.shape, bool)
+        mask[toks] = True
+        y = pair_outputs(store, l, s.E, x, s.adtype, ids, mask=mask)
+        ref = combine(w[toks], y[toks], np.zeros((len(toks), s.k), np.int32), None)
+        err = relative_max_error(got[toks], ref)
+        worst = max(worst, err)
+        assert err <= TOL, (l, err)
+    cache.close()
+    return worst, ora
+
+
+SMALL = Config("prefill_small", Shape(L=3, E=8, k=2, H=256, I=128, wdtype="bf16", adtype="bf16"),
+               T=300, steps=1, capacity=16, routing="softmax", seed=4321, prefill=True)
+
+
+def test_small_full_layer_double_buffer():
+    worst, ora = _run_prefill(SMALL, C=16, layers=[0, 1, 2])
+    assert worst < 5e-3
+
+
+def test_small_repeat_and_out_of_order_layers():
+    _run_prefill(SMALL, C=17, layers=[2, 0, 1, 1, 0])
+
+
+def test_small_on_demand_one_group():
+    _run_prefill(SMALL, C=12, layers=[0, 1, 2, 0])      # E <= C < 2E
+
+
+def test_small_on_demand_several_groups():
+    _run_prefill(SMALL, C=3, layers=[0, 1, 2])          # C < E: groups of 3 routed experts
+
+
+def test_ragged_tokens_and_tiny_chunk():
+    for T in (1, 7, 129):
+        _run_prefill(SMALL.with_(T=T), C=16, layers=[0, 1])
+
+
+def test_qwen3_shape_1k_tokens():
+    cfg = config("qwen3_prefill_8k").with_(T=1024)
+    _run_prefill(cfg, C=300, layers=[0, 1, 2], n_phys=64, sample=256)
+
+
+def test_qwen3_prefill_8k_all_layers_state_and_sampled_outputs():
+    import torch
+    cfg = config("qwen3_prefill_8k")
+    s = cfg.shape
+    dev = torch.device("cuda", 0)
+    cache, store = _make(cfg, cfg.capacity, n_phys=64)
+    ora = SlotCache(s.L, s.E, cfg.capacity, K=s.E, b_pcie=1000, b_cpu=0)
+    out = torch.empty(cfg.T, s.H, device=dev)
+    g = np.random.default_rng(7)
+    for l in range(s.L):
+        ids, w = prefill_routing(cfg, l)
+        x = activations(cfg, 0, l)
+        ora.prefill(l, ids)
+        cache.prefill(l, torch_act(x, dev), torch.from_numpy(ids).to(dev), torch.from_numpy(w).to(dev), out)
+        if l in (0, 23, 47):
+            torch.cuda.synchronize()
+            _check_state(cache, ora)
+            toks = np.sort(g.choice(cfg.T, size=48, replace=False))
+            mask = np.zeros(ids.shape, bool)
+            mask[toks] = True
+            y = pair_outputs(store, l, s.E, x, s.adtype, ids, mask=mask)
+            ref = combine(w[toks], y[toks], np.zeros((len(toks), s.k), np.int32), None)
+            err = relative_max_error(out.cpu().numpy()[toks], ref)
+            assert err <= TOL, (l, err)
+    torch.cuda.synchronize()
+    _check_state(cache, ora)
+    cache.close()
+
+
+def test_prefill_survivors_seed_decode():
+    # prefill and decode share one pool: decode after prefill starts from the survivors
+    import torch
+    cfg = SMALL
+    s = cfg.shape
+    dev = torch.device("cuda", 0)
+    cache, store = _make(cfg, 16, max_tokens=4)
+    ora = SlotCache(s.L, s.E, 16, K=s.E if False else min(s.E, 4 * s.k), b_pcie=1000, b_cpu=0)
+    out = torch.empty(cfg.T, s.H, device=dev)
+    for l in range(s.L):
+        ids, w = prefill_routing(cfg, l)
+        ora.prefill(l, ids)
+        cache.prefill(l, torch_act(activations(cfg, 0, l), dev), torch.from_numpy(ids).to(dev),
+                      torch.from_numpy(w).to(dev), out)
+    dcfg = cfg.with_(T=4, steps=6, prefill=False)
+    ids, w = routing_trace(dcfg)
+    sm = torch.empty(4, s.k, dtype=torch.int32, device=dev)
+    o4 = torch.empty(4, s.H, device=dev)
+    hits = 0
+    for st in range(dcfg.steps):
+        for l in range(s.L):
+            plan = ora.decode(l, ids[st, l])
+            hits += len(plan.hits)
+            cache.decode(l, torch_act(activations(dcfg, st, l), dev), torch.from_numpy(ids[st, l]).to(dev),
+                         torch.from_numpy(w[st, l]).to(dev), o4, slot_map=sm)
+            torch.cuda.synchronize()
+            assert np.array_equal(sm.cpu().numpy(), plan.slot_map)
+    _check_state(cache, ora)
+    assert hits > 0
+    cache.close()
+
+
+def test_prefill_rejects_bad_config():
+    import torch
+    from serving_layer_moe_gb300 import MoECache, MoEError
+    cfg = config("tiny")
+    s = cfg.shape
+    arena, offs = make_pool(s, cfg.seed)
+    with pytest.raises(MoEError):   # fp32 weights cannot run the bf16 tensor-core prefill
+        MoECache(L=s.L, E=s.E, H=s.H, I=s.I, top_k=s.k, max_tokens=4, wdtype="f32", adtype="f32",
+                 host_pool=arena, blob_offsets=offs, n_slots=4, max_prefill_tokens=64)

@@ -150,34 +150,27 @@ def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
 def f32_to_e4m3_codes(a: np.ndarray) -> np.ndarray:
     """Encode float32 as OCP FP8 E4M3 codes: nearest, ties to even, saturating at +-448.
 
-    Integer rounding of the float32 mantissa to 3 bits for normal results and
-    of |a| * 2**9 for subnormal results.  NaN inputs are not expected.
+    Normal results: round the binary32 pattern at mantissa bit 20 (carry runs
+    into the exponent), then rebias the exponent from 127 to 7.  Subnormal
+    results (|a| < 2**-6): rint(|a| * 2**9), which rounds half to even.
+    NaN inputs are not expected.
     """
     a = np.ascontiguousarray(a, dtype=np.float32)
-    sign = (a.view(np.uint32) >> 31).astype(np.uint8) << 7
-    v = np.abs(a).astype(np.float32)
-    out = np.zeros(v.shape, dtype=np.uint8)
-    # subnormal range of e4m3: |v| < 2**-6, step 2**-9
-    sub = v < np.float32(2.0 ** -6)
-    m_sub = np.rint(v[sub].astype(np.float64) * 512.0).astype(np.int64)  # rint = half-even
-    out[sub] = m_sub.astype(np.uint8)          # 8 -> 0x08 = smallest normal, as it should be
-    # normal range
-    nv = v[~sub]
-    bits = nv.view(np.uint32).astype(np.int64)
-    exp = ((bits >> 23) & 0xFF) - 127
-    mant = bits & 0x7FFFFF
-    r = mant >> 20
-    rem = mant & 0xFFFFF
-    up = (rem > 0x80000) | ((rem == 0x80000) & ((r & 1) == 1))
-    r = r + up
-    exp = exp + (r >> 3)
-    r = r & 7
-    e_biased = exp + 7
-    code = (e_biased << 3) | r
-    sat = (e_biased > 15) | ((e_biased == 15) & (r == 7))
-    code = np.where(sat, 0x7E, code)
-    out[~sub] = code.astype(np.uint8)
-    return out | sign
+    bits = a.view(np.uint32)
+    mag = bits & np.uint32(0x7FFFFFFF)
+    rnd = (mag >> 20) & np.uint32(1)
+    rnd += np.uint32(0x7FFFF)
+    rnd += mag
+    rnd >>= 20
+    code = rnd.astype(np.int32)
+    code -= 960
+    np.clip(code, 0, 0x7E, out=code)
+    sub = mag < np.uint32(0x3C800000)          # |a| < 2**-6
+    if sub.any():
+        code[sub] = np.rint(mag[sub].view(np.float32) * np.float32(512.0)).astype(np.int32)
+    out = code.astype(np.uint8)
+    out |= ((bits >> 24) & np.uint32(0x80)).astype(np.uint8)
+    return out
 
 
 # ----------------------------------------------------------------------------
