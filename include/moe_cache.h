@@ -221,6 +221,42 @@ moe_status moe_cache_profile(moe_cache* cache, int32_t enable, double* ms_host, 
 moe_status bench_bw(int32_t device, uint64_t expert_bytes, double* b_pcie_gbs, double* b_host_gbs,
                     int32_t* recommend_hybrid);
 
+/*
+ * One MoE layer's expert SwiGLU + combine without allocating any GPU memory.
+ * (This call has no counterpart on the pages; it is an addition for callers
+ * that may not allocate.)
+ *
+ * Who it is for: code that may not call cudaMalloc -- a plug-in running inside
+ * another framework's memory pool, a process that reserved all GPU memory at
+ * start-up, or a runtime that forbids allocations after start so its memory
+ * use stays fixed.  The caller passes inputs and outputs only; every
+ * intermediate lives in one fixed 16 MiB device array inside this library
+ * (every GPU that loads the library holds it until the process exits).
+ *
+ * What it computes: the same output as moe_layer_decode when every routed
+ * expert of the layer is resident and nothing is CPU-assigned:
+ *   out[t] = sum_j w[t,j] * SwiGLU_{ids[t,j]}(x[t]), summed in j order in fp32.
+ *   experts_dev  the layer's E expert blobs back to back (bank layout above,
+ *                S bytes each), device memory, 16-byte aligned
+ *   x_dev [T, H] in adtype, topk_ids_dev / topk_w_dev [T, k], out_dev [T, H] fp32
+ * Ids outside [0, E) contribute nothing.  Enqueued on `stream`; never blocks.
+ *
+ * Limits and sharing:
+ *   - scratch needed ~ T * top_k * (H + I) * 4 bytes plus small lists; a call
+ *     that needs more than 16 MiB returns MOE_ECAPACITY with a message.
+ *   - every call on a device uses the same scratch array and leaves its
+ *     contents behind; each call rewrites everything it reads first, so
+ *     nothing needs clearing, but calls that overlap on the GPU (different
+ *     streams, no ordering between them) race and corrupt each other.
+ *   - the first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ */
+moe_status moe_layer_ffn_noalloc(int32_t n_experts, int32_t hidden, int32_t inter, int32_t top_k,
+                                 int32_t wdtype, int32_t adtype, const void* experts_dev, int32_t T,
+                                 const void* x_dev, const int32_t* topk_ids_dev, const float* topk_w_dev,
+                                 float* out_dev, void* stream);
+
 /* The message of the last failed call on this thread ("" if none). */
 const char* moe_last_error(void);
 

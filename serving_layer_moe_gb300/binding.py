@@ -22,7 +22,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_EINVAL", 2: "MOE_ENOMEM", 3: "MOE_ECUDA", 4: "MOE
 # exported symbols of include/moe_cache.h
 SYMBOLS = ("moe_cache_create", "moe_cache_destroy", "moe_cache_resize", "moe_layer_decode",
            "moe_layer_prefill", "moe_cache_get_state", "moe_cache_get_plan", "moe_cache_info",
-           "moe_cache_profile", "bench_bw", "moe_last_error")
+           "moe_cache_profile", "bench_bw", "moe_layer_ffn_noalloc", "moe_last_error")
 
 
 class MoEConfigC(ctypes.Structure):
@@ -63,6 +63,7 @@ def load_library():
     lib.moe_cache_profile.argtypes = [P, I32, P, P]
     lib.bench_bw.argtypes = [I32, U64, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
                              ctypes.POINTER(I32)]
+    lib.moe_layer_ffn_noalloc.argtypes = [I32, I32, I32, I32, I32, I32, P, I32, P, P, P, P, P]
     lib.moe_last_error.restype = ctypes.c_char_p
     for name in SYMBOLS[:-1]:
         getattr(lib, name).restype = ctypes.c_int
@@ -209,3 +210,16 @@ def bench_bw(device: int, expert_bytes: int):
     bp, bh, rec = ctypes.c_double(), ctypes.c_double(), ctypes.c_int32()
     _check(lib.bench_bw(device, int(expert_bytes), ctypes.byref(bp), ctypes.byref(bh), ctypes.byref(rec)))
     return bp.value, bh.value, bool(rec.value)
+
+def ffn_noalloc(experts, x, topk_ids, topk_w, out, *, E, H, I, top_k, wdtype, adtype, stream=None):
+    """moe_layer_ffn_noalloc: all-resident expert SwiGLU + combine that allocates no GPU memory.
+
+    For callers that may not allocate: every intermediate lives in the
+    library's fixed device scratch array.  experts: the layer's E blobs back to
+    back on the device.  Calls that overlap on the GPU share that scratch and
+    race; order them on one stream.
+    """
+    T = topk_ids.shape[0]
+    _check(load_library().moe_layer_ffn_noalloc(E, H, I, top_k, DTYPES.get(wdtype, wdtype),
+                                                DTYPES.get(adtype, adtype), _ptr(experts), T, _ptr(x),
+                                                _ptr(topk_ids), _ptr(topk_w), _ptr(out), _stream(stream)))
