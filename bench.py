@@ -51,7 +51,12 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the oracle CPU baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-prefill", action="store_true")
+    p.add_argument("--mode", default="all", choices=["all", "decode", "prefill"],
+                   help="prefill: only the prefill measurement (small profiling runs)")
+    p.add_argument("--prefill-tokens", type=int, default=8192)
+    p.add_argument("--capacity", type=int, default=0, help="override the slot count (small profiling runs)")
     p.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
+    p.add_argument("--cpu-samples", type=int, default=1, help=argparse.SUPPRESS)
     return p.parse_args(argv)
 
 
@@ -127,8 +132,13 @@ class ClockSampler:
 # ----------------------------------------------------------------------------
 # the oracle as CPU baseline (runs in a fresh interpreter: no fork after CUDA init)
 # ----------------------------------------------------------------------------
-def cpu_worker(seconds: float, pool_blobs: int, bw):
-    """Oracle control + float64 SwiGLU on successive layer-steps of the workload until the budget ends."""
+def cpu_worker(seconds: float, pool_blobs: int, bw, samples: int = 1):
+    """Oracle control + float64 SwiGLU on successive layer-steps of the workload.
+
+    Prints one JSON line per sample; each sample runs until `seconds` of oracle
+    time are spent.  Generating the synthetic expert blobs (input synthesis) is
+    not counted; parsing them to float64 is (the oracle reads its weights).
+    """
     from oracle.cache import SlotCache
     from oracle.ffn import combine, swiglu_expert
     from oracle.formats import activations_to_f64, parse_blob
@@ -137,45 +147,50 @@ def cpu_worker(seconds: float, pool_blobs: int, bw):
     ids, w = routing_trace(cfg)
     K = default_max_fetch(s, cfg.T)
     ora = SlotCache(s.L, s.E, cfg.capacity, K, bw[0], bw[1])
-    blobs = {}
-    t0 = time.perf_counter()
-    n = 0
-    st = 0
-    while time.perf_counter() - t0 < seconds:
-        for l in range(s.L):
-            plan = ora.decode(l, ids[st % cfg.steps, l])
-            x = activations_to_f64(activations(cfg, st % cfg.steps, l), s.adtype)
+    raw = {}
+    st, l = 0, 0
+    for _ in range(samples):
+        spent, n = 0.0, 0
+        while spent < seconds:
+            sid = st % cfg.steps
+            need = {(l * s.E + int(e)) % pool_blobs for e in ids[sid, l].ravel()}
+            for p in need - raw.keys():
+                raw[p] = make_blob(s, cfg.seed, p)          # input synthesis, not timed
+            xs = activations(cfg, sid, l)
+            t0 = time.perf_counter()
+            plan = ora.decode(l, ids[sid, l])
+            x = activations_to_f64(xs, s.adtype)
             y = np.zeros((cfg.T, s.k, s.H))
             for t in range(cfg.T):
                 for j in range(s.k):
-                    f = l * s.E + int(ids[st % cfg.steps, l, t, j])
-                    p = f % pool_blobs
-                    if p not in blobs:
-                        blobs[p] = parse_blob(make_blob(s, cfg.seed, p), s.wdtype, s.H, s.I)
-                    y[t, j] = swiglu_expert(x[t], *blobs[p])
-            combine(w[st % cfg.steps, l], y, plan.slot_map, y)
+                    p = (l * s.E + int(ids[sid, l, t, j])) % pool_blobs
+                    y[t, j] = swiglu_expert(x[t], *parse_blob(raw[p], s.wdtype, s.H, s.I))
+            combine(w[sid, l], y, plan.slot_map, y)
+            spent += time.perf_counter() - t0
             n += 1
-            if time.perf_counter() - t0 >= seconds:
-                break
-        st += 1
-    dt = time.perf_counter() - t0
-    print(json.dumps({"layer_steps": n, "seconds": dt}))
+            l += 1
+            if l == s.L:
+                l, st = 0, st + 1
+        print(json.dumps({"layer_steps": n, "seconds": spent}), flush=True)
 
 
-def run_cpu_baseline(seconds: float, pool_blobs: int, bw):
+def run_cpu_baseline(seconds: float, pool_blobs: int, bw, samples: int = 1):
+    """Run the oracle in a fresh interpreter (no fork after CUDA init); one dict per sample."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
     cmd = [sys.executable, os.path.abspath(__file__), "--cpu-worker", "--cpu-seconds", str(seconds),
-           "--pool-blobs", str(pool_blobs)]
+           "--pool-blobs", str(pool_blobs), "--cpu-samples", str(samples)]
     env["BENCH_BW"] = f"{bw[0]},{bw[1]}"
-    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=seconds * 4 + 120)
-    line = [l for l in r.stdout.splitlines() if l.startswith("{")]
-    if r.returncode != 0 or not line:
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=samples * (seconds * 4 + 60) + 120)
+    lines = [json.loads(l) for l in r.stdout.splitlines() if l.startswith("{")]
+    if r.returncode != 0 or not lines:
         return None
-    d = json.loads(line[-1])
-    return {"value": d["layer_steps"] / d["seconds"], "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{d['layer_steps']} layer-steps of {WORKLOAD} from step 0 (list-LRU control + "
-                      f"float64 SwiGLU per routed pair + fixed-order combine), one thread, "
-                      f"{d['seconds']:.1f} s"}
+    out = []
+    for d in lines:
+        out.append({"value": d["layer_steps"] / d["seconds"], "unit": UNIT, "cores": 1, "kind": "oracle",
+                    "sample": f"{d['layer_steps']} layer-steps of {WORKLOAD} (list-LRU control + float64 SwiGLU "
+                              f"per routed pair from the host pool + fixed-order combine), one thread, "
+                              f"{d['seconds']:.1f} s of oracle time"})
+    return out if samples > 1 else out[0]
 
 
 # ----------------------------------------------------------------------------
@@ -194,10 +209,16 @@ def main(args):
         return reference_arm(args, world, rank)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if args.mode == "prefill":
+        if rank == 0:
+            print(json.dumps({"prefill": prefill_measure(args, dev, local)}))
+        return
 
     from serving_layer_moe_gb300 import MoECache, bench_bw
 
     cfg = config(WORKLOAD)
+    if args.capacity:
+        cfg = cfg.with_(capacity=args.capacity)
     s = cfg.shape
     # calibration: B_P through the fill path, B_H host read; B_cpu = residual
     bp_gbs, bh_gbs, rec = bench_bw(local, s.blob_bytes)
@@ -250,7 +271,7 @@ def main(args):
             enqueue_step()
         torch.cuda.synchronize(dev)
 
-    launches_per_layer = 7
+    launches_per_layer = 5    # control, fill, gate/up resident, gate/up filled, down + combine
     # ---- timed region: inputs resident in HBM ---------------------------------
     cnt0 = cache.state()[3].copy()
     if world > 1:
@@ -313,22 +334,34 @@ def main(args):
     h2d = xb.numel() * 2 + ib.numel() * 4 + wb.numel() * 4
     d2h = out.numel() * 4
 
-    # ---- kernel timing for the roofline (library CUDA events, eager launches) ----------
+    # ---- kernel timing for the roofline: library CUDA events captured into a graph ----
+    # (a second graph of the same step with an event pair around each kernel group;
+    # after each replay the pairs hold that replay's device times)
     prof_steps = 32
-    cnt_p0 = cache.state()[3].copy()
     cache.profile_start()
+    pgraph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(pgraph, stream=stream):
+        enqueue_step()
+    cache.profile_pause()
+    torch.cuda.synchronize(dev)
+    cnt_p0 = cache.state()[3].copy()
+    prof = {k: [0.0, 0] for k in cache.PROFILE_KINDS}
     with torch.cuda.stream(stream):
         for _ in range(prof_steps):
             stage(step)
-            enqueue_step()
+            pgraph.replay()
             step += 1
-    prof = cache.profile_stop()
+            for k, (ms_k, n_k) in cache.profile_read().items():
+                prof[k][0] += ms_k
+                prof[k][1] += n_k
+    cache.profile_stop()
     cnt_p1 = cache.state()[3].copy()
     hbm_peak, bf16_peak, bf16_sust, peak_src = measured_peaks()
     gpu_experts = int((cnt_p1[0] - cnt_p0[0]) + (cnt_p1[2] - cnt_p0[2]))   # hits + fills executed
     gemv_bytes = gpu_experts * s.blob_bytes
-    gemv_ms = prof["gemv_resident"][0] + prof["gemv_filled"][0]
-    gemv_launches = prof["gemv_resident"][1] + prof["gemv_filled"][1]
+    gemv_kinds = ("gate_up_resident", "gate_up_filled", "down_combine")
+    gemv_ms = sum(prof[k][0] for k in gemv_kinds)
+    gemv_launches = prof["down_combine"][1]          # one per MoE-layer decode
     fill_bytes = int(cnt_p1[2] - cnt_p0[2]) * s.blob_bytes
     total_prof_ms = sum(v[0] for v in prof.values())
 
@@ -352,21 +385,23 @@ def main(args):
         "e2e": {"value": round(e2e_steps * s.L * world / (ms_e2e / 1e3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": args.steps * s.L * launches_per_layer,
-        "roofline": {"bound": "hbm", "kernel": "expert GEMV (gate/up + down) over resident and filled slots",
+        "roofline": {"bound": "hbm", "kernel": "expert GEMV per layer-step: gate/up of resident + filled slots, "
+                                               "down projection fused with the combine",
                      "achieved": round(gemv_bytes / (gemv_ms / 1e3) / 1e9, 1) if gemv_ms > 0 else None,
                      "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(gemv_bytes / (gemv_ms / 1e3) / 1e9 / hbm_peak, 3) if gemv_ms > 0 else None,
                      "peak_source": peak_src, "traffic": None,
-                     "bytes_per_launch": round(gemv_bytes / max(1, gemv_launches)),
-                     "launches_timed": gemv_launches},
+                     "bytes_per_layer_step": round(gemv_bytes / max(1, gemv_launches)),
+                     "layer_steps_timed": gemv_launches},
         "kernel_ms_share": {k: round(v[0] / total_prof_ms, 3) for k, v in prof.items() if v[1]},
+        "kernel_us_per_layer": {k: round(1e3 * v[0] / max(1, v[1]), 2) for k, v in prof.items() if v[1]},
         "fill": {"achieved_gbs": round(fill_bytes / (prof["fill"][0] / 1e3) / 1e9, 1) if prof["fill"][0] > 0 else None,
                  "bench_bw_B_P_gbs": round(bp_gbs, 1), "note": "fill kernel time includes waiting for nothing; "
                  "it runs on the side stream concurrently with the resident-expert GEMV"},
         "control_us": round(1e3 * prof["control"][0] / max(1, prof["control"][1]), 2),
         "clocks": clk.summary(),
     }
-    if not args.no_prefill:
+    if not args.no_prefill and args.mode == "all":
         result["prefill"] = prefill_measure(args, dev, local)
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = run_cpu_baseline(args.cpu_seconds, args.pool_blobs, (b_pcie, b_cpu))
@@ -378,8 +413,80 @@ def main(args):
 
 
 def prefill_measure(args, dev, local):
-    """Prefill chunk: 8192 tokens through 48 layers with full-layer double buffering (if built)."""
-    return None
+    """Prefill chunk: 8192 tokens through all 48 layers with full-layer double buffering.
+
+    Reports the wall time of the chunk (bound by the host link: every layer's
+    experts cross it once), the grouped-GEMM TFLOP/s inside that run, and the
+    GEMM TFLOP/s of a layer whose experts are already resident (no concurrent
+    loads).  One activation matrix x (N(0,1), bf16) serves every layer.
+    """
+    import torch
+    from serving_layer_moe_gb300 import MoECache
+    cfg = config("qwen3_prefill_8k").with_(T=args.prefill_tokens)
+    s = cfg.shape
+    arena, offs = make_pool(s, cfg.seed, n_phys=args.pool_blobs)
+    pool = torch.from_numpy(arena).pin_memory()
+    del arena
+    cache = MoECache(L=s.L, E=s.E, H=s.H, I=s.I, top_k=s.k, max_tokens=1, wdtype=s.wdtype, adtype=s.adtype,
+                     host_pool=pool, blob_offsets=offs, n_slots=cfg.capacity, bw_pcie_mbps=1000, bw_cpu_mbps=0,
+                     device=local, max_prefill_tokens=cfg.T)
+    x = torch.from_numpy(activations(cfg, 0, 0).view(np.int16)).to(dev)
+    routes = [prefill_routing(cfg, l) for l in range(s.L)]
+    ids = [torch.from_numpy(r[0]).to(dev) for r in routes]
+    ws = [torch.from_numpy(r[1]).to(dev) for r in routes]
+    out = torch.empty(cfg.T, s.H, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    flops_layer = 6.0 * s.H * s.I * cfg.T * s.k
+    hbm_peak, bf16_peak, bf16_sust, src = measured_peaks()
+
+    def chunk():
+        for l in range(s.L):
+            cache.prefill(l, x, ids[l], ws[l], out, stream=stream)
+
+    with torch.cuda.stream(stream):
+        chunk()                                   # warm-up (cold cache)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        chunk()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    wall_ms = e0.elapsed_time(e1)
+    cache.profile_start()
+    with torch.cuda.stream(stream):
+        chunk()
+    prof = cache.profile_stop()
+    gemm_ms = prof["prefill_gemm"][0]
+    load_ms = prof["prefill_load"][0]
+    # isolated: layer 0 again and again, its experts (and layer 1's) stay resident
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            cache.prefill(0, x, ids[0], ws[0], out, stream=stream)
+    torch.cuda.synchronize(dev)
+    cnt0 = cache.state()[3].copy()
+    cache.profile_start()
+    reps = 10
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            cache.prefill(0, x, ids[0], ws[0], out, stream=stream)
+    iso = cache.profile_stop()
+    loads_iso = int(cache.state()[3][7] - cnt0[7])
+    cache.close()
+    iso_tf = reps * flops_layer / (iso["prefill_gemm"][0] / 1e3) / 1e12
+    return {"workload": f"qwen3_prefill_8k: {cfg.T} tokens, top-8 of 128 (N(0,1) logits), 48 layers, "
+                        f"C={cfg.capacity} slots, full-layer double buffering",
+            "wall_ms": round(wall_ms, 2), "tokens_per_s": round(cfg.T / (wall_ms / 1e3), 1),
+            "expert_bytes_per_chunk": int(s.L * s.E * s.blob_bytes),
+            "link_gbs_wall": round(s.L * s.E * s.blob_bytes / (wall_ms / 1e3) / 1e9, 1),
+            "gemm_ms_in_chunk": round(gemm_ms, 3),
+            "gemm_tflops_in_chunk": round(s.L * flops_layer / (gemm_ms / 1e3) / 1e12, 1),
+            "load_ms_in_chunk": round(load_ms, 2),
+            "gemm_tflops_isolated": round(iso_tf, 1),
+            "gemm_frac_isolated": round(iso_tf / bf16_peak, 3),
+            "tensor_peak_tflops": bf16_peak, "peak_source": src,
+            "loads_during_isolated": loads_iso,
+            "flops_per_layer": flops_layer}
 
 
 def reference_arm(args, world, rank):
@@ -389,11 +496,10 @@ def reference_arm(args, world, rank):
     b = os.environ.get("BENCH_BW", "200000,100000").split(",")
     bw = (int(b[0]), int(b[1]))
     per_step = max(2.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
-    vals = []
-    for i in range(args.warmup + args.steps):
-        r = run_cpu_baseline(per_step, args.pool_blobs, bw)
-        if r and i >= args.warmup:
-            vals.append(r["value"])
+    res = run_cpu_baseline(per_step, args.pool_blobs, bw, samples=args.warmup + args.steps)
+    if isinstance(res, dict):
+        res = [res]
+    vals = [r["value"] for r in (res or [])[args.warmup:]]
     v = statistics.mean(vals) if vals else None
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
@@ -409,6 +515,6 @@ if __name__ == "__main__":
     a = parse_args()
     if a.cpu_worker:
         b = os.environ.get("BENCH_BW", "200000,100000").split(",")
-        cpu_worker(a.cpu_seconds, a.pool_blobs, (int(b[0]), int(b[1])))
+        cpu_worker(a.cpu_seconds, a.pool_blobs, (int(b[0]), int(b[1])), samples=a.cpu_samples)
     else:
         main(a)

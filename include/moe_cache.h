@@ -199,15 +199,19 @@ moe_status moe_cache_get_plan(moe_cache* cache, int32_t* scalars_host, int32_t* 
 moe_status moe_cache_info(moe_cache* cache, uint64_t* info_host);
 
 /*
- * Kernel timing.  enable = 1: start recording a CUDA event pair around every kernel
- * group the cache launches (events are created on demand, so do not start profiling
- * while a stream is being captured).  enable = 0: stop, synchronise, and return per
- * kind the summed milliseconds and the number of timed groups since the start, kinds
- * 0 control, 1 fill, 2 GEMV of resident experts, 3 GEMV of filled experts, 4 combine,
+ * Kernel timing with CUDA event pairs around every kernel group the cache
+ * launches.  mode 1: start (reset; 4096 event pairs are created here, so a
+ * stream capture that follows records into existing events); mode 3: pause
+ * (keep the pairs recorded so far, e.g. those captured into a graph, record no
+ * new ones); mode 2: synchronise and read the sums over the recorded pairs
+ * (after each replay of a captured graph its pairs hold that replay's times);
+ * mode 0: stop, read and reset.  Per kind the summed milliseconds and the
+ * number of timed groups: 0 control, 1 fill, 2 gate/up GEMV of resident
+ * experts, 3 gate/up GEMV of filled experts, 4 down-projection GEMV + combine,
  * 5 prefill control, 6 prefill load, 7 prefill grouped GEMM.  ms_host[8] and
  * launches_host[8] may be NULL.
  */
-moe_status moe_cache_profile(moe_cache* cache, int32_t enable, double* ms_host, uint64_t* launches_host);
+moe_status moe_cache_profile(moe_cache* cache, int32_t mode, double* ms_host, uint64_t* launches_host);
 
 /*
  * Calibrate on `device` with expert-sized blobs of expert_bytes (rounded up to 16).

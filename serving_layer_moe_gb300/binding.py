@@ -174,18 +174,29 @@ class MoECache:
             out["y"] = y
         return out
 
-    PROFILE_KINDS = ("control", "fill", "gemv_resident", "gemv_filled", "combine",
+    PROFILE_KINDS = ("control", "fill", "gate_up_resident", "gate_up_filled", "down_combine",
                      "prefill_control", "prefill_load", "prefill_gemm")
 
     def profile_start(self):
         _check(load_library().moe_cache_profile(self._h, 1, None, None))
 
-    def profile_stop(self):
-        """{kind: (milliseconds, timed launches)} since profile_start()."""
+    def _profile(self, mode):
         ms = np.zeros(8, np.float64)
         n = np.zeros(8, np.uint64)
-        _check(load_library().moe_cache_profile(self._h, 0, _ptr(ms), _ptr(n)))
+        _check(load_library().moe_cache_profile(self._h, mode, _ptr(ms), _ptr(n)))
         return {k: (float(ms[i]), int(n[i])) for i, k in enumerate(self.PROFILE_KINDS)}
+
+    def profile_stop(self):
+        """{kind: (milliseconds, timed launches)} since profile_start(); stops and resets."""
+        return self._profile(0)
+
+    def profile_pause(self):
+        """Keep the pairs recorded so far (e.g. captured into a graph); record no new ones."""
+        _check(load_library().moe_cache_profile(self._h, 3, None, None))
+
+    def profile_read(self):
+        """{kind: (milliseconds, launches)} over the recorded pairs, without resetting."""
+        return self._profile(2)
 
     def info(self):
         info = np.empty(8, np.uint64)
@@ -210,6 +221,7 @@ def bench_bw(device: int, expert_bytes: int):
     bp, bh, rec = ctypes.c_double(), ctypes.c_double(), ctypes.c_int32()
     _check(lib.bench_bw(device, int(expert_bytes), ctypes.byref(bp), ctypes.byref(bh), ctypes.byref(rec)))
     return bp.value, bh.value, bool(rec.value)
+
 
 def ffn_noalloc(experts, x, topk_ids, topk_w, out, *, E, H, I, top_k, wdtype, adtype, stream=None):
     """moe_layer_ffn_noalloc: all-resident expert SwiGLU + combine that allocates no GPU memory.

@@ -187,6 +187,7 @@ extern "C" moe_status moe_cache_create(const moe_config* cfg, const void* host_p
   } while (0)
 
   CKB(setup_control_kernels());
+  CKB(setup_gemv_kernels());
   CKB(cudaMalloc(&c->offsets, nflat * sizeof(uint64_t)));
   CKB(cudaMemcpy(c->offsets, offs.data(), nflat * sizeof(uint64_t), cudaMemcpyHostToDevice));
   CKB(cudaMalloc(&c->slots, c->C * S));
@@ -232,7 +233,12 @@ extern "C" moe_status moe_cache_create(const moe_config* cfg, const void* host_p
   CKB(cudaHostAlloc(&c->err_host, sizeof(uint32_t), cudaHostAllocMapped));
   *c->err_host = 0;
   CKB(cudaHostGetDevicePointer(reinterpret_cast<void**>(&c->err_dev), c->err_host, 0));
-  CKB(cudaStreamCreateWithFlags(&c->fill_stream, cudaStreamNonBlocking));
+  {
+    // fills gate the filled experts' GEMV: give their CTAs first pick of free SM slots
+    int least = 0, greatest = 0;
+    CKB(cudaDeviceGetStreamPriorityRange(&least, &greatest));
+    CKB(cudaStreamCreateWithPriority(&c->fill_stream, cudaStreamNonBlocking, greatest));
+  }
   CKB(cudaEventCreateWithFlags(&c->ev_ctrl, cudaEventDisableTiming));
   CKB(cudaEventCreateWithFlags(&c->ev_fill, cudaEventDisableTiming));
   if (k.max_prefill_tokens > 0) {
@@ -251,8 +257,8 @@ extern "C" moe_status moe_cache_destroy(moe_cache* c) {
 }
 
 // ---------------------------------------------------------------------------
-// decode: control -> [fill on the side stream] -> GEMV of resident experts ->
-//         wait fills -> GEMV of filled experts -> combine
+// decode: control -> [fill on the side stream] -> gate/up of resident experts ->
+//         wait fills -> gate/up of filled experts -> down projection + combine
 // ---------------------------------------------------------------------------
 extern "C" moe_status moe_layer_decode(moe_cache* c, int32_t layer, int32_t T, const void* x,
                                        const int32_t* ids, const float* w, const float* cpu_part,
@@ -281,17 +287,17 @@ extern "C" moe_status moe_layer_decode(moe_cache* c, int32_t layer, int32_t T, c
   }
   CK(cudaEventRecord(c->ev_fill, c->fill_stream));
   {
-    ProfScope p(c, s, PROF_GEMV_RESIDENT);
-    CK(launch_expert_gemv(c->sh, 0, T, x, c->b, c->sms, s));
+    ProfScope p(c, s, PROF_GATE_UP_RESIDENT);
+    CK(launch_gate_up(c->sh, 0, T, x, c->b, c->sms, s));
   }
   CK(cudaStreamWaitEvent(s, c->ev_fill, 0));
   {
-    ProfScope p(c, s, PROF_GEMV_FILLED);
-    CK(launch_expert_gemv(c->sh, 1, T, x, c->b, c->sms, s));
+    ProfScope p(c, s, PROF_GATE_UP_FILLED);
+    CK(launch_gate_up(c->sh, 1, T, x, c->b, c->sms, s));
   }
   {
-    ProfScope p(c, s, PROF_COMBINE);
-    CK(launch_combine(c->sh, T, w, cpu_part, c->b, out, c->err_dev, s));
+    ProfScope p(c, s, PROF_DOWN_COMBINE);
+    CK(launch_down_combine(c->sh, T, w, cpu_part, c->b, out, c->err_dev, c->sms, s));
   }
   return MOE_OK;
 }
@@ -383,15 +389,27 @@ extern "C" moe_status moe_cache_resize(moe_cache* c, uint64_t n_slots) {
   return MOE_OK;
 }
 
-extern "C" moe_status moe_cache_profile(moe_cache* c, int32_t enable, double* ms_host, uint64_t* launches_host) {
+extern "C" moe_status moe_cache_profile(moe_cache* c, int32_t mode, double* ms_host, uint64_t* launches_host) {
   if (!c) return fail(MOE_EINVAL, "cache is NULL");
+  if (mode < 0 || mode > 3) return fail(MOE_EINVAL, "profile mode must be 0..3");
   DeviceGuard guard(c->cfg.device);
-  if (enable) {
+  if (mode == 1) {            // start: reset and record; pre-create events so capture never creates any
+    while (c->prof_events.size() < 2 * 4096) {
+      cudaEvent_t e;
+      CK(cudaEventCreate(&e));
+      c->prof_events.push_back(e);
+    }
+    c->prof_kind.resize(c->prof_events.size() / 2);
     c->prof_used = 0;
     c->profiling = true;
     return MOE_OK;
   }
-  c->profiling = false;
+  if (mode == 3) {            // pause: keep the recorded pairs, record no new ones
+    c->profiling = false;
+    return MOE_OK;
+  }
+  // 0 = stop + read + reset, 2 = read only
+  if (mode == 0) c->profiling = false;
   CK(cudaDeviceSynchronize());
   double ms[PROF_KINDS] = {0};
   uint64_t n[PROF_KINDS] = {0};
@@ -405,7 +423,7 @@ extern "C" moe_status moe_cache_profile(moe_cache* c, int32_t enable, double* ms
     if (ms_host) ms_host[k] = ms[k];
     if (launches_host) launches_host[k] = n[k];
   }
-  c->prof_used = 0;
+  if (mode == 0) c->prof_used = 0;
   return MOE_OK;
 }
 

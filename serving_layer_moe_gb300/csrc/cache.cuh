@@ -89,10 +89,18 @@ struct ProfScope {
     }
     idx = c->prof_used++;
     c->prof_kind[idx] = kind;
-    cudaEventRecord(c->prof_events[2 * idx], s);
+    record(c->prof_events[2 * idx]);
   }
   ~ProfScope() {
-    if (idx != (size_t)-1) cudaEventRecord(c->prof_events[2 * idx + 1], s);
+    if (idx != (size_t)-1) record(c->prof_events[2 * idx + 1]);
+  }
+  // inside a stream capture a plain record only joins streams; an external record
+  // becomes a real event node that every replay re-records
+  void record(cudaEvent_t e) {
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    cudaStreamIsCapturing(s, &st);
+    if (st == cudaStreamCaptureStatusActive) cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+    else cudaEventRecord(e, s);
   }
 };
 

@@ -23,18 +23,24 @@
 //     stamped in ascending flat id with the next values of one global clock;
 //     CPU-assigned experts are not touched.
 //
-// Design for one SM: the routed set is a bitmap over E experts in shared
-// memory (dedup = atomicOr, order = popcount prefix); hit/miss ranks come from
-// warp ballots; the K smallest of C 64-bit keys come from an MSB radix select
-// with 8-bit digits (a 256-bin shared histogram per digit, only the digits the
-// current clock can reach), after which the K survivors are ranked by
-// comparison.  Cost is a few passes over the stamp array regardless of how
-// many misses occurred.
+// Design for one SM: everything the decision needs (the routed ids, this
+// layer's slice of the flat-id -> slot table, every slot's LRU key, the clock)
+// is loaded into shared memory in one parallel pass, so the critical path has
+// a single global-memory round trip; the rest runs out of shared memory.  The
+// routed set is a bitmap over E experts (dedup = atomicOr, order = popcount
+// prefix), hit/miss ranks come from warp ballots.  The K smallest keys (K <=
+// 32) come from one pass in which each warp extracts its own K smallest by
+// repeated warp-minimum and warp 0 merges the 32 sorted lists; for larger K an
+// MSB radix select with 8-bit digits over the shared keys.  Cost does not
+// depend on how many misses occurred.
 #include "internal.cuh"
 
 namespace moe {
 
 namespace {
+
+constexpr int kSmemKeyCap = 12288;   // slots whose keys are cached in shared memory
+constexpr size_t kCtrlSmemLimit = 200 * 1024;
 
 struct CtrlArgs {
   int layer, T, k, E, C, K, n_shared;
@@ -48,6 +54,7 @@ struct CtrlArgs {
   const uint8_t* shared_blob;   // this layer's shared expert, or null
   uint32_t* err;
   int umax;                     // min(E, T*k)
+  int cache_keys;               // keys of all C slots fit in shared memory
 };
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
@@ -67,49 +74,75 @@ __device__ __forceinline__ uint32_t q_star(uint32_t m, uint32_t bp, uint32_t bc)
   return (uint32_t)q;
 }
 
+__device__ __forceinline__ unsigned long long warp_min_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
+    v = w < v ? w : v;
+  }
+  return v;
+}
+
 // shared scalars of the control CTA
 struct CtrlScalars {
-  int bad, u, h, m, q, keff, ngpu, ntouch, ncand, digit, kth, read_hits, read_misses;
+  int bad, u, h, m, q, keff, ncand, digit, kth, read_hits, read_misses;
   unsigned long long clock0;
 };
 
+template <bool kRadix>
 __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ CtrlScalars sc;
-  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31;
-  const int NW = (a.E + 31) >> 5;
+  __shared__ unsigned long long wcand[(kCtrlThreads / 32) * 32];   // per-warp sorted candidates (K <= 32)
+  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
+  const int E = a.E, NW = (E + 31) >> 5;
   const int P = a.T * a.k;
   const int U = a.umax;
+  const int C = a.C;
 
-  // shared layout
-  uint32_t* ebits = reinterpret_cast<uint32_t*>(smem);       // [NW]
-  uint32_t* ebase = ebits + NW;                                // [NW + 1]
-  int32_t* uniq_e = reinterpret_cast<int32_t*>(ebase + NW + 1);// [U]
-  int32_t* uniq_slot = uniq_e + U;                             // [U]
-  int32_t* uniq_rank = uniq_slot + U;                          // [U] hit rank or miss rank
-  int32_t* uniq_cls = uniq_rank + U;                           // [U] 0 hit, 1 fill, 2 cpu
-  int32_t* miss_list = uniq_cls + U;                           // [U] unique index by miss rank
-  int32_t* gcnt = miss_list + U;                               // [U + 2] pairs per GPU expert
-  uint32_t* hist = reinterpret_cast<uint32_t*>(gcnt + U + 2);  // [256]
+  // shared layout (8-byte arrays first)
+  unsigned long long* rawkey = reinterpret_cast<unsigned long long*>(smem);        // [C] if cached
+  int32_t* slotf = reinterpret_cast<int32_t*>(rawkey + (a.cache_keys ? C : 0));   // [C] if cached
+  int32_t* lslot = slotf + (a.cache_keys ? C : 0);                                 // [E] slot of each e of layer
+  int32_t* pid = lslot + E;                                                        // [P] routed ids
+  uint32_t* ebits = reinterpret_cast<uint32_t*>(pid + P);                          // [NW]
+  uint32_t* ebase = ebits + NW;                                                    // [NW + 1]
+  int32_t* uniq_e = reinterpret_cast<int32_t*>(ebase + NW + 1);                    // [U]
+  int32_t* uniq_slot = uniq_e + U;                                                 // [U]
+  int32_t* uniq_rank = uniq_slot + U;                                              // [U]
+  int32_t* uniq_cls = uniq_rank + U;                                               // [U] 0 hit, 1 fill, 2 cpu
+  int32_t* miss_list = uniq_cls + U;                                               // [U]
+  int32_t* gcnt = miss_list + U;                                                   // [U + 2]
+  int32_t* vict = gcnt + U + 2;                                                    // [K]
+  uint32_t* hist = reinterpret_cast<uint32_t*>(vict + a.K);                        // [256]
   unsigned long long* cand = reinterpret_cast<unsigned long long*>(
-      (reinterpret_cast<uintptr_t>(hist + 256) + 7) & ~uintptr_t(7));  // [K]
+      (reinterpret_cast<uintptr_t>(hist + 256) + 7) & ~uintptr_t(7));               // [K]
 
-  const int32_t* e2s = a.tab.e2s;
   int32_t* s2e = a.tab.s2e;
   uint64_t* stamp = a.tab.stamp;
-  const int fbase = a.layer * a.E;
+  const int fbase = a.layer * E;
 
-  // ---- 1. dedup: routed-expert bitmap ------------------------------------
-  for (int i = tid; i < NW; i += nt) ebits[i] = 0u;
+  // ---- 0. one parallel load of everything the decision reads ----------------
   if (tid == 0) {
     sc.bad = 0; sc.ncand = 0; sc.read_hits = 0; sc.read_misses = 0;
     sc.clock0 = (unsigned long long)*a.tab.clock;
   }
+  for (int i = tid; i < NW; i += nt) ebits[i] = 0u;
   for (int i = tid; i < U + 2; i += nt) gcnt[i] = 0;
+  for (int p = tid; p < P; p += nt) pid[p] = a.ids[p];
+  for (int e = tid; e < E; e += nt) lslot[e] = a.tab.e2s[fbase + e];
+  if (a.cache_keys) {
+    for (int s = tid; s < C; s += nt) {
+      slotf[s] = s2e[s];
+      rawkey[s] = ((unsigned long long)stamp[s] << kSlotBits) | (unsigned long long)s;
+    }
+  }
   __syncthreads();
+
+  // ---- 1. dedup: routed-expert bitmap ------------------------------------
   for (int p = tid; p < P; p += nt) {
-    const int e = a.ids[p];
-    if ((unsigned)e >= (unsigned)a.E) atomicOr(&sc.bad, 1);
+    const int e = pid[p];
+    if ((unsigned)e >= (unsigned)E) atomicOr(&sc.bad, 1);
     else atomicOr(&ebits[e >> 5], 1u << (e & 31));
   }
   __syncthreads();
@@ -131,17 +164,15 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
   }
   __syncthreads();
   const int u = sc.u;
-  for (int e = tid; e < a.E; e += nt) {
+  // ---- 2. unique list (ascending flat id) and classification --------------
+  for (int e = tid; e < E; e += nt) {
     const uint32_t wbits = ebits[e >> 5];
     if (wbits & (1u << (e & 31))) {
       const int idx = ebase[e >> 5] + __popc(wbits & ((1u << (e & 31)) - 1u));
       uniq_e[idx] = e;
+      uniq_slot[idx] = lslot[e];
     }
   }
-  __syncthreads();
-
-  // ---- 2. classify against the residency table ----------------------------
-  for (int i = tid; i < u; i += nt) uniq_slot[i] = e2s[fbase + uniq_e[i]];
   __syncthreads();
   if (tid < 32) {  // hit / miss ranks in ascending flat id
     int hb = 0, mb = 0;
@@ -166,7 +197,7 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
       sc.h = hb;
       sc.m = mb;
       // ---- 3. the split q ----------------------------------------------------
-      const int V = a.C - hb;  // slots this call may evict
+      const int V = C - hb;  // slots this call may evict
       int q = 0;
       if (mb > 0) {
         q = (int)q_star((uint32_t)mb, a.bp, a.bc);
@@ -181,17 +212,44 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
   __syncthreads();
   const int h = sc.h, m = sc.m, q = sc.q, keff = sc.keff;
 
-  // ---- 4. the K least-recently-used evictable slots, one radix select -------
+  // ---- 4. the K least-recently-used evictable slots, one pass ----------------
   // key(s) = (stamp << 20) | s, or all-ones when s holds one of this call's hits
   auto key_of = [&](int s) -> unsigned long long {
-    const int f = s2e[s];
-    if (f >= fbase && f < fbase + a.E) {
+    const int f = a.cache_keys ? slotf[s] : s2e[s];
+    if (f >= fbase && f < fbase + E) {
       const int e = f - fbase;
       if (ebits[e >> 5] & (1u << (e & 31))) return ~0ull;
     }
-    return ((unsigned long long)stamp[s] << kSlotBits) | (unsigned long long)s;
+    return a.cache_keys ? rawkey[s] : (((unsigned long long)stamp[s] << kSlotBits) | (unsigned long long)s);
   };
-  if (keff > 0) {
+  if (!kRadix && keff > 0) {
+    // each warp: its keff smallest keys, ascending, by repeated warp-minimum
+    unsigned long long last = 0ull;
+    bool first = true;
+    for (int r = 0; r < keff; ++r) {
+      unsigned long long mine = ~0ull;
+      for (int s = warp * 32 + lane; s < C; s += nt) {
+        const unsigned long long key = key_of(s);
+        if ((first || key > last) && key < mine) mine = key;
+      }
+      const unsigned long long wmin = warp_min_u64(mine);
+      if (lane == 0) wcand[warp * 32 + r] = wmin;
+      last = wmin;
+      first = false;
+    }
+    __syncthreads();
+    if (warp == 0) {  // merge the 32 sorted lists: lane l walks warp l's list
+      const int nwarps = nt >> 5;
+      int ptr = 0;
+      for (int r = 0; r < keff; ++r) {
+        const unsigned long long head = (lane < nwarps && ptr < keff) ? wcand[lane * 32 + ptr] : ~0ull;
+        const unsigned long long mn = warp_min_u64(head);
+        const uint32_t owner = __ballot_sync(0xffffffffu, head == mn);
+        if (lane == __ffs(owner) - 1) ++ptr;
+        if (lane == 0) vict[r] = (mn == ~0ull) ? -1 : (int)(mn & (kMaxSlots - 1));
+      }
+    }
+  } else if (kRadix && keff > 0) {
     const unsigned long long maxkey = (sc.clock0 << kSlotBits) | (kMaxSlots - 1);
     const int top = 63 - __clzll((long long)maxkey);
     unsigned long long prefix = 0ull, maskhi = 0ull;
@@ -199,7 +257,7 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
     for (int shift = (top / 8) * 8; shift >= 0; shift -= 8) {
       for (int i = tid; i < 256; i += nt) hist[i] = 0u;
       __syncthreads();
-      for (int s = tid; s < a.C; s += nt) {
+      for (int s = tid; s < C; s += nt) {
         const unsigned long long key = key_of(s);
         if ((key & maskhi) == prefix) atomicAdd(&hist[(key >> shift) & 255ull], 1u);
       }
@@ -215,8 +273,7 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
           if (lane >= o) incl += v;
         }
         const int excl = incl - c;
-        const bool here = (excl < kth) && (kth <= incl);
-        if (here) {
+        if ((excl < kth) && (kth <= incl)) {
           int run = excl, d = lane * 8;
           for (int j = 0; j < 8; ++j) {
             const int hj = (int)hist[lane * 8 + j];
@@ -234,7 +291,7 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
       __syncthreads();
     }
     // prefix is now the keff-th smallest key; keys are unique, so exactly keff are <= it
-    for (int s = tid; s < a.C; s += nt) {
+    for (int s = tid; s < C; s += nt) {
       const unsigned long long key = key_of(s);
       if (key <= prefix) {
         const int i = atomicAdd(&sc.ncand, 1);
@@ -246,19 +303,20 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
       const unsigned long long ki = cand[i];
       int r = 0;
       for (int j = 0; j < keff; ++j) r += (cand[j] < ki);
-      a.b.victims[r] = (int32_t)(ki & (kMaxSlots - 1));
+      vict[r] = (int32_t)(ki & (kMaxSlots - 1));
     }
   }
-  for (int i = keff + tid; i < a.K; i += nt) a.b.victims[i] = -1;
-  __syncthreads();  // victims visible to the block (global writes, same CTA)
+  for (int i = keff + tid; i < a.K; i += nt) vict[i] = -1;
+  __syncthreads();
 
   // ---- 5. rewrite: fills take victims in order, the rest go to the CPU ------
+  for (int i = tid; i < a.K; i += nt) a.b.victims[i] = vict[i];
   for (int r = tid; r < m; r += nt) {
     const int i = miss_list[r];
     const int f = fbase + uniq_e[i];
     if (r < q) {
-      const int v = a.b.victims[r];
-      const int old = s2e[v];
+      const int v = vict[r];
+      const int old = a.cache_keys ? slotf[v] : s2e[v];
       if (old >= 0) a.tab.e2s[old] = -1;
       s2e[v] = f;
       a.tab.e2s[f] = v;
@@ -283,7 +341,6 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
       tb += __popc(bt);
     }
     if (lane == 0) {
-      sc.ntouch = tb;
       *a.tab.clock = sc.clock0 + (unsigned long long)tb;
       if (((sc.clock0 + tb) >> (64 - kSlotBits)) != 0ull) atomicOr(&sc.bad, 2);
     }
@@ -305,9 +362,9 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
   // ---- 7. slot map and pair lists ---------------------------------------------
   int my_hits = 0, my_misses = 0;
   for (int p = tid; p < P; p += nt) {
-    const int e = a.ids[p];
+    const int e = pid[p];
     int slot = -1;
-    if ((unsigned)e < (unsigned)a.E) {
+    if ((unsigned)e < (unsigned)E) {
       const uint32_t wbits = ebits[e >> 5];
       const int i = ebase[e >> 5] + __popc(wbits & ((1u << (e & 31)) - 1u));
       const int cls = uniq_cls[i];
@@ -345,13 +402,11 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
   }
   __syncthreads();
   for (int p = tid; p < P; p += nt) {
-    const int slot = a.b.slot_map[p];
-    if (slot >= 0) {
-      const int e = a.ids[p];
+    const int e = pid[p];
+    if ((unsigned)e < (unsigned)E) {
       const uint32_t wbits = ebits[e >> 5];
       const int i = ebase[e >> 5] + __popc(wbits & ((1u << (e & 31)) - 1u));
-      const int pos = atomicAdd(&gcnt[uniq_rank[i]], 1);
-      a.b.gpu_pairs[pos] = p;
+      if (uniq_cls[i] < 2) a.b.gpu_pairs[atomicAdd(&gcnt[uniq_rank[i]], 1)] = p;
     }
   }
   if (ns) {
@@ -388,15 +443,22 @@ cudaError_t launch_decode_control(const Shape& sh, int layer, int T, int C, int 
   a.err = err;
   a.umax = min(sh.E, T * sh.k);
   const int NW = (sh.E + 31) / 32;
-  const size_t smem = (size_t)(2 * NW + 1) * 4 + (size_t)(6 * a.umax + 2) * 4 + 257 * 4 + 8 +
-                      (size_t)K * 8 + 16;
-  decode_control_kernel<<<1, kCtrlThreads, smem, s>>>(a);
+  const size_t base = (size_t)sh.E * 4 + (size_t)T * sh.k * 4 + (size_t)(2 * NW + 1) * 4 +
+                      (size_t)(6 * a.umax + 2) * 4 + (size_t)K * 4 + 256 * 4 + 8 + (size_t)K * 8 + 16;
+  a.cache_keys = (C <= kSmemKeyCap && base + (size_t)C * 12 <= kCtrlSmemLimit) ? 1 : 0;
+  const size_t smem = base + (a.cache_keys ? (size_t)C * 12 : 0);
+  if (smem > kCtrlSmemLimit) return cudaErrorInvalidConfiguration;
+  if (K <= 32) decode_control_kernel<false><<<1, kCtrlThreads, smem, s>>>(a);
+  else decode_control_kernel<true><<<1, kCtrlThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t setup_control_kernels() {
-  return cudaFuncSetAttribute(decode_control_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              200 * 1024);
+  cudaError_t e = cudaFuncSetAttribute(decode_control_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kCtrlSmemLimit);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(decode_control_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)kCtrlSmemLimit);
 }
 
 }  // namespace moe

@@ -105,11 +105,19 @@ template <> __device__ __forceinline__ void load_act<MOE_BF16, 4>(const void* x,
   f[2] = __uint_as_float(v.y << 16); f[3] = __uint_as_float(v.y & 0xffff0000u);
 }
 
-// weights are read once per step: stream them past L1
-__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+// Weights are read once per step: stream them past L1 and mark them first to
+// leave L2, so the kernels' code, the residency tables and the activations
+// stay cached between layers.
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint4 ld_stream(const uint4* p, uint64_t pol) {
   uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p), "l"(pol));
   return r;
 }
 
@@ -123,10 +131,17 @@ __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 
 struct GemvArgs {
   int H, I, k, T, P;             // P = T * k (pair ids >= P are shared-expert rows)
-  int pass;                      // 0: hits + shared, 1: fills
+  int pass;                      // 0: hits + shared, 1: fills, 2: every GPU expert
+  int n_shared;
   const void* x;
   DecodeBufs b;
 };
+
+__device__ __forceinline__ void pass_range(const GemvArgs& a, int& g0, int& g1) {
+  const int* plan = a.b.plan;
+  g0 = a.pass == 1 ? plan[P_NFIRST] : 0;
+  g1 = a.pass == 0 ? plan[P_NFIRST] : plan[P_NGPU];
+}
 
 __device__ __forceinline__ int token_of(int pid, int k, int P) { return pid < P ? pid / k : pid - P; }
 
@@ -135,9 +150,8 @@ template <int WT, int AT, int kTokGroup>
 __global__ void __launch_bounds__(kGemvThreads, kTokGroup == 1 ? 2 : 1) gate_up_kernel(GemvArgs a) {
   using F = WFmt<WT>;
   constexpr int V = F::V;
-  const int* plan = a.b.plan;
-  const int g0 = a.pass == 0 ? 0 : plan[P_NFIRST];
-  const int g1 = a.pass == 0 ? plan[P_NFIRST] : plan[P_NGPU];
+  int g0, g1;
+  pass_range(a, g0, g1);
   const int H = a.H, I = a.I;
   const long rows = (long)(g1 - g0) * I;
   const int lane = threadIdx.x & 31;
@@ -146,6 +160,7 @@ __global__ void __launch_bounds__(kGemvThreads, kTokGroup == 1 ? 2 : 1) gate_up_
   const int NCH = H / V;                       // 16-byte chunks per row
   const size_t row_bytes = (size_t)H * F::ES;
   const int HB = H / 128;                      // fp8 scale columns
+  const uint64_t pol = evict_first_policy();
 
   for (long r = wid; r < rows; r += nwarps) {
     const int g = g0 + (int)(r / I);
@@ -168,7 +183,7 @@ __global__ void __launch_bounds__(kGemvThreads, kTokGroup == 1 ? 2 : 1) gate_up_
 #pragma unroll
         for (int j = 0; j < kChunksPerLane; ++j) {
           const int c = seg + j * 32 + lane;
-          if (c < NCH) { wg[j] = ld_stream(gate + c); wu[j] = ld_stream(up + c); }
+          if (c < NCH) { wg[j] = ld_stream(gate + c, pol); wu[j] = ld_stream(up + c, pol); }
         }
 #pragma unroll
         for (int j = 0; j < kChunksPerLane; ++j) {
@@ -215,9 +230,8 @@ template <int WT, int kTokGroup>
 __global__ void __launch_bounds__(kGemvThreads, kTokGroup == 1 ? 2 : 1) down_kernel(GemvArgs a) {
   using F = WFmt<WT>;
   constexpr int V = F::V;
-  const int* plan = a.b.plan;
-  const int g0 = a.pass == 0 ? 0 : plan[P_NFIRST];
-  const int g1 = a.pass == 0 ? plan[P_NFIRST] : plan[P_NGPU];
+  int g0, g1;
+  pass_range(a, g0, g1);
   const int H = a.H, I = a.I;
   const long rows = (long)(g1 - g0) * H;
   const int lane = threadIdx.x & 31;
@@ -228,6 +242,7 @@ __global__ void __launch_bounds__(kGemvThreads, kTokGroup == 1 ? 2 : 1) down_ker
   const size_t down_off = 2ull * (size_t)I * (size_t)H * F::ES;
   const size_t sd_off = 3ull * (size_t)I * (size_t)H * F::ES + 4ull * (size_t)(2 * I / 128) * (H / 128);
   const int IB = I / 128;
+  const uint64_t pol = evict_first_policy();
 
   for (long r = wid; r < rows; r += nwarps) {
     const int g = g0 + (int)(r / H);
@@ -249,7 +264,7 @@ __global__ void __launch_bounds__(kGemvThreads, kTokGroup == 1 ? 2 : 1) down_ker
 #pragma unroll
         for (int j = 0; j < kChunksPerLane; ++j) {
           const int c = seg + j * 32 + lane;
-          if (c < NCH) w[j] = ld_stream(wrow + c);
+          if (c < NCH) w[j] = ld_stream(wrow + c, pol);
         }
 #pragma unroll
         for (int j = 0; j < kChunksPerLane; ++j) {
@@ -282,6 +297,133 @@ __global__ void __launch_bounds__(kGemvThreads, kTokGroup == 1 ? 2 : 1) down_ker
       }
     }
   }
+}
+
+// ---- down projection fused with the combine -------------------------------------
+// One warp per output row r: it streams row r of every GPU expert's W_down
+// (kDCGroup experts' rows in flight at once), dots it with the h of each of the
+// expert's pairs into a per-warp shared buffer y[pair], then forms
+// out[t, r] = sum_j w[t,j] * (slot >= 0 ? y[t,j] : cpu_part[t,j,r]) in j order,
+// plus the shared expert.  The h of every pair is staged once per CTA in shared
+// memory when it fits (the first expert group's weight loads are already in
+// flight meanwhile), so no dot product waits on a second global round trip.
+// Used when all pairs fit the per-warp buffer and a down row fits one pass of
+// kDCChunks 16-byte chunks per lane.
+constexpr int kDCWarps = 8;
+constexpr int kDCGroup = 4;
+constexpr int kDCChunks = 4;
+constexpr int kDCMaxPairs = 1024;
+constexpr size_t kDCHSmem = 96 * 1024;    // h staged in shared memory up to this size
+
+template <int WT>
+__global__ void __launch_bounds__(kDCWarps * 32) down_combine_kernel(GemvArgs a, const float* __restrict__ w,
+                                                                     const float* __restrict__ cpu,
+                                                                     float* __restrict__ out, uint32_t* err) {
+  using F = WFmt<WT>;
+  constexpr int V = F::V;
+  extern __shared__ __align__(16) float dsm[];
+  const int NP = a.P + a.T * a.n_shared;
+  const int H = a.H, I = a.I;
+  const bool h_smem = (size_t)NP * I * sizeof(float) <= kDCHSmem;
+  float* hs = dsm;                                            // [NP, I] if staged
+  float* ys = dsm + (h_smem ? (size_t)NP * I : 0) + (threadIdx.x >> 5) * NP;
+  const float* hsrc = h_smem ? hs : a.b.h;
+  const int lane = threadIdx.x & 31;
+  const int ngpu = a.b.plan[P_NGPU];
+  const int NCH = I / V;
+  const size_t row_bytes = (size_t)I * F::ES;
+  const size_t down_off = 2ull * (size_t)I * (size_t)H * F::ES;
+  const size_t sd_off = 3ull * (size_t)I * (size_t)H * F::ES + 4ull * (size_t)(2 * I / 128) * (H / 128);
+  const int IB = I / 128;
+  const int nwarps = gridDim.x * kDCWarps;
+  const uint64_t pol = evict_first_policy();
+  bool missing = false;
+
+  int r = blockIdx.x * kDCWarps + (threadIdx.x >> 5);
+  uint4 wv[kDCGroup][kDCChunks];
+  auto load_group = [&](int row, int g0) {
+#pragma unroll
+    for (int gi = 0; gi < kDCGroup; ++gi) {
+      if (g0 + gi < ngpu) {
+        const uint4* wrow = reinterpret_cast<const uint4*>(a.b.gpu_w[g0 + gi] + down_off + (size_t)row * row_bytes);
+#pragma unroll
+        for (int j = 0; j < kDCChunks; ++j) {
+          const int c = j * 32 + lane;
+          if (c < NCH) wv[gi][j] = ld_stream(wrow + c, pol);
+        }
+      }
+    }
+  };
+  if (r < H) load_group(r, 0);
+  if (h_smem) {   // stage every pair's h while the first weight rows are in flight
+    const float4* src = reinterpret_cast<const float4*>(a.b.h);
+    float4* dst = reinterpret_cast<float4*>(hs);
+    const int n4 = NP * I / 4;
+    for (int i = threadIdx.x; i < n4; i += blockDim.x) dst[i] = src[i];
+    __syncthreads();
+  }
+  for (; r < H; r += nwarps) {
+    for (int g0 = 0; g0 < ngpu; g0 += kDCGroup) {
+      if (g0 > 0) load_group(r, g0);
+#pragma unroll
+      for (int gi = 0; gi < kDCGroup; ++gi) {
+        const int g = g0 + gi;
+        if (g >= ngpu) break;
+        const float* sd = reinterpret_cast<const float*>(a.b.gpu_w[g] + sd_off);
+        const int pb = a.b.gpu_off[g], pe = a.b.gpu_off[g + 1];
+        for (int tp = pb; tp < pe; ++tp) {
+          const int pid = a.b.gpu_pairs[tp];
+          float acc = 0.f;
+#pragma unroll
+          for (int j = 0; j < kDCChunks; ++j) {
+            const int c = j * 32 + lane;
+            if (c < NCH) {
+              float fw[V], hv[V];
+              F::unpack(wv[gi][j], fw);
+              const float4* hp = reinterpret_cast<const float4*>(hsrc + (size_t)pid * I + (size_t)c * V);
+#pragma unroll
+              for (int v = 0; v < V; v += 4) {
+                const float4 q = hp[v / 4];
+                hv[v] = q.x; hv[v + 1] = q.y; hv[v + 2] = q.z; hv[v + 3] = q.w;
+              }
+              float d = 0.f;
+#pragma unroll
+              for (int v = 0; v < V; ++v) d = fmaf(fw[v], hv[v], d);
+              if (WT == MOE_FP8E4M3_B128) d *= __ldg(sd + (size_t)(r >> 7) * IB + ((c * V) >> 7));
+              acc += d;
+            }
+          }
+          acc = warp_sum(acc);
+          if (lane == 0) {
+            ys[pid] = acc;
+            a.b.y[(size_t)pid * H + r] = acc;   // per-pair output stays readable (moe_cache_get_plan)
+          }
+        }
+      }
+    }
+    __syncwarp();
+    for (int t = lane; t < a.T; t += 32) {
+      float acc = 0.f;
+      for (int j = 0; j < a.k; ++j) {
+        const int p = t * a.k + j;
+        float v;
+        if (a.b.slot_map[p] >= 0) {
+          v = ys[p];
+        } else if (cpu != nullptr) {
+          v = __ldg(cpu + (size_t)p * H + r);
+        } else {
+          v = 0.f;
+          missing = true;
+        }
+        acc = fmaf(__ldg(w + p), v, acc);
+      }
+      if (a.n_shared) acc += ys[a.P + t];
+      out[(size_t)t * H + r] = acc;
+    }
+    __syncwarp();
+    if (r + nwarps < H) load_group(r + nwarps, 0);
+  }
+  if (__any_sync(0xffffffffu, missing) && lane == 0) atomicOr_system(err, kErrMissingCpuPart);
 }
 
 // ---- combine: out[t] = sum_j w[t,j] * (slot >= 0 ? y : cpu_part) in j order (+ shared) --
@@ -370,9 +512,88 @@ cudaError_t launch_gemv_typed(const GemvArgs& a, int sms, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+template <int WT, int AT>
+cudaError_t launch_gate_up_typed(const GemvArgs& a, int sms, cudaStream_t s) {
+  if (a.T == 1) gate_up_kernel<WT, AT, 1><<<2 * sms, kGemvThreads, 0, s>>>(a);
+  else gate_up_kernel<WT, AT, 4><<<sms, kGemvThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int WT>
+cudaError_t launch_down_typed(const GemvArgs& a, int sms, cudaStream_t s) {
+  if (a.T == 1) down_kernel<WT, 1><<<2 * sms, kGemvThreads, 0, s>>>(a);
+  else down_kernel<WT, 4><<<sms, kGemvThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <int WT>
+cudaError_t launch_down_combine_typed(const GemvArgs& a, const float* w, const float* cpu, float* out,
+                                      uint32_t* err, int sms, cudaStream_t s) {
+  const size_t np = (size_t)(a.P + a.T * a.n_shared);
+  const size_t hbytes = np * a.I * sizeof(float);
+  const size_t smem = (size_t)kDCWarps * np * sizeof(float) + (hbytes <= kDCHSmem ? hbytes : 0);
+  const int blocks = (a.H + kDCWarps - 1) / kDCWarps;
+  down_combine_kernel<WT><<<blocks < 4 * sms ? blocks : 4 * sms, kDCWarps * 32, smem, s>>>(a, w, cpu, out, err);
+  return cudaGetLastError();
+}
+
+GemvArgs make_args(const Shape& sh, int pass, int T, const void* x, const DecodeBufs& b) {
+  GemvArgs a;
+  a.H = sh.H; a.I = sh.I; a.k = sh.k; a.T = T; a.P = T * sh.k; a.pass = pass; a.n_shared = sh.n_shared;
+  a.x = x; a.b = b;
+  return a;
+}
+
 }  // namespace
 
 int gemv_block_threads() { return kGemvThreads; }
+
+cudaError_t setup_gemv_kernels() {
+  const int smem = (int)(kDCHSmem + (size_t)kDCWarps * kDCMaxPairs * sizeof(float));
+  cudaError_t e = cudaFuncSetAttribute(down_combine_kernel<MOE_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(down_combine_kernel<MOE_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(down_combine_kernel<MOE_FP8E4M3_B128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem);
+  return e;
+}
+
+cudaError_t launch_gate_up(const Shape& sh, int pass, int T, const void* x, DecodeBufs b, int sms, cudaStream_t s) {
+  const GemvArgs a = make_args(sh, pass, T, x, b);
+  switch (sh.wdtype * 2 + sh.adtype) {
+    case MOE_F32 * 2 + MOE_F32: return launch_gate_up_typed<MOE_F32, MOE_F32>(a, sms, s);
+    case MOE_F32 * 2 + MOE_BF16: return launch_gate_up_typed<MOE_F32, MOE_BF16>(a, sms, s);
+    case MOE_BF16 * 2 + MOE_F32: return launch_gate_up_typed<MOE_BF16, MOE_F32>(a, sms, s);
+    case MOE_BF16 * 2 + MOE_BF16: return launch_gate_up_typed<MOE_BF16, MOE_BF16>(a, sms, s);
+    case MOE_FP8E4M3_B128 * 2 + MOE_F32: return launch_gate_up_typed<MOE_FP8E4M3_B128, MOE_F32>(a, sms, s);
+    case MOE_FP8E4M3_B128 * 2 + MOE_BF16: return launch_gate_up_typed<MOE_FP8E4M3_B128, MOE_BF16>(a, sms, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+bool down_combine_fits(const Shape& sh, int T) {
+  const int V = sh.wdtype == MOE_F32 ? 4 : sh.wdtype == MOE_BF16 ? 8 : 16;
+  return T * sh.k + T * sh.n_shared <= kDCMaxPairs && sh.I / V <= 32 * kDCChunks;
+}
+
+cudaError_t launch_down_combine(const Shape& sh, int T, const float* w, const float* cpu_part, DecodeBufs b,
+                                float* out, uint32_t* err, int sms, cudaStream_t s) {
+  if (down_combine_fits(sh, T)) {
+    const GemvArgs a = make_args(sh, 2, T, nullptr, b);
+    if (sh.wdtype == MOE_F32) return launch_down_combine_typed<MOE_F32>(a, w, cpu_part, out, err, sms, s);
+    if (sh.wdtype == MOE_BF16) return launch_down_combine_typed<MOE_BF16>(a, w, cpu_part, out, err, sms, s);
+    return launch_down_combine_typed<MOE_FP8E4M3_B128>(a, w, cpu_part, out, err, sms, s);
+  }
+  // large batches: down projection of every GPU expert, then the separate combine
+  const GemvArgs a = make_args(sh, 2, T, nullptr, b);
+  cudaError_t e;
+  if (sh.wdtype == MOE_F32) e = launch_down_typed<MOE_F32>(a, sms, s);
+  else if (sh.wdtype == MOE_BF16) e = launch_down_typed<MOE_BF16>(a, sms, s);
+  else e = launch_down_typed<MOE_FP8E4M3_B128>(a, sms, s);
+  if (e != cudaSuccess) return e;
+  return launch_combine(sh, T, w, cpu_part, b, out, err, s);
+}
 
 cudaError_t launch_fill(const Shape& sh, const int32_t* plan, const int32_t* fills,
                         const uint8_t* host_pool_dev, const uint64_t* offsets, uint8_t* slots,
@@ -390,7 +611,8 @@ cudaError_t launch_copy_blobs(const int32_t* count, const int32_t* skip, const i
 cudaError_t launch_expert_gemv(const Shape& sh, int pass, int T, const void* x, DecodeBufs b,
                                int sms, cudaStream_t s) {
   GemvArgs a;
-  a.H = sh.H; a.I = sh.I; a.k = sh.k; a.T = T; a.P = T * sh.k; a.pass = pass; a.x = x; a.b = b;
+  a.H = sh.H; a.I = sh.I; a.k = sh.k; a.T = T; a.P = T * sh.k; a.pass = pass; a.n_shared = sh.n_shared;
+  a.x = x; a.b = b;
   if (sh.wdtype == MOE_F32 && sh.adtype == MOE_F32) return launch_gemv_typed<MOE_F32, MOE_F32>(a, sms, s);
   if (sh.wdtype == MOE_F32 && sh.adtype == MOE_BF16) return launch_gemv_typed<MOE_F32, MOE_BF16>(a, sms, s);
   if (sh.wdtype == MOE_BF16 && sh.adtype == MOE_F32) return launch_gemv_typed<MOE_BF16, MOE_F32>(a, sms, s);

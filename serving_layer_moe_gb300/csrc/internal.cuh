@@ -18,7 +18,7 @@ constexpr int kMaxExperts = 4096;          // E: routed-expert bitmap of 128 wor
 constexpr int kMaxDecodeTokens = 1024;
 constexpr int kSlotBits = 20;              // slot index field of an LRU key
 constexpr uint64_t kMaxSlots = 1ull << kSlotBits;
-constexpr int kCtrlThreads = 1024;
+constexpr int kCtrlThreads = 512;
 
 // error word bits (device -> host through page-locked mapped memory)
 enum : uint32_t {
@@ -40,7 +40,7 @@ enum PlanIdx : int {
 
 // kernel groups timed by moe_cache_profile
 enum ProfKind : int {
-  PROF_CONTROL = 0, PROF_FILL = 1, PROF_GEMV_RESIDENT = 2, PROF_GEMV_FILLED = 3, PROF_COMBINE = 4,
+  PROF_CONTROL = 0, PROF_FILL = 1, PROF_GATE_UP_RESIDENT = 2, PROF_GATE_UP_FILLED = 3, PROF_DOWN_COMBINE = 4,
   PROF_PREFILL_CONTROL = 5, PROF_PREFILL_LOAD = 6, PROF_PREFILL_GEMM = 7, PROF_KINDS = 8,
 };
 
@@ -83,6 +83,7 @@ cudaError_t launch_decode_control(const Shape& sh, int layer, int T, int C, int 
                                   const uint8_t* shared_base, uint32_t* err, cudaStream_t s);
 
 cudaError_t setup_control_kernels();  // once per device, before the first launch
+cudaError_t setup_gemv_kernels();     // once per device, before the first launch
 
 // expert_gemv.cu
 cudaError_t launch_fill(const Shape& sh, const int32_t* plan, const int32_t* fills,
@@ -93,6 +94,10 @@ cudaError_t launch_copy_blobs(const int32_t* count, const int32_t* skip, const i
                               uint64_t S, int n_ctas, cudaStream_t s);
 cudaError_t launch_expert_gemv(const Shape& sh, int pass, int T, const void* x, DecodeBufs b,
                                int sms, cudaStream_t s);
+cudaError_t launch_gate_up(const Shape& sh, int pass, int T, const void* x, DecodeBufs b, int sms, cudaStream_t s);
+cudaError_t launch_down_combine(const Shape& sh, int T, const float* w, const float* cpu_part, DecodeBufs b,
+                                float* out, uint32_t* err, int sms, cudaStream_t s);
+bool down_combine_fits(const Shape& sh, int T);
 cudaError_t launch_combine(const Shape& sh, int T, const float* w, const float* cpu_part,
                            DecodeBufs b, float* out, uint32_t* err, cudaStream_t s);
 int gemv_block_threads();
