@@ -257,8 +257,8 @@ extern "C" moe_status moe_cache_destroy(moe_cache* c) {
 }
 
 // ---------------------------------------------------------------------------
-// decode: control -> [fill on the side stream] -> gate/up of resident experts ->
-//         wait fills -> gate/up of filled experts -> down projection + combine
+// decode: control -> [fill + gate/up of filled experts on the side stream] ->
+//         gate/up of resident experts -> wait fills -> down projection + combine
 // ---------------------------------------------------------------------------
 extern "C" moe_status moe_layer_decode(moe_cache* c, int32_t layer, int32_t T, const void* x,
                                        const int32_t* ids, const float* w, const float* cpu_part,
@@ -281,20 +281,16 @@ extern "C" moe_status moe_layer_decode(moe_cache* c, int32_t layer, int32_t T, c
   CK(cudaEventRecord(c->ev_ctrl, s));
   CK(cudaStreamWaitEvent(c->fill_stream, c->ev_ctrl, 0));
   {
+    // fills, and the gate/up GEMV of the filled experts on the way through
     ProfScope p(c, c->fill_stream, PROF_FILL);
-    CK(launch_fill(c->sh, c->b.plan, c->b.fills, c->host_pool_dev, c->offsets, c->slots, c->fill_ctas,
-                   c->fill_stream));
+    CK(launch_fill_gate_up(c->sh, T, x, c->b, c->host_pool_dev, c->offsets, c->slots, c->fill_ctas, c->fill_stream));
   }
   CK(cudaEventRecord(c->ev_fill, c->fill_stream));
   {
     ProfScope p(c, s, PROF_GATE_UP_RESIDENT);
-    CK(launch_gate_up(c->sh, 0, T, x, c->b, c->sms, s));
+    CK(launch_gate_up(c->sh, 0, T, x, c->b, c->sms, s, c->err_dev));
   }
   CK(cudaStreamWaitEvent(s, c->ev_fill, 0));
-  {
-    ProfScope p(c, s, PROF_GATE_UP_FILLED);
-    CK(launch_gate_up(c->sh, 1, T, x, c->b, c->sms, s));
-  }
   {
     ProfScope p(c, s, PROF_DOWN_COMBINE);
     CK(launch_down_combine(c->sh, T, w, cpu_part, c->b, out, c->err_dev, c->sms, s));

@@ -30,8 +30,9 @@
 // routed set is a bitmap over E experts (dedup = atomicOr, order = popcount
 // prefix), hit/miss ranks come from warp ballots.  The K smallest keys (K <=
 // 32) come from one pass in which each warp extracts its own K smallest by
-// repeated warp-minimum and warp 0 merges the 32 sorted lists; for larger K an
-// MSB radix select with 8-bit digits over the shared keys.  Cost does not
+// repeated warp-minimum (32-bit redux instructions over the high and low words
+// of register-resident keys) and warp 0 merges the sorted per-warp lists; for
+// larger K an MSB radix select with 8-bit digits over the shared keys.  Cost does not
 // depend on how many misses occurred.
 #include "internal.cuh"
 
@@ -74,14 +75,6 @@ __device__ __forceinline__ uint32_t q_star(uint32_t m, uint32_t bp, uint32_t bc)
   return (uint32_t)q;
 }
 
-__device__ __forceinline__ unsigned long long warp_min_u64(unsigned long long v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
-    v = w < v ? w : v;
-  }
-  return v;
-}
 
 // shared scalars of the control CTA
 struct CtrlScalars {
@@ -129,7 +122,8 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
   }
   for (int i = tid; i < NW; i += nt) ebits[i] = 0u;
   for (int i = tid; i < U + 2; i += nt) gcnt[i] = 0;
-  for (int p = tid; p < P; p += nt) pid[p] = a.ids[p];
+  // the residency tables were written by an earlier control kernel, not by the
+  // kernel this one may overlap: load them before waiting on the predecessor
   for (int e = tid; e < E; e += nt) lslot[e] = a.tab.e2s[fbase + e];
   if (a.cache_keys) {
     for (int s = tid; s < C; s += nt) {
@@ -137,6 +131,9 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
       rawkey[s] = ((unsigned long long)stamp[s] << kSlotBits) | (unsigned long long)s;
     }
   }
+  pdl_wait();       // the routed ids may come from the preceding kernel
+  pdl_trigger();
+  for (int p = tid; p < P; p += nt) pid[p] = a.ids[p];
   __syncthreads();
 
   // ---- 1. dedup: routed-expert bitmap ------------------------------------
@@ -223,27 +220,50 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
     return a.cache_keys ? rawkey[s] : (((unsigned long long)stamp[s] << kSlotBits) | (unsigned long long)s);
   };
   if (!kRadix && keff > 0) {
-    // each warp: its keff smallest keys, ascending, by repeated warp-minimum
+    // each warp: its keff smallest keys, ascending, by repeated warp-minimum; a
+    // thread holds the effective keys of its slots in registers (C <= 8 * 512)
+    // and a 64-bit warp minimum is two 32-bit reductions (high word, then the
+    // low word among the lanes that hold the minimal high word)
+    constexpr int KPT = 8;
+    const bool in_regs = C <= KPT * nt;
+    unsigned long long mykeys[KPT];
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+      const int s = tid + j * nt;
+      mykeys[j] = (in_regs && s < C) ? key_of(s) : ~0ull;
+    }
     unsigned long long last = 0ull;
     bool first = true;
     for (int r = 0; r < keff; ++r) {
       unsigned long long mine = ~0ull;
-      for (int s = warp * 32 + lane; s < C; s += nt) {
-        const unsigned long long key = key_of(s);
-        if ((first || key > last) && key < mine) mine = key;
+      if (in_regs) {
+#pragma unroll
+        for (int j = 0; j < KPT; ++j) {
+          const unsigned long long key = mykeys[j];
+          if ((first || key > last) && key < mine) mine = key;
+        }
+      } else {
+        for (int s = tid; s < C; s += nt) {
+          const unsigned long long key = key_of(s);
+          if ((first || key > last) && key < mine) mine = key;
+        }
       }
-      const unsigned long long wmin = warp_min_u64(mine);
+      const unsigned mhi = __reduce_min_sync(0xffffffffu, (unsigned)(mine >> 32));
+      const unsigned mlo = __reduce_min_sync(0xffffffffu, (unsigned)(mine >> 32) == mhi ? (unsigned)mine : ~0u);
+      const unsigned long long wmin = ((unsigned long long)mhi << 32) | mlo;
       if (lane == 0) wcand[warp * 32 + r] = wmin;
       last = wmin;
       first = false;
     }
     __syncthreads();
-    if (warp == 0) {  // merge the 32 sorted lists: lane l walks warp l's list
+    if (warp == 0) {  // merge the sorted per-warp lists: lane l walks warp l's list
       const int nwarps = nt >> 5;
       int ptr = 0;
       for (int r = 0; r < keff; ++r) {
         const unsigned long long head = (lane < nwarps && ptr < keff) ? wcand[lane * 32 + ptr] : ~0ull;
-        const unsigned long long mn = warp_min_u64(head);
+        const unsigned mhi = __reduce_min_sync(0xffffffffu, (unsigned)(head >> 32));
+        const unsigned mlo = __reduce_min_sync(0xffffffffu, (unsigned)(head >> 32) == mhi ? (unsigned)head : ~0u);
+        const unsigned long long mn = ((unsigned long long)mhi << 32) | mlo;
         const uint32_t owner = __ballot_sync(0xffffffffu, head == mn);
         if (lane == __ffs(owner) - 1) ++ptr;
         if (lane == 0) vict[r] = (mn == ~0ull) ? -1 : (int)(mn & (kMaxSlots - 1));
@@ -448,17 +468,17 @@ cudaError_t launch_decode_control(const Shape& sh, int layer, int T, int C, int 
   a.cache_keys = (C <= kSmemKeyCap && base + (size_t)C * 12 <= kCtrlSmemLimit) ? 1 : 0;
   const size_t smem = base + (a.cache_keys ? (size_t)C * 12 : 0);
   if (smem > kCtrlSmemLimit) return cudaErrorInvalidConfiguration;
-  if (K <= 32) decode_control_kernel<false><<<1, kCtrlThreads, smem, s>>>(a);
-  else decode_control_kernel<true><<<1, kCtrlThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  if (K <= 32) return launch_pdl(decode_control_kernel<false>, dim3(1), dim3(kCtrlThreads), smem, s, a);
+  return launch_pdl(decode_control_kernel<true>, dim3(1), dim3(kCtrlThreads), smem, s, a);
 }
 
 cudaError_t setup_control_kernels() {
-  cudaError_t e = cudaFuncSetAttribute(decode_control_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kCtrlSmemLimit);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(decode_control_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)kCtrlSmemLimit);
+  for (auto k : {decode_control_kernel<false>, decode_control_kernel<true>}) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCtrlSmemLimit);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, kDecodeCarveout);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace moe

@@ -26,6 +26,8 @@
 
 #include <cuda_fp8.h>
 
+#include <algorithm>
+
 namespace moe {
 
 namespace {
@@ -133,9 +135,64 @@ struct GemvArgs {
   int H, I, k, T, P;             // P = T * k (pair ids >= P are shared-expert rows)
   int pass;                      // 0: hits + shared, 1: fills, 2: every GPU expert
   int n_shared;
+  int max_g, max_p;              // bounds of the GPU-expert and pair lists of this call
+  int x_smem;                    // stage x in shared memory
   const void* x;
   DecodeBufs b;
 };
+
+// The plan the control kernel published, staged once per CTA in shared memory:
+// weight pointer and pair-list offsets of every GPU expert, pair ids and their
+// tokens.  One parallel round trip instead of a chain of dependent global reads
+// per expert.
+struct StagedPlan {
+  const uint8_t** w;   // [max_g]
+  int* off;            // [max_g + 1]
+  int* pid;            // [max_p]
+  int* tok;            // [max_p]
+  size_t bytes;
+};
+
+__host__ __device__ inline size_t staged_plan_bytes(int max_g, int max_p) {
+  return ((size_t)max_g * 8 + (size_t)(max_g + 1) * 4 + (size_t)max_p * 8 + 15) & ~size_t(15);
+}
+
+__device__ __forceinline__ StagedPlan stage_plan(uint8_t* smem, const GemvArgs& a) {
+  StagedPlan sp;
+  sp.w = reinterpret_cast<const uint8_t**>(smem);
+  sp.off = reinterpret_cast<int*>(sp.w + a.max_g);
+  sp.pid = sp.off + a.max_g + 1;
+  sp.tok = sp.pid + a.max_p;
+  sp.bytes = staged_plan_bytes(a.max_g, a.max_p);
+  for (int i = threadIdx.x; i < a.max_g; i += blockDim.x) sp.w[i] = a.b.gpu_w[i];
+  for (int i = threadIdx.x; i <= a.max_g; i += blockDim.x) sp.off[i] = a.b.gpu_off[i];
+  for (int i = threadIdx.x; i < a.max_p; i += blockDim.x) {
+    const int p = a.b.gpu_pairs[i];
+    sp.pid[i] = p;
+    sp.tok[i] = p < a.P ? p / a.k : p - a.P;
+  }
+  return sp;
+}
+
+// x values from shared or global memory (generic loads)
+template <int AT, int V> __device__ __forceinline__ void load_x(const void* x, size_t off, float* f) {
+  if (AT == MOE_F32) {
+    const float4* p = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(x) + off);
+#pragma unroll
+    for (int i = 0; i < V / 4; ++i) {
+      const float4 v = p[i];
+      f[4 * i] = v.x; f[4 * i + 1] = v.y; f[4 * i + 2] = v.z; f[4 * i + 3] = v.w;
+    }
+  } else if (V >= 8) {
+    const uint4* p = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(x) + off);
+#pragma unroll
+    for (int i = 0; i < V / 8; ++i) WFmt<MOE_BF16>::unpack(p[i], f + 8 * i);
+  } else {
+    const uint2 v = *reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(x) + off);
+    f[0] = __uint_as_float(v.x << 16); f[1] = __uint_as_float(v.x & 0xffff0000u);
+    f[2] = __uint_as_float(v.y << 16); f[3] = __uint_as_float(v.y & 0xffff0000u);
+  }
+}
 
 __device__ __forceinline__ void pass_range(const GemvArgs& a, int& g0, int& g1) {
   const int* plan = a.b.plan;
@@ -150,9 +207,22 @@ template <int WT, int AT, int kTokGroup>
 __global__ void __launch_bounds__(kGemvThreads, kTokGroup == 1 ? 2 : 1) gate_up_kernel(GemvArgs a) {
   using F = WFmt<WT>;
   constexpr int V = F::V;
+  extern __shared__ __align__(16) uint8_t gsm[];
+  pdl_wait();
+  pdl_trigger();
+  const StagedPlan sp = stage_plan(gsm, a);
+  const int H = a.H, I = a.I;
+  const void* xs = a.x;
+  if (a.x_smem) {   // stage x [T, H] next to the plan
+    uint4* dst = reinterpret_cast<uint4*>(gsm + sp.bytes);
+    const uint4* src = reinterpret_cast<const uint4*>(a.x);
+    const int n16 = (int)(((size_t)a.T * H * (AT == MOE_F32 ? 4 : 2)) >> 4);
+    for (int i = threadIdx.x; i < n16; i += blockDim.x) dst[i] = src[i];
+    xs = dst;
+  }
   int g0, g1;
   pass_range(a, g0, g1);
-  const int H = a.H, I = a.I;
+  __syncthreads();
   const long rows = (long)(g1 - g0) * I;
   const int lane = threadIdx.x & 31;
   const long nwarps = (long)gridDim.x * (blockDim.x >> 5);
@@ -165,16 +235,16 @@ __global__ void __launch_bounds__(kGemvThreads, kTokGroup == 1 ? 2 : 1) gate_up_
   for (long r = wid; r < rows; r += nwarps) {
     const int g = g0 + (int)(r / I);
     const int i = (int)(r % I);
-    const uint8_t* wb = a.b.gpu_w[g];
+    const uint8_t* wb = sp.w[g];
     const uint4* gate = reinterpret_cast<const uint4*>(wb + (size_t)i * row_bytes);
     const uint4* up = reinterpret_cast<const uint4*>(wb + (size_t)(I + i) * row_bytes);
     const float* sgu = reinterpret_cast<const float*>(wb + 3ull * (size_t)I * row_bytes);
-    const int pb = a.b.gpu_off[g], pe = a.b.gpu_off[g + 1];
+    const int pb = sp.off[g], pe = sp.off[g + 1];
     for (int tp = pb; tp < pe; tp += kTokGroup) {
       const int nt = min(kTokGroup, pe - tp);
       int tok[kTokGroup];
 #pragma unroll
-      for (int n = 0; n < kTokGroup; ++n) tok[n] = n < nt ? token_of(a.b.gpu_pairs[tp + n], a.k, a.P) : 0;
+      for (int n = 0; n < kTokGroup; ++n) tok[n] = n < nt ? sp.tok[tp + n] : 0;
       float ag[kTokGroup], au[kTokGroup];
 #pragma unroll
       for (int n = 0; n < kTokGroup; ++n) { ag[n] = 0.f; au[n] = 0.f; }
@@ -202,6 +272,135 @@ __global__ void __launch_bounds__(kGemvThreads, kTokGroup == 1 ? 2 : 1) gate_up_
             for (int n = 0; n < kTokGroup; ++n) {
               if (n < nt) {
                 float xv[V];
+                load_x<AT, V>(xs, (size_t)tok[n] * H + (size_t)c * V, xv);
+                float dg = 0.f, du = 0.f;
+#pragma unroll
+                for (int v = 0; v < V; ++v) { dg = fmaf(fg[v], xv[v], dg); du = fmaf(fu[v], xv[v], du); }
+                ag[n] = fmaf(dg, scg, ag[n]);
+                au[n] = fmaf(du, scu, au[n]);
+              }
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int n = 0; n < kTokGroup; ++n) {
+        if (n < nt) {
+          const float sg = warp_sum(ag[n]);
+          const float su = warp_sum(au[n]);
+          if (lane == 0) a.b.h[(size_t)sp.pid[tp + n] * I + i] = silu(sg) * su;
+        }
+      }
+    }
+  }
+}
+
+// ---- fill fused with the gate/up GEMV of the filled experts -----------------------
+// The fill path of decode.  For each filled expert (flat id f -> victim slot s):
+// every gate/up row pair is streamed from page-locked host memory over the host
+// link, written into the slot, and dotted with the expert's tokens on the way
+// through (h of its pairs, like gate_up_kernel); the rest of the blob (W_down
+// and, for fp8, the scales) is copied in 4 KB pieces.  The bytes cross the link
+// once and the filled experts need no separate gate/up pass.
+constexpr int kFillThreads = 256;   // small CTAs: they share SMs with the resident-expert GEMV
+
+template <int WT, int AT, int kTokGroup>
+__global__ void __launch_bounds__(kFillThreads, 2)
+fill_gate_up_kernel(GemvArgs a, const int32_t* __restrict__ fills, const uint8_t* __restrict__ host,
+                    const uint64_t* __restrict__ offs, uint8_t* __restrict__ slots, uint64_t S) {
+  using F = WFmt<WT>;
+  constexpr int V = F::V;
+  const int* plan = a.b.plan;
+  const int q = plan[P_Q];
+  if (q == 0) return;
+  const int nfirst = plan[P_NFIRST];
+  const int H = a.H, I = a.I;
+  const int lane = threadIdx.x & 31;
+  const long nwarps = (long)gridDim.x * (blockDim.x >> 5);
+  const long wid = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int NCH = H / V;
+  const size_t row_bytes = (size_t)H * F::ES;
+  const int HB = H / 128;
+  const size_t down_off = 2ull * (size_t)I * row_bytes;
+  const uint64_t tail16 = (S - down_off) >> 4;             // 16-byte chunks after W_gu
+  constexpr int kPiece = 256;                               // 16-byte chunks per copy item (4 KB)
+  const long pieces = (long)((tail16 + kPiece - 1) / kPiece);
+  const long row_items = (long)q * I;
+  const long items = row_items + (long)q * pieces;
+
+  for (long it = wid; it < items; it += nwarps) {
+    if (it >= row_items) {  // plain copy of a piece of W_down (+ scales)
+      const long k = it - row_items;
+      const int fi = (int)(k / pieces);
+      const uint64_t c0 = (uint64_t)(k % pieces) * kPiece;
+      const uint4* src = reinterpret_cast<const uint4*>(host + offs[fills[2 * fi]] + down_off);
+      uint4* dst = reinterpret_cast<uint4*>(slots + (size_t)fills[2 * fi + 1] * S + down_off);
+      const uint64_t c1 = min(tail16, c0 + kPiece);
+      uint4 v[kPiece / 32];
+#pragma unroll
+      for (int j = 0; j < kPiece / 32; ++j) {
+        const uint64_t c = c0 + (uint64_t)j * 32 + lane;
+        if (c < c1) v[j] = src[c];
+      }
+#pragma unroll
+      for (int j = 0; j < kPiece / 32; ++j) {
+        const uint64_t c = c0 + (uint64_t)j * 32 + lane;
+        if (c < c1) __stcs(dst + c, v[j]);
+      }
+      continue;
+    }
+    const int fi = (int)(it / I);
+    const int i = (int)(it % I);
+    const int g = nfirst + fi;
+    const uint8_t* sb = host + offs[fills[2 * fi]];
+    uint8_t* db = slots + (size_t)fills[2 * fi + 1] * S;
+    const uint4* gate = reinterpret_cast<const uint4*>(sb + (size_t)i * row_bytes);
+    const uint4* up = reinterpret_cast<const uint4*>(sb + (size_t)(I + i) * row_bytes);
+    uint4* dgate = reinterpret_cast<uint4*>(db + (size_t)i * row_bytes);
+    uint4* dup = reinterpret_cast<uint4*>(db + (size_t)(I + i) * row_bytes);
+    const float* sgu = reinterpret_cast<const float*>(sb + 3ull * (size_t)I * row_bytes);
+    const int pb = a.b.gpu_off[g], pe = a.b.gpu_off[g + 1];
+    int tok[kTokGroup];
+    float ag[kTokGroup], au[kTokGroup];
+    for (int tp = pb; tp < pe || tp == pb; tp += kTokGroup) {
+      const int nt = max(0, min(kTokGroup, pe - tp));
+#pragma unroll
+      for (int n = 0; n < kTokGroup; ++n) {
+        tok[n] = n < nt ? token_of(a.b.gpu_pairs[tp + n], a.k, a.P) : 0;
+        ag[n] = 0.f;
+        au[n] = 0.f;
+      }
+      for (int seg = 0; seg < NCH; seg += 32 * kChunksPerLane) {
+        uint4 wg[kChunksPerLane], wu[kChunksPerLane];
+#pragma unroll
+        for (int j = 0; j < kChunksPerLane; ++j) {
+          const int c = seg + j * 32 + lane;
+          if (c < NCH) { wg[j] = gate[c]; wu[j] = up[c]; }
+        }
+        if (tp == pb) {   // the first token group writes the rows into the slot
+#pragma unroll
+          for (int j = 0; j < kChunksPerLane; ++j) {
+            const int c = seg + j * 32 + lane;
+            if (c < NCH) { __stcs(dgate + c, wg[j]); __stcs(dup + c, wu[j]); }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < kChunksPerLane; ++j) {
+          const int c = seg + j * 32 + lane;
+          if (c < NCH) {
+            float fg[V], fu[V];
+            F::unpack(wg[j], fg);
+            F::unpack(wu[j], fu);
+            float scg = 1.f, scu = 1.f;
+            if (WT == MOE_FP8E4M3_B128) {
+              const int cb = (c * V) >> 7;
+              scg = sgu[(size_t)(i >> 7) * HB + cb];
+              scu = sgu[(size_t)((I + i) >> 7) * HB + cb];
+            }
+#pragma unroll
+            for (int n = 0; n < kTokGroup; ++n) {
+              if (n < nt) {
+                float xv[V];
                 load_act<AT, V>(a.x, (size_t)tok[n] * H + (size_t)c * V, xv);
                 float dg = 0.f, du = 0.f;
 #pragma unroll
@@ -221,6 +420,7 @@ __global__ void __launch_bounds__(kGemvThreads, kTokGroup == 1 ? 2 : 1) gate_up_
           if (lane == 0) a.b.h[(size_t)a.b.gpu_pairs[tp + n] * I + i] = silu(sg) * su;
         }
       }
+      if (pe <= pb) break;
     }
   }
 }
@@ -321,7 +521,14 @@ __global__ void __launch_bounds__(kDCWarps * 32) down_combine_kernel(GemvArgs a,
                                                                      float* __restrict__ out, uint32_t* err) {
   using F = WFmt<WT>;
   constexpr int V = F::V;
-  extern __shared__ __align__(16) float dsm[];
+  extern __shared__ __align__(16) uint8_t dsm8[];
+  pdl_wait();
+  pdl_trigger();
+  const StagedPlan sp = stage_plan(dsm8, a);
+  int* s_slot = reinterpret_cast<int*>(dsm8 + sp.bytes);                  // [P] slot map
+  float* s_wt = reinterpret_cast<float*>(s_slot + a.P);                   // [P] gates
+  for (int i = threadIdx.x; i < a.P; i += blockDim.x) { s_slot[i] = a.b.slot_map[i]; s_wt[i] = w[i]; }
+  float* dsm = reinterpret_cast<float*>(dsm8 + sp.bytes + (((size_t)a.P * 8 + 15) & ~size_t(15)));
   const int NP = a.P + a.T * a.n_shared;
   const int H = a.H, I = a.I;
   const bool h_smem = (size_t)NP * I * sizeof(float) <= kDCHSmem;
@@ -330,6 +537,7 @@ __global__ void __launch_bounds__(kDCWarps * 32) down_combine_kernel(GemvArgs a,
   const float* hsrc = h_smem ? hs : a.b.h;
   const int lane = threadIdx.x & 31;
   const int ngpu = a.b.plan[P_NGPU];
+  __syncthreads();   // staged plan visible
   const int NCH = I / V;
   const size_t row_bytes = (size_t)I * F::ES;
   const size_t down_off = 2ull * (size_t)I * (size_t)H * F::ES;
@@ -345,7 +553,7 @@ __global__ void __launch_bounds__(kDCWarps * 32) down_combine_kernel(GemvArgs a,
 #pragma unroll
     for (int gi = 0; gi < kDCGroup; ++gi) {
       if (g0 + gi < ngpu) {
-        const uint4* wrow = reinterpret_cast<const uint4*>(a.b.gpu_w[g0 + gi] + down_off + (size_t)row * row_bytes);
+        const uint4* wrow = reinterpret_cast<const uint4*>(sp.w[g0 + gi] + down_off + (size_t)row * row_bytes);
 #pragma unroll
         for (int j = 0; j < kDCChunks; ++j) {
           const int c = j * 32 + lane;
@@ -369,10 +577,10 @@ __global__ void __launch_bounds__(kDCWarps * 32) down_combine_kernel(GemvArgs a,
       for (int gi = 0; gi < kDCGroup; ++gi) {
         const int g = g0 + gi;
         if (g >= ngpu) break;
-        const float* sd = reinterpret_cast<const float*>(a.b.gpu_w[g] + sd_off);
-        const int pb = a.b.gpu_off[g], pe = a.b.gpu_off[g + 1];
+        const float* sd = reinterpret_cast<const float*>(sp.w[g] + sd_off);
+        const int pb = sp.off[g], pe = sp.off[g + 1];
         for (int tp = pb; tp < pe; ++tp) {
-          const int pid = a.b.gpu_pairs[tp];
+          const int pid = sp.pid[tp];
           float acc = 0.f;
 #pragma unroll
           for (int j = 0; j < kDCChunks; ++j) {
@@ -407,7 +615,7 @@ __global__ void __launch_bounds__(kDCWarps * 32) down_combine_kernel(GemvArgs a,
       for (int j = 0; j < a.k; ++j) {
         const int p = t * a.k + j;
         float v;
-        if (a.b.slot_map[p] >= 0) {
+        if (s_slot[p] >= 0) {
           v = ys[p];
         } else if (cpu != nullptr) {
           v = __ldg(cpu + (size_t)p * H + r);
@@ -415,7 +623,7 @@ __global__ void __launch_bounds__(kDCWarps * 32) down_combine_kernel(GemvArgs a,
           v = 0.f;
           missing = true;
         }
-        acc = fmaf(__ldg(w + p), v, acc);
+        acc = fmaf(s_wt[p], v, acc);
       }
       if (a.n_shared) acc += ys[a.P + t];
       out[(size_t)t * H + r] = acc;
@@ -424,6 +632,289 @@ __global__ void __launch_bounds__(kDCWarps * 32) down_combine_kernel(GemvArgs a,
     if (r + nwarps < H) load_group(r + nwarps, 0);
   }
   if (__any_sync(0xffffffffu, missing) && lane == 0) atomicOr_system(err, kErrMissingCpuPart);
+}
+
+// ---- TMA-bulk-streamed GEMVs ------------------------------------------------------
+// Each CTA owns a block of consecutive weight rows (the same rows of every GPU
+// expert).  One thread issues cp.async.bulk copies of that row block of each
+// expert into a ring of shared-memory slots (an mbarrier per slot counts the
+// bytes in), so all of a CTA's weight bytes are in flight without staging them
+// in registers; the warps compute from shared memory and the slot is refilled
+// with the next expert once every warp is done with it.  Every wait is bounded
+// by the global timer (2 s): on timeout the kernel flags the error word, lets
+// its own copies land and returns.
+constexpr unsigned long long kBulkWaitNs = 2000000000ull;
+constexpr size_t kBulkBlockCap = 48 * 1024;    // bytes of one expert's row block
+constexpr size_t kBulkSmemBudget = 200 * 1024;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ unsigned long long gtime() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void bar_init(uint64_t* bar) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ bool bar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool bar_wait(uint64_t* bar, uint32_t parity) {
+  if (bar_test(bar, parity)) return true;
+  const unsigned long long t0 = gtime();
+  for (uint32_t i = 1;; ++i) {
+    if (bar_test(bar, parity)) return true;
+    if ((i & 255u) == 0u && gtime() - t0 > kBulkWaitNs) return false;
+  }
+}
+// one bulk copy global -> shared, counted on `bar` (whose expect_tx covers it)
+__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                               uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
+      : "memory");
+}
+__device__ __forceinline__ void bar_expect(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+
+struct BulkGeom {
+  int R;        // rows per CTA
+  int NB;       // ring slots
+  size_t BB;    // bytes per ring slot
+  size_t ring_off, plan_off, extra_off, smem;
+};
+
+// gate/up of the resident experts (pass 0), CTA = rows [i0, i0 + R) of every expert
+template <int WT, int AT>
+__global__ void __launch_bounds__(256) gate_up_bulk_kernel(GemvArgs a, BulkGeom geo, uint32_t* err) {
+  using F = WFmt<WT>;
+  constexpr int V = F::V;
+  extern __shared__ __align__(128) uint8_t sm[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm);
+  uint8_t* ring = sm + geo.ring_off;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < geo.NB; ++i) bar_init(&bars[i]);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  pdl_wait();
+  pdl_trigger();
+  const StagedPlan sp = stage_plan(sm + geo.plan_off, a);
+  const int H = a.H, I = a.I;
+  uint8_t* xsm = sm + geo.extra_off;
+  {
+    uint4* dst = reinterpret_cast<uint4*>(xsm);
+    const uint4* src = reinterpret_cast<const uint4*>(a.x);
+    const int n16 = (int)(((size_t)a.T * H * (AT == MOE_F32 ? 4 : 2)) >> 4);
+    for (int i = threadIdx.x; i < n16; i += blockDim.x) dst[i] = src[i];
+  }
+  const int ng = a.b.plan[P_NFIRST];   // pass 0: hits and the shared expert
+  const int i0 = blockIdx.x * geo.R;
+  const int nr = min(geo.R, I - i0);
+  const size_t row_bytes = (size_t)H * F::ES;
+  const uint32_t half = (uint32_t)(nr * row_bytes);
+  const uint64_t pol = evict_first_policy();
+  __syncthreads();
+  int last_issued[4] = {-1, -1, -1, -1};   // thread 0: the expert each slot was last loaded with
+  auto issue = [&](int g) {
+    last_issued[g % geo.NB] = g;
+    uint64_t* bar = &bars[g % geo.NB];
+    uint8_t* dst = ring + (size_t)(g % geo.NB) * geo.BB;
+    bar_expect(bar, 2 * half);
+    bulk_copy(dst, sp.w[g] + (size_t)i0 * row_bytes, half, bar, pol);
+    bulk_copy(dst + half, sp.w[g] + (size_t)(I + i0) * row_bytes, half, bar, pol);
+  };
+  if (threadIdx.x == 0)
+    for (int g = 0; g < min(geo.NB, ng); ++g) issue(g);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int NCH = H / V;
+  const int HB = H / 128;
+  bool ok = true;
+  for (int g = 0; g < ng && ok; ++g) {
+    const int slot = g % geo.NB;
+    // a block-uniform decision: every thread must leave the loop together
+    if (!__syncthreads_and(bar_wait(&bars[slot], (uint32_t)((g / geo.NB) & 1)))) { ok = false; break; }
+    const uint8_t* blk = ring + (size_t)slot * geo.BB;
+    const float* sgu = reinterpret_cast<const float*>(sp.w[g] + 3ull * (size_t)I * row_bytes);
+    const int pb = sp.off[g], pe = sp.off[g + 1];
+    for (int r = warp; r < nr; r += nw) {
+      const uint4* gate = reinterpret_cast<const uint4*>(blk + (size_t)r * row_bytes);
+      const uint4* up = reinterpret_cast<const uint4*>(blk + half + (size_t)r * row_bytes);
+      const int i = i0 + r;
+      for (int tp = pb; tp < pe; ++tp) {
+        const int t = sp.tok[tp];
+        float ag = 0.f, au = 0.f;
+        for (int c = lane; c < NCH; c += 32) {
+          float fg[V], fu[V], xv[V];
+          F::unpack(gate[c], fg);
+          F::unpack(up[c], fu);
+          load_x<AT, V>(xsm, (size_t)t * H + (size_t)c * V, xv);
+          float dg = 0.f, du = 0.f;
+#pragma unroll
+          for (int v = 0; v < V; ++v) { dg = fmaf(fg[v], xv[v], dg); du = fmaf(fu[v], xv[v], du); }
+          if (WT == MOE_FP8E4M3_B128) {
+            const int cb = (c * V) >> 7;
+            dg *= __ldg(sgu + (size_t)(i >> 7) * HB + cb);
+            du *= __ldg(sgu + (size_t)((I + i) >> 7) * HB + cb);
+          }
+          ag += dg;
+          au += du;
+        }
+        ag = warp_sum(ag);
+        au = warp_sum(au);
+        if (lane == 0) a.b.h[(size_t)sp.pid[tp] * I + i] = silu(ag) * au;
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && g + geo.NB < ng) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(g + geo.NB);
+    }
+  }
+  if (!ok && threadIdx.x == 0) {  // flag the timeout and let our own copies land before the CTA exits
+    atomicOr_system(err, kErrTimeout);
+    for (int s2 = 0; s2 < geo.NB && s2 < 4; ++s2) {
+      if (last_issued[s2] < 0) continue;
+      const uint32_t par = (uint32_t)((last_issued[s2] / geo.NB) & 1);
+      const unsigned long long t0 = gtime();
+      while (!bar_test(&bars[s2], par) && gtime() - t0 < kBulkWaitNs) {
+      }
+    }
+  }
+}
+
+// down projection + combine, CTA = output rows [r0, r0 + R)
+template <int WT>
+__global__ void __launch_bounds__(256) down_bulk_kernel(GemvArgs a, BulkGeom geo, const float* __restrict__ w,
+                                                        const float* __restrict__ cpu, float* __restrict__ out,
+                                                        uint32_t* err) {
+  using F = WFmt<WT>;
+  constexpr int V = F::V;
+  extern __shared__ __align__(128) uint8_t sm[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm);
+  uint8_t* ring = sm + geo.ring_off;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < geo.NB; ++i) bar_init(&bars[i]);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  pdl_wait();
+  pdl_trigger();
+  const StagedPlan sp = stage_plan(sm + geo.plan_off, a);
+  const int H = a.H, I = a.I;
+  const int NP = a.P + a.T * a.n_shared;
+  int* s_slot = reinterpret_cast<int*>(sm + geo.extra_off);
+  float* s_wt = reinterpret_cast<float*>(s_slot + a.P);
+  float* hs = reinterpret_cast<float*>(sm + geo.extra_off + (((size_t)a.P * 8 + 15) & ~size_t(15)));
+  float* ys = hs + (size_t)NP * I;
+  for (int i = threadIdx.x; i < a.P; i += blockDim.x) { s_slot[i] = a.b.slot_map[i]; s_wt[i] = w[i]; }
+  {
+    const float4* src = reinterpret_cast<const float4*>(a.b.h);
+    float4* dst = reinterpret_cast<float4*>(hs);
+    for (int i = threadIdx.x; i < NP * I / 4; i += blockDim.x) dst[i] = src[i];
+  }
+  const int ng = a.b.plan[P_NGPU];
+  const int r0 = blockIdx.x * geo.R;
+  const int nr = min(geo.R, H - r0);
+  const size_t row_bytes = (size_t)I * F::ES;
+  const size_t down_off = 2ull * (size_t)I * (size_t)H * F::ES;
+  const size_t sd_off = 3ull * (size_t)I * (size_t)H * F::ES + 4ull * (size_t)(2 * I / 128) * (H / 128);
+  const uint32_t bytes = (uint32_t)(nr * row_bytes);
+  const uint64_t pol = evict_first_policy();
+  __syncthreads();
+  int last_issued[4] = {-1, -1, -1, -1};   // thread 0: the expert each slot was last loaded with
+  auto issue = [&](int g) {
+    last_issued[g % geo.NB] = g;
+    uint64_t* bar = &bars[g % geo.NB];
+    bar_expect(bar, bytes);
+    bulk_copy(ring + (size_t)(g % geo.NB) * geo.BB, sp.w[g] + down_off + (size_t)r0 * row_bytes, bytes, bar,
+                   pol);
+  };
+  if (threadIdx.x == 0)
+    for (int g = 0; g < min(geo.NB, ng); ++g) issue(g);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int NCH = I / V;
+  const int IB = I / 128;
+  bool ok = true;
+  for (int g = 0; g < ng && ok; ++g) {
+    const int slot = g % geo.NB;
+    if (!__syncthreads_and(bar_wait(&bars[slot], (uint32_t)((g / geo.NB) & 1)))) { ok = false; break; }
+    const uint8_t* blk = ring + (size_t)slot * geo.BB;
+    const float* sd = reinterpret_cast<const float*>(sp.w[g] + sd_off);
+    const int pb = sp.off[g], pe = sp.off[g + 1];
+    for (int r = warp; r < nr; r += nw) {
+      const uint4* wrow = reinterpret_cast<const uint4*>(blk + (size_t)r * row_bytes);
+      const int row = r0 + r;
+      for (int tp = pb; tp < pe; ++tp) {
+        const int pid = sp.pid[tp];
+        float acc = 0.f;
+        for (int c = lane; c < NCH; c += 32) {
+          float fw[V];
+          F::unpack(wrow[c], fw);
+          const float4* hp = reinterpret_cast<const float4*>(hs + (size_t)pid * I + (size_t)c * V);
+          float d = 0.f;
+#pragma unroll
+          for (int v = 0; v < V; v += 4) {
+            const float4 q = hp[v / 4];
+            d = fmaf(fw[v], q.x, d); d = fmaf(fw[v + 1], q.y, d); d = fmaf(fw[v + 2], q.z, d); d = fmaf(fw[v + 3], q.w, d);
+          }
+          if (WT == MOE_FP8E4M3_B128) d *= __ldg(sd + (size_t)(row >> 7) * IB + ((c * V) >> 7));
+          acc += d;
+        }
+        acc = warp_sum(acc);
+        if (lane == 0) {
+          ys[(size_t)r * NP + pid] = acc;
+          a.b.y[(size_t)pid * H + row] = acc;
+        }
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && g + geo.NB < ng) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(g + geo.NB);
+    }
+  }
+  if (!ok && threadIdx.x == 0) {  // flag the timeout and let our own copies land before the CTA exits
+    atomicOr_system(err, kErrTimeout);
+    for (int s2 = 0; s2 < geo.NB && s2 < 4; ++s2) {
+      if (last_issued[s2] < 0) continue;
+      const uint32_t par = (uint32_t)((last_issued[s2] / geo.NB) & 1);
+      const unsigned long long t0 = gtime();
+      while (!bar_test(&bars[s2], par) && gtime() - t0 < kBulkWaitNs) {
+      }
+    }
+  }
+  if (!ok) return;
+  bool missing = false;
+  for (int idx = threadIdx.x; idx < nr * a.T; idx += blockDim.x) {
+    const int r = idx / a.T, t = idx % a.T;
+    float acc = 0.f;
+    for (int j = 0; j < a.k; ++j) {
+      const int p = t * a.k + j;
+      float v;
+      if (s_slot[p] >= 0) {
+        v = ys[(size_t)r * NP + p];
+      } else if (cpu != nullptr) {
+        v = __ldg(cpu + (size_t)p * H + r0 + r);
+      } else {
+        v = 0.f;
+        missing = true;
+      }
+      acc = fmaf(s_wt[p], v, acc);
+    }
+    if (a.n_shared) acc += ys[(size_t)r * NP + a.P + t];
+    out[(size_t)t * H + r0 + r] = acc;
+  }
+  if (missing) atomicOr_system(err, kErrMissingCpuPart);
 }
 
 // ---- combine: out[t] = sum_j w[t,j] * (slot >= 0 ? y : cpu_part) in j order (+ shared) --
@@ -496,26 +987,46 @@ __global__ void __launch_bounds__(512) copy_blobs_kernel(const int32_t* __restri
   }
 }
 
+constexpr size_t kXSmem = 64 * 1024;      // x staged in shared memory up to this size
+
+GemvArgs make_args(const Shape& sh, int pass, int T, const void* x, const DecodeBufs& b) {
+  GemvArgs a;
+  a.H = sh.H; a.I = sh.I; a.k = sh.k; a.T = T; a.P = T * sh.k; a.pass = pass; a.n_shared = sh.n_shared;
+  a.max_g = (sh.E < T * sh.k ? sh.E : T * sh.k) + sh.n_shared;
+  a.max_p = T * sh.k + T * sh.n_shared;
+  a.x_smem = (size_t)T * sh.H * (sh.adtype == MOE_F32 ? 4 : 2) <= kXSmem ? 1 : 0;
+  a.x = x; a.b = b;
+  return a;
+}
+
+size_t gate_up_smem(const GemvArgs& a, int adtype) {
+  return staged_plan_bytes(a.max_g, a.max_p) +
+         (a.x_smem ? (size_t)a.T * a.H * (adtype == MOE_F32 ? 4 : 2) : 0);
+}
+
 template <int WT, int AT>
 cudaError_t launch_gemv_typed(const GemvArgs& a, int sms, cudaStream_t s) {
   if (a.T == 1) {
-    gate_up_kernel<WT, AT, 1><<<2 * sms, kGemvThreads, 0, s>>>(a);
+    gate_up_kernel<WT, AT, 1><<<2 * sms, kGemvThreads, gate_up_smem(a, AT), s>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     down_kernel<WT, 1><<<2 * sms, kGemvThreads, 0, s>>>(a);
     return cudaGetLastError();
   }
-  gate_up_kernel<WT, AT, 4><<<sms, kGemvThreads, 0, s>>>(a);
+  gate_up_kernel<WT, AT, 4><<<sms, kGemvThreads, gate_up_smem(a, AT), s>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   down_kernel<WT, 4><<<sms, kGemvThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 
+// A plain launch (not programmatic): launched early, its CTAs would hold every
+// SM's registers while waiting and keep the fill of the same layer off the GPU.
 template <int WT, int AT>
 cudaError_t launch_gate_up_typed(const GemvArgs& a, int sms, cudaStream_t s) {
-  if (a.T == 1) gate_up_kernel<WT, AT, 1><<<2 * sms, kGemvThreads, 0, s>>>(a);
-  else gate_up_kernel<WT, AT, 4><<<sms, kGemvThreads, 0, s>>>(a);
+  const size_t smem = gate_up_smem(a, AT);
+  if (a.T == 1) gate_up_kernel<WT, AT, 1><<<2 * sms, kGemvThreads, smem, s>>>(a);
+  else gate_up_kernel<WT, AT, 4><<<sms, kGemvThreads, smem, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -531,36 +1042,158 @@ cudaError_t launch_down_combine_typed(const GemvArgs& a, const float* w, const f
                                       uint32_t* err, int sms, cudaStream_t s) {
   const size_t np = (size_t)(a.P + a.T * a.n_shared);
   const size_t hbytes = np * a.I * sizeof(float);
-  const size_t smem = (size_t)kDCWarps * np * sizeof(float) + (hbytes <= kDCHSmem ? hbytes : 0);
+  const size_t smem = staged_plan_bytes(a.max_g, a.max_p) + (((size_t)a.P * 8 + 15) & ~size_t(15)) +
+                      (size_t)kDCWarps * np * sizeof(float) + (hbytes <= kDCHSmem ? hbytes : 0);
   const int blocks = (a.H + kDCWarps - 1) / kDCWarps;
-  down_combine_kernel<WT><<<blocks < 4 * sms ? blocks : 4 * sms, kDCWarps * 32, smem, s>>>(a, w, cpu, out, err);
-  return cudaGetLastError();
+  return launch_pdl(down_combine_kernel<WT>, dim3(blocks < 4 * sms ? blocks : 4 * sms), dim3(kDCWarps * 32), smem, s,
+                    a, w, cpu, out, err);
 }
 
-GemvArgs make_args(const Shape& sh, int pass, int T, const void* x, const DecodeBufs& b) {
-  GemvArgs a;
-  a.H = sh.H; a.I = sh.I; a.k = sh.k; a.T = T; a.P = T * sh.k; a.pass = pass; a.n_shared = sh.n_shared;
-  a.x = x; a.b = b;
-  return a;
-}
 
 }  // namespace
 
 int gemv_block_threads() { return kGemvThreads; }
 
+template <int WT, int AT>
+cudaError_t carveout_typed() {
+  const void* ks[] = {(const void*)gate_up_kernel<WT, AT, 1>, (const void*)gate_up_kernel<WT, AT, 4>,
+                      (const void*)fill_gate_up_kernel<WT, AT, 1>, (const void*)fill_gate_up_kernel<WT, AT, 4>};
+  for (const void* k : ks) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, kDecodeCarveout);
+    if (e != cudaSuccess) return e;
+  }
+  for (const void* k : {(const void*)gate_up_bulk_kernel<WT, AT>}) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, kDecodeCarveout);
+    if (e != cudaSuccess) return e;
+  }
+  // x (up to kXSmem) plus the staged plan of up to 1024 tokens x top-8 pairs
+  const int gu_smem = (int)(kXSmem + staged_plan_bytes(4096 + 1, 1024 * 8 + 1024));
+  for (const void* k : {(const void*)gate_up_kernel<WT, AT, 1>, (const void*)gate_up_kernel<WT, AT, 4>}) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, gu_smem);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 cudaError_t setup_gemv_kernels() {
-  const int smem = (int)(kDCHSmem + (size_t)kDCWarps * kDCMaxPairs * sizeof(float));
-  cudaError_t e = cudaFuncSetAttribute(down_combine_kernel<MOE_F32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(down_combine_kernel<MOE_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(down_combine_kernel<MOE_FP8E4M3_B128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem);
+  const int smem = (int)(kDCHSmem + (size_t)kDCWarps * kDCMaxPairs * sizeof(float) +
+                         staged_plan_bytes(4096 + 1, kDCMaxPairs) + (size_t)kDCMaxPairs * 8);
+  for (const void* k : {(const void*)down_bulk_kernel<MOE_F32>, (const void*)down_bulk_kernel<MOE_BF16>,
+                        (const void*)down_bulk_kernel<MOE_FP8E4M3_B128>}) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, kDecodeCarveout);
+    if (e != cudaSuccess) return e;
+  }
+  const void* dc[] = {(const void*)down_combine_kernel<MOE_F32>, (const void*)down_combine_kernel<MOE_BF16>,
+                      (const void*)down_combine_kernel<MOE_FP8E4M3_B128>};
+  for (const void* k : dc) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, kDecodeCarveout);
+    if (e != cudaSuccess) return e;
+  }
+  cudaError_t e = carveout_typed<MOE_F32, MOE_F32>();
+  if (e == cudaSuccess) e = carveout_typed<MOE_F32, MOE_BF16>();
+  if (e == cudaSuccess) e = carveout_typed<MOE_BF16, MOE_F32>();
+  if (e == cudaSuccess) e = carveout_typed<MOE_BF16, MOE_BF16>();
+  if (e == cudaSuccess) e = carveout_typed<MOE_FP8E4M3_B128, MOE_F32>();
+  if (e == cudaSuccess) e = carveout_typed<MOE_FP8E4M3_B128, MOE_BF16>();
   return e;
 }
 
-cudaError_t launch_gate_up(const Shape& sh, int pass, int T, const void* x, DecodeBufs b, int sms, cudaStream_t s) {
+template <int WT, int AT>
+cudaError_t launch_fill_gate_up_typed(const GemvArgs& a, const int32_t* fills, const uint8_t* host,
+                                      const uint64_t* offs, uint8_t* slots, uint64_t S, int n_ctas, cudaStream_t s) {
+  if (a.T == 1) fill_gate_up_kernel<WT, AT, 1><<<n_ctas, kFillThreads, 0, s>>>(a, fills, host, offs, slots, S);
+  else fill_gate_up_kernel<WT, AT, 4><<<n_ctas, kFillThreads, 0, s>>>(a, fills, host, offs, slots, S);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fill_gate_up(const Shape& sh, int T, const void* x, DecodeBufs b, const uint8_t* host_pool_dev,
+                                const uint64_t* offsets, uint8_t* slots, int n_ctas, cudaStream_t s) {
+  const GemvArgs a = make_args(sh, 1, T, x, b);
+  const int32_t* f = b.fills;
+  switch (sh.wdtype * 2 + sh.adtype) {
+    case MOE_F32 * 2 + MOE_F32:
+      return launch_fill_gate_up_typed<MOE_F32, MOE_F32>(a, f, host_pool_dev, offsets, slots, sh.S, n_ctas, s);
+    case MOE_F32 * 2 + MOE_BF16:
+      return launch_fill_gate_up_typed<MOE_F32, MOE_BF16>(a, f, host_pool_dev, offsets, slots, sh.S, n_ctas, s);
+    case MOE_BF16 * 2 + MOE_F32:
+      return launch_fill_gate_up_typed<MOE_BF16, MOE_F32>(a, f, host_pool_dev, offsets, slots, sh.S, n_ctas, s);
+    case MOE_BF16 * 2 + MOE_BF16:
+      return launch_fill_gate_up_typed<MOE_BF16, MOE_BF16>(a, f, host_pool_dev, offsets, slots, sh.S, n_ctas, s);
+    case MOE_FP8E4M3_B128 * 2 + MOE_F32:
+      return launch_fill_gate_up_typed<MOE_FP8E4M3_B128, MOE_F32>(a, f, host_pool_dev, offsets, slots, sh.S, n_ctas, s);
+    case MOE_FP8E4M3_B128 * 2 + MOE_BF16:
+      return launch_fill_gate_up_typed<MOE_FP8E4M3_B128, MOE_BF16>(a, f, host_pool_dev, offsets, slots, sh.S, n_ctas, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+int wbytes(int wdtype) { return wdtype == MOE_F32 ? 4 : wdtype == MOE_BF16 ? 2 : 1; }
+size_t up128(size_t x) { return (x + 127) & ~size_t(127); }
+
+// Row blocks, ring slots and shared-memory layout of the bulk-streamed kernels;
+// NB < 2 means the shape does not fit and the register-staged kernel runs.
+BulkGeom gate_up_geom(const GemvArgs& a, int wdtype, int adtype, int sms) {
+  BulkGeom g{};
+  const size_t row = (size_t)a.H * wbytes(wdtype);
+  const size_t xbytes = (size_t)a.T * a.H * (adtype == MOE_F32 ? 4 : 2);
+  int R = (a.I + sms - 1) / sms;
+  R = (int)std::min<size_t>((size_t)R, kBulkBlockCap / (2 * row));
+  g.R = R < 1 ? 1 : R;
+  g.BB = up128(2 * (size_t)g.R * row);
+  const size_t fixed = 128 + up128(staged_plan_bytes(a.max_g, a.max_p)) + up128(xbytes);
+  g.NB = (g.BB <= kBulkSmemBudget && fixed < kBulkSmemBudget)
+             ? (int)std::min<size_t>(4, (kBulkSmemBudget - fixed) / g.BB) : 0;
+  if (xbytes > kXSmem || 2 * row * (size_t)g.R > kBulkBlockCap * 2) g.NB = 0;
+  g.ring_off = 128;
+  g.plan_off = g.ring_off + (size_t)g.NB * g.BB;
+  g.extra_off = g.plan_off + up128(staged_plan_bytes(a.max_g, a.max_p));
+  g.smem = g.extra_off + up128(xbytes);
+  return g;
+}
+
+BulkGeom down_geom(const GemvArgs& a, int wdtype, int sms) {
+  BulkGeom g{};
+  const size_t row = (size_t)a.I * wbytes(wdtype);
+  const size_t np = (size_t)(a.P + a.T * a.n_shared);
+  int R = (a.H + sms - 1) / sms;
+  R = (int)std::min<size_t>((size_t)R, kBulkBlockCap / row);
+  g.R = R < 1 ? 1 : R;
+  g.BB = up128((size_t)g.R * row);
+  const size_t extra = (((size_t)a.P * 8 + 15) & ~size_t(15)) + np * a.I * 4 + (size_t)g.R * np * 4;
+  const size_t fixed = 128 + up128(staged_plan_bytes(a.max_g, a.max_p)) + up128(extra);
+  g.NB = fixed < kBulkSmemBudget ? (int)std::min<size_t>(4, (kBulkSmemBudget - fixed) / g.BB) : 0;
+  g.ring_off = 128;
+  g.plan_off = g.ring_off + (size_t)g.NB * g.BB;
+  g.extra_off = g.plan_off + up128(staged_plan_bytes(a.max_g, a.max_p));
+  g.smem = g.extra_off + up128(extra);
+  return g;
+}
+
+template <int WT, int AT>
+cudaError_t launch_gate_up_bulk(const GemvArgs& a, const BulkGeom& geo, uint32_t* err, cudaStream_t s) {
+  gate_up_bulk_kernel<WT, AT><<<(a.I + geo.R - 1) / geo.R, 256, geo.smem, s>>>(a, geo, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gate_up(const Shape& sh, int pass, int T, const void* x, DecodeBufs b, int sms, cudaStream_t s,
+                           uint32_t* err) {
   const GemvArgs a = make_args(sh, pass, T, x, b);
+  if (pass == 0 && err != nullptr) {
+    const BulkGeom geo = gate_up_geom(a, sh.wdtype, sh.adtype, sms);
+    if (geo.NB >= 2) {
+      switch (sh.wdtype * 2 + sh.adtype) {
+        case MOE_F32 * 2 + MOE_F32: return launch_gate_up_bulk<MOE_F32, MOE_F32>(a, geo, err, s);
+        case MOE_F32 * 2 + MOE_BF16: return launch_gate_up_bulk<MOE_F32, MOE_BF16>(a, geo, err, s);
+        case MOE_BF16 * 2 + MOE_F32: return launch_gate_up_bulk<MOE_BF16, MOE_F32>(a, geo, err, s);
+        case MOE_BF16 * 2 + MOE_BF16: return launch_gate_up_bulk<MOE_BF16, MOE_BF16>(a, geo, err, s);
+        case MOE_FP8E4M3_B128 * 2 + MOE_F32: return launch_gate_up_bulk<MOE_FP8E4M3_B128, MOE_F32>(a, geo, err, s);
+        case MOE_FP8E4M3_B128 * 2 + MOE_BF16: return launch_gate_up_bulk<MOE_FP8E4M3_B128, MOE_BF16>(a, geo, err, s);
+      }
+    }
+  }
   switch (sh.wdtype * 2 + sh.adtype) {
     case MOE_F32 * 2 + MOE_F32: return launch_gate_up_typed<MOE_F32, MOE_F32>(a, sms, s);
     case MOE_F32 * 2 + MOE_BF16: return launch_gate_up_typed<MOE_F32, MOE_BF16>(a, sms, s);
@@ -577,8 +1210,24 @@ bool down_combine_fits(const Shape& sh, int T) {
   return T * sh.k + T * sh.n_shared <= kDCMaxPairs && sh.I / V <= 32 * kDCChunks;
 }
 
+template <int WT>
+cudaError_t launch_down_bulk(const GemvArgs& a, const BulkGeom& geo, const float* w, const float* cpu, float* out,
+                             uint32_t* err, cudaStream_t s) {
+  return launch_pdl(down_bulk_kernel<WT>, dim3((a.H + geo.R - 1) / geo.R), dim3(256), geo.smem, s, a, geo, w, cpu,
+                    out, err);
+}
+
 cudaError_t launch_down_combine(const Shape& sh, int T, const float* w, const float* cpu_part, DecodeBufs b,
                                 float* out, uint32_t* err, int sms, cudaStream_t s) {
+  {
+    const GemvArgs a = make_args(sh, 2, T, nullptr, b);
+    const BulkGeom geo = down_geom(a, sh.wdtype, sms);
+    if (geo.NB >= 2) {
+      if (sh.wdtype == MOE_F32) return launch_down_bulk<MOE_F32>(a, geo, w, cpu_part, out, err, s);
+      if (sh.wdtype == MOE_BF16) return launch_down_bulk<MOE_BF16>(a, geo, w, cpu_part, out, err, s);
+      return launch_down_bulk<MOE_FP8E4M3_B128>(a, geo, w, cpu_part, out, err, s);
+    }
+  }
   if (down_combine_fits(sh, T)) {
     const GemvArgs a = make_args(sh, 2, T, nullptr, b);
     if (sh.wdtype == MOE_F32) return launch_down_combine_typed<MOE_F32>(a, w, cpu_part, out, err, sms, s);
@@ -610,9 +1259,7 @@ cudaError_t launch_copy_blobs(const int32_t* count, const int32_t* skip, const i
 
 cudaError_t launch_expert_gemv(const Shape& sh, int pass, int T, const void* x, DecodeBufs b,
                                int sms, cudaStream_t s) {
-  GemvArgs a;
-  a.H = sh.H; a.I = sh.I; a.k = sh.k; a.T = T; a.P = T * sh.k; a.pass = pass; a.n_shared = sh.n_shared;
-  a.x = x; a.b = b;
+  const GemvArgs a = make_args(sh, pass, T, x, b);
   if (sh.wdtype == MOE_F32 && sh.adtype == MOE_F32) return launch_gemv_typed<MOE_F32, MOE_F32>(a, sms, s);
   if (sh.wdtype == MOE_F32 && sh.adtype == MOE_BF16) return launch_gemv_typed<MOE_F32, MOE_BF16>(a, sms, s);
   if (sh.wdtype == MOE_BF16 && sh.adtype == MOE_F32) return launch_gemv_typed<MOE_BF16, MOE_F32>(a, sms, s);

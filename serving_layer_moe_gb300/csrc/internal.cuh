@@ -19,6 +19,9 @@ constexpr int kMaxDecodeTokens = 1024;
 constexpr int kSlotBits = 20;              // slot index field of an LRU key
 constexpr uint64_t kMaxSlots = 1ull << kSlotBits;
 constexpr int kCtrlThreads = 512;
+// one shared-memory carveout (percent) for every decode kernel: no L1/shared
+// reconfiguration between the kernels of a layer
+constexpr int kDecodeCarveout = 100;
 
 // error word bits (device -> host through page-locked mapped memory)
 enum : uint32_t {
@@ -94,13 +97,40 @@ cudaError_t launch_copy_blobs(const int32_t* count, const int32_t* skip, const i
                               uint64_t S, int n_ctas, cudaStream_t s);
 cudaError_t launch_expert_gemv(const Shape& sh, int pass, int T, const void* x, DecodeBufs b,
                                int sms, cudaStream_t s);
-cudaError_t launch_gate_up(const Shape& sh, int pass, int T, const void* x, DecodeBufs b, int sms, cudaStream_t s);
+cudaError_t launch_fill_gate_up(const Shape& sh, int T, const void* x, DecodeBufs b, const uint8_t* host_pool_dev,
+                                const uint64_t* offsets, uint8_t* slots, int n_ctas, cudaStream_t s);
+cudaError_t launch_gate_up(const Shape& sh, int pass, int T, const void* x, DecodeBufs b, int sms, cudaStream_t s,
+                           uint32_t* err);
 cudaError_t launch_down_combine(const Shape& sh, int T, const float* w, const float* cpu_part, DecodeBufs b,
                                 float* out, uint32_t* err, int sms, cudaStream_t s);
 bool down_combine_fits(const Shape& sh, int T);
 cudaError_t launch_combine(const Shape& sh, int T, const float* w, const float* cpu_part,
                            DecodeBufs b, float* out, uint32_t* err, cudaStream_t s);
 int gemv_block_threads();
+
+// Programmatic dependent launch: a kernel launched this way may start while its
+// predecessor in the stream is still running.  It must call pdl_wait() before
+// touching anything the predecessor writes (and always calls it, so that its own
+// completion implies the predecessor's), and calls pdl_trigger() only after that
+// wait, so the guarantee chains from kernel to kernel.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 // blob geometry
 inline uint64_t blob_bytes(int wdtype, int H, int I) {

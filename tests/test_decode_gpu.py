@@ -159,3 +159,92 @@ def test_bench_bw_reports_two_bandwidths():
     bp, bh, rec = bench_bw(0, 9437184)
     assert bp > 1.0 and bh > 1.0
     assert rec == (bh > 2.0 * bp)
+
+
+def _small_shape(E, k, wdtype="bf16", H=256, I=128):
+    from workloads import Shape
+    return Shape(L=3, E=E, k=k, H=H, I=I, wdtype=wdtype, adtype="bf16" if wdtype != "f32" else "f32")
+
+
+def test_odd_expert_count_and_top3():
+    # E = 40 (bitmap words partly used), k = 3, K <= 32 victim path
+    from workloads import Config
+    cfg = Config("odd", _small_shape(40, 3), T=5, steps=20, capacity=17, routing="softmax", seed=91)
+    res = run_decode_parity(cfg, (3000, 2000), fp_every=3)
+    _ok(res)
+    assert res.cpu_pairs > 0 and res.fills > 0
+
+
+def test_radix_victim_path_small():
+    # K = min(E, T*k) = 64 > 32 selects victims by radix select
+    from workloads import Config
+    cfg = Config("radix", _small_shape(64, 4), T=16, steps=12, capacity=40, routing="softmax_bias", bias_std=0.5,
+                 seed=92)
+    res = run_decode_parity(cfg, (1000, 1000), fp_every=5)
+    _ok(res)
+
+
+def test_random_resizes_grow_and_shrink():
+    import torch
+    from oracle.cache import SlotCache
+    from workloads import Config
+    cfg = Config("resz", _small_shape(16, 2), T=3, steps=40, capacity=10, routing="softmax", seed=93)
+    s = cfg.shape
+    arena, offs, pool = build_pool(cfg)
+    cache, K = make_cache(cfg, pool, offs, None, (500, 500))
+    ora = SlotCache(s.L, s.E, cfg.capacity, K, 500, 500)
+    dev = torch.device("cuda", 0)
+    ids, w = routing_trace(cfg)
+    g = np.random.default_rng(0)
+    sm = torch.empty(cfg.T, s.k, dtype=torch.int32, device=dev)
+    out = torch.empty(cfg.T, s.H, device=dev)
+    cpu = torch.zeros(cfg.T, s.k, s.H, device=dev)
+    for st in range(cfg.steps):
+        if st % 5 == 4:
+            newC = int(g.integers(1, 40))
+            ora.resize(newC)
+            cache.resize(newC)
+        for l in range(s.L):
+            plan = ora.decode(l, ids[st, l])
+            cache.decode(l, torch_act(activations(cfg, st, l), dev), torch.from_numpy(ids[st, l]).to(dev),
+                         torch.from_numpy(w[st, l]).to(dev), out, cpu_part=cpu, slot_map=sm)
+            torch.cuda.synchronize()
+            assert np.array_equal(sm.cpu().numpy(), plan.slot_map), (st, l)
+        gs, os_ = cache.state(), ora.state()
+        for a, b in zip(gs[:4], os_[:4]):
+            assert np.array_equal(a, b), st
+        assert gs[4] == os_[4]
+    cache.close()
+
+
+def test_varying_T_on_one_cache():
+    import torch
+    from oracle.cache import SlotCache
+    from oracle.ffn import ExpertStore, combine, pair_outputs, relative_max_error
+    from workloads import Config
+    cfg = Config("varT", _small_shape(24, 4), T=12, steps=16, capacity=30, routing="softmax", seed=94)
+    s = cfg.shape
+    arena, offs, pool = build_pool(cfg)
+    cache, K = make_cache(cfg, pool, offs, None, (1000, 400))
+    ora = SlotCache(s.L, s.E, cfg.capacity, K, 1000, 400)
+    store = ExpertStore(arena, offs, s.wdtype, s.H, s.I, s.blob_bytes, memo=64)
+    dev = torch.device("cuda", 0)
+    ids, w = routing_trace(cfg)
+    g = np.random.default_rng(1)
+    for st in range(cfg.steps):
+        for l in range(s.L):
+            T = int(g.integers(1, cfg.T + 1))
+            i_t, w_t = ids[st, l, :T].copy(), w[st, l, :T].copy()
+            x = activations(cfg, st, l)[:T].copy()
+            plan = ora.decode(l, i_t)
+            y = pair_outputs(store, l, s.E, x, s.adtype, i_t)
+            ref = combine(w_t, y, plan.slot_map, y)
+            cpu = torch.from_numpy(np.where(plan.slot_map[..., None] < 0, y, np.nan).astype(np.float32)).to(dev)
+            out = torch.empty(T, s.H, device=dev)
+            sm = torch.empty(T, s.k, dtype=torch.int32, device=dev)
+            cache.decode(l, torch_act(x, dev), torch.from_numpy(i_t).to(dev), torch.from_numpy(w_t).to(dev), out,
+                         cpu_part=cpu, slot_map=sm)
+            torch.cuda.synchronize()
+            assert np.array_equal(sm.cpu().numpy(), plan.slot_map)
+            assert relative_max_error(out.cpu().numpy(), ref) <= TOL
+    cache.close()
