@@ -271,7 +271,7 @@ def main(args):
             enqueue_step()
         torch.cuda.synchronize(dev)
 
-    launches_per_layer = 5    # control, fill, gate/up resident, gate/up filled, down + combine
+    launches_per_layer = 4    # control, fill fused with the filled experts' gate/up, gate/up resident, down + combine
     # ---- timed region: inputs resident in HBM ---------------------------------
     cnt0 = cache.state()[3].copy()
     if world > 1:
@@ -357,9 +357,12 @@ def main(args):
     cache.profile_stop()
     cnt_p1 = cache.state()[3].copy()
     hbm_peak, bf16_peak, bf16_sust, peak_src = measured_peaks()
-    gpu_experts = int((cnt_p1[0] - cnt_p0[0]) + (cnt_p1[2] - cnt_p0[2]))   # hits + fills executed
-    gemv_bytes = gpu_experts * s.blob_bytes
-    gemv_kinds = ("gate_up_resident", "gate_up_filled", "down_combine")
+    # The HBM-bound part of a layer-step: the resident experts' GEMV pair (gate/up
+    # grid, which also has L2 fetch their W_down, then the down + combine grid).
+    # Algorithmic bytes: every resident (hit) expert's whole blob, read once.
+    resident = int(cnt_p1[0] - cnt_p0[0])
+    gemv_bytes = resident * s.blob_bytes
+    gemv_kinds = ("gate_up_resident", "down_combine")
     gemv_ms = sum(prof[k][0] for k in gemv_kinds)
     gemv_launches = prof["down_combine"][1]          # one per MoE-layer decode
     fill_bytes = int(cnt_p1[2] - cnt_p0[2]) * s.blob_bytes
@@ -385,8 +388,8 @@ def main(args):
         "e2e": {"value": round(e2e_steps * s.L * world / (ms_e2e / 1e3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": args.steps * s.L * launches_per_layer,
-        "roofline": {"bound": "hbm", "kernel": "expert GEMV per layer-step: gate/up of resident + filled slots, "
-                                               "down projection fused with the combine",
+        "roofline": {"bound": "hbm", "kernel": "resident-expert GEMV pair per layer-step: gate/up grid (with the L2 "
+                                               "fetch of W_down) + down-projection grid fused with the combine",
                      "achieved": round(gemv_bytes / (gemv_ms / 1e3) / 1e9, 1) if gemv_ms > 0 else None,
                      "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(gemv_bytes / (gemv_ms / 1e3) / 1e9 / hbm_peak, 3) if gemv_ms > 0 else None,
@@ -396,8 +399,8 @@ def main(args):
         "kernel_ms_share": {k: round(v[0] / total_prof_ms, 3) for k, v in prof.items() if v[1]},
         "kernel_us_per_layer": {k: round(1e3 * v[0] / max(1, v[1]), 2) for k, v in prof.items() if v[1]},
         "fill": {"achieved_gbs": round(fill_bytes / (prof["fill"][0] / 1e3) / 1e9, 1) if prof["fill"][0] > 0 else None,
-                 "bench_bw_B_P_gbs": round(bp_gbs, 1), "note": "fill kernel time includes waiting for nothing; "
-                 "it runs on the side stream concurrently with the resident-expert GEMV"},
+                 "bench_bw_B_P_gbs": round(bp_gbs, 1), "note": "fill kernel (with the filled experts' gate/up) "
+                 "on the side stream, concurrent with the resident-expert GEMV; bytes = filled blobs"},
         "control_us": round(1e3 * prof["control"][0] / max(1, prof["control"][1]), 2),
         "clocks": clk.summary(),
     }

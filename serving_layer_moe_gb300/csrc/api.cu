@@ -213,7 +213,8 @@ extern "C" moe_status moe_cache_create(const moe_config* cfg, const void* host_p
                  o_fill = take((size_t)std::max(c->K, 1) * 8), o_cpu = take((size_t)umax * 4),
                  o_sm = take((size_t)k.max_tokens * k.top_k * 4), o_goff = take((size_t)(max_gpu + 1) * 4),
                  o_gp = take(max_pairs * 4), o_gw = take((size_t)max_gpu * 8),
-                 o_h = take(max_pairs * k.inter * 4), o_y = take(max_pairs * k.hidden * 4);
+                 o_h = take(max_pairs * k.inter * 4), o_y = take(max_pairs * k.hidden * 4),
+                 o_arr = take((size_t)k.hidden * 4);
     CKB(cudaMalloc(&c->work, off));
     CKB(cudaMemset(c->work, 0, off));
     uint8_t* w = static_cast<uint8_t*>(c->work);
@@ -227,6 +228,7 @@ extern "C" moe_status moe_cache_create(const moe_config* cfg, const void* host_p
     c->b.gpu_w = reinterpret_cast<const uint8_t**>(w + o_gw);
     c->b.h = reinterpret_cast<float*>(w + o_h);
     c->b.y = reinterpret_cast<float*>(w + o_y);
+    c->b.arrive = reinterpret_cast<uint32_t*>(w + o_arr);
     c->dev_bytes = off;
   }
   c->dev_bytes += c->C * S + nflat * 12 + c->C * 12 + (k.n_shared ? (uint64_t)k.n_layers * S : 0);
@@ -257,8 +259,13 @@ extern "C" moe_status moe_cache_destroy(moe_cache* c) {
 }
 
 // ---------------------------------------------------------------------------
-// decode: control -> [fill + gate/up of filled experts on the side stream] ->
-//         gate/up of resident experts -> wait fills -> down projection + combine
+// decode: control -> side stream: fill + gate/up of the filled experts, then
+//                    their down projection
+//                 -> gate/up of the resident experts, then their down projection
+//                 -> the second of the two down grids to finish a row block
+//                    forms its combine; the call ends with the streams joined.
+// Shapes whose h or down rows do not fit the split kernels run the down
+// projection of every GPU expert after the fills instead.
 // ---------------------------------------------------------------------------
 extern "C" moe_status moe_layer_decode(moe_cache* c, int32_t layer, int32_t T, const void* x,
                                        const int32_t* ids, const float* w, const float* cpu_part,
@@ -285,10 +292,23 @@ extern "C" moe_status moe_layer_decode(moe_cache* c, int32_t layer, int32_t T, c
     ProfScope p(c, c->fill_stream, PROF_FILL);
     CK(launch_fill_gate_up(c->sh, T, x, c->b, c->host_pool_dev, c->offsets, c->slots, c->fill_ctas, c->fill_stream));
   }
+  const bool split = down_split_ok(c->sh, T, c->sms);
+  if (split) {
+    ProfScope p(c, c->fill_stream, PROF_DOWN_FILLED);
+    CK(launch_down_split(c->sh, 1, T, w, cpu_part, c->b, out, c->err_dev, c->sms, c->fill_stream));
+  }
   CK(cudaEventRecord(c->ev_fill, c->fill_stream));
   {
     ProfScope p(c, s, PROF_GATE_UP_RESIDENT);
     CK(launch_gate_up(c->sh, 0, T, x, c->b, c->sms, s, c->err_dev));
+  }
+  if (split) {
+    {
+      ProfScope p(c, s, PROF_DOWN_COMBINE);
+      CK(launch_down_split(c->sh, 0, T, w, cpu_part, c->b, out, c->err_dev, c->sms, s));
+    }
+    CK(cudaStreamWaitEvent(s, c->ev_fill, 0));
+    return MOE_OK;
   }
   CK(cudaStreamWaitEvent(s, c->ev_fill, 0));
   {

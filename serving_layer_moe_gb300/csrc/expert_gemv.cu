@@ -300,7 +300,8 @@ __global__ void __launch_bounds__(kGemvThreads, kTokGroup == 1 ? 2 : 1) gate_up_
 // every gate/up row pair is streamed from page-locked host memory over the host
 // link, written into the slot, and dotted with the expert's tokens on the way
 // through (h of its pairs, like gate_up_kernel); the rest of the blob (W_down
-// and, for fp8, the scales) is copied in 4 KB pieces.  The bytes cross the link
+// and, for fp8, the scales) is copied in 4 KB pieces with default stores, so the
+// down projection that follows finds them in L2.  The bytes cross the link
 // once and the filled experts need no separate gate/up pass.
 constexpr int kFillThreads = 256;   // small CTAs: they share SMs with the resident-expert GEMV
 
@@ -310,6 +311,7 @@ fill_gate_up_kernel(GemvArgs a, const int32_t* __restrict__ fills, const uint8_t
                     const uint64_t* __restrict__ offs, uint8_t* __restrict__ slots, uint64_t S) {
   using F = WFmt<WT>;
   constexpr int V = F::V;
+  pdl_trigger();   // the filled-expert down grid may stage its plan meanwhile; it waits for this grid to finish
   const int* plan = a.b.plan;
   const int q = plan[P_Q];
   if (q == 0) return;
@@ -345,7 +347,7 @@ fill_gate_up_kernel(GemvArgs a, const int32_t* __restrict__ fills, const uint8_t
 #pragma unroll
       for (int j = 0; j < kPiece / 32; ++j) {
         const uint64_t c = c0 + (uint64_t)j * 32 + lane;
-        if (c < c1) __stcs(dst + c, v[j]);
+        if (c < c1) dst[c] = v[j];   // default policy: the down projection reads these next, from L2
       }
       continue;
     }
@@ -635,17 +637,14 @@ __global__ void __launch_bounds__(kDCWarps * 32) down_combine_kernel(GemvArgs a,
 }
 
 // ---- TMA-bulk-streamed GEMVs ------------------------------------------------------
-// Each CTA owns a block of consecutive weight rows (the same rows of every GPU
-// expert).  One thread issues cp.async.bulk copies of that row block of each
-// expert into a ring of shared-memory slots (an mbarrier per slot counts the
-// bytes in), so all of a CTA's weight bytes are in flight without staging them
-// in registers; the warps compute from shared memory and the slot is refilled
-// with the next expert once every warp is done with it.  Every wait is bounded
-// by the global timer (2 s): on timeout the kernel flags the error word, lets
-// its own copies land and returns.
+// Weight bytes go global -> shared memory by cp.async.bulk, so a CTA holds far
+// more bytes in flight than registers could stage.  Every warp owns a ring of
+// shared-memory stages with one mbarrier each: its lane 0 keeps the next items'
+// copies in flight while the warp computes the current one, and nothing but the
+// warp's own barrier orders its stream.  Every wait is bounded by the global
+// timer (2 s): on timeout the kernel flags the error word, lets its own copies
+// land and returns.
 constexpr unsigned long long kBulkWaitNs = 2000000000ull;
-constexpr size_t kBulkBlockCap = 48 * 1024;    // bytes of one expert's row block
-constexpr size_t kBulkSmemBudget = 200 * 1024;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -684,27 +683,80 @@ __device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t b
       "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
       : "memory");
 }
+// asks L2 to fetch [p, p + bytes) from HBM (16-byte aligned, 16-byte multiple); no completion
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+// the same without an L2 eviction hint (data that other CTAs read too)
+__device__ __forceinline__ void bulk_copy_keep(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_addr(dst)),
+               "l"(src), "r"(bytes), "r"(smem_addr(bar))
+               : "memory");
+}
 __device__ __forceinline__ void bar_expect(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
 }
 
+// Sums 16 per-lane values over the warp: 16 shuffles instead of 16 x 5.  Each
+// step halves the values a lane holds, exchanging the other half with the lane
+// `off` away; afterwards lane l holds the full sum of value (l >> 1).
+__device__ __forceinline__ float reduce16(float (&v)[16], int lane) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const bool hi = lane & 16;
+    const float send = hi ? v[j] : v[j + 8];
+    v[j] = (hi ? v[j + 8] : v[j]) + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const bool hi = lane & 8;
+    const float send = hi ? v[j] : v[j + 4];
+    v[j] = (hi ? v[j + 4] : v[j]) + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const bool hi = lane & 4;
+    const float send = hi ? v[j] : v[j + 2];
+    v[j] = (hi ? v[j + 2] : v[j]) + __shfl_xor_sync(0xffffffffu, send, 4);
+  }
+  {
+    const bool hi = lane & 2;
+    const float send = hi ? v[0] : v[1];
+    v[0] = (hi ? v[1] : v[0]) + __shfl_xor_sync(0xffffffffu, send, 2);
+  }
+  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+}
+
+constexpr int kDownRows = 16;   // output rows per CTA of the bulk down kernel, at most
+constexpr size_t kPrefetchPiece = 32 * 1024;
+// dynamic shared memory the bulk kernels may ask for (the down kernel also has a few static bytes)
+constexpr int kBulkSmemAttr = 224 * 1024;
+
 struct BulkGeom {
-  int R;        // rows per CTA
-  int NB;       // ring slots
-  size_t BB;    // bytes per ring slot
+  int R;        // down: output rows per CTA
+  int NS;       // ring stages per warp (< 2: the shape does not fit)
+  int NW;       // warps per CTA
+  int h_smem;   // down: h of every pair staged in shared memory
+  int grid;     // CTAs
+  size_t SB;    // bytes per stage
   size_t ring_off, plan_off, extra_off, smem;
 };
 
-// gate/up of the resident experts (pass 0), CTA = rows [i0, i0 + R) of every expert
+// Gate/up of the resident experts (pass 0).  A work item is one (expert, row i)
+// pair: gate row i and up row I + i, 2 H weight elements; warp w of the grid
+// takes items w, w + warps, ...  x is staged per CTA in shared memory while
+// the first items are in flight.
 template <int WT, int AT>
 __global__ void __launch_bounds__(256) gate_up_bulk_kernel(GemvArgs a, BulkGeom geo, uint32_t* err) {
   using F = WFmt<WT>;
   constexpr int V = F::V;
   extern __shared__ __align__(128) uint8_t sm[];
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm);
-  uint8_t* ring = sm + geo.ring_off;
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < geo.NB; ++i) bar_init(&bars[i]);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm) + warp * geo.NS;
+  uint8_t* ring = sm + geo.ring_off + (size_t)warp * geo.NS * geo.SB;
+  if (lane == 0) {
+    for (int i = 0; i < geo.NS; ++i) bar_init(&bars[i]);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   pdl_wait();
@@ -712,80 +764,98 @@ __global__ void __launch_bounds__(256) gate_up_bulk_kernel(GemvArgs a, BulkGeom 
   const StagedPlan sp = stage_plan(sm + geo.plan_off, a);
   const int H = a.H, I = a.I;
   uint8_t* xsm = sm + geo.extra_off;
+  const int ng = a.b.plan[P_NFIRST];   // pass 0: hits and the shared expert
+  __syncthreads();
+  const long items = (long)ng * I;
+  const long nwarps = (long)gridDim.x * geo.NW;
+  const long w0 = (long)blockIdx.x * geo.NW + warp;
+  const size_t row_bytes = (size_t)H * F::ES;
+  const uint64_t pol = evict_first_policy();
+  long last_issued[4] = {-1, -1, -1, -1};
+  auto issue = [&](long it, int st) {   // lane 0 only
+    const int g = (int)(it / I), i = (int)(it % I);
+    last_issued[st] = it;
+    bar_expect(&bars[st], (uint32_t)(2 * row_bytes));
+    uint8_t* dst = ring + (size_t)st * geo.SB;
+    bulk_copy(dst, sp.w[g] + (size_t)i * row_bytes, (uint32_t)row_bytes, &bars[st], pol);
+    bulk_copy(dst + row_bytes, sp.w[g] + (size_t)(I + i) * row_bytes, (uint32_t)row_bytes, &bars[st], pol);
+  };
+  // W_down of these experts is read by the down grid right after this one: once a
+  // warp has issued its last row copy it asks L2 to fetch its share of those bytes
+  // (32 KB pieces, piece p to warp p mod warps), so they queue behind the rows.
+  const size_t wd_bytes = (size_t)H * I * F::ES;
+  const long pf_per = (long)((wd_bytes + kPrefetchPiece - 1) / kPrefetchPiece);
+  auto prefetch_down = [&]() {   // lane 0 only
+    for (long p = w0; p < (long)ng * pf_per; p += nwarps) {
+      const int g = (int)(p / pf_per);
+      const size_t o = (size_t)(p % pf_per) * kPrefetchPiece;
+      const size_t n = wd_bytes - o < kPrefetchPiece ? wd_bytes - o : kPrefetchPiece;
+      bulk_prefetch_l2(sp.w[g] + 2ull * (size_t)I * row_bytes + o, (uint32_t)n);
+    }
+  };
+  const long n_mine = items > w0 ? (items - w0 + nwarps - 1) / nwarps : 0;
+  if (lane == 0) {
+    for (int k = 0; k < geo.NS; ++k) {
+      const long it = w0 + (long)k * nwarps;
+      if (it < items) issue(it, k);
+    }
+    if (n_mine <= geo.NS) prefetch_down();
+  }
   {
     uint4* dst = reinterpret_cast<uint4*>(xsm);
     const uint4* src = reinterpret_cast<const uint4*>(a.x);
     const int n16 = (int)(((size_t)a.T * H * (AT == MOE_F32 ? 4 : 2)) >> 4);
     for (int i = threadIdx.x; i < n16; i += blockDim.x) dst[i] = src[i];
   }
-  const int ng = a.b.plan[P_NFIRST];   // pass 0: hits and the shared expert
-  const int i0 = blockIdx.x * geo.R;
-  const int nr = min(geo.R, I - i0);
-  const size_t row_bytes = (size_t)H * F::ES;
-  const uint32_t half = (uint32_t)(nr * row_bytes);
-  const uint64_t pol = evict_first_policy();
   __syncthreads();
-  int last_issued[4] = {-1, -1, -1, -1};   // thread 0: the expert each slot was last loaded with
-  auto issue = [&](int g) {
-    last_issued[g % geo.NB] = g;
-    uint64_t* bar = &bars[g % geo.NB];
-    uint8_t* dst = ring + (size_t)(g % geo.NB) * geo.BB;
-    bar_expect(bar, 2 * half);
-    bulk_copy(dst, sp.w[g] + (size_t)i0 * row_bytes, half, bar, pol);
-    bulk_copy(dst + half, sp.w[g] + (size_t)(I + i0) * row_bytes, half, bar, pol);
-  };
-  if (threadIdx.x == 0)
-    for (int g = 0; g < min(geo.NB, ng); ++g) issue(g);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const int NCH = H / V;
   const int HB = H / 128;
   bool ok = true;
-  for (int g = 0; g < ng && ok; ++g) {
-    const int slot = g % geo.NB;
-    // a block-uniform decision: every thread must leave the loop together
-    if (!__syncthreads_and(bar_wait(&bars[slot], (uint32_t)((g / geo.NB) & 1)))) { ok = false; break; }
-    const uint8_t* blk = ring + (size_t)slot * geo.BB;
+  int k = 0;
+  for (long it = w0; it < items; it += nwarps, ++k) {
+    const int st = k % geo.NS;
+    if (!__all_sync(0xffffffffu, bar_wait(&bars[st], (uint32_t)((k / geo.NS) & 1)))) { ok = false; break; }
+    const int g = (int)(it / I), i = (int)(it % I);
+    const uint4* gate = reinterpret_cast<const uint4*>(ring + (size_t)st * geo.SB);
+    const uint4* up = reinterpret_cast<const uint4*>(ring + (size_t)st * geo.SB + row_bytes);
     const float* sgu = reinterpret_cast<const float*>(sp.w[g] + 3ull * (size_t)I * row_bytes);
     const int pb = sp.off[g], pe = sp.off[g + 1];
-    for (int r = warp; r < nr; r += nw) {
-      const uint4* gate = reinterpret_cast<const uint4*>(blk + (size_t)r * row_bytes);
-      const uint4* up = reinterpret_cast<const uint4*>(blk + half + (size_t)r * row_bytes);
-      const int i = i0 + r;
-      for (int tp = pb; tp < pe; ++tp) {
-        const int t = sp.tok[tp];
-        float ag = 0.f, au = 0.f;
-        for (int c = lane; c < NCH; c += 32) {
-          float fg[V], fu[V], xv[V];
-          F::unpack(gate[c], fg);
-          F::unpack(up[c], fu);
-          load_x<AT, V>(xsm, (size_t)t * H + (size_t)c * V, xv);
-          float dg = 0.f, du = 0.f;
+    for (int tp = pb; tp < pe; ++tp) {
+      const int t = sp.tok[tp];
+      float ag = 0.f, au = 0.f;
+      for (int c = lane; c < NCH; c += 32) {
+        float fg[V], fu[V], xv[V];
+        F::unpack(gate[c], fg);
+        F::unpack(up[c], fu);
+        load_x<AT, V>(xsm, (size_t)t * H + (size_t)c * V, xv);
+        float dg = 0.f, du = 0.f;
 #pragma unroll
-          for (int v = 0; v < V; ++v) { dg = fmaf(fg[v], xv[v], dg); du = fmaf(fu[v], xv[v], du); }
-          if (WT == MOE_FP8E4M3_B128) {
-            const int cb = (c * V) >> 7;
-            dg *= __ldg(sgu + (size_t)(i >> 7) * HB + cb);
-            du *= __ldg(sgu + (size_t)((I + i) >> 7) * HB + cb);
-          }
-          ag += dg;
-          au += du;
+        for (int v = 0; v < V; ++v) { dg = fmaf(fg[v], xv[v], dg); du = fmaf(fu[v], xv[v], du); }
+        if (WT == MOE_FP8E4M3_B128) {
+          const int cb = (c * V) >> 7;
+          dg *= __ldg(sgu + (size_t)(i >> 7) * HB + cb);
+          du *= __ldg(sgu + (size_t)((I + i) >> 7) * HB + cb);
         }
-        ag = warp_sum(ag);
-        au = warp_sum(au);
-        if (lane == 0) a.b.h[(size_t)sp.pid[tp] * I + i] = silu(ag) * au;
+        ag += dg;
+        au += du;
       }
+      ag = warp_sum(ag);
+      au = warp_sum(au);
+      if (lane == 0) a.b.h[(size_t)sp.pid[tp] * I + i] = silu(ag) * au;
     }
-    __syncthreads();
-    if (threadIdx.x == 0 && g + geo.NB < ng) {
+    __syncwarp();
+    if (lane == 0 && it + (long)geo.NS * nwarps < items) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      issue(g + geo.NB);
+      issue(it + (long)geo.NS * nwarps, st);
+      if (k == n_mine - geo.NS - 1) prefetch_down();   // that was this warp's last row copy
     }
   }
-  if (!ok && threadIdx.x == 0) {  // flag the timeout and let our own copies land before the CTA exits
+  if (!ok && lane == 0) {  // flag the timeout; this warp's copies land before it exits
     atomicOr_system(err, kErrTimeout);
-    for (int s2 = 0; s2 < geo.NB && s2 < 4; ++s2) {
+    for (int s2 = 0; s2 < geo.NS; ++s2) {
       if (last_issued[s2] < 0) continue;
-      const uint32_t par = (uint32_t)((last_issued[s2] / geo.NB) & 1);
+      const long kk = (last_issued[s2] - w0) / nwarps;
+      const uint32_t par = (uint32_t)((kk / geo.NS) & 1);
       const unsigned long long t0 = gtime();
       while (!bar_test(&bars[s2], par) && gtime() - t0 < kBulkWaitNs) {
       }
@@ -793,36 +863,58 @@ __global__ void __launch_bounds__(256) gate_up_bulk_kernel(GemvArgs a, BulkGeom 
   }
 }
 
-// down projection + combine, CTA = output rows [r0, r0 + R)
-template <int WT>
+// Down projection fused with the combine.  A CTA owns output rows [r0, r0 + R),
+// R <= 16, of the GPU experts of its pass (0: resident, 1: filled, 2: all).
+// Warp w takes experts g0 + w, g0 + w + NW, ...  With kRing, their row blocks
+// (R rows x I) stream through the warp's ring of shared-memory stages by bulk
+// copy; without it (the filled experts, just written by the fill and still in
+// L2) the rows are loaded directly.  Per pair, each lane holds its columns of h
+// in registers and accumulates all R rows; one 16-value warp reduction leaves
+// row (lane >> 1) in lane pairs.  The weight copies need only the control
+// kernel's plan and the slot contents, both complete before this grid starts
+// (a fill is a full dependency), so they are issued before the wait on the
+// gate/up grid; h comes by bulk copy (pair rows) after it.
+//
+// Combine, out[t, r] = sum_j w[t,j] * (slot >= 0 ? y : cpu_part) in j order
+// (+ shared): pass 2 forms it from shared memory after one barrier.  Passes 0
+// and 1 are two grids over the same row blocks: each publishes its y, counts
+// itself in arrive[block], and the second of the two (odd count before its
+// increment) forms the block's combine from y in global memory.
+template <int WT, bool kRing>
 __global__ void __launch_bounds__(256) down_bulk_kernel(GemvArgs a, BulkGeom geo, const float* __restrict__ w,
                                                         const float* __restrict__ cpu, float* __restrict__ out,
                                                         uint32_t* err) {
   using F = WFmt<WT>;
   constexpr int V = F::V;
+  constexpr int J = 32 / V;   // 16-byte chunks per lane per column segment (32 h values in registers)
   extern __shared__ __align__(128) uint8_t sm[];
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm);
-  uint8_t* ring = sm + geo.ring_off;
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < geo.NB; ++i) bar_init(&bars[i]);
+  __shared__ uint32_t s_second;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm) + warp * geo.NS;
+  uint64_t* hbar = reinterpret_cast<uint64_t*>(sm) + 31;   // ring barriers use at most 8 x 2
+  uint8_t* ring = sm + geo.ring_off + (size_t)warp * geo.NS * geo.SB;
+  if (lane == 0) {
+    if (kRing)
+      for (int i = 0; i < geo.NS; ++i) bar_init(&bars[i]);
+    if (warp == 0) bar_init(hbar);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  pdl_wait();
-  pdl_trigger();
   const StagedPlan sp = stage_plan(sm + geo.plan_off, a);
   const int H = a.H, I = a.I;
   const int NP = a.P + a.T * a.n_shared;
   int* s_slot = reinterpret_cast<int*>(sm + geo.extra_off);
   float* s_wt = reinterpret_cast<float*>(s_slot + a.P);
-  float* hs = reinterpret_cast<float*>(sm + geo.extra_off + (((size_t)a.P * 8 + 15) & ~size_t(15)));
-  float* ys = hs + (size_t)NP * I;
+  float* ys = reinterpret_cast<float*>(sm + geo.extra_off + (((size_t)a.P * 8 + 127) & ~size_t(127)));
+  float* hs = ys + ((((size_t)geo.R * NP * 4 + NP + 127) & ~size_t(127)) >> 2);
   for (int i = threadIdx.x; i < a.P; i += blockDim.x) { s_slot[i] = a.b.slot_map[i]; s_wt[i] = w[i]; }
-  {
-    const float4* src = reinterpret_cast<const float4*>(a.b.h);
-    float4* dst = reinterpret_cast<float4*>(hs);
-    for (int i = threadIdx.x; i < NP * I / 4; i += blockDim.x) dst[i] = src[i];
-  }
-  const int ng = a.b.plan[P_NGPU];
+  const float* hsrc = geo.h_smem ? hs : a.b.h;
+  int g0, g1;
+  pass_range(a, g0, g1);
+  uint8_t* s_mine = reinterpret_cast<uint8_t*>(ys + (size_t)geo.R * NP);   // [NP] pairs of this grid's experts
+  __syncthreads();   // staged plan visible
+  for (int i = threadIdx.x; i < NP; i += blockDim.x) s_mine[i] = 0;
+  __syncthreads();
+  for (int tp = sp.off[g0] + threadIdx.x; tp < sp.off[g1]; tp += blockDim.x) s_mine[sp.pid[tp]] = 1;
   const int r0 = blockIdx.x * geo.R;
   const int nr = min(geo.R, H - r0);
   const size_t row_bytes = (size_t)I * F::ES;
@@ -830,70 +922,185 @@ __global__ void __launch_bounds__(256) down_bulk_kernel(GemvArgs a, BulkGeom geo
   const size_t sd_off = 3ull * (size_t)I * (size_t)H * F::ES + 4ull * (size_t)(2 * I / 128) * (H / 128);
   const uint32_t bytes = (uint32_t)(nr * row_bytes);
   const uint64_t pol = evict_first_policy();
+  const bool h_copy = geo.h_smem && g1 > g0;
   __syncthreads();
-  int last_issued[4] = {-1, -1, -1, -1};   // thread 0: the expert each slot was last loaded with
-  auto issue = [&](int g) {
-    last_issued[g % geo.NB] = g;
-    uint64_t* bar = &bars[g % geo.NB];
-    bar_expect(bar, bytes);
-    bulk_copy(ring + (size_t)(g % geo.NB) * geo.BB, sp.w[g] + down_off + (size_t)r0 * row_bytes, bytes, bar,
-                   pol);
+  int last_issued[2] = {-1, -1};
+  auto issue = [&](int g, int st) {   // lane 0 only
+    last_issued[st] = g;
+    bar_expect(&bars[st], bytes);
+    bulk_copy(ring + (size_t)st * geo.SB, sp.w[g] + down_off + (size_t)r0 * row_bytes, bytes, &bars[st], pol);
   };
-  if (threadIdx.x == 0)
-    for (int g = 0; g < min(geo.NB, ng); ++g) issue(g);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  if (kRing && lane == 0)
+    for (int k = 0; k < geo.NS; ++k) {
+      const int g = g0 + warp + k * geo.NW;
+      if (g < g1) issue(g, k);
+    }
+  pdl_wait();   // h of the resident experts is complete from here on
+  pdl_trigger();
+  if (h_copy && threadIdx.x == 0) {   // the h rows (I floats, a 16-byte multiple) of this pass's pairs
+    const int pb = sp.off[g0], pe = sp.off[g1];
+    bar_expect(hbar, (uint32_t)((size_t)(pe - pb) * I * 4));
+    for (int tp = pb; tp < pe; ++tp) {
+      const size_t o = (size_t)sp.pid[tp] * I;
+      bulk_copy_keep(hs + o, a.b.h + o, (uint32_t)(I * 4), hbar);
+    }
+  }
   const int NCH = I / V;
   const int IB = I / 128;
   bool ok = true;
-  for (int g = 0; g < ng && ok; ++g) {
-    const int slot = g % geo.NB;
-    if (!__syncthreads_and(bar_wait(&bars[slot], (uint32_t)((g / geo.NB) & 1)))) { ok = false; break; }
-    const uint8_t* blk = ring + (size_t)slot * geo.BB;
-    const float* sd = reinterpret_cast<const float*>(sp.w[g] + sd_off);
-    const int pb = sp.off[g], pe = sp.off[g + 1];
-    for (int r = warp; r < nr; r += nw) {
-      const uint4* wrow = reinterpret_cast<const uint4*>(blk + (size_t)r * row_bytes);
-      const int row = r0 + r;
-      for (int tp = pb; tp < pe; ++tp) {
+  if (!kRing) {   // (expert, row) items over all warps; the per-lane sums and the butterfly match the ring path
+    if (h_copy && !__all_sync(0xffffffffu, bar_wait(hbar, 0))) ok = false;
+    const int n_items = (g1 - g0) * nr;
+    for (int item = warp; ok && item < n_items; item += geo.NW) {
+      const int g = g0 + item / nr, r = item % nr;
+      const uint4* wrow = reinterpret_cast<const uint4*>(sp.w[g] + down_off + (size_t)(r0 + r) * row_bytes);
+      const float* sd = reinterpret_cast<const float*>(sp.w[g] + sd_off);
+      if (item + geo.NW < n_items && lane == 0) {   // the warp's next row: on its way to L1 meanwhile
+        const int g2 = g0 + (item + geo.NW) / nr, r2 = (item + geo.NW) % nr;
+        const uint8_t* nx = sp.w[g2] + down_off + (size_t)(r0 + r2) * row_bytes;
+        for (size_t o = 0; o < row_bytes; o += 128) asm volatile("prefetch.global.L1 [%0];" ::"l"(nx + o));
+      }
+      for (int tp = sp.off[g]; tp < sp.off[g + 1]; ++tp) {
         const int pid = sp.pid[tp];
         float acc = 0.f;
-        for (int c = lane; c < NCH; c += 32) {
-          float fw[V];
-          F::unpack(wrow[c], fw);
-          const float4* hp = reinterpret_cast<const float4*>(hs + (size_t)pid * I + (size_t)c * V);
+        for (int c0 = 0; c0 < NCH; c0 += 32 * J) {
           float d = 0.f;
 #pragma unroll
-          for (int v = 0; v < V; v += 4) {
-            const float4 q = hp[v / 4];
-            d = fmaf(fw[v], q.x, d); d = fmaf(fw[v + 1], q.y, d); d = fmaf(fw[v + 2], q.z, d); d = fmaf(fw[v + 3], q.w, d);
+          for (int j = 0; j < J; ++j) {
+            const int c = c0 + j * 32 + lane;
+            if (c < NCH) {
+              float fw[V];
+              F::unpack(wrow[c], fw);
+              const float4* hp = reinterpret_cast<const float4*>(hsrc + (size_t)pid * I + (size_t)c * V);
+              float dj = 0.f;
+#pragma unroll
+              for (int v = 0; v < V; v += 4) {
+                const float4 q = hp[v / 4];
+                dj = fmaf(fw[v], q.x, dj);
+                dj = fmaf(fw[v + 1], q.y, dj);
+                dj = fmaf(fw[v + 2], q.z, dj);
+                dj = fmaf(fw[v + 3], q.w, dj);
+              }
+              if (WT == MOE_FP8E4M3_B128) dj *= __ldg(sd + (size_t)((r0 + r) >> 7) * IB + ((c * V) >> 7));
+              d += dj;
+            }
           }
-          if (WT == MOE_FP8E4M3_B128) d *= __ldg(sd + (size_t)(row >> 7) * IB + ((c * V) >> 7));
           acc += d;
         }
         acc = warp_sum(acc);
         if (lane == 0) {
           ys[(size_t)r * NP + pid] = acc;
-          a.b.y[(size_t)pid * H + row] = acc;
+          a.b.y[(size_t)pid * H + r0 + r] = acc;
         }
       }
     }
-    __syncthreads();
-    if (threadIdx.x == 0 && g + geo.NB < ng) {
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      issue(g + geo.NB);
-    }
   }
-  if (!ok && threadIdx.x == 0) {  // flag the timeout and let our own copies land before the CTA exits
-    atomicOr_system(err, kErrTimeout);
-    for (int s2 = 0; s2 < geo.NB && s2 < 4; ++s2) {
-      if (last_issued[s2] < 0) continue;
-      const uint32_t par = (uint32_t)((last_issued[s2] / geo.NB) & 1);
-      const unsigned long long t0 = gtime();
-      while (!bar_test(&bars[s2], par) && gtime() - t0 < kBulkWaitNs) {
+  int k = 0;
+  for (int g = g0 + warp; kRing && g < g1; g += geo.NW, ++k) {
+    const int st = k % geo.NS;
+    if (k == 0 && h_copy && !__all_sync(0xffffffffu, bar_wait(hbar, 0))) { ok = false; break; }
+    if (!__all_sync(0xffffffffu, bar_wait(&bars[st], (uint32_t)((k / geo.NS) & 1)))) { ok = false; break; }
+    const uint8_t* blk = ring + (size_t)st * geo.SB;
+    const float* sd = reinterpret_cast<const float*>(sp.w[g] + sd_off);
+    const int pb = sp.off[g], pe = sp.off[g + 1];
+    for (int tp = pb; tp < pe; ++tp) {
+      const int pid = sp.pid[tp];
+      float acc[kDownRows];
+#pragma unroll
+      for (int r = 0; r < kDownRows; ++r) acc[r] = 0.f;
+      for (int c0 = 0; c0 < NCH; c0 += 32 * J) {
+        float hv[J][V];
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+          const int c = c0 + j * 32 + lane;
+          if (c < NCH) {
+            const float4* hp = reinterpret_cast<const float4*>(hsrc + (size_t)pid * I + (size_t)c * V);
+#pragma unroll
+            for (int v = 0; v < V; v += 4) {
+              const float4 q = hp[v / 4];
+              hv[j][v] = q.x; hv[j][v + 1] = q.y; hv[j][v + 2] = q.z; hv[j][v + 3] = q.w;
+            }
+          } else {
+#pragma unroll
+            for (int v = 0; v < V; ++v) hv[j][v] = 0.f;
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < kDownRows; ++r) {
+          if (r < nr) {
+            const uint4* wrow = reinterpret_cast<const uint4*>(blk + (size_t)r * row_bytes);
+            float d = 0.f;
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+              const int c = c0 + j * 32 + lane;
+              if (c < NCH) {
+                float fw[V];
+                F::unpack(wrow[c], fw);
+                float dj = 0.f;
+#pragma unroll
+                for (int v = 0; v < V; ++v) dj = fmaf(fw[v], hv[j][v], dj);
+                if (WT == MOE_FP8E4M3_B128) dj *= __ldg(sd + (size_t)((r0 + r) >> 7) * IB + ((c * V) >> 7));
+                d += dj;
+              }
+            }
+            acc[r] += d;
+          }
+        }
+      }
+      const float v = reduce16(acc, lane);
+      const int r = lane >> 1;
+      if ((lane & 1) == 0 && r < nr) {
+        ys[(size_t)r * NP + pid] = v;
+        a.b.y[(size_t)pid * H + r0 + r] = v;   // per-pair output stays readable (moe_cache_get_plan)
       }
     }
+    __syncwarp();
+    if (lane == 0 && g + geo.NS * geo.NW < g1) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(g + geo.NS * geo.NW, st);
+    }
   }
-  if (!ok) return;
+  if (!ok && lane == 0) {   // flag the timeout; this warp's copies land before the CTA exits
+    atomicOr_system(err, kErrTimeout);
+    if (kRing)
+      for (int s2 = 0; s2 < geo.NS; ++s2) {
+        if (last_issued[s2] < 0) continue;
+        const int kk = (last_issued[s2] - g0 - warp) / geo.NW;
+        const uint32_t par = (uint32_t)((kk / geo.NS) & 1);
+        const unsigned long long t0 = gtime();
+        while (!bar_test(&bars[s2], par) && gtime() - t0 < kBulkWaitNs) {
+        }
+      }
+  }
+  if (h_copy && threadIdx.x == 0) {   // the h copy has landed before the CTA may exit
+    const unsigned long long t0 = gtime();
+    while (!bar_test(hbar, 0) && gtime() - t0 < kBulkWaitNs) {
+    }
+  }
+  const bool all_ok = __syncthreads_and(ok);
+  const bool split = a.pass != 2;
+  if (split) {
+    // Publish y and count this grid's arrival: the barrier orders every thread's y
+    // stores before thread 0's gpu-scope acquire-release increment; the grid that
+    // sees an odd count arrives second and combines.  It takes the other grid's
+    // pairs from global memory (gathered in one parallel round trip into ys).
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      uint32_t old;
+      asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(a.b.arrive + blockIdx.x) : "memory");
+      s_second = old & 1u;
+    }
+    __syncthreads();
+    if (!s_second) return;
+    for (int idx = threadIdx.x; idx < nr * NP; idx += blockDim.x) {
+      const int r = idx / NP, p = idx % NP;
+      const bool gpu = p >= a.P || s_slot[p] >= 0;
+      if (gpu && !s_mine[p]) ys[(size_t)r * NP + p] = __ldcg(a.b.y + (size_t)p * H + r0 + r);
+    }
+    __syncthreads();
+  } else if (!all_ok) {
+    return;
+  }
   bool missing = false;
   for (int idx = threadIdx.x; idx < nr * a.T; idx += blockDim.x) {
     const int r = idx / a.T, t = idx % a.T;
@@ -1063,7 +1270,7 @@ cudaError_t carveout_typed() {
     if (e != cudaSuccess) return e;
   }
   for (const void* k : {(const void*)gate_up_bulk_kernel<WT, AT>}) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kBulkSmemAttr);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, kDecodeCarveout);
     if (e != cudaSuccess) return e;
   }
@@ -1079,9 +1286,11 @@ cudaError_t carveout_typed() {
 cudaError_t setup_gemv_kernels() {
   const int smem = (int)(kDCHSmem + (size_t)kDCWarps * kDCMaxPairs * sizeof(float) +
                          staged_plan_bytes(4096 + 1, kDCMaxPairs) + (size_t)kDCMaxPairs * 8);
-  for (const void* k : {(const void*)down_bulk_kernel<MOE_F32>, (const void*)down_bulk_kernel<MOE_BF16>,
-                        (const void*)down_bulk_kernel<MOE_FP8E4M3_B128>}) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  for (const void* k : {(const void*)down_bulk_kernel<MOE_F32, true>, (const void*)down_bulk_kernel<MOE_BF16, true>,
+                        (const void*)down_bulk_kernel<MOE_FP8E4M3_B128, true>,
+                        (const void*)down_bulk_kernel<MOE_F32, false>, (const void*)down_bulk_kernel<MOE_BF16, false>,
+                        (const void*)down_bulk_kernel<MOE_FP8E4M3_B128, false>}) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kBulkSmemAttr);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, kDecodeCarveout);
     if (e != cudaSuccess) return e;
   }
@@ -1133,49 +1342,75 @@ cudaError_t launch_fill_gate_up(const Shape& sh, int T, const void* x, DecodeBuf
 int wbytes(int wdtype) { return wdtype == MOE_F32 ? 4 : wdtype == MOE_BF16 ? 2 : 1; }
 size_t up128(size_t x) { return (x + 127) & ~size_t(127); }
 
-// Row blocks, ring slots and shared-memory layout of the bulk-streamed kernels;
-// NB < 2 means the shape does not fit and the register-staged kernel runs.
+// Ring geometry and shared-memory layout of the bulk-streamed kernels; NS = 0
+// (gate/up: NS < 2) means the shape does not fit and the register-staged
+// kernel runs instead.
+constexpr size_t kRingBudget = 220 * 1024;
+
+// Gate/up: one CTA per SM, up to 8 warps with 2 stages of one row pair each (about
+// 130 KB, so the filled-expert down grid fits beside it).
 BulkGeom gate_up_geom(const GemvArgs& a, int wdtype, int adtype, int sms) {
   BulkGeom g{};
+  g.grid = sms;
   const size_t row = (size_t)a.H * wbytes(wdtype);
   const size_t xbytes = (size_t)a.T * a.H * (adtype == MOE_F32 ? 4 : 2);
-  int R = (a.I + sms - 1) / sms;
-  R = (int)std::min<size_t>((size_t)R, kBulkBlockCap / (2 * row));
-  g.R = R < 1 ? 1 : R;
-  g.BB = up128(2 * (size_t)g.R * row);
-  const size_t fixed = 128 + up128(staged_plan_bytes(a.max_g, a.max_p)) + up128(xbytes);
-  g.NB = (g.BB <= kBulkSmemBudget && fixed < kBulkSmemBudget)
-             ? (int)std::min<size_t>(4, (kBulkSmemBudget - fixed) / g.BB) : 0;
-  if (xbytes > kXSmem || 2 * row * (size_t)g.R > kBulkBlockCap * 2) g.NB = 0;
-  g.ring_off = 128;
-  g.plan_off = g.ring_off + (size_t)g.NB * g.BB;
-  g.extra_off = g.plan_off + up128(staged_plan_bytes(a.max_g, a.max_p));
+  const size_t plan = up128(staged_plan_bytes(a.max_g, a.max_p));
+  g.SB = up128(2 * row);
+  const size_t fixed = 256 + plan + up128(xbytes);
+  if (xbytes > kXSmem || fixed >= kRingBudget) return g;
+  const size_t room = kRingBudget - fixed;
+  for (g.NW = 8; g.NW >= 2; --g.NW) {
+    g.NS = (int)std::min<size_t>(2, room / ((size_t)g.NW * g.SB));
+    if (g.NS >= 2) break;
+  }
+  if (g.NS < 2) { g.NS = 0; return g; }
+  g.ring_off = 256;
+  g.plan_off = g.ring_off + (size_t)g.NW * g.NS * g.SB;
+  g.extra_off = g.plan_off + plan;
   g.smem = g.extra_off + up128(xbytes);
   return g;
 }
 
+// Down: min(ceil(H / sms), 16) output rows per CTA, with one stage for each of 8
+// warps when there are at most 8 GPU experts, else two-stage rings of at least
+// four warps; fewer rows per CTA when that does not fit.
 BulkGeom down_geom(const GemvArgs& a, int wdtype, int sms) {
   BulkGeom g{};
   const size_t row = (size_t)a.I * wbytes(wdtype);
   const size_t np = (size_t)(a.P + a.T * a.n_shared);
-  int R = (a.H + sms - 1) / sms;
-  R = (int)std::min<size_t>((size_t)R, kBulkBlockCap / row);
-  g.R = R < 1 ? 1 : R;
-  g.BB = up128((size_t)g.R * row);
-  const size_t extra = (((size_t)a.P * 8 + 15) & ~size_t(15)) + np * a.I * 4 + (size_t)g.R * np * 4;
-  const size_t fixed = 128 + up128(staged_plan_bytes(a.max_g, a.max_p)) + up128(extra);
-  g.NB = fixed < kBulkSmemBudget ? (int)std::min<size_t>(4, (kBulkSmemBudget - fixed) / g.BB) : 0;
-  g.ring_off = 128;
-  g.plan_off = g.ring_off + (size_t)g.NB * g.BB;
-  g.extra_off = g.plan_off + up128(staged_plan_bytes(a.max_g, a.max_p));
-  g.smem = g.extra_off + up128(extra);
+  const size_t hbytes = np * a.I * 4;
+  const size_t plan = up128(staged_plan_bytes(a.max_g, a.max_p));
+  g.h_smem = hbytes <= 64 * 1024 ? 1 : 0;
+  for (int R = std::min((a.H + sms - 1) / sms, kDownRows); R >= 1; --R) {
+    g.SB = up128((size_t)R * row);
+    const size_t extra = up128((size_t)a.P * 8) + up128((size_t)R * np * 4 + np) + (g.h_smem ? hbytes : 0);
+    const size_t fixed = 256 + plan + up128(extra);
+    if (fixed >= kRingBudget) continue;
+    const size_t room = kRingBudget - fixed;
+    if (a.max_g <= 8 && 8 * g.SB <= room) {
+      g.NS = 1;
+      g.NW = 8;
+    } else {
+      g.NS = 2;
+      g.NW = (int)std::min<size_t>(8, room / (2 * g.SB));
+    }
+    if (g.NW >= 4) {
+      g.R = R;
+      g.grid = (a.H + R - 1) / R;
+      g.ring_off = 256;
+      g.plan_off = g.ring_off + (size_t)g.NW * g.NS * g.SB;
+      g.extra_off = g.plan_off + plan;
+      g.smem = g.extra_off + up128(extra);
+      return g;
+    }
+  }
+  g.NS = 0;
   return g;
 }
 
 template <int WT, int AT>
 cudaError_t launch_gate_up_bulk(const GemvArgs& a, const BulkGeom& geo, uint32_t* err, cudaStream_t s) {
-  gate_up_bulk_kernel<WT, AT><<<(a.I + geo.R - 1) / geo.R, 256, geo.smem, s>>>(a, geo, err);
-  return cudaGetLastError();
+  return launch_pdl(gate_up_bulk_kernel<WT, AT>, dim3(geo.grid), dim3(geo.NW * 32), geo.smem, s, a, geo, err);
 }
 
 cudaError_t launch_gate_up(const Shape& sh, int pass, int T, const void* x, DecodeBufs b, int sms, cudaStream_t s,
@@ -1183,7 +1418,7 @@ cudaError_t launch_gate_up(const Shape& sh, int pass, int T, const void* x, Deco
   const GemvArgs a = make_args(sh, pass, T, x, b);
   if (pass == 0 && err != nullptr) {
     const BulkGeom geo = gate_up_geom(a, sh.wdtype, sh.adtype, sms);
-    if (geo.NB >= 2) {
+    if (geo.NS >= 2) {
       switch (sh.wdtype * 2 + sh.adtype) {
         case MOE_F32 * 2 + MOE_F32: return launch_gate_up_bulk<MOE_F32, MOE_F32>(a, geo, err, s);
         case MOE_F32 * 2 + MOE_BF16: return launch_gate_up_bulk<MOE_F32, MOE_BF16>(a, geo, err, s);
@@ -1211,10 +1446,55 @@ bool down_combine_fits(const Shape& sh, int T) {
 }
 
 template <int WT>
-cudaError_t launch_down_bulk(const GemvArgs& a, const BulkGeom& geo, const float* w, const float* cpu, float* out,
-                             uint32_t* err, cudaStream_t s) {
-  return launch_pdl(down_bulk_kernel<WT>, dim3((a.H + geo.R - 1) / geo.R), dim3(256), geo.smem, s, a, geo, w, cpu,
-                    out, err);
+cudaError_t launch_down_bulk(const GemvArgs& a, const BulkGeom& geo, bool ring, bool pdl, const float* w,
+                             const float* cpu, float* out, uint32_t* err, cudaStream_t s) {
+  if (!ring) {   // same rows per CTA, no ring and h read through L1: a few KB of shared memory
+    BulkGeom d = geo;
+    d.NS = 0;
+    d.NW = 8;
+    const size_t shift = geo.plan_off - geo.ring_off;
+    d.plan_off -= shift;
+    d.extra_off -= shift;
+    d.smem -= shift;
+    if (d.h_smem) {
+      d.smem -= (size_t)(a.P + a.T * a.n_shared) * a.I * 4;
+      d.h_smem = 0;
+    }
+    if (pdl)
+      return launch_pdl(down_bulk_kernel<WT, false>, dim3(d.grid), dim3(d.NW * 32), d.smem, s, a, d, w, cpu, out,
+                        err);
+    down_bulk_kernel<WT, false><<<d.grid, d.NW * 32, d.smem, s>>>(a, d, w, cpu, out, err);
+    return cudaGetLastError();
+  }
+  if (pdl)
+    return launch_pdl(down_bulk_kernel<WT, true>, dim3(geo.grid), dim3(geo.NW * 32), geo.smem, s, a, geo, w, cpu,
+                      out, err);
+  down_bulk_kernel<WT, true><<<geo.grid, geo.NW * 32, geo.smem, s>>>(a, geo, w, cpu, out, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_down_bulk_any(const Shape& sh, const GemvArgs& a, const BulkGeom& geo, bool ring, bool pdl,
+                                 const float* w, const float* cpu, float* out, uint32_t* err, cudaStream_t s) {
+  if (sh.wdtype == MOE_F32) return launch_down_bulk<MOE_F32>(a, geo, ring, pdl, w, cpu, out, err, s);
+  if (sh.wdtype == MOE_BF16) return launch_down_bulk<MOE_BF16>(a, geo, ring, pdl, w, cpu, out, err, s);
+  return launch_down_bulk<MOE_FP8E4M3_B128>(a, geo, ring, pdl, w, cpu, out, err, s);
+}
+
+// The bulk down kernel runs when its ring fits and every pair's h fits in
+// shared memory; the split into resident / filled grids rides on it.
+bool down_split_ok(const Shape& sh, int T, int sms) {
+  const GemvArgs a = make_args(sh, 2, T, nullptr, DecodeBufs{});
+  const BulkGeom geo = down_geom(a, sh.wdtype, sms);
+  return geo.NS >= 1 && geo.h_smem;
+}
+
+cudaError_t launch_down_split(const Shape& sh, int pass, int T, const float* w, const float* cpu_part, DecodeBufs b,
+                              float* out, uint32_t* err, int sms, cudaStream_t s) {
+  if (pass != 0 && pass != 1) return cudaErrorInvalidValue;
+  const GemvArgs a = make_args(sh, pass, T, nullptr, b);
+  const BulkGeom geo = down_geom(a, sh.wdtype, sms);
+  // pass 0 follows its gate/up grid, pass 1 the fill, both as programmatic dependencies
+  return launch_down_bulk_any(sh, a, geo, pass == 0, true, w, cpu_part, out, err, s);
 }
 
 cudaError_t launch_down_combine(const Shape& sh, int T, const float* w, const float* cpu_part, DecodeBufs b,
@@ -1222,11 +1502,7 @@ cudaError_t launch_down_combine(const Shape& sh, int T, const float* w, const fl
   {
     const GemvArgs a = make_args(sh, 2, T, nullptr, b);
     const BulkGeom geo = down_geom(a, sh.wdtype, sms);
-    if (geo.NB >= 2) {
-      if (sh.wdtype == MOE_F32) return launch_down_bulk<MOE_F32>(a, geo, w, cpu_part, out, err, s);
-      if (sh.wdtype == MOE_BF16) return launch_down_bulk<MOE_BF16>(a, geo, w, cpu_part, out, err, s);
-      return launch_down_bulk<MOE_FP8E4M3_B128>(a, geo, w, cpu_part, out, err, s);
-    }
+    if (geo.NS >= 1 && geo.h_smem) return launch_down_bulk_any(sh, a, geo, true, true, w, cpu_part, out, err, s);
   }
   if (down_combine_fits(sh, T)) {
     const GemvArgs a = make_args(sh, 2, T, nullptr, b);

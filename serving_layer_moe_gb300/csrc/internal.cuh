@@ -43,7 +43,7 @@ enum PlanIdx : int {
 
 // kernel groups timed by moe_cache_profile
 enum ProfKind : int {
-  PROF_CONTROL = 0, PROF_FILL = 1, PROF_GATE_UP_RESIDENT = 2, PROF_GATE_UP_FILLED = 3, PROF_DOWN_COMBINE = 4,
+  PROF_CONTROL = 0, PROF_FILL = 1, PROF_GATE_UP_RESIDENT = 2, PROF_DOWN_FILLED = 3, PROF_DOWN_COMBINE = 4,
   PROF_PREFILL_CONTROL = 5, PROF_PREFILL_LOAD = 6, PROF_PREFILL_GEMM = 7, PROF_KINDS = 8,
 };
 
@@ -59,6 +59,7 @@ struct DecodeBufs {
   const uint8_t** gpu_w;  // [max_gpu]      weight blob of each GPU expert
   float* h;               // [max_pairs, I] SwiGLU activations
   float* y;               // [max_pairs, H] expert outputs (unweighted)
+  uint32_t* arrive;       // [H] arrivals of the two split down kernels per row block (parity = who combines)
 };
 
 struct CacheTables {
@@ -104,6 +105,12 @@ cudaError_t launch_gate_up(const Shape& sh, int pass, int T, const void* x, Deco
 cudaError_t launch_down_combine(const Shape& sh, int T, const float* w, const float* cpu_part, DecodeBufs b,
                                 float* out, uint32_t* err, int sms, cudaStream_t s);
 bool down_combine_fits(const Shape& sh, int T);
+// Split down projection: pass 0 = resident experts (main stream, after their
+// gate/up), pass 1 = filled experts (fill stream, after the fill); the second
+// of the two CTAs of each row block to finish forms that block's combine.
+bool down_split_ok(const Shape& sh, int T, int sms);
+cudaError_t launch_down_split(const Shape& sh, int pass, int T, const float* w, const float* cpu_part, DecodeBufs b,
+                              float* out, uint32_t* err, int sms, cudaStream_t s);
 cudaError_t launch_combine(const Shape& sh, int T, const float* w, const float* cpu_part,
                            DecodeBufs b, float* out, uint32_t* err, cudaStream_t s);
 int gemv_block_threads();
