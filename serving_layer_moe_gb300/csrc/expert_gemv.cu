@@ -22,6 +22,8 @@
 // over the host link (NVLink-C2C on a Grace host), because the fill list is
 // decided on the device and a copy-engine memcpy would need host-known
 // addresses.
+#include <vector>
+
 #include "internal.cuh"
 
 #include <cuda_fp8.h>
@@ -130,6 +132,16 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
+
+// acc + w.lo * x.lo, then + w.hi * x.hi, on bf16 pairs with an f32 accumulator:
+// the products of two bf16 values are exact in f32, so each step rounds once,
+// exactly like fmaf on the widened operands.
+__device__ __forceinline__ float fma_bf16x2(uint32_t w, uint32_t x, float acc) {
+  asm("{\n .reg .b16 wl, wh, xl, xh;\n mov.b32 {wl, wh}, %1;\n mov.b32 {xl, xh}, %2;\n"
+      " fma.rn.f32.bf16 %0, wl, xl, %0;\n fma.rn.f32.bf16 %0, wh, xh, %0;\n}"
+      : "+f"(acc) : "r"(w), "r"(x));
+  return acc;
+}
 
 struct GemvArgs {
   int H, I, k, T, P;             // P = T * k (pair ids >= P are shared-expert rows)
@@ -747,7 +759,7 @@ struct BulkGeom {
 // pair: gate row i and up row I + i, 2 H weight elements; warp w of the grid
 // takes items w, w + warps, ...  x is staged per CTA in shared memory while
 // the first items are in flight.
-template <int WT, int AT>
+template <int WT, int AT, int kJX>
 __global__ void __launch_bounds__(256) gate_up_bulk_kernel(GemvArgs a, BulkGeom geo, uint32_t* err) {
   using F = WFmt<WT>;
   constexpr int V = F::V;
@@ -810,6 +822,13 @@ __global__ void __launch_bounds__(256) gate_up_bulk_kernel(GemvArgs a, BulkGeom 
   __syncthreads();
   const int NCH = H / V;
   const int HB = H / 128;
+  // kJX > 0: one bf16 token, bf16 weights, NCH = 32 kJX: a lane's x chunks stay in
+  // registers and each weight pair feeds one mixed-precision FMA
+  uint4 xr[kJX > 0 ? kJX : 1];
+  if (kJX > 0) {
+#pragma unroll
+    for (int j = 0; j < kJX; ++j) xr[j] = reinterpret_cast<const uint4*>(xsm)[j * 32 + lane];
+  }
   bool ok = true;
   int k = 0;
   for (long it = w0; it < items; it += nwarps, ++k) {
@@ -820,7 +839,25 @@ __global__ void __launch_bounds__(256) gate_up_bulk_kernel(GemvArgs a, BulkGeom 
     const uint4* up = reinterpret_cast<const uint4*>(ring + (size_t)st * geo.SB + row_bytes);
     const float* sgu = reinterpret_cast<const float*>(sp.w[g] + 3ull * (size_t)I * row_bytes);
     const int pb = sp.off[g], pe = sp.off[g + 1];
-    for (int tp = pb; tp < pe; ++tp) {
+    if (kJX > 0) {   // same per-chunk partials and order as the generic loop below
+      float ag = 0.f, au = 0.f;
+#pragma unroll
+      for (int j = 0; j < kJX; ++j) {
+        const uint4 wg = gate[j * 32 + lane], wu = up[j * 32 + lane];
+        float pg = 0.f, pu = 0.f;
+        pg = fma_bf16x2(wg.x, xr[j].x, pg); pu = fma_bf16x2(wu.x, xr[j].x, pu);
+        pg = fma_bf16x2(wg.y, xr[j].y, pg); pu = fma_bf16x2(wu.y, xr[j].y, pu);
+        pg = fma_bf16x2(wg.z, xr[j].z, pg); pu = fma_bf16x2(wu.z, xr[j].z, pu);
+        pg = fma_bf16x2(wg.w, xr[j].w, pg); pu = fma_bf16x2(wu.w, xr[j].w, pu);
+        ag += pg;
+        au += pu;
+      }
+      ag = warp_sum(ag);
+      au = warp_sum(au);
+      if (lane == 0)
+        for (int tp = pb; tp < pe; ++tp) a.b.h[(size_t)sp.pid[tp] * I + i] = silu(ag) * au;
+    }
+    for (int tp = pb; kJX == 0 && tp < pe; ++tp) {
       const int t = sp.tok[tp];
       float ag = 0.f, au = 0.f;
       for (int c = lane; c < NCH; c += 32) {
@@ -880,8 +917,8 @@ __global__ void __launch_bounds__(256) gate_up_bulk_kernel(GemvArgs a, BulkGeom 
 // and 1 are two grids over the same row blocks: each publishes its y, counts
 // itself in arrive[block], and the second of the two (odd count before its
 // increment) forms the block's combine from y in global memory.
-template <int WT, bool kRing>
-__global__ void __launch_bounds__(256) down_bulk_kernel(GemvArgs a, BulkGeom geo, const float* __restrict__ w,
+template <int WT, bool kRing, int kJN>
+__global__ void __launch_bounds__(kRing ? 256 : 512) down_bulk_kernel(GemvArgs a, BulkGeom geo, const float* __restrict__ w,
                                                         const float* __restrict__ cpu, float* __restrict__ out,
                                                         uint32_t* err) {
   using F = WFmt<WT>;
@@ -889,6 +926,16 @@ __global__ void __launch_bounds__(256) down_bulk_kernel(GemvArgs a, BulkGeom geo
   constexpr int J = 32 / V;   // 16-byte chunks per lane per column segment (32 h values in registers)
   extern __shared__ __align__(128) uint8_t sm[];
   __shared__ uint32_t s_second;
+  // Split passes: when one of the two expert sets is empty the other grid combines
+  // alone (no arrival is counted) and the empty grid leaves at once; with both
+  // empty (every pair on the CPU) the resident grid combines.
+  const bool split = a.pass != 2;
+  bool alone = !split;
+  if (split) {
+    const int nfirst = a.b.plan[P_NFIRST], ngpu = a.b.plan[P_NGPU];
+    if (a.pass == 1 ? ngpu == nfirst : (nfirst == 0 && ngpu > 0)) return;
+    alone = a.pass == 0 ? ngpu == nfirst : nfirst == 0;
+  }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm) + warp * geo.NS;
   uint64_t* hbar = reinterpret_cast<uint64_t*>(sm) + 31;   // ring barriers use at most 8 x 2
@@ -1008,7 +1055,39 @@ __global__ void __launch_bounds__(256) down_bulk_kernel(GemvArgs a, BulkGeom geo
       float acc[kDownRows];
 #pragma unroll
       for (int r = 0; r < kDownRows; ++r) acc[r] = 0.f;
-      for (int c0 = 0; c0 < NCH; c0 += 32 * J) {
+      if (kJN > 0) {
+        // NCH = 32 kJN: one column segment, no guards; rows past nr repeat the
+        // last row (their sums are never stored), so the whole block is one
+        // straight run of independent chains
+        float hv[kJN > 0 ? kJN : 1][V];
+#pragma unroll
+        for (int j = 0; j < kJN; ++j) {
+          const float4* hp = reinterpret_cast<const float4*>(hsrc + (size_t)pid * I + (size_t)(j * 32 + lane) * V);
+#pragma unroll
+          for (int v = 0; v < V; v += 4) {
+            const float4 q = hp[v / 4];
+            hv[j][v] = q.x; hv[j][v + 1] = q.y; hv[j][v + 2] = q.z; hv[j][v + 3] = q.w;
+          }
+        }
+#pragma unroll
+        for (int r = 0; r < kDownRows; ++r) {
+          const int rr = r < nr ? r : nr - 1;
+          const uint4* wrow = reinterpret_cast<const uint4*>(blk + (size_t)rr * row_bytes);
+          float d = 0.f;
+#pragma unroll
+          for (int j = 0; j < kJN; ++j) {
+            float fw[V];
+            F::unpack(wrow[j * 32 + lane], fw);
+            float dj = 0.f;
+#pragma unroll
+            for (int v = 0; v < V; ++v) dj = fmaf(fw[v], hv[j][v], dj);
+            if (WT == MOE_FP8E4M3_B128) dj *= __ldg(sd + (size_t)((r0 + rr) >> 7) * IB + (((j * 32 + lane) * V) >> 7));
+            d += dj;
+          }
+          acc[r] += d;
+        }
+      }
+      for (int c0 = 0; kJN == 0 && c0 < NCH; c0 += 32 * J) {
         float hv[J][V];
 #pragma unroll
         for (int j = 0; j < J; ++j) {
@@ -1078,8 +1157,7 @@ __global__ void __launch_bounds__(256) down_bulk_kernel(GemvArgs a, BulkGeom geo
     }
   }
   const bool all_ok = __syncthreads_and(ok);
-  const bool split = a.pass != 2;
-  if (split) {
+  if (!alone) {
     // Publish y and count this grid's arrival: the barrier orders every thread's y
     // stores before thread 0's gpu-scope acquire-release increment; the grid that
     // sees an odd count arrives second and combines.  It takes the other grid's
@@ -1101,6 +1179,7 @@ __global__ void __launch_bounds__(256) down_bulk_kernel(GemvArgs a, BulkGeom geo
   } else if (!all_ok) {
     return;
   }
+  // (alone: every GPU pair of the call is this grid's own, in ys)
   bool missing = false;
   for (int idx = threadIdx.x; idx < nr * a.T; idx += blockDim.x) {
     const int r = idx / a.T, t = idx % a.T;
@@ -1269,7 +1348,12 @@ cudaError_t carveout_typed() {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, kDecodeCarveout);
     if (e != cudaSuccess) return e;
   }
-  for (const void* k : {(const void*)gate_up_bulk_kernel<WT, AT>}) {
+  std::vector<const void*> bulk = {(const void*)gate_up_bulk_kernel<WT, AT, 0>};
+  if constexpr (WT == MOE_BF16 && AT == MOE_BF16) {
+    bulk.push_back((const void*)gate_up_bulk_kernel<WT, AT, 4>);
+    bulk.push_back((const void*)gate_up_bulk_kernel<WT, AT, 8>);
+  }
+  for (const void* k : bulk) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kBulkSmemAttr);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, kDecodeCarveout);
     if (e != cudaSuccess) return e;
@@ -1286,10 +1370,11 @@ cudaError_t carveout_typed() {
 cudaError_t setup_gemv_kernels() {
   const int smem = (int)(kDCHSmem + (size_t)kDCWarps * kDCMaxPairs * sizeof(float) +
                          staged_plan_bytes(4096 + 1, kDCMaxPairs) + (size_t)kDCMaxPairs * 8);
-  for (const void* k : {(const void*)down_bulk_kernel<MOE_F32, true>, (const void*)down_bulk_kernel<MOE_BF16, true>,
-                        (const void*)down_bulk_kernel<MOE_FP8E4M3_B128, true>,
-                        (const void*)down_bulk_kernel<MOE_F32, false>, (const void*)down_bulk_kernel<MOE_BF16, false>,
-                        (const void*)down_bulk_kernel<MOE_FP8E4M3_B128, false>}) {
+  for (const void* k : {(const void*)down_bulk_kernel<MOE_F32, true, 0>, (const void*)down_bulk_kernel<MOE_BF16, true, 0>,
+                        (const void*)down_bulk_kernel<MOE_BF16, true, 3>, (const void*)down_bulk_kernel<MOE_BF16, true, 4>,
+                        (const void*)down_bulk_kernel<MOE_FP8E4M3_B128, true, 0>,
+                        (const void*)down_bulk_kernel<MOE_F32, false, 0>, (const void*)down_bulk_kernel<MOE_BF16, false, 0>,
+                        (const void*)down_bulk_kernel<MOE_FP8E4M3_B128, false, 0>}) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kBulkSmemAttr);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, kDecodeCarveout);
     if (e != cudaSuccess) return e;
@@ -1410,7 +1495,15 @@ BulkGeom down_geom(const GemvArgs& a, int wdtype, int sms) {
 
 template <int WT, int AT>
 cudaError_t launch_gate_up_bulk(const GemvArgs& a, const BulkGeom& geo, uint32_t* err, cudaStream_t s) {
-  return launch_pdl(gate_up_bulk_kernel<WT, AT>, dim3(geo.grid), dim3(geo.NW * 32), geo.smem, s, a, geo, err);
+  // one bf16 token over bf16 rows of 4 or 8 16-byte chunks per lane: the register-x path
+  if constexpr (WT == MOE_BF16 && AT == MOE_BF16) {
+    const int jx = (a.T == 1 && (a.H / 8) % 32 == 0) ? a.H / 8 / 32 : 0;
+    if (jx == 8)
+      return launch_pdl(gate_up_bulk_kernel<WT, AT, 8>, dim3(geo.grid), dim3(geo.NW * 32), geo.smem, s, a, geo, err);
+    if (jx == 4)
+      return launch_pdl(gate_up_bulk_kernel<WT, AT, 4>, dim3(geo.grid), dim3(geo.NW * 32), geo.smem, s, a, geo, err);
+  }
+  return launch_pdl(gate_up_bulk_kernel<WT, AT, 0>, dim3(geo.grid), dim3(geo.NW * 32), geo.smem, s, a, geo, err);
 }
 
 cudaError_t launch_gate_up(const Shape& sh, int pass, int T, const void* x, DecodeBufs b, int sms, cudaStream_t s,
@@ -1451,7 +1544,7 @@ cudaError_t launch_down_bulk(const GemvArgs& a, const BulkGeom& geo, bool ring, 
   if (!ring) {   // same rows per CTA, no ring and h read through L1: a few KB of shared memory
     BulkGeom d = geo;
     d.NS = 0;
-    d.NW = 8;
+    d.NW = 16;
     const size_t shift = geo.plan_off - geo.ring_off;
     d.plan_off -= shift;
     d.extra_off -= shift;
@@ -1461,16 +1554,22 @@ cudaError_t launch_down_bulk(const GemvArgs& a, const BulkGeom& geo, bool ring, 
       d.h_smem = 0;
     }
     if (pdl)
-      return launch_pdl(down_bulk_kernel<WT, false>, dim3(d.grid), dim3(d.NW * 32), d.smem, s, a, d, w, cpu, out,
+      return launch_pdl(down_bulk_kernel<WT, false, 0>, dim3(d.grid), dim3(d.NW * 32), d.smem, s, a, d, w, cpu, out,
                         err);
-    down_bulk_kernel<WT, false><<<d.grid, d.NW * 32, d.smem, s>>>(a, d, w, cpu, out, err);
+    down_bulk_kernel<WT, false, 0><<<d.grid, d.NW * 32, d.smem, s>>>(a, d, w, cpu, out, err);
     return cudaGetLastError();
   }
-  if (pdl)
-    return launch_pdl(down_bulk_kernel<WT, true>, dim3(geo.grid), dim3(geo.NW * 32), geo.smem, s, a, geo, w, cpu,
-                      out, err);
-  down_bulk_kernel<WT, true><<<geo.grid, geo.NW * 32, geo.smem, s>>>(a, geo, w, cpu, out, err);
-  return cudaGetLastError();
+  auto go = [&](auto kern) -> cudaError_t {
+    if (pdl) return launch_pdl(kern, dim3(geo.grid), dim3(geo.NW * 32), geo.smem, s, a, geo, w, cpu, out, err);
+    kern<<<geo.grid, geo.NW * 32, geo.smem, s>>>(a, geo, w, cpu, out, err);
+    return cudaGetLastError();
+  };
+  if constexpr (WT == MOE_BF16) {   // rows of 3 or 4 chunks per lane: the unguarded straight-line path
+    const int nch = a.I / 8;
+    if (nch == 96) return go(down_bulk_kernel<WT, true, 3>);
+    if (nch == 128) return go(down_bulk_kernel<WT, true, 4>);
+  }
+  return go(down_bulk_kernel<WT, true, 0>);
 }
 
 cudaError_t launch_down_bulk_any(const Shape& sh, const GemvArgs& a, const BulkGeom& geo, bool ring, bool pdl,
