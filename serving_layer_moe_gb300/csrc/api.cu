@@ -79,6 +79,7 @@ static void destroy_impl(moe_cache* c) {
   cudaFree(c->tab.stamp);
   cudaFree(c->tab.clock);
   cudaFree(c->tab.counters);
+  cudaFree(c->tab.pool);
   cudaFree(c->work);
   if (c->err_host) cudaFreeHost(c->err_host);
   if (c->registered_here) cudaHostUnregister(const_cast<uint8_t*>(c->host_pool));
@@ -198,6 +199,8 @@ extern "C" moe_status moe_cache_create(const moe_config* cfg, const void* host_p
   CKB(cudaMemset(c->tab.clock, 0, sizeof(uint64_t)));
   CKB(cudaMalloc(&c->tab.counters, 8 * sizeof(uint64_t)));
   CKB(cudaMemset(c->tab.counters, 0, 8 * sizeof(uint64_t)));
+  CKB(cudaMalloc(&c->tab.pool, (kPoolN + 1) * sizeof(uint64_t)));
+  CKB(cudaMemset(c->tab.pool, 0, (kPoolN + 1) * sizeof(uint64_t)));   // count 0: rebuilt at the first call
   if (k.n_shared) {
     CKB(cudaMalloc(&c->shared, (uint64_t)k.n_layers * S));
     CKB(cudaMemcpy(c->shared, shared_host, (uint64_t)k.n_layers * S, cudaMemcpyHostToDevice));
@@ -388,6 +391,8 @@ extern "C" moe_status moe_cache_resize(moe_cache* c, uint64_t n_slots) {
   e = launch_resize_plan((int)c->C, (int)n_slots, c->tab.s2e, c->tab.stamp, new_s2e, new_stamp, new2old, n_keep, s);
   if (e == cudaSuccess) e = launch_resize_copy(new2old, n_keep, (int)n_slots, c->slots, new_slots, S, s);
   if (e == cudaSuccess) e = launch_rebuild_e2s(c->sh.L * c->sh.E, (int)n_slots, new_s2e, c->tab.e2s, s);
+  // new slots enter empty (stamp 0, below every kept candidate): drop the decode candidate pool
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->tab.pool + kPoolN, 0, sizeof(uint64_t), s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) {
     cleanup();

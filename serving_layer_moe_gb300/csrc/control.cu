@@ -32,8 +32,10 @@
 // 32) come from one pass in which each warp extracts its own K smallest by
 // repeated warp-minimum (32-bit redux instructions over the high and low words
 // of register-resident keys) and warp 0 merges the sorted per-warp lists; for
-// larger K an MSB radix select with 8-bit digits over the shared keys.  Cost does not
-// depend on how many misses occurred.
+// larger K an MSB radix select with 8-bit digits over the shared keys.  For K <=
+// 16 the kernel keeps, between calls, the 64 smallest keys of its last full
+// selection: since keys only grow, the first valid entries of that pool are
+// the victims, and the full selection reruns only when the pool runs short.
 #include "internal.cuh"
 
 namespace moe {
@@ -78,11 +80,13 @@ __device__ __forceinline__ uint32_t q_star(uint32_t m, uint32_t bp, uint32_t bc)
 
 // shared scalars of the control CTA
 struct CtrlScalars {
-  int bad, u, h, m, q, keff, ncand, digit, kth, read_hits, read_misses;
+  int bad, u, h, m, q, keff, ncand, digit, kth, read_hits, read_misses, pool_n, enough;
   unsigned long long clock0;
 };
 
-template <bool kRadix>
+// kSel: 0 = K <= 32 by warp minima, 1 = radix select, 2 = K <= kPoolMaxK from the
+// kept candidate pool (rebuilt by radix select when it runs short)
+template <int kSel>
 __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ CtrlScalars sc;
@@ -109,7 +113,8 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
   int32_t* vict = gcnt + U + 2;                                                    // [K]
   uint32_t* hist = reinterpret_cast<uint32_t*>(vict + a.K);                        // [256]
   unsigned long long* cand = reinterpret_cast<unsigned long long*>(
-      (reinterpret_cast<uintptr_t>(hist + 256) + 7) & ~uintptr_t(7));               // [K]
+      (reinterpret_cast<uintptr_t>(hist + 256) + 7) & ~uintptr_t(7));               // [max(K, kPoolN)]
+  unsigned long long* s_pool = cand + (a.K > kPoolN ? a.K : kPoolN);               // [kPoolN]
 
   int32_t* s2e = a.tab.s2e;
   uint64_t* stamp = a.tab.stamp;
@@ -130,6 +135,10 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
       slotf[s] = s2e[s];
       rawkey[s] = ((unsigned long long)stamp[s] << kSlotBits) | (unsigned long long)s;
     }
+  }
+  if (kSel == 2) {
+    for (int i = tid; i < kPoolN; i += nt) s_pool[i] = a.tab.pool[i];
+    if (tid == 0) sc.pool_n = (int)a.tab.pool[kPoolN];
   }
   pdl_wait();       // the routed ids may come from the preceding kernel
   pdl_trigger();
@@ -219,7 +228,108 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
     }
     return a.cache_keys ? rawkey[s] : (((unsigned long long)stamp[s] << kSlotBits) | (unsigned long long)s);
   };
-  if (!kRadix && keff > 0) {
+  // The n_want smallest keys (keyfn; keys unique, n_want <= number of keys),
+  // emitted ascending as emit(rank, key): MSB radix select with 8-bit digits,
+  // then a rank sort of the candidates.
+  auto radix_smallest = [&](int n_want, auto keyfn, auto emit) {
+    const unsigned long long maxkey = (sc.clock0 << kSlotBits) | (kMaxSlots - 1);
+    const int top = 63 - __clzll((long long)maxkey);
+    unsigned long long prefix = 0ull, maskhi = 0ull;
+    int kth = n_want;  // 1-based rank still to find below the current prefix
+    for (int shift = (top / 8) * 8; shift >= 0; shift -= 8) {
+      for (int i = tid; i < 256; i += nt) hist[i] = 0u;
+      if (tid == 0) sc.ncand = 0;
+      __syncthreads();
+      for (int s = tid; s < C; s += nt) {
+        const unsigned long long key = keyfn(s);
+        if ((key & maskhi) == prefix) atomicAdd(&hist[(key >> shift) & 255ull], 1u);
+      }
+      __syncthreads();
+      if (tid < 32) {
+        int c = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) c += (int)hist[lane * 8 + j];
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        const int excl = incl - c;
+        if ((excl < kth) && (kth <= incl)) {
+          int run = excl, d = lane * 8;
+          for (int j = 0; j < 8; ++j) {
+            const int hj = (int)hist[lane * 8 + j];
+            if (run + hj >= kth) { d = lane * 8 + j; break; }
+            run += hj;
+          }
+          sc.digit = d;
+          sc.kth = kth - run;
+        }
+      }
+      __syncthreads();
+      prefix |= (unsigned long long)sc.digit << shift;
+      maskhi |= 255ull << shift;
+      kth = sc.kth;
+      __syncthreads();
+    }
+    // prefix is now the n_want-th smallest key; exactly n_want keys are <= it
+    for (int s = tid; s < C; s += nt) {
+      const unsigned long long key = keyfn(s);
+      if (key <= prefix) {
+        const int i = atomicAdd(&sc.ncand, 1);
+        if (i < n_want) cand[i] = key;
+      }
+    }
+    __syncthreads();
+    for (int i = tid; i < n_want; i += nt) {
+      const unsigned long long ki = cand[i];
+      int r = 0;
+      for (int j = 0; j < n_want; ++j) r += (cand[j] < ki);
+      emit(r, ki);
+    }
+    __syncthreads();
+  };
+  auto raw_key = [&](int s) -> unsigned long long {
+    return a.cache_keys ? rawkey[s] : (((unsigned long long)stamp[s] << kSlotBits) | (unsigned long long)s);
+  };
+  if (kSel == 2 && keff > 0) {
+    // Every slot outside the pool had a larger key than the pool's largest at the
+    // rebuild, and a slot's key only changes by a new stamp from the clock, which
+    // is larger still; so the valid entries (key unchanged) are exactly the slots
+    // below that bound and the keff smallest evictable keys are the first keff
+    // valid entries that are not this call's hits, whenever there are that many.
+    for (int attempt = 0; attempt < 2; ++attempt) {
+      if (warp == 0) {
+        const int pn = sc.pool_n;
+        int taken = 0;
+        for (int i0 = 0; i0 < pn; i0 += 32) {
+          const int i = i0 + lane;
+          const unsigned long long k = i < pn ? s_pool[i] : ~0ull;
+          const bool ok = i < pn && key_of((int)(k & (kMaxSlots - 1))) == k;
+          const uint32_t bal = __ballot_sync(0xffffffffu, ok);
+          const int r = taken + __popc(bal & lanemask_lt());
+          if (ok && r < keff) vict[r] = (int)(k & (kMaxSlots - 1));
+          taken += __popc(bal);
+        }
+        if (lane == 0) sc.enough = taken >= keff;
+      }
+      __syncthreads();
+      if (sc.enough || attempt == 1) break;
+      // rebuild: the kPoolN smallest keys over all slots (hits included); with
+      // C <= kPoolN every slot, so keff <= C - h entries are always evictable
+      const int n = C < kPoolN ? C : kPoolN;
+      radix_smallest(n, raw_key, [&](int r, unsigned long long key) {
+        s_pool[r] = key;
+        a.tab.pool[r] = key;
+      });
+      if (tid == 0) {
+        sc.pool_n = n;
+        a.tab.pool[kPoolN] = (uint64_t)n;
+      }
+      __syncthreads();
+    }
+  } else if (kSel == 0 && keff > 0) {
     // each warp: its keff smallest keys, ascending, by repeated warp-minimum; a
     // thread holds the effective keys of its slots in registers (C <= 8 * 512)
     // and a 64-bit warp minimum is two 32-bit reductions (high word, then the
@@ -269,62 +379,8 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
         if (lane == 0) vict[r] = (mn == ~0ull) ? -1 : (int)(mn & (kMaxSlots - 1));
       }
     }
-  } else if (kRadix && keff > 0) {
-    const unsigned long long maxkey = (sc.clock0 << kSlotBits) | (kMaxSlots - 1);
-    const int top = 63 - __clzll((long long)maxkey);
-    unsigned long long prefix = 0ull, maskhi = 0ull;
-    int kth = keff;  // 1-based rank still to find below the current prefix
-    for (int shift = (top / 8) * 8; shift >= 0; shift -= 8) {
-      for (int i = tid; i < 256; i += nt) hist[i] = 0u;
-      __syncthreads();
-      for (int s = tid; s < C; s += nt) {
-        const unsigned long long key = key_of(s);
-        if ((key & maskhi) == prefix) atomicAdd(&hist[(key >> shift) & 255ull], 1u);
-      }
-      __syncthreads();
-      if (tid < 32) {
-        int c = 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) c += (int)hist[lane * 8 + j];
-        int incl = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int v = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += v;
-        }
-        const int excl = incl - c;
-        if ((excl < kth) && (kth <= incl)) {
-          int run = excl, d = lane * 8;
-          for (int j = 0; j < 8; ++j) {
-            const int hj = (int)hist[lane * 8 + j];
-            if (run + hj >= kth) { d = lane * 8 + j; break; }
-            run += hj;
-          }
-          sc.digit = d;
-          sc.kth = kth - run;
-        }
-      }
-      __syncthreads();
-      prefix |= (unsigned long long)sc.digit << shift;
-      maskhi |= 255ull << shift;
-      kth = sc.kth;
-      __syncthreads();
-    }
-    // prefix is now the keff-th smallest key; keys are unique, so exactly keff are <= it
-    for (int s = tid; s < C; s += nt) {
-      const unsigned long long key = key_of(s);
-      if (key <= prefix) {
-        const int i = atomicAdd(&sc.ncand, 1);
-        if (i < keff) cand[i] = key;
-      }
-    }
-    __syncthreads();
-    for (int i = tid; i < keff; i += nt) {
-      const unsigned long long ki = cand[i];
-      int r = 0;
-      for (int j = 0; j < keff; ++j) r += (cand[j] < ki);
-      vict[r] = (int32_t)(ki & (kMaxSlots - 1));
-    }
+  } else if (kSel == 1 && keff > 0) {
+    radix_smallest(keff, key_of, [&](int r, unsigned long long key) { vict[r] = (int32_t)(key & (kMaxSlots - 1)); });
   }
   for (int i = keff + tid; i < a.K; i += nt) vict[i] = -1;
   __syncthreads();
@@ -464,16 +520,18 @@ cudaError_t launch_decode_control(const Shape& sh, int layer, int T, int C, int 
   a.umax = min(sh.E, T * sh.k);
   const int NW = (sh.E + 31) / 32;
   const size_t base = (size_t)sh.E * 4 + (size_t)T * sh.k * 4 + (size_t)(2 * NW + 1) * 4 +
-                      (size_t)(6 * a.umax + 2) * 4 + (size_t)K * 4 + 256 * 4 + 8 + (size_t)K * 8 + 16;
+                      (size_t)(6 * a.umax + 2) * 4 + (size_t)K * 4 + 256 * 4 + 8 +
+                      (size_t)(K > kPoolN ? K : kPoolN) * 8 + (size_t)kPoolN * 8 + 16;
   a.cache_keys = (C <= kSmemKeyCap && base + (size_t)C * 12 <= kCtrlSmemLimit) ? 1 : 0;
   const size_t smem = base + (a.cache_keys ? (size_t)C * 12 : 0);
   if (smem > kCtrlSmemLimit) return cudaErrorInvalidConfiguration;
-  if (K <= 32) return launch_pdl(decode_control_kernel<false>, dim3(1), dim3(kCtrlThreads), smem, s, a);
-  return launch_pdl(decode_control_kernel<true>, dim3(1), dim3(kCtrlThreads), smem, s, a);
+  if (K <= kPoolMaxK) return launch_pdl(decode_control_kernel<2>, dim3(1), dim3(kCtrlThreads), smem, s, a);
+  if (K <= 32) return launch_pdl(decode_control_kernel<0>, dim3(1), dim3(kCtrlThreads), smem, s, a);
+  return launch_pdl(decode_control_kernel<1>, dim3(1), dim3(kCtrlThreads), smem, s, a);
 }
 
 cudaError_t setup_control_kernels() {
-  for (auto k : {decode_control_kernel<false>, decode_control_kernel<true>}) {
+  for (auto k : {decode_control_kernel<0>, decode_control_kernel<1>, decode_control_kernel<2>}) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCtrlSmemLimit);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, kDecodeCarveout);
     if (e != cudaSuccess) return e;

@@ -68,7 +68,13 @@ struct CacheTables {
   uint64_t* stamp;        // [C]
   uint64_t* clock;        // [1]
   uint64_t* counters;     // [8]
+  uint64_t* pool;         // [kPoolN + 1]: oldest LRU keys at the last rebuild, ascending; [kPoolN] = count
 };
+
+// Decode victim candidates kept between calls (K <= kPoolMaxK): the kPoolN
+// smallest LRU keys as of the last full selection.
+constexpr int kPoolN = 64;
+constexpr int kPoolMaxK = 16;
 
 struct Shape {
   int L, E, H, I, k;

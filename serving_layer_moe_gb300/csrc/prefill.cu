@@ -844,6 +844,8 @@ extern "C" moe_status moe_layer_prefill(moe_cache* c, int32_t layer, int32_t T, 
   {
     ProfScope p(c, s, PROF_PREFILL_CONTROL);
     CK(cudaMemsetAsync(out, 0, (size_t)T * sh.H * sizeof(float), s));
+    // prefill rewrites slots and stamps by its own rules: the decode candidate pool is rebuilt afterwards
+    CK(cudaMemsetAsync(c->tab.pool + kPoolN, 0, sizeof(uint64_t), s));
     CK(cudaMemsetAsync(ps->counts, 0, (size_t)E * 4, s));
     const int g = std::max(1, std::min(c->sms * 4, (P + 255) / 256));
     route_count_kernel<<<g, 256, 0, s>>>(ids, P, E, ps->counts, c->err_dev);

@@ -164,6 +164,42 @@ def test_prefill_survivors_seed_decode():
     cache.close()
 
 
+def test_decode_prefill_decode_interleaved():
+    # decode keeps victim candidates between calls; a prefill in between rewrites
+    # slots and stamps, and the decode calls after it must still match the oracle
+    import torch
+    cfg = SMALL.with_(shape=Shape(L=3, E=24, k=2, H=256, I=128, wdtype="bf16", adtype="bf16"))
+    s = cfg.shape
+    dev = torch.device("cuda", 0)
+    C = 20
+    cache, store = _make(cfg, C, max_tokens=4)
+    K = min(s.E, 4 * s.k)
+    ora = SlotCache(s.L, s.E, C, K=K, b_pcie=1000, b_cpu=0)
+    dcfg = cfg.with_(T=4, steps=12, prefill=False)
+    ids, w = routing_trace(dcfg)
+    sm = torch.empty(4, s.k, dtype=torch.int32, device=dev)
+    o4 = torch.empty(4, s.H, device=dev)
+    out = torch.empty(cfg.T, s.H, device=dev)
+    for st in range(dcfg.steps):
+        if st in (4, 9):   # a prefill of one layer between decode steps
+            l = st % s.L
+            pids, pw = prefill_routing(cfg, l)
+            ora.prefill(l, pids)
+            cache.prefill(l, torch_act(activations(cfg, 0, l), dev), torch.from_numpy(pids).to(dev),
+                          torch.from_numpy(pw).to(dev), out)
+            torch.cuda.synchronize()
+            _check_state(cache, ora)
+        for l in range(s.L):
+            plan = ora.decode(l, ids[st, l])
+            cache.decode(l, torch_act(activations(dcfg, st, l), dev), torch.from_numpy(ids[st, l]).to(dev),
+                         torch.from_numpy(w[st, l]).to(dev), o4, slot_map=sm)
+            torch.cuda.synchronize()
+            assert np.array_equal(sm.cpu().numpy(), plan.slot_map), (st, l)
+            assert np.array_equal(cache.plan(T=4)["victims"], plan.victims), (st, l)
+    _check_state(cache, ora)
+    cache.close()
+
+
 def test_prefill_rejects_bad_config():
     import torch
     from serving_layer_moe_gb300 import MoECache, MoEError
