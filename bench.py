@@ -38,6 +38,14 @@ from workloads import (activations, config, default_max_fetch, make_blob, make_p
 WORKLOAD = "qwen3_decode_b1"
 METRIC = "MoE-layer decode steps/s"
 UNIT = "layer-steps/s"
+# DRAM bytes (read + write) of the resident-expert GEMV pair per layer-step, from
+# one ncu capture of both grids (cache control off, all-resident layers of the
+# qwen3 b1 shape, 8 resident experts each: the same work per layer-step as the
+# roofline replay); see profiles/decode_gemv_pair_qwen3_b1.md.
+TRAFFIC_PER_LAYER_STEP = 75_200_000
+TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of the gate/up and down grids of one "
+                  "layer-step, mean of 4 all-resident layer-steps of bench.py --mode profile-decode "
+                  "(16-layer qwen3 b1 shape, 8 resident experts per layer); profiles/decode_gemv_pair_qwen3_b1.md")
 
 
 def parse_args(argv=None):
@@ -51,10 +59,13 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the oracle CPU baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-prefill", action="store_true")
-    p.add_argument("--mode", default="all", choices=["all", "decode", "prefill"],
+    p.add_argument("--mode", default="all", choices=["all", "decode", "prefill", "profile-decode"],
                    help="prefill: only the prefill measurement (small profiling runs)")
     p.add_argument("--prefill-tokens", type=int, default=8192)
     p.add_argument("--capacity", type=int, default=0, help="override the slot count (small profiling runs)")
+    p.add_argument("--profile-layers", type=int, default=16, help="profile-decode: MoE layers of the small case")
+    p.add_argument("--profile-allhit", action="store_true",
+                   help="profile-decode: replay one step so every routed expert is resident after the first")
     p.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
     p.add_argument("--cpu-samples", type=int, default=1, help=argparse.SUPPRESS)
     return p.parse_args(argv)
@@ -213,6 +224,8 @@ def main(args):
         if rank == 0:
             print(json.dumps({"prefill": prefill_measure(args, dev, local)}))
         return
+    if args.mode == "profile-decode":
+        return profile_case(args, dev)
 
     from serving_layer_moe_gb300 import MoECache, bench_bw
 
@@ -354,17 +367,56 @@ def main(args):
             for k, (ms_k, n_k) in cache.profile_read().items():
                 prof[k][0] += ms_k
                 prof[k][1] += n_k
-    cache.profile_stop()
     cnt_p1 = cache.state()[3].copy()
+    # ---- roofline of the dominant HBM kernels, the resident-expert GEMV pair
+    # (gate/up grid, which also has L2 fetch the experts' W_down, then the down +
+    # combine grid), with nothing beside them: one step's inputs are replayed
+    # until every routed expert is resident (all hits, no fill), then the same
+    # event pairs time the two grids on their stream.  Algorithmic bytes: each
+    # resident expert's whole blob, read once.
+    res_reps = 16
+    with torch.cuda.stream(stream):
+        stage(step)
+        for _ in range(3):
+            pgraph.replay()
+            cache.profile_read()
+    torch.cuda.synchronize(dev)
+    cnt_r0 = cache.state()[3].copy()
+    res_prof = {k: [0.0, 0] for k in cache.PROFILE_KINDS}
+    with torch.cuda.stream(stream):
+        for _ in range(res_reps):
+            pgraph.replay()
+            for k, (ms_k, n_k) in cache.profile_read().items():
+                res_prof[k][0] += ms_k
+                res_prof[k][1] += n_k
+    cnt_r1 = cache.state()[3].copy()
+    cache.profile_stop()
+    e4 = torch.cuda.Event(enable_timing=True)
+    e5 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):   # the same all-hit step without event pairs: whole-layer time
+        e4.record(stream)
+        for _ in range(res_reps):
+            if graph is not None:
+                graph.replay()
+            else:
+                enqueue_step()
+        e5.record(stream)
+    torch.cuda.synchronize(dev)
+    ms_res = e4.elapsed_time(e5)
+    step += 1
     hbm_peak, bf16_peak, bf16_sust, peak_src = measured_peaks()
-    # The HBM-bound part of a layer-step: the resident experts' GEMV pair (gate/up
-    # grid, which also has L2 fetch their W_down, then the down + combine grid).
-    # Algorithmic bytes: every resident (hit) expert's whole blob, read once.
+    res_hits = int(cnt_r1[0] - cnt_r0[0])
+    res_fills = int(cnt_r1[2] - cnt_r0[2])
+    gemv_kinds = ("gemv_resident", "down_combine")   # split: the pair is one group; down_combine stays 0
+    res_ms = sum(res_prof[k][0] for k in gemv_kinds)
+    res_launches = res_prof["gemv_resident"][1]
+    res_bytes = res_hits * s.blob_bytes
+    res_gbs = res_bytes / (res_ms / 1e3) / 1e9 if res_ms > 0 else None
+    # the same pair inside the timed step's mix (concurrent fills, event pairs in the graph)
     resident = int(cnt_p1[0] - cnt_p0[0])
     gemv_bytes = resident * s.blob_bytes
-    gemv_kinds = ("gate_up_resident", "down_combine")
     gemv_ms = sum(prof[k][0] for k in gemv_kinds)
-    gemv_launches = prof["down_combine"][1]          # one per MoE-layer decode
+    gemv_launches = prof["gemv_resident"][1]         # one per MoE-layer decode
     fill_bytes = int(cnt_p1[2] - cnt_p0[2]) * s.blob_bytes
     total_prof_ms = sum(v[0] for v in prof.values())
 
@@ -388,14 +440,23 @@ def main(args):
         "e2e": {"value": round(e2e_steps * s.L * world / (ms_e2e / 1e3), 1), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": args.steps * s.L * launches_per_layer,
-        "roofline": {"bound": "hbm", "kernel": "resident-expert GEMV pair per layer-step: gate/up grid (with the L2 "
-                                               "fetch of W_down) + down-projection grid fused with the combine",
-                     "achieved": round(gemv_bytes / (gemv_ms / 1e3) / 1e9, 1) if gemv_ms > 0 else None,
-                     "peak": hbm_peak, "unit": "GB/s",
-                     "frac": round(gemv_bytes / (gemv_ms / 1e3) / 1e9 / hbm_peak, 3) if gemv_ms > 0 else None,
-                     "peak_source": peak_src, "traffic": None,
-                     "bytes_per_layer_step": round(gemv_bytes / max(1, gemv_launches)),
-                     "layer_steps_timed": gemv_launches},
+        "roofline": {"bound": "hbm",
+                     "kernel": "resident-expert GEMV pair per layer-step: gate/up grid (with the L2 fetch of W_down) "
+                               "+ down-projection grid fused with the combine; one step replayed with every routed "
+                               "expert resident, event pairs around the two grids",
+                     "achieved": round(res_gbs, 1) if res_gbs else None, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(res_gbs / hbm_peak, 3) if res_gbs else None, "peak_source": peak_src,
+                     "traffic": TRAFFIC_PER_LAYER_STEP,
+                     "traffic_source": TRAFFIC_SOURCE,
+                     "bytes_per_layer_step": round(res_bytes / max(1, res_launches)),
+                     "us_per_layer_step": round(1e3 * res_ms / max(1, res_launches), 2),
+                     "layer_steps_timed": res_launches, "fills_during": res_fills,
+                     "all_resident_layer_us": round(1e3 * ms_res / (res_reps * s.L), 2)},
+        "in_step_gemv": {"note": "the same two grids inside the timed step's mix (fills beside them; the event "
+                                 "pairs in the graph also drop their programmatic overlap)",
+                         "achieved_gbs": round(gemv_bytes / (gemv_ms / 1e3) / 1e9, 1) if gemv_ms > 0 else None,
+                         "bytes_per_layer_step": round(gemv_bytes / max(1, gemv_launches)),
+                         "us_per_layer_step": round(1e3 * gemv_ms / max(1, gemv_launches), 2)},
         "kernel_ms_share": {k: round(v[0] / total_prof_ms, 3) for k, v in prof.items() if v[1]},
         "kernel_us_per_layer": {k: round(1e3 * v[0] / max(1, v[1]), 2) for k, v in prof.items() if v[1]},
         "fill": {"achieved_gbs": round(fill_bytes / (prof["fill"][0] / 1e3) / 1e9, 1) if prof["fill"][0] > 0 else None,
@@ -413,6 +474,34 @@ def main(args):
     cache.close()
     if world > 1:
         dist.destroy_process_group()
+
+
+def profile_case(args, dev):
+    """A small decode case for ncu captures (a few GB on the device): the qwen3 b1
+    shape with --profile-layers layers and 256 slots (--capacity to change),
+    --steps eager steps of single decode calls, no graph, no timing."""
+    import torch
+    from serving_layer_moe_gb300 import MoECache
+    base = config(WORKLOAD)
+    cfg = base.with_(shape=base.shape.__class__(**{**base.shape.__dict__, "L": args.profile_layers}))
+    s = cfg.shape
+    arena, offs = make_pool(s, cfg.seed, n_phys=16)
+    pool = torch.from_numpy(arena).pin_memory()
+    cache = MoECache(L=s.L, E=s.E, H=s.H, I=s.I, top_k=s.k, max_tokens=1, wdtype=s.wdtype, adtype=s.adtype,
+                     host_pool=pool, blob_offsets=offs, n_slots=args.capacity or 256, bw_pcie_mbps=192000,
+                     bw_cpu_mbps=0, device=dev.index or 0)
+    ids, w = routing_trace(cfg)
+    out = torch.empty(1, s.H, device=dev)
+    for st0 in range(args.steps):
+        st = 0 if args.profile_allhit else st0 % cfg.steps
+        for l in range(s.L):
+            x = torch.from_numpy(activations(cfg, st, l).view(np.int16)).to(dev)
+            cache.decode(l, x, torch.from_numpy(ids[st, l]).to(dev), torch.from_numpy(w[st, l]).to(dev), out)
+    torch.cuda.synchronize(dev)
+    c = cache.state()[3]
+    print(json.dumps({"profile_case": f"{WORKLOAD} shape, {s.L} layers, {int(cache.info()[1])} slots",
+                      "hits": int(c[0]), "misses": int(c[1]), "fills": int(c[2])}))
+    cache.close()
 
 
 def prefill_measure(args, dev, local):

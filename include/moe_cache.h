@@ -207,10 +207,10 @@ moe_status moe_cache_info(moe_cache* cache, uint64_t* info_host);
  * (after each replay of a captured graph its pairs hold that replay's times);
  * mode 0: stop, read and reset.  Per kind the summed milliseconds and the
  * number of timed groups: 0 control, 1 fill (with the gate/up GEMV of the
- * filled experts), 2 gate/up GEMV of resident experts, 3 down-projection GEMV of
- * the filled experts (when the down projection is split), 4 down-projection GEMV
- * of the resident experts (or of all) + combine, 5 prefill control, 6 prefill
- * load, 7 prefill grouped GEMM.  ms_host[8] and
+ * filled experts), 2 GEMV of the resident experts (gate/up, and, when the down
+ * projection is split, their down projection + combine), 3 down-projection GEMV
+ * of the filled experts (split), 4 down-projection GEMV of every GPU expert +
+ * combine (not split), 5 prefill control, 6 prefill load, 7 prefill grouped GEMM.  ms_host[8] and
  * launches_host[8] may be NULL.
  */
 moe_status moe_cache_profile(moe_cache* cache, int32_t mode, double* ms_host, uint64_t* launches_host);

@@ -174,7 +174,7 @@ class MoECache:
             out["y"] = y
         return out
 
-    PROFILE_KINDS = ("control", "fill", "gate_up_resident", "down_filled", "down_combine",
+    PROFILE_KINDS = ("control", "fill", "gemv_resident", "down_filled", "down_combine",
                      "prefill_control", "prefill_load", "prefill_gemm")
 
     def profile_start(self):

@@ -43,7 +43,7 @@ enum PlanIdx : int {
 
 // kernel groups timed by moe_cache_profile
 enum ProfKind : int {
-  PROF_CONTROL = 0, PROF_FILL = 1, PROF_GATE_UP_RESIDENT = 2, PROF_DOWN_FILLED = 3, PROF_DOWN_COMBINE = 4,
+  PROF_CONTROL = 0, PROF_FILL = 1, PROF_GEMV_RESIDENT = 2, PROF_DOWN_FILLED = 3, PROF_DOWN_COMBINE = 4,
   PROF_PREFILL_CONTROL = 5, PROF_PREFILL_LOAD = 6, PROF_PREFILL_GEMM = 7, PROF_KINDS = 8,
 };
 
