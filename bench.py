@@ -515,6 +515,8 @@ def prefill_measure(args, dev, local):
     import torch
     from serving_layer_moe_gb300 import MoECache
     cfg = config("qwen3_prefill_8k").with_(T=args.prefill_tokens)
+    if args.capacity:
+        cfg = cfg.with_(capacity=args.capacity)
     s = cfg.shape
     arena, offs = make_pool(s, cfg.seed, n_phys=args.pool_blobs)
     pool = torch.from_numpy(arena).pin_memory()

@@ -57,9 +57,13 @@ constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;          // 16 KB
 constexpr int B_BYTES = BN * BK * 2;          // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int GEMM_THREADS = 192;             // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int GEMM_THREADS = 320;             // GEMM 1: warp 0 TMA, warp 1 MMA, warps 2-9 epilogue (two per TMEM lane quarter)
+constexpr int GEMM2_THREADS = 576;            // GEMM 2: warps 2-17 epilogue (four per TMEM lane quarter)
+constexpr int GEMM2_STAGES = 3;               // GEMM 2's short K (I) needs fewer stages; the room goes to staging
 constexpr int TMEM_COLS = 512;                // two 128 x 256 fp32 accumulators
 constexpr size_t GEMM_SMEM = (size_t)STAGES * STAGE_BYTES + 1024 + 256;
+constexpr size_t GEMM2_SMEM = (size_t)GEMM2_STAGES * STAGE_BYTES + 1024 + 256 +
+                              (size_t)(GEMM2_THREADS - 64) * 144;   // + a 128-byte reduce staging buffer per epilogue thread
 constexpr unsigned long long kWaitNs = 2000000000ull;   // 2 s bound on any wait
 
 struct PrefillState {
@@ -194,8 +198,11 @@ struct GemmArgs {
 };
 
 template <int EPI>
-__global__ void __launch_bounds__(GEMM_THREADS, 1)
+__global__ void __launch_bounds__(EPI == 0 ? GEMM_THREADS : GEMM2_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs a) {
+  constexpr int STAGES = EPI == 0 ? ::moe::STAGES : GEMM2_STAGES;
+  constexpr int NEPI = EPI == 0 ? 8 : 16;         // epilogue warps; NEPI / 4 of them share a TMEM lane quarter
+  constexpr int CSPLIT = NEPI / 4;                // ... and split its columns
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -209,7 +216,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-    for (int s = 0; s < 2; ++s) { mbar_init(&tfull[s], 1); mbar_init(&tempty[s], 128); }
+    for (int s = 0; s < 2; ++s) { mbar_init(&tfull[s], 1); mbar_init(&tempty[s], 32 * NEPI); }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -290,6 +297,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   } else if (warp >= 2) {
     // ---------------- epilogue: 4 warps, one TMEM lane (= tile row) per thread ----------------
     const int sub = warp & 3;
+    const int part = (warp - 2) >> 2;   // which column share of the lane quarter
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
@@ -307,7 +315,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       if (EPI == 0) {
         uint16_t* dst = a.hs + (size_t)row * a.I + (size_t)nt * (BN / 2);
 #pragma unroll 1
-        for (int c = 0; c < BN / 2; c += 32) {
+        for (int c = part * (BN / 2 / CSPLIT); c < (part + 1) * (BN / 2 / CSPLIT); c += 32) {
           uint32_t g[32], u[32];
           tmem_ld32(tbase + c, g);
           tmem_ld32(tbase + BN / 2 + c, u);
@@ -336,19 +344,29 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           t = p / a.k;
           wt = a.w[p];
         }
+        // Each row's 32 gated columns go through this thread's 128-byte staging
+        // buffer into one bulk reduce-add on the row of out: the TMA unit does the
+        // fp32 adds in L2 as one contiguous 128-byte request, and the thread moves
+        // on (it only waits for the buffer to have been read before refilling it).
         float* dst = a.out + (size_t)t * a.H + (size_t)nt * BN;
+        // (thread stride 144 B: the eight 16-byte stores of a warp spread over all banks)
+        float4* stg = reinterpret_cast<float4*>(smem + STAGES * STAGE_BYTES + 256) + (threadIdx.x - 64) * 9;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = part * (BN / CSPLIT); c < (part + 1) * (BN / CSPLIT); c += 32) {
           uint32_t v[32];
           tmem_ld32(tbase + c, v);
           tmem_ld_wait();
           if (valid) {
+            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              float4 q = make_float4(wt * __uint_as_float(v[4 * i]), wt * __uint_as_float(v[4 * i + 1]),
-                                     wt * __uint_as_float(v[4 * i + 2]), wt * __uint_as_float(v[4 * i + 3]));
-              atomicAdd(reinterpret_cast<float4*>(dst + c + 4 * i), q);
-            }
+            for (int i = 0; i < 8; ++i)
+              stg[i] = make_float4(wt * __uint_as_float(v[4 * i]), wt * __uint_as_float(v[4 * i + 1]),
+                                   wt * __uint_as_float(v[4 * i + 2]), wt * __uint_as_float(v[4 * i + 3]));
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], 128;" ::"l"(dst + c),
+                         "r"(smem_u32(stg))
+                         : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
           }
         }
       }
@@ -357,6 +375,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
+    if (EPI == 1) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");   // every reduce has landed
   }
   fence_before();
   __syncthreads();
@@ -760,7 +779,7 @@ moe_status prefill_init(moe_cache* c) {
   CK(cudaEventCreateWithFlags(&ps->ev_ctrl, cudaEventDisableTiming));
   CK(cudaEventCreateWithFlags(&ps->ev_cur, cudaEventDisableTiming));
   CK(cudaFuncSetAttribute(grouped_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GEMM_SMEM));
-  CK(cudaFuncSetAttribute(grouped_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GEMM_SMEM));
+  CK(cudaFuncSetAttribute(grouped_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)GEMM2_SMEM));
   CK(cudaFuncSetAttribute(prefill_control_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
   return refresh_b_maps(c);
 }
@@ -810,7 +829,7 @@ static moe_status run_gemms(moe_cache* c, int T, const float* w, float* out, cud
   g.b_row_off = 2 * sh.H;
   g.b_half_off = BN / 2;
   g.b_n_step = BN;
-  grouped_gemm_kernel<1><<<c->sms, GEMM_THREADS, GEMM_SMEM, s>>>(ps->tm_a2, ps->tm_b2, g);
+  grouped_gemm_kernel<1><<<c->sms, GEMM2_THREADS, GEMM2_SMEM, s>>>(ps->tm_a2, ps->tm_b2, g);
   CK(cudaGetLastError());
   return MOE_OK;
 }
