@@ -284,7 +284,9 @@ def main(args):
             enqueue_step()
         torch.cuda.synchronize(dev)
 
-    launches_per_layer = 4    # control, fill fused with the filled experts' gate/up, gate/up resident, down + combine
+    # control, fill (+ the filled experts' gate/up), the filled experts' down grid,
+    # the resident gate/up grid, the resident down + combine grid
+    launches_per_layer = 5
     # ---- timed region: inputs resident in HBM ---------------------------------
     cnt0 = cache.state()[3].copy()
     if world > 1:
