@@ -740,6 +740,31 @@ __device__ __forceinline__ float reduce16(float (&v)[16], int lane) {
   return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
 }
 
+// The same for 8 values: afterwards lane l holds the full sum of value (l >> 2) & 7.
+// The pairing of lanes (16, 8, 4, 2, 1) is that of warp_sum and reduce16, so a
+// row's sum is the same bit for bit whichever of them forms it.
+__device__ __forceinline__ float reduce8(float (&v)[8], int lane) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const bool hi = lane & 16;
+    const float send = hi ? v[j] : v[j + 4];
+    v[j] = (hi ? v[j + 4] : v[j]) + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const bool hi = lane & 8;
+    const float send = hi ? v[j] : v[j + 2];
+    v[j] = (hi ? v[j + 2] : v[j]) + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+  {
+    const bool hi = lane & 4;
+    const float send = hi ? v[0] : v[1];
+    v[0] = (hi ? v[1] : v[0]) + __shfl_xor_sync(0xffffffffu, send, 4);
+  }
+  v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
+  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+}
+
 constexpr int kDownRows = 16;   // output rows per CTA of the bulk down kernel, at most
 constexpr size_t kPrefetchPiece = 32 * 1024;
 // dynamic shared memory the bulk kernels may ask for (the down kernel also has a few static bytes)
@@ -917,10 +942,13 @@ __global__ void __launch_bounds__(256) gate_up_bulk_kernel(GemvArgs a, BulkGeom 
 // and 1 are two grids over the same row blocks: each publishes its y, counts
 // itself in arrive[block], and the second of the two (odd count before its
 // increment) forms the block's combine from y in global memory.
-template <int WT, bool kRing, int kJN>
-__global__ void __launch_bounds__(kRing ? 256 : 512) down_bulk_kernel(GemvArgs a, BulkGeom geo, const float* __restrict__ w,
+template <int WT, bool kRing, int kJN, bool kPair = false>
+__global__ void __launch_bounds__((kRing && !kPair) ? 256 : 512) down_bulk_kernel(GemvArgs a, BulkGeom geo,
+                                                        const float* __restrict__ w,
                                                         const float* __restrict__ cpu, float* __restrict__ out,
                                                         uint32_t* err) {
+  // kPair: two warps per ring stage (one expert each pair), each taking 8 of its rows
+  static_assert(!kPair || (kRing && kJN > 0), "pair mode is the straight-line ring path");
   using F = WFmt<WT>;
   constexpr int V = F::V;
   constexpr int J = 32 / V;   // 16-byte chunks per lane per column segment (32 h values in registers)
@@ -937,11 +965,14 @@ __global__ void __launch_bounds__(kRing ? 256 : 512) down_bulk_kernel(GemvArgs a
     alone = a.pass == 0 ? ngpu == nfirst : nfirst == 0;
   }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm) + warp * geo.NS;
+  const int rw = kPair ? (warp >> 1) : warp;      // owner of the ring stages this warp reads
+  const int half = kPair ? (warp & 1) : 0;        // pair mode: rows [8 half, 8 half + 8)
+  const bool owner = !kPair || half == 0;         // issues and re-arms the stages
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm) + rw * geo.NS;
   uint64_t* hbar = reinterpret_cast<uint64_t*>(sm) + 31;   // ring barriers use at most 8 x 2
-  uint8_t* ring = sm + geo.ring_off + (size_t)warp * geo.NS * geo.SB;
+  uint8_t* ring = sm + geo.ring_off + (size_t)rw * geo.NS * geo.SB;
   if (lane == 0) {
-    if (kRing)
+    if (kRing && owner)
       for (int i = 0; i < geo.NS; ++i) bar_init(&bars[i]);
     if (warp == 0) bar_init(hbar);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -977,9 +1008,9 @@ __global__ void __launch_bounds__(kRing ? 256 : 512) down_bulk_kernel(GemvArgs a
     bar_expect(&bars[st], bytes);
     bulk_copy(ring + (size_t)st * geo.SB, sp.w[g] + down_off + (size_t)r0 * row_bytes, bytes, &bars[st], pol);
   };
-  if (kRing && lane == 0)
+  if (kRing && lane == 0 && owner)
     for (int k = 0; k < geo.NS; ++k) {
-      const int g = g0 + warp + k * geo.NW;
+      const int g = g0 + rw + k * geo.NW;
       if (g < g1) issue(g, k);
     }
   pdl_wait();   // h of the resident experts is complete from here on
@@ -1043,18 +1074,20 @@ __global__ void __launch_bounds__(kRing ? 256 : 512) down_bulk_kernel(GemvArgs a
     }
   }
   int k = 0;
-  for (int g = g0 + warp; kRing && g < g1; g += geo.NW, ++k) {
+  for (int g = g0 + rw; kRing && g < g1; g += geo.NW, ++k) {
     const int st = k % geo.NS;
     if (k == 0 && h_copy && !__all_sync(0xffffffffu, bar_wait(hbar, 0))) { ok = false; break; }
     if (!__all_sync(0xffffffffu, bar_wait(&bars[st], (uint32_t)((k / geo.NS) & 1)))) { ok = false; break; }
     const uint8_t* blk = ring + (size_t)st * geo.SB;
     const float* sd = reinterpret_cast<const float*>(sp.w[g] + sd_off);
     const int pb = sp.off[g], pe = sp.off[g + 1];
+    constexpr int kRW = kPair ? 8 : kDownRows;   // rows this warp accumulates
+    const int rbase = kPair ? 8 * half : 0;
     for (int tp = pb; tp < pe; ++tp) {
       const int pid = sp.pid[tp];
-      float acc[kDownRows];
+      float acc[kRW];
 #pragma unroll
-      for (int r = 0; r < kDownRows; ++r) acc[r] = 0.f;
+      for (int r = 0; r < kRW; ++r) acc[r] = 0.f;
       if (kJN > 0) {
         // NCH = 32 kJN: one column segment, no guards; rows past nr repeat the
         // last row (their sums are never stored), so the whole block is one
@@ -1070,8 +1103,8 @@ __global__ void __launch_bounds__(kRing ? 256 : 512) down_bulk_kernel(GemvArgs a
           }
         }
 #pragma unroll
-        for (int r = 0; r < kDownRows; ++r) {
-          const int rr = r < nr ? r : nr - 1;
+        for (int r = 0; r < kRW; ++r) {
+          const int rr = rbase + r < nr ? rbase + r : nr - 1;
           const uint4* wrow = reinterpret_cast<const uint4*>(blk + (size_t)rr * row_bytes);
           float d = 0.f;
 #pragma unroll
@@ -1126,15 +1159,25 @@ __global__ void __launch_bounds__(kRing ? 256 : 512) down_bulk_kernel(GemvArgs a
           }
         }
       }
-      const float v = reduce16(acc, lane);
-      const int r = lane >> 1;
-      if ((lane & 1) == 0 && r < nr) {
+      float v;
+      int r;
+      bool mine;
+      if constexpr (kPair) {
+        v = reduce8(acc, lane);
+        r = rbase + ((lane >> 2) & 7);
+        mine = (lane & 3) == 0;
+      } else {
+        v = reduce16(acc, lane);
+        r = lane >> 1;
+        mine = (lane & 1) == 0;
+      }
+      if (mine && r < nr) {
         ys[(size_t)r * NP + pid] = v;
         a.b.y[(size_t)pid * H + r0 + r] = v;   // per-pair output stays readable (moe_cache_get_plan)
       }
     }
     __syncwarp();
-    if (lane == 0 && g + geo.NS * geo.NW < g1) {
+    if (lane == 0 && owner && g + geo.NS * geo.NW < g1) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       issue(g + geo.NS * geo.NW, st);
     }
@@ -1372,6 +1415,8 @@ cudaError_t setup_gemv_kernels() {
                          staged_plan_bytes(4096 + 1, kDCMaxPairs) + (size_t)kDCMaxPairs * 8);
   for (const void* k : {(const void*)down_bulk_kernel<MOE_F32, true, 0>, (const void*)down_bulk_kernel<MOE_BF16, true, 0>,
                         (const void*)down_bulk_kernel<MOE_BF16, true, 3>, (const void*)down_bulk_kernel<MOE_BF16, true, 4>,
+                        (const void*)down_bulk_kernel<MOE_BF16, true, 3, true>,
+                        (const void*)down_bulk_kernel<MOE_BF16, true, 4, true>,
                         (const void*)down_bulk_kernel<MOE_FP8E4M3_B128, true, 0>,
                         (const void*)down_bulk_kernel<MOE_F32, false, 0>, (const void*)down_bulk_kernel<MOE_BF16, false, 0>,
                         (const void*)down_bulk_kernel<MOE_FP8E4M3_B128, false, 0>}) {
@@ -1559,17 +1604,21 @@ cudaError_t launch_down_bulk(const GemvArgs& a, const BulkGeom& geo, bool ring, 
     down_bulk_kernel<WT, false, 0><<<d.grid, d.NW * 32, d.smem, s>>>(a, d, w, cpu, out, err);
     return cudaGetLastError();
   }
-  auto go = [&](auto kern) -> cudaError_t {
-    if (pdl) return launch_pdl(kern, dim3(geo.grid), dim3(geo.NW * 32), geo.smem, s, a, geo, w, cpu, out, err);
-    kern<<<geo.grid, geo.NW * 32, geo.smem, s>>>(a, geo, w, cpu, out, err);
+  auto go = [&](auto kern, int threads) -> cudaError_t {
+    if (pdl) return launch_pdl(kern, dim3(geo.grid), dim3(threads), geo.smem, s, a, geo, w, cpu, out, err);
+    kern<<<geo.grid, threads, geo.smem, s>>>(a, geo, w, cpu, out, err);
     return cudaGetLastError();
   };
   if constexpr (WT == MOE_BF16) {   // rows of 3 or 4 chunks per lane: the unguarded straight-line path
     const int nch = a.I / 8;
-    if (nch == 96) return go(down_bulk_kernel<WT, true, 3>);
-    if (nch == 128) return go(down_bulk_kernel<WT, true, 4>);
+    // one stage per expert for at most 8 experts: two warps per stage, 8 rows each
+    const bool pair = geo.NS == 1 && geo.NW == 8 && a.max_g <= 8 && geo.R <= 16;
+    if (nch == 96)
+      return pair ? go(down_bulk_kernel<WT, true, 3, true>, 512) : go(down_bulk_kernel<WT, true, 3>, geo.NW * 32);
+    if (nch == 128)
+      return pair ? go(down_bulk_kernel<WT, true, 4, true>, 512) : go(down_bulk_kernel<WT, true, 4>, geo.NW * 32);
   }
-  return go(down_bulk_kernel<WT, true, 0>);
+  return go(down_bulk_kernel<WT, true, 0>, geo.NW * 32);
 }
 
 cudaError_t launch_down_bulk_any(const Shape& sh, const GemvArgs& a, const BulkGeom& geo, bool ring, bool pdl,
