@@ -68,6 +68,8 @@ def parse_args(argv=None):
                    help="profile-decode: replay one step so every routed expert is resident after the first")
     p.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
     p.add_argument("--cpu-samples", type=int, default=1, help=argparse.SUPPRESS)
+    p.add_argument("--ref-seconds", type=float, default=0.0,
+                   help="reference arm: oracle seconds per bench step (0: fit the run into about two minutes)")
     return p.parse_args(argv)
 
 
@@ -591,7 +593,7 @@ def reference_arm(args, world, rank):
         return
     b = os.environ.get("BENCH_BW", "200000,100000").split(",")
     bw = (int(b[0]), int(b[1]))
-    per_step = max(2.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    per_step = args.ref_seconds or max(2.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
     res = run_cpu_baseline(per_step, args.pool_blobs, bw, samples=args.warmup + args.steps)
     if isinstance(res, dict):
         res = [res]
