@@ -79,7 +79,8 @@ typedef enum moe_status {
 typedef enum moe_dtype {
   MOE_F32 = 0,            /* IEEE binary32 */
   MOE_BF16 = 1,           /* bfloat16 */
-  MOE_FP8E4M3_B128 = 2    /* OCP e4m3 codes with one fp32 scale per 128x128 block */
+  MOE_FP8E4M3_B128 = 2,   /* OCP e4m3 codes with one fp32 scale per 128x128 block */
+  MOE_NVFP4 = 3           /* e2m1 codes, one e4m3 scale per 16 row elements, one fp32 scale per matrix */
 } moe_dtype;
 
 /*
@@ -87,8 +88,14 @@ typedef enum moe_dtype {
  *   W_gu [2I, H] row-major in wdtype (rows 0..I-1 gate, rows I..2I-1 up),
  *   W_d  [H, I]  row-major in wdtype,
  *   MOE_FP8E4M3_B128 only: s_gu [2I/128, H/128] fp32, s_d [H/128, I/128] fp32.
- * S = 3*I*H*sizeof(w) (+ 4*(2I*H + H*I)/16384 for fp8).  H and I must be
- * multiples of 128 (fp8) or 8 (f32, bf16).
+ *   MOE_NVFP4: W_gu and W_d hold two e2m1 codes per byte (the even element in
+ *   the low nibble), then s_gu [2I, H/16] and s_d [H, I/16] e4m3 codes (one per
+ *   16 consecutive elements of a row), then fp32 g_gu, g_d and 8 bytes of zero;
+ *   a weight is e2m1(code) * e4m3(its block's scale) * g of its matrix.
+ * S = 3*I*H*sizeof(w) (+ 4*(2I*H + H*I)/16384 for fp8; 3*I*H/2 + 3*I*H/16 + 16
+ * for nvfp4).  H and I must be multiples of 128 (fp8), 32 (nvfp4) or 8 (f32,
+ * bf16).  NVFP4 experts serve decode calls of up to 2 tokens (max_tokens <= 2)
+ * and no prefill (max_prefill_tokens = 0).
  */
 typedef struct moe_config {
   int32_t n_layers;       /* L */
@@ -246,6 +253,7 @@ moe_status bench_bw(int32_t device, uint64_t expert_bytes, double* b_pcie_gbs, d
  *                S bytes each), device memory, 16-byte aligned
  *   x_dev [T, H] in adtype, topk_ids_dev / topk_w_dev [T, k], out_dev [T, H] fp32
  * Ids outside [0, E) contribute nothing.  Enqueued on `stream`; never blocks.
+ * wdtype MOE_F32, MOE_BF16 or MOE_FP8E4M3_B128 (MOE_NVFP4 is MOE_EINVAL here).
  *
  * Limits and sharing:
  *   - scratch needed ~ T * top_k * (H + I) * 4 bytes plus small lists; a call

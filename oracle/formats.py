@@ -9,6 +9,11 @@ bit layout; the layouts here are the standard definitions:
            no infinities, S.1111.111 is NaN, max finite 448, subnormals
            (exponent field 0) are m/8 * 2**-6.
   blockscale: value = e4m3(code) * scale[row // 128, col // 128].
+  e2m1   : FP4 E2M1: 1 sign, 2 exponent (bias 1), 1 mantissa bit, no
+           infinities or NaN; exponent field 0 is m/2, otherwise
+           (1 + m/2) * 2**(e-1): magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+  nvfp4  : value = e2m1(code) * e4m3(scale of its 16-element row block) * g of
+           the matrix; two codes per byte, the even element in the low nibble.
 
 Nothing here rounds: every bf16 / e4m3 value is exactly representable in
 float64.
@@ -41,6 +46,32 @@ def e4m3_codes_to_f64(codes: np.ndarray) -> np.ndarray:
     return E4M3_TABLE[np.asarray(codes, dtype=np.uint8)]
 
 
+def _e2m1_value(code: int) -> float:
+    s = -1.0 if code & 0x8 else 1.0
+    e = (code >> 1) & 0x3
+    m = code & 0x1
+    if e == 0:
+        return s * m / 2.0
+    return s * (1.0 + m / 2.0) * 2.0 ** (e - 1)
+
+
+E2M1_TABLE = np.array([_e2m1_value(c) for c in range(16)], dtype=np.float64)
+
+
+def nvfp4_dequant(packed: np.ndarray, scales: np.ndarray, g: float) -> np.ndarray:
+    """packed [R, C/2] (even element in the low nibble), scales [R, C/16] e4m3 codes,
+    g fp32 -> float64 [R, C]."""
+    packed = np.asarray(packed, dtype=np.uint8)
+    R, C2 = packed.shape
+    C = 2 * C2
+    codes = np.empty((R, C), np.uint8)
+    codes[:, 0::2] = packed & 0xF
+    codes[:, 1::2] = packed >> 4
+    assert scales.shape == (R, C // 16)
+    s = e4m3_codes_to_f64(scales)
+    return E2M1_TABLE[codes] * np.repeat(s, 16, axis=1) * float(np.float32(g))
+
+
 def blockscale_dequant(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
     """codes [R, C] e4m3, scales [R/128, C/128] fp32 -> float64 [R, C]."""
     R, C = codes.shape
@@ -55,7 +86,9 @@ def parse_blob(blob: np.ndarray, wdtype: str, H: int, I: int):
 
     Bank layout: W_gu [2I, H] row-major (gate rows first, then up rows), then
     W_down [H, I] row-major; fp8 blobs append s_gu [2I/128, H/128] and
-    s_d [H/128, I/128] fp32 scales.
+    s_d [H/128, I/128] fp32 scales; nvfp4 blobs hold packed e2m1 codes, then
+    per-16-element e4m3 row-block scales s_gu [2I, H/16] and s_d [H, I/16],
+    then the two fp32 matrix scales (g_gu, g_d) and 8 bytes of padding.
     """
     blob = np.asarray(blob, dtype=np.uint8)
     if wdtype == "f32":
@@ -78,6 +111,15 @@ def parse_blob(blob: np.ndarray, wdtype: str, H: int, I: int):
         s_d = blob[o + 4 * n_sgu:o + 4 * (n_sgu + n_sd)].view(np.float32).reshape(H // 128, I // 128)
         w_gu = blockscale_dequant(c_gu, s_gu)
         w_d = blockscale_dequant(c_d, s_d)
+    elif wdtype == "nvfp4":
+        o = 0
+        p_gu = blob[o:o + I * H].reshape(2 * I, H // 2); o += I * H
+        p_d = blob[o:o + H * I // 2].reshape(H, I // 2); o += H * I // 2
+        s_gu = blob[o:o + 2 * I * H // 16].reshape(2 * I, H // 16); o += 2 * I * H // 16
+        s_d = blob[o:o + H * I // 16].reshape(H, I // 16); o += H * I // 16
+        g = blob[o:o + 16].view(np.float32)
+        w_gu = nvfp4_dequant(p_gu, s_gu, g[0])
+        w_d = nvfp4_dequant(p_d, s_d, g[1])
     else:
         raise ValueError(wdtype)
     return w_gu[:I], w_gu[I:], w_d

@@ -27,6 +27,7 @@
 #include "internal.cuh"
 
 #include <cuda_fp8.h>
+#include <cuda_fp4.h>
 
 #include <algorithm>
 
@@ -39,15 +40,21 @@ constexpr int kChunksPerLane = 4;
 
 // ---- weight formats: one 16-byte chunk -> V floats ---------------------------
 template <int WT> struct WFmt;
+// row(n): bytes of n elements; sgu_off / sd_off / g_off: offsets of the scale
+// arrays (and NVFP4's matrix scales) inside a blob of the format
 template <> struct WFmt<MOE_F32> {
-  static constexpr int V = 4, ES = 4;
+  static constexpr int V = 4;
+  __host__ __device__ static constexpr size_t row(size_t n) { return n * 4; }
+  __host__ __device__ static constexpr size_t sd_off(size_t, size_t) { return 0; }
   __device__ static void unpack(const uint4& w, float* f) {
     f[0] = __uint_as_float(w.x); f[1] = __uint_as_float(w.y);
     f[2] = __uint_as_float(w.z); f[3] = __uint_as_float(w.w);
   }
 };
 template <> struct WFmt<MOE_BF16> {
-  static constexpr int V = 8, ES = 2;
+  static constexpr int V = 8;
+  __host__ __device__ static constexpr size_t row(size_t n) { return n * 2; }
+  __host__ __device__ static constexpr size_t sd_off(size_t, size_t) { return 0; }
   __device__ static void unpack(const uint4& w, float* f) {
     const uint32_t v[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -58,7 +65,11 @@ template <> struct WFmt<MOE_BF16> {
   }
 };
 template <> struct WFmt<MOE_FP8E4M3_B128> {
-  static constexpr int V = 16, ES = 1;
+  static constexpr int V = 16;
+  __host__ __device__ static constexpr size_t row(size_t n) { return n; }
+  __host__ __device__ static constexpr size_t sd_off(size_t H, size_t I) {
+    return 3 * I * H + 4 * (2 * I / 128) * (H / 128);
+  }
   __device__ static void unpack(const uint4& w, float* f) {
     const uint32_t v[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -71,6 +82,44 @@ template <> struct WFmt<MOE_FP8E4M3_B128> {
     }
   }
 };
+
+template <> struct WFmt<MOE_NVFP4> {
+  static constexpr int V = 32;   // two elements per byte
+  __host__ __device__ static constexpr size_t row(size_t n) { return n / 2; }
+  __host__ __device__ static constexpr size_t sgu_off(size_t H, size_t I) { return 3 * I * H / 2; }
+  __host__ __device__ static constexpr size_t sd_off(size_t H, size_t I) { return 3 * I * H / 2 + 2 * I * H / 16; }
+  __host__ __device__ static constexpr size_t g_off(size_t H, size_t I) { return sd_off(H, I) + H * I / 16; }
+  // the 32 e2m1 values of a 16-byte chunk, element 2j from the low nibble of byte j
+  __device__ static void unpack(const uint4& w, float* f) {
+    const uint32_t v[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const __half2_raw h = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)((v[i] >> (8 * b)) & 0xffu), __NV_E2M1);
+        const float2 p = __half22float2(*reinterpret_cast<const __half2*>(&h));
+        f[8 * i + 2 * b] = p.x;
+        f[8 * i + 2 * b + 1] = p.y;
+      }
+  }
+};
+
+// One NVFP4 chunk (32 weights = two 16-element blocks; s2 = their two e4m3
+// scale codes, the first block's in the low byte) against 32 activations:
+// (sum of the first 16 products) * scale_0 + (sum of the last 16) * scale_1.
+// Every NVFP4 path uses this, so a row's value does not depend on the kernel.
+__device__ __forceinline__ float dot_nvfp4(const uint4& w, uint32_t s2, const float* x) {
+  float f[32];
+  WFmt<MOE_NVFP4>::unpack(w, f);
+  float lo = 0.f, hi = 0.f;
+#pragma unroll
+  for (int v = 0; v < 16; ++v) lo = fmaf(f[v], x[v], lo);
+#pragma unroll
+  for (int v = 0; v < 16; ++v) hi = fmaf(f[16 + v], x[16 + v], hi);
+  const __half2_raw sr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(s2 & 0xffffu), __NV_E4M3);
+  const float2 sf = __half22float2(*reinterpret_cast<const __half2*>(&sr));
+  return fmaf(hi, sf.y, lo * sf.x);
+}
 
 // ---- activations: V consecutive values as floats --------------------------
 template <int AT, int V> __device__ __forceinline__ void load_act(const void* x, size_t off, float* f);
@@ -90,6 +139,9 @@ template <> __device__ __forceinline__ void load_act<MOE_F32, 8>(const void* x, 
 template <> __device__ __forceinline__ void load_act<MOE_F32, 16>(const void* x, size_t off, float* f) {
   load_act_f32<16>(reinterpret_cast<const float*>(x) + off, f);
 }
+template <> __device__ __forceinline__ void load_act<MOE_F32, 32>(const void* x, size_t off, float* f) {
+  load_act_f32<32>(reinterpret_cast<const float*>(x) + off, f);
+}
 template <int V> __device__ __forceinline__ void load_act_bf16(const uint16_t* p, float* f) {
 #pragma unroll
   for (int i = 0; i < V; i += 8) {
@@ -102,6 +154,9 @@ template <> __device__ __forceinline__ void load_act<MOE_BF16, 8>(const void* x,
 }
 template <> __device__ __forceinline__ void load_act<MOE_BF16, 16>(const void* x, size_t off, float* f) {
   load_act_bf16<16>(reinterpret_cast<const uint16_t*>(x) + off, f);
+}
+template <> __device__ __forceinline__ void load_act<MOE_BF16, 32>(const void* x, size_t off, float* f) {
+  load_act_bf16<32>(reinterpret_cast<const uint16_t*>(x) + off, f);
 }
 template <> __device__ __forceinline__ void load_act<MOE_BF16, 4>(const void* x, size_t off, float* f) {
   const uint2 v = __ldg(reinterpret_cast<const uint2*>(reinterpret_cast<const uint16_t*>(x) + off));
@@ -240,7 +295,7 @@ __global__ void __launch_bounds__(kGemvThreads, kTokGroup == 1 ? 2 : 1) gate_up_
   const long nwarps = (long)gridDim.x * (blockDim.x >> 5);
   const long wid = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int NCH = H / V;                       // 16-byte chunks per row
-  const size_t row_bytes = (size_t)H * F::ES;
+  const size_t row_bytes = F::row(H);
   const int HB = H / 128;                      // fp8 scale columns
   const uint64_t pol = evict_first_policy();
 
@@ -333,7 +388,7 @@ fill_gate_up_kernel(GemvArgs a, const int32_t* __restrict__ fills, const uint8_t
   const long nwarps = (long)gridDim.x * (blockDim.x >> 5);
   const long wid = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int NCH = H / V;
-  const size_t row_bytes = (size_t)H * F::ES;
+  const size_t row_bytes = F::row(H);
   const int HB = H / 128;
   const size_t down_off = 2ull * (size_t)I * row_bytes;
   const uint64_t tail16 = (S - down_off) >> 4;             // 16-byte chunks after W_gu
@@ -402,25 +457,39 @@ fill_gate_up_kernel(GemvArgs a, const int32_t* __restrict__ fills, const uint8_t
         for (int j = 0; j < kChunksPerLane; ++j) {
           const int c = seg + j * 32 + lane;
           if (c < NCH) {
-            float fg[V], fu[V];
-            F::unpack(wg[j], fg);
-            F::unpack(wu[j], fu);
-            float scg = 1.f, scu = 1.f;
-            if (WT == MOE_FP8E4M3_B128) {
-              const int cb = (c * V) >> 7;
-              scg = sgu[(size_t)(i >> 7) * HB + cb];
-              scu = sgu[(size_t)((I + i) >> 7) * HB + cb];
-            }
+            if constexpr (WT == MOE_NVFP4) {   // scales straight from the host blob
+              const uint16_t* srow = reinterpret_cast<const uint16_t*>(sb + F::sgu_off(H, I));
+              const uint32_t sg2 = srow[(size_t)i * (H / 32) + c], su2 = srow[(size_t)(I + i) * (H / 32) + c];
 #pragma unroll
-            for (int n = 0; n < kTokGroup; ++n) {
-              if (n < nt) {
-                float xv[V];
-                load_act<AT, V>(a.x, (size_t)tok[n] * H + (size_t)c * V, xv);
-                float dg = 0.f, du = 0.f;
+              for (int n = 0; n < kTokGroup; ++n) {
+                if (n < nt) {
+                  float xv[V];
+                  load_act<AT, V>(a.x, (size_t)tok[n] * H + (size_t)c * V, xv);
+                  ag[n] += dot_nvfp4(wg[j], sg2, xv);
+                  au[n] += dot_nvfp4(wu[j], su2, xv);
+                }
+              }
+            } else {
+              float fg[V], fu[V];
+              F::unpack(wg[j], fg);
+              F::unpack(wu[j], fu);
+              float scg = 1.f, scu = 1.f;
+              if (WT == MOE_FP8E4M3_B128) {
+                const int cb = (c * V) >> 7;
+                scg = sgu[(size_t)(i >> 7) * HB + cb];
+                scu = sgu[(size_t)((I + i) >> 7) * HB + cb];
+              }
 #pragma unroll
-                for (int v = 0; v < V; ++v) { dg = fmaf(fg[v], xv[v], dg); du = fmaf(fu[v], xv[v], du); }
-                ag[n] = fmaf(dg, scg, ag[n]);
-                au[n] = fmaf(du, scu, au[n]);
+              for (int n = 0; n < kTokGroup; ++n) {
+                if (n < nt) {
+                  float xv[V];
+                  load_act<AT, V>(a.x, (size_t)tok[n] * H + (size_t)c * V, xv);
+                  float dg = 0.f, du = 0.f;
+#pragma unroll
+                  for (int v = 0; v < V; ++v) { dg = fmaf(fg[v], xv[v], dg); du = fmaf(fu[v], xv[v], du); }
+                  ag[n] = fmaf(dg, scg, ag[n]);
+                  au[n] = fmaf(du, scu, au[n]);
+                }
               }
             }
           }
@@ -429,8 +498,13 @@ fill_gate_up_kernel(GemvArgs a, const int32_t* __restrict__ fills, const uint8_t
 #pragma unroll
       for (int n = 0; n < kTokGroup; ++n) {
         if (n < nt) {
-          const float sg = warp_sum(ag[n]);
-          const float su = warp_sum(au[n]);
+          float sg = warp_sum(ag[n]);
+          float su = warp_sum(au[n]);
+          if constexpr (WT == MOE_NVFP4) {
+            const float gg = *reinterpret_cast<const float*>(sb + F::g_off(H, I));
+            sg *= gg;
+            su *= gg;
+          }
           if (lane == 0) a.b.h[(size_t)a.b.gpu_pairs[tp + n] * I + i] = silu(sg) * su;
         }
       }
@@ -452,9 +526,9 @@ __global__ void __launch_bounds__(kGemvThreads, kTokGroup == 1 ? 2 : 1) down_ker
   const long nwarps = (long)gridDim.x * (blockDim.x >> 5);
   const long wid = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int NCH = I / V;
-  const size_t row_bytes = (size_t)I * F::ES;
-  const size_t down_off = 2ull * (size_t)I * (size_t)H * F::ES;
-  const size_t sd_off = 3ull * (size_t)I * (size_t)H * F::ES + 4ull * (size_t)(2 * I / 128) * (H / 128);
+  const size_t row_bytes = F::row(I);
+  const size_t down_off = 2ull * (size_t)I * F::row(H);
+  const size_t sd_off = F::sd_off(H, I);
   const int IB = I / 128;
   const uint64_t pol = evict_first_policy();
 
@@ -553,9 +627,9 @@ __global__ void __launch_bounds__(kDCWarps * 32) down_combine_kernel(GemvArgs a,
   const int ngpu = a.b.plan[P_NGPU];
   __syncthreads();   // staged plan visible
   const int NCH = I / V;
-  const size_t row_bytes = (size_t)I * F::ES;
-  const size_t down_off = 2ull * (size_t)I * (size_t)H * F::ES;
-  const size_t sd_off = 3ull * (size_t)I * (size_t)H * F::ES + 4ull * (size_t)(2 * I / 128) * (H / 128);
+  const size_t row_bytes = F::row(I);
+  const size_t down_off = 2ull * (size_t)I * F::row(H);
+  const size_t sd_off = F::sd_off(H, I);
   const int IB = I / 128;
   const int nwarps = gridDim.x * kDCWarps;
   const uint64_t pol = evict_first_policy();
@@ -806,7 +880,7 @@ __global__ void __launch_bounds__(256) gate_up_bulk_kernel(GemvArgs a, BulkGeom 
   const long items = (long)ng * I;
   const long nwarps = (long)gridDim.x * geo.NW;
   const long w0 = (long)blockIdx.x * geo.NW + warp;
-  const size_t row_bytes = (size_t)H * F::ES;
+  const size_t row_bytes = F::row(H);
   const uint64_t pol = evict_first_policy();
   long last_issued[4] = {-1, -1, -1, -1};
   auto issue = [&](long it, int st) {   // lane 0 only
@@ -820,7 +894,7 @@ __global__ void __launch_bounds__(256) gate_up_bulk_kernel(GemvArgs a, BulkGeom 
   // W_down of these experts is read by the down grid right after this one: once a
   // warp has issued its last row copy it asks L2 to fetch its share of those bytes
   // (32 KB pieces, piece p to warp p mod warps), so they queue behind the rows.
-  const size_t wd_bytes = (size_t)H * I * F::ES;
+  const size_t wd_bytes = (size_t)H * F::row(I);
   const long pf_per = (long)((wd_bytes + kPrefetchPiece - 1) / kPrefetchPiece);
   auto prefetch_down = [&]() {   // lane 0 only
     for (long p = w0; p < (long)ng * pf_per; p += nwarps) {
@@ -886,23 +960,36 @@ __global__ void __launch_bounds__(256) gate_up_bulk_kernel(GemvArgs a, BulkGeom 
       const int t = sp.tok[tp];
       float ag = 0.f, au = 0.f;
       for (int c = lane; c < NCH; c += 32) {
-        float fg[V], fu[V], xv[V];
-        F::unpack(gate[c], fg);
-        F::unpack(up[c], fu);
-        load_x<AT, V>(xsm, (size_t)t * H + (size_t)c * V, xv);
         float dg = 0.f, du = 0.f;
+        if constexpr (WT == MOE_NVFP4) {
+          float xv[V];
+          load_x<AT, V>(xsm, (size_t)t * H + (size_t)c * V, xv);
+          const uint16_t* srow = reinterpret_cast<const uint16_t*>(sp.w[g] + F::sgu_off(H, I));
+          dg = dot_nvfp4(gate[c], __ldg(srow + (size_t)i * (H / 32) + c), xv);
+          du = dot_nvfp4(up[c], __ldg(srow + (size_t)(I + i) * (H / 32) + c), xv);
+        } else {
+          float fg[V], fu[V], xv[V];
+          F::unpack(gate[c], fg);
+          F::unpack(up[c], fu);
+          load_x<AT, V>(xsm, (size_t)t * H + (size_t)c * V, xv);
 #pragma unroll
-        for (int v = 0; v < V; ++v) { dg = fmaf(fg[v], xv[v], dg); du = fmaf(fu[v], xv[v], du); }
-        if (WT == MOE_FP8E4M3_B128) {
-          const int cb = (c * V) >> 7;
-          dg *= __ldg(sgu + (size_t)(i >> 7) * HB + cb);
-          du *= __ldg(sgu + (size_t)((I + i) >> 7) * HB + cb);
+          for (int v = 0; v < V; ++v) { dg = fmaf(fg[v], xv[v], dg); du = fmaf(fu[v], xv[v], du); }
+          if (WT == MOE_FP8E4M3_B128) {
+            const int cb = (c * V) >> 7;
+            dg *= __ldg(sgu + (size_t)(i >> 7) * HB + cb);
+            du *= __ldg(sgu + (size_t)((I + i) >> 7) * HB + cb);
+          }
         }
         ag += dg;
         au += du;
       }
       ag = warp_sum(ag);
       au = warp_sum(au);
+      if constexpr (WT == MOE_NVFP4) {   // the gate/up matrix's fp32 scale
+        const float gg = __ldg(reinterpret_cast<const float*>(sp.w[g] + F::g_off(H, I)));
+        ag *= gg;
+        au *= gg;
+      }
       if (lane == 0) a.b.h[(size_t)sp.pid[tp] * I + i] = silu(ag) * au;
     }
     __syncwarp();
@@ -995,9 +1082,9 @@ __global__ void __launch_bounds__((kRing && !kPair) ? 256 : 512) down_bulk_kerne
   for (int tp = sp.off[g0] + threadIdx.x; tp < sp.off[g1]; tp += blockDim.x) s_mine[sp.pid[tp]] = 1;
   const int r0 = blockIdx.x * geo.R;
   const int nr = min(geo.R, H - r0);
-  const size_t row_bytes = (size_t)I * F::ES;
-  const size_t down_off = 2ull * (size_t)I * (size_t)H * F::ES;
-  const size_t sd_off = 3ull * (size_t)I * (size_t)H * F::ES + 4ull * (size_t)(2 * I / 128) * (H / 128);
+  const size_t row_bytes = F::row(I);
+  const size_t down_off = 2ull * (size_t)I * F::row(H);
+  const size_t sd_off = F::sd_off(H, I);
   const uint32_t bytes = (uint32_t)(nr * row_bytes);
   const uint64_t pol = evict_first_policy();
   const bool h_copy = geo.h_smem && g1 > g0;
@@ -1047,25 +1134,37 @@ __global__ void __launch_bounds__((kRing && !kPair) ? 256 : 512) down_bulk_kerne
           for (int j = 0; j < J; ++j) {
             const int c = c0 + j * 32 + lane;
             if (c < NCH) {
-              float fw[V];
-              F::unpack(wrow[c], fw);
               const float4* hp = reinterpret_cast<const float4*>(hsrc + (size_t)pid * I + (size_t)c * V);
               float dj = 0.f;
+              if constexpr (WT == MOE_NVFP4) {
+                float hv[V];
 #pragma unroll
-              for (int v = 0; v < V; v += 4) {
-                const float4 q = hp[v / 4];
-                dj = fmaf(fw[v], q.x, dj);
-                dj = fmaf(fw[v + 1], q.y, dj);
-                dj = fmaf(fw[v + 2], q.z, dj);
-                dj = fmaf(fw[v + 3], q.w, dj);
+                for (int v = 0; v < V; v += 4) {
+                  const float4 q = hp[v / 4];
+                  hv[v] = q.x; hv[v + 1] = q.y; hv[v + 2] = q.z; hv[v + 3] = q.w;
+                }
+                const uint16_t* srow = reinterpret_cast<const uint16_t*>(sp.w[g] + sd_off);
+                dj = dot_nvfp4(wrow[c], __ldg(srow + (size_t)(r0 + r) * (I / 32) + c), hv);
+              } else {
+                float fw[V];
+                F::unpack(wrow[c], fw);
+#pragma unroll
+                for (int v = 0; v < V; v += 4) {
+                  const float4 q = hp[v / 4];
+                  dj = fmaf(fw[v], q.x, dj);
+                  dj = fmaf(fw[v + 1], q.y, dj);
+                  dj = fmaf(fw[v + 2], q.z, dj);
+                  dj = fmaf(fw[v + 3], q.w, dj);
+                }
+                if (WT == MOE_FP8E4M3_B128) dj *= __ldg(sd + (size_t)((r0 + r) >> 7) * IB + ((c * V) >> 7));
               }
-              if (WT == MOE_FP8E4M3_B128) dj *= __ldg(sd + (size_t)((r0 + r) >> 7) * IB + ((c * V) >> 7));
               d += dj;
             }
           }
           acc += d;
         }
         acc = warp_sum(acc);
+        if constexpr (WT == MOE_NVFP4) acc *= __ldg(reinterpret_cast<const float*>(sp.w[g] + F::g_off(H, I)) + 1);
         if (lane == 0) {
           ys[(size_t)r * NP + pid] = acc;
           a.b.y[(size_t)pid * H + r0 + r] = acc;
@@ -1146,12 +1245,17 @@ __global__ void __launch_bounds__((kRing && !kPair) ? 256 : 512) down_bulk_kerne
             for (int j = 0; j < J; ++j) {
               const int c = c0 + j * 32 + lane;
               if (c < NCH) {
-                float fw[V];
-                F::unpack(wrow[c], fw);
                 float dj = 0.f;
+                if constexpr (WT == MOE_NVFP4) {
+                  const uint16_t* srow = reinterpret_cast<const uint16_t*>(sp.w[g] + sd_off);
+                  dj = dot_nvfp4(wrow[c], __ldg(srow + (size_t)(r0 + r) * (I / 32) + c), hv[j]);
+                } else {
+                  float fw[V];
+                  F::unpack(wrow[c], fw);
 #pragma unroll
-                for (int v = 0; v < V; ++v) dj = fmaf(fw[v], hv[j][v], dj);
-                if (WT == MOE_FP8E4M3_B128) dj *= __ldg(sd + (size_t)((r0 + r) >> 7) * IB + ((c * V) >> 7));
+                  for (int v = 0; v < V; ++v) dj = fmaf(fw[v], hv[j][v], dj);
+                  if (WT == MOE_FP8E4M3_B128) dj *= __ldg(sd + (size_t)((r0 + r) >> 7) * IB + ((c * V) >> 7));
+                }
                 d += dj;
               }
             }
@@ -1171,6 +1275,7 @@ __global__ void __launch_bounds__((kRing && !kPair) ? 256 : 512) down_bulk_kerne
         r = lane >> 1;
         mine = (lane & 1) == 0;
       }
+      if constexpr (WT == MOE_NVFP4) v *= __ldg(reinterpret_cast<const float*>(sp.w[g] + F::g_off(H, I)) + 1);
       if (mine && r < nr) {
         ys[(size_t)r * NP + pid] = v;
         a.b.y[(size_t)pid * H + r0 + r] = v;   // per-pair output stays readable (moe_cache_get_plan)
@@ -1419,7 +1524,10 @@ cudaError_t setup_gemv_kernels() {
                         (const void*)down_bulk_kernel<MOE_BF16, true, 4, true>,
                         (const void*)down_bulk_kernel<MOE_FP8E4M3_B128, true, 0>,
                         (const void*)down_bulk_kernel<MOE_F32, false, 0>, (const void*)down_bulk_kernel<MOE_BF16, false, 0>,
-                        (const void*)down_bulk_kernel<MOE_FP8E4M3_B128, false, 0>}) {
+                        (const void*)down_bulk_kernel<MOE_FP8E4M3_B128, false, 0>,
+                        (const void*)down_bulk_kernel<MOE_NVFP4, true, 0>, (const void*)down_bulk_kernel<MOE_NVFP4, false, 0>,
+                        (const void*)gate_up_bulk_kernel<MOE_NVFP4, MOE_F32, 0>,
+                        (const void*)gate_up_bulk_kernel<MOE_NVFP4, MOE_BF16, 0>}) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kBulkSmemAttr);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, kDecodeCarveout);
     if (e != cudaSuccess) return e;
@@ -1465,11 +1573,18 @@ cudaError_t launch_fill_gate_up(const Shape& sh, int T, const void* x, DecodeBuf
       return launch_fill_gate_up_typed<MOE_FP8E4M3_B128, MOE_F32>(a, f, host_pool_dev, offsets, slots, sh.S, n_ctas, s);
     case MOE_FP8E4M3_B128 * 2 + MOE_BF16:
       return launch_fill_gate_up_typed<MOE_FP8E4M3_B128, MOE_BF16>(a, f, host_pool_dev, offsets, slots, sh.S, n_ctas, s);
+    case MOE_NVFP4 * 2 + MOE_F32:
+      return launch_fill_gate_up_typed<MOE_NVFP4, MOE_F32>(a, f, host_pool_dev, offsets, slots, sh.S, n_ctas, s);
+    case MOE_NVFP4 * 2 + MOE_BF16:
+      return launch_fill_gate_up_typed<MOE_NVFP4, MOE_BF16>(a, f, host_pool_dev, offsets, slots, sh.S, n_ctas, s);
   }
   return cudaErrorInvalidValue;
 }
 
-int wbytes(int wdtype) { return wdtype == MOE_F32 ? 4 : wdtype == MOE_BF16 ? 2 : 1; }
+// bytes of n weight elements
+size_t wrow(int wdtype, size_t n) {
+  return wdtype == MOE_F32 ? 4 * n : wdtype == MOE_BF16 ? 2 * n : wdtype == MOE_NVFP4 ? n / 2 : n;
+}
 size_t up128(size_t x) { return (x + 127) & ~size_t(127); }
 
 // Ring geometry and shared-memory layout of the bulk-streamed kernels; NS = 0
@@ -1482,7 +1597,7 @@ constexpr size_t kRingBudget = 220 * 1024;
 BulkGeom gate_up_geom(const GemvArgs& a, int wdtype, int adtype, int sms) {
   BulkGeom g{};
   g.grid = sms;
-  const size_t row = (size_t)a.H * wbytes(wdtype);
+  const size_t row = wrow(wdtype, (size_t)a.H);
   const size_t xbytes = (size_t)a.T * a.H * (adtype == MOE_F32 ? 4 : 2);
   const size_t plan = up128(staged_plan_bytes(a.max_g, a.max_p));
   g.SB = up128(2 * row);
@@ -1506,7 +1621,7 @@ BulkGeom gate_up_geom(const GemvArgs& a, int wdtype, int adtype, int sms) {
 // four warps; fewer rows per CTA when that does not fit.
 BulkGeom down_geom(const GemvArgs& a, int wdtype, int sms) {
   BulkGeom g{};
-  const size_t row = (size_t)a.I * wbytes(wdtype);
+  const size_t row = wrow(wdtype, (size_t)a.I);
   const size_t np = (size_t)(a.P + a.T * a.n_shared);
   const size_t hbytes = np * a.I * 4;
   const size_t plan = up128(staged_plan_bytes(a.max_g, a.max_p));
@@ -1564,10 +1679,12 @@ cudaError_t launch_gate_up(const Shape& sh, int pass, int T, const void* x, Deco
         case MOE_BF16 * 2 + MOE_BF16: return launch_gate_up_bulk<MOE_BF16, MOE_BF16>(a, geo, err, s);
         case MOE_FP8E4M3_B128 * 2 + MOE_F32: return launch_gate_up_bulk<MOE_FP8E4M3_B128, MOE_F32>(a, geo, err, s);
         case MOE_FP8E4M3_B128 * 2 + MOE_BF16: return launch_gate_up_bulk<MOE_FP8E4M3_B128, MOE_BF16>(a, geo, err, s);
+        case MOE_NVFP4 * 2 + MOE_F32: return launch_gate_up_bulk<MOE_NVFP4, MOE_F32>(a, geo, err, s);
+        case MOE_NVFP4 * 2 + MOE_BF16: return launch_gate_up_bulk<MOE_NVFP4, MOE_BF16>(a, geo, err, s);
       }
     }
   }
-  switch (sh.wdtype * 2 + sh.adtype) {
+  switch (sh.wdtype * 2 + sh.adtype) {   // register-staged kernels (no NVFP4: the create call rules it out)
     case MOE_F32 * 2 + MOE_F32: return launch_gate_up_typed<MOE_F32, MOE_F32>(a, sms, s);
     case MOE_F32 * 2 + MOE_BF16: return launch_gate_up_typed<MOE_F32, MOE_BF16>(a, sms, s);
     case MOE_BF16 * 2 + MOE_F32: return launch_gate_up_typed<MOE_BF16, MOE_F32>(a, sms, s);
@@ -1625,7 +1742,16 @@ cudaError_t launch_down_bulk_any(const Shape& sh, const GemvArgs& a, const BulkG
                                  const float* w, const float* cpu, float* out, uint32_t* err, cudaStream_t s) {
   if (sh.wdtype == MOE_F32) return launch_down_bulk<MOE_F32>(a, geo, ring, pdl, w, cpu, out, err, s);
   if (sh.wdtype == MOE_BF16) return launch_down_bulk<MOE_BF16>(a, geo, ring, pdl, w, cpu, out, err, s);
+  if (sh.wdtype == MOE_NVFP4) return launch_down_bulk<MOE_NVFP4>(a, geo, ring, pdl, w, cpu, out, err, s);
   return launch_down_bulk<MOE_FP8E4M3_B128>(a, geo, ring, pdl, w, cpu, out, err, s);
+}
+
+bool nvfp4_decode_fits(const Shape& sh, int max_tokens, int sms) {
+  for (int T = 1; T <= max_tokens; ++T) {
+    const GemvArgs a = make_args(sh, 0, T, nullptr, DecodeBufs{});
+    if (gate_up_geom(a, sh.wdtype, sh.adtype, sms).NS < 2 || !down_split_ok(sh, T, sms)) return false;
+  }
+  return true;
 }
 
 // The bulk down kernel runs when its ring fits and every pair's h fits in
@@ -1652,6 +1778,7 @@ cudaError_t launch_down_combine(const Shape& sh, int T, const float* w, const fl
     const BulkGeom geo = down_geom(a, sh.wdtype, sms);
     if (geo.NS >= 1 && geo.h_smem) return launch_down_bulk_any(sh, a, geo, true, true, w, cpu_part, out, err, s);
   }
+  if (sh.wdtype == MOE_NVFP4) return cudaErrorInvalidValue;   // bulk kernels only (checked at create)
   if (down_combine_fits(sh, T)) {
     const GemvArgs a = make_args(sh, 2, T, nullptr, b);
     if (sh.wdtype == MOE_F32) return launch_down_combine_typed<MOE_F32>(a, w, cpu_part, out, err, sms, s);

@@ -248,3 +248,64 @@ def test_varying_T_on_one_cache():
             assert np.array_equal(sm.cpu().numpy(), plan.slot_map)
             assert relative_max_error(out.cpu().numpy(), ref) <= TOL
     cache.close()
+
+
+# ---- NVFP4 experts (e2m1 codes, e4m3 scales per 16 row elements, fp32 per matrix) ----
+
+def test_nvfp4_small_decode_two_tokens():
+    from workloads import Config, Shape
+    cfg = Config("nvfp4_small", Shape(L=3, E=24, k=4, H=256, I=128, wdtype="nvfp4", adtype="bf16"), T=2, steps=24,
+                 capacity=20, routing="softmax", seed=95)
+    res = run_decode_parity(cfg, (1000, 0), fp_every=1)
+    _ok(res)
+    assert res.fills > 0 and res.fp_checked == 24 * 3
+
+
+def test_nvfp4_qwen3_shape_batch1():
+    cfg = config("qwen3_decode_b1")
+    cfg = cfg.with_(shape=cfg.shape.__class__(**{**cfg.shape.__dict__, "wdtype": "nvfp4"}), steps=24)
+    res = run_decode_parity(cfg, (200000, 0), n_phys=24, fp_every=37, state_every=8)
+    _ok(res)
+    assert res.calls == 24 * 48 and res.fp_checked >= 20
+
+
+def test_nvfp4_split_merges_exactly():
+    # resident and filled experts give the same y bits, so CPU partials equal to the
+    # GPU's own values merge into a bit-identical output (see test_exact_merge_...)
+    import torch
+    from workloads import Config, Shape
+    cfg = Config("nvfp4_merge", Shape(L=1, E=8, k=2, H=256, I=128, wdtype="nvfp4", adtype="bf16"), T=2, steps=1,
+                 capacity=8, routing="softmax", seed=96)
+    s = cfg.shape
+    arena, offs, pool = build_pool(cfg)
+    dev = torch.device("cuda", 0)
+    ids, w = routing_trace(cfg)
+    x = torch_act(activations(cfg, 0, 0), dev)
+    i_d, w_d = torch.from_numpy(ids[0, 0]).to(dev), torch.from_numpy(w[0, 0]).to(dev)
+    big, _ = make_cache(cfg, pool, offs, None, (1000, 0), n_slots=8)
+    out_all = torch.empty(cfg.T, s.H, device=dev)
+    big.decode(0, x, i_d, w_d, out_all)                 # fills every expert
+    big.decode(0, x, i_d, w_d, out_all)                 # every expert resident now
+    y_all = big.plan(T=cfg.T)["y"]
+    small, _ = make_cache(cfg.with_(max_fetch=1), pool, offs, None, (100, 900), n_slots=2)
+    sm = torch.empty(cfg.T, s.k, dtype=torch.int32, device=dev)
+    out_split = torch.empty(cfg.T, s.H, device=dev)
+    small.decode(0, x, i_d, w_d, out_split, cpu_part=torch.from_numpy(y_all).to(dev), slot_map=sm)
+    torch.cuda.synchronize()
+    assert (sm < 0).any()
+    assert torch.equal(out_split, out_all)
+    big.close()
+    small.close()
+
+
+def test_nvfp4_rejects_larger_batches_and_prefill():
+    import torch
+    from serving_layer_moe_gb300 import MoECache, MoEError
+    from workloads import Shape
+    s = Shape(L=1, E=8, k=2, H=256, I=128, wdtype="nvfp4", adtype="bf16")
+    pool = torch.zeros(8 * s.blob_bytes, dtype=torch.uint8).pin_memory()
+    for kw in ({"max_tokens": 4}, {"max_tokens": 1, "max_prefill_tokens": 64}):
+        with pytest.raises(MoEError) as ei:
+            MoECache(L=1, E=8, H=256, I=128, top_k=2, wdtype="nvfp4", adtype="bf16", host_pool=pool, n_slots=4,
+                     bw_pcie_mbps=1000, bw_cpu_mbps=0, **kw)
+        assert ei.value.status == 1

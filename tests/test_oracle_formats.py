@@ -90,3 +90,53 @@ def test_parse_blob_roundtrip(wdtype):
     assert np.allclose(wg, gu[:128], rtol=rel, atol=1e-3 * (wdtype == "fp8"))
     assert np.allclose(wu, gu[128:], rtol=rel, atol=1e-3 * (wdtype == "fp8"))
     assert np.allclose(wd, d, rtol=rel, atol=1e-3 * (wdtype == "fp8"))
+
+
+# ---- NVFP4: e2m1 elements, e4m3 scales per 16 row elements, fp32 per matrix ----
+
+def test_e2m1_closed_form_values():
+    from oracle.formats import E2M1_TABLE
+    # bit 3 sign, bits 2-1 exponent (bias 1), bit 0 mantissa
+    assert list(E2M1_TABLE[:8]) == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    assert list(E2M1_TABLE[8:]) == [-0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]
+    assert np.signbit(E2M1_TABLE[8])
+
+
+def test_generator_e2m1_encoder_nearest_ties_to_even_saturating():
+    from oracle.formats import E2M1_TABLE
+    from workloads import f32_to_e2m1_codes
+    mags = E2M1_TABLE[:8]
+    grid = np.concatenate([np.arange(0, 8.0, 1 / 64.0), mags, (mags[1:] + mags[:-1]) / 2, [6.0, 6.5, 100.0]])
+    x = np.concatenate([grid, -grid]).astype(np.float32)
+    codes = f32_to_e2m1_codes(x)
+    for v, c in zip(x, codes):
+        d = np.abs(mags - abs(float(v)))
+        best = np.flatnonzero(d == d.min())
+        want = best[0] if len(best) == 1 else [b for b in best if b % 2 == 0][0]   # ties: even code
+        if abs(v) > 6.0:
+            want = 7                                                             # saturate
+        assert (c & 7) == want, (v, c, want)
+        assert (c >> 3) == (1 if np.signbit(v) else 0)
+
+
+def test_nvfp4_blob_dequantises_within_one_block_step():
+    # each element is within one step (decoded block scale x g) of the float32 draw
+    from oracle.formats import E4M3_TABLE, parse_blob
+    from workloads import WEIGHT_STD, _rng
+    s = Shape(L=1, E=4, k=1, H=128, I=64, wdtype="nvfp4", adtype="bf16")
+    for idx in range(3):
+        blob = make_blob(s, 77, idx)
+        g = _rng(77, 0xB10B, idx)
+        w_gu = g.standard_normal((2 * s.I, s.H), dtype=np.float32) * np.float32(WEIGHT_STD)
+        w_d = g.standard_normal((s.H, s.I), dtype=np.float32) * np.float32(WEIGHT_STD)
+        gate, up, down = parse_blob(blob, "nvfp4", s.H, s.I)
+        o = 3 * s.I * s.H // 2
+        s_gu = blob[o:o + 2 * s.I * s.H // 16].reshape(2 * s.I, s.H // 16)
+        s_d = blob[o + 2 * s.I * s.H // 16:o + 3 * s.I * s.H // 16].reshape(s.H, s.I // 16)
+        gg = blob[-16:].view(np.float32)
+        for w, deq, sc, gm in ((w_gu, np.vstack([gate, up]), s_gu, gg[0]), (w_d, down, s_d, gg[1])):
+            step = np.repeat(E4M3_TABLE[sc], 16, axis=1) * float(gm)
+            err = np.abs(deq - w.astype(np.float64))
+            assert np.all(err <= step + 1e-12)
+            assert np.mean(err) < 0.1 * np.mean(np.abs(w))        # not a constant or a dropped factor
+            assert gm == np.float32(np.abs(w).max() / (6.0 * 448.0))

@@ -17,6 +17,13 @@ decision one: the slot is a complete expert):
       W_gu  [2I, H] e4m3 codes, W_d [H, I] e4m3 codes,
       s_gu  [2I/128, H/128] fp32, s_d [H/128, I/128] fp32
       (dequantised value = e4m3(code) * scale of the 128x128 block)
+  nvfp4 (e2m1 codes, one e4m3 scale per 16 consecutive elements of a row, one
+  fp32 scale per matrix):
+      W_gu  [2I, H/2] bytes, W_d [H, I/2] bytes (element 2j in the low nibble
+      of byte j, element 2j+1 in the high nibble),
+      s_gu  [2I, H/16] e4m3 codes, s_d [H, I/16] e4m3 codes,
+      g     [4] fp32 = (g_gu, g_d, 0, 0)
+      (dequantised value = e2m1(code) * e4m3(block scale) * g of the matrix)
 
 bf16 values are carried as uint16 bit patterns, e4m3 as uint8 codes.
 
@@ -32,7 +39,7 @@ import numpy as np
 
 __all__ = [
     "Shape", "Config", "CONFIGS", "config", "blob_bytes", "f32_to_bf16_bits",
-    "f32_to_e4m3_codes", "make_blob", "make_pool", "make_shared",
+    "f32_to_e4m3_codes", "f32_to_e2m1_codes", "make_blob", "make_pool", "make_shared",
     "routing_trace", "prefill_routing", "activations", "default_max_fetch",
 ]
 
@@ -48,7 +55,7 @@ class Shape:
     k: int          # top-k
     H: int          # hidden size
     I: int          # expert (SwiGLU) intermediate size
-    wdtype: str     # 'f32' | 'bf16' | 'fp8'
+    wdtype: str     # 'f32' | 'bf16' | 'fp8' | 'nvfp4'
     adtype: str     # 'f32' | 'bf16'   activation dtype
     n_shared: int = 0   # always-resident shared expert per layer (0 or 1)
 
@@ -92,6 +99,9 @@ def blob_bytes(s: Shape) -> int:
         assert s.H % 128 == 0 and s.I % 128 == 0
         n_scales = (2 * s.I // 128) * (s.H // 128) + (s.H // 128) * (s.I // 128)
         return 3 * s.I * s.H + 4 * n_scales
+    if s.wdtype == "nvfp4":
+        assert s.H % 32 == 0 and s.I % 32 == 0
+        return 3 * s.I * s.H // 2 + 3 * s.I * s.H // 16 + 16
     raise ValueError(s.wdtype)
 
 
@@ -173,6 +183,45 @@ def f32_to_e4m3_codes(a: np.ndarray) -> np.ndarray:
     return out
 
 
+_E2M1_MIDPOINTS = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], np.float32)
+
+
+def f32_to_e2m1_codes(a: np.ndarray) -> np.ndarray:
+    """Encode float32 as FP4 E2M1 codes (bit 3 sign, magnitudes 0, 0.5, 1, 1.5, 2, 3,
+    4, 6 for codes 0..7): nearest, ties to the even code, saturating at +-6."""
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    mag = np.abs(a)
+    idx = np.searchsorted(_E2M1_MIDPOINTS, mag, side="left")      # midpoints strictly below |a|
+    tie = mag == _E2M1_MIDPOINTS[np.minimum(idx, 6)]
+    code = (idx + (tie & (idx % 2 == 1))).astype(np.uint8)
+    code |= (np.signbit(a).astype(np.uint8) << 3)
+    return code
+
+
+def _nvfp4(w: np.ndarray):
+    """NVFP4 quantisation of one matrix [R, C]: global g = amax / (6 * 448); block
+    scale (16 consecutive row elements) = e4m3 code of amax_b / 6 / g; element code =
+    e2m1 of w / (decoded block scale * g).  Returns packed codes [R, C/2], scale codes
+    [R, C/16] and g."""
+    R, C = w.shape
+    amax = float(np.abs(w).max())
+    g = np.float32(amax / (6.0 * 448.0)) if amax > 0 else np.float32(1.0)
+    blk = w.reshape(R, C // 16, 16)
+    bmax = np.abs(blk).max(axis=2).astype(np.float32)
+    sc = f32_to_e4m3_codes((bmax / np.float32(6.0) / g).astype(np.float32))
+    # decoded block scale (e4m3 is exact in float32), times g
+    e = ((sc >> 3) & 0xF).astype(np.int32)
+    m = (sc & 0x7).astype(np.float32)
+    dec = np.where(e == 0, m / np.float32(8.0) * np.float32(2.0 ** -6),
+                   (np.float32(1.0) + m / np.float32(8.0)) * np.ldexp(np.float32(1.0), e - 7)).astype(np.float32)
+    step = (dec * g).astype(np.float32)
+    q = np.where(step[:, :, None] > 0, blk / np.where(step > 0, step, np.float32(1.0))[:, :, None],
+                 np.float32(0.0)).astype(np.float32)
+    codes = f32_to_e2m1_codes(q).reshape(R, C)
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    return packed, sc, g
+
+
 # ----------------------------------------------------------------------------
 # expert blobs and the host pool
 # ----------------------------------------------------------------------------
@@ -184,7 +233,7 @@ def make_blob(shape: Shape, seed: int, index: int, tag: int = 0xB10B) -> np.ndar
 
     Weights ~ N(0, 0.02) drawn in float32, then stored in the shape's weight
     dtype (bf16: nearest-even; fp8: per-128x128-block scale = amax/448 and
-    e4m3 codes of value/scale).
+    e4m3 codes of value/scale; nvfp4: see _nvfp4).
     """
     H, I = shape.H, shape.I
     g = _rng(seed, tag, index)
@@ -200,6 +249,11 @@ def make_blob(shape: Shape, seed: int, index: int, tag: int = 0xB10B) -> np.ndar
         codes_d, s_d = _blockscale_e4m3(w_d)
         parts = [codes_gu.ravel(), codes_d.ravel(),
                  s_gu.view(np.uint8).ravel(), s_d.view(np.uint8).ravel()]
+    elif shape.wdtype == "nvfp4":
+        p_gu, s_gu, g_gu = _nvfp4(w_gu)
+        p_d, s_d, g_d = _nvfp4(w_d)
+        parts = [p_gu.ravel(), p_d.ravel(), s_gu.ravel(), s_d.ravel(),
+                 np.array([g_gu, g_d, 0, 0], np.float32).view(np.uint8)]
     else:
         raise ValueError(shape.wdtype)
     blob = np.concatenate(parts)
