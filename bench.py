@@ -59,6 +59,7 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the oracle CPU baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-prefill", action="store_true")
+    p.add_argument("--no-nvfp4", action="store_true", help="skip the NVFP4-expert variant of the decode workload")
     p.add_argument("--mode", default="all", choices=["all", "decode", "prefill", "profile-decode"],
                    help="prefill: only the prefill measurement (small profiling runs)")
     p.add_argument("--prefill-tokens", type=int, default=8192)
@@ -469,6 +470,9 @@ def main(args):
         "control_us": round(1e3 * prof["control"][0] / max(1, prof["control"][1]), 2),
         "clocks": clk.summary(),
     }
+    if args.mode == "all" and not args.no_nvfp4:
+        cache.close()
+        result["nvfp4_decode"] = nvfp4_measure(args, dev, local, b_pcie, b_cpu)
     if not args.no_prefill and args.mode == "all":
         result["prefill"] = prefill_measure(args, dev, local)
     if rank == 0 and not args.no_cpu_baseline:
@@ -506,6 +510,70 @@ def profile_case(args, dev):
     print(json.dumps({"profile_case": f"{WORKLOAD} shape, {s.L} layers, {int(cache.info()[1])} slots",
                       "hits": int(c[0]), "misses": int(c[1]), "fills": int(c[2])}))
     cache.close()
+
+
+def nvfp4_measure(args, dev, local, b_pcie, b_cpu, steps=64, warmup=8):
+    """The decode workload with NVFP4 experts (same shape, routing and slot count):
+    a blob is 2.66 MB instead of 9.44 MB, so fills and the resident GEMVs move
+    about 3.5x fewer bytes.  Graph replay of whole steps, inputs resident."""
+    import torch
+    from serving_layer_moe_gb300 import MoECache
+    base = config(WORKLOAD)
+    cfg = base.with_(shape=base.shape.__class__(**{**base.shape.__dict__, "wdtype": "nvfp4"}))
+    s = cfg.shape
+    arena, offs = make_pool(s, cfg.seed, n_phys=args.pool_blobs)
+    pool = torch.from_numpy(arena).pin_memory()
+    del arena
+    K = default_max_fetch(s, cfg.T)
+    cache = MoECache(L=s.L, E=s.E, H=s.H, I=s.I, top_k=s.k, max_tokens=cfg.T, wdtype=s.wdtype, adtype=s.adtype,
+                     host_pool=pool, blob_offsets=offs, n_slots=cfg.capacity, max_fetch=K, bw_pcie_mbps=b_pcie,
+                     bw_cpu_mbps=b_cpu, device=local)
+    ids, w = routing_trace(cfg)
+    xs = np.stack([np.stack([activations(cfg, st, l) for l in range(s.L)]) for st in range(cfg.steps)])
+    x_all = torch.from_numpy(xs.view(np.int16)).to(dev)
+    ids_all = torch.from_numpy(ids).to(dev)
+    w_all = torch.from_numpy(w).to(dev)
+    xb, ib, wb = torch.empty_like(x_all[0]), torch.empty_like(ids_all[0]), torch.empty_like(w_all[0])
+    out = torch.empty(s.L, cfg.T, s.H, dtype=torch.float32, device=dev)
+    cpu_part = torch.zeros(cfg.T, s.k, s.H, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    sp = stream.cuda_stream
+
+    def enqueue_step():
+        for l in range(s.L):
+            cache.decode_ptrs(l, cfg.T, xb[l].data_ptr(), ib[l].data_ptr(), wb[l].data_ptr(), cpu_part.data_ptr(),
+                              out[l].data_ptr(), None, sp)
+
+    def stage(st):
+        xb.copy_(x_all[st % cfg.steps], non_blocking=True)
+        ib.copy_(ids_all[st % cfg.steps], non_blocking=True)
+        wb.copy_(w_all[st % cfg.steps], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for st in range(warmup):
+            stage(st)
+            enqueue_step()
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        enqueue_step()
+    torch.cuda.synchronize(dev)
+    cnt0 = cache.state()[3].copy()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for st in range(warmup, warmup + steps):
+            stage(st)
+            graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1)
+    cnt1 = cache.state()[3].copy()
+    cache.close()
+    return {"workload": f"{WORKLOAD} with NVFP4 experts (e2m1 + e4m3 per 16 + fp32 per matrix), C={cfg.capacity} slots",
+            "value": round(steps * s.L / (ms / 1e3), 1), "unit": UNIT, "steps": steps,
+            "ms_per_step": round(ms / steps, 4), "blob_bytes": int(s.blob_bytes),
+            "fills": int(cnt1[2] - cnt0[2]), "hits": int(cnt1[0] - cnt0[0])}
 
 
 def prefill_measure(args, dev, local):
