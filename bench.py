@@ -46,6 +46,9 @@ TRAFFIC_PER_LAYER_STEP = 75_200_000
 TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of the gate/up and down grids of one "
                   "layer-step, mean of 4 all-resident layer-steps of bench.py --mode profile-decode "
                   "(16-layer qwen3 b1 shape, 8 resident experts per layer); profiles/decode_gemv_pair_qwen3_b1.md")
+# the same for the one-grid resident kernel (None until an ncu capture of it is summarised)
+FLOW_TRAFFIC_PER_LAYER_STEP = None
+FLOW_TRAFFIC_SOURCE = None
 
 
 def parse_args(argv=None):
@@ -287,9 +290,11 @@ def main(args):
             enqueue_step()
         torch.cuda.synchronize(dev)
 
-    # control, fill (+ the filled experts' gate/up), the filled experts' down grid,
-    # the resident gate/up grid, the resident down + combine grid
-    launches_per_layer = 5
+    # control, fill (+ the filled experts' gate/up), the filled experts' down grid and
+    # the resident experts' gate/up grid and down + combine grid (one grid with
+    # MOE_DECODE_ONE_GRID=1), as the library reports
+    launches_per_layer = int(cache.info()[6])
+    one_grid = launches_per_layer == 4
     # ---- timed region: inputs resident in HBM ---------------------------------
     cnt0 = cache.state()[3].copy()
     if world > 1:
@@ -446,19 +451,22 @@ def main(args):
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": args.steps * s.L * launches_per_layer,
         "roofline": {"bound": "hbm",
-                     "kernel": "resident-expert GEMV pair per layer-step: gate/up grid (with the L2 fetch of W_down) "
-                               "+ down-projection grid fused with the combine; one step replayed with every routed "
-                               "expert resident, event pairs around the two grids",
+                     "kernel": ("resident-expert SwiGLU per layer-step, one grid (gate/up warps beside down warps, "
+                                "fused with the combine); one step replayed with every routed expert resident, an "
+                                "event pair around the grid") if one_grid else
+                               ("resident-expert GEMV pair per layer-step: gate/up grid (with the L2 fetch of W_down) "
+                                "+ down-projection grid fused with the combine; one step replayed with every routed "
+                                "expert resident, event pairs around the two grids"),
                      "achieved": round(res_gbs, 1) if res_gbs else None, "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(res_gbs / hbm_peak, 3) if res_gbs else None, "peak_source": peak_src,
-                     "traffic": TRAFFIC_PER_LAYER_STEP,
-                     "traffic_source": TRAFFIC_SOURCE,
+                     "traffic": FLOW_TRAFFIC_PER_LAYER_STEP if one_grid else TRAFFIC_PER_LAYER_STEP,
+                     "traffic_source": FLOW_TRAFFIC_SOURCE if one_grid else TRAFFIC_SOURCE,
                      "bytes_per_layer_step": round(res_bytes / max(1, res_launches)),
                      "us_per_layer_step": round(1e3 * res_ms / max(1, res_launches), 2),
                      "layer_steps_timed": res_launches, "fills_during": res_fills,
                      "all_resident_layer_us": round(1e3 * ms_res / (res_reps * s.L), 2)},
-        "in_step_gemv": {"note": "the same two grids inside the timed step's mix (fills beside them; the event "
-                                 "pairs in the graph also drop their programmatic overlap)",
+        "in_step_gemv": {"note": "the same resident-expert kernels inside the timed step's mix (fills beside "
+                                 "them; the event pairs in the graph also drop their programmatic overlap)",
                          "achieved_gbs": round(gemv_bytes / (gemv_ms / 1e3) / 1e9, 1) if gemv_ms > 0 else None,
                          "bytes_per_layer_step": round(gemv_bytes / max(1, gemv_launches)),
                          "us_per_layer_step": round(1e3 * gemv_ms / max(1, gemv_launches), 2)},

@@ -155,6 +155,10 @@ moe_status moe_cache_resize(moe_cache* cache, uint64_t n_slots);
  *   out_dev      [T, H] fp32: sum_j w[t,j] * y[t,j] in j order (+ shared expert)
  *   slot_map_dev [T, k] int32 out, may be NULL: the slot each pair ran from, -1 = CPU
  * Errors: MOE_EINVAL, MOE_EDEVICE (earlier violation), MOE_ECUDA.
+ * The resident experts run as a gate/up grid then a down + combine grid.  With
+ * the environment variable MOE_DECODE_ONE_GRID=1 set when the cache is created,
+ * bf16 caches of up to 2 tokens per call run them as one grid instead (same
+ * outputs bit for bit).
  */
 moe_status moe_layer_decode(moe_cache* cache, int32_t layer, int32_t T, const void* x_dev,
                             const int32_t* topk_ids_dev, const float* topk_w_dev,
@@ -201,7 +205,8 @@ moe_status moe_cache_get_plan(moe_cache* cache, int32_t* scalars_host, int32_t* 
 
 /*
  * Sizes of a cache: info_host[8] uint64: slot bytes S, slots C, K, L*E,
- * device bytes held, host pool bytes, 0, 0.
+ * device bytes held, host pool bytes, kernel launches of one decode call of
+ * max_tokens tokens, 0.
  */
 moe_status moe_cache_info(moe_cache* cache, uint64_t* info_host);
 

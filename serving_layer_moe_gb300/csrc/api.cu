@@ -17,6 +17,7 @@
 
 #include <algorithm>
 #include <cstdarg>
+#include <cstdlib>
 #include <cstdio>
 #include <cstring>
 #include <string>
@@ -50,6 +51,8 @@ moe_status fail(moe_status st, const char* fmt, ...) {
 
 
 #include "cache.cuh"
+
+#include <cstdlib>
 
 static moe_status check_err_word(moe_cache* c) {
   const uint32_t e = *reinterpret_cast<volatile uint32_t*>(c->err_host);
@@ -163,6 +166,13 @@ extern "C" moe_status moe_cache_create(const moe_config* cfg, const void* host_p
   c->sms = prop.multiProcessorCount;
   c->gemv_grid = 2 * c->sms;
   c->fill_ctas = c->sms / 2;
+  {
+    // The resident experts of a decode call run as two grids (gate/up, then down +
+    // combine).  MOE_DECODE_ONE_GRID=1 selects the one-grid kernel instead where
+    // the shape allows: faster as a kernel, slightly slower as a whole layer-step.
+    const char* ev = getenv("MOE_DECODE_ONE_GRID");
+    c->flow = ev && ev[0] == '1';
+  }
   if (k.wdtype == MOE_NVFP4 && !nvfp4_decode_fits(c->sh, k.max_tokens, c->sms))
     return bail(fail(MOE_EINVAL, "nvfp4 weights: H / I too large for the bulk decode kernels"));
 
@@ -224,9 +234,12 @@ extern "C" moe_status moe_cache_create(const moe_config* cfg, const void* host_p
                  o_sm = take((size_t)k.max_tokens * k.top_k * 4), o_goff = take((size_t)(max_gpu + 1) * 4),
                  o_gp = take(max_pairs * 4), o_gw = take((size_t)max_gpu * 8),
                  o_h = take(max_pairs * k.inter * 4), o_y = take(max_pairs * k.hidden * 4),
-                 o_arr = take((size_t)k.hidden * 4);
+                 o_arr = take((size_t)k.hidden * 4),
+                 o_flow = take(((size_t)kFlowSlices * max_gpu + 1) * kFlowStride * 4),
+                 o_fh = take(2 * max_pairs * k.inter * 4);
     CKB(cudaMalloc(&c->work, off));
     CKB(cudaMemset(c->work, 0, off));
+    CKB(cudaMemset(static_cast<uint8_t*>(c->work) + o_fh, 0xff, 2 * max_pairs * k.inter * 4));   // sentinel
     uint8_t* w = static_cast<uint8_t*>(c->work);
     c->b.plan = reinterpret_cast<int32_t*>(w + o_plan);
     c->b.victims = reinterpret_cast<int32_t*>(w + o_vict);
@@ -239,6 +252,9 @@ extern "C" moe_status moe_cache_create(const moe_config* cfg, const void* host_p
     c->b.h = reinterpret_cast<float*>(w + o_h);
     c->b.y = reinterpret_cast<float*>(w + o_y);
     c->b.arrive = reinterpret_cast<uint32_t*>(w + o_arr);
+    c->b.flow = reinterpret_cast<uint32_t*>(w + o_flow);
+    c->b.flow_h = reinterpret_cast<float*>(w + o_fh);
+    c->b.flow_pairs = (int)max_pairs;
     c->dev_bytes = off;
   }
   c->dev_bytes += c->C * S + nflat * 12 + c->C * 12 + (k.n_shared ? (uint64_t)k.n_layers * S : 0);
@@ -290,10 +306,12 @@ extern "C" moe_status moe_layer_decode(moe_cache* c, int32_t layer, int32_t T, c
   DeviceGuard guard(c->cfg.device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   c->last_T = T;
+  const bool split = down_split_ok(c->sh, T, c->sms);
+  const bool one_grid = split && c->flow && resident_flow_ok(c->sh, T, c->sms);
   {
     ProfScope p(c, s, PROF_CONTROL);
     CK(launch_decode_control(c->sh, layer, T, (int)c->C, c->K, c->cfg.bw_pcie_mbps, c->cfg.bw_cpu_mbps, ids,
-                             c->tab, c->b, slot_map, c->slots, c->shared, c->err_dev, s));
+                             c->tab, c->b, slot_map, c->slots, c->shared, c->err_dev, one_grid, s));
   }
   CK(cudaEventRecord(c->ev_ctrl, s));
   CK(cudaStreamWaitEvent(c->fill_stream, c->ev_ctrl, 0));
@@ -302,18 +320,24 @@ extern "C" moe_status moe_layer_decode(moe_cache* c, int32_t layer, int32_t T, c
     ProfScope p(c, c->fill_stream, PROF_FILL);
     CK(launch_fill_gate_up(c->sh, T, x, c->b, c->host_pool_dev, c->offsets, c->slots, c->fill_ctas, c->fill_stream));
   }
-  const bool split = down_split_ok(c->sh, T, c->sms);
   if (split) {
+    // Beside the one-grid resident kernel, whose CTAs wait on one another, the
+    // filled-expert grid is a plain launch: launched early, its CTAs would sit on
+    // SMs for the whole fill and could keep some of the one-grid CTAs off the GPU.
     ProfScope p(c, c->fill_stream, PROF_DOWN_FILLED);
-    CK(launch_down_split(c->sh, 1, T, w, cpu_part, c->b, out, c->err_dev, c->sms, c->fill_stream));
+    CK(launch_down_split(c->sh, 1, T, w, cpu_part, c->b, out, c->err_dev, c->sms, c->fill_stream, !one_grid));
   }
   CK(cudaEventRecord(c->ev_fill, c->fill_stream));
   if (split) {
     {
       // one timed group: the two grids run back to back under a programmatic dependency
       ProfScope p(c, s, PROF_GEMV_RESIDENT);
-      CK(launch_gate_up(c->sh, 0, T, x, c->b, c->sms, s, c->err_dev));
-      CK(launch_down_split(c->sh, 0, T, w, cpu_part, c->b, out, c->err_dev, c->sms, s));
+      if (one_grid) {
+        CK(launch_resident_flow(c->sh, T, x, w, cpu_part, c->b, out, c->err_dev, c->sms, s));
+      } else {
+        CK(launch_gate_up(c->sh, 0, T, x, c->b, c->sms, s, c->err_dev));
+        CK(launch_down_split(c->sh, 0, T, w, cpu_part, c->b, out, c->err_dev, c->sms, s));
+      }
     }
     CK(cudaStreamWaitEvent(s, c->ev_fill, 0));
     return MOE_OK;
@@ -366,7 +390,16 @@ extern "C" moe_status moe_cache_get_plan(moe_cache* c, int32_t* scalars, int32_t
 extern "C" moe_status moe_cache_info(moe_cache* c, uint64_t* info) {
   if (!c || !info) return fail(MOE_EINVAL, "NULL argument");
   info[0] = c->sh.S; info[1] = c->C; info[2] = (uint64_t)c->K; info[3] = (uint64_t)c->sh.L * c->sh.E;
-  info[4] = c->dev_bytes; info[5] = c->host_bytes; info[6] = 0; info[7] = 0;
+  info[4] = c->dev_bytes; info[5] = c->host_bytes; info[7] = 0;
+  {
+    // control + fill + resident experts (one grid, or gate/up + down) + filled-expert down,
+    // or control + fill + gate/up + the down/combine kernels where the split ones do not fit
+    const int T = c->cfg.max_tokens;
+    if (down_split_ok(c->sh, T, c->sms))
+      info[6] = (c->flow && resident_flow_ok(c->sh, T, c->sms)) ? 4 : 5;
+    else
+      info[6] = 3 + (uint64_t)down_combine_launches(c->sh, T, c->sms);
+  }
   return MOE_OK;
 }
 

@@ -1,0 +1,104 @@
+"""The one-grid resident-expert decode kernel (bf16 weights, up to 2 tokens).
+
+It computes each resident expert's gate/up rows, down rows and the combine in
+the same arithmetic order as the two-grid path (gate/up grid, then down grid),
+so on the same trace the two give bit-identical layer outputs; it is also held
+to the oracle (slot maps bit-exact, outputs within 2e-2).  The traces start
+cold, so they also cover calls with fills but no resident expert, and calls
+whose pairs all go to the CPU.
+"""
+import os
+from dataclasses import replace
+
+import numpy as np
+import pytest
+
+from tests.harness import TOL, build_pool, make_cache, run_decode_parity, torch_act
+from workloads import QWEN3, activations, config, routing_trace
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import serving_layer_moe_gb300 as m
+    m.load_library()
+
+
+def _qwen3_small(T, steps, layers=6, **kw):
+    shape = replace(QWEN3, L=layers)
+    return config("qwen3_decode_b1").with_(shape=shape, T=T, steps=steps,
+                                           capacity=int(0.37 * layers * shape.E), **kw)
+
+
+def _cache(cfg, pool, offs, bw, one_grid):
+    old = os.environ.get("MOE_DECODE_ONE_GRID")
+    os.environ["MOE_DECODE_ONE_GRID"] = "1" if one_grid else "0"
+    try:
+        return make_cache(cfg, pool, offs, None, bw)[0]
+    finally:
+        if old is None:
+            del os.environ["MOE_DECODE_ONE_GRID"]
+        else:
+            os.environ["MOE_DECODE_ONE_GRID"] = old
+
+
+def _one_grid_equals_two_grids(cfg, bw):
+    import torch
+    s = cfg.shape
+    dev = torch.device("cuda", 0)
+    arena, offs, pool = build_pool(cfg, n_phys=16)
+    one = _cache(cfg, pool, offs, bw, True)
+    two = _cache(cfg, pool, offs, bw, False)
+    assert int(one.info()[6]) == 4 and int(two.info()[6]) == 5   # kernels per decode call
+    ids, w = routing_trace(cfg)
+    gen = torch.Generator(device="cpu").manual_seed(7)
+    cpu = torch.randn(cfg.T, s.k, s.H, generator=gen).to(dev)     # read only where a pair goes to the CPU
+    out1 = torch.empty(cfg.T, s.H, device=dev)
+    out2 = torch.empty(cfg.T, s.H, device=dev)
+    sm1 = torch.empty(cfg.T, s.k, dtype=torch.int32, device=dev)
+    sm2 = torch.empty_like(sm1)
+    n_cpu = n_fill_only = 0
+    for st in range(cfg.steps):
+        for l in range(s.L):
+            x = torch_act(activations(cfg, st, l), dev)
+            i_d = torch.from_numpy(ids[st, l]).to(dev)
+            w_d = torch.from_numpy(w[st, l]).to(dev)
+            one.decode(l, x, i_d, w_d, out1, cpu_part=cpu, slot_map=sm1)
+            two.decode(l, x, i_d, w_d, out2, cpu_part=cpu, slot_map=sm2)
+            torch.cuda.synchronize()
+            assert torch.equal(sm1, sm2), (st, l)
+            assert torch.equal(out1, out2), (st, l, float((out1 - out2).abs().max()))
+            p = one.plan()
+            n_cpu += int((sm1 < 0).sum())
+            n_fill_only += int(p["h"] == 0 and p["q"] > 0)
+    one.close()
+    two.close()
+    return n_cpu, n_fill_only
+
+
+def test_one_grid_bit_identical_to_two_grids_b1_offload():
+    n_cpu, n_fill_only = _one_grid_equals_two_grids(_qwen3_small(T=1, steps=20), (100000, 0))
+    assert n_cpu == 0 and n_fill_only > 0
+
+
+def test_one_grid_bit_identical_to_two_grids_b2_hybrid():
+    n_cpu, _ = _one_grid_equals_two_grids(_qwen3_small(T=2, steps=16), (100000, 900000))
+    assert n_cpu > 0
+
+
+def test_one_grid_bit_identical_all_cpu_calls():
+    # K = 0: no fill ever; cold calls send every pair to the CPU
+    n_cpu, _ = _one_grid_equals_two_grids(_qwen3_small(T=1, steps=4, layers=3, max_fetch=0), (1000, 1000))
+    assert n_cpu > 0
+
+
+def test_one_grid_oracle_parity_two_tokens():
+    cfg = _qwen3_small(T=2, steps=24)
+    res = run_decode_parity(cfg, (100000, 100000), n_phys=24, fp_every=7, state_every=6)
+    assert not res.mismatches, res.mismatches[:1]
+    assert res.max_err <= TOL, res.max_err
+    assert res.fp_checked >= 15 and res.cpu_pairs > 0 and res.fills > 0
