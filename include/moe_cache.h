@@ -179,6 +179,20 @@ moe_status moe_layer_prefill(moe_cache* cache, int32_t layer, int32_t T, const v
                              void* stream);
 
 /*
+ * The second prefill buffer on (on = 1, the default) or off (on = 0), for the
+ * no-second-buffer comparison of ai.thesatyajit.com "FreeToken: a 753B model
+ * on one GPU, and the two bandwidths that decide everything", section
+ * "Prefill: hide the pool behind the wire" (also snackonai "FreeToken, or why
+ * your laptop was never the bottleneck", section "It In Action").  Off, a
+ * full-layer prefill call loads only the missing experts of its own layer,
+ * into victims that exclude that layer's slots, and its GEMMs start once those
+ * loads are done: nothing of the next layer loads while this one computes.
+ * Takes effect from the next prefill call.  Errors: MOE_EINVAL (NULL cache,
+ * prefill disabled, on not 0 or 1).
+ */
+moe_status moe_cache_set_prefill_prefetch(moe_cache* cache, int32_t on);
+
+/*
  * Copy the residency state to host arrays (synchronises the device); any pointer may be NULL.
  *   slot_to_expert_host [C] int32 (-1 = empty), stamps_host [C] uint64 (0 = empty; a
  *   larger stamp = more recently used), expert_to_slot_host [L*E] int32 (-1 = not resident),

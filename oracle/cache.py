@@ -15,8 +15,9 @@ Passages followed:
     admits, an eviction removes the least recently demanded entry),
     "Prefill: hide the pool behind the wire" (two full-layer buffers out of
     the shared pool; the next layer loads while this one computes; on-demand
-    loading when two layers do not fit) and "Elastic memory ..." (rebuild
-    the cache for a new budget; cold start).
+    loading when two layers do not fit; with the second buffer disabled the
+    loads and the computation run one after the other) and "Elastic memory
+    ..." (rebuild the cache for a new budget; cold start).
 
 The LRU order is an explicit Python list (least recent first).  Slots are
 dicts.  Stamps are kept alongside only because they are part of the state the
@@ -39,6 +40,10 @@ Readings taken where the pages are silent:
     just loaded (ascending e).  When C < 2E: on-demand, the routed experts of
     l in ascending order in groups of at most C, each group loaded into
     victims that exclude the group's own resident slots, then touched.
+  * prefill without the second buffer (prefetch_next=False, C >= 2E): the
+    call for layer l loads only what is missing of l, into victims that
+    exclude the slots of l, and touches the E experts of l; nothing of l+1
+    is loaded ahead.
   * resize: keep the min(C_new, resident) most recent entries, packed into
     slots 0.. in ascending old-slot order with their recency kept.
 """
@@ -152,7 +157,7 @@ class SlotCache:
         return DecodePlan(layer, uniq, hits, misses, q, victims, fills, cpu, slot_map)
 
     # -- prefill: one MoE layer of a chunk ------------------------------------
-    def prefill(self, layer: int, topk_ids: np.ndarray) -> PrefillPlan:
+    def prefill(self, layer: int, topk_ids: np.ndarray, prefetch_next: bool = True) -> PrefillPlan:
         ids = np.asarray(topk_ids)
         E = self.E
         if ids.size and (ids.min() < 0 or ids.max() >= E):
@@ -160,7 +165,7 @@ class SlotCache:
         flat = np.asarray(ids, dtype=np.int64) + layer * E
         if self.C >= 2 * E:
             cur = list(range(layer * E, (layer + 1) * E))
-            nxt = list(range((layer + 1) * E, (layer + 2) * E)) if layer + 1 < self.L else []
+            nxt = list(range((layer + 1) * E, (layer + 2) * E)) if prefetch_next and layer + 1 < self.L else []
             need_cur = [f for f in cur if f not in self.slot_of]
             need_nxt = [f for f in nxt if f not in self.slot_of]
             protected = {self.slot_of[f] for f in cur + nxt if f in self.slot_of}

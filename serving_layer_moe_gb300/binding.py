@@ -22,7 +22,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_EINVAL", 2: "MOE_ENOMEM", 3: "MOE_ECUDA", 4: "MOE
 # exported symbols of include/moe_cache.h
 SYMBOLS = ("moe_cache_create", "moe_cache_destroy", "moe_cache_resize", "moe_layer_decode",
            "moe_layer_prefill", "moe_cache_get_state", "moe_cache_get_plan", "moe_cache_info",
-           "moe_cache_profile", "bench_bw", "moe_layer_ffn_noalloc", "moe_last_error")
+           "moe_cache_profile", "moe_cache_set_prefill_prefetch", "bench_bw", "moe_layer_ffn_noalloc",
+           "moe_last_error")
 
 
 class MoEConfigC(ctypes.Structure):
@@ -61,6 +62,7 @@ def load_library():
     lib.moe_cache_get_plan.argtypes = [P, P, P, P, P]
     lib.moe_cache_info.argtypes = [P, P]
     lib.moe_cache_profile.argtypes = [P, I32, P, P]
+    lib.moe_cache_set_prefill_prefetch.argtypes = [P, I32]
     lib.bench_bw.argtypes = [I32, U64, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
                              ctypes.POINTER(I32)]
     lib.moe_layer_ffn_noalloc.argtypes = [I32, I32, I32, I32, I32, I32, P, I32, P, P, P, P, P]
@@ -146,6 +148,10 @@ class MoECache:
         T = topk_ids.shape[0]
         _check(load_library().moe_layer_prefill(self._h, layer, T, _ptr(x), _ptr(topk_ids), _ptr(topk_w),
                                                 _ptr(out), _stream(stream)))
+
+    def set_prefill_prefetch(self, on: bool):
+        """The second prefill buffer (the next layer loads during this one's GEMMs) on or off."""
+        _check(load_library().moe_cache_set_prefill_prefetch(self._h, 1 if on else 0))
 
     def resize(self, n_slots):
         _check(load_library().moe_cache_resize(self._h, int(n_slots)))

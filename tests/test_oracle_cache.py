@@ -53,12 +53,12 @@ class HistoryModel:
         sm = [[where[f] if f in touched else -1 for f in row] for row in flat]
         return q, victims, np.array(sm, np.int32)
 
-    def prefill(self, layer, ids):
+    def prefill(self, layer, ids, prefetch_next=True):
         E = self.E
         where = {f: s for s, f in enumerate(self.content) if f is not None}
         if self.C >= 2 * E:
             cur = list(range(layer * E, layer * E + E))
-            nxt = list(range(layer * E + E, layer * E + 2 * E)) if layer + 1 < self.L else []
+            nxt = list(range(layer * E + E, layer * E + 2 * E)) if prefetch_next and layer + 1 < self.L else []
             need = [f for f in cur if f not in where] + [f for f in nxt if f not in where]
             order = self.order({where[f] for f in cur + nxt if f in where})
             for f, s in zip(need, order):
@@ -146,8 +146,9 @@ def test_prefill_and_resize_match_history_model(seed):
         if r < 0.35:
             layer = int(g.integers(0, L))
             ids = _random_ids(g, int(g.integers(1, 6)), k, E)
-            o.prefill(layer, ids)
-            h.prefill(layer, ids)
+            nxt = bool(g.random() < 0.7)   # with or without the second buffer
+            o.prefill(layer, ids, prefetch_next=nxt)
+            h.prefill(layer, ids, prefetch_next=nxt)
         elif r < 0.85:
             layer = int(g.integers(0, L))
             ids = _random_ids(g, int(g.integers(1, 3)), k, E)
@@ -172,6 +173,25 @@ def test_full_layer_prefill_leaves_layer_and_next_resident():
         for f in range(l * 3, min(4, l + 2) * 3):
             assert f in o.slot_of
         assert np.all(p.slot_map >= 0)
+
+
+def test_prefill_without_second_buffer_loads_only_its_layer():
+    # Cold cache, C >= 2E: with the second buffer each call after the first
+    # finds its layer resident (loaded ahead by the call before); without it,
+    # every call loads its own E experts and nothing of the next layer.
+    L, E = 4, 3
+    ids = np.array([[0, 1], [2, 0]], np.int32)
+    two = SlotCache(L, E, C=2 * E, K=E, b_pcie=1, b_cpu=0)
+    one = SlotCache(L, E, C=2 * E, K=E, b_pcie=1, b_cpu=0)
+    for l in range(L):
+        p2 = two.prefill(l, ids)
+        p1 = one.prefill(l, ids, prefetch_next=False)
+        assert len(p2.loads) == (E if l == 0 else 0)
+        assert len(p2.prefetch) == (E if l + 1 < L else 0)
+        assert sorted(f for f, _ in p1.loads) == list(range(l * E, (l + 1) * E)) and p1.prefetch == []
+        assert all(f not in one.slot_of for f in range((l + 1) * E, L * E))
+    # both moved every expert across the link once
+    assert two.counters[7] == one.counters[7] == L * E
 
 
 def test_single_expert_offload_is_a_textbook_lru():

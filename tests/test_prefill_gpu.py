@@ -42,7 +42,8 @@ def _check_state(cache, ora):
     assert g[4] == o[4]
 
 
-def _run_prefill(cfg, C, layers, n_phys=None, sample=None, seed=0):
+def _run_prefill(cfg, C, layers, n_phys=None, sample=None, seed=0, prefetch_next=True):
+    """prefetch_next: the second buffer on or off, for every call or per call (a list)."""
     import torch
     s = cfg.shape
     dev = torch.device("cuda", 0)
@@ -51,10 +52,12 @@ def _run_prefill(cfg, C, layers, n_phys=None, sample=None, seed=0):
     out = torch.empty(cfg.T, s.H, device=dev)
     worst = 0.0
     g = np.random.default_rng(seed)
-    for l in layers:
+    modes = prefetch_next if isinstance(prefetch_next, list) else [prefetch_next] * len(layers)
+    for l, nxt in zip(layers, modes):
         ids, w = prefill_routing(cfg, l)
         x = activations(cfg, 0, l)
-        plan = ora.prefill(l, ids)
+        cache.set_prefill_prefetch(nxt)
+        plan = ora.prefill(l, ids, prefetch_next=nxt)
         cache.prefill(l, torch_act(x, dev), torch.from_numpy(ids).to(dev), torch.from_numpy(w).to(dev), out)
         torch.cuda.synchronize()
         _check_state(cache, ora)
@@ -83,6 +86,23 @@ def test_small_full_layer_double_buffer():
 
 def test_small_repeat_and_out_of_order_layers():
     _run_prefill(SMALL, C=17, layers=[2, 0, 1, 1, 0])
+
+
+def test_small_without_second_buffer():
+    # each call loads only its own layer (the pages' no-second-buffer comparison)
+    worst, ora = _run_prefill(SMALL, C=16, layers=[0, 1, 2, 1], prefetch_next=False)
+    assert worst < 5e-3
+
+
+def test_second_buffer_switch_midway_and_bad_values():
+    import serving_layer_moe_gb300 as m
+    # on, off (layer 1 is already resident: nothing to load), on, off
+    _run_prefill(SMALL, C=17, layers=[0, 1, 2, 0, 1], prefetch_next=[True, False, True, False, False])
+    cache, _ = _make(SMALL, 16)
+    lib = m.load_library()
+    assert lib.moe_cache_set_prefill_prefetch(cache._h, 2) == 1
+    assert lib.moe_cache_set_prefill_prefetch(None, 1) == 1
+    cache.close()
 
 
 def test_small_on_demand_one_group():
