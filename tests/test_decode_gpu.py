@@ -75,6 +75,20 @@ def test_dsv3_fp8_shared_expert():
     assert res.fp_checked >= 5
 
 
+def test_control_one_warp_path_at_its_limit():
+    # The control kernel takes calls of at most 32 routed pairs (and K <= 16) in
+    # one warp: 4 tokens x top-8 is exactly 32; 5 tokens (40 pairs) take the
+    # block-wide path.  Both against the oracle, with CPU-assigned pairs.
+    from dataclasses import replace
+    from workloads import QWEN3
+    for T in (4, 5):
+        cfg = config("qwen3_decode_b1").with_(shape=replace(QWEN3, L=4), T=T, steps=12,
+                                              capacity=int(0.3 * 4 * 128), max_fetch=8)
+        res = run_decode_parity(cfg, (100000, 100000), n_phys=16, fp_every=5, state_every=2)
+        _ok(res)
+        assert res.cpu_pairs > 0 and res.fills > 0
+
+
 def test_ragged_T_and_empty_call():
     import torch
     cfg = config("qwen3_decode_b16").with_(steps=3)
