@@ -46,9 +46,10 @@ TRAFFIC_PER_LAYER_STEP = 75_200_000
 TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of the gate/up and down grids of one "
                   "layer-step, mean of 4 all-resident layer-steps of bench.py --mode profile-decode "
                   "(16-layer qwen3 b1 shape, 8 resident experts per layer); profiles/decode_gemv_pair_qwen3_b1.md")
-# the same for the one-grid resident kernel (None until an ncu capture of it is summarised)
-FLOW_TRAFFIC_PER_LAYER_STEP = None
-FLOW_TRAFFIC_SOURCE = None
+# the same for the fused resident launch (MOE_DECODE_FUSED=1; None until an ncu
+# capture of the kernel as it stands is summarised)
+FUSED_TRAFFIC_PER_LAYER_STEP = None
+FUSED_TRAFFIC_SOURCE = None
 
 
 def parse_args(argv=None):
@@ -293,10 +294,10 @@ def main(args):
         torch.cuda.synchronize(dev)
 
     # control, fill (+ the filled experts' gate/up), the filled experts' down grid and
-    # the resident experts' gate/up grid and down + combine grid (one grid with
-    # MOE_DECODE_ONE_GRID=1), as the library reports
+    # the resident experts' kernels (one launch, or a gate/up grid and a down +
+    # combine grid), as the library reports
     launches_per_layer = int(cache.info()[6])
-    one_grid = launches_per_layer == 4
+    resident_path = int(cache.info()[7])   # 0: two grids, 1: one launch with a grid barrier
     # ---- timed region: inputs resident in HBM ---------------------------------
     cnt0 = cache.state()[3].copy()
     if world > 1:
@@ -453,16 +454,18 @@ def main(args):
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": args.steps * s.L * launches_per_layer,
         "roofline": {"bound": "hbm",
-                     "kernel": ("resident-expert SwiGLU per layer-step, one grid (gate/up warps beside down warps, "
-                                "fused with the combine); one step replayed with every routed expert resident, an "
-                                "event pair around the grid") if one_grid else
-                               ("resident-expert GEMV pair per layer-step: gate/up grid (with the L2 fetch of W_down) "
-                                "+ down-projection grid fused with the combine; one step replayed with every routed "
-                                "expert resident, event pairs around the two grids"),
+                     "kernel": {
+                         0: "resident-expert GEMV pair per layer-step: gate/up grid (with the L2 fetch of W_down) "
+                            "+ down-projection grid fused with the combine; one step replayed with every routed "
+                            "expert resident, event pairs around the two grids",
+                         1: "resident-expert SwiGLU per layer-step, one launch: the gate/up stream (with the L2 "
+                            "fetch of W_down), a grid-wide barrier, then the down projection fused with the "
+                            "combine; one step replayed with every routed expert resident, an event pair around "
+                            "the launch"}[resident_path],
                      "achieved": round(res_gbs, 1) if res_gbs else None, "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(res_gbs / hbm_peak, 3) if res_gbs else None, "peak_source": peak_src,
-                     "traffic": FLOW_TRAFFIC_PER_LAYER_STEP if one_grid else TRAFFIC_PER_LAYER_STEP,
-                     "traffic_source": FLOW_TRAFFIC_SOURCE if one_grid else TRAFFIC_SOURCE,
+                     "traffic": TRAFFIC_PER_LAYER_STEP if resident_path == 0 else FUSED_TRAFFIC_PER_LAYER_STEP,
+                     "traffic_source": TRAFFIC_SOURCE if resident_path == 0 else FUSED_TRAFFIC_SOURCE,
                      "bytes_per_layer_step": round(res_bytes / max(1, res_launches)),
                      "us_per_layer_step": round(1e3 * res_ms / max(1, res_launches), 2),
                      "layer_steps_timed": res_launches, "fills_during": res_fills,

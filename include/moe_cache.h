@@ -156,8 +156,9 @@ moe_status moe_cache_resize(moe_cache* cache, uint64_t n_slots);
  *   slot_map_dev [T, k] int32 out, may be NULL: the slot each pair ran from, -1 = CPU
  * Errors: MOE_EINVAL, MOE_EDEVICE (earlier violation), MOE_ECUDA.
  * The resident experts run as a gate/up grid then a down + combine grid.  With
- * the environment variable MOE_DECODE_ONE_GRID=1 set when the cache is created,
- * bf16 caches of up to 2 tokens per call run them as one grid instead (same
+ * MOE_DECODE_FUSED=1 in the environment when the cache is created, one-token
+ * calls on bf16 caches with at most top-8 routed experts and no shared expert
+ * run both in one launch with a grid-wide barrier between them instead (same
  * outputs bit for bit).
  */
 moe_status moe_layer_decode(moe_cache* cache, int32_t layer, int32_t T, const void* x_dev,
@@ -220,7 +221,9 @@ moe_status moe_cache_get_plan(moe_cache* cache, int32_t* scalars_host, int32_t* 
 /*
  * Sizes of a cache: info_host[8] uint64: slot bytes S, slots C, K, L*E,
  * device bytes held, host pool bytes, kernel launches of one decode call of
- * max_tokens tokens, 0.
+ * max_tokens tokens, and how such a call runs its resident experts: 0 = a
+ * gate/up grid then a down + combine grid, 1 = one launch with a grid-wide
+ * barrier between gate/up and down + combine.
  */
 moe_status moe_cache_info(moe_cache* cache, uint64_t* info_host);
 

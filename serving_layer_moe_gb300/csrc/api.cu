@@ -168,10 +168,12 @@ extern "C" moe_status moe_cache_create(const moe_config* cfg, const void* host_p
   c->fill_ctas = c->sms / 2;
   {
     // The resident experts of a decode call run as two grids (gate/up, then down +
-    // combine).  MOE_DECODE_ONE_GRID=1 selects the one-grid kernel instead where
-    // the shape allows: faster as a kernel, slightly slower as a whole layer-step.
-    const char* ev = getenv("MOE_DECODE_ONE_GRID");
-    c->flow = ev && ev[0] == '1';
+    // combine).  MOE_DECODE_FUSED=1 runs one-token calls as one launch with a
+    // grid-wide barrier between the two instead: faster in layer-steps without
+    // fills, slower in those with fills (the barrier waits for CTAs on the SMs the
+    // fill's host reads slow down).
+    const char* ef = getenv("MOE_DECODE_FUSED");
+    c->fused = ef && ef[0] == '1';
   }
   if (k.wdtype == MOE_NVFP4 && !nvfp4_decode_fits(c->sh, k.max_tokens, c->sms))
     return bail(fail(MOE_EINVAL, "nvfp4 weights: H / I too large for the bulk decode kernels"));
@@ -234,12 +236,9 @@ extern "C" moe_status moe_cache_create(const moe_config* cfg, const void* host_p
                  o_sm = take((size_t)k.max_tokens * k.top_k * 4), o_goff = take((size_t)(max_gpu + 1) * 4),
                  o_gp = take(max_pairs * 4), o_gw = take((size_t)max_gpu * 8),
                  o_h = take(max_pairs * k.inter * 4), o_y = take(max_pairs * k.hidden * 4),
-                 o_arr = take((size_t)k.hidden * 4),
-                 o_flow = take(((size_t)kFlowSlices * max_gpu + 1) * kFlowStride * 4),
-                 o_fh = take(2 * max_pairs * k.inter * 4);
+                 o_arr = take((size_t)k.hidden * 4), o_fb = take(8);
     CKB(cudaMalloc(&c->work, off));
     CKB(cudaMemset(c->work, 0, off));
-    CKB(cudaMemset(static_cast<uint8_t*>(c->work) + o_fh, 0xff, 2 * max_pairs * k.inter * 4));   // sentinel
     uint8_t* w = static_cast<uint8_t*>(c->work);
     c->b.plan = reinterpret_cast<int32_t*>(w + o_plan);
     c->b.victims = reinterpret_cast<int32_t*>(w + o_vict);
@@ -252,9 +251,7 @@ extern "C" moe_status moe_cache_create(const moe_config* cfg, const void* host_p
     c->b.h = reinterpret_cast<float*>(w + o_h);
     c->b.y = reinterpret_cast<float*>(w + o_y);
     c->b.arrive = reinterpret_cast<uint32_t*>(w + o_arr);
-    c->b.flow = reinterpret_cast<uint32_t*>(w + o_flow);
-    c->b.flow_h = reinterpret_cast<float*>(w + o_fh);
-    c->b.flow_pairs = (int)max_pairs;
+    c->b.fused_bar = reinterpret_cast<unsigned long long*>(w + o_fb);
     c->dev_bytes = off;
   }
   c->dev_bytes += c->C * S + nflat * 12 + c->C * 12 + (k.n_shared ? (uint64_t)k.n_layers * S : 0);
@@ -307,11 +304,11 @@ extern "C" moe_status moe_layer_decode(moe_cache* c, int32_t layer, int32_t T, c
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   c->last_T = T;
   const bool split = down_split_ok(c->sh, T, c->sms);
-  const bool one_grid = split && c->flow && resident_flow_ok(c->sh, T, c->sms);
+  const bool fused = split && c->fused && resident_fused_ok(c->sh, T, c->sms);
   {
     ProfScope p(c, s, PROF_CONTROL);
     CK(launch_decode_control(c->sh, layer, T, (int)c->C, c->K, c->cfg.bw_pcie_mbps, c->cfg.bw_cpu_mbps, ids,
-                             c->tab, c->b, slot_map, c->slots, c->shared, c->err_dev, one_grid, s));
+                             c->tab, c->b, slot_map, c->slots, c->shared, c->err_dev, s));
   }
   CK(cudaEventRecord(c->ev_ctrl, s));
   CK(cudaStreamWaitEvent(c->fill_stream, c->ev_ctrl, 0));
@@ -321,19 +318,19 @@ extern "C" moe_status moe_layer_decode(moe_cache* c, int32_t layer, int32_t T, c
     CK(launch_fill_gate_up(c->sh, T, x, c->b, c->host_pool_dev, c->offsets, c->slots, c->fill_ctas, c->fill_stream));
   }
   if (split) {
-    // Beside the one-grid resident kernel, whose CTAs wait on one another, the
-    // filled-expert grid is a plain launch: launched early, its CTAs would sit on
-    // SMs for the whole fill and could keep some of the one-grid CTAs off the GPU.
+    // Beside the fused resident launch, whose CTAs wait on one another at its grid
+    // barrier, the filled-expert grid is a plain launch: launched early, its CTAs
+    // would sit on SMs for the whole fill and could keep some fused CTAs off the GPU.
     ProfScope p(c, c->fill_stream, PROF_DOWN_FILLED);
-    CK(launch_down_split(c->sh, 1, T, w, cpu_part, c->b, out, c->err_dev, c->sms, c->fill_stream, !one_grid));
+    CK(launch_down_split(c->sh, 1, T, w, cpu_part, c->b, out, c->err_dev, c->sms, c->fill_stream, !fused));
   }
   CK(cudaEventRecord(c->ev_fill, c->fill_stream));
   if (split) {
     {
       // one timed group: the two grids run back to back under a programmatic dependency
       ProfScope p(c, s, PROF_GEMV_RESIDENT);
-      if (one_grid) {
-        CK(launch_resident_flow(c->sh, T, x, w, cpu_part, c->b, out, c->err_dev, c->sms, s));
+      if (fused) {
+        CK(launch_resident_fused(c->sh, T, x, w, cpu_part, c->b, out, c->err_dev, c->sms, s));
       } else {
         CK(launch_gate_up(c->sh, 0, T, x, c->b, c->sms, s, c->err_dev));
         CK(launch_down_split(c->sh, 0, T, w, cpu_part, c->b, out, c->err_dev, c->sms, s));
@@ -392,11 +389,15 @@ extern "C" moe_status moe_cache_info(moe_cache* c, uint64_t* info) {
   info[0] = c->sh.S; info[1] = c->C; info[2] = (uint64_t)c->K; info[3] = (uint64_t)c->sh.L * c->sh.E;
   info[4] = c->dev_bytes; info[5] = c->host_bytes; info[7] = 0;
   {
+    const int T = c->cfg.max_tokens;
+    if (down_split_ok(c->sh, T, c->sms) && c->fused && resident_fused_ok(c->sh, T, c->sms)) info[7] = 1;
+  }
+  {
     // control + fill + resident experts (one grid, or gate/up + down) + filled-expert down,
     // or control + fill + gate/up + the down/combine kernels where the split ones do not fit
     const int T = c->cfg.max_tokens;
     if (down_split_ok(c->sh, T, c->sms))
-      info[6] = (c->flow && resident_flow_ok(c->sh, T, c->sms)) ? 4 : 5;
+      info[6] = (c->fused && resident_fused_ok(c->sh, T, c->sms)) ? 4 : 5;
     else
       info[6] = 3 + (uint64_t)down_combine_launches(c->sh, T, c->sms);
   }

@@ -43,7 +43,7 @@ struct moe_cache {
   int sms = 0;
   int gemv_grid = 0;
   int fill_ctas = 0;
-  bool flow = false;               // resident experts in one grid where the shape allows (MOE_DECODE_ONE_GRID=1)
+  bool fused = false;              // one-token resident gate/up + down in one launch (MOE_DECODE_FUSED=1)
   // host pool
   const uint8_t* host_pool = nullptr;
   const uint8_t* host_pool_dev = nullptr;

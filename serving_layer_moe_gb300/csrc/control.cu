@@ -61,7 +61,6 @@ struct CtrlArgs {
   const uint8_t* shared_blob;   // this layer's shared expert, or null
   uint32_t* err;
   int umax;                     // min(E, T*k)
-  uint32_t* flow;               // this call takes the one-grid resident path: its state, else null
   int cache_keys;               // keys of all C slots fit in shared memory
 };
 
@@ -160,11 +159,6 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
   }
   pdl_wait();       // the routed ids may come from the preceding kernel
   pdl_trigger();
-  if (a.flow) {   // the one-grid resident path runs next: fresh row counters, the other h buffer
-    const int nc = kFlowSlices * (U + a.n_shared);
-    for (int i = tid; i < nc; i += nt) a.flow[(size_t)(i + 1) * kFlowStride] = 0u;
-    if (tid == 0) a.flow[0] += 1u;
-  }
   if (kSel == 2 && P + a.n_shared <= 32 && NW <= 32) {
     // ---- one warp for calls of at most 32 routed pairs ---------------------------
     // The steps below for a handful of pairs, in warp 0 with ballots and warp
@@ -694,7 +688,7 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
 cudaError_t launch_decode_control(const Shape& sh, int layer, int T, int C, int K, uint32_t bp,
                                   uint32_t bc, const int32_t* ids, CacheTables tab, DecodeBufs b,
                                   int32_t* slot_map_out, const uint8_t* slots_base,
-                                  const uint8_t* shared_base, uint32_t* err, bool flow_call, cudaStream_t s) {
+                                  const uint8_t* shared_base, uint32_t* err, cudaStream_t s) {
   CtrlArgs a;
   a.layer = layer; a.T = T; a.k = sh.k; a.E = sh.E; a.C = C; a.K = K; a.n_shared = sh.n_shared;
   a.bp = bp; a.bc = bc; a.S = sh.S; a.ids = ids; a.tab = tab; a.b = b;
@@ -702,7 +696,6 @@ cudaError_t launch_decode_control(const Shape& sh, int layer, int T, int C, int 
   a.shared_blob = sh.n_shared ? shared_base + (size_t)layer * sh.S : nullptr;
   a.err = err;
   a.umax = min(sh.E, T * sh.k);
-  a.flow = flow_call ? b.flow : nullptr;
   const int NW = (sh.E + 31) / 32;
   const size_t base = (size_t)sh.E * 4 + (size_t)T * sh.k * 4 + (size_t)(2 * NW + 1) * 4 +
                       (size_t)(6 * a.umax + 2) * 4 + (size_t)K * 4 + 256 * 4 + 8 +

@@ -1351,400 +1351,271 @@ __global__ void __launch_bounds__((kRing && !kPair) ? 256 : 512) down_bulk_kerne
   if (missing) atomicOr_system(err, kErrMissingCpuPart);
 }
 
-// ---- resident experts in one grid: gate/up warps beside down warps --------------------
-// Gate/up, down projection and combine of the resident experts (hits and the
-// shared expert) in one persistent grid, bf16 weights and activations.
-//
-// Warps 0 .. NWG-1 stream gate/up row pairs like gate_up_bulk_kernel.  Items are
-// expert-major over the whole grid, so the experts' h complete one after
-// another.  h goes to a buffer of its own whose entries start as a sentinel bit
-// pattern (all ones: a NaN that no arithmetic produces, the GPU's computed NaN
-// being 0x7fffffff).  The warp's lane 0 then counts the row in its expert's
-// counter (four slices on separate L2 lines).  Neither the store nor the count
-// waits for anything.
-//
-// Warps NWG .. NWG+NWD-1 own the CTA's output rows [r0, r0 + R), the row blocks
-// of the split down kernels.  Each takes experts g = dw, dw + NWD, ... and reads
-// the R x I block of W_down of each into its stage: the first once half of its
-// expert's rows are counted (read at the start, the blocks would hold back the
-// gate/up rows), each later one right after the block before it is used.  Once
-// most of an expert's rows are counted it loads h, reloading any value that
-// still reads as the sentinel (the counts are not ordered with the h stores),
-// and forms y for the expert's pairs.  So W_down is read beside the gate/up
-// stream rather than after it, and only the last expert's rows remain once the
-// last gate/up row is done.  The combine is that of down_bulk_kernel pass 0:
-// resident and filled grids count their arrivals per row block and the second
-// combines.
-//
-// Two h buffers alternate between calls, by the parity of a call count that
-// the control kernel of the call advances (it also zeroes the counters).
-// While a call uses one buffer, its CTAs put the sentinel back into the other.
-//
-// The down warps wait on counts that other CTAs of this grid advance, so all
-// CTAs must run at once.  The grid is one CTA per row block, fewer than the SMs
-// (147 of 152 for H = 2048), so all of them are placed at launch even while the
-// control kernel (one CTA) still holds its SM, and the next layer's control
-// kernel finds a free SM for the work it does before its wait.  The fill and the filled-expert down grid never wait on this grid, and its
-// dependents launch only once every CTA of it has triggered.  Every wait is
-// bounded by the global timer; a timeout flags the error word.
-constexpr int kFlowDownWarps = 4;
-constexpr int kFlowMaxWarps = 12;
-// registers per thread, at most: 384 threads x 80 plus one fill CTA (256 x 128)
-// fit an SM's 64 K registers, so the fill of the same layer is never shut out
-constexpr int kFlowMaxRegs = 80;
-constexpr size_t kFlowSmemMax = 226 * 1024;   // dynamic shared memory of one CTA, at most
+constexpr size_t kFusedSmemMax = 226 * 1024;   // dynamic shared memory of one CTA, at most
 
-struct FlowGeom {
-  int NWG, NSG, NWD, R, nblk;
-  size_t SBG, SBD;
-  size_t gu_off, d_off, plan_off, x_off, extra_off, smem;
+// ---- resident experts: the gate/up grid and its down projection in one launch ------
+// One bf16 token, at most 8 resident experts (no shared expert).  Phase 1 is
+// gate_up_bulk_kernel unchanged: per-warp rings of row pairs, and once a warp
+// has issued its last row copy it has L2 fetch its share of the experts' W_down
+// (cp.async.bulk.prefetch.L2), bytes in flight that need no shared memory.
+// Then one grid-wide barrier (every h written), and phase 2 is the down
+// projection + combine of down_bulk_kernel pass 0 by the same CTAs: warp g
+// reads expert g's R x I block of W_down (from L2 by now) into the shared
+// memory the rings used and its pair's h into registers (loads at L2), and the
+// combine follows the split protocol (the resident and filled-expert grids
+// count their arrivals per row block; the second combines).  Compared with two
+// grids this saves the second grid's launch, its wait for the first grid's CTAs
+// to leave their SMs, and its plan staging.
+//
+// The barrier needs every CTA of the grid on the GPU at once: one CTA per SM,
+// and no kernel that could keep an SM waits on this one (the fill and the
+// filled-expert down grid never do).  Its count only grows: a CTA's arrival
+// number tells it which launch it belongs to.  The wait is bounded by the
+// global timer; a timeout flags the error word.
+constexpr int kFusedWarps = 8;
+
+struct FusedGeom {
+  int NS;             // gate/up ring stages per warp
+  int R, nblk;        // down: rows per CTA, CTAs with rows
+  size_t SBG, SBD;    // stage bytes: one gate/up row pair, one down row block
+  size_t ring_off, plan_off, x_off, extra_off, smem;
 };
 
-// lane 0 polls the four slices of an expert's counter until they sum to `target`
-// (a hint of how much of the expert's h is written; the sentinel check decides).
-// The pause between polls shrinks as the count nears `target`, so the many
-// waiting warps do not crowd the counters' L2 lines while the stream runs.
-__device__ __forceinline__ bool wait_rows(const uint32_t* c4, uint32_t target, uint32_t I, int lane) {
-  int ok = 1;
-  if (lane == 0) {
-    const unsigned long long t0 = gtime();
-    for (uint32_t it = 0;; ++it) {
-      uint32_t s = 0;
-#pragma unroll
-      for (int q = 0; q < kFlowSlices; ++q) {
-        uint32_t v;
-        asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c4 + q * kFlowStride) : "memory");
-        s += v;
-      }
-      if (s >= target) break;
-      if ((it & 15u) == 15u && gtime() - t0 > kBulkWaitNs) { ok = 0; break; }
-      const uint32_t left = target - s;
-      __nanosleep(left > I / 2 ? 1024 : left > I / 8 ? 256 : 64);
-    }
-  }
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  __syncwarp();
-  return ok != 0;
-}
-
-__device__ __forceinline__ void st_relaxed(float* p, float v) {
-  asm volatile("st.relaxed.gpu.global.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
-}
-
-// A lane's 8 kJN h values of one pair (columns (j * 32 + lane) * 8 ..), loaded
-// until none reads as the sentinel; false after the wait bound.
-template <int kJN>
-__device__ __forceinline__ bool load_h_ready(const float* hrow, int lane, float (&hv)[kJN][8]) {
-  const unsigned long long t0 = gtime();
-  for (uint32_t it = 0;; ++it) {
-    bool bad = false;
-#pragma unroll
-    for (int j = 0; j < kJN; ++j) {
-      const float* p = hrow + (size_t)(j * 32 + lane) * 8;
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        uint32_t r0, r1, r2, r3;
-        asm volatile("ld.relaxed.gpu.global.v4.b32 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                     : "l"(p + 4 * h2)
-                     : "memory");
-        bad |= (r0 == ~0u) | (r1 == ~0u) | (r2 == ~0u) | (r3 == ~0u);
-        hv[j][4 * h2] = __uint_as_float(r0);
-        hv[j][4 * h2 + 1] = __uint_as_float(r1);
-        hv[j][4 * h2 + 2] = __uint_as_float(r2);
-        hv[j][4 * h2 + 3] = __uint_as_float(r3);
-      }
-    }
-    if (!__any_sync(0xffffffffu, bad)) return true;
-    int late = 0;
-    if (lane == 0) late = (it & 15u) == 15u && gtime() - t0 > kBulkWaitNs;
-    if (__shfl_sync(0xffffffffu, late, 0)) return false;
-    __nanosleep(64);
-  }
-}
-
 template <int kJX, int kJN>
-__global__ void __maxnreg__(kFlowMaxRegs) resident_flow_kernel(GemvArgs a, FlowGeom geo,
-                                                                              const float* __restrict__ w,
-                                                                              const float* __restrict__ cpu,
-                                                                              float* __restrict__ out, uint32_t* err) {
+__global__ void __launch_bounds__(kFusedWarps * 32, 2) resident_fused_kernel(GemvArgs a, FusedGeom geo,
+                                                                             const float* __restrict__ w,
+                                                                             const float* __restrict__ cpu,
+                                                                             float* __restrict__ out, uint32_t* err) {
   using F = WFmt<MOE_BF16>;
   constexpr int V = 8;
   extern __shared__ __align__(128) uint8_t sm[];
   __shared__ uint32_t s_second;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int NWG = geo.NWG;
-  const bool is_gu = warp < NWG;
-  const int dw = warp - NWG;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm);   // [NWG * NSG] gate/up rings, then [NWD] down stages
-  uint64_t* mybars = is_gu ? bars + warp * geo.NSG : bars + NWG * geo.NSG + dw;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm) + warp * geo.NS;                 // phase 1
+  uint64_t* dbar = reinterpret_cast<uint64_t*>(sm) + kFusedWarps * geo.NS + warp;   // phase 2
   if (lane == 0) {
-    const int nb = is_gu ? geo.NSG : 1;
-    for (int i = 0; i < nb; ++i) bar_init(&mybars[i]);
+    for (int i = 0; i < geo.NS; ++i) bar_init(&bars[i]);
+    bar_init(dbar);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   pdl_wait();
   pdl_trigger();
-  const int H = a.H, I = a.I;
-  const uint32_t* gen = a.b.flow;                // call count, advanced by this call's control kernel
-  uint32_t* cnt = a.b.flow + kFlowStride;        // h-row counters: expert g, slice q at (g * kFlowSlices + q) * kFlowStride
-  const size_t hbuf = (size_t)a.b.flow_pairs * a.I;
-  uint32_t call;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(call) : "l"(gen) : "memory");
-  float* hq = a.b.flow_h + (call & 1u) * hbuf;
-  uint4* hclear = reinterpret_cast<uint4*>(a.b.flow_h + ((call & 1u) ^ 1u) * hbuf);
-  const int nfirst = a.b.plan[P_NFIRST], ngpu = a.b.plan[P_NGPU];
-  // no resident expert but some filled one: the filled-expert grid combines alone
-  const bool skip = nfirst == 0 && ngpu > 0;
-  const bool alone = ngpu == nfirst;
   const StagedPlan sp = stage_plan(sm + geo.plan_off, a);
-  const int NP = a.P + a.T * a.n_shared;
+  const int H = a.H, I = a.I;
+  const int nfirst = a.b.plan[P_NFIRST], ngpu = a.b.plan[P_NGPU];
+  const bool skip = nfirst == 0 && ngpu > 0;   // only filled experts: their grid combines alone
+  const bool alone = ngpu == nfirst;           // no filled expert: this grid combines alone
+  const int ng = skip ? 0 : nfirst;
+  uint8_t* ring = sm + geo.ring_off;
   uint8_t* xsm = sm + geo.x_off;
-  int* s_slot = reinterpret_cast<int*>(sm + geo.extra_off);
-  float* s_wt = reinterpret_cast<float*>(s_slot + a.P);
-  float* ys = reinterpret_cast<float*>(sm + geo.extra_off + (((size_t)a.P * 8 + 127) & ~size_t(127)));
-  uint8_t* s_mine = reinterpret_cast<uint8_t*>(ys + (size_t)geo.R * NP);
-  const int r0 = blockIdx.x * geo.R;
-  const int nr = blockIdx.x < geo.nblk ? min(geo.R, H - r0) : 0;
+  __syncthreads();
+
+  // ---- phase 1: h = silu(gate . x) * (up . x), the gate_up_bulk_kernel stream ----------
+  const long items = (long)ng * I;
+  const long nwarps = (long)gridDim.x * kFusedWarps;
+  const long w0 = (long)blockIdx.x * kFusedWarps + warp;
   const size_t row_h = F::row(H), row_i = F::row(I);
   const size_t down_off = 2ull * (size_t)I * row_h;
   const uint64_t pol = evict_first_policy();
-  const int ng = skip ? 0 : nfirst;
-
-  // down warps: W_down blocks need only the plan and the slot contents
-  int d_k = 0;          // blocks this warp has consumed
-  int d_issued = -1;    // expert of the block in flight
-  auto d_issue = [&](int g) {   // lane 0 only
-    d_issued = g;
-    const uint32_t bytes = (uint32_t)(nr * row_i);
-    bar_expect(mybars, bytes);
-    bulk_copy(sm + geo.d_off + (size_t)dw * geo.SBD, sp.w[g] + down_off + (size_t)r0 * row_i, bytes, mybars, pol);
-  };
-  // gate/up warps
-  // Every gate/up warp takes row pairs w0, w0 + nwarps, ...: the bytes each
-  // has in flight bound the stream, so all of them take part.
-  const long items = (long)ng * I;
-  const long nwarps = (long)gridDim.x * NWG;
-  const long w0 = (long)warp * gridDim.x + blockIdx.x;
-  const long first = w0;
   long last_issued[4] = {-1, -1, -1, -1};
-  auto gu_issue = [&](long it, int st) {   // lane 0 only
+  auto issue = [&](long it, int st) {   // lane 0 only
     const int g = (int)(it / I), i = (int)(it % I);
     last_issued[st] = it;
-    bar_expect(&mybars[st], (uint32_t)(2 * row_h));
-    uint8_t* dst = sm + geo.gu_off + ((size_t)warp * geo.NSG + st) * geo.SBG;
-    bulk_copy(dst, sp.w[g] + (size_t)i * row_h, (uint32_t)row_h, &mybars[st], pol);
-    bulk_copy(dst + row_h, sp.w[g] + (size_t)(I + i) * row_h, (uint32_t)row_h, &mybars[st], pol);
+    bar_expect(&bars[st], (uint32_t)(2 * row_h));
+    uint8_t* dst = ring + ((size_t)warp * geo.NS + st) * geo.SBG;
+    bulk_copy(dst, sp.w[g] + (size_t)i * row_h, (uint32_t)row_h, &bars[st], pol);
+    bulk_copy(dst + row_h, sp.w[g] + (size_t)(I + i) * row_h, (uint32_t)row_h, &bars[st], pol);
   };
-  __syncthreads();   // staged plan visible
-  if (lane == 0) {
-    if (is_gu) {
-      for (int k = 0; k < geo.NSG; ++k) {
-        const long it = first + (long)k * nwarps;
-        if (it < items) gu_issue(it, k);
-      }
-
+  const size_t wd_bytes = (size_t)H * row_i;
+  const long pf_per = (long)((wd_bytes + kPrefetchPiece - 1) / kPrefetchPiece);
+  auto prefetch_down = [&]() {   // lane 0 only: this warp's share of the experts' W_down into L2
+    for (long p = w0; p < (long)ng * pf_per; p += nwarps) {
+      const int g = (int)(p / pf_per);
+      const size_t o = (size_t)(p % pf_per) * kPrefetchPiece;
+      const size_t n = wd_bytes - o < kPrefetchPiece ? wd_bytes - o : kPrefetchPiece;
+      bulk_prefetch_l2(sp.w[g] + down_off + o, (uint32_t)n);
     }
+  };
+  const long n_mine = items > w0 ? (items - w0 + nwarps - 1) / nwarps : 0;
+  if (lane == 0) {
+    for (int k = 0; k < geo.NS; ++k) {
+      const long it = w0 + (long)k * nwarps;
+      if (it < items) issue(it, k);
+    }
+    if (n_mine <= geo.NS) prefetch_down();
   }
   {
     uint4* dst = reinterpret_cast<uint4*>(xsm);
     const uint4* src = reinterpret_cast<const uint4*>(a.x);
-    const int n16 = (int)(((size_t)a.T * H * 2) >> 4);
+    const int n16 = (int)(((size_t)H * 2) >> 4);
     for (int i = threadIdx.x; i < n16; i += blockDim.x) dst[i] = src[i];
   }
-  for (int i = threadIdx.x; i < a.P; i += blockDim.x) { s_slot[i] = a.b.slot_map[i]; s_wt[i] = w[i]; }
-  for (int i = threadIdx.x; i < NP; i += blockDim.x) s_mine[i] = 0;
-  {   // this CTA's share of the other h buffer back to the sentinel, for the next call
-    const size_t n16 = hbuf >> 2, per = (n16 + gridDim.x - 1) / gridDim.x;
-    const size_t c0 = per * blockIdx.x, c1 = min(n16, c0 + per);
-    for (size_t c = c0 + threadIdx.x; c < c1; c += blockDim.x) hclear[c] = make_uint4(~0u, ~0u, ~0u, ~0u);
+  __syncthreads();
+  uint4 xr[kJX];
+#pragma unroll
+  for (int j = 0; j < kJX; ++j) xr[j] = reinterpret_cast<const uint4*>(xsm)[j * 32 + lane];
+  bool ok = true;
+  int k = 0;
+  for (long it = w0; it < items; it += nwarps, ++k) {
+    const int st = k % geo.NS;
+    if (!__all_sync(0xffffffffu, bar_wait(&bars[st], (uint32_t)((k / geo.NS) & 1)))) { ok = false; break; }
+    const int g = (int)(it / I), i = (int)(it % I);
+    const uint4* gate = reinterpret_cast<const uint4*>(ring + ((size_t)warp * geo.NS + st) * geo.SBG);
+    const uint4* up = reinterpret_cast<const uint4*>(ring + ((size_t)warp * geo.NS + st) * geo.SBG + row_h);
+    float ag = 0.f, au = 0.f;   // the per-chunk partials and order of gate_up_bulk_kernel
+#pragma unroll
+    for (int j = 0; j < kJX; ++j) {
+      const uint4 wg = gate[j * 32 + lane], wu = up[j * 32 + lane];
+      float pg = 0.f, pu = 0.f;
+      pg = fma_bf16x2(wg.x, xr[j].x, pg); pu = fma_bf16x2(wu.x, xr[j].x, pu);
+      pg = fma_bf16x2(wg.y, xr[j].y, pg); pu = fma_bf16x2(wu.y, xr[j].y, pu);
+      pg = fma_bf16x2(wg.z, xr[j].z, pg); pu = fma_bf16x2(wu.z, xr[j].z, pu);
+      pg = fma_bf16x2(wg.w, xr[j].w, pg); pu = fma_bf16x2(wu.w, xr[j].w, pu);
+      ag += pg;
+      au += pu;
+    }
+    ag = warp_sum(ag);
+    au = warp_sum(au);
+    if (lane == 0)
+      for (int tp = sp.off[g]; tp < sp.off[g + 1]; ++tp) a.b.h[(size_t)sp.pid[tp] * I + i] = silu(ag) * au;
+    __syncwarp();
+    if (lane == 0 && it + (long)geo.NS * nwarps < items) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(it + (long)geo.NS * nwarps, st);
+      if (k == n_mine - geo.NS - 1) prefetch_down();   // that was this warp's last row copy
+    }
   }
+  if (!ok && lane == 0) {   // flag the timeout; this warp's copies land before the ring is reused
+    atomicOr_system(err, kErrTimeout);
+    for (int s2 = 0; s2 < geo.NS; ++s2) {
+      if (last_issued[s2] < 0) continue;
+      const long kk = (last_issued[s2] - w0) / nwarps;
+      const uint32_t par = (uint32_t)((kk / geo.NS) & 1);
+      const unsigned long long t0 = gtime();
+      while (!bar_test(&bars[s2], par) && gtime() - t0 < kBulkWaitNs) {
+      }
+    }
+  }
+
+  // ---- this CTA's W_down blocks, then the grid-wide barrier (every CTA's h written) ------
+  // The blocks do not depend on h: they head for the rings as soon as this CTA's
+  // warps are done with them, and land while the CTA waits at the barrier.
+  const int r0 = blockIdx.x * geo.R;
+  const int nr = blockIdx.x < geo.nblk ? min(geo.R, H - r0) : 0;
+  __syncthreads();
+  if (lane == 0 && warp < ng && nr > 0) {   // warp g: expert g's row block
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    const uint32_t bytes = (uint32_t)(nr * row_i);
+    bar_expect(dbar, bytes);
+    bulk_copy(ring + (size_t)warp * geo.SBD, sp.w[warp] + down_off + (size_t)r0 * row_i, bytes, dbar, pol);
+  }
+  if (threadIdx.x == 0) {
+    unsigned long long old;
+    asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], 1;" : "=l"(old) : "l"(a.b.fused_bar) : "memory");
+    const unsigned long long target = (old / gridDim.x + 1ull) * gridDim.x;
+    const unsigned long long t0 = gtime();
+    for (uint32_t it = 0;; ++it) {
+      unsigned long long v;
+      asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a.b.fused_bar) : "memory");
+      if (v >= target) break;
+      if ((it & 15u) == 15u && gtime() - t0 > kBulkWaitNs) { atomicOr_system(err, kErrTimeout); break; }
+      __nanosleep(32);
+    }
+  }
+  __syncthreads();
+
+  // ---- phase 2: down rows [r0, r0 + nr) of the resident experts, then the combine ----------
+  if (nr == 0 || skip) return;   // the same for the whole CTA
+  const int NP = a.P;
+  int* s_slot = reinterpret_cast<int*>(sm + geo.extra_off);
+  float* s_wt = reinterpret_cast<float*>(s_slot + a.P);
+  float* ys = reinterpret_cast<float*>(sm + geo.extra_off + (((size_t)a.P * 8 + 127) & ~size_t(127)));
+  uint8_t* s_mine = reinterpret_cast<uint8_t*>(ys + (size_t)geo.R * NP);
+  for (int i = threadIdx.x; i < a.P; i += blockDim.x) { s_slot[i] = a.b.slot_map[i]; s_wt[i] = w[i]; s_mine[i] = 0; }
   __syncthreads();
   for (int tp = sp.off[0] + threadIdx.x; tp < sp.off[ng]; tp += blockDim.x) s_mine[sp.pid[tp]] = 1;
-  __syncthreads();
-
-  bool ok = true;
-  if (is_gu) {
-    const int NCH = H / V;
-    uint4 xr[kJX > 0 ? kJX : 1];
-    if (kJX > 0) {
+  bool dok = true;
+  if (warp < ng) {   // one token: expert `warp` has exactly one pair
+    const uint8_t* blk = ring + (size_t)warp * geo.SBD;
+    const int pid = sp.pid[sp.off[warp]];
+    // the lane's h values of the pair, written by every CTA before the barrier:
+    // all 2 kJN loads at L2 in flight together, ahead of the wait for the block
+    float hv[kJN][V];
 #pragma unroll
-      for (int j = 0; j < kJX; ++j) xr[j] = reinterpret_cast<const uint4*>(xsm)[j * 32 + lane];
+    for (int j = 0; j < kJN; ++j) {
+      const float4* hp = reinterpret_cast<const float4*>(a.b.h + (size_t)pid * I + (size_t)(j * 32 + lane) * V);
+      const float4 q0 = __ldcg(hp), q1 = __ldcg(hp + 1);
+      hv[j][0] = q0.x; hv[j][1] = q0.y; hv[j][2] = q0.z; hv[j][3] = q0.w;
+      hv[j][4] = q1.x; hv[j][5] = q1.y; hv[j][6] = q1.z; hv[j][7] = q1.w;
     }
-    uint32_t* my_cnt = cnt + (w0 & (kFlowSlices - 1)) * kFlowStride;
-    int k = 0;
-    for (long it = first; it < items; it += nwarps, ++k) {
-      const int st = k % geo.NSG;
-      if (!__all_sync(0xffffffffu, bar_wait(&mybars[st], (uint32_t)((k / geo.NSG) & 1)))) { ok = false; break; }
-      const int g = (int)(it / I), i = (int)(it % I);
-      const uint8_t* stage = sm + geo.gu_off + ((size_t)warp * geo.NSG + st) * geo.SBG;
-      const uint4* gate = reinterpret_cast<const uint4*>(stage);
-      const uint4* up = reinterpret_cast<const uint4*>(stage + row_h);
-      const int pb = sp.off[g], pe = sp.off[g + 1];
-      if (kJX > 0) {   // the per-chunk partials and order of gate_up_bulk_kernel
-        float ag = 0.f, au = 0.f;
+    dok = __all_sync(0xffffffffu, bar_wait(dbar, 0u));
+    if (dok) {
+      // the straight-line row block of down_bulk_kernel: rows past nr repeat the last
+      // row (never stored), per-lane sums in the same order, then the 16-value butterfly
+      float acc[kDownRows];
 #pragma unroll
-        for (int j = 0; j < kJX; ++j) {
-          const uint4 wg = gate[j * 32 + lane], wu = up[j * 32 + lane];
-          float pg = 0.f, pu = 0.f;
-          pg = fma_bf16x2(wg.x, xr[j].x, pg); pu = fma_bf16x2(wu.x, xr[j].x, pu);
-          pg = fma_bf16x2(wg.y, xr[j].y, pg); pu = fma_bf16x2(wu.y, xr[j].y, pu);
-          pg = fma_bf16x2(wg.z, xr[j].z, pg); pu = fma_bf16x2(wu.z, xr[j].z, pu);
-          pg = fma_bf16x2(wg.w, xr[j].w, pg); pu = fma_bf16x2(wu.w, xr[j].w, pu);
-          ag += pg;
-          au += pu;
-        }
-        ag = warp_sum(ag);
-        au = warp_sum(au);
-        if (lane == 0)
-          for (int tp = pb; tp < pe; ++tp) st_relaxed(hq + (size_t)sp.pid[tp] * I + i, silu(ag) * au);
-      }
-      for (int tp = pb; kJX == 0 && tp < pe; ++tp) {
-        const int t = sp.tok[tp];
-        float ag = 0.f, au = 0.f;
-        for (int c = lane; c < NCH; c += 32) {
-          float fg[V], fu[V], xv[V];
-          F::unpack(gate[c], fg);
-          F::unpack(up[c], fu);
-          load_x<MOE_BF16, V>(xsm, (size_t)t * H + (size_t)c * V, xv);
-          float dg = 0.f, du = 0.f;
+      for (int r = 0; r < kDownRows; ++r) {
+        const int rr = r < nr ? r : nr - 1;
+        const uint4* wrow = reinterpret_cast<const uint4*>(blk + (size_t)rr * row_i);
+        float d = 0.f;
 #pragma unroll
-          for (int v = 0; v < V; ++v) { dg = fmaf(fg[v], xv[v], dg); du = fmaf(fu[v], xv[v], du); }
-          ag += dg;
-          au += du;
+        for (int j = 0; j < kJN; ++j) {
+          float fw[V];
+          F::unpack(wrow[j * 32 + lane], fw);
+          float dj = 0.f;
+#pragma unroll
+          for (int v = 0; v < V; ++v) dj = fmaf(fw[v], hv[j][v], dj);
+          d += dj;
         }
-        ag = warp_sum(ag);
-        au = warp_sum(au);
-        if (lane == 0) st_relaxed(hq + (size_t)sp.pid[tp] * I + i, silu(ag) * au);
+        acc[r] = 0.f + d;
       }
-      __syncwarp();
-      if (lane == 0) {
-        if (it + (long)geo.NSG * nwarps < items) {
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          gu_issue(it + (long)geo.NSG * nwarps, st);
-        }
-        asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(my_cnt + (size_t)g * kFlowSlices * kFlowStride)
-                     : "memory");
+      const float v = reduce16(acc, lane);
+      const int r = lane >> 1;
+      if ((lane & 1) == 0 && r < nr) {
+        ys[(size_t)r * NP + pid] = v;
+        a.b.y[(size_t)pid * H + r0 + r] = v;   // per-pair output stays readable (moe_cache_get_plan)
       }
     }
-    if (!ok && lane == 0) {   // flag the timeout; this warp's copies land before the CTA exits
+    if (!dok && lane == 0) {   // flag the timeout; the block lands before the CTA exits
       atomicOr_system(err, kErrTimeout);
-      for (int s2 = 0; s2 < geo.NSG; ++s2) {
-        if (last_issued[s2] < 0) continue;
-        const long kk = (last_issued[s2] - first) / nwarps;
-        const uint32_t par = (uint32_t)((kk / geo.NSG) & 1);
-        const unsigned long long t0 = gtime();
-        while (!bar_test(&mybars[s2], par) && gtime() - t0 < kBulkWaitNs) {
-        }
-      }
-    }
-  } else if (nr > 0) {
-    // down warp dw: experts dw, dw + NWD, ... over the CTA's rows [r0, r0 + nr)
-    const uint8_t* blk = sm + geo.d_off + (size_t)dw * geo.SBD;
-    for (int g = dw; g < ng; g += geo.NWD, ++d_k) {
-      const uint32_t* c4 = cnt + (size_t)g * kFlowSlices * kFlowStride;
-      if (d_k == 0) {
-        // the first block is read into the stage once half its expert's rows are
-        // counted (read at the start, the blocks would hold back the gate/up rows);
-        // each later one right after the block before it is used
-        if (!wait_rows(c4, (uint32_t)(I / 2), (uint32_t)I, lane)) { ok = false; break; }
-        if (lane == 0) d_issue(g);
-      }
-      // most rows counted: from here the h loads poll for the rest themselves
-      if (!wait_rows(c4, (uint32_t)(I - I / 8), (uint32_t)I, lane)) { ok = false; break; }
-      if (!__all_sync(0xffffffffu, bar_wait(mybars, (uint32_t)(d_k & 1)))) { ok = false; break; }
-      for (int tp = sp.off[g]; tp < sp.off[g + 1]; ++tp) {
-        const int pid = sp.pid[tp];
-        float hv[kJN][V];
-        if (!load_h_ready<kJN>(hq + (size_t)pid * I, lane, hv)) { ok = false; break; }
-        // the straight-line row block of down_bulk_kernel: rows past nr repeat the last
-        // row (never stored), per-lane sums in the same order, then the 16-value butterfly
-        float acc[kDownRows];
-#pragma unroll
-        for (int r = 0; r < kDownRows; ++r) {
-          const int rr = r < nr ? r : nr - 1;
-          const uint4* wrow = reinterpret_cast<const uint4*>(blk + (size_t)rr * row_i);
-          float d = 0.f;
-#pragma unroll
-          for (int j = 0; j < kJN; ++j) {
-            float fw[V];
-            F::unpack(wrow[j * 32 + lane], fw);
-            float dj = 0.f;
-#pragma unroll
-            for (int v = 0; v < V; ++v) dj = fmaf(fw[v], hv[j][v], dj);
-            d += dj;
-          }
-          acc[r] = 0.f + d;
-        }
-        const float v = reduce16(acc, lane);
-        const int r = lane >> 1;
-        if ((lane & 1) == 0 && r < nr) {
-          ys[(size_t)r * NP + pid] = v;
-          a.b.y[(size_t)pid * H + r0 + r] = v;   // per-pair output stays readable (moe_cache_get_plan)
-        }
-      }
-      if (!ok) break;
-      __syncwarp();
-      if (lane == 0 && g + geo.NWD < ng) {
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        d_issue(g + geo.NWD);
-      }
-    }
-    if (!ok && lane == 0) {
-      atomicOr_system(err, kErrTimeout);
-      if (d_issued >= 0) {   // the block in flight lands before the CTA exits
-        const int kk = (d_issued - dw) / geo.NWD;
-        const unsigned long long t0 = gtime();
-        while (!bar_test(mybars, (uint32_t)(kk & 1)) && gtime() - t0 < kBulkWaitNs) {
-        }
+      const unsigned long long t0 = gtime();
+      while (!bar_test(dbar, 0u) && gtime() - t0 < kBulkWaitNs) {
       }
     }
   }
-
-  // combine, by the down warps of CTAs that own rows (named barrier 1)
-  const int nthr_d = geo.NWD * 32;
-  const int td = threadIdx.x - NWG * 32;
-  if (!is_gu && nr > 0) {
-    asm volatile("bar.sync 1, %0;" ::"r"(nthr_d) : "memory");
-    if (td == 0 && !skip && !alone) {
+  __syncthreads();
+  if (!alone) {   // the split protocol of down_bulk_kernel
+    if (threadIdx.x == 0) {
       uint32_t old;
       asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(a.b.arrive + blockIdx.x) : "memory");
       s_second = old & 1u;
     }
-    if (!skip && !alone) asm volatile("bar.sync 1, %0;" ::"r"(nthr_d) : "memory");
-    const bool go = !skip && (alone || s_second != 0);
-    if (go && !alone) {
-      for (int idx = td; idx < nr * NP; idx += nthr_d) {
-        const int r = idx / NP, p = idx % NP;
-        const bool gpu = p >= a.P || s_slot[p] >= 0;
-        if (gpu && !s_mine[p]) ys[(size_t)r * NP + p] = __ldcg(a.b.y + (size_t)p * H + r0 + r);
-      }
-      asm volatile("bar.sync 1, %0;" ::"r"(nthr_d) : "memory");
+    __syncthreads();
+    if (!s_second) return;
+    for (int idx = threadIdx.x; idx < nr * NP; idx += blockDim.x) {
+      const int r = idx / NP, p = idx % NP;
+      if (s_slot[p] >= 0 && !s_mine[p]) ys[(size_t)r * NP + p] = __ldcg(a.b.y + (size_t)p * H + r0 + r);
     }
-    if (go) {
-      bool missing = false;
-      for (int idx = td; idx < nr * a.T; idx += nthr_d) {
-        const int r = idx / a.T, t = idx % a.T;
-        float acc = 0.f;
-        for (int j = 0; j < a.k; ++j) {
-          const int p = t * a.k + j;
-          float v;
-          if (s_slot[p] >= 0) {
-            v = ys[(size_t)r * NP + p];
-          } else if (cpu != nullptr) {
-            v = __ldg(cpu + (size_t)p * H + r0 + r);
-          } else {
-            v = 0.f;
-            missing = true;
-          }
-          acc = fmaf(s_wt[p], v, acc);
-        }
-        if (a.n_shared) acc += ys[(size_t)r * NP + a.P + t];
-        out[(size_t)t * H + r0 + r] = acc;
-      }
-      if (missing) atomicOr_system(err, kErrMissingCpuPart);
-    }
+    __syncthreads();
   }
+  bool missing = false;
+  for (int r = threadIdx.x; r < nr; r += blockDim.x) {   // one token
+    float acc = 0.f;
+    for (int j = 0; j < a.k; ++j) {
+      float v;
+      if (s_slot[j] >= 0) {
+        v = ys[(size_t)r * NP + j];
+      } else if (cpu != nullptr) {
+        v = __ldg(cpu + (size_t)j * H + r0 + r);
+      } else {
+        v = 0.f;
+        missing = true;
+      }
+      acc = fmaf(s_wt[j], v, acc);
+    }
+    out[r0 + r] = acc;
+  }
+  if (missing) atomicOr_system(err, kErrMissingCpuPart);
 }
 
 // ---- combine: out[t] = sum_j w[t,j] * (slot >= 0 ? y : cpu_part) in j order (+ shared) --
@@ -1928,10 +1799,9 @@ cudaError_t setup_gemv_kernels() {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, kDecodeCarveout);
     if (e != cudaSuccess) return e;
   }
-  for (const void* k : {(const void*)resident_flow_kernel<0, 3>, (const void*)resident_flow_kernel<4, 3>,
-                        (const void*)resident_flow_kernel<8, 3>, (const void*)resident_flow_kernel<0, 4>,
-                        (const void*)resident_flow_kernel<4, 4>, (const void*)resident_flow_kernel<8, 4>}) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFlowSmemMax);
+  for (const void* k : {(const void*)resident_fused_kernel<8, 3>, (const void*)resident_fused_kernel<8, 4>,
+                        (const void*)resident_fused_kernel<4, 3>, (const void*)resident_fused_kernel<4, 4>}) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFusedSmemMax);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, kDecodeCarveout);
     if (e != cudaSuccess) return e;
   }
@@ -2175,46 +2045,6 @@ cudaError_t launch_down_split(const Shape& sh, int pass, int T, const float* w, 
   return launch_down_bulk_any(sh, a, geo, pass == 0, pdl, w, cpu_part, out, err, s);
 }
 
-// Geometry of resident_flow_kernel, or NWG = 0 when the shape does not take it:
-// bf16 weights and activations, T <= 2, W_down rows of 3 or 4 16-byte chunks per
-// lane, gate/up rows of whole 16-byte chunk rounds, and the row blocks of the
-// split down kernels, one per CTA, on fewer CTAs than SMs.
-FlowGeom flow_geom(const GemvArgs& a, int wdtype, int adtype, int sms) {
-  FlowGeom f{};
-  if (wdtype != MOE_BF16 || adtype != MOE_BF16 || a.T > 2 || a.H % 256 != 0 || a.I % 8 != 0) return f;
-  const int nch = a.I / 8;
-  if (nch != 96 && nch != 128) return f;
-  const BulkGeom dg = down_geom(a, wdtype, sms);
-  if (dg.NS < 1 || !dg.h_smem || dg.grid > sms - 1 || dg.R < 1 || dg.R > kDownRows) return f;
-  f.R = dg.R;
-  f.nblk = dg.grid;
-  f.NWD = kFlowDownWarps;
-  f.SBG = up128(2 * wrow(MOE_BF16, (size_t)a.H));
-  f.SBD = up128((size_t)f.R * wrow(MOE_BF16, (size_t)a.I));
-  const size_t np = (size_t)(a.P + a.T * a.n_shared);
-  const size_t plan = up128(staged_plan_bytes(a.max_g, a.max_p));
-  const size_t xb = up128((size_t)a.T * a.H * 2);
-  const size_t extra = up128((size_t)a.P * 8) + up128((size_t)f.R * np * 4 + np);
-  f.NSG = 2;
-  for (f.NWG = kFlowMaxWarps - kFlowDownWarps; f.NWG >= 4; --f.NWG) {
-    f.gu_off = 256;
-    f.d_off = f.gu_off + (size_t)f.NWG * f.NSG * f.SBG;
-    f.plan_off = f.d_off + (size_t)f.NWD * f.SBD;
-    f.x_off = f.plan_off + plan;
-    f.extra_off = f.x_off + xb;
-    f.smem = f.extra_off + extra;
-    if (f.smem <= kFlowSmemMax) return f;
-  }
-  f.NWG = 0;
-  return f;
-}
-
-template <int kJX, int kJN>
-cudaError_t launch_flow_typed(const GemvArgs& a, const FlowGeom& g, const float* w, const float* cpu, float* out,
-                              uint32_t* err, int sms, cudaStream_t s) {
-  return launch_pdl(resident_flow_kernel<kJX, kJN>, dim3(g.nblk), dim3((g.NWG + g.NWD) * 32), g.smem, s, a, g, w,
-                    cpu, out, err);
-}
 
 int down_combine_launches(const Shape& sh, int T, int sms) {
   const GemvArgs a = make_args(sh, 2, T, nullptr, DecodeBufs{});
@@ -2223,27 +2053,54 @@ int down_combine_launches(const Shape& sh, int T, int sms) {
   return 2;
 }
 
-bool resident_flow_ok(const Shape& sh, int T, int sms) {
-  const GemvArgs a = make_args(sh, 0, T, nullptr, DecodeBufs{});
-  return flow_geom(a, sh.wdtype, sh.adtype, sms).NWG > 0;
+// Geometry of resident_fused_kernel, or NS = 0 when the call does not take it: bf16
+// weights and activations, one token, no shared expert, at most 8 resident
+// experts (one down stage per warp), gate/up rows of 4 or 8 16-byte chunks per
+// lane, W_down rows of 3 or 4, and the row blocks of the split down kernels.
+FusedGeom fused_geom(const GemvArgs& a, int wdtype, int adtype, int sms) {
+  FusedGeom f{};
+  if (wdtype != MOE_BF16 || adtype != MOE_BF16 || a.T != 1 || a.n_shared != 0 || a.max_g > kFusedWarps) return f;
+  if (a.H % 256 != 0 || (a.H / 256 != 4 && a.H / 256 != 8) || a.I % 256 != 0 || (a.I / 256 != 3 && a.I / 256 != 4))
+    return f;
+  const BulkGeom dg = down_geom(a, wdtype, sms);
+  if (dg.NS < 1 || !dg.h_smem || dg.grid > sms || dg.R < 1 || dg.R > kDownRows) return f;
+  f.R = dg.R;
+  f.nblk = dg.grid;
+  f.SBG = up128(2 * wrow(MOE_BF16, (size_t)a.H));
+  f.SBD = up128((size_t)f.R * wrow(MOE_BF16, (size_t)a.I));
+  const size_t np = (size_t)a.P;
+  const size_t plan = up128(staged_plan_bytes(a.max_g, a.max_p));
+  const size_t xb = up128((size_t)a.H * 2);
+  const size_t extra = up128(np * 8) + up128((size_t)f.R * np * 4 + np);
+  f.NS = 2;
+  const size_t ring = std::max((size_t)kFusedWarps * f.NS * f.SBG, (size_t)kFusedWarps * f.SBD);
+  f.ring_off = 256;
+  f.plan_off = f.ring_off + ring;
+  f.x_off = f.plan_off + plan;
+  f.extra_off = f.x_off + xb;
+  f.smem = f.extra_off + extra;
+  if (f.smem > kFusedSmemMax) f.NS = 0;
+  return f;
 }
 
-cudaError_t launch_resident_flow(const Shape& sh, int T, const void* x, const float* w, const float* cpu_part,
-                                 DecodeBufs b, float* out, uint32_t* err, int sms, cudaStream_t s) {
-  const GemvArgs a = make_args(sh, 0, T, x, b);
-  const FlowGeom g = flow_geom(a, sh.wdtype, sh.adtype, sms);
-  if (g.NWG == 0 || b.flow == nullptr) return cudaErrorInvalidValue;
-  const int jx = T == 1 ? a.H / 256 : 0;
-  const int jn = a.I / 8 / 32;
-  if (jn == 3) {
-    if (jx == 8) return launch_flow_typed<8, 3>(a, g, w, cpu_part, out, err, sms, s);
-    if (jx == 4) return launch_flow_typed<4, 3>(a, g, w, cpu_part, out, err, sms, s);
-    return launch_flow_typed<0, 3>(a, g, w, cpu_part, out, err, sms, s);
-  }
-  if (jx == 8) return launch_flow_typed<8, 4>(a, g, w, cpu_part, out, err, sms, s);
-  if (jx == 4) return launch_flow_typed<4, 4>(a, g, w, cpu_part, out, err, sms, s);
-  return launch_flow_typed<0, 4>(a, g, w, cpu_part, out, err, sms, s);
+bool resident_fused_ok(const Shape& sh, int T, int sms) {
+  const GemvArgs a = make_args(sh, 0, T, nullptr, DecodeBufs{});
+  return fused_geom(a, sh.wdtype, sh.adtype, sms).NS > 0;
 }
+
+cudaError_t launch_resident_fused(const Shape& sh, int T, const void* x, const float* w, const float* cpu_part,
+                                  DecodeBufs b, float* out, uint32_t* err, int sms, cudaStream_t s) {
+  const GemvArgs a = make_args(sh, 0, T, x, b);
+  const FusedGeom g = fused_geom(a, sh.wdtype, sh.adtype, sms);
+  if (g.NS == 0 || b.fused_bar == nullptr) return cudaErrorInvalidValue;
+  const dim3 grid(sms), block(kFusedWarps * 32);
+  const int jx = a.H / 256, jn = a.I / 256;
+  if (jx == 8 && jn == 3) return launch_pdl(resident_fused_kernel<8, 3>, grid, block, g.smem, s, a, g, w, cpu_part, out, err);
+  if (jx == 8 && jn == 4) return launch_pdl(resident_fused_kernel<8, 4>, grid, block, g.smem, s, a, g, w, cpu_part, out, err);
+  if (jx == 4 && jn == 3) return launch_pdl(resident_fused_kernel<4, 3>, grid, block, g.smem, s, a, g, w, cpu_part, out, err);
+  return launch_pdl(resident_fused_kernel<4, 4>, grid, block, g.smem, s, a, g, w, cpu_part, out, err);
+}
+
 
 cudaError_t launch_down_combine(const Shape& sh, int T, const float* w, const float* cpu_part, DecodeBufs b,
                                 float* out, uint32_t* err, int sms, cudaStream_t s) {

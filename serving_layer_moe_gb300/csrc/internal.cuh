@@ -60,9 +60,7 @@ struct DecodeBufs {
   float* h;               // [max_pairs, I] SwiGLU activations
   float* y;               // [max_pairs, H] expert outputs (unweighted)
   uint32_t* arrive;       // [H] arrivals of the two split down kernels per row block (parity = who combines)
-  uint32_t* flow;         // one-grid resident path: call count, 4 h-row counts per GPU expert (128 B apart)
-  float* flow_h;          // one-grid resident path: 2 x [flow_pairs, I] h buffers (sentinel-filled between uses)
-  int flow_pairs;         // pairs per h buffer (max_tokens * (k + shared))
+  unsigned long long* fused_bar;   // grid-barrier arrivals of the fused resident kernel (only grows)
 };
 
 struct CacheTables {
@@ -73,14 +71,6 @@ struct CacheTables {
   uint64_t* counters;     // [8]
   uint64_t* pool;         // [kPoolN + 1]: oldest LRU keys at the last rebuild, ascending; [kPoolN] = count
 };
-
-// State of the one-grid resident path (DecodeBufs::flow), one 128-byte line per
-// word: [0] the call count (its parity picks the h buffer), then kFlowSlices
-// h-row counters per GPU expert (expert g, slice q at line 1 + g * kFlowSlices + q).
-// The decode control kernel of a call that takes that path zeroes the counters
-// and advances the count.
-constexpr int kFlowStride = 32;
-constexpr int kFlowSlices = 4;
 
 // Decode victim candidates kept between calls (K <= kPoolMaxK): the kPoolN
 // smallest LRU keys as of the last full selection.
@@ -101,7 +91,7 @@ struct Shape {
 cudaError_t launch_decode_control(const Shape& sh, int layer, int T, int C, int K, uint32_t bp,
                                   uint32_t bc, const int32_t* ids, CacheTables tab, DecodeBufs b,
                                   int32_t* slot_map_out, const uint8_t* slots_base,
-                                  const uint8_t* shared_base, uint32_t* err, bool flow_call, cudaStream_t s);
+                                  const uint8_t* shared_base, uint32_t* err, cudaStream_t s);
 
 cudaError_t setup_control_kernels();  // once per device, before the first launch
 cudaError_t setup_gemv_kernels();     // once per device, before the first launch
@@ -134,12 +124,13 @@ cudaError_t launch_down_split(const Shape& sh, int pass, int T, const float* w, 
                               float* out, uint32_t* err, int sms, cudaStream_t s, bool pdl = true);
 cudaError_t launch_combine(const Shape& sh, int T, const float* w, const float* cpu_part,
                            DecodeBufs b, float* out, uint32_t* err, cudaStream_t s);
-// Gate/up + down + combine of the resident experts in one grid (bf16, T <= 2):
-// replaces launch_gate_up(pass 0) + launch_down_split(pass 0) where it fits.
-bool resident_flow_ok(const Shape& sh, int T, int sms);
+// Gate/up + down + combine of the resident experts in one launch with a grid-wide
+// barrier between them (bf16, one token, up to 8 resident experts, no shared
+// expert): can replace launch_gate_up(pass 0) + launch_down_split(pass 0).
+bool resident_fused_ok(const Shape& sh, int T, int sms);
+cudaError_t launch_resident_fused(const Shape& sh, int T, const void* x, const float* w, const float* cpu_part,
+                                  DecodeBufs b, float* out, uint32_t* err, int sms, cudaStream_t s);
 int down_combine_launches(const Shape& sh, int T, int sms);   // kernels of launch_down_combine
-cudaError_t launch_resident_flow(const Shape& sh, int T, const void* x, const float* w, const float* cpu_part,
-                                 DecodeBufs b, float* out, uint32_t* err, int sms, cudaStream_t s);
 int gemv_block_threads();
 
 // Programmatic dependent launch: a kernel launched this way may start while its

@@ -1,16 +1,17 @@
-"""The one-grid resident-expert decode kernel (bf16 weights, up to 2 tokens).
+"""The two ways a decode call can run its resident experts, against each other.
 
-It computes each resident expert's gate/up rows, down rows and the combine in
-the same arithmetic order as the two-grid path (gate/up grid, then down grid),
-so on the same trace the two give bit-identical layer outputs; it is also held
-to the oracle (slot maps bit-exact, outputs within 2e-2).  The traces start
-cold, so they also cover calls with fills but no resident expert, and calls
-whose pairs all go to the CPU.
+By default a gate/up grid then a down + combine grid; with MOE_DECODE_FUSED=1
+set when the cache is created, one-token bf16 calls run both in one launch
+with a grid-wide barrier between them.  Both compute each resident expert's
+gate/up rows, down rows and the combine in the same arithmetic order, so on
+the same trace they give bit-identical layer outputs; the fused launch is also
+held to the oracle (slot maps bit-exact, outputs within 2e-2).  The traces
+start cold, so they also cover calls with fills but no resident expert, and
+calls whose pairs all go to the CPU.
 """
 import os
 from dataclasses import replace
 
-import numpy as np
 import pytest
 
 from tests.harness import TOL, build_pool, make_cache, run_decode_parity, torch_act
@@ -34,19 +35,19 @@ def _qwen3_small(T, steps, layers=6, **kw):
                                            capacity=int(0.37 * layers * shape.E), **kw)
 
 
-def _cache(cfg, pool, offs, bw, one_grid):
-    old = os.environ.get("MOE_DECODE_ONE_GRID")
-    os.environ["MOE_DECODE_ONE_GRID"] = "1" if one_grid else "0"
+def _cache(cfg, pool, offs, bw, fused):
+    saved = os.environ.get("MOE_DECODE_FUSED")
+    os.environ["MOE_DECODE_FUSED"] = "1" if fused else "0"
     try:
         return make_cache(cfg, pool, offs, None, bw)[0]
     finally:
-        if old is None:
-            del os.environ["MOE_DECODE_ONE_GRID"]
+        if saved is None:
+            del os.environ["MOE_DECODE_FUSED"]
         else:
-            os.environ["MOE_DECODE_ONE_GRID"] = old
+            os.environ["MOE_DECODE_FUSED"] = saved
 
 
-def _one_grid_equals_two_grids(cfg, bw):
+def _fused_equals_two_grids(cfg, bw):
     import torch
     s = cfg.shape
     dev = torch.device("cuda", 0)
@@ -54,6 +55,7 @@ def _one_grid_equals_two_grids(cfg, bw):
     one = _cache(cfg, pool, offs, bw, True)
     two = _cache(cfg, pool, offs, bw, False)
     assert int(one.info()[6]) == 4 and int(two.info()[6]) == 5   # kernels per decode call
+    assert int(one.info()[7]) == 1 and int(two.info()[7]) == 0   # how the resident experts run
     ids, w = routing_trace(cfg)
     gen = torch.Generator(device="cpu").manual_seed(7)
     cpu = torch.randn(cfg.T, s.k, s.H, generator=gen).to(dev)     # read only where a pair goes to the CPU
@@ -80,25 +82,38 @@ def _one_grid_equals_two_grids(cfg, bw):
     return n_cpu, n_fill_only
 
 
-def test_one_grid_bit_identical_to_two_grids_b1_offload():
-    n_cpu, n_fill_only = _one_grid_equals_two_grids(_qwen3_small(T=1, steps=20), (100000, 0))
+def test_fused_bit_identical_to_two_grids_offload():
+    n_cpu, n_fill_only = _fused_equals_two_grids(_qwen3_small(T=1, steps=20), (100000, 0))
     assert n_cpu == 0 and n_fill_only > 0
 
 
-def test_one_grid_bit_identical_to_two_grids_b2_hybrid():
-    n_cpu, _ = _one_grid_equals_two_grids(_qwen3_small(T=2, steps=16), (100000, 900000))
+def test_fused_bit_identical_to_two_grids_hybrid():
+    n_cpu, _ = _fused_equals_two_grids(_qwen3_small(T=1, steps=20), (100000, 900000))
     assert n_cpu > 0
 
 
-def test_one_grid_bit_identical_all_cpu_calls():
+def test_fused_bit_identical_all_cpu_calls():
     # K = 0: no fill ever; cold calls send every pair to the CPU
-    n_cpu, _ = _one_grid_equals_two_grids(_qwen3_small(T=1, steps=4, layers=3, max_fetch=0), (1000, 1000))
+    n_cpu, _ = _fused_equals_two_grids(_qwen3_small(T=1, steps=4, layers=3, max_fetch=0), (1000, 1000))
     assert n_cpu > 0
 
 
-def test_one_grid_oracle_parity_two_tokens():
-    cfg = _qwen3_small(T=2, steps=24)
-    res = run_decode_parity(cfg, (100000, 100000), n_phys=24, fp_every=7, state_every=6)
+def test_fused_oracle_parity_one_token(monkeypatch):
+    monkeypatch.setenv("MOE_DECODE_FUSED", "1")
+    cfg = _qwen3_small(T=1, steps=40)
+    res = run_decode_parity(cfg, (100000, 100000), n_phys=24, fp_every=5, state_every=8)
     assert not res.mismatches, res.mismatches[:1]
     assert res.max_err <= TOL, res.max_err
-    assert res.fp_checked >= 15 and res.cpu_pairs > 0 and res.fills > 0
+    assert res.fp_checked >= 40 and res.cpu_pairs > 0 and res.fills > 0
+
+
+def test_fused_falls_back_where_it_does_not_apply(monkeypatch):
+    # two tokens per call: the fused launch does not apply and the two grids run
+    monkeypatch.setenv("MOE_DECODE_FUSED", "1")
+    cfg = _qwen3_small(T=2, steps=6, layers=3)
+    arena, offs, pool = build_pool(cfg, n_phys=8)
+    c, _ = make_cache(cfg, pool, offs, None, (100000, 100000))
+    assert int(c.info()[7]) == 0 and int(c.info()[6]) == 5
+    c.close()
+    res = run_decode_parity(cfg, (100000, 100000), n_phys=8, fp_every=3, state_every=3)
+    assert not res.mismatches and res.max_err <= TOL
