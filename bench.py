@@ -46,10 +46,12 @@ TRAFFIC_PER_LAYER_STEP = 75_200_000
 TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of the gate/up and down grids of one "
                   "layer-step, mean of 4 all-resident layer-steps of bench.py --mode profile-decode "
                   "(16-layer qwen3 b1 shape, 8 resident experts per layer); profiles/decode_gemv_pair_qwen3_b1.md")
-# the same for the fused resident launch (MOE_DECODE_FUSED=1; None until an ncu
-# capture of the kernel as it stands is summarised)
-FUSED_TRAFFIC_PER_LAYER_STEP = None
-FUSED_TRAFFIC_SOURCE = None
+# the same for the fused resident launch (MOE_DECODE_FUSED=1): one ncu capture of
+# the launch, mean of 8 all-resident layer-steps; profiles/decode_fused_resident_qwen3_b1.md
+FUSED_TRAFFIC_PER_LAYER_STEP = 80_870_000
+FUSED_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of the fused resident launch, mean of 8 "
+                        "all-resident layer-steps of MOE_DECODE_FUSED=1 bench.py --mode profile-decode (16-layer "
+                        "qwen3 b1 shape, 8 resident experts per layer); profiles/decode_fused_resident_qwen3_b1.md")
 
 
 def parse_args(argv=None):
