@@ -393,7 +393,7 @@ extern "C" moe_status moe_cache_info(moe_cache* c, uint64_t* info) {
     if (down_split_ok(c->sh, T, c->sms) && c->fused && resident_fused_ok(c->sh, T, c->sms)) info[7] = 1;
   }
   {
-    // control + fill + resident experts (one grid, or gate/up + down) + filled-expert down,
+    // control + fill + resident experts (one fused launch, or gate/up + down) + filled-expert down,
     // or control + fill + gate/up + the down/combine kernels where the split ones do not fit
     const int T = c->cfg.max_tokens;
     if (down_split_ok(c->sh, T, c->sms))
