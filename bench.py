@@ -42,7 +42,7 @@ UNIT = "layer-steps/s"
 # one ncu capture of both grids (cache control off, all-resident layers of the
 # qwen3 b1 shape, 8 resident experts each: the same work per layer-step as the
 # roofline replay); see profiles/decode_gemv_pair_qwen3_b1.md.
-TRAFFIC_PER_LAYER_STEP = 75_200_000
+TRAFFIC_PER_LAYER_STEP = 75_280_000
 TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of the gate/up and down grids of one "
                   "layer-step, mean of 4 all-resident layer-steps of bench.py --mode profile-decode "
                   "(16-layer qwen3 b1 shape, 8 resident experts per layer); profiles/decode_gemv_pair_qwen3_b1.md")

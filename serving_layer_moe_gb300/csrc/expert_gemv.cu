@@ -1865,8 +1865,9 @@ size_t up128(size_t x) { return (x + 127) & ~size_t(127); }
 // kernel runs instead.
 constexpr size_t kRingBudget = 220 * 1024;
 
-// Gate/up: one CTA per SM, up to 8 warps with 2 stages of one row pair each (about
-// 130 KB, so the filled-expert down grid fits beside it).
+// Gate/up: one CTA per SM, up to 8 warps with up to 3 stages of one row pair each
+// (about 200 KB for the Qwen3 shape: the stream is bound by the bytes each SM has
+// in flight; the fill and the filled-expert down grid still fit beside it).
 BulkGeom gate_up_geom(const GemvArgs& a, int wdtype, int adtype, int sms) {
   BulkGeom g{};
   g.grid = sms;
@@ -1878,7 +1879,7 @@ BulkGeom gate_up_geom(const GemvArgs& a, int wdtype, int adtype, int sms) {
   if (xbytes > kXSmem || fixed >= kRingBudget) return g;
   const size_t room = kRingBudget - fixed;
   for (g.NW = 8; g.NW >= 2; --g.NW) {
-    g.NS = (int)std::min<size_t>(2, room / ((size_t)g.NW * g.SB));
+    g.NS = (int)std::min<size_t>(3, room / ((size_t)g.NW * g.SB));
     if (g.NS >= 2) break;
   }
   if (g.NS < 2) { g.NS = 0; return g; }
