@@ -14,6 +14,10 @@ bit layout; the layouts here are the standard definitions:
            (1 + m/2) * 2**(e-1): magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6.
   nvfp4  : value = e2m1(code) * e4m3(scale of its 16-element row block) * g of
            the matrix; two codes per byte, the even element in the low nibble.
+  e8m0   : OCP Microscaling (MX) shared scale: an unsigned 8-bit biased
+           exponent, value 2**(code - 127); code 255 is NaN.
+  mxfp4  : OCP MX block of 32: value = e2m1(code) * e8m0(scale of its
+           32-element row block); codes packed as in nvfp4, no matrix scale.
 
 Nothing here rounds: every bf16 / e4m3 value is exactly representable in
 float64.
@@ -72,6 +76,25 @@ def nvfp4_dequant(packed: np.ndarray, scales: np.ndarray, g: float) -> np.ndarra
     return E2M1_TABLE[codes] * np.repeat(s, 16, axis=1) * float(np.float32(g))
 
 
+def e8m0_codes_to_f64(codes: np.ndarray) -> np.ndarray:
+    """OCP MX E8M0 scale codes -> float64: 2**(code - 127), NaN for code 255."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    return np.where(c == 255, np.nan, np.ldexp(1.0, c - 127))
+
+
+def mxfp4_dequant(packed: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """packed [R, C/2] (even element in the low nibble), scales [R, C/32] e8m0 codes
+    -> float64 [R, C]."""
+    packed = np.asarray(packed, dtype=np.uint8)
+    R, C2 = packed.shape
+    C = 2 * C2
+    codes = np.empty((R, C), np.uint8)
+    codes[:, 0::2] = packed & 0xF
+    codes[:, 1::2] = packed >> 4
+    assert scales.shape == (R, C // 32)
+    return E2M1_TABLE[codes] * np.repeat(e8m0_codes_to_f64(scales), 32, axis=1)
+
+
 def blockscale_dequant(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
     """codes [R, C] e4m3, scales [R/128, C/128] fp32 -> float64 [R, C]."""
     R, C = codes.shape
@@ -88,7 +111,9 @@ def parse_blob(blob: np.ndarray, wdtype: str, H: int, I: int):
     W_down [H, I] row-major; fp8 blobs append s_gu [2I/128, H/128] and
     s_d [H/128, I/128] fp32 scales; nvfp4 blobs hold packed e2m1 codes, then
     per-16-element e4m3 row-block scales s_gu [2I, H/16] and s_d [H, I/16],
-    then the two fp32 matrix scales (g_gu, g_d) and 8 bytes of padding.
+    then the two fp32 matrix scales (g_gu, g_d) and 8 bytes of padding; mxfp4
+    blobs hold the same packed codes, then per-32-element e8m0 row-block scales
+    s_gu [2I, H/32] and s_d [H, I/32].
     """
     blob = np.asarray(blob, dtype=np.uint8)
     if wdtype == "f32":
@@ -120,6 +145,14 @@ def parse_blob(blob: np.ndarray, wdtype: str, H: int, I: int):
         g = blob[o:o + 16].view(np.float32)
         w_gu = nvfp4_dequant(p_gu, s_gu, g[0])
         w_d = nvfp4_dequant(p_d, s_d, g[1])
+    elif wdtype == "mxfp4":
+        o = 0
+        p_gu = blob[o:o + I * H].reshape(2 * I, H // 2); o += I * H
+        p_d = blob[o:o + H * I // 2].reshape(H, I // 2); o += H * I // 2
+        s_gu = blob[o:o + 2 * I * H // 32].reshape(2 * I, H // 32); o += 2 * I * H // 32
+        s_d = blob[o:o + H * I // 32].reshape(H, I // 32)
+        w_gu = mxfp4_dequant(p_gu, s_gu)
+        w_d = mxfp4_dequant(p_d, s_d)
     else:
         raise ValueError(wdtype)
     return w_gu[:I], w_gu[I:], w_d

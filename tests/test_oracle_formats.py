@@ -140,3 +140,79 @@ def test_nvfp4_blob_dequantises_within_one_block_step():
             assert np.all(err <= step + 1e-12)
             assert np.mean(err) < 0.1 * np.mean(np.abs(w))        # not a constant or a dropped factor
             assert gm == np.float32(np.abs(w).max() / (6.0 * 448.0))
+
+
+# ---- MXFP4 (OCP Microscaling): e2m1 elements, one e8m0 scale per 32 row elements ----
+
+def test_e8m0_closed_form_values():
+    from oracle.formats import e8m0_codes_to_f64
+    v = e8m0_codes_to_f64(np.array([127, 128, 126, 0, 254, 255, 121], np.uint8))
+    assert v[0] == 1.0 and v[1] == 2.0 and v[2] == 0.5
+    assert v[3] == 2.0 ** -127 and v[4] == 2.0 ** 127
+    assert np.isnan(v[5])
+    assert v[6] == 1.0 / 64
+
+
+def test_e8m0_matches_torch_all_codes():
+    from oracle.formats import e8m0_codes_to_f64
+    dt = getattr(torch, "float8_e8m0fnu", None)
+    if dt is None:
+        pytest.skip("this torch has no float8_e8m0fnu")
+    codes = np.arange(256, dtype=np.uint8)
+    lib = torch.from_numpy(codes).view(dt).to(torch.float64).numpy()
+    ours = e8m0_codes_to_f64(codes)
+    assert np.array_equal(np.isnan(lib), np.isnan(ours))
+    assert np.array_equal(lib[:255], ours[:255])
+
+
+def test_mxfp4_hand_built_blob_indexes_scales_by_row_and_32_block():
+    # every code fixed by hand: element 2j of a row is code 0x2 (1.0), element
+    # 2j+1 code 0xC (-2.0); each (row, 32-element block) has its own scale code,
+    # so a scale taken from the wrong row, block width or matrix shows up.
+    from oracle.formats import parse_blob
+    H, I = 64, 32
+    p_gu = np.full((2 * I, H // 2), 0xC2, np.uint8)
+    p_d = np.full((H, I // 2), 0xC2, np.uint8)
+    s_gu = ((np.arange(2 * I)[:, None] * 3 + np.arange(H // 32)[None, :] * 5) % 40 + 100).astype(np.uint8)
+    s_d = ((np.arange(H)[:, None] * 7) % 30 + 110).astype(np.uint8)
+    blob = np.concatenate([p_gu.ravel(), p_d.ravel(), s_gu.ravel(), s_d.ravel()])
+    assert blob.size == Shape(L=1, E=1, k=1, H=H, I=I, wdtype="mxfp4", adtype="bf16").blob_bytes
+    gate, up, down = parse_blob(blob, "mxfp4", H, I)
+    for r in range(2 * I):
+        for c in range(H):
+            want = (1.0 if c % 2 == 0 else -2.0) * 2.0 ** (int(s_gu[r, c // 32]) - 127)
+            got = gate[r, c] if r < I else up[r - I, c]
+            assert got == want, (r, c)
+    for r in range(H):
+        for c in range(I):
+            assert down[r, c] == (1.0 if c % 2 == 0 else -2.0) * 2.0 ** (int(s_d[r, 0]) - 127)
+
+
+def test_mxfp4_blob_follows_the_mx_conversion():
+    # the generator's blob against the float32 draw: the scale of each 32-element
+    # block is 2**(floor(log2 amax) - 2); an element below the saturation point is
+    # within half an e2m1 step (at most 2**X) of the draw, one above it decodes to
+    # +-6 * 2**X; and the quantisation is not degenerate.
+    import math
+    from workloads import _rng, WEIGHT_STD
+    s = Shape(L=1, E=4, k=1, H=128, I=64, wdtype="mxfp4", adtype="bf16")
+    for idx in range(3):
+        blob = make_blob(s, 78, idx)
+        g = _rng(78, 0xB10B, idx)
+        w_gu = g.standard_normal((2 * s.I, s.H), dtype=np.float32) * np.float32(WEIGHT_STD)
+        w_d = g.standard_normal((s.H, s.I), dtype=np.float32) * np.float32(WEIGHT_STD)
+        gate, up, down = parse_blob(blob, "mxfp4", s.H, s.I)
+        for w, deq in ((w_gu, np.vstack([gate, up])), (w_d, down)):
+            R, C = w.shape
+            for r in range(R):
+                for b in range(C // 32):
+                    blk = w[r, 32 * b:32 * b + 32].astype(np.float64)
+                    X = math.floor(math.log2(np.abs(blk).max())) - 2
+                    d = deq[r, 32 * b:32 * b + 32]
+                    big = np.abs(blk) > 6.0 * 2.0 ** X
+                    assert np.all(d[big] == np.sign(blk[big]) * 6.0 * 2.0 ** X)
+                    assert np.all(np.abs(d[~big] - blk[~big]) <= 2.0 ** X)
+                    # every decoded value is an e2m1 magnitude times the scale
+                    assert np.all(np.isin(np.abs(d) / 2.0 ** X, [0, 0.5, 1, 1.5, 2, 3, 4, 6]))
+            err = np.abs(deq - w.astype(np.float64))
+            assert np.mean(err) < 0.15 * np.mean(np.abs(w))

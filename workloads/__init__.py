@@ -24,6 +24,11 @@ decision one: the slot is a complete expert):
       s_gu  [2I, H/16] e4m3 codes, s_d [H, I/16] e4m3 codes,
       g     [4] fp32 = (g_gu, g_d, 0, 0)
       (dequantised value = e2m1(code) * e4m3(block scale) * g of the matrix)
+  mxfp4 (OCP MX: e2m1 codes, one e8m0 scale per 32 consecutive elements of a
+  row, no matrix scale):
+      W_gu  [2I, H/2] bytes, W_d [H, I/2] bytes (packed as nvfp4),
+      s_gu  [2I, H/32] e8m0 codes, s_d [H, I/32] e8m0 codes
+      (dequantised value = e2m1(code) * 2**(scale code - 127))
 
 bf16 values are carried as uint16 bit patterns, e4m3 as uint8 codes.
 
@@ -55,7 +60,7 @@ class Shape:
     k: int          # top-k
     H: int          # hidden size
     I: int          # expert (SwiGLU) intermediate size
-    wdtype: str     # 'f32' | 'bf16' | 'fp8' | 'nvfp4'
+    wdtype: str     # 'f32' | 'bf16' | 'fp8' | 'nvfp4' | 'mxfp4'
     adtype: str     # 'f32' | 'bf16'   activation dtype
     n_shared: int = 0   # always-resident shared expert per layer (0 or 1)
 
@@ -102,6 +107,9 @@ def blob_bytes(s: Shape) -> int:
     if s.wdtype == "nvfp4":
         assert s.H % 32 == 0 and s.I % 32 == 0
         return 3 * s.I * s.H // 2 + 3 * s.I * s.H // 16 + 16
+    if s.wdtype == "mxfp4":
+        assert s.H % 32 == 0 and s.I % 32 == 0
+        return 3 * s.I * s.H // 2 + 3 * s.I * s.H // 32
     raise ValueError(s.wdtype)
 
 
@@ -222,6 +230,24 @@ def _nvfp4(w: np.ndarray):
     return packed, sc, g
 
 
+def _mxfp4(w: np.ndarray):
+    """MXFP4 quantisation of one matrix [R, C], the OCP Microscaling conversion of
+    each block of 32 consecutive row elements: shared exponent X = floor(log2 amax)
+    - 2 (2 = the largest E2M1 exponent), clamped to the E8M0 range [-127, 127];
+    scale code X + 127; element code = e2m1 of w / 2**X (nearest, ties to even,
+    saturating at +-6).  An all-zero block takes X = 0.  Returns packed codes
+    [R, C/2] and scale codes [R, C/32]."""
+    R, C = w.shape
+    blk = np.ascontiguousarray(w, dtype=np.float32).reshape(R, C // 32, 32)
+    amax = np.abs(blk).max(axis=2)
+    _, e = np.frexp(amax)                      # amax = m * 2**e, m in [0.5, 1)
+    X = np.clip(np.where(amax > 0, e.astype(np.int64) - 1 - 2, 0), -127, 127)
+    q = (blk.astype(np.float64) * np.ldexp(1.0, -X)[:, :, None]).astype(np.float32)
+    codes = f32_to_e2m1_codes(q).reshape(R, C)
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    return packed, (X + 127).astype(np.uint8)
+
+
 # ----------------------------------------------------------------------------
 # expert blobs and the host pool
 # ----------------------------------------------------------------------------
@@ -233,7 +259,7 @@ def make_blob(shape: Shape, seed: int, index: int, tag: int = 0xB10B) -> np.ndar
 
     Weights ~ N(0, 0.02) drawn in float32, then stored in the shape's weight
     dtype (bf16: nearest-even; fp8: per-128x128-block scale = amax/448 and
-    e4m3 codes of value/scale; nvfp4: see _nvfp4).
+    e4m3 codes of value/scale; nvfp4: see _nvfp4; mxfp4: see _mxfp4).
     """
     H, I = shape.H, shape.I
     g = _rng(seed, tag, index)
@@ -254,6 +280,10 @@ def make_blob(shape: Shape, seed: int, index: int, tag: int = 0xB10B) -> np.ndar
         p_d, s_d, g_d = _nvfp4(w_d)
         parts = [p_gu.ravel(), p_d.ravel(), s_gu.ravel(), s_d.ravel(),
                  np.array([g_gu, g_d, 0, 0], np.float32).view(np.uint8)]
+    elif shape.wdtype == "mxfp4":
+        p_gu, s_gu = _mxfp4(w_gu)
+        p_d, s_d = _mxfp4(w_d)
+        parts = [p_gu.ravel(), p_d.ravel(), s_gu.ravel(), s_d.ravel()]
     else:
         raise ValueError(shape.wdtype)
     blob = np.concatenate(parts)
