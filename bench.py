@@ -65,7 +65,8 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the oracle CPU baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-prefill", action="store_true")
-    p.add_argument("--no-nvfp4", action="store_true", help="skip the NVFP4-expert variant of the decode workload")
+    p.add_argument("--no-nvfp4", action="store_true",
+                   help="skip the 4-bit-expert variants (NVFP4, MXFP4) of the decode workload")
     p.add_argument("--mode", default="all", choices=["all", "decode", "prefill", "profile-decode"],
                    help="prefill: only the prefill measurement (small profiling runs)")
     p.add_argument("--prefill-tokens", type=int, default=8192)
@@ -487,7 +488,8 @@ def main(args):
     }
     if args.mode == "all" and not args.no_nvfp4:
         cache.close()
-        result["nvfp4_decode"] = nvfp4_measure(args, dev, local, b_pcie, b_cpu)
+        result["nvfp4_decode"] = fp4_measure(args, dev, local, b_pcie, b_cpu, "nvfp4")
+        result["mxfp4_decode"] = fp4_measure(args, dev, local, b_pcie, b_cpu, "mxfp4")
     if not args.no_prefill and args.mode == "all":
         result["prefill"] = prefill_measure(args, dev, local)
     if rank == 0 and not args.no_cpu_baseline:
@@ -527,14 +529,19 @@ def profile_case(args, dev):
     cache.close()
 
 
-def nvfp4_measure(args, dev, local, b_pcie, b_cpu, steps=64, warmup=8):
-    """The decode workload with NVFP4 experts (same shape, routing and slot count):
-    a blob is 2.66 MB instead of 9.44 MB, so fills and the resident GEMVs move
-    about 3.5x fewer bytes.  Graph replay of whole steps, inputs resident."""
+FP4_DESC = {"nvfp4": "NVFP4 experts (e2m1 + e4m3 per 16 + fp32 per matrix)",
+            "mxfp4": "MXFP4 experts (e2m1 + e8m0 per 32)"}
+
+
+def fp4_measure(args, dev, local, b_pcie, b_cpu, fmt, steps=64, warmup=8):
+    """The decode workload with 4-bit experts (same shape, routing and slot count):
+    a blob is 2.65 MB (NVFP4) or 2.51 MB (MXFP4) instead of 9.44 MB, so fills
+    and the resident GEMVs move 3.6x or 3.8x fewer bytes.  Graph replay of whole
+    steps, inputs resident."""
     import torch
     from serving_layer_moe_gb300 import MoECache
     base = config(WORKLOAD)
-    cfg = base.with_(shape=base.shape.__class__(**{**base.shape.__dict__, "wdtype": "nvfp4"}))
+    cfg = base.with_(shape=base.shape.__class__(**{**base.shape.__dict__, "wdtype": fmt}))
     s = cfg.shape
     arena, offs = make_pool(s, cfg.seed, n_phys=args.pool_blobs)
     pool = torch.from_numpy(arena).pin_memory()
@@ -585,7 +592,7 @@ def nvfp4_measure(args, dev, local, b_pcie, b_cpu, steps=64, warmup=8):
     ms = e0.elapsed_time(e1)
     cnt1 = cache.state()[3].copy()
     cache.close()
-    return {"workload": f"{WORKLOAD} with NVFP4 experts (e2m1 + e4m3 per 16 + fp32 per matrix), C={cfg.capacity} slots",
+    return {"workload": f"{WORKLOAD} with {FP4_DESC[fmt]}, C={cfg.capacity} slots",
             "value": round(steps * s.L / (ms / 1e3), 1), "unit": UNIT, "steps": steps,
             "ms_per_step": round(ms / steps, 4), "blob_bytes": int(s.blob_bytes),
             "fills": int(cnt1[2] - cnt0[2]), "hits": int(cnt1[0] - cnt0[0])}

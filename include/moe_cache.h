@@ -80,7 +80,8 @@ typedef enum moe_dtype {
   MOE_F32 = 0,            /* IEEE binary32 */
   MOE_BF16 = 1,           /* bfloat16 */
   MOE_FP8E4M3_B128 = 2,   /* OCP e4m3 codes with one fp32 scale per 128x128 block */
-  MOE_NVFP4 = 3           /* e2m1 codes, one e4m3 scale per 16 row elements, one fp32 scale per matrix */
+  MOE_NVFP4 = 3,          /* e2m1 codes, one e4m3 scale per 16 row elements, one fp32 scale per matrix */
+  MOE_MXFP4 = 4           /* OCP MX: e2m1 codes, one e8m0 scale per 32 row elements */
 } moe_dtype;
 
 /*
@@ -92,10 +93,16 @@ typedef enum moe_dtype {
  *   the low nibble), then s_gu [2I, H/16] and s_d [H, I/16] e4m3 codes (one per
  *   16 consecutive elements of a row), then fp32 g_gu, g_d and 8 bytes of zero;
  *   a weight is e2m1(code) * e4m3(its block's scale) * g of its matrix.
+ *   MOE_MXFP4 (the OCP Microscaling format, one of the formats FreeToken
+ *   serves: "FreeToken: a 753B model on one GPU ...", "Why this one
+ *   matters"): W_gu and W_d packed as for MOE_NVFP4, then s_gu [2I, H/32] and
+ *   s_d [H, I/32] e8m0 codes (one per 32 consecutive elements of a row); a
+ *   weight is e2m1(code) * 2^(scale code - 127), scale code 255 being NaN.
  * S = 3*I*H*sizeof(w) (+ 4*(2I*H + H*I)/16384 for fp8; 3*I*H/2 + 3*I*H/16 + 16
- * for nvfp4).  H and I must be multiples of 128 (fp8), 32 (nvfp4) or 8 (f32,
- * bf16).  NVFP4 experts serve decode calls of up to 2 tokens (max_tokens <= 2)
- * and no prefill (max_prefill_tokens = 0).
+ * for nvfp4; 3*I*H/2 + 3*I*H/32 for mxfp4).  H and I must be multiples of 128
+ * (fp8), 32 (nvfp4, mxfp4) or 8 (f32, bf16).  NVFP4 and MXFP4 experts serve
+ * decode calls of up to 2 tokens (max_tokens <= 2) and no prefill
+ * (max_prefill_tokens = 0).
  */
 typedef struct moe_config {
   int32_t n_layers;       /* L */
@@ -275,7 +282,8 @@ moe_status bench_bw(int32_t device, uint64_t expert_bytes, double* b_pcie_gbs, d
  *                S bytes each), device memory, 16-byte aligned
  *   x_dev [T, H] in adtype, topk_ids_dev / topk_w_dev [T, k], out_dev [T, H] fp32
  * Ids outside [0, E) contribute nothing.  Enqueued on `stream`; never blocks.
- * wdtype MOE_F32, MOE_BF16 or MOE_FP8E4M3_B128 (MOE_NVFP4 is MOE_EINVAL here).
+ * wdtype MOE_F32, MOE_BF16 or MOE_FP8E4M3_B128 (MOE_NVFP4 and MOE_MXFP4 are
+ * MOE_EINVAL here).
  *
  * Limits and sharing:
  *   - scratch needed ~ T * top_k * (H + I) * 4 bytes plus small lists; a call

@@ -14,8 +14,8 @@ import numpy as np
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libmoecache.so")
 
-MOE_F32, MOE_BF16, MOE_FP8E4M3_B128, MOE_NVFP4 = 0, 1, 2, 3
-DTYPES = {"f32": MOE_F32, "bf16": MOE_BF16, "fp8": MOE_FP8E4M3_B128, "nvfp4": MOE_NVFP4}
+MOE_F32, MOE_BF16, MOE_FP8E4M3_B128, MOE_NVFP4, MOE_MXFP4 = 0, 1, 2, 3, 4
+DTYPES = {"f32": MOE_F32, "bf16": MOE_BF16, "fp8": MOE_FP8E4M3_B128, "nvfp4": MOE_NVFP4, "mxfp4": MOE_MXFP4}
 STATUS = {0: "MOE_OK", 1: "MOE_EINVAL", 2: "MOE_ENOMEM", 3: "MOE_ECUDA", 4: "MOE_ECAPACITY",
           5: "MOE_EBUSY", 6: "MOE_EDEVICE"}
 

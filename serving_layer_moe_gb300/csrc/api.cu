@@ -89,7 +89,8 @@ static void destroy_impl(moe_cache* c) {
   delete c;
 }
 
-static bool valid_dtype(int d) { return d == MOE_F32 || d == MOE_BF16 || d == MOE_FP8E4M3_B128 || d == MOE_NVFP4; }
+static bool valid_dtype(int d) { return d == MOE_F32 || d == MOE_BF16 || d == MOE_FP8E4M3_B128 || d == MOE_NVFP4 ||
+                                         d == MOE_MXFP4; }
 
 static moe_status alloc_tables(moe_cache* c, uint64_t C) {
   const uint64_t nflat = (uint64_t)c->sh.L * c->sh.E;
@@ -118,10 +119,10 @@ extern "C" moe_status moe_cache_create(const moe_config* cfg, const void* host_p
     return fail(MOE_EINVAL, "H and I must be positive multiples of 8");
   if (k.wdtype == MOE_FP8E4M3_B128 && (k.hidden % 128 || k.inter % 128))
     return fail(MOE_EINVAL, "fp8 block-scaled weights need H and I multiples of 128");
-  if (k.wdtype == MOE_NVFP4) {
-    if (k.hidden % 32 || k.inter % 32) return fail(MOE_EINVAL, "nvfp4 weights need H and I multiples of 32");
-    if (k.max_tokens > 2) return fail(MOE_EINVAL, "nvfp4 weights serve decode calls of at most 2 tokens");
-    if (k.max_prefill_tokens != 0) return fail(MOE_EINVAL, "nvfp4 weights have no prefill path");
+  if (k.wdtype == MOE_NVFP4 || k.wdtype == MOE_MXFP4) {
+    if (k.hidden % 32 || k.inter % 32) return fail(MOE_EINVAL, "fp4 weights need H and I multiples of 32");
+    if (k.max_tokens > 2) return fail(MOE_EINVAL, "fp4 weights serve decode calls of at most 2 tokens");
+    if (k.max_prefill_tokens != 0) return fail(MOE_EINVAL, "fp4 weights have no prefill path");
   }
   if (k.n_shared != 0 && k.n_shared != 1) return fail(MOE_EINVAL, "n_shared must be 0 or 1");
   if (k.n_shared && !shared_host) return fail(MOE_EINVAL, "n_shared = 1 needs shared_host");
@@ -175,8 +176,8 @@ extern "C" moe_status moe_cache_create(const moe_config* cfg, const void* host_p
     const char* ef = getenv("MOE_DECODE_FUSED");
     c->fused = ef && ef[0] == '1';
   }
-  if (k.wdtype == MOE_NVFP4 && !nvfp4_decode_fits(c->sh, k.max_tokens, c->sms))
-    return bail(fail(MOE_EINVAL, "nvfp4 weights: H / I too large for the bulk decode kernels"));
+  if ((k.wdtype == MOE_NVFP4 || k.wdtype == MOE_MXFP4) && !fp4_decode_fits(c->sh, k.max_tokens, c->sms))
+    return bail(fail(MOE_EINVAL, "fp4 weights: H / I too large for the bulk decode kernels"));
 
   // host pool: page-lock (mapped) unless it already is
   cudaPointerAttributes attr;

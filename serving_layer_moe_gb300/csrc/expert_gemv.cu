@@ -83,13 +83,11 @@ template <> struct WFmt<MOE_FP8E4M3_B128> {
   }
 };
 
-template <> struct WFmt<MOE_NVFP4> {
+// The e2m1 code layout of the two 4-bit formats: 32 values per 16-byte chunk,
+// element 2j from the low nibble of byte j.
+struct E2M1Codes {
   static constexpr int V = 32;   // two elements per byte
   __host__ __device__ static constexpr size_t row(size_t n) { return n / 2; }
-  __host__ __device__ static constexpr size_t sgu_off(size_t H, size_t I) { return 3 * I * H / 2; }
-  __host__ __device__ static constexpr size_t sd_off(size_t H, size_t I) { return 3 * I * H / 2 + 2 * I * H / 16; }
-  __host__ __device__ static constexpr size_t g_off(size_t H, size_t I) { return sd_off(H, I) + H * I / 16; }
-  // the 32 e2m1 values of a 16-byte chunk, element 2j from the low nibble of byte j
   __device__ static void unpack(const uint4& w, float* f) {
     const uint32_t v[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -104,22 +102,56 @@ template <> struct WFmt<MOE_NVFP4> {
   }
 };
 
-// One NVFP4 chunk (32 weights = two 16-element blocks; s2 = their two e4m3
-// scale codes, the first block's in the low byte) against 32 activations:
-// (sum of the first 16 products) * scale_0 + (sum of the last 16) * scale_1.
-// Every NVFP4 path uses this, so a row's value does not depend on the kernel.
-__device__ __forceinline__ float dot_nvfp4(const uint4& w, uint32_t s2, const float* x) {
-  float f[32];
-  WFmt<MOE_NVFP4>::unpack(w, f);
-  float lo = 0.f, hi = 0.f;
+// NVFP4: one e4m3 scale per 16 row elements, one fp32 scale per matrix (g_off).
+template <> struct WFmt<MOE_NVFP4> : E2M1Codes {
+  using scale_t = uint16_t;   // the two e4m3 block scales of one 32-value chunk
+  __host__ __device__ static constexpr size_t sgu_off(size_t H, size_t I) { return 3 * I * H / 2; }
+  __host__ __device__ static constexpr size_t sd_off(size_t H, size_t I) { return 3 * I * H / 2 + 2 * I * H / 16; }
+  __host__ __device__ static constexpr size_t g_off(size_t H, size_t I) { return sd_off(H, I) + H * I / 16; }
+  // One chunk (two 16-element blocks; s2 = their e4m3 scale codes, the first
+  // block's in the low byte) against 32 activations: (sum of the first 16
+  // products) * scale_0 + (sum of the last 16) * scale_1.  Every NVFP4 path
+  // uses this, so a row's value does not depend on the kernel.
+  __device__ static __forceinline__ float dot(const uint4& w, uint32_t s2, const float* x) {
+    float f[32];
+    unpack(w, f);
+    float lo = 0.f, hi = 0.f;
 #pragma unroll
-  for (int v = 0; v < 16; ++v) lo = fmaf(f[v], x[v], lo);
+    for (int v = 0; v < 16; ++v) lo = fmaf(f[v], x[v], lo);
 #pragma unroll
-  for (int v = 0; v < 16; ++v) hi = fmaf(f[16 + v], x[16 + v], hi);
-  const __half2_raw sr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(s2 & 0xffffu), __NV_E4M3);
-  const float2 sf = __half22float2(*reinterpret_cast<const __half2*>(&sr));
-  return fmaf(hi, sf.y, lo * sf.x);
+    for (int v = 0; v < 16; ++v) hi = fmaf(f[16 + v], x[16 + v], hi);
+    const __half2_raw sr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(s2 & 0xffffu), __NV_E4M3);
+    const float2 sf = __half22float2(*reinterpret_cast<const __half2*>(&sr));
+    return fmaf(hi, sf.y, lo * sf.x);
+  }
+};
+
+// OCP MX E8M0 scale: 2^(code - 127), code 255 NaN.  Codes 1..254 are the fp32
+// exponent field itself; code 0 (2^-127) is the fp32 subnormal 0x00400000.
+__device__ __forceinline__ float e8m0_to_f32(uint32_t code) {
+  return code == 0 ? __uint_as_float(0x00400000u) : code == 255 ? __uint_as_float(0x7fc00000u) : __uint_as_float(code << 23);
 }
+
+// MXFP4 (OCP Microscaling): one e8m0 scale per 32 row elements, i.e. per chunk;
+// no matrix scale.
+template <> struct WFmt<MOE_MXFP4> : E2M1Codes {
+  using scale_t = uint8_t;    // the chunk's e8m0 block scale
+  __host__ __device__ static constexpr size_t sgu_off(size_t H, size_t I) { return 3 * I * H / 2; }
+  __host__ __device__ static constexpr size_t sd_off(size_t H, size_t I) { return 3 * I * H / 2 + 2 * I * H / 32; }
+  // One chunk against 32 activations: (two 16-product partial sums, added) * scale.
+  __device__ static __forceinline__ float dot(const uint4& w, uint32_t s, const float* x) {
+    float f[32];
+    unpack(w, f);
+    float lo = 0.f, hi = 0.f;
+#pragma unroll
+    for (int v = 0; v < 16; ++v) lo = fmaf(f[v], x[v], lo);
+#pragma unroll
+    for (int v = 0; v < 16; ++v) hi = fmaf(f[16 + v], x[16 + v], hi);
+    return (lo + hi) * e8m0_to_f32(s & 0xffu);
+  }
+};
+
+template <int WT> constexpr bool kFp4 = WT == MOE_NVFP4 || WT == MOE_MXFP4;
 
 // ---- activations: V consecutive values as floats --------------------------
 template <int AT, int V> __device__ __forceinline__ void load_act(const void* x, size_t off, float* f);
@@ -457,16 +489,16 @@ fill_gate_up_kernel(GemvArgs a, const int32_t* __restrict__ fills, const uint8_t
         for (int j = 0; j < kChunksPerLane; ++j) {
           const int c = seg + j * 32 + lane;
           if (c < NCH) {
-            if constexpr (WT == MOE_NVFP4) {   // scales straight from the host blob
-              const uint16_t* srow = reinterpret_cast<const uint16_t*>(sb + F::sgu_off(H, I));
+            if constexpr (kFp4<WT>) {   // scales straight from the host blob
+              const auto* srow = reinterpret_cast<const typename F::scale_t*>(sb + F::sgu_off(H, I));
               const uint32_t sg2 = srow[(size_t)i * (H / 32) + c], su2 = srow[(size_t)(I + i) * (H / 32) + c];
 #pragma unroll
               for (int n = 0; n < kTokGroup; ++n) {
                 if (n < nt) {
                   float xv[V];
                   load_act<AT, V>(a.x, (size_t)tok[n] * H + (size_t)c * V, xv);
-                  ag[n] += dot_nvfp4(wg[j], sg2, xv);
-                  au[n] += dot_nvfp4(wu[j], su2, xv);
+                  ag[n] += F::dot(wg[j], sg2, xv);
+                  au[n] += F::dot(wu[j], su2, xv);
                 }
               }
             } else {
@@ -961,12 +993,12 @@ __global__ void __launch_bounds__(256) gate_up_bulk_kernel(GemvArgs a, BulkGeom 
       float ag = 0.f, au = 0.f;
       for (int c = lane; c < NCH; c += 32) {
         float dg = 0.f, du = 0.f;
-        if constexpr (WT == MOE_NVFP4) {
+        if constexpr (kFp4<WT>) {
           float xv[V];
           load_x<AT, V>(xsm, (size_t)t * H + (size_t)c * V, xv);
-          const uint16_t* srow = reinterpret_cast<const uint16_t*>(sp.w[g] + F::sgu_off(H, I));
-          dg = dot_nvfp4(gate[c], __ldg(srow + (size_t)i * (H / 32) + c), xv);
-          du = dot_nvfp4(up[c], __ldg(srow + (size_t)(I + i) * (H / 32) + c), xv);
+          const auto* srow = reinterpret_cast<const typename F::scale_t*>(sp.w[g] + F::sgu_off(H, I));
+          dg = F::dot(gate[c], __ldg(srow + (size_t)i * (H / 32) + c), xv);
+          du = F::dot(up[c], __ldg(srow + (size_t)(I + i) * (H / 32) + c), xv);
         } else {
           float fg[V], fu[V], xv[V];
           F::unpack(gate[c], fg);
@@ -1136,15 +1168,15 @@ __global__ void __launch_bounds__((kRing && !kPair) ? 256 : 512) down_bulk_kerne
             if (c < NCH) {
               const float4* hp = reinterpret_cast<const float4*>(hsrc + (size_t)pid * I + (size_t)c * V);
               float dj = 0.f;
-              if constexpr (WT == MOE_NVFP4) {
+              if constexpr (kFp4<WT>) {
                 float hv[V];
 #pragma unroll
                 for (int v = 0; v < V; v += 4) {
                   const float4 q = hp[v / 4];
                   hv[v] = q.x; hv[v + 1] = q.y; hv[v + 2] = q.z; hv[v + 3] = q.w;
                 }
-                const uint16_t* srow = reinterpret_cast<const uint16_t*>(sp.w[g] + sd_off);
-                dj = dot_nvfp4(wrow[c], __ldg(srow + (size_t)(r0 + r) * (I / 32) + c), hv);
+                const auto* srow = reinterpret_cast<const typename F::scale_t*>(sp.w[g] + sd_off);
+                dj = F::dot(wrow[c], __ldg(srow + (size_t)(r0 + r) * (I / 32) + c), hv);
               } else {
                 float fw[V];
                 F::unpack(wrow[c], fw);
@@ -1246,9 +1278,9 @@ __global__ void __launch_bounds__((kRing && !kPair) ? 256 : 512) down_bulk_kerne
               const int c = c0 + j * 32 + lane;
               if (c < NCH) {
                 float dj = 0.f;
-                if constexpr (WT == MOE_NVFP4) {
-                  const uint16_t* srow = reinterpret_cast<const uint16_t*>(sp.w[g] + sd_off);
-                  dj = dot_nvfp4(wrow[c], __ldg(srow + (size_t)(r0 + r) * (I / 32) + c), hv[j]);
+                if constexpr (kFp4<WT>) {
+                  const auto* srow = reinterpret_cast<const typename F::scale_t*>(sp.w[g] + sd_off);
+                  dj = F::dot(wrow[c], __ldg(srow + (size_t)(r0 + r) * (I / 32) + c), hv[j]);
                 } else {
                   float fw[V];
                   F::unpack(wrow[c], fw);
@@ -1794,7 +1826,10 @@ cudaError_t setup_gemv_kernels() {
                         (const void*)down_bulk_kernel<MOE_FP8E4M3_B128, false, 0>,
                         (const void*)down_bulk_kernel<MOE_NVFP4, true, 0>, (const void*)down_bulk_kernel<MOE_NVFP4, false, 0>,
                         (const void*)gate_up_bulk_kernel<MOE_NVFP4, MOE_F32, 0>,
-                        (const void*)gate_up_bulk_kernel<MOE_NVFP4, MOE_BF16, 0>}) {
+                        (const void*)gate_up_bulk_kernel<MOE_NVFP4, MOE_BF16, 0>,
+                        (const void*)down_bulk_kernel<MOE_MXFP4, true, 0>, (const void*)down_bulk_kernel<MOE_MXFP4, false, 0>,
+                        (const void*)gate_up_bulk_kernel<MOE_MXFP4, MOE_F32, 0>,
+                        (const void*)gate_up_bulk_kernel<MOE_MXFP4, MOE_BF16, 0>}) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kBulkSmemAttr);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, kDecodeCarveout);
     if (e != cudaSuccess) return e;
@@ -1850,13 +1885,17 @@ cudaError_t launch_fill_gate_up(const Shape& sh, int T, const void* x, DecodeBuf
       return launch_fill_gate_up_typed<MOE_NVFP4, MOE_F32>(a, f, host_pool_dev, offsets, slots, sh.S, n_ctas, s);
     case MOE_NVFP4 * 2 + MOE_BF16:
       return launch_fill_gate_up_typed<MOE_NVFP4, MOE_BF16>(a, f, host_pool_dev, offsets, slots, sh.S, n_ctas, s);
+    case MOE_MXFP4 * 2 + MOE_F32:
+      return launch_fill_gate_up_typed<MOE_MXFP4, MOE_F32>(a, f, host_pool_dev, offsets, slots, sh.S, n_ctas, s);
+    case MOE_MXFP4 * 2 + MOE_BF16:
+      return launch_fill_gate_up_typed<MOE_MXFP4, MOE_BF16>(a, f, host_pool_dev, offsets, slots, sh.S, n_ctas, s);
   }
   return cudaErrorInvalidValue;
 }
 
 // bytes of n weight elements
 size_t wrow(int wdtype, size_t n) {
-  return wdtype == MOE_F32 ? 4 * n : wdtype == MOE_BF16 ? 2 * n : wdtype == MOE_NVFP4 ? n / 2 : n;
+  return wdtype == MOE_F32 ? 4 * n : wdtype == MOE_BF16 ? 2 * n : (wdtype == MOE_NVFP4 || wdtype == MOE_MXFP4) ? n / 2 : n;
 }
 size_t up128(size_t x) { return (x + 127) & ~size_t(127); }
 
@@ -1955,6 +1994,8 @@ cudaError_t launch_gate_up(const Shape& sh, int pass, int T, const void* x, Deco
         case MOE_FP8E4M3_B128 * 2 + MOE_BF16: return launch_gate_up_bulk<MOE_FP8E4M3_B128, MOE_BF16>(a, geo, err, s);
         case MOE_NVFP4 * 2 + MOE_F32: return launch_gate_up_bulk<MOE_NVFP4, MOE_F32>(a, geo, err, s);
         case MOE_NVFP4 * 2 + MOE_BF16: return launch_gate_up_bulk<MOE_NVFP4, MOE_BF16>(a, geo, err, s);
+        case MOE_MXFP4 * 2 + MOE_F32: return launch_gate_up_bulk<MOE_MXFP4, MOE_F32>(a, geo, err, s);
+        case MOE_MXFP4 * 2 + MOE_BF16: return launch_gate_up_bulk<MOE_MXFP4, MOE_BF16>(a, geo, err, s);
       }
     }
   }
@@ -2017,10 +2058,11 @@ cudaError_t launch_down_bulk_any(const Shape& sh, const GemvArgs& a, const BulkG
   if (sh.wdtype == MOE_F32) return launch_down_bulk<MOE_F32>(a, geo, ring, pdl, w, cpu, out, err, s);
   if (sh.wdtype == MOE_BF16) return launch_down_bulk<MOE_BF16>(a, geo, ring, pdl, w, cpu, out, err, s);
   if (sh.wdtype == MOE_NVFP4) return launch_down_bulk<MOE_NVFP4>(a, geo, ring, pdl, w, cpu, out, err, s);
+  if (sh.wdtype == MOE_MXFP4) return launch_down_bulk<MOE_MXFP4>(a, geo, ring, pdl, w, cpu, out, err, s);
   return launch_down_bulk<MOE_FP8E4M3_B128>(a, geo, ring, pdl, w, cpu, out, err, s);
 }
 
-bool nvfp4_decode_fits(const Shape& sh, int max_tokens, int sms) {
+bool fp4_decode_fits(const Shape& sh, int max_tokens, int sms) {
   for (int T = 1; T <= max_tokens; ++T) {
     const GemvArgs a = make_args(sh, 0, T, nullptr, DecodeBufs{});
     if (gate_up_geom(a, sh.wdtype, sh.adtype, sms).NS < 2 || !down_split_ok(sh, T, sms)) return false;
@@ -2110,7 +2152,7 @@ cudaError_t launch_down_combine(const Shape& sh, int T, const float* w, const fl
     const BulkGeom geo = down_geom(a, sh.wdtype, sms);
     if (geo.NS >= 1 && geo.h_smem) return launch_down_bulk_any(sh, a, geo, true, true, w, cpu_part, out, err, s);
   }
-  if (sh.wdtype == MOE_NVFP4) return cudaErrorInvalidValue;   // bulk kernels only (checked at create)
+  if (sh.wdtype == MOE_NVFP4 || sh.wdtype == MOE_MXFP4) return cudaErrorInvalidValue;   // bulk kernels only (checked at create)
   if (down_combine_fits(sh, T)) {
     const GemvArgs a = make_args(sh, 2, T, nullptr, b);
     if (sh.wdtype == MOE_F32) return launch_down_combine_typed<MOE_F32>(a, w, cpu_part, out, err, sms, s);

@@ -116,9 +116,9 @@ bool down_combine_fits(const Shape& sh, int T);
 // gate/up), pass 1 = filled experts (fill stream, after the fill); the second
 // of the two CTAs of each row block to finish forms that block's combine.
 bool down_split_ok(const Shape& sh, int T, int sms);
-// NVFP4 experts run only on the bulk gate/up and split down kernels: true when
+// NVFP4 and MXFP4 experts run only on the bulk gate/up and split down kernels: true when
 // both fit every call of up to max_tokens tokens
-bool nvfp4_decode_fits(const Shape& sh, int max_tokens, int sms);
+bool fp4_decode_fits(const Shape& sh, int max_tokens, int sms);
 // pdl = false: a plain launch, whose CTAs hold no SM while the predecessor runs.
 cudaError_t launch_down_split(const Shape& sh, int pass, int T, const float* w, const float* cpu_part, DecodeBufs b,
                               float* out, uint32_t* err, int sms, cudaStream_t s, bool pdl = true);
@@ -163,6 +163,7 @@ inline uint64_t blob_bytes(int wdtype, int H, int I) {
   if (wdtype == MOE_F32) return 12ull * HI;
   if (wdtype == MOE_BF16) return 6ull * HI;
   if (wdtype == MOE_NVFP4) return 3ull * HI / 2 + 3ull * HI / 16 + 16;
+  if (wdtype == MOE_MXFP4) return 3ull * HI / 2 + 3ull * HI / 32;
   uint64_t ns = (uint64_t)(2 * I / 128) * (H / 128) + (uint64_t)(H / 128) * (I / 128);
   return 3ull * HI + 4ull * ns;
 }

@@ -264,31 +264,37 @@ def test_varying_T_on_one_cache():
     cache.close()
 
 
-# ---- NVFP4 experts (e2m1 codes, e4m3 scales per 16 row elements, fp32 per matrix) ----
+# ---- 4-bit experts: NVFP4 (e2m1 codes, e4m3 scales per 16 row elements, fp32 per
+# matrix) and MXFP4 (e2m1 codes, e8m0 scales per 32 row elements) ----
 
-def test_nvfp4_small_decode_two_tokens():
+FP4 = ["nvfp4", "mxfp4"]
+
+@pytest.mark.parametrize("fmt,adtype", [("nvfp4", "bf16"), ("mxfp4", "bf16"), ("mxfp4", "f32")])
+def test_fp4_small_decode_two_tokens(fmt, adtype):
     from workloads import Config, Shape
-    cfg = Config("nvfp4_small", Shape(L=3, E=24, k=4, H=256, I=128, wdtype="nvfp4", adtype="bf16"), T=2, steps=24,
+    cfg = Config(f"{fmt}_small", Shape(L=3, E=24, k=4, H=256, I=128, wdtype=fmt, adtype=adtype), T=2, steps=24,
                  capacity=20, routing="softmax", seed=95)
     res = run_decode_parity(cfg, (1000, 0), fp_every=1)
     _ok(res)
     assert res.fills > 0 and res.fp_checked == 24 * 3
 
 
-def test_nvfp4_qwen3_shape_batch1():
+@pytest.mark.parametrize("fmt", FP4)
+def test_fp4_qwen3_shape_batch1(fmt):
     cfg = config("qwen3_decode_b1")
-    cfg = cfg.with_(shape=cfg.shape.__class__(**{**cfg.shape.__dict__, "wdtype": "nvfp4"}), steps=24)
+    cfg = cfg.with_(shape=cfg.shape.__class__(**{**cfg.shape.__dict__, "wdtype": fmt}), steps=24)
     res = run_decode_parity(cfg, (200000, 0), n_phys=24, fp_every=37, state_every=8)
     _ok(res)
     assert res.calls == 24 * 48 and res.fp_checked >= 20
 
 
-def test_nvfp4_split_merges_exactly():
+@pytest.mark.parametrize("fmt", FP4)
+def test_fp4_split_merges_exactly(fmt):
     # resident and filled experts give the same y bits, so CPU partials equal to the
     # GPU's own values merge into a bit-identical output (see test_exact_merge_...)
     import torch
     from workloads import Config, Shape
-    cfg = Config("nvfp4_merge", Shape(L=1, E=8, k=2, H=256, I=128, wdtype="nvfp4", adtype="bf16"), T=2, steps=1,
+    cfg = Config(f"{fmt}_merge", Shape(L=1, E=8, k=2, H=256, I=128, wdtype=fmt, adtype="bf16"), T=2, steps=1,
                  capacity=8, routing="softmax", seed=96)
     s = cfg.shape
     arena, offs, pool = build_pool(cfg)
@@ -312,14 +318,15 @@ def test_nvfp4_split_merges_exactly():
     small.close()
 
 
-def test_nvfp4_rejects_larger_batches_and_prefill():
+@pytest.mark.parametrize("fmt", FP4)
+def test_fp4_rejects_larger_batches_and_prefill(fmt):
     import torch
     from serving_layer_moe_gb300 import MoECache, MoEError
     from workloads import Shape
-    s = Shape(L=1, E=8, k=2, H=256, I=128, wdtype="nvfp4", adtype="bf16")
+    s = Shape(L=1, E=8, k=2, H=256, I=128, wdtype=fmt, adtype="bf16")
     pool = torch.zeros(8 * s.blob_bytes, dtype=torch.uint8).pin_memory()
     for kw in ({"max_tokens": 4}, {"max_tokens": 1, "max_prefill_tokens": 64}):
         with pytest.raises(MoEError) as ei:
-            MoECache(L=1, E=8, H=256, I=128, top_k=2, wdtype="nvfp4", adtype="bf16", host_pool=pool, n_slots=4,
+            MoECache(L=1, E=8, H=256, I=128, top_k=2, wdtype=fmt, adtype="bf16", host_pool=pool, n_slots=4,
                      bw_pcie_mbps=1000, bw_cpu_mbps=0, **kw)
         assert ei.value.status == 1
