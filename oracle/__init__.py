@@ -16,12 +16,14 @@ that describe the FreeToken MoE serving engine:
     inference platform" (dev.to summary)
 
 Modules:
-  formats       exact decoding of f32 / bf16 / e4m3 (+128x128 block scales)
+  formats       exact decoding of f32 / bf16 / e4m3 (+128x128 block scales),
+                NVFP4 and MXFP4
   policy        the miss split q* and its clamps, branch times
   cache         list-based global LRU of (layer, expert) slots: decode control,
                 full-layer prefill residency, resize
   ffn           SwiGLU expert in float64 and the fixed-order combine
-  static_split  the routing-blind static placement comparator
+  static_split  the static placement comparators: routing-blind split and
+                prefill-pinned hot subset
 
 Every function says which passage it follows.  Readings of passages the
 pages leave open are listed with the function that takes them.

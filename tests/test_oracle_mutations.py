@@ -92,3 +92,58 @@ def test_transposed_down_projection_is_caught(monkeypatch):
         return (ffn_mod.silu(x @ wg.T) * (x @ wu.T)) @ wd
     monkeypatch.setattr(tf, "swiglu_expert", transposed)
     _fails(tf.test_hand_derived_expert)
+
+
+def test_e8m0_bias_off_by_one_is_caught(monkeypatch):
+    import oracle.formats as formats_mod
+    from tests import test_oracle_formats as tfm
+    monkeypatch.setattr(formats_mod, "e8m0_codes_to_f64",
+                        lambda c: np.ldexp(1.0, np.asarray(c, np.uint8).astype(np.int64) - 126))
+    _fails(tfm.test_e8m0_closed_form_values)
+    _fails(tfm.test_mxfp4_hand_built_blob_indexes_scales_by_row_and_32_block)
+
+
+def test_mxfp4_nibble_order_swapped_is_caught(monkeypatch):
+    import oracle.formats as formats_mod
+    from tests import test_oracle_formats as tfm
+    orig = formats_mod.mxfp4_dequant
+
+    def swapped(packed, scales):
+        p = np.asarray(packed, np.uint8)
+        return orig(((p >> 4) | (p << 4)).astype(np.uint8), scales)
+    monkeypatch.setattr(formats_mod, "mxfp4_dequant", swapped)
+    _fails(tfm.test_mxfp4_hand_built_blob_indexes_scales_by_row_and_32_block)
+    _fails(tfm.test_mxfp4_blob_follows_the_mx_conversion)
+
+
+def test_pinning_the_least_read_experts_is_caught(monkeypatch):
+    import oracle.static_split as ss_mod
+    from tests import test_oracle_static as ts
+
+    def coldest(prefill_ids, C, E):
+        L = len(prefill_ids)
+        reads = np.zeros(L * E, np.int64)
+        for l, ids in enumerate(prefill_ids):
+            for e in np.asarray(ids).ravel():
+                reads[l * E + int(e)] += 1
+        return set(sorted(range(L * E), key=lambda f: (int(reads[f]), f))[:max(0, min(C, L * E))])
+    monkeypatch.setattr(ss_mod, "prefill_pinned_placement", coldest)
+    _fails(ts.test_prefill_pinned_hand_example)
+    _fails(ts.test_prefill_pinned_is_a_maximum_coverage_subset_brute_force)
+
+
+def test_pinned_counts_merged_across_layers_is_caught(monkeypatch):
+    # counts reads per expert index, not per (layer, expert)
+    import oracle.static_split as ss_mod
+    from tests import test_oracle_static as ts
+
+    def merged(prefill_ids, C, E):
+        L = len(prefill_ids)
+        reads = np.zeros(E, np.int64)
+        for ids in prefill_ids:
+            for e in np.asarray(ids).ravel():
+                reads[int(e)] += 1
+        order = sorted(range(L * E), key=lambda f: (-int(reads[f % E]), f))
+        return set(order[:max(0, min(C, L * E))])
+    monkeypatch.setattr(ss_mod, "prefill_pinned_placement", merged)
+    _fails(ts.test_prefill_pinned_hand_example)
