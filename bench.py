@@ -492,6 +492,8 @@ def main(args):
         result["mxfp4_decode"] = fp4_measure(args, dev, local, b_pcie, b_cpu, "mxfp4")
     if not args.no_prefill and args.mode == "all":
         result["prefill"] = prefill_measure(args, dev, local)
+        if not args.no_nvfp4:
+            result["prefill_mxfp4"] = prefill_fp4_measure(args, dev, local, "mxfp4")
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = run_cpu_baseline(args.cpu_seconds, args.pool_blobs, (b_pcie, b_cpu))
     if rank == 0:
@@ -713,6 +715,58 @@ def prefill_measure(args, dev, local):
                         "throughput_loss = 1 - double/single wall time; the pages' 5090 figures: 0.19 at 4096, "
                         "0.25 at 8192, 0.26 at 16384 tokens",
                 "by_tokens": ablation}}
+
+
+def prefill_fp4_measure(args, dev, local, fmt):
+    """The prefill chunk with 4-bit experts: the host link carries 4-bit blobs
+    (2.51 MB for MXFP4 instead of 9.44 MB), and before its GEMMs each layer's
+    routed experts are decoded to bf16 in HBM.  Wall time of one chunk after a
+    warm-up chunk; the profile splits it into loads and decode + GEMMs."""
+    import torch
+    from serving_layer_moe_gb300 import MoECache
+    base = config("qwen3_prefill_8k").with_(T=args.prefill_tokens)
+    if args.capacity:
+        base = base.with_(capacity=args.capacity)
+    cfg = base.with_(shape=base.shape.__class__(**{**base.shape.__dict__, "wdtype": fmt}))
+    s = cfg.shape
+    arena, offs = make_pool(s, cfg.seed, n_phys=args.pool_blobs)
+    pool = torch.from_numpy(arena).pin_memory()
+    del arena
+    cache = MoECache(L=s.L, E=s.E, H=s.H, I=s.I, top_k=s.k, max_tokens=1, wdtype=s.wdtype, adtype=s.adtype,
+                     host_pool=pool, blob_offsets=offs, n_slots=cfg.capacity, bw_pcie_mbps=1000, bw_cpu_mbps=0,
+                     device=local, max_prefill_tokens=cfg.T)
+    x = torch.from_numpy(activations(cfg, 0, 0).view(np.int16)).to(dev)
+    routes = [prefill_routing(cfg, l) for l in range(s.L)]
+    ids = [torch.from_numpy(r[0]).to(dev) for r in routes]
+    ws = [torch.from_numpy(r[1]).to(dev) for r in routes]
+    out = torch.empty(cfg.T, s.H, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def chunk():
+        for l in range(s.L):
+            cache.prefill(l, x, ids[l], ws[l], out, stream=stream)
+
+    with torch.cuda.stream(stream):
+        chunk()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        chunk()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    wall_ms = e0.elapsed_time(e1)
+    cache.profile_start()
+    with torch.cuda.stream(stream):
+        chunk()
+    prof = cache.profile_stop()
+    cache.close()
+    return {"workload": f"qwen3_prefill_8k with {FP4_DESC[fmt]}: {cfg.T} tokens, 48 layers, C={cfg.capacity} slots",
+            "wall_ms": round(wall_ms, 2), "tokens_per_s": round(cfg.T / (wall_ms / 1e3), 1),
+            "blob_bytes": int(s.blob_bytes), "expert_bytes_per_chunk": int(s.L * s.E * s.blob_bytes),
+            "link_gbs_wall": round(s.L * s.E * s.blob_bytes / (wall_ms / 1e3) / 1e9, 1),
+            "decode_and_gemm_ms_in_chunk": round(prof["prefill_gemm"][0], 3),
+            "load_ms_in_chunk": round(prof["prefill_load"][0], 2)}
 
 
 def reference_arm(args, world, rank):

@@ -101,8 +101,8 @@ typedef enum moe_dtype {
  * S = 3*I*H*sizeof(w) (+ 4*(2I*H + H*I)/16384 for fp8; 3*I*H/2 + 3*I*H/16 + 16
  * for nvfp4; 3*I*H/2 + 3*I*H/32 for mxfp4).  H and I must be multiples of 128
  * (fp8), 32 (nvfp4, mxfp4) or 8 (f32, bf16).  NVFP4 and MXFP4 experts serve
- * decode calls of up to 2 tokens (max_tokens <= 2) and no prefill
- * (max_prefill_tokens = 0).
+ * decode calls of up to 2 tokens (max_tokens <= 2); their prefill decodes each
+ * layer's routed experts to bf16 for the grouped GEMM (see moe_layer_prefill).
  */
 typedef struct moe_config {
   int32_t n_layers;       /* L */
@@ -113,7 +113,7 @@ typedef struct moe_config {
   int32_t max_tokens;     /* largest T of a decode call (1..1024) */
   int32_t max_fetch;      /* K: fills per layer per call; < 0 = min(E, max_tokens * k) */
   int32_t wdtype;         /* moe_dtype of the expert weights */
-  int32_t adtype;         /* activations: MOE_F32 or MOE_BF16 (prefill needs MOE_BF16 + bf16 weights) */
+  int32_t adtype;         /* activations: MOE_F32 or MOE_BF16 (prefill needs MOE_BF16 and bf16 / nvfp4 / mxfp4 weights) */
   int32_t n_shared;       /* 0, or 1 always-resident shared expert per layer (gate 1.0) */
   uint32_t bw_pcie_mbps;  /* B_pcie in MB/s (> 0 unless bw_cpu_mbps > 0) */
   uint32_t bw_cpu_mbps;   /* B_cpu = B_H - B_P in MB/s; 0 = offload mode (every miss fills, up to K) */
@@ -175,10 +175,14 @@ moe_status moe_layer_decode(moe_cache* cache, int32_t layer, int32_t T, const vo
 
 /*
  * One MoE layer of a prefill chunk of T tokens (1 <= T <= max_prefill_tokens), bf16
- * activations and bf16 weights.  Full-layer mode (C >= 2E): makes layer `layer`
- * resident, starts loading all of layer+1 on the transfer stream, runs the grouped
- * GEMM on `stream`, and marks the layer's E experts used.  C < 2E: loads the routed
- * experts of the layer on demand, at most C at a time.
+ * activations and bf16, nvfp4 or mxfp4 weights.  Full-layer mode (C >= 2E): makes
+ * layer `layer` resident, starts loading all of layer+1 on the transfer stream, runs
+ * the grouped GEMM on `stream`, and marks the layer's E experts used.  C < 2E: loads
+ * the routed experts of the layer on demand, at most C at a time.  4-bit experts stay
+ * 4-bit in their slots (the host link carries 4-bit blobs); before the GEMMs each
+ * routed expert is decoded to a bf16 blob in a device staging area of E * 6*I*H
+ * bytes that the cache allocates at create time (MXFP4 values are exact in bf16,
+ * NVFP4 values e2m1 * e4m3 * g are rounded to nearest bf16).
  *   x_dev [T, H] bf16, topk_ids_dev / topk_w_dev [T, k], out_dev [T, H] fp32 (overwritten).
  * Errors: MOE_EINVAL, MOE_EDEVICE, MOE_ECUDA.
  */

@@ -122,7 +122,6 @@ extern "C" moe_status moe_cache_create(const moe_config* cfg, const void* host_p
   if (k.wdtype == MOE_NVFP4 || k.wdtype == MOE_MXFP4) {
     if (k.hidden % 32 || k.inter % 32) return fail(MOE_EINVAL, "fp4 weights need H and I multiples of 32");
     if (k.max_tokens > 2) return fail(MOE_EINVAL, "fp4 weights serve decode calls of at most 2 tokens");
-    if (k.max_prefill_tokens != 0) return fail(MOE_EINVAL, "fp4 weights have no prefill path");
   }
   if (k.n_shared != 0 && k.n_shared != 1) return fail(MOE_EINVAL, "n_shared must be 0 or 1");
   if (k.n_shared && !shared_host) return fail(MOE_EINVAL, "n_shared = 1 needs shared_host");

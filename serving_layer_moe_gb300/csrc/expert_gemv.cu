@@ -26,6 +26,7 @@
 
 #include "internal.cuh"
 
+#include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_fp4.h>
 
@@ -124,6 +125,15 @@ template <> struct WFmt<MOE_NVFP4> : E2M1Codes {
     const float2 sf = __half22float2(*reinterpret_cast<const __half2*>(&sr));
     return fmaf(hi, sf.y, lo * sf.x);
   }
+  // the chunk's 32 weights: e2m1 * block scale * g (g = the matrix's fp32 scale)
+  __device__ static __forceinline__ void decode32(const uint4& w, uint32_t s2, float g, float* f) {
+    unpack(w, f);
+    const __half2_raw sr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(s2 & 0xffffu), __NV_E4M3);
+    const float2 sf = __half22float2(*reinterpret_cast<const __half2*>(&sr));
+    const float a = sf.x * g, b = sf.y * g;
+#pragma unroll
+    for (int v = 0; v < 16; ++v) { f[v] *= a; f[16 + v] *= b; }
+  }
 };
 
 // OCP MX E8M0 scale: 2^(code - 127), code 255 NaN.  Codes 1..254 are the fp32
@@ -148,6 +158,13 @@ template <> struct WFmt<MOE_MXFP4> : E2M1Codes {
 #pragma unroll
     for (int v = 0; v < 16; ++v) hi = fmaf(f[16 + v], x[16 + v], hi);
     return (lo + hi) * e8m0_to_f32(s & 0xffu);
+  }
+  // the chunk's 32 weights: e2m1 * 2^(scale - 127), exact in fp32 and in bf16
+  __device__ static __forceinline__ void decode32(const uint4& w, uint32_t s, float, float* f) {
+    unpack(w, f);
+    const float sc = e8m0_to_f32(s & 0xffu);
+#pragma unroll
+    for (int v = 0; v < 32; ++v) f[v] *= sc;
   }
 };
 
@@ -1687,6 +1704,46 @@ __global__ void combine_kernel(int T, int H, int k, int n_shared, const float* _
 }
 
 // ---- blob copy: complete experts host pool -> slots ---------------------------------
+// Prefill with 4-bit experts: every active expert e of the layer that has routed
+// rows (offsets[e + 1] > offsets[e]), read from its slot wslot[e], is written as a bf16 blob of the bank layout (W_gu [2I, H], then
+// W_d [H, I]) at staging + e * 3IH, which the grouped GEMMs read.  One thread per
+// 16-byte chunk of codes (32 weights); the chunks of W_gu and W_d are contiguous in
+// the slot, and so are their scale entries (one scale_t per chunk).
+template <int WT>
+__global__ void __launch_bounds__(256) fp4_to_bf16_kernel(const int32_t* __restrict__ wslot,
+                                                          const int32_t* __restrict__ active,
+                                                          const int32_t* __restrict__ offsets, int E, int H, int I,
+                                                          const uint8_t* __restrict__ slots, uint64_t S,
+                                                          uint16_t* __restrict__ staging) {
+  using F = WFmt<WT>;
+  const long n_gu = (long)2 * I * H / 32;               // chunks of W_gu
+  const long per = n_gu + (long)H * I / 32;             // chunks per expert
+  const long total = (long)E * per;
+  for (long it = (long)blockIdx.x * blockDim.x + threadIdx.x; it < total; it += (long)gridDim.x * blockDim.x) {
+    const int e = (int)(it / per);
+    const int slot = wslot[e];
+    if (!active[e] || slot < 0 || offsets[e + 1] <= offsets[e]) continue;
+    const long c = it - (long)e * per;
+    const uint8_t* b = slots + (size_t)slot * S;
+    const uint4 w = __ldcs(reinterpret_cast<const uint4*>(b) + c);
+    const uint32_t sc = reinterpret_cast<const typename F::scale_t*>(b + F::sgu_off(H, I))[c];
+    float g = 1.f;
+    if constexpr (WT == MOE_NVFP4) g = reinterpret_cast<const float*>(b + F::g_off(H, I))[c < n_gu ? 0 : 1];
+    float f[32];
+    F::decode32(w, sc, g, f);
+    uint4 o[4];
+    uint32_t* ow = reinterpret_cast<uint32_t*>(o);
+#pragma unroll
+    for (int v = 0; v < 16; ++v) {
+      const __nv_bfloat162 p = __floats2bfloat162_rn(f[2 * v], f[2 * v + 1]);
+      ow[v] = *reinterpret_cast<const uint32_t*>(&p);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(staging + (size_t)e * 3 * (size_t)I * H + (size_t)c * 32);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) dst[q] = o[q];
+  }
+}
+
 // list = (flat id, slot) pairs; the copy starts at pair *skip (if skip) and takes *count
 // pairs.  Every CTA copies its 1/gridDim share of every blob, so one launch spreads
 // any number of blobs over the whole grid with 16-byte loads, 4 in flight per thread.
@@ -2179,6 +2236,18 @@ cudaError_t launch_copy_blobs(const int32_t* count, const int32_t* skip, const i
                               const uint8_t* host_pool_dev, const uint64_t* offsets, uint8_t* slots,
                               uint64_t S, int n_ctas, cudaStream_t s) {
   copy_blobs_kernel<<<n_ctas, 512, 0, s>>>(count, skip, list, host_pool_dev, offsets, slots, S);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fp4_to_bf16(const Shape& sh, const int32_t* wslot, const int32_t* active, const int32_t* offsets,
+                               const uint8_t* slots, uint16_t* staging, int sms, cudaStream_t s) {
+  const int grid = sms * 8;
+  if (sh.wdtype == MOE_NVFP4)
+    fp4_to_bf16_kernel<MOE_NVFP4><<<grid, 256, 0, s>>>(wslot, active, offsets, sh.E, sh.H, sh.I, slots, sh.S, staging);
+  else if (sh.wdtype == MOE_MXFP4)
+    fp4_to_bf16_kernel<MOE_MXFP4><<<grid, 256, 0, s>>>(wslot, active, offsets, sh.E, sh.H, sh.I, slots, sh.S, staging);
+  else
+    return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
 

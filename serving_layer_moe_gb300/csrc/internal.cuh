@@ -103,6 +103,11 @@ cudaError_t launch_fill(const Shape& sh, const int32_t* plan, const int32_t* fil
 cudaError_t launch_copy_blobs(const int32_t* count, const int32_t* skip, const int32_t* list,
                               const uint8_t* host_pool_dev, const uint64_t* offsets, uint8_t* slots,
                               uint64_t S, int n_ctas, cudaStream_t s);
+// Prefill with NVFP4 / MXFP4 experts: the active experts of the layer that have
+// routed rows (active[e] != 0, offsets[e + 1] > offsets[e], slot wslot[e]) decoded
+// from their slots to bf16 blobs at staging + e * 3IH.
+cudaError_t launch_fp4_to_bf16(const Shape& sh, const int32_t* wslot, const int32_t* active, const int32_t* offsets,
+                               const uint8_t* slots, uint16_t* staging, int sms, cudaStream_t s);
 cudaError_t launch_expert_gemv(const Shape& sh, int pass, int T, const void* x, DecodeBufs b,
                                int sms, cudaStream_t s);
 cudaError_t launch_fill_gate_up(const Shape& sh, int T, const void* x, DecodeBufs b, const uint8_t* host_pool_dev,

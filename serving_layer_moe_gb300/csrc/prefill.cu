@@ -53,6 +53,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <vector>
 
 namespace moe {
 
@@ -86,6 +87,8 @@ struct PrefillState {
   int32_t* active = nullptr;    // [E] expert computed in this round
   int32_t* loads = nullptr;     // [2 * 2E] (flat id, slot): this layer's loads, then prefetch
   int32_t* n_loads = nullptr;   // [2] loads of this layer, prefetched loads of the next
+  uint16_t* wbf = nullptr;      // 4-bit experts: [E, 3IH] bf16 blobs the GEMMs read, expert e at e * 3IH
+  int32_t* ident = nullptr;     // 4-bit experts: [E] = 0..E-1, the GEMMs' "slot" of expert e in wbf
   CUtensorMap tm_a1, tm_a2, tm_b1, tm_b2;
   const void* b_maps_pool = nullptr;  // pool the B maps were built for
   uint64_t b_maps_C = 0;
@@ -739,10 +742,22 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool fp4_weights(const moe_cache* c) { return c->sh.wdtype == MOE_NVFP4 || c->sh.wdtype == MOE_MXFP4; }
+
+// The B maps view bf16 expert blobs as rows: the slot pool itself, or for 4-bit
+// experts the bf16 staging area (fixed; built once).
 moe_status refresh_b_maps(moe_cache* c) {
   PrefillState* ps = state_of(c);
-  if (ps->b_maps_pool == c->slots && ps->b_maps_C == c->C) return MOE_OK;
   const uint64_t H = c->sh.H, I = c->sh.I;
+  if (fp4_weights(c)) {
+    if (ps->b_maps_pool == ps->wbf) return MOE_OK;
+    const uint64_t E = c->sh.E;
+    if (!make_map(&ps->tm_b1, ps->wbf, H, E * 3 * I) || !make_map(&ps->tm_b2, ps->wbf, I, E * 3 * H))
+      return fail(MOE_ECUDA, "cuTensorMapEncodeTiled failed for the bf16 staging area");
+    ps->b_maps_pool = ps->wbf;
+    return MOE_OK;
+  }
+  if (ps->b_maps_pool == c->slots && ps->b_maps_C == c->C) return MOE_OK;
   if (!make_map(&ps->tm_b1, c->slots, H, c->C * 3 * I) || !make_map(&ps->tm_b2, c->slots, I, c->C * 3 * H))
     return fail(MOE_ECUDA, "cuTensorMapEncodeTiled failed for the slot pool");
   ps->b_maps_pool = c->slots;
@@ -754,8 +769,8 @@ moe_status refresh_b_maps(moe_cache* c) {
 
 moe_status prefill_init(moe_cache* c) {
   const moe_config& k = c->cfg;
-  if (k.wdtype != MOE_BF16 || k.adtype != MOE_BF16)
-    return fail(MOE_EINVAL, "prefill needs bf16 weights and bf16 activations");
+  if ((k.wdtype != MOE_BF16 && k.wdtype != MOE_NVFP4 && k.wdtype != MOE_MXFP4) || k.adtype != MOE_BF16)
+    return fail(MOE_EINVAL, "prefill needs bf16, nvfp4 or mxfp4 weights and bf16 activations");
   if (k.hidden % BN || k.inter % 128)
     return fail(MOE_EINVAL, "prefill needs H a multiple of 256 and I a multiple of 128");
   if (!get_encode()) return fail(MOE_ECUDA, "cuTensorMapEncodeTiled is not available");
@@ -781,6 +796,15 @@ moe_status prefill_init(moe_cache* c) {
   ps->loads = p; p += 4 * E;
   ps->n_loads = p; p += 2;
   c->dev_bytes += (size_t)ps->P_max * (k.hidden + k.inter) * 2 + ints * 4;
+  if (fp4_weights(c)) {
+    const size_t wb = (size_t)E * 3 * k.inter * k.hidden * 2;
+    CK(cudaMalloc(&ps->wbf, wb));
+    CK(cudaMalloc(&ps->ident, (size_t)E * 4));
+    std::vector<int32_t> id(E);
+    for (int e = 0; e < E; ++e) id[e] = e;
+    CK(cudaMemcpy(ps->ident, id.data(), (size_t)E * 4, cudaMemcpyHostToDevice));
+    c->dev_bytes += wb + (size_t)E * 4;
+  }
   if (!make_map(&ps->tm_a1, ps->xs, k.hidden, ps->P_max) || !make_map(&ps->tm_a2, ps->hs, k.inter, ps->P_max))
     return fail(MOE_ECUDA, "cuTensorMapEncodeTiled failed for the activation buffers");
   CK(cudaEventCreateWithFlags(&ps->ev_ctrl, cudaEventDisableTiming));
@@ -797,6 +821,8 @@ void prefill_free(moe_cache* c) {
   cudaFree(ps->xs);
   cudaFree(ps->hs);
   cudaFree(ps->ibuf);
+  cudaFree(ps->wbf);
+  cudaFree(ps->ident);
   if (ps->ev_ctrl) cudaEventDestroy(ps->ev_ctrl);
   if (ps->ev_cur) cudaEventDestroy(ps->ev_cur);
   delete ps;
@@ -810,7 +836,7 @@ static moe_status run_gemms(moe_cache* c, int T, const float* w, float* out, cud
   GemmArgs g{};
   g.mtiles = ps->mtiles;
   g.n_mtiles = ps->n_mtiles;
-  g.wslot = ps->wslot;
+  g.wslot = fp4_weights(c) ? ps->ident : ps->wslot;
   g.hs = ps->hs;
   g.I = sh.I;
   g.perm = ps->perm;
@@ -922,6 +948,8 @@ extern "C" moe_status moe_layer_prefill(moe_cache* c, int32_t layer, int32_t T, 
     CK(cudaStreamWaitEvent(s, ps->ev_cur, 0));
     {
       ProfScope p(c, s, PROF_PREFILL_GEMM);
+      if (fp4_weights(c))   // this round's experts, now resident, decoded to bf16 for the GEMMs
+        CK(launch_fp4_to_bf16(sh, ps->wslot, ps->active, ps->offsets, c->slots, ps->wbf, c->sms, s));
       st = run_gemms(c, T, w, out, s);
       if (st != MOE_OK) return st;
     }

@@ -319,14 +319,22 @@ def test_fp4_split_merges_exactly(fmt):
 
 
 @pytest.mark.parametrize("fmt", FP4)
-def test_fp4_rejects_larger_batches_and_prefill(fmt):
+def test_fp4_rejects_larger_batches_and_misshaped_prefill(fmt):
     import torch
     from serving_layer_moe_gb300 import MoECache, MoEError
     from workloads import Shape
     s = Shape(L=1, E=8, k=2, H=256, I=128, wdtype=fmt, adtype="bf16")
     pool = torch.zeros(8 * s.blob_bytes, dtype=torch.uint8).pin_memory()
-    for kw in ({"max_tokens": 4}, {"max_tokens": 1, "max_prefill_tokens": 64}):
+    # decode batches above 2 tokens; prefill with fp32 activations or H not a multiple of 256
+    for kw in ({"max_tokens": 4}, {"max_tokens": 1, "max_prefill_tokens": 64, "adtype": "f32"},
+               {"max_tokens": 1, "max_prefill_tokens": 64, "H": 160}):
+        args = dict(L=1, E=8, H=256, I=128, top_k=2, wdtype=fmt, adtype="bf16", host_pool=pool, n_slots=4,
+                    bw_pcie_mbps=1000, bw_cpu_mbps=0)
+        args.update(kw)
         with pytest.raises(MoEError) as ei:
-            MoECache(L=1, E=8, H=256, I=128, top_k=2, wdtype=fmt, adtype="bf16", host_pool=pool, n_slots=4,
-                     bw_pcie_mbps=1000, bw_cpu_mbps=0, **kw)
+            MoECache(**args)
         assert ei.value.status == 1
+    # a 2-token decode cache with prefill is fine
+    c = MoECache(L=1, E=8, H=256, I=128, top_k=2, wdtype=fmt, adtype="bf16", host_pool=pool, n_slots=4,
+                 bw_pcie_mbps=1000, bw_cpu_mbps=0, max_tokens=2, max_prefill_tokens=64)
+    c.close()

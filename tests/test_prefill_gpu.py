@@ -27,7 +27,9 @@ def _make(cfg, C, n_phys=None, max_tokens=None):
     s = cfg.shape
     arena, offs = make_pool(s, cfg.seed, n_phys=n_phys)
     pool = torch.from_numpy(arena).pin_memory()
-    cache = MoECache(L=s.L, E=s.E, H=s.H, I=s.I, top_k=s.k, max_tokens=max_tokens or 16, wdtype=s.wdtype,
+    if max_tokens is None:   # 4-bit caches take decode calls of at most 2 tokens
+        max_tokens = 2 if s.wdtype in ("nvfp4", "mxfp4") else 16
+    cache = MoECache(L=s.L, E=s.E, H=s.H, I=s.I, top_k=s.k, max_tokens=max_tokens, wdtype=s.wdtype,
                      adtype=s.adtype, host_pool=pool, blob_offsets=offs, n_slots=C, bw_pcie_mbps=1000,
                      bw_cpu_mbps=0, device=0, max_prefill_tokens=cfg.T)
     store = ExpertStore(arena, offs, s.wdtype, s.H, s.I, s.blob_bytes, memo=2 * s.E + 4)
@@ -229,3 +231,66 @@ def test_prefill_rejects_bad_config():
     with pytest.raises(MoEError):   # fp32 weights cannot run the bf16 tensor-core prefill
         MoECache(L=s.L, E=s.E, H=s.H, I=s.I, top_k=s.k, max_tokens=4, wdtype="f32", adtype="f32",
                  host_pool=arena, blob_offsets=offs, n_slots=4, max_prefill_tokens=64)
+
+
+# ---- 4-bit experts: the slots and the host link carry NVFP4 / MXFP4 blobs; the
+# grouped GEMMs read each routed expert decoded to bf16 ----
+
+FP4 = ["nvfp4", "mxfp4"]
+
+
+def _fp4(cfg, fmt):
+    return cfg.with_(shape=Shape(**{**cfg.shape.__dict__, "wdtype": fmt}))
+
+
+@pytest.mark.parametrize("fmt", FP4)
+def test_fp4_small_full_layer_on_demand_and_ragged(fmt):
+    cfg = _fp4(SMALL, fmt)
+    worst, _ = _run_prefill(cfg, C=16, layers=[0, 1, 2])
+    assert worst <= (5e-3 if fmt == "mxfp4" else TOL)     # MXFP4 weights are exact in bf16
+    _run_prefill(cfg, C=3, layers=[0, 1, 2])               # on demand, groups of 3 routed experts
+    _run_prefill(cfg.with_(T=7), C=12, layers=[1, 0, 1])   # ragged chunk, one on-demand group
+    _run_prefill(cfg, C=17, layers=[2, 0, 1], prefetch_next=[True, False, True])
+
+
+@pytest.mark.parametrize("fmt", FP4)
+def test_fp4_qwen3_shape_1k_tokens(fmt):
+    cfg = _fp4(config("qwen3_prefill_8k").with_(T=1024), fmt)
+    _run_prefill(cfg, C=300, layers=[0, 1, 2], n_phys=64, sample=128)
+
+
+def test_mxfp4_prefill_survivors_seed_decode():
+    # the 4-bit slots a prefill loads are the ones decode then reads
+    import torch
+    cfg = _fp4(SMALL, "mxfp4")
+    s = cfg.shape
+    dev = torch.device("cuda", 0)
+    cache, store = _make(cfg, 16, max_tokens=2)
+    ora = SlotCache(s.L, s.E, 16, K=min(s.E, 2 * s.k), b_pcie=1000, b_cpu=0)
+    out = torch.empty(cfg.T, s.H, device=dev)
+    for l in range(s.L):
+        ids, w = prefill_routing(cfg, l)
+        ora.prefill(l, ids)
+        cache.prefill(l, torch_act(activations(cfg, 0, l), dev), torch.from_numpy(ids).to(dev),
+                      torch.from_numpy(w).to(dev), out)
+    dcfg = cfg.with_(T=2, steps=6, prefill=False)
+    ids, w = routing_trace(dcfg)
+    sm = torch.empty(2, s.k, dtype=torch.int32, device=dev)
+    o2 = torch.empty(2, s.H, device=dev)
+    hits = 0
+    for st in range(dcfg.steps):
+        for l in range(s.L):
+            plan = ora.decode(l, ids[st, l])
+            hits += len(plan.hits)
+            x = activations(dcfg, st, l)
+            cache.decode(l, torch_act(x, dev), torch.from_numpy(ids[st, l]).to(dev),
+                         torch.from_numpy(w[st, l]).to(dev), o2, slot_map=sm)
+            torch.cuda.synchronize()
+            assert np.array_equal(sm.cpu().numpy(), plan.slot_map)
+            if (plan.slot_map >= 0).all():
+                y = pair_outputs(store, l, s.E, x, s.adtype, ids[st, l])
+                ref = combine(w[st, l], y, plan.slot_map, None)
+                assert relative_max_error(o2.cpu().numpy(), ref) <= TOL
+    _check_state(cache, ora)
+    assert hits > 0
+    cache.close()
