@@ -484,6 +484,9 @@ def main(args):
                  "bench_bw_B_P_gbs": round(bp_gbs, 1), "note": "fill kernel (with the filled experts' gate/up) "
                  "on the side stream, concurrent with the resident-expert GEMV; bytes = filled blobs"},
         "control_us": round(1e3 * prof["control"][0] / max(1, prof["control"][1]), 2),
+        "control_us_all_resident": round(1e3 * res_prof["control"][0] / max(1, res_prof["control"][1]), 2),
+        "control_note": "event pair around the control kernel in the replayed graph (its launch and grid-"
+                        "dependency wait included), in the timed step and in the all-resident replay",
         "clocks": clk.summary(),
     }
     if args.mode == "all" and not args.no_nvfp4:
