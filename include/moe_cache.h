@@ -100,9 +100,12 @@ typedef enum moe_dtype {
  *   weight is e2m1(code) * 2^(scale code - 127), scale code 255 being NaN.
  * S = 3*I*H*sizeof(w) (+ 4*(2I*H + H*I)/16384 for fp8; 3*I*H/2 + 3*I*H/16 + 16
  * for nvfp4; 3*I*H/2 + 3*I*H/32 for mxfp4).  H and I must be multiples of 128
- * (fp8), 32 (nvfp4, mxfp4) or 8 (f32, bf16).  NVFP4 and MXFP4 experts serve
- * decode calls of up to 2 tokens (max_tokens <= 2); their prefill decodes each
- * layer's routed experts to bf16 for the grouped GEMM (see moe_layer_prefill).
+ * (fp8), 32 (nvfp4, mxfp4) or 8 (f32, bf16), and S a multiple of 16 bytes (for
+ * fp8: the scale count (2I/128)(H/128) + (H/128)(I/128) a multiple of 4);
+ * otherwise moe_cache_create and moe_layer_ffn_noalloc return MOE_EINVAL.
+ * NVFP4 and MXFP4 experts serve decode calls of up to 2 tokens (max_tokens <=
+ * 2); their prefill decodes each layer's routed experts to bf16 for the
+ * grouped GEMM (see moe_layer_prefill).
  */
 typedef struct moe_config {
   int32_t n_layers;       /* L */

@@ -123,6 +123,11 @@ extern "C" moe_status moe_cache_create(const moe_config* cfg, const void* host_p
     if (k.hidden % 32 || k.inter % 32) return fail(MOE_EINVAL, "fp4 weights need H and I multiples of 32");
     if (k.max_tokens > 2) return fail(MOE_EINVAL, "fp4 weights serve decode calls of at most 2 tokens");
   }
+  // every slot and host blob starts on a 16-byte boundary (the kernels move 16-byte chunks)
+  if (blob_bytes(k.wdtype, k.hidden, k.inter) % 16)
+    return fail(MOE_EINVAL, "blob size S = %llu is not a multiple of 16 bytes (fp8: the scale count "
+                "(2I/128)(H/128) + (H/128)(I/128) must be a multiple of 4)",
+                (unsigned long long)blob_bytes(k.wdtype, k.hidden, k.inter));
   if (k.n_shared != 0 && k.n_shared != 1) return fail(MOE_EINVAL, "n_shared must be 0 or 1");
   if (k.n_shared && !shared_host) return fail(MOE_EINVAL, "n_shared = 1 needs shared_host");
   if ((uint64_t)k.bw_pcie_mbps + k.bw_cpu_mbps == 0) return fail(MOE_EINVAL, "B_pcie + B_cpu must be > 0");

@@ -153,6 +153,10 @@ extern "C" moe_status moe_layer_ffn_noalloc(int32_t n_experts, int32_t hidden, i
     return fail(MOE_EINVAL, "H and I must be positive multiples of 8");
   if (wdtype == MOE_FP8E4M3_B128 && (hidden % 128 || inter % 128))
     return fail(MOE_EINVAL, "fp8 block-scaled weights need H and I multiples of 128");
+  if (blob_bytes(wdtype, hidden, inter) % 16)   // expert e starts at e * S, read in 16-byte chunks
+    return fail(MOE_EINVAL, "blob size S = %llu is not a multiple of 16 bytes (fp8: the scale count "
+                "(2I/128)(H/128) + (H/128)(I/128) must be a multiple of 4)",
+                (unsigned long long)blob_bytes(wdtype, hidden, inter));
   if (T < 0) return fail(MOE_EINVAL, "T must be >= 0");
   if (T == 0) return MOE_OK;
   if (!experts_dev || !x_dev || !topk_ids_dev || !topk_w_dev || !out_dev)
