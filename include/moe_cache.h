@@ -164,6 +164,8 @@ moe_status moe_cache_resize(moe_cache* cache, uint64_t n_slots);
  *                CPU-assigned (offload mode with K >= k*T and enough slots)
  *   out_dev      [T, H] fp32: sum_j w[t,j] * y[t,j] in j order (+ shared expert)
  *   slot_map_dev [T, k] int32 out, may be NULL: the slot each pair ran from, -1 = CPU
+ * x_dev, cpu_part_dev and out_dev must be 16-byte aligned, the int32 / fp32
+ * arrays 4-byte aligned (MOE_EINVAL otherwise, before anything is enqueued).
  * Errors: MOE_EINVAL, MOE_EDEVICE (earlier violation), MOE_ECUDA.
  * The resident experts run as a gate/up grid then a down + combine grid.  With
  * MOE_DECODE_FUSED=1 in the environment when the cache is created, one-token
@@ -187,6 +189,7 @@ moe_status moe_layer_decode(moe_cache* cache, int32_t layer, int32_t T, const vo
  * bytes that the cache allocates at create time (MXFP4 values are exact in bf16,
  * NVFP4 values e2m1 * e4m3 * g are rounded to nearest bf16).
  *   x_dev [T, H] bf16, topk_ids_dev / topk_w_dev [T, k], out_dev [T, H] fp32 (overwritten).
+ * x_dev and out_dev 16-byte aligned, topk_ids_dev / topk_w_dev 4-byte aligned.
  * Errors: MOE_EINVAL, MOE_EDEVICE, MOE_ECUDA.
  */
 moe_status moe_layer_prefill(moe_cache* cache, int32_t layer, int32_t T, const void* x_dev,
@@ -288,6 +291,7 @@ moe_status bench_bw(int32_t device, uint64_t expert_bytes, double* b_pcie_gbs, d
  *   experts_dev  the layer's E expert blobs back to back (bank layout above,
  *                S bytes each), device memory, 16-byte aligned
  *   x_dev [T, H] in adtype, topk_ids_dev / topk_w_dev [T, k], out_dev [T, H] fp32
+ *   (x_dev and out_dev 16-byte aligned, the id and gate arrays 4-byte aligned)
  * Ids outside [0, E) contribute nothing.  Enqueued on `stream`; never blocks.
  * wdtype MOE_F32, MOE_BF16 or MOE_FP8E4M3_B128 (MOE_NVFP4 and MOE_MXFP4 are
  * MOE_EINVAL here).

@@ -305,6 +305,10 @@ extern "C" moe_status moe_layer_decode(moe_cache* c, int32_t layer, int32_t T, c
   if (T < 0 || T > c->cfg.max_tokens) return fail(MOE_EINVAL, "T = %d outside [0, max_tokens]", T);
   if (T == 0) return MOE_OK;
   if (!x || !ids || !w || !out) return fail(MOE_EINVAL, "x, topk_ids, topk_w and out must not be NULL");
+  if (!aligned_to(x, 16) || !aligned_to(out, 16) || (cpu_part && !aligned_to(cpu_part, 16)))
+    return fail(MOE_EINVAL, "x, out and cpu_part must be 16-byte aligned");
+  if (!aligned_to(ids, 4) || !aligned_to(w, 4) || (slot_map && !aligned_to(slot_map, 4)))
+    return fail(MOE_EINVAL, "topk_ids, topk_w and slot_map must be 4-byte aligned");
   DeviceGuard guard(c->cfg.device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   c->last_T = T;

@@ -162,6 +162,9 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// pointer alignment the kernels' vector loads and bulk copies assume
+inline bool aligned_to(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
 // blob geometry
 inline uint64_t blob_bytes(int wdtype, int H, int I) {
   uint64_t HI = (uint64_t)H * (uint64_t)I;

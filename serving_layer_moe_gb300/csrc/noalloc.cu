@@ -162,6 +162,9 @@ extern "C" moe_status moe_layer_ffn_noalloc(int32_t n_experts, int32_t hidden, i
   if (!experts_dev || !x_dev || !topk_ids_dev || !topk_w_dev || !out_dev)
     return fail(MOE_EINVAL, "experts, x, topk_ids, topk_w and out must not be NULL");
   if (reinterpret_cast<uintptr_t>(experts_dev) % 16) return fail(MOE_EINVAL, "experts_dev must be 16-byte aligned");
+  if (!aligned_to(x_dev, 16) || !aligned_to(out_dev, 16)) return fail(MOE_EINVAL, "x and out must be 16-byte aligned");
+  if (!aligned_to(topk_ids_dev, 4) || !aligned_to(topk_w_dev, 4))
+    return fail(MOE_EINVAL, "topk_ids and topk_w must be 4-byte aligned");
   const NoAllocLayout lay = layout_for(T, top_k, n_experts, hidden, inter);
   if (lay.total > kNoAllocScratchBytes)
     return fail(MOE_ECAPACITY, "T * top_k * (H + I) needs %zu bytes of scratch; the fixed scratch holds %zu",

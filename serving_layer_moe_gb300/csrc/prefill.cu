@@ -894,6 +894,8 @@ extern "C" moe_status moe_layer_prefill(moe_cache* c, int32_t layer, int32_t T, 
   }
   if (T == 0) return MOE_OK;
   if (!x || !ids || !w || !out) return fail(MOE_EINVAL, "x, topk_ids, topk_w and out must not be NULL");
+  if (!aligned_to(x, 16) || !aligned_to(out, 16)) return fail(MOE_EINVAL, "x and out must be 16-byte aligned");
+  if (!aligned_to(ids, 4) || !aligned_to(w, 4)) return fail(MOE_EINVAL, "topk_ids and topk_w must be 4-byte aligned");
   DeviceGuard guard(c->cfg.device);
   moe_status st = refresh_b_maps(c);
   if (st != MOE_OK) return st;

@@ -114,3 +114,18 @@ def test_blob_sizes_off_the_16_byte_grid_are_refused_without_a_device_call(lib):
     cfg = MoEConfigC(1, 8, 512, 256, 2, 1, -1, MOE_FP8E4M3_B128, 1, 0, 1000, 0, 0, 0)
     assert lib.moe_cache_create(ctypes.byref(cfg), None, 0, None, None, 4, ctypes.byref(h)) == 1
     assert b"host_pool" in lib.moe_last_error()
+
+
+def test_noalloc_refuses_unaligned_pointers_without_a_device_call(lib):
+    # the pointers are never dereferenced: the checks run before any CUDA call
+    import ctypes
+    from serving_layer_moe_gb300.binding import MOE_BF16
+    P = ctypes.c_void_p
+    good = dict(e=P(0x10000), x=P(0x20000), i=P(0x30000), w=P(0x40000), o=P(0x50000))
+    for key, bad, word in (("x", 0x20008, b"16-byte"), ("o", 0x50004, b"16-byte"), ("i", 0x30002, b"4-byte"),
+                           ("w", 0x40001, b"4-byte")):
+        a = dict(good)
+        a[key] = P(bad)
+        st = lib.moe_layer_ffn_noalloc(8, 256, 512, 2, MOE_BF16, MOE_BF16, a["e"], 1, a["x"], a["i"], a["w"], a["o"],
+                                       None)
+        assert st == 1 and word in lib.moe_last_error(), key
