@@ -133,15 +133,26 @@ class MoECache:
         _check(load_library().moe_layer_decode(self._h, layer, T, x, ids, w, cpu_part, out, slot_map, stream))
 
     def decode_from_host(self, layer, x_host, ids_host, w_host, out_host, cpu_part=None, stream=None):
-        """decode() on page-locked host tensors: copy in, run, copy the output back (stream-ordered)."""
+        """decode() on page-locked host tensors: the copies in (cpu_part too, if it
+        is on the host), the call and the copy of the output back, all enqueued on
+        one stream (`stream`, else torch's current stream).  Returns out_host once
+        the copy back is enqueued: synchronise that stream before reading it."""
         import torch
         dev = torch.device("cuda", torch.cuda.current_device())
-        x = x_host.to(dev, non_blocking=True)
-        ids = ids_host.to(dev, non_blocking=True)
-        w = w_host.to(dev, non_blocking=True)
-        out = torch.empty(out_host.shape, dtype=torch.float32, device=dev)
-        self.decode(layer, x, ids, w, out, cpu_part=cpu_part, stream=stream)
-        out_host.copy_(out, non_blocking=True)
+        if stream is None:
+            s = torch.cuda.current_stream(dev)
+        elif isinstance(stream, torch.cuda.Stream):
+            s = stream
+        else:
+            s = torch.cuda.ExternalStream(int(stream), device=dev)
+        with torch.cuda.stream(s):
+            x = x_host.to(dev, non_blocking=True)
+            ids = ids_host.to(dev, non_blocking=True)
+            w = w_host.to(dev, non_blocking=True)
+            cp = None if cpu_part is None else cpu_part.to(dev, non_blocking=True)
+            out = torch.empty(out_host.shape, dtype=torch.float32, device=dev)
+            self.decode(layer, x, ids, w, out, cpu_part=cp, stream=s)
+            out_host.copy_(out, non_blocking=True)
         return out_host
 
     def prefill(self, layer, x, topk_ids, topk_w, out, stream=None):
