@@ -66,3 +66,21 @@ def test_pool_offsets_and_aliasing():
     arena2, offs2 = make_pool(c.shape, 5, n_phys=3)
     assert list(offs2) == [(i % 3) * c.shape.blob_bytes for i in range(8)]
     assert np.array_equal(arena2[: 3 * c.shape.blob_bytes], arena[: 3 * c.shape.blob_bytes])
+
+
+def test_four_bit_blobs_are_seeded_and_sized():
+    # the 4-bit variants of the Qwen3 shape: sizes the bench quotes, seeded bytes,
+    # and the host pool's flat-id -> blob mapping unchanged by the format
+    base = config("qwen3_decode_b1").shape
+    for fmt, size in (("nvfp4", 2654224), ("mxfp4", 2506752)):
+        s = base.__class__(**{**base.__dict__, "wdtype": fmt})
+        assert blob_bytes(s) == size and size % 16 == 0
+        small = base.__class__(L=2, E=4, k=2, H=256, I=128, wdtype=fmt, adtype="bf16")
+        assert np.array_equal(make_blob(small, 5, 1), make_blob(small, 5, 1))
+        assert not np.array_equal(make_blob(small, 5, 1), make_blob(small, 5, 2))
+        arena, offs = make_pool(small, 5, n_phys=3)
+        assert offs.shape == (small.L * small.E,)
+        for f in range(small.L * small.E):
+            o = int(offs[f])
+            assert o % 16 == 0
+            assert np.array_equal(arena[o:o + small.blob_bytes], make_blob(small, 5, f % 3))
