@@ -61,6 +61,8 @@ C_HITS, C_MISSES, C_FILLS, C_CPU, C_READ_HITS, C_READ_MISSES, C_DECODE_CALLS, C_
 
 @dataclass
 class DecodePlan:
+    """What one decode call decided (snackonai "The Architecture, Unpacked":
+    dedup, classify, split, victims, rewrite)."""
     layer: int
     uniq: list            # unique flat ids, ascending
     hits: list            # resident unique flat ids, ascending
@@ -74,6 +76,8 @@ class DecodePlan:
 
 @dataclass
 class PrefillPlan:
+    """What one prefill call loaded and computed (ai.thesatyajit.com "Prefill:
+    hide the pool behind the wire")."""
     layer: int
     loads: list           # [(flat id, slot)]: missing experts of this layer (or group) first
     prefetch: list        # [(flat id, slot)]: experts of layer+1 loaded ahead (full-layer mode)
@@ -84,6 +88,10 @@ class PrefillPlan:
 
 @dataclass
 class SlotCache:
+    """C slots shared by every layer, indexed by flat id l*E+e, with one LRU
+    list (snackonai "The Architecture, Unpacked"; ai.thesatyajit.com
+    "Residency that follows the router").  b_pcie / b_cpu are the two
+    bandwidths of the split rule, K the fetch cap."""
     L: int
     E: int
     C: int
@@ -121,6 +129,10 @@ class SlotCache:
 
     # -- decode: one MoE layer -------------------------------------------------
     def decode(self, layer: int, topk_ids: np.ndarray) -> DecodePlan:
+        """One MoE layer's decode control (snackonai "The Architecture, Unpacked",
+        "The split policy itself"): dedup the routed flat ids, classify them,
+        fill the first q misses into the K least-recent victims, send the rest
+        to the CPU, and refresh the recency of every GPU-run expert."""
         ids = np.asarray(topk_ids)
         assert ids.ndim == 2
         assert 0 <= layer < self.L
@@ -158,6 +170,10 @@ class SlotCache:
 
     # -- prefill: one MoE layer of a chunk ------------------------------------
     def prefill(self, layer: int, topk_ids: np.ndarray, prefetch_next: bool = True) -> PrefillPlan:
+        """One MoE layer of a prefill chunk (ai.thesatyajit.com "Prefill: hide the
+        pool behind the wire"): full-layer residency of l (and of l+1 when
+        prefetch_next) if C >= 2E, else the routed experts of l on demand in
+        groups of at most C."""
         ids = np.asarray(topk_ids)
         E = self.E
         if ids.size and (ids.min() < 0 or ids.max() >= E):
@@ -223,6 +239,8 @@ class SlotCache:
 
     # -- state readout --------------------------------------------------------
     def state(self):
+        """(slot -> flat id, slot stamps, flat id -> slot, counters, clock): the
+        state the CUDA library reads out, in the same layout."""
         s2e = np.full(self.C, -1, np.int32)
         st = np.zeros(self.C, np.uint64)
         e2s = np.full(self.L * self.E, -1, np.int32)

@@ -30,6 +30,8 @@ from .formats import activations_to_f64, parse_blob
 
 
 def silu(z: np.ndarray) -> np.ndarray:
+    """silu(z) = z * sigmoid(z), the SwiGLU gate of the expert (reading: the
+    pages do not write the expert out; Qwen3 and DeepSeek-V3 experts are SwiGLU)."""
     z = np.asarray(z, dtype=np.float64)
     return z / (1.0 + np.exp(-z))
 
@@ -100,10 +102,13 @@ class ExpertStore:
         self._n = memo
 
     def blob(self, f: int) -> np.ndarray:
+        """The S bytes of flat id f in the pool (snackonai "The Architecture,
+        Unpacked": a slot, like a pool entry, holds one complete expert)."""
         o = int(self.offsets[f])
         return self.arena[o:o + self.S]
 
     def weights(self, f: int):
+        """(W_gate, W_up, W_down) of flat id f as float64, decoded exactly."""
         key = int(self.offsets[f])
         if key in self._memo:
             self._memo.move_to_end(key)
@@ -115,6 +120,7 @@ class ExpertStore:
         return w
 
     def expert(self, f: int, x: np.ndarray) -> np.ndarray:
+        """The SwiGLU expert f applied to x [..., H] in float64."""
         return swiglu_expert(x, *self.weights(f))
 
 
@@ -139,6 +145,9 @@ def pair_outputs(store: ExpertStore, layer: int, E: int, x: np.ndarray, adtype: 
 
 def shared_outputs(shared_blobs: np.ndarray, layer: int, wdtype: str, H: int, I: int,
                    blob_bytes: int, x: np.ndarray, adtype: str) -> np.ndarray:
+    """The always-resident shared expert of `layer` applied to x (reading: the
+    DeepSeek-V3 shape's shared expert; signalovernoise.tech and dev.to: the
+    non-expert weights stay on the GPU), added last by the combine."""
     blob = shared_blobs[layer * blob_bytes:(layer + 1) * blob_bytes]
     return swiglu_expert(activations_to_f64(x, adtype), *parse_blob(blob, wdtype, H, I))
 

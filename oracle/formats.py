@@ -28,6 +28,7 @@ import numpy as np
 
 
 def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> float64: the upper half of a binary32."""
     u = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
     return u.view(np.float32).astype(np.float64)
 
@@ -47,6 +48,7 @@ E4M3_TABLE = np.array([_e4m3_value(c) for c in range(256)], dtype=np.float64)
 
 
 def e4m3_codes_to_f64(codes: np.ndarray) -> np.ndarray:
+    """OCP e4m3 ("fn") codes -> float64 through the 256-entry table above."""
     return E4M3_TABLE[np.asarray(codes, dtype=np.uint8)]
 
 
@@ -159,6 +161,7 @@ def parse_blob(blob: np.ndarray, wdtype: str, H: int, I: int):
 
 
 def activations_to_f64(x: np.ndarray, adtype: str) -> np.ndarray:
+    """Activations as carried (float32, or bf16 bit patterns) -> float64."""
     if adtype == "f32":
         return np.asarray(x, dtype=np.float32).astype(np.float64)
     if adtype == "bf16":
