@@ -435,6 +435,32 @@ def main(args):
     gemv_launches = prof["gemv_resident"][1]         # one per MoE-layer decode
     fill_bytes = int(cnt_p1[2] - cnt_p0[2]) * s.blob_bytes
     total_prof_ms = sum(v[0] for v in prof.values())
+    # Distribution of whole MoE-layer decode times (median, p90), after the timed
+    # region: eager calls, one event pair around each layer's call on its stream,
+    # fills included where they occur.  Reported beside the means; a failure here
+    # leaves the rest of the line intact.
+    try:
+        lat_steps = 8
+        lat_ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(s.L)] for _ in range(lat_steps)]
+        with torch.cuda.stream(stream):
+            for st_i in range(lat_steps):
+                stage(step)
+                step += 1
+                for l in range(s.L):
+                    xp, ip, wp, op = layer_bytes[l]
+                    lat_ev[st_i][l][0].record(stream)
+                    cache.decode_ptrs(l, cfg.T, xp, ip, wp, cpu_part.data_ptr(), op, None, sp)
+                    lat_ev[st_i][l][1].record(stream)
+        torch.cuda.synchronize(dev)
+        lat_us = np.array([1e3 * a.elapsed_time(b) for row in lat_ev for a, b in row])
+        layer_step_us = {"median": round(float(np.median(lat_us)), 2),
+                         "p90": round(float(np.percentile(lat_us, 90)), 2),
+                         "mean": round(float(lat_us.mean()), 2), "n": int(lat_us.size),
+                         "note": "eager calls after the timed region, an event pair around each MoE-layer "
+                                 "decode (launch gaps included, so above the graph-replayed mean)"}
+    except Exception as exc:   # diagnostics only
+        layer_step_us = {"error": repr(exc)[:200]}
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -484,6 +510,7 @@ def main(args):
                  "bench_bw_B_P_gbs": round(bp_gbs, 1), "note": "fill kernel (with the filled experts' gate/up) "
                  "on the side stream, concurrent with the resident-expert GEMV; bytes = filled blobs"},
         "control_us": round(1e3 * prof["control"][0] / max(1, prof["control"][1]), 2),
+        "layer_step_us": layer_step_us,
         "control_us_all_resident": round(1e3 * res_prof["control"][0] / max(1, res_prof["control"][1]), 2),
         "control_note": "event pair around the control kernel in the replayed graph (its launch and grid-"
                         "dependency wait included), in the timed step and in the all-resident replay",
