@@ -41,10 +41,11 @@ def lru_miss_rate(counters) -> float:
 #
 # Passage followed: "FreeToken: a 753B model on one GPU, and the two bandwidths
 # that decide everything" (ai.thesatyajit.com), section "Residency that follows
-# the router": the comparator engine pins a hot subset of experts chosen at
-# prefill time and serves the rest from the CPU; replayed on the same routing
-# at equal capacity its prefill-updated placement misses more decode reads than
-# the global LRU and fewer than the routing-blind split.
+# the router": the comparator engine decides, when a prompt is prefilled, which
+# frequently used experts stay on the GPU, keeps that choice fixed while it
+# decodes, and runs every other expert on the CPU.  On identical routing and
+# capacity, that placement loses more decode reads to misses than the global
+# LRU and fewer than the routing-blind split.
 #
 # Readings taken (the pages name the policy but give no rule):
 #   * the hot subset is the C (layer, expert) pairs read most often by the
