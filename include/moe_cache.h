@@ -1,19 +1,20 @@
 /*
- * moe_cache.h -- C ABI of libmoecache.so: one MoE layer over a global cache of
- * complete (layer, expert) slots in GPU memory, for one GB300 (sm_103a).
+ * moe_cache.h -- C ABI of libmoecache.so: one MoE layer over a GPU-memory cache
+ * whose slots each hold one whole (layer, expert), for one GB300 (sm_103a).
  *
  * What the library computes (FreeToken, as described on four web pages):
  *
- *  - The complete routed-expert pool lives in host memory and is the source of
- *    truth; the GPU memory set aside for experts is ONE least-recently-used
- *    cache of complete (layer, expert) slots, every bank indexed by the flat
- *    id f = layer * E + expert.  (snackonai deep dive "FreeToken, or why your
+ *  - Every routed expert of the model is kept in host memory, and that copy is
+ *    authoritative.  The GPU memory reserved for experts forms a single LRU
+ *    cache whose slots each hold one whole expert; every table is indexed by
+ *    f = layer * E + expert.  (snackonai deep dive "FreeToken, or why your
  *    laptop was never the bottleneck", sections "What It Actually Does" and
  *    "The Architecture, Unpacked".)
- *  - Per decode layer one device-side control kernel dedups the routed
- *    experts, classifies them against the residency table, derives the miss
- *    split q, surfaces the K least-recently-used victim slots in one pass and
- *    rewrites expert ids into slot ids or a CPU flag, with no host sync.
+ *  - For each decode layer, a single kernel on the device removes duplicate
+ *    routed ids, looks each one up in the residency table, computes the miss
+ *    split q, finds the K slots used longest ago in a single pass, and turns
+ *    each expert id into a slot id or a mark for the CPU; the host never
+ *    waits on it.
  *    (same page, "The Architecture, Unpacked", decision three; ai.thesatyajit
  *    article "FreeToken: a 753B model on one GPU ...", section "Residency that
  *    follows the router", last paragraph.)
@@ -27,10 +28,10 @@
  *    the GPU partial sums with caller-supplied partial sums of CPU-assigned
  *    experts, weighted by the router gates, in fixed top-k order.
  *    (snackonai, "The split policy itself", closing note; "What It Actually
- *    Does": the partial sums merge exactly.)
- *  - Prefill: two full-layer buffers out of the same slot pool; while layer l
- *    computes, a transfer stream loads all experts of layer l+1; on-demand
- *    loading when two layers do not fit.  (thesatyajit, "Prefill: hide the
+ *    Does": the merge of the partial sums is exact.)
+ *  - Prefill: the slot pool lends room for two whole layers; layer l+1's
+ *    experts all load on a copy stream while layer l is computed; if two
+ *    layers do not fit, the routed experts load as they are needed.  (thesatyajit, "Prefill: hide the
  *    pool behind the wire"; snackonai, decision two.)
  *  - Resize: rebuild the cache for a new slot count without touching the
  *    host pool.  (snackonai, "Resizing the cache without a restart";

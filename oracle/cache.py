@@ -1,23 +1,22 @@
-"""Global LRU cache of complete (layer, expert) slots (oracle, test infrastructure).
+"""One LRU cache of whole experts, one slot per resident (layer, expert) (oracle, test infrastructure).
 
 Passages followed:
   * snackonai deep dive "FreeToken, or why your laptop was never the
-    bottleneck", section "The Architecture, Unpacked": every bank is indexed
-    by the flat id l*E+e; prefill and decode share one slot pool; one kernel
-    per MoE layer dedups the routed experts, classifies them against the
-    residency table, derives q, picks victims and rewrites logical ids into
-    slot ids or a CPU flag; victim selection surfaces the K least recently
-    used slots in one pass.
+    bottleneck", section "The Architecture, Unpacked": all tables use the flat
+    id l*E+e; the prefill and the decode draw on the same slots; for each MoE
+    layer one kernel removes duplicate routed ids, looks them up, computes q,
+    chooses victims and maps every id to a slot or to the CPU; the victims
+    are the K slots used longest ago, found in a single pass.
   * same page, "The split policy itself": the first q misses fill, the rest
     run on the CPU; and "Resizing the cache without a restart".
   * ai.thesatyajit.com "FreeToken: a 753B model on one GPU ...", sections
-    "Residency that follows the router" (a hit refreshes recency, a fill
-    admits, an eviction removes the least recently demanded entry),
-    "Prefill: hide the pool behind the wire" (two full-layer buffers out of
-    the shared pool; the next layer loads while this one computes; on-demand
-    loading when two layers do not fit; with the second buffer disabled the
-    loads and the computation run one after the other) and "Elastic memory
-    ..." (rebuild the cache for a new budget; cold start).
+    "Residency that follows the router" (a hit makes an expert the most
+    recent, a fill brings one in, an eviction drops the one whose last use is
+    oldest), "Prefill: hide the pool behind the wire" (the pool lends room for
+    two whole layers; layer l+1 loads while layer l computes; experts load as
+    needed when two layers do not fit; with the second buffer off, loading
+    and computing take turns) and "Elastic memory ..." (rebuild the cache for
+    a new budget; cold start).
 
 The LRU order is an explicit Python list (least recent first).  Slots are
 dicts.  Stamps are kept alongside only because they are part of the state the

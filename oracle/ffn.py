@@ -2,14 +2,14 @@
 
 Passages followed:
   * snackonai deep dive "FreeToken, or why your laptop was never the
-    bottleneck", section "What It Actually Does": GPU and CPU partial sums
-    merge exactly, so the routed computation is bit-faithful to the
-    checkpoint (no approximation).
+    bottleneck", section "What It Actually Does": the merge of the GPU's and
+    the CPU's partial sums is exact; nothing in the routed computation is
+    approximated.
   * same page, section "The split policy itself" (closing note): hits and
     filled experts are evaluated as grouped work on the GPU; misses assigned
     to the CPU execute where their weights live.
   * ai.thesatyajit.com article, section "Decode: the one equation": the two
-    partial sums merge exactly.
+    partial sums are combined without approximation.
 
 The pages do not write out the expert.  The expert is the SwiGLU feed-forward
 of the Qwen3 / DeepSeek-V3 MoE families the workloads are shaped after:
@@ -146,8 +146,8 @@ def pair_outputs(store: ExpertStore, layer: int, E: int, x: np.ndarray, adtype: 
 def shared_outputs(shared_blobs: np.ndarray, layer: int, wdtype: str, H: int, I: int,
                    blob_bytes: int, x: np.ndarray, adtype: str) -> np.ndarray:
     """The always-resident shared expert of `layer` applied to x (reading: the
-    DeepSeek-V3 shape's shared expert; signalovernoise.tech and dev.to: the
-    non-expert weights stay on the GPU), added last by the combine."""
+    DeepSeek-V3 shape's shared expert; signalovernoise.tech and dev.to: only
+    the routed experts leave the GPU), added last by the combine."""
     blob = shared_blobs[layer * blob_bytes:(layer + 1) * blob_bytes]
     return swiglu_expert(activations_to_f64(x, adtype), *parse_blob(blob, wdtype, H, I))
 

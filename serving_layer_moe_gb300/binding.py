@@ -97,7 +97,7 @@ def _stream(stream):
 
 
 class MoECache:
-    """A global LRU cache of complete (layer, expert) slots on one GPU (libmoecache.so).
+    """One LRU cache of whole experts on one GPU, a slot per resident (layer, expert) (libmoecache.so).
 
     host_pool: page-locked or pageable host memory (torch uint8 tensor or numpy
     array) holding the expert blobs; it is kept referenced by this object.

@@ -2,9 +2,10 @@
 //
 // The cache is FreeToken's global expert-slot cache (snackonai deep dive
 // "FreeToken, or why your laptop was never the bottleneck", sections "What It
-// Actually Does" and "The Architecture, Unpacked"): the host pool is the
-// source of truth, GPU memory holds C complete expert blobs, and residency,
-// lookup, eviction and execution all use the flat id l*E+e.
+// Actually Does" and "The Architecture, Unpacked"): the host copy of every
+// expert is authoritative, GPU memory holds C complete expert blobs, and every
+// table (where an expert lives, which slot goes next, what runs) is keyed by the
+// flat id l*E+e.
 //
 // GB300 layout: the slot pool is one device allocation of C*S bytes (slot s at
 // s*S, every blob 16-byte aligned); the residency tables are int32 arrays

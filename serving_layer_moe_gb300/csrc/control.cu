@@ -1,15 +1,15 @@
 // Routing-control kernel of one decode MoE layer (one CTA, no host sync).
 //
 // Follows the snackonai deep dive "FreeToken, or why your laptop was never the
-// bottleneck", section "The Architecture, Unpacked" (decision three: one
-// kernel per MoE layer dedups the routed experts, classifies them against the
-// residency table, derives q, picks victims and rewrites logical ids into
-// physical slot ids or a CPU flag; victim selection is one pass that surfaces
-// the K least recently used slots) and section "The split policy itself"
+// bottleneck", section "The Architecture, Unpacked" (decision three: for each
+// MoE layer a single kernel removes duplicate routed ids, looks them up in the
+// residency table, computes q, chooses victims and maps every id to a slot or
+// to the CPU; the victims, the K slots used longest ago, come out of a single
+// pass) and section "The split policy itself"
 // (q* = round(m B_P / B_H), clamp max(1, min(q, m)), the first q misses fill).
 // Recency follows ai.thesatyajit.com "FreeToken: a 753B model on one GPU ...",
-// section "Residency that follows the router": a hit refreshes recency, a
-// fill admits, an eviction removes the least recently demanded entry.
+// section "Residency that follows the router": a hit makes an expert the most
+// recent, a fill brings one in, an eviction drops the one unused longest.
 //
 // Readings (the pages leave these open):
 //   * B_H = B_pcie + B_cpu, so q* = round_half_even(m B_pcie / (B_pcie + B_cpu))

@@ -2,9 +2,10 @@
 // resident slots, and the fixed-order combine.
 //
 // Follows the snackonai deep dive "FreeToken, or why your laptop was never the
-// bottleneck", section "The split policy itself" (closing note: the GPU miss
-// path runs its cache update, batched copy and grouped evaluation) and section
-// "What It Actually Does" (GPU and CPU partial sums merge exactly); the
+// bottleneck", section "The split policy itself" (closing note: on the GPU
+// side a miss means updating the cache, copying the experts in as a batch and
+// evaluating them grouped) and section "What It Actually Does" (the GPU and CPU
+// partial sums are merged without approximation); the
 // dev.to summary "FreeToken runs frontier-scale MoE models ...", section "When
 // it misses": RAM -> link -> VRAM -> GPU execute.
 //

@@ -3,13 +3,13 @@
 //
 // Follows the ai.thesatyajit.com article "FreeToken: a 753B model on one GPU,
 // and the two bandwidths that decide everything", section "Prefill: hide the
-// pool behind the wire" (two full-layer buffers out of the same slot pool the
-// decode cache uses; while the GPU computes layer l a transfer stream fills the
-// complete expert set of layer l+1, started before l+1's routing is known;
-// whatever survives prefill seeds decode), the snackonai deep dive "FreeToken,
-// or why your laptop was never the bottleneck", section "The Architecture,
-// Unpacked", decision two (prefill and decode share one pool; when the pool
-// cannot spare two full layers, on-demand loading), and the signalovernoise
+// pool behind the wire" (the decode cache's slot pool lends room for two whole
+// layers; as the GPU computes layer l, a copy stream brings in every expert of
+// layer l+1, before l+1's routing exists; the experts left resident after the
+// prefill are where decode starts), the snackonai deep dive "FreeToken, or why
+// your laptop was never the bottleneck", section "The Architecture, Unpacked",
+// decision two (one pool for both; when it is too small for two whole layers,
+// experts load as they are needed), and the signalovernoise
 // newsletter "FreeToken: treat the whole PC as one" (same mechanism).
 //
 // Readings:

@@ -2,10 +2,11 @@
 //
 // Follows the snackonai deep dive "FreeToken, or why your laptop was never the
 // bottleneck", section "Resizing the cache without a restart" (rebuild the
-// expert cache to a new slot count; legal because the host pool is the source
-// of truth, so shrinking costs throughput and nothing else) and the
+// expert cache to a new slot count; safe because the host copy of every expert
+// is authoritative: a smaller cache only costs speed) and the
 // ai.thesatyajit.com article, section "Elastic memory, because the machine is
-// not yours" (rebuild at a scheduler safe point without reloading the pool).
+// not yours" (the rebuild happens between steps, and the host pool is not
+// loaded again).
 //
 // Reading: keep the min(C_new, resident) most recently used experts, packed
 // into slots 0.. in ascending old-slot order, each with its recency stamp;

@@ -8,7 +8,7 @@ of their own.
 
 Expert blob byte layout ("bank layout", one contiguous blob per (layer,
 expert), the unit a cache slot holds; FreeToken, "The Architecture, Unpacked",
-decision one: the slot is a complete expert):
+decision one: a slot holds a whole expert, never a part of one):
 
   f32 / bf16 weights:
       W_gu  [2I, H] row-major   rows 0..I-1 = gate projection, I..2I-1 = up
