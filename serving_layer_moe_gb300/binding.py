@@ -83,9 +83,11 @@ def _ptr(t) -> int | None:
     if t is None:
         return None
     if isinstance(t, np.ndarray):
-        assert t.flags["C_CONTIGUOUS"]
+        if not t.flags["C_CONTIGUOUS"]:
+            raise ValueError("arrays passed to the library must be C-contiguous")
         return t.ctypes.data
-    assert t.is_contiguous(), "tensors must be contiguous"
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the library must be contiguous")
     return t.data_ptr()
 
 

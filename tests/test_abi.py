@@ -129,3 +129,18 @@ def test_noalloc_refuses_unaligned_pointers_without_a_device_call(lib):
         st = lib.moe_layer_ffn_noalloc(8, 256, 512, 2, MOE_BF16, MOE_BF16, a["e"], 1, a["x"], a["i"], a["w"], a["o"],
                                        None)
         assert st == 1 and word in lib.moe_last_error(), key
+
+
+def test_binding_refuses_non_contiguous_buffers():
+    import numpy as np
+    import torch
+    from serving_layer_moe_gb300.binding import _ptr
+    assert _ptr(None) is None
+    a = np.zeros((4, 4), np.float32)
+    assert _ptr(a) == a.ctypes.data
+    with pytest.raises(ValueError):
+        _ptr(a[:, ::2])
+    t = torch.zeros(4, 4)
+    assert _ptr(t) == t.data_ptr()
+    with pytest.raises(ValueError):
+        _ptr(t.t())
