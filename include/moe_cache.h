@@ -299,7 +299,11 @@ moe_status bench_bw(int32_t device, uint64_t expert_bytes, double* b_pcie_gbs, d
  *
  * Limits and sharing:
  *   - scratch needed ~ T * top_k * (H + I) * 4 bytes plus small lists; a call
- *     that needs more than 16 MiB returns MOE_ECAPACITY with a message.
+ *     that needs more than 16 MiB, or that routes more than 9216 pairs
+ *     (T * top_k), returns MOE_ECAPACITY with a message.
+ *   - range violations the GPU finds in this call (an id outside [0, E)) are
+ *     not reported: such a pair contributes nothing and no later call returns
+ *     MOE_EDEVICE for it.
  *   - every call on a device uses the same scratch array and leaves its
  *     contents behind; each call rewrites everything it reads first, so
  *     nothing needs clearing, but calls that overlap on the GPU (different

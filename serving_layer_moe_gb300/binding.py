@@ -242,15 +242,63 @@ def bench_bw(device: int, expert_bytes: int):
     return bp.value, bh.value, bool(rec.value)
 
 
+def blob_bytes(wdtype, H: int, I: int) -> int:
+    """S, the bytes of one expert blob in the bank layout moe_cache.h states."""
+    wd = DTYPES.get(wdtype, wdtype)
+    HI = H * I
+    if wd == MOE_F32:
+        return 12 * HI
+    if wd == MOE_BF16:
+        return 6 * HI
+    if wd == MOE_FP8E4M3_B128:
+        return 3 * HI + 4 * ((2 * I // 128) * (H // 128) + (H // 128) * (I // 128))
+    if wd == MOE_NVFP4:
+        return 3 * HI // 2 + 3 * HI // 16 + 16
+    if wd == MOE_MXFP4:
+        return 3 * HI // 2 + 3 * HI // 32
+    raise ValueError(f"unknown weight dtype {wdtype!r}")
+
+
+def _nbytes(t) -> int:
+    return t.nbytes if isinstance(t, np.ndarray) else t.numel() * t.element_size()
+
+
+def _check_noalloc_args(experts, x, topk_ids, topk_w, out, E, H, I, top_k, wdtype, adtype):
+    """Refuse arguments the kernels would read or write out of bounds (ValueError)."""
+    import torch
+    wd, ad = DTYPES.get(wdtype, wdtype), DTYPES.get(adtype, adtype)
+    if ad not in (MOE_F32, MOE_BF16):
+        raise ValueError(f"adtype must be f32 or bf16, not {adtype!r}")
+    if topk_ids.dtype != torch.int32 or topk_ids.dim() != 2 or topk_ids.shape[1] != top_k:
+        raise ValueError(f"topk_ids must be int32 [T, {top_k}], got {topk_ids.dtype} {tuple(topk_ids.shape)}")
+    T = topk_ids.shape[0]
+    if topk_w.dtype != torch.float32 or tuple(topk_w.shape) != (T, top_k):
+        raise ValueError(f"topk_w must be float32 [{T}, {top_k}], got {topk_w.dtype} {tuple(topk_w.shape)}")
+    if out.dtype != torch.float32 or tuple(out.shape) != (T, H):
+        raise ValueError(f"out must be float32 [{T}, {H}], got {out.dtype} {tuple(out.shape)}")
+    want_es = 4 if ad == MOE_F32 else 2
+    if x.element_size() != want_es or x.dim() != 2 or tuple(x.shape) != (T, H):
+        raise ValueError(f"x must be [{T}, {H}] with {want_es}-byte elements for adtype {adtype!r}, "
+                         f"got {x.dtype} {tuple(x.shape)}")
+    need = E * blob_bytes(wd, H, I)
+    if _nbytes(experts) < need:
+        raise ValueError(f"experts holds {_nbytes(experts)} bytes; E = {E} blobs need {need}")
+    devs = {t.device for t in (experts, x, topk_ids, topk_w, out)}
+    if len(devs) != 1 or next(iter(devs)).type != "cuda":
+        raise ValueError(f"experts, x, topk_ids, topk_w and out must be on one CUDA device, got {sorted(map(str, devs))}")
+    return T
+
+
 def ffn_noalloc(experts, x, topk_ids, topk_w, out, *, E, H, I, top_k, wdtype, adtype, stream=None):
     """moe_layer_ffn_noalloc: all-resident expert SwiGLU + combine that allocates no GPU memory.
 
     For callers that may not allocate: every intermediate lives in the
     library's fixed device scratch array.  experts: the layer's E blobs back to
     back on the device.  Calls that overlap on the GPU share that scratch and
-    race; order them on one stream.
+    race; order them on one stream.  Arguments whose sizes, dtypes or devices
+    do not match E, H, I, top_k and the dtypes raise ValueError before the call.
     """
-    T = topk_ids.shape[0]
+    T = _check_noalloc_args(experts, x, topk_ids, topk_w, out, E, H, I, top_k, wdtype, adtype)
     _check(load_library().moe_layer_ffn_noalloc(E, H, I, top_k, DTYPES.get(wdtype, wdtype),
                                                 DTYPES.get(adtype, adtype), _ptr(experts), T, _ptr(x),
                                                 _ptr(topk_ids), _ptr(topk_w), _ptr(out), _stream(stream)))

@@ -1845,6 +1845,13 @@ cudaError_t launch_down_combine_typed(const GemvArgs& a, const float* w, const f
 
 int gemv_block_threads() { return kGemvThreads; }
 
+// The register-staged gate/up kernel stages the plan (and x, up to kXSmem) in
+// dynamic shared memory; setup_gemv_kernels() allows it at most this much.
+size_t expert_gemv_smem(const Shape& sh, int T) {
+  return gate_up_smem(make_args(sh, 0, T, nullptr, DecodeBufs{}), sh.adtype);
+}
+size_t expert_gemv_smem_limit() { return kXSmem + staged_plan_bytes(4096 + 1, 1024 * 8 + 1024); }
+
 template <int WT, int AT>
 cudaError_t carveout_typed() {
   const void* ks[] = {(const void*)gate_up_kernel<WT, AT, 1>, (const void*)gate_up_kernel<WT, AT, 4>,
@@ -1864,7 +1871,7 @@ cudaError_t carveout_typed() {
     if (e != cudaSuccess) return e;
   }
   // x (up to kXSmem) plus the staged plan of up to 1024 tokens x top-8 pairs
-  const int gu_smem = (int)(kXSmem + staged_plan_bytes(4096 + 1, 1024 * 8 + 1024));
+  const int gu_smem = (int)expert_gemv_smem_limit();
   for (const void* k : {(const void*)gate_up_kernel<WT, AT, 1>, (const void*)gate_up_kernel<WT, AT, 4>}) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, gu_smem);
     if (e != cudaSuccess) return e;

@@ -110,6 +110,10 @@ cudaError_t launch_fp4_to_bf16(const Shape& sh, const int32_t* wslot, const int3
                                const uint8_t* slots, uint16_t* staging, int sms, cudaStream_t s);
 cudaError_t launch_expert_gemv(const Shape& sh, int pass, int T, const void* x, DecodeBufs b,
                                int sms, cudaStream_t s);
+// dynamic shared memory launch_expert_gemv's gate/up kernel needs for T tokens,
+// and the most setup_gemv_kernels() allows it (a call above that cannot launch)
+size_t expert_gemv_smem(const Shape& sh, int T);
+size_t expert_gemv_smem_limit();
 cudaError_t launch_fill_gate_up(const Shape& sh, int T, const void* x, DecodeBufs b, const uint8_t* host_pool_dev,
                                 const uint64_t* offsets, uint8_t* slots, int n_ctas, cudaStream_t s);
 cudaError_t launch_gate_up(const Shape& sh, int pass, int T, const void* x, DecodeBufs b, int sms, cudaStream_t s,

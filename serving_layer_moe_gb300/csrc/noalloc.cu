@@ -29,6 +29,9 @@ constexpr size_t kNoAllocScratchBytes = 16u << 20;   // 16 MiB
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 64;
+// Routed pairs (T * top_k) of one call, at most: the gate/up kernel stages the
+// pair lists in shared memory, and this many always fit what set-up allows it.
+constexpr int kNoAllocMaxPairs = 9216;
 std::mutex g_setup_mu;
 uint8_t* g_scratch_ptr[kMaxDevices] = {};   // device address of g_noalloc_scratch, per device
 int g_sms[kMaxDevices] = {};
@@ -169,6 +172,9 @@ extern "C" moe_status moe_layer_ffn_noalloc(int32_t n_experts, int32_t hidden, i
   if (lay.total > kNoAllocScratchBytes)
     return fail(MOE_ECAPACITY, "T * top_k * (H + I) needs %zu bytes of scratch; the fixed scratch holds %zu",
                 lay.total, kNoAllocScratchBytes);
+  if ((int64_t)T * top_k > kNoAllocMaxPairs)
+    return fail(MOE_ECAPACITY, "T * top_k = %lld routed pairs; one call takes at most %d",
+                (long long)T * top_k, kNoAllocMaxPairs);
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
@@ -176,9 +182,16 @@ extern "C" moe_status moe_layer_ffn_noalloc(int32_t n_experts, int32_t hidden, i
   uint8_t* scratch = nullptr;
   int sms = 0;
   {
-    // first call on this device: look up the device address of the static array
+    // first call on this device: let the GEMV kernels use the shared memory they
+    // stage into (a process may call this without ever creating a cache), then
+    // look up the device address of the static array
     std::lock_guard<std::mutex> lock(g_setup_mu);
     if (!g_scratch_ptr[dev]) {
+      const cudaError_t ke = setup_gemv_kernels();
+      if (ke != cudaSuccess) {
+        cudaGetLastError();
+        return fail(MOE_ECUDA, "setting up the GEMV kernels: %s", cudaGetErrorString(ke));
+      }
       void* p = nullptr;
       const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
       if (e != cudaSuccess || !p) {
@@ -201,6 +214,9 @@ extern "C" moe_status moe_layer_ffn_noalloc(int32_t n_experts, int32_t hidden, i
   sh.L = 1; sh.E = n_experts; sh.H = hidden; sh.I = inter; sh.k = top_k;
   sh.wdtype = wdtype; sh.adtype = adtype; sh.n_shared = 0;
   sh.S = blob_bytes(wdtype, hidden, inter);
+  if (expert_gemv_smem(sh, T) > expert_gemv_smem_limit())   // not reached within kNoAllocMaxPairs
+    return fail(MOE_ECAPACITY, "the call's pair lists need %zu bytes of shared memory; at most %zu",
+                expert_gemv_smem(sh, T), expert_gemv_smem_limit());
   DecodeBufs b{};
   b.plan = reinterpret_cast<int32_t*>(scratch + lay.plan);
   b.slot_map = reinterpret_cast<int32_t*>(scratch + lay.slot_map);
