@@ -9,6 +9,16 @@ control kernel, the slot fills on the side stream, the grouped SwiGLU GEMV
 over resident and filled experts, and the combine with supplied CPU partial
 sums.  Metric: MoE-layer decode steps per second (48 per bench step).
 
+The timed window is trace steps [64, 64 + K) (mod the 256-step trace): the
+first 64 steps run untimed, the last W of them as warm-up, so the window never
+starts from a cold cache and does not move with --steps.  The end-to-end figure
+replays the same prefix on a fresh cache, then times the same K steps with
+host-resident inputs copied in and the outputs copied out every step.
+
+Beside the headline line the run measures the other decode workloads (tiny,
+Qwen3 shape at batch 16 across its mid-run resize, the DeepSeek-V3 fp8 slice),
+the 4-bit-expert variants of the headline, and the prefill chunk.
+
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 Under torchrun each rank runs an independent replica on its own GPU (the path
@@ -32,7 +42,7 @@ if ROOT not in sys.path:
 
 import numpy as np  # noqa: E402
 
-from workloads import (activations, config, default_max_fetch, make_blob, make_pool,  # noqa: E402
+from workloads import (activations, config, default_max_fetch, make_blob, make_pool, make_shared,  # noqa: E402
                        prefill_routing, routing_trace)
 
 WORKLOAD = "qwen3_decode_b1"
@@ -54,6 +64,12 @@ FUSED_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of the
                         "qwen3 b1 shape, 8 resident experts per layer); profiles/decode_fused_resident_qwen3_b1.md")
 
 
+# DRAM bytes per launch of the other workloads' dominant kernel group, from ncu
+# captures (none yet: the roofline's traffic stays null).
+WORKLOAD_TRAFFIC: dict = {}
+WORKLOAD_TRAFFIC_SOURCE: dict = {}
+
+
 def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -67,8 +83,12 @@ def parse_args(argv=None):
     p.add_argument("--no-prefill", action="store_true")
     p.add_argument("--no-nvfp4", action="store_true",
                    help="skip the 4-bit-expert variants (NVFP4, MXFP4) of the decode workload")
-    p.add_argument("--mode", default="all", choices=["all", "decode", "prefill", "profile-decode"],
-                   help="prefill: only the prefill measurement (small profiling runs)")
+    p.add_argument("--mode", default="all", choices=["all", "decode", "prefill", "profile-decode", "workloads"],
+                   help="prefill: only the prefill measurement; workloads: only the tiny, batch-16 and "
+                        "DeepSeek-V3 decode workloads")
+    p.add_argument("--no-workloads", action="store_true",
+                   help="skip the tiny, batch-16 and DeepSeek-V3 decode workloads")
+    p.add_argument("--cpu-workload", default=WORKLOAD, help=argparse.SUPPRESS)
     p.add_argument("--prefill-tokens", type=int, default=8192)
     p.add_argument("--no-prefill-ablation", action="store_true",
                    help="skip the prefill chunks without the second buffer (4k / 8k / 16k tokens)")
@@ -155,8 +175,8 @@ class ClockSampler:
 # ----------------------------------------------------------------------------
 # the oracle as CPU baseline (runs in a fresh interpreter: no fork after CUDA init)
 # ----------------------------------------------------------------------------
-def cpu_worker(seconds: float, pool_blobs: int, bw, samples: int = 1):
-    """Oracle control + float64 SwiGLU on successive layer-steps of the workload.
+def cpu_worker(seconds: float, pool_blobs: int, bw, samples: int = 1, workload: str = WORKLOAD):
+    """Oracle control + float64 SwiGLU on successive layer-steps of a workload.
 
     Prints one JSON line per sample; each sample runs until `seconds` of oracle
     time are spent.  Generating the synthetic expert blobs (input synthesis) is
@@ -165,20 +185,23 @@ def cpu_worker(seconds: float, pool_blobs: int, bw, samples: int = 1):
     from oracle.cache import SlotCache
     from oracle.ffn import combine, swiglu_expert
     from oracle.formats import activations_to_f64, parse_blob
-    cfg = config(WORKLOAD)
+    cfg = config(workload)
     s = cfg.shape
+    n_phys = min(pool_blobs, s.n_flat)
     ids, w = routing_trace(cfg)
     K = default_max_fetch(s, cfg.T)
     ora = SlotCache(s.L, s.E, cfg.capacity, K, bw[0], bw[1])
-    raw = {}
+    raw, shared_raw = {}, {}
     st, l = 0, 0
     for _ in range(samples):
         spent, n = 0.0, 0
         while spent < seconds:
             sid = st % cfg.steps
-            need = {(l * s.E + int(e)) % pool_blobs for e in ids[sid, l].ravel()}
+            need = {(l * s.E + int(e)) % n_phys for e in ids[sid, l].ravel()}
             for p in need - raw.keys():
                 raw[p] = make_blob(s, cfg.seed, p)          # input synthesis, not timed
+            if s.n_shared and l not in shared_raw:
+                shared_raw[l] = make_blob(s, cfg.seed, l, tag=0x5AED)
             xs = activations(cfg, sid, l)
             t0 = time.perf_counter()
             plan = ora.decode(l, ids[sid, l])
@@ -186,9 +209,10 @@ def cpu_worker(seconds: float, pool_blobs: int, bw, samples: int = 1):
             y = np.zeros((cfg.T, s.k, s.H))
             for t in range(cfg.T):
                 for j in range(s.k):
-                    p = (l * s.E + int(ids[sid, l, t, j])) % pool_blobs
+                    p = (l * s.E + int(ids[sid, l, t, j])) % n_phys
                     y[t, j] = swiglu_expert(x[t], *parse_blob(raw[p], s.wdtype, s.H, s.I))
-            combine(w[sid, l], y, plan.slot_map, y)
+            sh_y = swiglu_expert(x, *parse_blob(shared_raw[l], s.wdtype, s.H, s.I)) if s.n_shared else None
+            combine(w[sid, l], y, plan.slot_map, y, shared_y=sh_y)
             spent += time.perf_counter() - t0
             n += 1
             l += 1
@@ -197,23 +221,262 @@ def cpu_worker(seconds: float, pool_blobs: int, bw, samples: int = 1):
         print(json.dumps({"layer_steps": n, "seconds": spent}), flush=True)
 
 
-def run_cpu_baseline(seconds: float, pool_blobs: int, bw, samples: int = 1):
-    """Run the oracle in a fresh interpreter (no fork after CUDA init); one dict per sample."""
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+def run_cpu_baseline(seconds: float, pool_blobs: int, bw, samples: int = 1, workload: str = WORKLOAD,
+                     threads: int = 1):
+    """Run the oracle in a fresh interpreter (no fork after CUDA init); one dict per sample.
+
+    threads = 1 is the oracle alone; more threads let NumPy's BLAS spread the
+    float64 matrix-vector products of the SwiGLU over that many host cores.
+    """
+    env = dict(os.environ, OMP_NUM_THREADS=str(threads), OPENBLAS_NUM_THREADS=str(threads),
+               MKL_NUM_THREADS=str(threads))
     cmd = [sys.executable, os.path.abspath(__file__), "--cpu-worker", "--cpu-seconds", str(seconds),
-           "--pool-blobs", str(pool_blobs), "--cpu-samples", str(samples)]
+           "--pool-blobs", str(pool_blobs), "--cpu-samples", str(samples), "--cpu-workload", workload]
     env["BENCH_BW"] = f"{bw[0]},{bw[1]}"
-    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=samples * (seconds * 4 + 60) + 120)
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=samples * (seconds * 4 + 120) + 180)
     lines = [json.loads(l) for l in r.stdout.splitlines() if l.startswith("{")]
     if r.returncode != 0 or not lines:
         return None
     out = []
+    how = "one thread" if threads == 1 else f"BLAS on {threads} threads"
     for d in lines:
-        out.append({"value": d["layer_steps"] / d["seconds"], "unit": UNIT, "cores": 1, "kind": "oracle",
-                    "sample": f"{d['layer_steps']} layer-steps of {WORKLOAD} (list-LRU control + float64 SwiGLU "
-                              f"per routed pair from the host pool + fixed-order combine), one thread, "
+        out.append({"value": d["layer_steps"] / d["seconds"], "unit": UNIT, "cores": threads, "kind": "oracle",
+                    "sample": f"{d['layer_steps']} layer-steps of {workload} from its first step (list-LRU control "
+                              f"+ float64 SwiGLU per routed pair from the host pool + fixed-order combine), {how}, "
                               f"{d['seconds']:.1f} s of oracle time"})
     return out if samples > 1 else out[0]
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------------------
+# a decode workload on one cache, replayed step by step
+# ----------------------------------------------------------------------------
+# Trace steps replayed untimed before a timed window, so the window never starts
+# from a cold cache and does not move with --steps (the warm-up steps are the
+# last of these).
+PREFIX_STEPS = 64
+
+
+def expert_bytes(s) -> tuple[int, int]:
+    """(gate/up bytes, down bytes) of one expert blob, each with its scales (they sum to S)."""
+    H, I = s.H, s.I
+    if s.wdtype == "f32":
+        return 8 * I * H, 4 * I * H
+    if s.wdtype == "bf16":
+        return 4 * I * H, 2 * I * H
+    if s.wdtype == "fp8":
+        return 2 * I * H + 4 * (2 * I // 128) * (H // 128), H * I + 4 * (H // 128) * (I // 128)
+    if s.wdtype == "nvfp4":
+        return I * H + 2 * I * H // 16 + 8, H * I // 2 + H * I // 16 + 8
+    return I * H + 2 * I * H // 32, H * I // 2 + H * I // 32   # mxfp4
+
+
+class DecodeRunner:
+    """One decode workload on one cache: the inputs of the trace steps it runs in
+    HBM, one whole decode step (L MoE-layer calls) captured in a CUDA graph and
+    replayed per step.  Run step n uses trace step n mod steps.  A workload with a
+    mid-run resize resizes once, before run step resize_step, and re-captures the
+    graph (the slot pool moves)."""
+
+    def __init__(self, cfg, pool, offs, shared, bw, dev, need_steps, K=None):
+        import torch
+        from serving_layer_moe_gb300 import MoECache
+        s = cfg.shape
+        self.torch = torch
+        self.cfg, self.s, self.dev = cfg, s, dev
+        self.K = default_max_fetch(s, cfg.T) if K is None else K
+        self.cache = MoECache(L=s.L, E=s.E, H=s.H, I=s.I, top_k=s.k, max_tokens=cfg.T, wdtype=s.wdtype,
+                              adtype=s.adtype, host_pool=pool, blob_offsets=offs, shared=shared,
+                              n_slots=cfg.capacity, max_fetch=self.K, bw_pcie_mbps=bw[0], bw_cpu_mbps=bw[1],
+                              device=dev.index or 0)
+        self.n_trace = min(cfg.steps, need_steps)
+        ids, w = routing_trace(cfg)
+        acts = np.stack([np.stack([activations(cfg, st, l) for l in range(s.L)]) for st in range(self.n_trace)])
+        self.acts = acts.view(np.int16) if acts.dtype == np.uint16 else acts
+        self.ids, self.w = ids[:self.n_trace], w[:self.n_trace]
+        self.x_all = torch.from_numpy(self.acts).to(dev)            # [steps, L, T, H]
+        self.ids_all = torch.from_numpy(self.ids).to(dev)           # [steps, L, T, k]
+        self.w_all = torch.from_numpy(self.w).to(dev)
+        self.xb = torch.empty_like(self.x_all[0])
+        self.ib = torch.empty_like(self.ids_all[0])
+        self.wb = torch.empty_like(self.w_all[0])
+        self.out = torch.empty(s.L, cfg.T, s.H, dtype=torch.float32, device=dev)
+        # caller-supplied CPU partial sums: the combine reads them where a pair is CPU-assigned
+        self.cpu_part = torch.zeros(cfg.T, s.k, s.H, dtype=torch.float32, device=dev)
+        self.stream = torch.cuda.Stream(device=dev)
+        self.ptrs = [(self.xb[l].data_ptr(), self.ib[l].data_ptr(), self.wb[l].data_ptr(), self.out[l].data_ptr())
+                     for l in range(s.L)]
+        self.step = 0
+        self.graph = None
+        self.resized = cfg.resize_step is None
+        self.resize_ms = None
+
+    def trace_index(self, n: int) -> int:
+        st = n % self.cfg.steps
+        assert st < self.n_trace, "run step beyond the trace steps held on the device"
+        return st
+
+    def enqueue(self):
+        sp = self.stream.cuda_stream
+        for l in range(self.s.L):
+            xp, ip, wp, op = self.ptrs[l]
+            self.cache.decode_ptrs(l, self.cfg.T, xp, ip, wp, self.cpu_part.data_ptr(), op, None, sp)
+
+    def stage(self, n: int):
+        st = self.trace_index(n)
+        self.xb.copy_(self.x_all[st], non_blocking=True)
+        self.ib.copy_(self.ids_all[st], non_blocking=True)
+        self.wb.copy_(self.w_all[st], non_blocking=True)
+
+    def capture(self):
+        torch = self.torch
+        torch.cuda.synchronize(self.dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            self.enqueue()
+        torch.cuda.synchronize(self.dev)
+        self.graph = g
+
+    def _maybe_resize(self):
+        if not self.resized and self.step == self.cfg.resize_step:
+            t0 = time.perf_counter()
+            self.cache.resize(self.cfg.resize_to)     # a safe point: synchronises the device
+            if self.graph is not None:
+                self.capture()
+            self.resize_ms = 1e3 * (time.perf_counter() - t0)
+            self.resized = True
+
+    def warm(self, prefix: int):
+        """Run steps 0 .. prefix-1 untimed: two eager steps, then graph replays."""
+        with self.torch.cuda.stream(self.stream):
+            for _ in range(min(2, prefix)):
+                self._maybe_resize()
+                self.stage(self.step)
+                self.enqueue()
+                self.step += 1
+        self.capture()
+        self.advance(prefix - self.step)
+
+    def advance(self, n: int):
+        with self.torch.cuda.stream(self.stream):
+            for _ in range(n):
+                self._maybe_resize()
+                self.stage(self.step)
+                self.graph.replay()
+                self.step += 1
+
+    def advance_host(self, n: int, x_h, ids_h, w_h, out_h):
+        """n steps from page-locked host inputs, the outputs copied back every step."""
+        with self.torch.cuda.stream(self.stream):
+            for _ in range(n):
+                self._maybe_resize()
+                st = self.trace_index(self.step)
+                self.xb.copy_(x_h[st], non_blocking=True)
+                self.ib.copy_(ids_h[st], non_blocking=True)
+                self.wb.copy_(w_h[st], non_blocking=True)
+                self.graph.replay()
+                out_h.copy_(self.out, non_blocking=True)
+                self.step += 1
+
+    def timed(self, n: int, clocks=None):
+        """(milliseconds, counter delta) of n steps between two events on the stream."""
+        torch = self.torch
+        cnt0 = self.cache.state()[3].copy()
+        torch.cuda.synchronize(self.dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(self.stream)
+        self.advance(n)
+        e1.record(self.stream)
+        torch.cuda.synchronize(self.dev)
+        return e0.elapsed_time(e1), self.cache.state()[3].copy() - cnt0
+
+    def profiled(self, n: int, same_step: bool = False):
+        """Kernel-group times over n replays of a second graph of the step with the
+        library's event pair around each kernel group: ({kind: [ms, launches]},
+        counter delta).  same_step replays the current step's inputs every time."""
+        torch = self.torch
+        cache = self.cache
+        cache.profile_start()
+        pgraph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(pgraph, stream=self.stream):
+            self.enqueue()
+        cache.profile_pause()
+        torch.cuda.synchronize(self.dev)
+        prof = {k: [0.0, 0] for k in cache.PROFILE_KINDS}
+        cnt0 = cache.state()[3].copy()
+        with torch.cuda.stream(self.stream):
+            if same_step:
+                self.stage(self.step)
+            for _ in range(n):
+                if not same_step:
+                    assert self.resized or self.step + 1 < self.cfg.resize_step, "profiled replays across the resize"
+                    self.stage(self.step)
+                    self.step += 1
+                pgraph.replay()
+                for k, (ms_k, n_k) in cache.profile_read().items():
+                    prof[k][0] += ms_k
+                    prof[k][1] += n_k
+        cnt1 = cache.state()[3].copy()
+        cache.profile_stop()
+        return prof, cnt1 - cnt0
+
+    def close(self):
+        self.cache.close()
+
+
+def kernel_groups(s, prof, dcnt):
+    """Algorithmic HBM bytes and event time of the decode kernel groups over profiled
+    replays: {kind: (bytes, ms, launches)}.  Resident experts are this window's
+    unique hits (+ the shared expert of every launch); each weight byte counts
+    once.  Split path ("down_filled" present): the resident gate/up + down +
+    combine is one group over whole blobs.  Otherwise the resident gate/up grid
+    reads W_gu and the down + combine grid reads W_down of every GPU expert."""
+    gu, wd = expert_bytes(s)
+    hits, fills = int(dcnt[0]), int(dcnt[2])
+    launches = prof["gemv_resident"][1]
+    shared = s.n_shared * launches
+    out = {}
+    if prof["down_filled"][1]:
+        out["gemv_resident"] = ((hits + shared) * s.blob_bytes, prof["gemv_resident"][0], launches)
+        out["down_filled"] = (fills * wd, prof["down_filled"][0], prof["down_filled"][1])
+    else:
+        out["gemv_resident"] = ((hits + shared) * gu, prof["gemv_resident"][0], launches)
+        out["down_combine"] = ((hits + fills + shared) * wd, prof["down_combine"][0], prof["down_combine"][1])
+    return out
+
+
+KERNEL_NAMES = {
+    "gemv_resident_split": "resident-expert GEMV pair: gate_up_bulk_kernel (with the L2 fetch of W_down) + "
+                           "down_bulk_kernel pass 0 fused with the combine",
+    "gemv_resident": "resident-expert gate/up grid (gate_up_bulk_kernel)",
+    "down_combine": "down projection of every GPU expert fused with the combine (down_combine_kernel)",
+}
+
+
+def roofline_from_groups(groups, hbm_peak, peak_src, traffic=None, traffic_source=None):
+    """The roofline object of the group with the most event time (all are HBM-bound)."""
+    kind, (b, ms, n) = max(groups.items(), key=lambda kv: kv[1][1])
+    if ms <= 0 or n == 0:
+        return None
+    split = "down_filled" in groups
+    achieved = b / (ms / 1e3) / 1e9
+    return {"bound": "hbm",
+            "kernel": KERNEL_NAMES["gemv_resident_split" if (split and kind == "gemv_resident") else kind],
+            "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 3),
+            "peak_source": peak_src, "traffic": traffic, "traffic_source": traffic_source,
+            "bytes_per_launch": round(b / n), "us_per_launch": round(1e3 * ms / n, 2), "launches_timed": n}
+
+
+def cache_stats(dcnt):
+    reads = float(dcnt[4] + dcnt[5])
+    return {"hits": int(dcnt[0]), "misses": int(dcnt[1]), "fills": int(dcnt[2]), "cpu_assigned": int(dcnt[3]),
+            "read_miss_rate": round(float(dcnt[5]) / max(1.0, reads), 4)}
 
 
 # ----------------------------------------------------------------------------
@@ -239,7 +502,7 @@ def main(args):
     if args.mode == "profile-decode":
         return profile_case(args, dev)
 
-    from serving_layer_moe_gb300 import MoECache, bench_bw
+    from serving_layer_moe_gb300 import bench_bw
 
     cfg = config(WORKLOAD)
     if args.capacity:
@@ -249,209 +512,90 @@ def main(args):
     bp_gbs, bh_gbs, rec = bench_bw(local, s.blob_bytes)
     b_pcie = max(1, int(bp_gbs * 1000))
     b_cpu = max(0, int(bh_gbs * 1000) - b_pcie)
+    hbm_peak, bf16_peak, bf16_sust, peak_src = measured_peaks()
+
+    if args.mode == "workloads":
+        res = {n: decode_workload_measure(n, args, dev, (b_pcie, b_cpu), hbm_peak, peak_src, rank == 0)
+               for n in EXTRA_WORKLOADS}
+        if rank == 0:
+            print(json.dumps({"workloads": res}))
+        return
 
     arena, offs = make_pool(s, cfg.seed, n_phys=args.pool_blobs)
     pool = torch.from_numpy(arena).pin_memory()
     del arena
-    K = default_max_fetch(s, cfg.T)
-    cache = MoECache(L=s.L, E=s.E, H=s.H, I=s.I, top_k=s.k, max_tokens=cfg.T, wdtype=s.wdtype,
-                     adtype=s.adtype, host_pool=pool, blob_offsets=offs, n_slots=cfg.capacity,
-                     max_fetch=K, bw_pcie_mbps=b_pcie, bw_cpu_mbps=b_cpu, device=local)
-
-    ids, w = routing_trace(cfg)
-    xs = np.stack([np.stack([activations(cfg, st, l) for l in range(s.L)]) for st in range(cfg.steps)])
-    x_all = torch.from_numpy(xs.view(np.int16)).to(dev)            # [steps, L, T, H] bf16 bits
-    ids_all = torch.from_numpy(ids).to(dev)                         # [steps, L, T, k]
-    w_all = torch.from_numpy(w).to(dev)
-    xb = torch.empty_like(x_all[0])
-    ib = torch.empty_like(ids_all[0])
-    wb = torch.empty_like(w_all[0])
-    out = torch.empty(s.L, cfg.T, s.H, dtype=torch.float32, device=dev)
-    cpu_part = torch.zeros(cfg.T, s.k, s.H, dtype=torch.float32, device=dev)
-    stream = torch.cuda.Stream(device=dev)
-    sp = stream.cuda_stream
-    layer_bytes = [(xb[l].data_ptr(), ib[l].data_ptr(), wb[l].data_ptr(), out[l].data_ptr()) for l in range(s.L)]
-
-    def enqueue_step():
-        for l in range(s.L):
-            xp, ip, wp, op = layer_bytes[l]
-            cache.decode_ptrs(l, cfg.T, xp, ip, wp, cpu_part.data_ptr(), op, None, sp)
-
-    def stage(st):
-        xb.copy_(x_all[st % cfg.steps], non_blocking=True)
-        ib.copy_(ids_all[st % cfg.steps], non_blocking=True)
-        wb.copy_(w_all[st % cfg.steps], non_blocking=True)
-
-    step = 0
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            stage(step)
-            enqueue_step()
-            step += 1
-    torch.cuda.synchronize(dev)
-    graph = None
-    if not args.no_graph:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            enqueue_step()
-        torch.cuda.synchronize(dev)
-
+    prefix = max(PREFIX_STEPS, args.warmup + 2)
+    need = prefix + args.steps + 64
+    run = DecodeRunner(cfg, pool, offs, None, (b_pcie, b_cpu), dev, need)
+    K = run.K
+    run.warm(prefix)
     # control, fill (+ the filled experts' gate/up), the filled experts' down grid and
     # the resident experts' kernels (one launch, or a gate/up grid and a down +
     # combine grid), as the library reports
-    launches_per_layer = int(cache.info()[6])
-    resident_path = int(cache.info()[7])   # 0: two grids, 1: one launch with a grid barrier
-    # ---- timed region: inputs resident in HBM ---------------------------------
-    cnt0 = cache.state()[3].copy()
+    launches_per_layer = int(run.cache.info()[6])
+    resident_path = int(run.cache.info()[7])   # 0: two grids, 1: one launch with a grid barrier
+
+    # ---- timed region: inputs resident in HBM; trace steps [prefix, prefix + steps) ----
     if world > 1:
         dist.barrier()
-    torch.cuda.synchronize(dev)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk, torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(args.steps):
-            stage(step)
-            if graph is not None:
-                graph.replay()
-            else:
-                enqueue_step()
-            step += 1
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-    ms = e0.elapsed_time(e1)
+    with ClockSampler(local) as clk:
+        ms, dcnt = run.timed(args.steps)
     if world > 1:
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
         dist.barrier()
-    cnt1 = cache.state()[3].copy()
     layer_steps = args.steps * s.L * world
     value = layer_steps / (ms / 1e3)
+    window = {"trace_steps": f"[{prefix}, {prefix + args.steps}) mod {cfg.steps}",
+              "untimed_prefix_steps": prefix, **cache_stats(dcnt)}
 
-    # ---- end to end: host buffers in, result out, every step ------------------------
-    x_h = torch.from_numpy(xs.view(np.int16)).pin_memory()
-    ids_h = torch.from_numpy(ids).pin_memory()
-    w_h = torch.from_numpy(w).pin_memory()
-    out_h = torch.empty(s.L, cfg.T, s.H, dtype=torch.float32).pin_memory()
-    e2e_steps = max(8, args.steps // 2)
-    torch.cuda.synchronize(dev)
-    if world > 1:
-        dist.barrier()
-    e2 = torch.cuda.Event(enable_timing=True)
-    e3 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e2.record(stream)
-        for _ in range(e2e_steps):
-            st = step % cfg.steps
-            xb.copy_(x_h[st], non_blocking=True)
-            ib.copy_(ids_h[st], non_blocking=True)
-            wb.copy_(w_h[st], non_blocking=True)
-            if graph is not None:
-                graph.replay()
-            else:
-                enqueue_step()
-            out_h.copy_(out, non_blocking=True)
-            step += 1
-        e3.record(stream)
-        torch.cuda.synchronize(dev)
-    ms_e2e = e2.elapsed_time(e3)
-    if world > 1:
-        t = torch.tensor([ms_e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_e2e = float(t.item())
-    h2d = xb.numel() * 2 + ib.numel() * 4 + wb.numel() * 4
-    d2h = out.numel() * 4
-
-    # ---- kernel timing for the roofline: library CUDA events captured into a graph ----
-    # (a second graph of the same step with an event pair around each kernel group;
-    # after each replay the pairs hold that replay's device times)
-    prof_steps = 32
-    cache.profile_start()
-    pgraph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(pgraph, stream=stream):
-        enqueue_step()
-    cache.profile_pause()
-    torch.cuda.synchronize(dev)
-    cnt_p0 = cache.state()[3].copy()
-    prof = {k: [0.0, 0] for k in cache.PROFILE_KINDS}
-    with torch.cuda.stream(stream):
-        for _ in range(prof_steps):
-            stage(step)
-            pgraph.replay()
-            step += 1
-            for k, (ms_k, n_k) in cache.profile_read().items():
-                prof[k][0] += ms_k
-                prof[k][1] += n_k
-    cnt_p1 = cache.state()[3].copy()
-    # ---- roofline of the dominant HBM kernels, the resident-expert GEMV pair
-    # (gate/up grid, which also has L2 fetch the experts' W_down, then the down +
-    # combine grid), with nothing beside them: one step's inputs are replayed
-    # until every routed expert is resident (all hits, no fill), then the same
-    # event pairs time the two grids on their stream.  Algorithmic bytes: each
-    # resident expert's whole blob, read once.
+    # ---- kernel timing inside the step's mix: a second graph of the step with the
+    # library's event pair around each kernel group, over the next 32 steps ----------
+    prof, dcnt_p = run.profiled(32)
+    groups = kernel_groups(s, prof, dcnt_p)
+    total_prof_ms = sum(v[0] for v in prof.values())
+    gb, gms, gn = groups["gemv_resident"]
+    fill_bytes = int(dcnt_p[2]) * s.blob_bytes
+    # ---- roofline of the dominant HBM kernels, the resident-expert GEMV pair, with
+    # nothing beside them: one step's inputs replayed until every routed expert is
+    # resident (all hits, no fill), the same event pairs around the resident grids.
+    # Algorithmic bytes: each resident expert's whole blob, read once.
     res_reps = 16
-    with torch.cuda.stream(stream):
-        stage(step)
-        for _ in range(3):
-            pgraph.replay()
-            cache.profile_read()
-    torch.cuda.synchronize(dev)
-    cnt_r0 = cache.state()[3].copy()
-    res_prof = {k: [0.0, 0] for k in cache.PROFILE_KINDS}
-    with torch.cuda.stream(stream):
+    run.profiled(3, same_step=True)
+    res_prof, dcnt_r = run.profiled(res_reps, same_step=True)
+    with torch.cuda.stream(run.stream):   # the same all-hit step without event pairs: whole-layer time
+        e4, e5 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e4.record(run.stream)
         for _ in range(res_reps):
-            pgraph.replay()
-            for k, (ms_k, n_k) in cache.profile_read().items():
-                res_prof[k][0] += ms_k
-                res_prof[k][1] += n_k
-    cnt_r1 = cache.state()[3].copy()
-    cache.profile_stop()
-    e4 = torch.cuda.Event(enable_timing=True)
-    e5 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):   # the same all-hit step without event pairs: whole-layer time
-        e4.record(stream)
-        for _ in range(res_reps):
-            if graph is not None:
-                graph.replay()
-            else:
-                enqueue_step()
-        e5.record(stream)
+            run.graph.replay()
+        e5.record(run.stream)
     torch.cuda.synchronize(dev)
     ms_res = e4.elapsed_time(e5)
-    step += 1
-    hbm_peak, bf16_peak, bf16_sust, peak_src = measured_peaks()
-    res_hits = int(cnt_r1[0] - cnt_r0[0])
-    res_fills = int(cnt_r1[2] - cnt_r0[2])
+    res_hits, res_fills = int(dcnt_r[0]), int(dcnt_r[2])
     gemv_kinds = ("gemv_resident", "down_combine")   # split: the pair is one group; down_combine stays 0
     res_ms = sum(res_prof[k][0] for k in gemv_kinds)
     res_launches = res_prof["gemv_resident"][1]
     res_bytes = res_hits * s.blob_bytes
     res_gbs = res_bytes / (res_ms / 1e3) / 1e9 if res_ms > 0 else None
-    # the same pair inside the timed step's mix (concurrent fills, event pairs in the graph)
-    resident = int(cnt_p1[0] - cnt_p0[0])
-    gemv_bytes = resident * s.blob_bytes
-    gemv_ms = sum(prof[k][0] for k in gemv_kinds)
-    gemv_launches = prof["gemv_resident"][1]         # one per MoE-layer decode
-    fill_bytes = int(cnt_p1[2] - cnt_p0[2]) * s.blob_bytes
-    total_prof_ms = sum(v[0] for v in prof.values())
-    # Distribution of whole MoE-layer decode times (median, p90), after the timed
-    # region: eager calls, one event pair around each layer's call on its stream,
-    # fills included where they occur.  Reported beside the means; a failure here
-    # leaves the rest of the line intact.
+    run.step += 1
+    # Distribution of whole MoE-layer decode times (median, p90): eager calls, one
+    # event pair around each layer's call on its stream, fills included where they
+    # occur.  Reported beside the means; a failure here leaves the rest of the line intact.
     try:
         lat_steps = 8
         lat_ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(s.L)] for _ in range(lat_steps)]
-        with torch.cuda.stream(stream):
+        with torch.cuda.stream(run.stream):
             for st_i in range(lat_steps):
-                stage(step)
-                step += 1
+                run.stage(run.step)
+                run.step += 1
                 for l in range(s.L):
-                    xp, ip, wp, op = layer_bytes[l]
-                    lat_ev[st_i][l][0].record(stream)
-                    cache.decode_ptrs(l, cfg.T, xp, ip, wp, cpu_part.data_ptr(), op, None, sp)
-                    lat_ev[st_i][l][1].record(stream)
+                    xp, ip, wp, op = run.ptrs[l]
+                    lat_ev[st_i][l][0].record(run.stream)
+                    run.cache.decode_ptrs(l, cfg.T, xp, ip, wp, run.cpu_part.data_ptr(), op, None,
+                                          run.stream.cuda_stream)
+                    lat_ev[st_i][l][1].record(run.stream)
         torch.cuda.synchronize(dev)
         lat_us = np.array([1e3 * a.elapsed_time(b) for row in lat_ev for a, b in row])
         layer_step_us = {"median": round(float(np.median(lat_us)), 2),
@@ -461,6 +605,35 @@ def main(args):
                                  "decode (launch gaps included, so above the graph-replayed mean)"}
     except Exception as exc:   # diagnostics only
         layer_step_us = {"error": repr(exc)[:200]}
+    run.close()
+
+    # ---- end to end: a fresh cache, the same untimed prefix, then the same trace
+    # steps as the timed region with host buffers in and the result out every step ----
+    run2 = DecodeRunner(cfg, pool, offs, None, (b_pcie, b_cpu), dev, need)
+    run2.warm(prefix)
+    x_h = torch.from_numpy(run2.acts).pin_memory()
+    ids_h = torch.from_numpy(run2.ids).pin_memory()
+    w_h = torch.from_numpy(run2.w).pin_memory()
+    out_h = torch.empty(s.L, cfg.T, s.H, dtype=torch.float32).pin_memory()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    cnt_e0 = run2.cache.state()[3].copy()
+    e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2.record(run2.stream)
+    run2.advance_host(args.steps, x_h, ids_h, w_h, out_h)
+    e3.record(run2.stream)
+    torch.cuda.synchronize(dev)
+    ms_e2e = e2.elapsed_time(e3)
+    dcnt_e = run2.cache.state()[3].copy() - cnt_e0
+    if world > 1:
+        t = torch.tensor([ms_e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+    h2d = run2.xb.numel() * run2.xb.element_size() + run2.ib.numel() * 4 + run2.wb.numel() * 4
+    d2h = run2.out.numel() * 4
+    run2.close()
+    del pool
 
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -474,13 +647,14 @@ def main(args):
                    "recommend_hybrid": rec, "K": K,
                    "host_pool": f"{args.pool_blobs} distinct seeded expert blobs in a page-locked arena, "
                                 f"flat id f -> blob f mod {args.pool_blobs}",
-                   "graph": graph is not None,
+                   "graph": True,
                    "l2": "inputs larger than L2: each step reads ~48 x 8 x 9.4 MB of expert weights"},
-        "cache_stats": {"hits": int(cnt1[0] - cnt0[0]), "misses": int(cnt1[1] - cnt0[1]),
-                        "fills": int(cnt1[2] - cnt0[2]), "cpu_assigned": int(cnt1[3] - cnt0[3]),
-                        "read_miss_rate": round(float(cnt1[5] - cnt0[5]) / max(1, float(cnt1[4] + cnt1[5] - cnt0[4] - cnt0[5])), 4)},
-        "e2e": {"value": round(e2e_steps * s.L * world / (ms_e2e / 1e3), 1), "unit": UNIT,
-                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "window": window,
+        "cache_stats": cache_stats(dcnt),
+        "e2e": {"value": round(args.steps * s.L * world / (ms_e2e / 1e3), 1), "unit": UNIT,
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "window": f"the timed region's trace steps on a fresh cache after the same untimed prefix "
+                          f"(fills {int(dcnt_e[2])} vs {int(dcnt[2])} in the timed region)"},
         "gpu_launches": args.steps * s.L * launches_per_layer,
         "roofline": {"bound": "hbm",
                      "kernel": {
@@ -499,11 +673,13 @@ def main(args):
                      "us_per_layer_step": round(1e3 * res_ms / max(1, res_launches), 2),
                      "layer_steps_timed": res_launches, "fills_during": res_fills,
                      "all_resident_layer_us": round(1e3 * ms_res / (res_reps * s.L), 2)},
-        "in_step_gemv": {"note": "the same resident-expert kernels inside the timed step's mix (fills beside "
-                                 "them; the event pairs in the graph also drop their programmatic overlap)",
-                         "achieved_gbs": round(gemv_bytes / (gemv_ms / 1e3) / 1e9, 1) if gemv_ms > 0 else None,
-                         "bytes_per_layer_step": round(gemv_bytes / max(1, gemv_launches)),
-                         "us_per_layer_step": round(1e3 * gemv_ms / max(1, gemv_launches), 2)},
+        "in_step_gemv": {"note": "the same resident-expert kernels inside the step's mix (fills beside them; the "
+                                 "event pairs in the graph also drop their programmatic overlap), 32 steps after "
+                                 "the timed region",
+                         "achieved_gbs": round(gb / (gms / 1e3) / 1e9, 1) if gms > 0 else None,
+                         "frac": round(gb / (gms / 1e3) / 1e9 / hbm_peak, 3) if gms > 0 else None,
+                         "bytes_per_layer_step": round(gb / max(1, gn)),
+                         "us_per_layer_step": round(1e3 * gms / max(1, gn), 2)},
         "kernel_ms_share": {k: round(v[0] / total_prof_ms, 3) for k, v in prof.items() if v[1]},
         "kernel_us_per_layer": {k: round(1e3 * v[0] / max(1, v[1]), 2) for k, v in prof.items() if v[1]},
         "fill": {"achieved_gbs": round(fill_bytes / (prof["fill"][0] / 1e3) / 1e9, 1) if prof["fill"][0] > 0 else None,
@@ -516,8 +692,11 @@ def main(args):
                         "dependency wait included), in the timed step and in the all-resident replay",
         "clocks": clk.summary(),
     }
+    if args.mode == "all" and not args.no_workloads:
+        result["workloads"] = {n: decode_workload_measure(n, args, dev, (b_pcie, b_cpu), hbm_peak, peak_src,
+                                                          rank == 0 and not args.no_cpu_baseline)
+                               for n in EXTRA_WORKLOADS}
     if args.mode == "all" and not args.no_nvfp4:
-        cache.close()
         result["nvfp4_decode"] = fp4_measure(args, dev, local, b_pcie, b_cpu, "nvfp4")
         result["mxfp4_decode"] = fp4_measure(args, dev, local, b_pcie, b_cpu, "mxfp4")
     if not args.no_prefill and args.mode == "all":
@@ -526,11 +705,91 @@ def main(args):
             result["prefill_mxfp4"] = prefill_fp4_measure(args, dev, local, "mxfp4")
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = run_cpu_baseline(args.cpu_seconds, args.pool_blobs, (b_pcie, b_cpu))
+        cores = host_cores()
+        if cores > 1:
+            result["cpu_baseline_all_cores"] = run_cpu_baseline(args.cpu_seconds / 2, args.pool_blobs,
+                                                                (b_pcie, b_cpu), threads=cores)
     if rank == 0:
         print(json.dumps(result))
-    cache.close()
     if world > 1:
         dist.destroy_process_group()
+
+
+# The other decode workloads, measured beside the headline: (untimed prefix, timed
+# steps, distinct host-pool blobs, all-resident roofline possible).
+EXTRA_WORKLOADS = {
+    # 32-step trace of one layer: the window wraps around it
+    "tiny": (8, 256, None, False),
+    # the window spans the resize from 1228 to 737 slots before step 128
+    "qwen3_decode_b16": (96, 64, 64, False),
+    # 4 layers x (8 routed + 1 shared) fp8 experts; 32 routed experts fit C = 112
+    "dsv3_decode_slice": (32, 64, 8, True),
+}
+WORKLOAD_DESC = {
+    "tiny": "tiny single MoE layer: E=8, top-2, H 256, I 512, fp32 weights and activations, T=4, C=4 slots, "
+            "B_pcie:B_cpu = 2:1",
+    "qwen3_decode_b16": "Qwen3-30B-A3B-shaped decode at batch 16: 48 layers x 128 experts, top-8, bf16, "
+                        "N(0,1) logits + per-expert bias N(0,0.5), B_pcie:B_cpu = 1:1, C = 1228 slots (20%) "
+                        "resized to 737 (12%) before step 128",
+    "dsv3_decode_slice": "DeepSeek-V3-shaped decode slice: 4 layers x 256 routed + 1 shared expert, top-8, "
+                         "H 7168, I 2048, fp8 e4m3 with 128x128 fp32 scales (44 MB blobs), batch 1, C = 112 "
+                         "slots (11%), Zipf(1.0) routing with 80% reuse",
+}
+
+
+def decode_workload_measure(name, args, dev, bw_measured, hbm_peak, peak_src, with_cpu):
+    """One of the other decode workloads: graph-replayed steps after an untimed
+    prefix, the kernel groups' event times over profiled replays after the
+    window, and a bounded oracle sample of the same workload."""
+    import torch
+    prefix, steps, n_phys, all_resident = EXTRA_WORKLOADS[name]
+    cfg = config(name)
+    s = cfg.shape
+    bw = cfg.bw_mbps or bw_measured
+    arena, offs = make_pool(s, cfg.seed, n_phys=n_phys)
+    pool = torch.from_numpy(arena).pin_memory()
+    del arena
+    shared = make_shared(s, cfg.seed) if s.n_shared else None
+    prof_steps = 16
+    run = DecodeRunner(cfg, pool, offs, shared, bw, dev, prefix + steps + prof_steps + 8)
+    run.warm(prefix)
+    ms, dcnt = run.timed(steps)
+    launches = int(run.cache.info()[6])
+    prof, dcnt_p = run.profiled(prof_steps)
+    groups = kernel_groups(s, prof, dcnt_p)
+    total_prof_ms = sum(v[0] for v in prof.values())
+    res = {"workload": WORKLOAD_DESC[name],
+           "value": round(steps * s.L / (ms / 1e3), 1), "unit": UNIT, "steps": steps,
+           "ms_per_step": round(ms / steps, 4),
+           "window": {"trace_steps": f"[{prefix}, {prefix + steps}) mod {cfg.steps}", "untimed_prefix_steps": prefix},
+           "cache_stats": cache_stats(dcnt), "gpu_launches": steps * s.L * launches,
+           "B_pcie_mbps": bw[0], "B_cpu_mbps": bw[1], "blob_bytes": int(s.blob_bytes),
+           "host_pool": f"{n_phys or s.n_flat} distinct seeded expert blobs, flat id f -> blob f mod "
+                        f"{n_phys or s.n_flat}",
+           "roofline": roofline_from_groups(groups, hbm_peak, peak_src, WORKLOAD_TRAFFIC.get(name),
+                                            WORKLOAD_TRAFFIC_SOURCE.get(name)),
+           "roofline_note": "the kernel group with the most event time, over profiled replays of the "
+                            f"{prof_steps} steps after the timed window (fills and CPU-assigned pairs as they occur)",
+           "kernel_groups": {k: {"bytes_per_launch": round(b / max(1, n)), "us_per_launch": round(1e3 * m / max(1, n), 2),
+                                 "gbs": round(b / (m / 1e3) / 1e9, 1) if m > 0 else None}
+                             for k, (b, m, n) in groups.items()},
+           "kernel_ms_share": {k: round(v[0] / total_prof_ms, 3) for k, v in prof.items() if v[1]},
+           "control_us": round(1e3 * prof["control"][0] / max(1, prof["control"][1]), 2)}
+    if run.resize_ms is not None:
+        res["resize_ms"] = round(run.resize_ms, 2)
+        res["resize_note"] = "moe_cache_resize (a safe point that synchronises) plus the graph re-capture, inside " \
+                             "the timed window"
+    if all_resident:
+        run.profiled(3, same_step=True)
+        rp, dr = run.profiled(16, same_step=True)
+        rg = kernel_groups(s, rp, dr)
+        res["roofline_all_resident"] = roofline_from_groups({"gemv_resident": rg["gemv_resident"]}, hbm_peak, peak_src)
+        res["roofline_all_resident_note"] = "one step's inputs replayed until every routed expert is resident; " \
+                                            f"{int(dr[2])} fills during the 16 replays"
+    run.close()
+    if with_cpu:
+        res["cpu_baseline"] = run_cpu_baseline(min(args.cpu_seconds, 6.0), n_phys or s.n_flat, bw, workload=name)
+    return res
 
 
 def profile_case(args, dev):
@@ -565,69 +824,27 @@ FP4_DESC = {"nvfp4": "NVFP4 experts (e2m1 + e4m3 per 16 + fp32 per matrix)",
             "mxfp4": "MXFP4 experts (e2m1 + e8m0 per 32)"}
 
 
-def fp4_measure(args, dev, local, b_pcie, b_cpu, fmt, steps=64, warmup=8):
+def fp4_measure(args, dev, local, b_pcie, b_cpu, fmt, steps=64):
     """The decode workload with 4-bit experts (same shape, routing and slot count):
     a blob is 2.65 MB (NVFP4) or 2.51 MB (MXFP4) instead of 9.44 MB, so fills
     and the resident GEMVs move 3.6x or 3.8x fewer bytes.  Graph replay of whole
-    steps, inputs resident."""
+    steps after the same untimed prefix as the headline, inputs resident."""
     import torch
-    from serving_layer_moe_gb300 import MoECache
     base = config(WORKLOAD)
     cfg = base.with_(shape=base.shape.__class__(**{**base.shape.__dict__, "wdtype": fmt}))
     s = cfg.shape
     arena, offs = make_pool(s, cfg.seed, n_phys=args.pool_blobs)
     pool = torch.from_numpy(arena).pin_memory()
     del arena
-    K = default_max_fetch(s, cfg.T)
-    cache = MoECache(L=s.L, E=s.E, H=s.H, I=s.I, top_k=s.k, max_tokens=cfg.T, wdtype=s.wdtype, adtype=s.adtype,
-                     host_pool=pool, blob_offsets=offs, n_slots=cfg.capacity, max_fetch=K, bw_pcie_mbps=b_pcie,
-                     bw_cpu_mbps=b_cpu, device=local)
-    ids, w = routing_trace(cfg)
-    xs = np.stack([np.stack([activations(cfg, st, l) for l in range(s.L)]) for st in range(cfg.steps)])
-    x_all = torch.from_numpy(xs.view(np.int16)).to(dev)
-    ids_all = torch.from_numpy(ids).to(dev)
-    w_all = torch.from_numpy(w).to(dev)
-    xb, ib, wb = torch.empty_like(x_all[0]), torch.empty_like(ids_all[0]), torch.empty_like(w_all[0])
-    out = torch.empty(s.L, cfg.T, s.H, dtype=torch.float32, device=dev)
-    cpu_part = torch.zeros(cfg.T, s.k, s.H, dtype=torch.float32, device=dev)
-    stream = torch.cuda.Stream(device=dev)
-    sp = stream.cuda_stream
-
-    def enqueue_step():
-        for l in range(s.L):
-            cache.decode_ptrs(l, cfg.T, xb[l].data_ptr(), ib[l].data_ptr(), wb[l].data_ptr(), cpu_part.data_ptr(),
-                              out[l].data_ptr(), None, sp)
-
-    def stage(st):
-        xb.copy_(x_all[st % cfg.steps], non_blocking=True)
-        ib.copy_(ids_all[st % cfg.steps], non_blocking=True)
-        wb.copy_(w_all[st % cfg.steps], non_blocking=True)
-
-    with torch.cuda.stream(stream):
-        for st in range(warmup):
-            stage(st)
-            enqueue_step()
-    torch.cuda.synchronize(dev)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        enqueue_step()
-    torch.cuda.synchronize(dev)
-    cnt0 = cache.state()[3].copy()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for st in range(warmup, warmup + steps):
-            stage(st)
-            graph.replay()
-        e1.record(stream)
-    torch.cuda.synchronize(dev)
-    ms = e0.elapsed_time(e1)
-    cnt1 = cache.state()[3].copy()
-    cache.close()
+    run = DecodeRunner(cfg, pool, offs, None, (b_pcie, b_cpu), dev, PREFIX_STEPS + steps)
+    run.warm(PREFIX_STEPS)
+    ms, dcnt = run.timed(steps)
+    run.close()
     return {"workload": f"{WORKLOAD} with {FP4_DESC[fmt]}, C={cfg.capacity} slots",
             "value": round(steps * s.L / (ms / 1e3), 1), "unit": UNIT, "steps": steps,
+            "window": f"trace steps [{PREFIX_STEPS}, {PREFIX_STEPS + steps})",
             "ms_per_step": round(ms / steps, 4), "blob_bytes": int(s.blob_bytes),
-            "fills": int(cnt1[2] - cnt0[2]), "hits": int(cnt1[0] - cnt0[0])}
+            "fills": int(dcnt[2]), "hits": int(dcnt[0])}
 
 
 def prefill_measure(args, dev, local):
@@ -825,6 +1042,7 @@ if __name__ == "__main__":
     a = parse_args()
     if a.cpu_worker:
         b = os.environ.get("BENCH_BW", "200000,100000").split(",")
-        cpu_worker(a.cpu_seconds, a.pool_blobs, (int(b[0]), int(b[1])), samples=a.cpu_samples)
+        cpu_worker(a.cpu_seconds, a.pool_blobs, (int(b[0]), int(b[1])), samples=a.cpu_samples,
+                   workload=a.cpu_workload)
     else:
         main(a)
