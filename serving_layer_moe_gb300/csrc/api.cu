@@ -173,13 +173,19 @@ extern "C" moe_status moe_cache_create(const moe_config* cfg, const void* host_p
   c->gemv_grid = 2 * c->sms;
   c->fill_ctas = c->sms / 2;
   {
-    // The resident experts of a decode call run as two grids (gate/up, then down +
-    // combine).  MOE_DECODE_FUSED=1 runs one-token calls as one launch with a
-    // grid-wide barrier between the two instead: faster in layer-steps without
-    // fills, slower in those with fills (the barrier waits for CTAs on the SMs the
-    // fill's host reads slow down).
+    // One-token calls run their resident experts as one expert-major stream of
+    // gate/up and down items (the default), or, chosen by MOE_DECODE_RESIDENT when
+    // the cache is created: "grids" = a gate/up grid then a down + combine grid,
+    // "fused" = one launch with a grid-wide barrier between the two (also
+    // MOE_DECODE_FUSED=1).  All three give the same outputs bit for bit.
+    const char* er = getenv("MOE_DECODE_RESIDENT");
     const char* ef = getenv("MOE_DECODE_FUSED");
-    c->fused = ef && ef[0] == '1';
+    c->resident_mode = 2;
+    if (ef && ef[0] == '1') c->resident_mode = 1;
+    if (er && strcmp(er, "grids") == 0) c->resident_mode = 0;
+    else if (er && strcmp(er, "fused") == 0) c->resident_mode = 1;
+    else if (er && strcmp(er, "stream") == 0) c->resident_mode = 2;
+    else if (er && er[0]) return bail(fail(MOE_EINVAL, "MOE_DECODE_RESIDENT must be grids, fused or stream"));
   }
   if ((k.wdtype == MOE_NVFP4 || k.wdtype == MOE_MXFP4) && !fp4_decode_fits(c->sh, k.max_tokens, c->sms))
     return bail(fail(MOE_EINVAL, "fp4 weights: H / I too large for the bulk decode kernels"));
@@ -242,7 +248,8 @@ extern "C" moe_status moe_cache_create(const moe_config* cfg, const void* host_p
                  o_sm = take((size_t)k.max_tokens * k.top_k * 4), o_goff = take((size_t)(max_gpu + 1) * 4),
                  o_gp = take(max_pairs * 4), o_gw = take((size_t)max_gpu * 8),
                  o_h = take(max_pairs * k.inter * 4), o_y = take(max_pairs * k.hidden * 4),
-                 o_arr = take((size_t)k.hidden * 4), o_fb = take(8);
+                 o_arr = take((size_t)k.hidden * 4), o_fb = take(8),
+                 o_sc = take((size_t)(max_gpu + k.hidden) * 4);
     CKB(cudaMalloc(&c->work, off));
     CKB(cudaMemset(c->work, 0, off));
     uint8_t* w = static_cast<uint8_t*>(c->work);
@@ -258,6 +265,9 @@ extern "C" moe_status moe_cache_create(const moe_config* cfg, const void* host_p
     c->b.y = reinterpret_cast<float*>(w + o_y);
     c->b.arrive = reinterpret_cast<uint32_t*>(w + o_arr);
     c->b.fused_bar = reinterpret_cast<unsigned long long*>(w + o_fb);
+    c->b.scnt = reinterpret_cast<uint32_t*>(w + o_sc);
+    // one-token calls are the only ones the stream kernel takes
+    c->b.n_scnt = c->resident_mode == 2 ? resident_stream_counters(c->sh, 1, c->sms) : 0;
     c->dev_bytes = off;
   }
   c->dev_bytes += c->C * S + nflat * 12 + c->C * 12 + (k.n_shared ? (uint64_t)k.n_layers * S : 0);
@@ -314,7 +324,7 @@ extern "C" moe_status moe_layer_decode(moe_cache* c, int32_t layer, int32_t T, c
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   c->last_T = T;
   const bool split = down_split_ok(c->sh, T, c->sms);
-  const bool fused = split && c->fused && resident_fused_ok(c->sh, T, c->sms);
+  const int path = resident_path(c, T);
   {
     ProfScope p(c, s, PROF_CONTROL);
     CK(launch_decode_control(c->sh, layer, T, (int)c->C, c->K, c->cfg.bw_pcie_mbps, c->cfg.bw_cpu_mbps, ids,
@@ -328,18 +338,21 @@ extern "C" moe_status moe_layer_decode(moe_cache* c, int32_t layer, int32_t T, c
     CK(launch_fill_gate_up(c->sh, T, x, c->b, c->host_pool_dev, c->offsets, c->slots, c->fill_ctas, c->fill_stream));
   }
   if (split) {
-    // Beside the fused resident launch, whose CTAs wait on one another at its grid
-    // barrier, the filled-expert grid is a plain launch: launched early, its CTAs
-    // would sit on SMs for the whole fill and could keep some fused CTAs off the GPU.
+    // Beside a resident launch whose warps wait on one another (the fused launch's
+    // grid barrier, the stream's per-expert counts), the filled-expert grid is a
+    // plain launch: launched early, its CTAs would sit on SMs for the whole fill
+    // and could keep some of that launch's CTAs off the GPU.
     ProfScope p(c, c->fill_stream, PROF_DOWN_FILLED);
-    CK(launch_down_split(c->sh, 1, T, w, cpu_part, c->b, out, c->err_dev, c->sms, c->fill_stream, !fused));
+    CK(launch_down_split(c->sh, 1, T, w, cpu_part, c->b, out, c->err_dev, c->sms, c->fill_stream, path == 0));
   }
   CK(cudaEventRecord(c->ev_fill, c->fill_stream));
   if (split) {
     {
       // one timed group: the two grids run back to back under a programmatic dependency
       ProfScope p(c, s, PROF_GEMV_RESIDENT);
-      if (fused) {
+      if (path == 2) {
+        CK(launch_resident_stream(c->sh, T, x, w, cpu_part, c->b, out, c->err_dev, c->sms, s));
+      } else if (path == 1) {
         CK(launch_resident_fused(c->sh, T, x, w, cpu_part, c->b, out, c->err_dev, c->sms, s));
       } else {
         CK(launch_gate_up(c->sh, 0, T, x, c->b, c->sms, s, c->err_dev));
@@ -400,14 +413,14 @@ extern "C" moe_status moe_cache_info(moe_cache* c, uint64_t* info) {
   info[4] = c->dev_bytes; info[5] = c->host_bytes; info[7] = 0;
   {
     const int T = c->cfg.max_tokens;
-    if (down_split_ok(c->sh, T, c->sms) && c->fused && resident_fused_ok(c->sh, T, c->sms)) info[7] = 1;
+    info[7] = (uint64_t)resident_path(c, T);
   }
   {
     // control + fill + resident experts (one fused launch, or gate/up + down) + filled-expert down,
     // or control + fill + gate/up + the down/combine kernels where the split ones do not fit
     const int T = c->cfg.max_tokens;
     if (down_split_ok(c->sh, T, c->sms))
-      info[6] = (c->fused && resident_fused_ok(c->sh, T, c->sms)) ? 4 : 5;
+      info[6] = resident_path(c, T) != 0 ? 4 : 5;
     else
       info[6] = 3 + (uint64_t)down_combine_launches(c->sh, T, c->sms);
   }

@@ -43,7 +43,9 @@ struct moe_cache {
   int sms = 0;
   int gemv_grid = 0;
   int fill_ctas = 0;
-  bool fused = false;              // one-token resident gate/up + down in one launch (MOE_DECODE_FUSED=1)
+  // how one-token calls run their resident experts: 0 a gate/up grid then a down +
+  // combine grid, 1 one launch with a grid-wide barrier, 2 one expert-major stream
+  int resident_mode = 2;
   // host pool
   const uint8_t* host_pool = nullptr;
   const uint8_t* host_pool_dev = nullptr;
@@ -72,6 +74,15 @@ struct moe_cache {
   std::vector<int> prof_kind;               // kind of each pair
   size_t prof_used = 0;
 };
+
+// The resident-expert path a call of T tokens takes (0, 1 or 2 as resident_mode;
+// only split-down shapes take 1 or 2, and only where that kernel applies).
+inline int resident_path(const moe_cache* c, int T) {
+  if (!down_split_ok(c->sh, T, c->sms)) return 0;
+  if (c->resident_mode == 2 && resident_stream_ok(c->sh, T, c->sms)) return 2;
+  if (c->resident_mode == 1 && resident_fused_ok(c->sh, T, c->sms)) return 1;
+  return 0;
+}
 
 // Record a start/stop event pair around a kernel group of `kind` when profiling.
 struct ProfScope {

@@ -159,6 +159,9 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
   }
   pdl_wait();       // the routed ids may come from the preceding kernel
   pdl_trigger();
+  // the resident stream kernel's counters start each call at zero (its previous
+  // launch has completed: it precedes this kernel in the stream)
+  for (int i = tid; i < a.b.n_scnt; i += nt) a.b.scnt[i] = 0u;
   if (kSel == 2 && P + a.n_shared <= 32 && NW <= 32) {
     // ---- one warp for calls of at most 32 routed pairs ---------------------------
     // The steps below for a handful of pairs, in warp 0 with ballots and warp

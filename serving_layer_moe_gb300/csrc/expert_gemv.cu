@@ -1668,6 +1668,292 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 2) resident_fused_kernel(Gem
   if (missing) atomicOr_system(err, kErrMissingCpuPart);
 }
 
+// ---- resident experts, one token: gate/up and down rows as one expert-major stream --------
+// One bf16 token, bf16 weights, no shared expert.  Every byte the resident
+// experts need flows through the per-warp rings of one item list:
+//   items [0, ng*I):         gate row i + up row i of expert g (n = g*I + i)
+//   items [ng*I, ng*I + D):  RS rows of one row block b of expert g's W_down
+//                            (expert-major, then block, then sub-block q)
+// and warp w of the grid takes items w, w + warps, ...  Weight copies do not
+// depend on h, so lane 0 keeps NS items in flight whatever they are; only the
+// arithmetic of a down item waits, for its expert's h.  Because every gate/up
+// item precedes every down item, a warp holding a gate/up item never waits on
+// anything but its own copies, so no wait can close a cycle, and the h of the
+// early experts is complete long before their down items come up: the down
+// projection runs inside the weight stream instead of after a grid-wide
+// barrier, and only the last expert's down rows trail it.
+//
+// Completion is counted per expert (gate/up rows done, zeroed by the control
+// kernel): a gate/up item publishes h with a release increment.  A down item
+// takes its expert's h with its weights when the count is complete at issue
+// time (checked with an acquire load, a proxy fence, then the bulk copy into the
+// same stage), else it waits for the count and reads h from L2.  The down items
+// of a row block are counted too; the warp that completes a block forms its
+// combine, or joins the split protocol with the filled-expert down grid (both
+// count themselves in arrive[b]; the second forms the combine from y in global
+// memory).  Arithmetic order is that of gate_up_bulk_kernel and down_bulk_kernel
+// (per-lane chunk sums, the same shuffle tree), so h, y and the layer output are
+// bit-identical to the two grids'.  Every wait is bounded by the global timer.
+constexpr int kStreamWarps = 8;
+constexpr int kStreamRows = 8;   // rows per down item, at most (one reduce8)
+
+struct StreamGeom {
+  int NS;            // ring stages per warp
+  int R, nblk;       // row blocks of the split down protocol: rows per block, blocks
+  int RS, Q;         // rows per down item, down items per (expert, row block)
+  size_t SB;         // stage bytes: a gate/up row pair, or RS down rows + the expert's h
+  size_t ring_off, plan_off, x_off, extra_off, smem;
+};
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+template <int kJX, int kJN>
+__global__ void __launch_bounds__(kStreamWarps * 32, 1) resident_stream_kernel(GemvArgs a, StreamGeom geo,
+                                                                              const float* __restrict__ w,
+                                                                              const float* __restrict__ cpu,
+                                                                              float* __restrict__ out, uint32_t* err) {
+  using F = WFmt<MOE_BF16>;
+  constexpr int V = 8;
+  extern __shared__ __align__(128) uint8_t sm[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm) + warp * geo.NS;
+  uint8_t* ring = sm + geo.ring_off + (size_t)warp * geo.NS * geo.SB;
+  if (lane == 0) {
+    for (int i = 0; i < geo.NS; ++i) bar_init(&bars[i]);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  pdl_wait();
+  pdl_trigger();
+  const StagedPlan sp = stage_plan(sm + geo.plan_off, a);
+  const int H = a.H, I = a.I, k = a.k;
+  const int nfirst = a.b.plan[P_NFIRST], ngpu = a.b.plan[P_NGPU];
+  const bool skip = nfirst == 0 && ngpu > 0;   // only filled experts: their grid combines alone
+  const bool alone = ngpu == nfirst;           // no filled expert: this kernel combines alone
+  const int ng = skip ? 0 : nfirst;
+  uint32_t* gcnt = a.b.scnt;                   // [max_g] gate/up rows done per resident expert
+  uint32_t* bcnt = a.b.scnt + a.max_g;         // [nblk] down items done per row block
+  int* s_slot = reinterpret_cast<int*>(sm + geo.extra_off);
+  float* s_wt = reinterpret_cast<float*>(s_slot + k);
+  uint8_t* xsm = sm + geo.x_off;
+  for (int i = threadIdx.x; i < k; i += blockDim.x) { s_slot[i] = a.b.slot_map[i]; s_wt[i] = w[i]; }
+  {
+    uint4* dst = reinterpret_cast<uint4*>(xsm);
+    const uint4* src = reinterpret_cast<const uint4*>(a.x);
+    for (int i = threadIdx.x; i < H / 8; i += blockDim.x) dst[i] = src[i];
+  }
+  __syncthreads();
+  const long nwarps = (long)gridDim.x * kStreamWarps;
+  const long w0 = (long)blockIdx.x * kStreamWarps + warp;
+  const size_t row_h = F::row(H), row_i = F::row(I);
+  const size_t down_off = 2ull * (size_t)I * row_h;
+  const size_t hbytes = (size_t)I * 4;
+  const int per_e = geo.nblk * geo.Q;
+  const long n_gu = (long)ng * I;
+  const long items = n_gu + (long)ng * per_e;
+  const uint64_t pol = evict_first_policy();
+  bool missing = false;
+
+  // the combine of row block b by this warp: out[r] = sum_j w[j] * (slot >= 0 ? y : cpu)
+  auto combine_block = [&](int b) {
+    bool second = true;
+    if (!alone) {
+      uint32_t old = 0;
+      if (lane == 0)
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(a.b.arrive + b) : "memory");
+      second = (__shfl_sync(0xffffffffu, old, 0) & 1u) != 0u;
+    }
+    __syncwarp();
+    if (!second) return;
+    const int rb = b * geo.R;
+    const int nrb = min(geo.R, H - rb);
+    if (lane < nrb) {
+      const int r = rb + lane;
+      float acc = 0.f;
+      for (int j = 0; j < k; ++j) {
+        float v;
+        if (s_slot[j] >= 0) {
+          v = __ldcg(a.b.y + (size_t)j * H + r);
+        } else if (cpu != nullptr) {
+          v = __ldg(cpu + (size_t)j * H + r);
+        } else {
+          v = 0.f;
+          missing = true;
+        }
+        acc = fmaf(s_wt[j], v, acc);
+      }
+      out[r] = acc;
+    }
+  };
+
+  if (ng == 0) {   // every pair on the CPU (or only filled experts: their grid combines)
+    if (!skip)
+      for (long b = w0; b < geo.nblk; b += nwarps) combine_block((int)b);
+    if (missing) atomicOr_system(err, kErrMissingCpuPart);
+    return;
+  }
+
+  struct DownItem { int g, b, r0, nr; };
+  auto down_item = [&](long it) {
+    DownItem d;
+    const int m = (int)(it - n_gu);
+    d.g = m / per_e;
+    const int rem = m - d.g * per_e;
+    d.b = rem / geo.Q;
+    const int q = rem - d.b * geo.Q;
+    d.r0 = d.b * geo.R + q * geo.RS;
+    d.nr = min(geo.RS, min(geo.R, H - d.b * geo.R) - q * geo.RS);
+    return d;
+  };
+  long last_issued[4] = {-1, -1, -1, -1};
+  bool h_staged[4] = {false, false, false, false};   // lane 0: the stage holds its expert's h
+  auto issue = [&](long it, int st) {   // lane 0 only
+    last_issued[st] = it;
+    uint8_t* dst = ring + (size_t)st * geo.SB;
+    if (it < n_gu) {
+      const int g = (int)(it / I), i = (int)(it % I);
+      bar_expect(&bars[st], (uint32_t)(2 * row_h));
+      bulk_copy(dst, sp.w[g] + (size_t)i * row_h, (uint32_t)row_h, &bars[st], pol);
+      bulk_copy(dst + row_h, sp.w[g] + (size_t)(I + i) * row_h, (uint32_t)row_h, &bars[st], pol);
+      return;
+    }
+    const DownItem d = down_item(it);
+    if (d.nr <= 0) {   // past the last row: an empty item, counted like the others
+      bar_expect(&bars[st], 0u);
+      h_staged[st] = false;
+      return;
+    }
+    const uint32_t wb = (uint32_t)(d.nr * row_i);
+    // h is final once every gate/up row of the expert is counted; then it rides along
+    const bool hs = ld_acquire_u32(gcnt + d.g) >= (uint32_t)I;
+    h_staged[st] = hs;
+    bar_expect(&bars[st], wb + (hs ? (uint32_t)hbytes : 0u));
+    bulk_copy(dst, sp.w[d.g] + down_off + (size_t)d.r0 * row_i, wb, &bars[st], pol);
+    if (hs) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      const int pid = sp.pid[sp.off[d.g]];
+      bulk_copy_keep(dst + (size_t)geo.RS * row_i, a.b.h + (size_t)pid * I, (uint32_t)hbytes, &bars[st]);
+    }
+  };
+  const long n_mine = items > w0 ? (items - w0 + nwarps - 1) / nwarps : 0;
+  if (lane == 0)
+    for (int kk = 0; kk < geo.NS && kk < n_mine; ++kk) issue(w0 + (long)kk * nwarps, kk);
+  uint4 xr[kJX];
+#pragma unroll
+  for (int j = 0; j < kJX; ++j) xr[j] = reinterpret_cast<const uint4*>(xsm)[j * 32 + lane];
+  bool ok = true;
+  int kk = 0;
+  for (long it = w0; it < items; it += nwarps, ++kk) {
+    const int st = kk % geo.NS;
+    if (!__all_sync(0xffffffffu, bar_wait(&bars[st], (uint32_t)((kk / geo.NS) & 1)))) { ok = false; break; }
+    const uint8_t* stage = ring + (size_t)st * geo.SB;
+    if (it < n_gu) {
+      const int g = (int)(it / I), i = (int)(it % I);
+      const uint4* gate = reinterpret_cast<const uint4*>(stage);
+      const uint4* up = reinterpret_cast<const uint4*>(stage + row_h);
+      float ag = 0.f, au = 0.f;   // the per-chunk partials and order of gate_up_bulk_kernel
+#pragma unroll
+      for (int j = 0; j < kJX; ++j) {
+        const uint4 wg = gate[j * 32 + lane], wu = up[j * 32 + lane];
+        float pg = 0.f, pu = 0.f;
+        pg = fma_bf16x2(wg.x, xr[j].x, pg); pu = fma_bf16x2(wu.x, xr[j].x, pu);
+        pg = fma_bf16x2(wg.y, xr[j].y, pg); pu = fma_bf16x2(wu.y, xr[j].y, pu);
+        pg = fma_bf16x2(wg.z, xr[j].z, pg); pu = fma_bf16x2(wu.z, xr[j].z, pu);
+        pg = fma_bf16x2(wg.w, xr[j].w, pg); pu = fma_bf16x2(wu.w, xr[j].w, pu);
+        ag += pg;
+        au += pu;
+      }
+      ag = warp_sum(ag);
+      au = warp_sum(au);
+      if (lane == 0) {
+        a.b.h[(size_t)sp.pid[sp.off[g]] * I + i] = silu(ag) * au;
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(gcnt + g) : "memory");
+      }
+    } else {
+      const DownItem d = down_item(it);
+      if (d.nr > 0) {
+        const int pid = sp.pid[sp.off[d.g]];
+        const bool hs = __shfl_sync(0xffffffffu, lane == 0 ? (int)h_staged[st] : 0, 0) != 0;
+        float hv[kJN][V];
+        if (hs) {
+          const float* hsm = reinterpret_cast<const float*>(stage + (size_t)geo.RS * row_i);
+#pragma unroll
+          for (int j = 0; j < kJN; ++j) {
+            const float4* hp = reinterpret_cast<const float4*>(hsm + (size_t)(j * 32 + lane) * V);
+            const float4 q0 = hp[0], q1 = hp[1];
+            hv[j][0] = q0.x; hv[j][1] = q0.y; hv[j][2] = q0.z; hv[j][3] = q0.w;
+            hv[j][4] = q1.x; hv[j][5] = q1.y; hv[j][6] = q1.z; hv[j][7] = q1.w;
+          }
+        } else {
+          // wait for the expert's h (its last gate/up rows are still on their way)
+          bool done = true;
+          if (lane == 0) {
+            const unsigned long long t0 = gtime();
+            for (uint32_t n = 0; ld_acquire_u32(gcnt + d.g) < (uint32_t)I; ++n)
+              if ((n & 15u) == 15u && gtime() - t0 > kBulkWaitNs) { done = false; break; }
+          }
+          if (!__shfl_sync(0xffffffffu, (int)done, 0)) { ok = false; break; }
+#pragma unroll
+          for (int j = 0; j < kJN; ++j) {
+            const float4* hp = reinterpret_cast<const float4*>(a.b.h + (size_t)pid * I + (size_t)(j * 32 + lane) * V);
+            const float4 q0 = __ldcg(hp), q1 = __ldcg(hp + 1);
+            hv[j][0] = q0.x; hv[j][1] = q0.y; hv[j][2] = q0.z; hv[j][3] = q0.w;
+            hv[j][4] = q1.x; hv[j][5] = q1.y; hv[j][6] = q1.z; hv[j][7] = q1.w;
+          }
+        }
+        // the straight-line rows of down_bulk_kernel: rows past nr repeat the last
+        // row (never stored), per-lane sums in the same order, the same shuffle tree
+        float acc[kStreamRows];
+#pragma unroll
+        for (int r = 0; r < kStreamRows; ++r) {
+          const int rr = r < d.nr ? r : d.nr - 1;
+          const uint4* wrow = reinterpret_cast<const uint4*>(stage + (size_t)rr * row_i);
+          float dsum = 0.f;
+#pragma unroll
+          for (int j = 0; j < kJN; ++j) {
+            float fw[V];
+            F::unpack(wrow[j * 32 + lane], fw);
+            float dj = 0.f;
+#pragma unroll
+            for (int v = 0; v < V; ++v) dj = fmaf(fw[v], hv[j][v], dj);
+            dsum += dj;
+          }
+          acc[r] = 0.f + dsum;
+        }
+        const float v = reduce8(acc, lane);
+        const int r = (lane >> 2) & 7;
+        if ((lane & 3) == 0 && r < d.nr) a.b.y[(size_t)pid * H + d.r0 + r] = v;
+      }
+      // count the item in its row block; the warp that completes the block combines it
+      __syncwarp();
+      uint32_t old = 0;
+      if (lane == 0)
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(bcnt + d.b) : "memory");
+      if (__shfl_sync(0xffffffffu, old, 0) + 1u == (uint32_t)(ng * geo.Q)) combine_block(d.b);
+    }
+    __syncwarp();
+    if (lane == 0 && it + (long)geo.NS * nwarps < items) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(it + (long)geo.NS * nwarps, st);
+    }
+  }
+  if (!ok && lane == 0) {   // flag the timeout; this warp's copies land before the CTA exits
+    atomicOr_system(err, kErrTimeout);
+    for (int s2 = 0; s2 < geo.NS; ++s2) {
+      if (last_issued[s2] < 0) continue;
+      const long k2 = (last_issued[s2] - w0) / nwarps;
+      const uint32_t par = (uint32_t)((k2 / geo.NS) & 1);
+      const unsigned long long t0 = gtime();
+      while (!bar_test(&bars[s2], par) && gtime() - t0 < kBulkWaitNs) {
+      }
+    }
+  }
+  if (missing) atomicOr_system(err, kErrMissingCpuPart);
+}
+
 // ---- combine: out[t] = sum_j w[t,j] * (slot >= 0 ? y : cpu_part) in j order (+ shared) --
 __global__ void combine_kernel(int T, int H, int k, int n_shared, const float* __restrict__ w,
                                const int32_t* __restrict__ sm, const float* __restrict__ y,
@@ -1900,7 +2186,9 @@ cudaError_t setup_gemv_kernels() {
     if (e != cudaSuccess) return e;
   }
   for (const void* k : {(const void*)resident_fused_kernel<8, 3>, (const void*)resident_fused_kernel<8, 4>,
-                        (const void*)resident_fused_kernel<4, 3>, (const void*)resident_fused_kernel<4, 4>}) {
+                        (const void*)resident_fused_kernel<4, 3>, (const void*)resident_fused_kernel<4, 4>,
+                        (const void*)resident_stream_kernel<8, 3>, (const void*)resident_stream_kernel<8, 4>,
+                        (const void*)resident_stream_kernel<4, 3>, (const void*)resident_stream_kernel<4, 4>}) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFusedSmemMax);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, kDecodeCarveout);
     if (e != cudaSuccess) return e;
@@ -2209,6 +2497,63 @@ cudaError_t launch_resident_fused(const Shape& sh, int T, const void* x, const f
   return launch_pdl(resident_fused_kernel<4, 4>, grid, block, g.smem, s, a, g, w, cpu_part, out, err);
 }
 
+
+// Geometry of resident_stream_kernel, or NS = 0 when the call does not take it:
+// bf16 weights and activations, one token, no shared expert, gate/up rows of 4 or
+// 8 16-byte chunks per lane, W_down rows of 3 or 4, and the row blocks of the
+// split down kernels (the filled-expert grid's combine protocol counts per block).
+// A stage holds a gate/up row pair, or RS down rows plus the expert's h.
+StreamGeom stream_geom(const GemvArgs& a, int wdtype, int adtype, int sms) {
+  StreamGeom g{};
+  if (wdtype != MOE_BF16 || adtype != MOE_BF16 || a.T != 1 || a.n_shared != 0) return g;
+  if (a.H % 256 != 0 || (a.H / 256 != 4 && a.H / 256 != 8) || a.I % 256 != 0 || (a.I / 256 != 3 && a.I / 256 != 4))
+    return g;
+  const BulkGeom dg = down_geom(a, wdtype, sms);
+  if (dg.NS < 1 || !dg.h_smem || dg.R < 1) return g;
+  g.R = dg.R;
+  g.nblk = dg.grid;
+  const size_t row_h = wrow(MOE_BF16, (size_t)a.H), row_i = wrow(MOE_BF16, (size_t)a.I), hb = (size_t)a.I * 4;
+  g.SB = up128(std::max(2 * row_h, hb + 2 * row_i));
+  g.RS = (int)std::min<size_t>(std::min<size_t>((size_t)kStreamRows, (size_t)g.R), (g.SB - hb) / row_i);
+  g.Q = (g.R + g.RS - 1) / g.RS;
+  const size_t plan = up128(staged_plan_bytes(a.max_g, a.max_p));
+  const size_t xb = up128((size_t)a.H * 2);
+  const size_t extra = up128((size_t)a.k * 8);
+  g.ring_off = 256;
+  for (g.NS = 3; g.NS >= 2; --g.NS) {
+    g.plan_off = g.ring_off + (size_t)kStreamWarps * g.NS * g.SB;
+    g.x_off = g.plan_off + plan;
+    g.extra_off = g.x_off + xb;
+    g.smem = g.extra_off + extra;
+    if (g.smem <= kFusedSmemMax) return g;
+  }
+  g.NS = 0;
+  return g;
+}
+
+bool resident_stream_ok(const Shape& sh, int T, int sms) {
+  const GemvArgs a = make_args(sh, 0, T, nullptr, DecodeBufs{});
+  return stream_geom(a, sh.wdtype, sh.adtype, sms).NS > 0;
+}
+
+int resident_stream_counters(const Shape& sh, int T, int sms) {
+  const GemvArgs a = make_args(sh, 0, T, nullptr, DecodeBufs{});
+  const StreamGeom g = stream_geom(a, sh.wdtype, sh.adtype, sms);
+  return g.NS > 0 ? a.max_g + g.nblk : 0;
+}
+
+cudaError_t launch_resident_stream(const Shape& sh, int T, const void* x, const float* w, const float* cpu_part,
+                                   DecodeBufs b, float* out, uint32_t* err, int sms, cudaStream_t s) {
+  const GemvArgs a = make_args(sh, 0, T, x, b);
+  const StreamGeom g = stream_geom(a, sh.wdtype, sh.adtype, sms);
+  if (g.NS == 0 || b.scnt == nullptr || b.n_scnt < a.max_g + g.nblk) return cudaErrorInvalidValue;
+  const dim3 grid(sms), block(kStreamWarps * 32);
+  const int jx = a.H / 256, jn = a.I / 256;
+  if (jx == 8 && jn == 3) return launch_pdl(resident_stream_kernel<8, 3>, grid, block, g.smem, s, a, g, w, cpu_part, out, err);
+  if (jx == 8 && jn == 4) return launch_pdl(resident_stream_kernel<8, 4>, grid, block, g.smem, s, a, g, w, cpu_part, out, err);
+  if (jx == 4 && jn == 3) return launch_pdl(resident_stream_kernel<4, 3>, grid, block, g.smem, s, a, g, w, cpu_part, out, err);
+  return launch_pdl(resident_stream_kernel<4, 4>, grid, block, g.smem, s, a, g, w, cpu_part, out, err);
+}
 
 cudaError_t launch_down_combine(const Shape& sh, int T, const float* w, const float* cpu_part, DecodeBufs b,
                                 float* out, uint32_t* err, int sms, cudaStream_t s) {

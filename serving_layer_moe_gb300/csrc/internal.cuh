@@ -61,6 +61,8 @@ struct DecodeBufs {
   float* y;               // [max_pairs, H] expert outputs (unweighted)
   uint32_t* arrive;       // [H] arrivals of the two split down kernels per row block (parity = who combines)
   unsigned long long* fused_bar;   // grid-barrier arrivals of the fused resident kernel (only grows)
+  uint32_t* scnt;         // [n_scnt] per-call counters of the resident stream kernel, zeroed by the control kernel
+  int n_scnt;
 };
 
 struct CacheTables {
@@ -139,6 +141,16 @@ cudaError_t launch_combine(const Shape& sh, int T, const float* w, const float* 
 bool resident_fused_ok(const Shape& sh, int T, int sms);
 cudaError_t launch_resident_fused(const Shape& sh, int T, const void* x, const float* w, const float* cpu_part,
                                   DecodeBufs b, float* out, uint32_t* err, int sms, cudaStream_t s);
+// Gate/up + down + combine of the resident experts as one expert-major stream of
+// weight items (bf16, one token, no shared expert): down rows start while later
+// experts' gate/up rows still stream, counted per expert and per row block, no
+// grid-wide barrier.  Can replace launch_gate_up(pass 0) + launch_down_split(pass 0).
+// It needs b.scnt with resident_stream_counters() entries zeroed before each call
+// (the control kernel does it).
+bool resident_stream_ok(const Shape& sh, int T, int sms);
+int resident_stream_counters(const Shape& sh, int T, int sms);
+cudaError_t launch_resident_stream(const Shape& sh, int T, const void* x, const float* w, const float* cpu_part,
+                                   DecodeBufs b, float* out, uint32_t* err, int sms, cudaStream_t s);
 int down_combine_launches(const Shape& sh, int T, int sms);   // kernels of launch_down_combine
 int gemv_block_threads();
 

@@ -1,13 +1,14 @@
-"""The two ways a decode call can run its resident experts, against each other.
+"""The three ways a decode call can run its resident experts, against each other.
 
-By default a gate/up grid then a down + combine grid; with MOE_DECODE_FUSED=1
-set when the cache is created, one-token bf16 calls run both in one launch
-with a grid-wide barrier between them.  Both compute each resident expert's
-gate/up rows, down rows and the combine in the same arithmetic order, so on
-the same trace they give bit-identical layer outputs; the fused launch is also
-held to the oracle (slot maps bit-exact, outputs within 2e-2).  The traces
-start cold, so they also cover calls with fills but no resident expert, and
-calls whose pairs all go to the CPU.
+One-token bf16 calls run by default as one expert-major stream of gate/up and
+down items (MOE_DECODE_RESIDENT=stream); "grids" runs a gate/up grid then a
+down + combine grid, "fused" one launch with a grid-wide barrier between them
+(also MOE_DECODE_FUSED=1).  All three compute each resident expert's gate/up
+rows, down rows and the combine in the same arithmetic order, so on the same
+trace they give bit-identical layer outputs; the stream and the fused launch
+are also held to the oracle (slot maps bit-exact, outputs within 2e-2).  The
+traces start cold, so they also cover calls with fills but no resident expert,
+and calls whose pairs all go to the CPU.
 """
 import os
 from dataclasses import replace
@@ -35,27 +36,32 @@ def _qwen3_small(T, steps, layers=6, **kw):
                                            capacity=int(0.37 * layers * shape.E), **kw)
 
 
-def _cache(cfg, pool, offs, bw, fused):
-    saved = os.environ.get("MOE_DECODE_FUSED")
-    os.environ["MOE_DECODE_FUSED"] = "1" if fused else "0"
+MODE_PATH = {"grids": 0, "fused": 1, "stream": 2}
+
+
+def _cache(cfg, pool, offs, bw, mode):
+    saved = {k: os.environ.get(k) for k in ("MOE_DECODE_FUSED", "MOE_DECODE_RESIDENT")}
+    os.environ.pop("MOE_DECODE_FUSED", None)
+    os.environ["MOE_DECODE_RESIDENT"] = mode
     try:
         return make_cache(cfg, pool, offs, None, bw)[0]
     finally:
-        if saved is None:
-            del os.environ["MOE_DECODE_FUSED"]
-        else:
-            os.environ["MOE_DECODE_FUSED"] = saved
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
 
 
-def _fused_equals_two_grids(cfg, bw):
+def _path_equals_two_grids(cfg, bw, mode):
     import torch
     s = cfg.shape
     dev = torch.device("cuda", 0)
     arena, offs, pool = build_pool(cfg, n_phys=16)
-    one = _cache(cfg, pool, offs, bw, True)
-    two = _cache(cfg, pool, offs, bw, False)
+    one = _cache(cfg, pool, offs, bw, mode)
+    two = _cache(cfg, pool, offs, bw, "grids")
     assert int(one.info()[6]) == 4 and int(two.info()[6]) == 5   # kernels per decode call
-    assert int(one.info()[7]) == 1 and int(two.info()[7]) == 0   # how the resident experts run
+    assert int(one.info()[7]) == MODE_PATH[mode] and int(two.info()[7]) == 0   # how the resident experts run
     ids, w = routing_trace(cfg)
     gen = torch.Generator(device="cpu").manual_seed(7)
     cpu = torch.randn(cfg.T, s.k, s.H, generator=gen).to(dev)     # read only where a pair goes to the CPU
@@ -82,24 +88,37 @@ def _fused_equals_two_grids(cfg, bw):
     return n_cpu, n_fill_only
 
 
-def test_fused_bit_identical_to_two_grids_offload():
-    n_cpu, n_fill_only = _fused_equals_two_grids(_qwen3_small(T=1, steps=20), (100000, 0))
+@pytest.mark.parametrize("mode", ["stream", "fused"])
+def test_bit_identical_to_two_grids_offload(mode):
+    n_cpu, n_fill_only = _path_equals_two_grids(_qwen3_small(T=1, steps=20), (100000, 0), mode)
     assert n_cpu == 0 and n_fill_only > 0
 
 
-def test_fused_bit_identical_to_two_grids_hybrid():
-    n_cpu, _ = _fused_equals_two_grids(_qwen3_small(T=1, steps=20), (100000, 900000))
+@pytest.mark.parametrize("mode", ["stream", "fused"])
+def test_bit_identical_to_two_grids_hybrid(mode):
+    n_cpu, _ = _path_equals_two_grids(_qwen3_small(T=1, steps=20), (100000, 900000), mode)
     assert n_cpu > 0
 
 
-def test_fused_bit_identical_all_cpu_calls():
+@pytest.mark.parametrize("mode", ["stream", "fused"])
+def test_bit_identical_all_cpu_calls(mode):
     # K = 0: no fill ever; cold calls send every pair to the CPU
-    n_cpu, _ = _fused_equals_two_grids(_qwen3_small(T=1, steps=4, layers=3, max_fetch=0), (1000, 1000))
+    n_cpu, _ = _path_equals_two_grids(_qwen3_small(T=1, steps=4, layers=3, max_fetch=0), (1000, 1000), mode)
     assert n_cpu > 0
 
 
-def test_fused_oracle_parity_one_token(monkeypatch):
-    monkeypatch.setenv("MOE_DECODE_FUSED", "1")
+def test_stream_bit_identical_hidden_1024_inter_1024():
+    # the other geometry the stream kernel takes: 4 x-chunks and 4 h-chunks per lane
+    shape = replace(QWEN3, L=4, E=32, H=1024, I=1024)
+    cfg = config("qwen3_decode_b1").with_(shape=shape, T=1, steps=12, capacity=40)
+    n_cpu, _ = _path_equals_two_grids(cfg, (100000, 100000), "stream")
+    assert n_cpu > 0
+
+
+@pytest.mark.parametrize("mode", ["stream", "fused"])
+def test_oracle_parity_one_token(monkeypatch, mode):
+    monkeypatch.delenv("MOE_DECODE_FUSED", raising=False)
+    monkeypatch.setenv("MOE_DECODE_RESIDENT", mode)
     cfg = _qwen3_small(T=1, steps=40)
     res = run_decode_parity(cfg, (100000, 100000), n_phys=24, fp_every=5, state_every=8)
     assert not res.mismatches, res.mismatches[:1]
@@ -107,9 +126,11 @@ def test_fused_oracle_parity_one_token(monkeypatch):
     assert res.fp_checked >= 40 and res.cpu_pairs > 0 and res.fills > 0
 
 
-def test_fused_falls_back_where_it_does_not_apply(monkeypatch):
-    # two tokens per call: the fused launch does not apply and the two grids run
-    monkeypatch.setenv("MOE_DECODE_FUSED", "1")
+@pytest.mark.parametrize("mode", ["stream", "fused"])
+def test_one_token_paths_fall_back_where_they_do_not_apply(monkeypatch, mode):
+    # two tokens per call: neither the stream nor the fused launch applies and the two grids run
+    monkeypatch.delenv("MOE_DECODE_FUSED", raising=False)
+    monkeypatch.setenv("MOE_DECODE_RESIDENT", mode)
     cfg = _qwen3_small(T=2, steps=6, layers=3)
     arena, offs, pool = build_pool(cfg, n_phys=8)
     c, _ = make_cache(cfg, pool, offs, None, (100000, 100000))
@@ -117,3 +138,13 @@ def test_fused_falls_back_where_it_does_not_apply(monkeypatch):
     c.close()
     res = run_decode_parity(cfg, (100000, 100000), n_phys=8, fp_every=3, state_every=3)
     assert not res.mismatches and res.max_err <= TOL
+
+
+def test_bad_resident_mode_is_refused(monkeypatch):
+    from serving_layer_moe_gb300 import MoEError
+    monkeypatch.setenv("MOE_DECODE_RESIDENT", "bogus")
+    cfg = _qwen3_small(T=1, steps=2, layers=2)
+    arena, offs, pool = build_pool(cfg, n_phys=4)
+    with pytest.raises(MoEError) as ei:
+        make_cache(cfg, pool, offs, None, (1000, 0))
+    assert ei.value.status == 1
