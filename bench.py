@@ -88,7 +88,8 @@ def parse_args(argv=None):
     p.add_argument("--no-prefill", action="store_true")
     p.add_argument("--no-nvfp4", action="store_true",
                    help="skip the 4-bit-expert variants (NVFP4, MXFP4) of the decode workload")
-    p.add_argument("--mode", default="all", choices=["all", "decode", "prefill", "profile-decode", "workloads"],
+    p.add_argument("--mode", default="all", choices=["all", "decode", "prefill", "profile-decode", "workloads",
+                                                     "cpu-branch"],
                    help="prefill: only the prefill measurement; workloads: only the tiny, batch-16 and "
                         "DeepSeek-V3 decode workloads")
     p.add_argument("--no-workloads", action="store_true",
@@ -339,18 +340,23 @@ class DecodeRunner:
         self.ib.copy_(self.ids_all[st], non_blocking=True)
         self.wb.copy_(self.w_all[st], non_blocking=True)
 
+    def sync(self):
+        """Wait for the device through the library (its call releases the interpreter lock,
+        which a registered CPU branch's host function takes on a driver thread)."""
+        self.cache.plan()
+
     def capture(self):
         torch = self.torch
-        torch.cuda.synchronize(self.dev)
+        self.sync()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=self.stream):
             self.enqueue()
-        torch.cuda.synchronize(self.dev)
+        self.sync()
         self.graph = g
 
     def _maybe_resize(self):
         if not self.resized and self.step == self.cfg.resize_step:
-            self.torch.cuda.synchronize(self.dev)   # the steps queued so far are not part of the resize
+            self.sync()   # the steps queued so far are not part of the resize
             t0 = time.perf_counter()
             self.cache.resize(self.cfg.resize_to)     # a safe point: synchronises the device
             if self.graph is not None:
@@ -394,12 +400,11 @@ class DecodeRunner:
         """(milliseconds, counter delta) of n steps between two events on the stream."""
         torch = self.torch
         cnt0 = self.cache.state()[3].copy()
-        torch.cuda.synchronize(self.dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(self.stream)
         self.advance(n)
         e1.record(self.stream)
-        torch.cuda.synchronize(self.dev)
+        self.sync()
         return e0.elapsed_time(e1), self.cache.state()[3].copy() - cnt0
 
     def profiled(self, n: int, same_step: bool = False):
@@ -520,6 +525,10 @@ def main(args):
     b_cpu = max(0, int(bh_gbs * 1000) - b_pcie)
     hbm_peak, bf16_peak, bf16_sust, peak_src = measured_peaks()
 
+    if args.mode == "cpu-branch":
+        if rank == 0:
+            print(json.dumps({"cpu_branch": cpu_branch_measure(args, dev)}))
+        return
     if args.mode == "workloads":
         res = {n: decode_workload_measure(n, args, dev, (b_pcie, b_cpu), hbm_peak, peak_src, rank == 0)
                for n in EXTRA_WORKLOADS}
@@ -724,6 +733,53 @@ def main(args):
         print(json.dumps(result))
     if world > 1:
         dist.destroy_process_group()
+
+
+def cpu_branch_measure(args, dev, steps=32):
+    """The CPU branch of the decode step (moe_cache_set_cpu_branch), on the headline
+    shape with B_pcie = B_cpu, so about half the misses go to the CPU: the same
+    trace steps with the CPU partial sums supplied by the caller, then computed
+    by a registered host function from the page-locked copies of x, the ids and
+    the slot map (a host node in the replayed step graph).  The host function
+    here does the least a CPU branch can (it writes zeros for its pairs): the
+    difference is the branch's own cost (the copies, the host node, the combine
+    kernel after both branches) where it does not overlap the GPU path."""
+    import torch
+    cfg = config(WORKLOAD)
+    s = cfg.shape
+    arena, offs = make_pool(s, cfg.seed, n_phys=args.pool_blobs)
+    pool = torch.from_numpy(arena).pin_memory()
+    del arena
+    bw = (100000, 100000)
+    out = {"workload": f"{WORKLOAD} with B_pcie = B_cpu (hybrid: about half the misses to the CPU), "
+                       f"C={cfg.capacity} slots", "steps": steps,
+           "window": f"trace steps [{PREFIX_STEPS}, {PREFIX_STEPS + steps})"}
+    for mode in ("supplied", "branch"):
+        run = DecodeRunner(cfg, pool, offs, None, bw, dev, PREFIX_STEPS + steps + 8)
+        host = {"calls": 0, "s": 0.0, "pairs": 0}
+        if mode == "branch":
+            def fn(layer, T, x, ids, sm, cp, host=host):
+                t0 = time.perf_counter()
+                cpu = sm < 0
+                cp[cpu] = 0.0
+                host["calls"] += 1
+                host["pairs"] += int(cpu.sum())
+                host["s"] += time.perf_counter() - t0
+            run.cache.set_cpu_branch(fn)
+        run.warm(PREFIX_STEPS)
+        host.update(calls=0, s=0.0, pairs=0)
+        ms, dcnt = run.timed(steps)
+        out[mode] = {"value": round(steps * s.L / (ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(ms / steps, 4),
+                     "cpu_assigned": int(dcnt[3]), "fills": int(dcnt[2]),
+                     "kernels_per_layer": int(run.cache.info()[6])}
+        if mode == "branch":
+            out[mode]["host_calls"] = host["calls"]
+            out[mode]["host_pairs"] = host["pairs"]
+            out[mode]["host_us_per_call"] = round(1e6 * host["s"] / max(1, host["calls"]), 2)
+            run.cache.set_cpu_branch(None)
+        run.close()
+    out["branch_cost_us_per_layer"] = round(1e3 * (out["branch"]["ms_per_step"] - out["supplied"]["ms_per_step"]) / s.L, 2)
+    return out
 
 
 # The other decode workloads, measured beside the headline: (untimed prefix, timed

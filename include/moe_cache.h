@@ -169,10 +169,14 @@ moe_status moe_cache_resize(moe_cache* cache, uint64_t n_slots);
  * arrays 4-byte aligned (MOE_EINVAL otherwise, before anything is enqueued).
  * Errors: MOE_EINVAL, MOE_EDEVICE (earlier violation), MOE_ECUDA.
  * The resident experts run as a gate/up grid then a down + combine grid.  With
- * MOE_DECODE_FUSED=1 in the environment when the cache is created, one-token
- * calls on bf16 caches with at most top-8 routed experts and no shared expert
- * run both in one launch with a grid-wide barrier between them instead (same
- * outputs bit for bit).
+ * MOE_DECODE_RESIDENT=fused (or MOE_DECODE_FUSED=1) in the environment when the
+ * cache is created, one-token calls on bf16 caches with at most top-8 routed
+ * experts and no shared expert run both in one launch with a grid-wide barrier
+ * between them instead; with MOE_DECODE_RESIDENT=stream, one-token bf16 calls
+ * without a shared expert run them as one launch streaming gate/up rows and
+ * W_down row blocks as one expert-major item list (same outputs bit for bit).
+ * With a CPU branch registered (moe_cache_set_cpu_branch) cpu_part_dev is
+ * ignored.
  */
 moe_status moe_layer_decode(moe_cache* cache, int32_t layer, int32_t T, const void* x_dev,
                             const int32_t* topk_ids_dev, const float* topk_w_dev,
@@ -239,9 +243,11 @@ moe_status moe_cache_get_plan(moe_cache* cache, int32_t* scalars_host, int32_t* 
 /*
  * Sizes of a cache: info_host[8] uint64: slot bytes S, slots C, K, L*E,
  * device bytes held, host pool bytes, kernel launches of one decode call of
- * max_tokens tokens, and how such a call runs its resident experts: 0 = a
- * gate/up grid then a down + combine grid, 1 = one launch with a grid-wide
- * barrier between gate/up and down + combine.
+ * max_tokens tokens (with a CPU branch registered: its combine kernel
+ * included), and how such a call runs its resident experts: 0 = a gate/up grid
+ * then a down + combine grid, 1 = one launch with a grid-wide barrier between
+ * gate/up and down + combine, 2 = one launch streaming gate/up and down rows as
+ * one expert-major item list.
  */
 moe_status moe_cache_info(moe_cache* cache, uint64_t* info_host);
 
@@ -316,6 +322,41 @@ moe_status moe_layer_ffn_noalloc(int32_t n_experts, int32_t hidden, int32_t inte
                                  int32_t wdtype, int32_t adtype, const void* experts_dev, int32_t T,
                                  const void* x_dev, const int32_t* topk_ids_dev, const float* topk_w_dev,
                                  float* out_dev, void* stream);
+
+/*
+ * The CPU branch of the decode step.  The CPU-assigned experts run on the host,
+ * started from a host-function node of the same captured graph, between a copy
+ * to the host of what they read and a copy back of their partial sums; the GPU
+ * path runs beside them and the exact merge waits for both, so a layer costs the
+ * longer of the two branches.  (ai.thesatyajit.com "FreeToken: a 753B model on
+ * one GPU ...", section "Residency that follows the router", last paragraph;
+ * snackonai "FreeToken, or why your laptop was never the bottleneck", section
+ * "It In Action".)  The library has no CPU expert executor of its own: the
+ * caller registers the function that computes the CPU-assigned pairs.
+ *
+ * With fn registered, every moe_layer_decode call on the cache enqueues, after
+ * its control kernel and on a stream of the library: copies of x, the routed
+ * ids and the slot map into page-locked memory the library owns; a host
+ * function (cudaLaunchHostFunc) that calls
+ *   fn(user, layer, T, x_host [T, H] in adtype, topk_ids_host [T, k] int32,
+ *      slot_map_host [T, k] int32, cpu_part_host [T, k, H] fp32)
+ * which must write cpu_part_host[t, j, :], the unweighted output of expert
+ * topk_ids[t, j] applied to x[t], wherever slot_map_host[t, j] < 0 (other
+ * entries are not read); then a copy of cpu_part_host to device memory the
+ * library owns.  The down kernels of the call only store the GPU pairs'
+ * outputs; one combine kernel on the caller's stream waits for both branches
+ * and forms out in top-k order.  The call's cpu_part_dev argument is ignored.
+ * fn runs on a CUDA driver thread, must not call CUDA, and must not wait on
+ * anything that waits on the stream; the pointers it gets are valid only
+ * during the call.  Everything is stream-ordered and capturable in a CUDA
+ * graph (the host function becomes a host node; a graph captured before fn is
+ * registered again must be captured again).  fn NULL removes the branch.
+ * Synchronises the device.  Errors: MOE_EINVAL (NULL cache), MOE_ENOMEM.
+ */
+typedef void (*moe_cpu_branch_fn)(void* user, int32_t layer, int32_t T, const void* x_host,
+                                  const int32_t* topk_ids_host, const int32_t* slot_map_host,
+                                  float* cpu_part_host);
+moe_status moe_cache_set_cpu_branch(moe_cache* cache, moe_cpu_branch_fn fn, void* user);
 
 /* The message of the last failed call on this thread ("" if none). */
 const char* moe_last_error(void);

@@ -22,8 +22,13 @@ STATUS = {0: "MOE_OK", 1: "MOE_EINVAL", 2: "MOE_ENOMEM", 3: "MOE_ECUDA", 4: "MOE
 # exported symbols of include/moe_cache.h
 SYMBOLS = ("moe_cache_create", "moe_cache_destroy", "moe_cache_resize", "moe_layer_decode",
            "moe_layer_prefill", "moe_cache_get_state", "moe_cache_get_plan", "moe_cache_info",
-           "moe_cache_profile", "moe_cache_set_prefill_prefetch", "bench_bw", "moe_layer_ffn_noalloc",
-           "moe_last_error")
+           "moe_cache_profile", "moe_cache_set_prefill_prefetch", "moe_cache_set_cpu_branch", "bench_bw",
+           "moe_layer_ffn_noalloc", "moe_last_error")
+
+# moe_cpu_branch_fn: (user, layer, T, x_host, topk_ids_host, slot_map_host, cpu_part_host)
+CPU_BRANCH_FN = ctypes.CFUNCTYPE(None, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                                 ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
+                                 ctypes.POINTER(ctypes.c_float))
 
 
 class MoEConfigC(ctypes.Structure):
@@ -63,6 +68,7 @@ def load_library():
     lib.moe_cache_info.argtypes = [P, P]
     lib.moe_cache_profile.argtypes = [P, I32, P, P]
     lib.moe_cache_set_prefill_prefetch.argtypes = [P, I32]
+    lib.moe_cache_set_cpu_branch.argtypes = [P, CPU_BRANCH_FN, P]
     lib.bench_bw.argtypes = [I32, U64, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
                              ctypes.POINTER(I32)]
     lib.moe_layer_ffn_noalloc.argtypes = [I32, I32, I32, I32, I32, I32, P, I32, P, P, P, P, P]
@@ -121,6 +127,7 @@ class MoECache:
                                     int(n_slots), ctypes.byref(handle)))
         self._h = handle
         self.L, self.E, self.H, self.I, self.k = L, E, H, I, top_k
+        self._adtype = DTYPES.get(adtype, adtype)
         info = self.info()
         self.S, self.C, self.K = int(info[0]), int(info[1]), int(info[2])
 
@@ -165,6 +172,34 @@ class MoECache:
     def set_prefill_prefetch(self, on: bool):
         """The second prefill buffer (the next layer loads during this one's GEMMs) on or off."""
         _check(load_library().moe_cache_set_prefill_prefetch(self._h, 1 if on else 0))
+
+    def set_cpu_branch(self, fn):
+        """Register fn(layer, T, x, topk_ids, slot_map, cpu_part) as the CPU branch of every
+        decode call (None removes it).  The library calls it from a CUDA host node with
+        numpy views of its page-locked staging: x [T, H] (uint16 bf16 bits or float32),
+        topk_ids and slot_map [T, k] int32, and cpu_part [T, k, H] float32, which fn fills
+        wherever slot_map < 0.  It runs on a driver thread: wait for a decode call through
+        this library (state(), which releases the interpreter lock), not through calls that
+        hold the lock while the stream drains."""
+        lib = load_library()
+        if fn is None:
+            _check(lib.moe_cache_set_cpu_branch(self._h, CPU_BRANCH_FN(), None))
+            self._cpu_cb = None
+            return
+        H, k = self.H, self.k
+        xdt = np.float32 if self._adtype == MOE_F32 else np.uint16
+
+        def trampoline(_user, layer, T, x_ptr, ids_ptr, sm_ptr, cp_ptr):
+            x = np.ctypeslib.as_array(ctypes.cast(x_ptr, ctypes.POINTER(
+                ctypes.c_float if xdt is np.float32 else ctypes.c_uint16)), shape=(T, H))
+            ids = np.ctypeslib.as_array(ids_ptr, shape=(T, k))
+            sm = np.ctypeslib.as_array(sm_ptr, shape=(T, k))
+            cp = np.ctypeslib.as_array(cp_ptr, shape=(T, k, H))
+            fn(int(layer), int(T), x, ids, sm, cp)
+
+        cb = CPU_BRANCH_FN(trampoline)
+        _check(lib.moe_cache_set_cpu_branch(self._h, cb, None))
+        self._cpu_cb = cb   # the library holds the pointer: keep the callback alive
 
     def resize(self, n_slots):
         _check(load_library().moe_cache_resize(self._h, int(n_slots)))

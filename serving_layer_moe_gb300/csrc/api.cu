@@ -55,6 +55,28 @@ moe_status fail(moe_status st, const char* fmt, ...) {
 
 #include <cstdlib>
 
+static thread_local int g_inject_at = 0;      // the allocation that fails (0: none)
+static thread_local int g_alloc_seen = 0;     // allocations so far in this create / resize call
+
+void alloc_injection_begin() {
+  const char* e = getenv("MOE_INJECT_ALLOC_FAILURE");
+  g_inject_at = e ? atoi(e) : 0;
+  g_alloc_seen = 0;
+}
+static bool injected_failure() { return g_inject_at > 0 && ++g_alloc_seen == g_inject_at; }
+cudaError_t moe_malloc(void** p, size_t bytes) {
+  if (injected_failure()) return cudaErrorMemoryAllocation;
+  return cudaMalloc(p, bytes);
+}
+cudaError_t moe_host_alloc(void** p, size_t bytes, unsigned flags) {
+  if (injected_failure()) return cudaErrorMemoryAllocation;
+  return cudaHostAlloc(p, bytes, flags);
+}
+cudaError_t moe_host_register(void* p, size_t bytes, unsigned flags) {
+  if (injected_failure()) return cudaErrorMemoryAllocation;
+  return cudaHostRegister(p, bytes, flags);
+}
+
 static moe_status check_err_word(moe_cache* c) {
   const uint32_t e = *reinterpret_cast<volatile uint32_t*>(c->err_host);
   if (e == 0) return MOE_OK;
@@ -67,11 +89,26 @@ static moe_status check_err_word(moe_cache* c) {
               (e & kErrTimeout) ? "device wait timed out; " : "");
 }
 
+static void free_cpu_branch(moe_cache* c) {
+  if (c->ev_cpu) cudaEventDestroy(c->ev_cpu);
+  if (c->cpu_stream) cudaStreamDestroy(c->cpu_stream);
+  if (c->cpu_x_host) cudaFreeHost(c->cpu_x_host);
+  if (c->cpu_ids_host) cudaFreeHost(c->cpu_ids_host);
+  if (c->cpu_sm_host) cudaFreeHost(c->cpu_sm_host);
+  if (c->cpu_part_host) cudaFreeHost(c->cpu_part_host);
+  cudaFree(c->cpu_part_dev);
+  c->ev_cpu = nullptr; c->cpu_stream = nullptr; c->cpu_x_host = nullptr; c->cpu_ids_host = nullptr;
+  c->cpu_sm_host = nullptr; c->cpu_part_host = nullptr; c->cpu_part_dev = nullptr;
+  c->cpu_fn = nullptr; c->cpu_user = nullptr;
+  c->cpu_calls.clear();
+}
+
 static void destroy_impl(moe_cache* c) {
   if (!c) return;
   DeviceGuard g(c->cfg.device);
   cudaDeviceSynchronize();
   moe::prefill_free(c);
+  free_cpu_branch(c);
   if (c->ev_ctrl) cudaEventDestroy(c->ev_ctrl);
   if (c->ev_fill) cudaEventDestroy(c->ev_fill);
   if (c->fill_stream) cudaStreamDestroy(c->fill_stream);
@@ -95,8 +132,8 @@ static bool valid_dtype(int d) { return d == MOE_F32 || d == MOE_BF16 || d == MO
 
 static moe_status alloc_tables(moe_cache* c, uint64_t C) {
   const uint64_t nflat = (uint64_t)c->sh.L * c->sh.E;
-  CK(cudaMalloc(&c->tab.s2e, C * sizeof(int32_t)));
-  CK(cudaMalloc(&c->tab.stamp, C * sizeof(uint64_t)));
+  CK(moe_malloc(&c->tab.s2e, C * sizeof(int32_t)));
+  CK(moe_malloc(&c->tab.stamp, C * sizeof(uint64_t)));
   CK(cudaMemset(c->tab.s2e, 0xff, C * sizeof(int32_t)));
   CK(cudaMemset(c->tab.stamp, 0, C * sizeof(uint64_t)));
   (void)nflat;
@@ -108,6 +145,7 @@ extern "C" moe_status moe_cache_create(const moe_config* cfg, const void* host_p
                                        moe_cache** out) {
   if (!cfg || !out) return fail(MOE_EINVAL, "cfg and out must not be NULL");
   *out = nullptr;
+  alloc_injection_begin();
   const moe_config& k = *cfg;
   if (k.n_layers < 1 || k.n_experts < 1 || k.n_experts > kMaxExperts)
     return fail(MOE_EINVAL, "need 1 <= L and 1 <= E <= %d", kMaxExperts);
@@ -173,14 +211,15 @@ extern "C" moe_status moe_cache_create(const moe_config* cfg, const void* host_p
   c->gemv_grid = 2 * c->sms;
   c->fill_ctas = c->sms / 2;
   {
-    // One-token calls run their resident experts as one expert-major stream of
-    // gate/up and down items (the default), or, chosen by MOE_DECODE_RESIDENT when
-    // the cache is created: "grids" = a gate/up grid then a down + combine grid,
-    // "fused" = one launch with a grid-wide barrier between the two (also
-    // MOE_DECODE_FUSED=1).  All three give the same outputs bit for bit.
+    // The resident experts of a decode call run as a gate/up grid then a down +
+    // combine grid (the default, "grids"), or, for one-token calls, chosen by
+    // MOE_DECODE_RESIDENT when the cache is created: "fused" = one launch with a
+    // grid-wide barrier between the two (also MOE_DECODE_FUSED=1), "stream" = one
+    // launch streaming gate/up and down rows as one expert-major item list.  All
+    // three give the same outputs bit for bit.
     const char* er = getenv("MOE_DECODE_RESIDENT");
     const char* ef = getenv("MOE_DECODE_FUSED");
-    c->resident_mode = 2;
+    c->resident_mode = 0;
     if (ef && ef[0] == '1') c->resident_mode = 1;
     if (er && strcmp(er, "grids") == 0) c->resident_mode = 0;
     else if (er && strcmp(er, "fused") == 0) c->resident_mode = 1;
@@ -195,9 +234,9 @@ extern "C" moe_status moe_cache_create(const moe_config* cfg, const void* host_p
   cudaError_t ae = cudaPointerGetAttributes(&attr, host_pool);
   if (ae != cudaSuccess) cudaGetLastError();
   if (ae != cudaSuccess || attr.type != cudaMemoryTypeHost) {
-    cudaError_t re = cudaHostRegister(const_cast<void*>(host_pool), host_pool_bytes,
-                                      cudaHostRegisterMapped | cudaHostRegisterReadOnly);
-    if (re != cudaSuccess) {
+    cudaError_t re = moe_host_register(const_cast<void*>(host_pool), host_pool_bytes,
+                                       cudaHostRegisterMapped | cudaHostRegisterReadOnly);
+    if (re != cudaSuccess && re != cudaErrorMemoryAllocation) {   // read-only mapping refused: plain mapped
       cudaGetLastError();
       re = cudaHostRegister(const_cast<void*>(host_pool), host_pool_bytes, cudaHostRegisterMapped);
     }
@@ -220,20 +259,20 @@ extern "C" moe_status moe_cache_create(const moe_config* cfg, const void* host_p
 
   CKB(setup_control_kernels());
   CKB(setup_gemv_kernels());
-  CKB(cudaMalloc(&c->offsets, nflat * sizeof(uint64_t)));
+  CKB(moe_malloc(&c->offsets, nflat * sizeof(uint64_t)));
   CKB(cudaMemcpy(c->offsets, offs.data(), nflat * sizeof(uint64_t), cudaMemcpyHostToDevice));
-  CKB(cudaMalloc(&c->slots, c->C * S));
-  CKB(cudaMalloc(&c->tab.e2s, nflat * sizeof(int32_t)));
+  CKB(moe_malloc(&c->slots, c->C * S));
+  CKB(moe_malloc(&c->tab.e2s, nflat * sizeof(int32_t)));
   CKB(cudaMemset(c->tab.e2s, 0xff, nflat * sizeof(int32_t)));
   if ((st = alloc_tables(c, c->C)) != MOE_OK) return bail(st);
-  CKB(cudaMalloc(&c->tab.clock, sizeof(uint64_t)));
+  CKB(moe_malloc(&c->tab.clock, sizeof(uint64_t)));
   CKB(cudaMemset(c->tab.clock, 0, sizeof(uint64_t)));
-  CKB(cudaMalloc(&c->tab.counters, 8 * sizeof(uint64_t)));
+  CKB(moe_malloc(&c->tab.counters, 8 * sizeof(uint64_t)));
   CKB(cudaMemset(c->tab.counters, 0, 8 * sizeof(uint64_t)));
-  CKB(cudaMalloc(&c->tab.pool, (kPoolN + 1) * sizeof(uint64_t)));
+  CKB(moe_malloc(&c->tab.pool, (kPoolN + 1) * sizeof(uint64_t)));
   CKB(cudaMemset(c->tab.pool, 0, (kPoolN + 1) * sizeof(uint64_t)));   // count 0: rebuilt at the first call
   if (k.n_shared) {
-    CKB(cudaMalloc(&c->shared, (uint64_t)k.n_layers * S));
+    CKB(moe_malloc(&c->shared, (uint64_t)k.n_layers * S));
     CKB(cudaMemcpy(c->shared, shared_host, (uint64_t)k.n_layers * S, cudaMemcpyHostToDevice));
   }
   // work buffers
@@ -248,9 +287,10 @@ extern "C" moe_status moe_cache_create(const moe_config* cfg, const void* host_p
                  o_sm = take((size_t)k.max_tokens * k.top_k * 4), o_goff = take((size_t)(max_gpu + 1) * 4),
                  o_gp = take(max_pairs * 4), o_gw = take((size_t)max_gpu * 8),
                  o_h = take(max_pairs * k.inter * 4), o_y = take(max_pairs * k.hidden * 4),
-                 o_arr = take((size_t)k.hidden * 4), o_fb = take(8),
-                 o_sc = take((size_t)(max_gpu + k.hidden) * 4);
-    CKB(cudaMalloc(&c->work, off));
+                 o_arr = take((size_t)k.hidden * 4), o_fb = take(8), o_seq = take(4),
+                 o_hs2 = take(2 * (size_t)max_gpu * k.inter * 4), o_ys2 = take(2 * (size_t)k.top_k * k.hidden * 4),
+                 o_ns = take(4);
+    CKB(moe_malloc(&c->work, off));
     CKB(cudaMemset(c->work, 0, off));
     uint8_t* w = static_cast<uint8_t*>(c->work);
     c->b.plan = reinterpret_cast<int32_t*>(w + o_plan);
@@ -265,13 +305,28 @@ extern "C" moe_status moe_cache_create(const moe_config* cfg, const void* host_p
     c->b.y = reinterpret_cast<float*>(w + o_y);
     c->b.arrive = reinterpret_cast<uint32_t*>(w + o_arr);
     c->b.fused_bar = reinterpret_cast<unsigned long long*>(w + o_fb);
-    c->b.scnt = reinterpret_cast<uint32_t*>(w + o_sc);
-    // one-token calls are the only ones the stream kernel takes
-    c->b.n_scnt = c->resident_mode == 2 ? resident_stream_counters(c->sh, 1, c->sms) : 0;
+    c->b.sseq = reinterpret_cast<uint32_t*>(w + o_seq);
+    c->b.hs2 = reinterpret_cast<float*>(w + o_hs2);
+    c->b.ys2 = reinterpret_cast<float*>(w + o_ys2);
+    // one-token calls are the only ones the stream kernel takes; its h and y
+    // buffers start empty
+    c->b.stream = resident_path(c, 1) == 2 ? 1 : 0;
+    CKB(cudaMemset(w + o_hs2, 0xff, 2 * (size_t)max_gpu * k.inter * 4));
+    CKB(cudaMemset(w + o_ys2, 0xff, 2 * (size_t)k.top_k * k.hidden * 4));
+    // A test of the bounded waits (MOE_TEST_UNSET_WAIT=1 when the cache is created):
+    // the resident experts' down kernel (or the stream kernel's block-finishing
+    // warps) also waits for a word nothing writes, gives up after 20 ms, flags the
+    // timeout and returns; the next call reports MOE_EDEVICE.  Off unless set.
+    CKB(cudaMemset(w + o_ns, 0xff, 4));
+    c->b.never_set = reinterpret_cast<const float*>(w + o_ns);
+    {
+      const char* tw = getenv("MOE_TEST_UNSET_WAIT");
+      c->b.test_wait = (tw && tw[0] == '1') ? 1 : 0;
+    }
     c->dev_bytes = off;
   }
   c->dev_bytes += c->C * S + nflat * 12 + c->C * 12 + (k.n_shared ? (uint64_t)k.n_layers * S : 0);
-  CKB(cudaHostAlloc(&c->err_host, sizeof(uint32_t), cudaHostAllocMapped));
+  CKB(moe_host_alloc(reinterpret_cast<void**>(&c->err_host), sizeof(uint32_t), cudaHostAllocMapped));
   *c->err_host = 0;
   CKB(cudaHostGetDevicePointer(reinterpret_cast<void**>(&c->err_dev), c->err_host, 0));
   {
@@ -294,6 +349,54 @@ extern "C" moe_status moe_cache_create(const moe_config* cfg, const void* host_p
 
 extern "C" moe_status moe_cache_destroy(moe_cache* c) {
   destroy_impl(c);
+  return MOE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// CPU branch
+// ---------------------------------------------------------------------------
+// The host node of a decode call's CPU branch (runs on a CUDA driver thread).
+static void CUDART_CB cpu_branch_host(void* p) {
+  const moe_cache::CpuCall* a = static_cast<const moe_cache::CpuCall*>(p);
+  moe_cache* c = a->c;
+  c->cpu_fn(c->cpu_user, a->layer, a->T, c->cpu_x_host, c->cpu_ids_host, c->cpu_sm_host, c->cpu_part_host);
+}
+
+// The exact merge once both branches are done: y of the GPU pairs, the CPU
+// branch's partial sums, top-k order (+ shared expert).
+static moe_status combine_after_cpu_branch(moe_cache* c, int T, const float* w, float* out, cudaStream_t s) {
+  CK(cudaStreamWaitEvent(s, c->ev_cpu, 0));
+  ProfScope p(c, s, PROF_DOWN_COMBINE);
+  CK(launch_combine(c->sh, T, w, c->cpu_part_dev, c->b, out, c->err_dev, s));
+  return MOE_OK;
+}
+
+extern "C" moe_status moe_cache_set_cpu_branch(moe_cache* c, moe_cpu_branch_fn fn, void* user) {
+  if (!c) return fail(MOE_EINVAL, "cache is NULL");
+  DeviceGuard guard(c->cfg.device);
+  CK(cudaDeviceSynchronize());
+  free_cpu_branch(c);
+  if (!fn) return MOE_OK;
+  const size_t T = (size_t)c->cfg.max_tokens, k = (size_t)c->sh.k, H = (size_t)c->sh.H;
+  const size_t xb = T * H * (c->sh.adtype == MOE_F32 ? 4 : 2);
+  cudaError_t e = cudaHostAlloc(reinterpret_cast<void**>(&c->cpu_x_host), xb, cudaHostAllocDefault);
+  if (e == cudaSuccess) e = cudaHostAlloc(reinterpret_cast<void**>(&c->cpu_ids_host), T * k * 4, cudaHostAllocDefault);
+  if (e == cudaSuccess) e = cudaHostAlloc(reinterpret_cast<void**>(&c->cpu_sm_host), T * k * 4, cudaHostAllocDefault);
+  if (e == cudaSuccess) e = cudaHostAlloc(reinterpret_cast<void**>(&c->cpu_part_host), T * k * H * 4, cudaHostAllocDefault);
+  if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&c->cpu_part_dev), T * k * H * 4);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->cpu_stream, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->ev_cpu, cudaEventDisableTiming);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    free_cpu_branch(c);
+    return fail(e == cudaErrorMemoryAllocation ? MOE_ENOMEM : MOE_ECUDA, "CPU branch set-up: %s", cudaGetErrorString(e));
+  }
+  memset(c->cpu_part_host, 0, T * k * H * 4);
+  c->cpu_calls.resize((size_t)c->sh.L * T);
+  for (int l = 0; l < c->sh.L; ++l)
+    for (size_t t = 0; t < T; ++t) c->cpu_calls[(size_t)l * T + t] = {c, l, (int)t + 1};
+  c->cpu_fn = fn;
+  c->cpu_user = user;
   return MOE_OK;
 }
 
@@ -325,17 +428,36 @@ extern "C" moe_status moe_layer_decode(moe_cache* c, int32_t layer, int32_t T, c
   c->last_T = T;
   const bool split = down_split_ok(c->sh, T, c->sms);
   const int path = resident_path(c, T);
+  // with a CPU branch the down kernels only store y; one combine kernel follows both branches
+  const bool branch = c->cpu_fn != nullptr;
+  DecodeBufs b = c->b;
+  b.defer_combine = branch ? 1 : 0;
+  if (branch) cpu_part = nullptr;
   {
     ProfScope p(c, s, PROF_CONTROL);
     CK(launch_decode_control(c->sh, layer, T, (int)c->C, c->K, c->cfg.bw_pcie_mbps, c->cfg.bw_cpu_mbps, ids,
-                             c->tab, c->b, slot_map, c->slots, c->shared, c->err_dev, s));
+                             c->tab, b, slot_map, c->slots, c->shared, c->err_dev, s));
   }
   CK(cudaEventRecord(c->ev_ctrl, s));
   CK(cudaStreamWaitEvent(c->fill_stream, c->ev_ctrl, 0));
+  if (branch) {
+    // The CPU branch: what the CPU-assigned experts read goes to the host, the
+    // registered function computes their partial sums, and those come back
+    const size_t kT = (size_t)T * c->sh.k;
+    const size_t xb = (size_t)T * c->sh.H * (c->sh.adtype == MOE_F32 ? 4 : 2);
+    CK(cudaStreamWaitEvent(c->cpu_stream, c->ev_ctrl, 0));
+    CK(cudaMemcpyAsync(c->cpu_x_host, x, xb, cudaMemcpyDeviceToHost, c->cpu_stream));
+    CK(cudaMemcpyAsync(c->cpu_ids_host, ids, kT * 4, cudaMemcpyDeviceToHost, c->cpu_stream));
+    CK(cudaMemcpyAsync(c->cpu_sm_host, c->b.slot_map, kT * 4, cudaMemcpyDeviceToHost, c->cpu_stream));
+    CK(cudaLaunchHostFunc(c->cpu_stream, cpu_branch_host,
+                          &c->cpu_calls[(size_t)layer * c->cfg.max_tokens + (T - 1)]));
+    CK(cudaMemcpyAsync(c->cpu_part_dev, c->cpu_part_host, kT * c->sh.H * 4, cudaMemcpyHostToDevice, c->cpu_stream));
+    CK(cudaEventRecord(c->ev_cpu, c->cpu_stream));
+  }
   {
     // fills, and the gate/up GEMV of the filled experts on the way through
     ProfScope p(c, c->fill_stream, PROF_FILL);
-    CK(launch_fill_gate_up(c->sh, T, x, c->b, c->host_pool_dev, c->offsets, c->slots, c->fill_ctas, c->fill_stream));
+    CK(launch_fill_gate_up(c->sh, T, x, b, c->host_pool_dev, c->offsets, c->slots, c->fill_ctas, c->fill_stream));
   }
   if (split) {
     // Beside a resident launch whose warps wait on one another (the fused launch's
@@ -343,7 +465,7 @@ extern "C" moe_status moe_layer_decode(moe_cache* c, int32_t layer, int32_t T, c
     // plain launch: launched early, its CTAs would sit on SMs for the whole fill
     // and could keep some of that launch's CTAs off the GPU.
     ProfScope p(c, c->fill_stream, PROF_DOWN_FILLED);
-    CK(launch_down_split(c->sh, 1, T, w, cpu_part, c->b, out, c->err_dev, c->sms, c->fill_stream, path == 0));
+    CK(launch_down_split(c->sh, 1, T, w, cpu_part, b, out, c->err_dev, c->sms, c->fill_stream, path == 0));
   }
   CK(cudaEventRecord(c->ev_fill, c->fill_stream));
   if (split) {
@@ -351,27 +473,27 @@ extern "C" moe_status moe_layer_decode(moe_cache* c, int32_t layer, int32_t T, c
       // one timed group: the two grids run back to back under a programmatic dependency
       ProfScope p(c, s, PROF_GEMV_RESIDENT);
       if (path == 2) {
-        CK(launch_resident_stream(c->sh, T, x, w, cpu_part, c->b, out, c->err_dev, c->sms, s));
+        CK(launch_resident_stream(c->sh, T, x, w, cpu_part, b, out, c->err_dev, c->sms, s));
       } else if (path == 1) {
-        CK(launch_resident_fused(c->sh, T, x, w, cpu_part, c->b, out, c->err_dev, c->sms, s));
+        CK(launch_resident_fused(c->sh, T, x, w, cpu_part, b, out, c->err_dev, c->sms, s));
       } else {
-        CK(launch_gate_up(c->sh, 0, T, x, c->b, c->sms, s, c->err_dev));
-        CK(launch_down_split(c->sh, 0, T, w, cpu_part, c->b, out, c->err_dev, c->sms, s));
+        CK(launch_gate_up(c->sh, 0, T, x, b, c->sms, s, c->err_dev));
+        CK(launch_down_split(c->sh, 0, T, w, cpu_part, b, out, c->err_dev, c->sms, s));
       }
     }
     CK(cudaStreamWaitEvent(s, c->ev_fill, 0));
-    return MOE_OK;
+    return branch ? combine_after_cpu_branch(c, T, w, out, s) : MOE_OK;
   }
   {
     ProfScope p(c, s, PROF_GEMV_RESIDENT);
-    CK(launch_gate_up(c->sh, 0, T, x, c->b, c->sms, s, c->err_dev));
+    CK(launch_gate_up(c->sh, 0, T, x, b, c->sms, s, c->err_dev));
   }
   CK(cudaStreamWaitEvent(s, c->ev_fill, 0));
   {
     ProfScope p(c, s, PROF_DOWN_COMBINE);
-    CK(launch_down_combine(c->sh, T, w, cpu_part, c->b, out, c->err_dev, c->sms, s));
+    CK(launch_down_combine(c->sh, T, w, cpu_part, b, out, c->err_dev, c->sms, s));
   }
-  return MOE_OK;
+  return branch ? combine_after_cpu_branch(c, T, w, out, s) : MOE_OK;
 }
 
 // ---------------------------------------------------------------------------
@@ -423,6 +545,7 @@ extern "C" moe_status moe_cache_info(moe_cache* c, uint64_t* info) {
       info[6] = resident_path(c, T) != 0 ? 4 : 5;
     else
       info[6] = 3 + (uint64_t)down_combine_launches(c->sh, T, c->sms);
+    if (c->cpu_fn) info[6] += 1;   // the combine kernel after the CPU branch
   }
   return MOE_OK;
 }
@@ -442,10 +565,11 @@ extern "C" moe_status moe_cache_resize(moe_cache* c, uint64_t n_slots) {
   int32_t *new_s2e = nullptr, *new2old = nullptr;
   uint64_t* new_stamp = nullptr;
   auto cleanup = [&]() { cudaFree(new_slots); cudaFree(new_s2e); cudaFree(new2old); cudaFree(new_stamp); };
-  cudaError_t e = cudaMalloc(&new_slots, n_slots * S);
-  if (e == cudaSuccess) e = cudaMalloc(&new_s2e, n_slots * 4);
-  if (e == cudaSuccess) e = cudaMalloc(&new_stamp, n_slots * 8);
-  if (e == cudaSuccess) e = cudaMalloc(&new2old, (n_slots + 1) * 4);
+  alloc_injection_begin();
+  cudaError_t e = moe_malloc(&new_slots, n_slots * S);
+  if (e == cudaSuccess) e = moe_malloc(&new_s2e, n_slots * 4);
+  if (e == cudaSuccess) e = moe_malloc(&new_stamp, n_slots * 8);
+  if (e == cudaSuccess) e = moe_malloc(&new2old, (n_slots + 1) * 4);
   if (e != cudaSuccess) {
     cudaGetLastError();
     cleanup();

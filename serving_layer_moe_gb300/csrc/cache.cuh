@@ -10,6 +10,19 @@
 // set the thread's last error message and return `st`
 moe_status fail(moe_status st, const char* fmt, ...);
 
+// Host-side fault injection for tests.  With MOE_INJECT_ALLOC_FAILURE=n in the
+// environment, the n-th device or page-locked allocation (or host-pool
+// registration) of one moe_cache_create or moe_cache_resize call reports out of
+// memory instead of allocating (n >= 1; unset or 0: off).  The count starts over
+// at each such call.  Every allocation of those calls goes through these.
+void alloc_injection_begin();
+cudaError_t moe_malloc(void** p, size_t bytes);
+cudaError_t moe_host_alloc(void** p, size_t bytes, unsigned flags);
+cudaError_t moe_host_register(void* p, size_t bytes, unsigned flags);
+template <typename T> cudaError_t moe_malloc(T** p, size_t bytes) {
+  return moe_malloc(reinterpret_cast<void**>(p), bytes);
+}
+
 #define CK(call)                                                                      \
   do {                                                                                \
     cudaError_t e_ = (call);                                                          \
@@ -45,7 +58,7 @@ struct moe_cache {
   int fill_ctas = 0;
   // how one-token calls run their resident experts: 0 a gate/up grid then a down +
   // combine grid, 1 one launch with a grid-wide barrier, 2 one expert-major stream
-  int resident_mode = 2;
+  int resident_mode = 0;
   // host pool
   const uint8_t* host_pool = nullptr;
   const uint8_t* host_pool_dev = nullptr;
@@ -66,6 +79,20 @@ struct moe_cache {
   // streams / events
   cudaStream_t fill_stream = nullptr;
   cudaEvent_t ev_ctrl = nullptr, ev_fill = nullptr;
+  // CPU branch (moe_cache_set_cpu_branch): the registered function, its stream and
+  // event, page-locked staging of what it reads and writes, the device copy of its
+  // partial sums, and one host-node argument per (layer, T)
+  struct CpuCall { moe_cache* c; int layer, T; };
+  moe_cpu_branch_fn cpu_fn = nullptr;
+  void* cpu_user = nullptr;
+  cudaStream_t cpu_stream = nullptr;
+  cudaEvent_t ev_cpu = nullptr;
+  uint8_t* cpu_x_host = nullptr;
+  int32_t* cpu_ids_host = nullptr;
+  int32_t* cpu_sm_host = nullptr;
+  float* cpu_part_host = nullptr;
+  float* cpu_part_dev = nullptr;
+  std::vector<CpuCall> cpu_calls;
   // prefill state (prefill.cu)
   void* prefill = nullptr;
   // kernel timing (moe_cache_profile)

@@ -95,6 +95,16 @@ __device__ __forceinline__ unsigned long long key_of_fast(const CtrlArgs& a, con
   return a.cache_keys ? rawkey[s] : (((unsigned long long)a.tab.stamp[s] << kSlotBits) | (unsigned long long)s);
 }
 
+// This call's launch number of the resident stream kernel (one thread; the
+// control kernels of a cache run one after another), or 0 when the call does not
+// run it.  Its parity picks the stream kernel's h / y buffers.
+__device__ __forceinline__ int32_t stream_seq(const CtrlArgs& a) {
+  if (!a.b.stream || a.T != 1) return 0;
+  const uint32_t n = *a.b.sseq + 1u;
+  *a.b.sseq = n;
+  return (int32_t)(n & 0x7fffffffu);
+}
+
 // shared scalars of the control CTA
 struct CtrlScalars {
   int bad, u, h, m, q, keff, ncand, digit, kth, read_hits, read_misses, pool_n, enough;
@@ -159,9 +169,6 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
   }
   pdl_wait();       // the routed ids may come from the preceding kernel
   pdl_trigger();
-  // the resident stream kernel's counters start each call at zero (its previous
-  // launch has completed: it precedes this kernel in the stream)
-  for (int i = tid; i < a.b.n_scnt; i += nt) a.b.scnt[i] = 0u;
   if (kSel == 2 && P + a.n_shared <= 32 && NW <= 32) {
     // ---- one warp for calls of at most 32 routed pairs ---------------------------
     // The steps below for a handful of pairs, in warp 0 with ballots and warp
@@ -304,6 +311,7 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
         int32_t* pl = a.b.plan;
         pl[P_LAYER] = a.layer; pl[P_U] = u; pl[P_H] = h; pl[P_M] = m; pl[P_Q] = q;
         pl[P_NCPU] = m - q; pl[P_NGPU] = ngpu; pl[P_NFIRST] = nfirst;
+        pl[P_SEQ] = stream_seq(a);
         unsigned long long* cn = reinterpret_cast<unsigned long long*>(a.tab.counters);
         atomicAdd(cn + 0, (unsigned long long)h);
         atomicAdd(cn + 1, (unsigned long long)m);
@@ -673,6 +681,7 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
     int32_t* pl = a.b.plan;
     pl[P_LAYER] = a.layer; pl[P_U] = u; pl[P_H] = h; pl[P_M] = m; pl[P_Q] = q;
     pl[P_NCPU] = m - q; pl[P_NGPU] = ngpu; pl[P_NFIRST] = nfirst;
+    pl[P_SEQ] = stream_seq(a);
     // reductions, not read-modify-writes: nothing waits for the old values
     unsigned long long* c = reinterpret_cast<unsigned long long*>(a.tab.counters);
     atomicAdd(c + 0, (unsigned long long)h); atomicAdd(c + 1, (unsigned long long)m);

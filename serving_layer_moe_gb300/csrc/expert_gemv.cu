@@ -748,7 +748,7 @@ __global__ void __launch_bounds__(kDCWarps * 32) down_combine_kernel(GemvArgs a,
       }
     }
     __syncwarp();
-    for (int t = lane; t < a.T; t += 32) {
+    for (int t = lane; !a.b.defer_combine && t < a.T; t += 32) {
       float acc = 0.f;
       for (int j = 0; j < a.k; ++j) {
         const int p = t * a.k + j;
@@ -781,6 +781,7 @@ __global__ void __launch_bounds__(kDCWarps * 32) down_combine_kernel(GemvArgs a,
 // timer (2 s): on timeout the kernel flags the error word, lets its own copies
 // land and returns.
 constexpr unsigned long long kBulkWaitNs = 2000000000ull;
+constexpr unsigned long long kTestWaitNs = 20000000ull;   // the test wait's limit (20 ms)
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -888,6 +889,40 @@ __device__ __forceinline__ float reduce8(float (&v)[8], int lane) {
   v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
   return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
 }
+
+// The same for 4 values: afterwards lane l holds the full sum of value (l >> 3) & 3;
+// and for 2 values: value (l >> 4) & 1.  Same lane pairing as above.
+__device__ __forceinline__ float reduce4(float (&v)[4], int lane) {
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const bool hi = lane & 16;
+    const float send = hi ? v[j] : v[j + 2];
+    v[j] = (hi ? v[j + 2] : v[j]) + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+  {
+    const bool hi = lane & 8;
+    const float send = hi ? v[0] : v[1];
+    v[0] = (hi ? v[1] : v[0]) + __shfl_xor_sync(0xffffffffu, send, 8);
+  }
+  v[0] += __shfl_xor_sync(0xffffffffu, v[0], 4);
+  v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
+  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+}
+__device__ __forceinline__ float reduce2(float (&v)[2], int lane) {
+  {
+    const bool hi = lane & 16;
+    const float send = hi ? v[0] : v[1];
+    v[0] = (hi ? v[1] : v[0]) + __shfl_xor_sync(0xffffffffu, send, 16);
+  }
+  v[0] += __shfl_xor_sync(0xffffffffu, v[0], 8);
+  v[0] += __shfl_xor_sync(0xffffffffu, v[0], 4);
+  v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
+  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+}
+template <int N> __device__ __forceinline__ float reduce_rows(float (&v)[N], int lane);
+template <> __device__ __forceinline__ float reduce_rows<2>(float (&v)[2], int lane) { return reduce2(v, lane); }
+template <> __device__ __forceinline__ float reduce_rows<4>(float (&v)[4], int lane) { return reduce4(v, lane); }
+template <> __device__ __forceinline__ float reduce_rows<8>(float (&v)[8], int lane) { return reduce8(v, lane); }
 
 constexpr int kDownRows = 16;   // output rows per CTA of the bulk down kernel, at most
 constexpr size_t kPrefetchPiece = 32 * 1024;
@@ -1354,7 +1389,21 @@ __global__ void __launch_bounds__((kRing && !kPair) ? 256 : 512) down_bulk_kerne
     while (!bar_test(hbar, 0) && gtime() - t0 < kBulkWaitNs) {
     }
   }
+  if (a.b.test_wait && a.pass == 0 && threadIdx.x == 0) {
+    // a test of the bounded waits: a word nothing writes, given up on after 20 ms
+    const unsigned long long t0 = gtime();
+    bool set = false;
+    for (uint32_t n = 0; !set; ++n) {
+      set = __float_as_uint(*reinterpret_cast<const volatile float*>(a.b.never_set)) != 0xFFFFFFFFu;
+      if ((n & 15u) == 15u && gtime() - t0 > kTestWaitNs) break;
+    }
+    if (!set) {
+      ok = false;
+      atomicOr_system(err, kErrTimeout);
+    }
+  }
   const bool all_ok = __syncthreads_and(ok);
+  if (a.b.defer_combine) return;   // y is stored; the combine runs after the CPU branch
   if (!alone) {
     // Publish y and count this grid's arrival: the barrier orders every thread's y
     // stores before thread 0's gpu-scope acquire-release increment; the grid that
@@ -1634,6 +1683,7 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 2) resident_fused_kernel(Gem
     }
   }
   __syncthreads();
+  if (a.b.defer_combine) return;   // y is stored; the combine runs after the CPU branch
   if (!alone) {   // the split protocol of down_bulk_kernel
     if (threadIdx.x == 0) {
       uint32_t old;
@@ -1670,32 +1720,36 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 2) resident_fused_kernel(Gem
 
 // ---- resident experts, one token: gate/up and down rows as one expert-major stream --------
 // One bf16 token, bf16 weights, no shared expert.  Every byte the resident
-// experts need flows through the per-warp rings of one item list:
-//   items [0, ng*I):         gate row i + up row i of expert g (n = g*I + i)
-//   items [ng*I, ng*I + D):  RS rows of one row block b of expert g's W_down
-//                            (expert-major, then block, then sub-block q)
-// and warp w of the grid takes items w, w + warps, ...  Weight copies do not
-// depend on h, so lane 0 keeps NS items in flight whatever they are; only the
-// arithmetic of a down item waits, for its expert's h.  Because every gate/up
-// item precedes every down item, a warp holding a gate/up item never waits on
-// anything but its own copies, so no wait can close a cycle, and the h of the
-// early experts is complete long before their down items come up: the down
-// projection runs inside the weight stream instead of after a grid-wide
-// barrier, and only the last expert's down rows trail it.
+// experts need flows through the per-warp rings of one item list, and warp w of
+// the grid takes items w, w + warps, ...:
+//   items [0, ng*I): gate row i + up row i of expert g (n = g*I + i), so the
+//     experts' h complete one after another;
+//   then rounds of down items: in every round column c (the warp that owns it)
+//     takes RS rows of expert c mod ng's W_down, the next sub-block of that
+//     expert in each round.  A warp thus stays on one expert for all its down
+//     items and reads that expert's h once, into registers.
+// Weight copies do not depend on h, so lane 0 keeps NS items in flight whatever
+// they are; only the arithmetic of a down item waits, for its expert's h.
+// Every gate/up item precedes every down item and an item only waits for items
+// before it, so no wait can close a cycle.  The down projection runs inside
+// the weight stream instead of after a grid-wide barrier.
 //
-// Completion is counted per expert (gate/up rows done, zeroed by the control
-// kernel): a gate/up item publishes h with a release increment.  A down item
-// takes its expert's h with its weights when the count is complete at issue
-// time (checked with an acquire load, a proxy fence, then the bulk copy into the
-// same stage), else it waits for the count and reads h from L2.  The down items
-// of a row block are counted too; the warp that completes a block forms its
-// combine, or joins the split protocol with the filled-expert down grid (both
-// count themselves in arrive[b]; the second forms the combine from y in global
-// memory).  Arithmetic order is that of gate_up_bulk_kernel and down_bulk_kernel
-// (per-lane chunk sums, the same shuffle tree), so h, y and the layer output are
-// bit-identical to the two grids'.  Every wait is bounded by the global timer.
+// No fences or counters order the items: h and y of the resident pairs live in
+// two buffers per cache, used by alternate launches (the parity of the launch
+// number the control kernel writes), and a launch sets the other buffers to the
+// empty mark for the next one.  A value is published by storing it; a reader
+// takes a value once it is not the empty mark (4-byte stores and loads are
+// single-copy atomic).  A warp's first down item copies its expert's h into the
+// stage with its rows; entries still empty then are re-read from L2, 8 at a
+// time, until written.  The warp holding the last sub-block of the last
+// expert's rows of row block b waits in the same way for every resident y of
+// that block, stores them to y for the caller and the filled-expert grid, and
+// forms the block's combine, or joins the split protocol with the filled-expert
+// down grid (both count themselves in arrive[b]; the second forms the combine).
+// Arithmetic order is that of gate_up_bulk_kernel and down_bulk_kernel
+// (per-lane chunk sums, the same shuffle tree), so h, y and the layer output
+// are bit-identical to the two grids'.  Every wait is bounded by the global timer.
 constexpr int kStreamWarps = 8;
-constexpr int kStreamRows = 8;   // rows per down item, at most (one reduce8)
 
 struct StreamGeom {
   int NS;            // ring stages per warp
@@ -1705,13 +1759,27 @@ struct StreamGeom {
   size_t ring_off, plan_off, x_off, extra_off, smem;
 };
 
-__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+__device__ __forceinline__ bool stream_empty(float v) { return __float_as_uint(v) == kStreamEmpty; }
+
+__device__ __forceinline__ float ld_relaxed_f32(const float* p) {
+  float v;
+  asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
   return v;
 }
+__device__ __forceinline__ float4 ld_relaxed_f32x4(const float* p) {
+  float4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ bool any_empty8(const float* v) {
+  bool e = false;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) e |= stream_empty(v[i]);
+  return e;
+}
 
-template <int kJX, int kJN>
+template <int kJX, int kJN, int kRS>
 __global__ void __launch_bounds__(kStreamWarps * 32, 1) resident_stream_kernel(GemvArgs a, StreamGeom geo,
                                                                               const float* __restrict__ w,
                                                                               const float* __restrict__ cpu,
@@ -1731,85 +1799,48 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1) resident_stream_kernel(G
   const StagedPlan sp = stage_plan(sm + geo.plan_off, a);
   const int H = a.H, I = a.I, k = a.k;
   const int nfirst = a.b.plan[P_NFIRST], ngpu = a.b.plan[P_NGPU];
+  const int par = a.b.plan[P_SEQ] & 1;
   const bool skip = nfirst == 0 && ngpu > 0;   // only filled experts: their grid combines alone
   const bool alone = ngpu == nfirst;           // no filled expert: this kernel combines alone
   const int ng = skip ? 0 : nfirst;
-  uint32_t* gcnt = a.b.scnt;                   // [max_g] gate/up rows done per resident expert
-  uint32_t* bcnt = a.b.scnt + a.max_g;         // [nblk] down items done per row block
+  const size_t hn = (size_t)a.max_g * I, yn = (size_t)k * H;   // floats per h / y buffer
+  float* hb = a.b.hs2 + (size_t)par * hn;                      // this launch's h ...
+  float* yb = a.b.ys2 + (size_t)par * yn;                      // ... and y
+  const long nwarps = (long)gridDim.x * kStreamWarps;
+  const long w0 = (long)blockIdx.x * kStreamWarps + warp;
   int* s_slot = reinterpret_cast<int*>(sm + geo.extra_off);
   float* s_wt = reinterpret_cast<float*>(s_slot + k);
   uint8_t* xsm = sm + geo.x_off;
   for (int i = threadIdx.x; i < k; i += blockDim.x) { s_slot[i] = a.b.slot_map[i]; s_wt[i] = w[i]; }
-  {
-    uint4* dst = reinterpret_cast<uint4*>(xsm);
-    const uint4* src = reinterpret_cast<const uint4*>(a.x);
-    for (int i = threadIdx.x; i < H / 8; i += blockDim.x) dst[i] = src[i];
-  }
-  __syncthreads();
-  const long nwarps = (long)gridDim.x * kStreamWarps;
-  const long w0 = (long)blockIdx.x * kStreamWarps + warp;
+  __syncthreads();   // the staged plan
   const size_t row_h = F::row(H), row_i = F::row(I);
   const size_t down_off = 2ull * (size_t)I * row_h;
   const size_t hbytes = (size_t)I * 4;
-  const int per_e = geo.nblk * geo.Q;
+  const int per_e = geo.nblk * geo.Q;                  // down items of one expert
+  const int cpe = ng > 0 ? (int)(nwarps / ng) : 0;     // down columns of one expert
+  const int drounds = cpe > 0 ? (per_e + cpe - 1) / cpe : 0;
   const long n_gu = (long)ng * I;
-  const long items = n_gu + (long)ng * per_e;
+  const long items = n_gu + (long)drounds * nwarps;
   const uint64_t pol = evict_first_policy();
   bool missing = false;
 
-  // the combine of row block b by this warp: out[r] = sum_j w[j] * (slot >= 0 ? y : cpu)
-  auto combine_block = [&](int b) {
-    bool second = true;
-    if (!alone) {
-      uint32_t old = 0;
-      if (lane == 0)
-        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(a.b.arrive + b) : "memory");
-      second = (__shfl_sync(0xffffffffu, old, 0) & 1u) != 0u;
-    }
-    __syncwarp();
-    if (!second) return;
-    const int rb = b * geo.R;
-    const int nrb = min(geo.R, H - rb);
-    if (lane < nrb) {
-      const int r = rb + lane;
-      float acc = 0.f;
-      for (int j = 0; j < k; ++j) {
-        float v;
-        if (s_slot[j] >= 0) {
-          v = __ldcg(a.b.y + (size_t)j * H + r);
-        } else if (cpu != nullptr) {
-          v = __ldg(cpu + (size_t)j * H + r);
-        } else {
-          v = 0.f;
-          missing = true;
-        }
-        acc = fmaf(s_wt[j], v, acc);
-      }
-      out[r] = acc;
-    }
-  };
-
-  if (ng == 0) {   // every pair on the CPU (or only filled experts: their grid combines)
-    if (!skip)
-      for (long b = w0; b < geo.nblk; b += nwarps) combine_block((int)b);
-    if (missing) atomicOr_system(err, kErrMissingCpuPart);
-    return;
-  }
-
-  struct DownItem { int g, b, r0, nr; };
+  struct DownItem { int g, b, q, r0, nr; };   // g < 0: no item in this slot
   auto down_item = [&](long it) {
-    DownItem d;
-    const int m = (int)(it - n_gu);
-    d.g = m / per_e;
-    const int rem = m - d.g * per_e;
-    d.b = rem / geo.Q;
-    const int q = rem - d.b * geo.Q;
-    d.r0 = d.b * geo.R + q * geo.RS;
-    d.nr = min(geo.RS, min(geo.R, H - d.b * geo.R) - q * geo.RS);
+    DownItem d{-1, 0, 0, 0, 0};
+    const long m = it - n_gu;
+    const int c = (int)(m % nwarps), r = (int)(m / nwarps);
+    if (c >= cpe * ng) return d;
+    const int j = r * cpe + c / ng;
+    if (j >= per_e) return d;
+    d.g = c % ng;
+    d.b = j / geo.Q;
+    d.q = j - d.b * geo.Q;
+    d.r0 = d.b * geo.R + d.q * geo.RS;
+    d.nr = min(geo.RS, min(geo.R, H - d.b * geo.R) - d.q * geo.RS);
     return d;
   };
   long last_issued[4] = {-1, -1, -1, -1};
-  bool h_staged[4] = {false, false, false, false};   // lane 0: the stage holds its expert's h
+  bool h_sent = false;   // lane 0: this warp's expert's h went out with an earlier down item
   auto issue = [&](long it, int st) {   // lane 0 only
     last_issued[st] = it;
     uint8_t* dst = ring + (size_t)st * geo.SB;
@@ -1821,29 +1852,136 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1) resident_stream_kernel(G
       return;
     }
     const DownItem d = down_item(it);
-    if (d.nr <= 0) {   // past the last row: an empty item, counted like the others
+    if (d.g < 0 || d.nr <= 0) {   // no rows here
       bar_expect(&bars[st], 0u);
-      h_staged[st] = false;
       return;
     }
     const uint32_t wb = (uint32_t)(d.nr * row_i);
-    // h is final once every gate/up row of the expert is counted; then it rides along
-    const bool hs = ld_acquire_u32(gcnt + d.g) >= (uint32_t)I;
-    h_staged[st] = hs;
-    bar_expect(&bars[st], wb + (hs ? (uint32_t)hbytes : 0u));
+    bar_expect(&bars[st], wb + (h_sent ? 0u : (uint32_t)hbytes));
     bulk_copy(dst, sp.w[d.g] + down_off + (size_t)d.r0 * row_i, wb, &bars[st], pol);
-    if (hs) {
-      asm volatile("fence.proxy.async.global;" ::: "memory");
-      const int pid = sp.pid[sp.off[d.g]];
-      bulk_copy_keep(dst + (size_t)geo.RS * row_i, a.b.h + (size_t)pid * I, (uint32_t)hbytes, &bars[st]);
-    }
+    if (!h_sent)   // the expert's h as it stands (checked entry by entry before use)
+      bulk_copy_keep(dst + (size_t)geo.RS * row_i, hb + (size_t)d.g * I, (uint32_t)hbytes, &bars[st]);
+    h_sent = true;
   };
   const long n_mine = items > w0 ? (items - w0 + nwarps - 1) / nwarps : 0;
   if (lane == 0)
     for (int kk = 0; kk < geo.NS && kk < n_mine; ++kk) issue(w0 + (long)kk * nwarps, kk);
+  {
+    // x while the first copies are in flight; and the other h / y buffers emptied
+    // for the next launch (the launch before this one, which used them, is complete)
+    uint4* dst = reinterpret_cast<uint4*>(xsm);
+    const uint4* src = reinterpret_cast<const uint4*>(a.x);
+    for (int i = threadIdx.x; i < H / 8; i += blockDim.x) dst[i] = src[i];
+    float* ho = a.b.hs2 + (size_t)(par ^ 1) * hn;
+    float* yo = a.b.ys2 + (size_t)(par ^ 1) * yn;
+    const float e = __uint_as_float(kStreamEmpty);
+    for (size_t i = (size_t)(w0 * 32 + lane); i < hn + yn; i += (size_t)nwarps * 32) {
+      if (i < hn) ho[i] = e;
+      else yo[i - hn] = e;
+    }
+  }
+  __syncthreads();
+
+  // Row block b: wait for every resident y of the block, store it to y, then form
+  // out[r] = sum_j w[j] * (slot >= 0 ? y : cpu) (or leave it to the filled-expert
+  // grid when that one arrives second).  false after the wait limit.
+  auto finish_block = [&](int b) -> bool {
+    if (a.b.test_wait) {   // a wait that runs out: the word is never written
+      bool set = false;
+      if (lane == 0) {
+        const unsigned long long t0 = gtime();
+        for (uint32_t n = 0; !set; ++n) {
+          set = !stream_empty(ld_relaxed_f32(a.b.never_set));
+          if ((n & 15u) == 15u && gtime() - t0 > kTestWaitNs) break;
+        }
+      }
+      if (!__shfl_sync(0xffffffffu, (int)set, 0)) return false;
+    }
+    const int rb = b * geo.R;
+    const int nrb = min(geo.R, H - rb);
+    constexpr int kPer = (kStreamWarps * 2 * 16 + 31) / 32;   // entries per lane: 8 experts x 16 rows at most
+    float v[kPer];
+    size_t o[kPer];
+    int pidv[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int e = lane + 32 * u;
+      o[u] = 0;
+      pidv[u] = -1;
+      v[u] = 0.f;
+      if (e < ng * nrb) {
+        const int g = e / nrb, r = rb + e % nrb;
+        pidv[u] = sp.pid[sp.off[g]];
+        o[u] = (size_t)pidv[u] * H + r;
+        v[u] = ld_relaxed_f32(yb + o[u]);
+      }
+    }
+    bool done = true;
+    {
+      const unsigned long long t0 = gtime();
+      for (uint32_t n = 0;; ++n) {
+        bool again = false;
+#pragma unroll
+        for (int u = 0; u < kPer; ++u)
+          if (pidv[u] >= 0 && stream_empty(v[u])) { v[u] = ld_relaxed_f32(yb + o[u]); again = true; }
+        if (!again) break;
+        if ((n & 15u) == 15u && gtime() - t0 > kBulkWaitNs) { done = false; break; }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u)
+      if (pidv[u] >= 0) a.b.y[o[u]] = v[u];   // per-pair output stays readable (moe_cache_get_plan)
+    if (!__all_sync(0xffffffffu, done)) return false;
+    __syncwarp();   // the y stores above precede lane 0's release and the combine's loads
+    if (a.b.defer_combine) return true;   // the combine runs after the CPU branch
+    bool second = true;
+    if (!alone) {
+      uint32_t old = 0;
+      if (lane == 0)
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(a.b.arrive + b) : "memory");
+      second = (__shfl_sync(0xffffffffu, old, 0) & 1u) != 0u;
+    }
+    if (!second) return true;
+    if (lane < nrb) {
+      const int r = rb + lane;
+      float acc = 0.f;
+      for (int j = 0; j < k; ++j) {
+        float vv;
+        if (s_slot[j] >= 0) {
+          vv = __ldcg(a.b.y + (size_t)j * H + r);
+        } else if (cpu != nullptr) {
+          vv = __ldg(cpu + (size_t)j * H + r);
+        } else {
+          vv = 0.f;
+          missing = true;
+        }
+        acc = fmaf(s_wt[j], vv, acc);
+      }
+      out[r] = acc;
+    }
+    return true;
+  };
+
+  if (ng == 0) {   // every pair on the CPU (or only filled experts: their grid combines)
+    if (!skip)
+      for (long b = w0; b < geo.nblk; b += nwarps) finish_block((int)b);
+    if (missing) atomicOr_system(err, kErrMissingCpuPart);
+    return;
+  }
+
+  // the warp is done reading stage st (item it): lane 0 refills it with the item NS ahead
+  auto rearm = [&](long it, int st) {
+    __syncwarp();
+    if (lane == 0 && it + (long)geo.NS * nwarps < items) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(it + (long)geo.NS * nwarps, st);
+    }
+  };
   uint4 xr[kJX];
 #pragma unroll
   for (int j = 0; j < kJX; ++j) xr[j] = reinterpret_cast<const uint4*>(xsm)[j * 32 + lane];
+  float hv[kJN][V];       // the h of this warp's down expert, once loaded
+  bool h_loaded = false;
   bool ok = true;
   int kk = 0;
   for (long it = w0; it < items; it += nwarps, ++kk) {
@@ -1868,86 +2006,84 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1) resident_stream_kernel(G
       }
       ag = warp_sum(ag);
       au = warp_sum(au);
+      rearm(it, st);
       if (lane == 0) {
-        a.b.h[(size_t)sp.pid[sp.off[g]] * I + i] = silu(ag) * au;
-        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(gcnt + g) : "memory");
+        const float h1 = silu(ag) * au;
+        asm volatile("st.relaxed.gpu.global.f32 [%0], %1;" ::"l"(hb + (size_t)g * I + i), "f"(h1) : "memory");
       }
-    } else {
-      const DownItem d = down_item(it);
-      if (d.nr > 0) {
-        const int pid = sp.pid[sp.off[d.g]];
-        const bool hs = __shfl_sync(0xffffffffu, lane == 0 ? (int)h_staged[st] : 0, 0) != 0;
-        float hv[kJN][V];
-        if (hs) {
-          const float* hsm = reinterpret_cast<const float*>(stage + (size_t)geo.RS * row_i);
+      continue;
+    }
+    const DownItem d = down_item(it);
+    if (d.g >= 0 && d.nr > 0) {
+      const int pid = sp.pid[sp.off[d.g]];
+      if (!h_loaded) {
+        // the expert's h from the stage; entries still empty when it was copied
+        // are re-read from L2, 8 at a time, until written
+        const float* hsm = reinterpret_cast<const float*>(stage + (size_t)geo.RS * row_i);
+        const float* hg = hb + (size_t)d.g * I;
 #pragma unroll
-          for (int j = 0; j < kJN; ++j) {
-            const float4* hp = reinterpret_cast<const float4*>(hsm + (size_t)(j * 32 + lane) * V);
-            const float4 q0 = hp[0], q1 = hp[1];
-            hv[j][0] = q0.x; hv[j][1] = q0.y; hv[j][2] = q0.z; hv[j][3] = q0.w;
-            hv[j][4] = q1.x; hv[j][5] = q1.y; hv[j][6] = q1.z; hv[j][7] = q1.w;
-          }
-        } else {
-          // wait for the expert's h (its last gate/up rows are still on their way)
-          bool done = true;
-          if (lane == 0) {
-            const unsigned long long t0 = gtime();
-            for (uint32_t n = 0; ld_acquire_u32(gcnt + d.g) < (uint32_t)I; ++n)
-              if ((n & 15u) == 15u && gtime() - t0 > kBulkWaitNs) { done = false; break; }
-          }
-          if (!__shfl_sync(0xffffffffu, (int)done, 0)) { ok = false; break; }
-#pragma unroll
-          for (int j = 0; j < kJN; ++j) {
-            const float4* hp = reinterpret_cast<const float4*>(a.b.h + (size_t)pid * I + (size_t)(j * 32 + lane) * V);
-            const float4 q0 = __ldcg(hp), q1 = __ldcg(hp + 1);
-            hv[j][0] = q0.x; hv[j][1] = q0.y; hv[j][2] = q0.z; hv[j][3] = q0.w;
-            hv[j][4] = q1.x; hv[j][5] = q1.y; hv[j][6] = q1.z; hv[j][7] = q1.w;
-          }
+        for (int j = 0; j < kJN; ++j) {
+          const float4* hp = reinterpret_cast<const float4*>(hsm + (size_t)(j * 32 + lane) * V);
+          const float4 q0 = hp[0], q1 = hp[1];
+          hv[j][0] = q0.x; hv[j][1] = q0.y; hv[j][2] = q0.z; hv[j][3] = q0.w;
+          hv[j][4] = q1.x; hv[j][5] = q1.y; hv[j][6] = q1.z; hv[j][7] = q1.w;
         }
-        // the straight-line rows of down_bulk_kernel: rows past nr repeat the last
-        // row (never stored), per-lane sums in the same order, the same shuffle tree
-        float acc[kStreamRows];
-#pragma unroll
-        for (int r = 0; r < kStreamRows; ++r) {
-          const int rr = r < d.nr ? r : d.nr - 1;
-          const uint4* wrow = reinterpret_cast<const uint4*>(stage + (size_t)rr * row_i);
-          float dsum = 0.f;
+        bool hok = true;
+        const unsigned long long t0 = gtime();
+        for (uint32_t n = 0;; ++n) {
+          bool again = false;
 #pragma unroll
           for (int j = 0; j < kJN; ++j) {
-            float fw[V];
-            F::unpack(wrow[j * 32 + lane], fw);
-            float dj = 0.f;
-#pragma unroll
-            for (int v = 0; v < V; ++v) dj = fmaf(fw[v], hv[j][v], dj);
-            dsum += dj;
+            if (any_empty8(hv[j])) {
+              const float* src = hg + (size_t)(j * 32 + lane) * V;
+              const float4 q0 = ld_relaxed_f32x4(src), q1 = ld_relaxed_f32x4(src + 4);
+              hv[j][0] = q0.x; hv[j][1] = q0.y; hv[j][2] = q0.z; hv[j][3] = q0.w;
+              hv[j][4] = q1.x; hv[j][5] = q1.y; hv[j][6] = q1.z; hv[j][7] = q1.w;
+              again = true;
+            }
           }
-          acc[r] = 0.f + dsum;
+          if (!again) break;
+          if ((n & 15u) == 15u && gtime() - t0 > kBulkWaitNs) { hok = false; break; }
         }
-        const float v = reduce8(acc, lane);
-        const int r = (lane >> 2) & 7;
-        if ((lane & 3) == 0 && r < d.nr) a.b.y[(size_t)pid * H + d.r0 + r] = v;
+        if (!__all_sync(0xffffffffu, hok)) { ok = false; break; }
+        h_loaded = true;
       }
-      // count the item in its row block; the warp that completes the block combines it
-      __syncwarp();
-      uint32_t old = 0;
-      if (lane == 0)
-        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(bcnt + d.b) : "memory");
-      if (__shfl_sync(0xffffffffu, old, 0) + 1u == (uint32_t)(ng * geo.Q)) combine_block(d.b);
+      // the straight-line rows of down_bulk_kernel: rows past nr repeat the last
+      // row (never stored), per-lane sums in the same order, the same shuffle tree
+      float acc[kRS];
+#pragma unroll
+      for (int r = 0; r < kRS; ++r) {
+        const int rr = r < d.nr ? r : d.nr - 1;
+        const uint4* wrow = reinterpret_cast<const uint4*>(stage + (size_t)rr * row_i);
+        float dsum = 0.f;
+#pragma unroll
+        for (int j = 0; j < kJN; ++j) {
+          float fw[V];
+          F::unpack(wrow[j * 32 + lane], fw);
+          float dj = 0.f;
+#pragma unroll
+          for (int v = 0; v < V; ++v) dj = fmaf(fw[v], hv[j][v], dj);
+          dsum += dj;
+        }
+        acc[r] = 0.f + dsum;
+      }
+      const float v = reduce_rows<kRS>(acc, lane);
+      const int r = (lane >> (5 - (kRS == 2 ? 1 : kRS == 4 ? 2 : 3))) & (kRS - 1);
+      if ((lane & (32 / kRS - 1)) == 0 && r < d.nr)
+        asm volatile("st.relaxed.gpu.global.f32 [%0], %1;" ::"l"(yb + (size_t)pid * H + d.r0 + r), "f"(v) : "memory");
     }
-    __syncwarp();
-    if (lane == 0 && it + (long)geo.NS * nwarps < items) {
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      issue(it + (long)geo.NS * nwarps, st);
-    }
+    rearm(it, st);
+    // the last sub-block of the last expert's rows of a block finishes the block
+    if (d.g == ng - 1 && d.q == geo.Q - 1 && !finish_block(d.b)) { ok = false; break; }
   }
   if (!ok && lane == 0) {   // flag the timeout; this warp's copies land before the CTA exits
     atomicOr_system(err, kErrTimeout);
     for (int s2 = 0; s2 < geo.NS; ++s2) {
       if (last_issued[s2] < 0) continue;
       const long k2 = (last_issued[s2] - w0) / nwarps;
-      const uint32_t par = (uint32_t)((k2 / geo.NS) & 1);
+      const uint32_t par2 = (uint32_t)((k2 / geo.NS) & 1);
       const unsigned long long t0 = gtime();
-      while (!bar_test(&bars[s2], par) && gtime() - t0 < kBulkWaitNs) {
+      while (!bar_test(&bars[s2], par2) && gtime() - t0 < kBulkWaitNs) {
       }
     }
   }
@@ -2187,8 +2323,10 @@ cudaError_t setup_gemv_kernels() {
   }
   for (const void* k : {(const void*)resident_fused_kernel<8, 3>, (const void*)resident_fused_kernel<8, 4>,
                         (const void*)resident_fused_kernel<4, 3>, (const void*)resident_fused_kernel<4, 4>,
-                        (const void*)resident_stream_kernel<8, 3>, (const void*)resident_stream_kernel<8, 4>,
-                        (const void*)resident_stream_kernel<4, 3>, (const void*)resident_stream_kernel<4, 4>}) {
+                        (const void*)resident_stream_kernel<8, 3, 4>, (const void*)resident_stream_kernel<8, 3, 2>,
+                        (const void*)resident_stream_kernel<8, 4, 4>, (const void*)resident_stream_kernel<8, 4, 2>,
+                        (const void*)resident_stream_kernel<4, 3, 4>, (const void*)resident_stream_kernel<4, 3, 2>,
+                        (const void*)resident_stream_kernel<4, 4, 4>, (const void*)resident_stream_kernel<4, 4, 2>}) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFusedSmemMax);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, kDecodeCarveout);
     if (e != cudaSuccess) return e;
@@ -2424,11 +2562,13 @@ bool fp4_decode_fits(const Shape& sh, int max_tokens, int sms) {
 }
 
 // The bulk down kernel runs when its ring fits and every pair's h fits in
-// shared memory; the split into resident / filled grids rides on it.
+// shared memory, or, for one token, when only the ring fits: each warp then
+// reads its pair's h through L1 (the DeepSeek-V3 shape: 9 pairs x 2048 fp32 =
+// 72 KB of h).  The split into resident / filled grids rides on it.
 bool down_split_ok(const Shape& sh, int T, int sms) {
   const GemvArgs a = make_args(sh, 2, T, nullptr, DecodeBufs{});
   const BulkGeom geo = down_geom(a, sh.wdtype, sms);
-  return geo.NS >= 1 && geo.h_smem;
+  return geo.NS >= 1 && (geo.h_smem || T == 1);
 }
 
 cudaError_t launch_down_split(const Shape& sh, int pass, int T, const float* w, const float* cpu_part, DecodeBufs b,
@@ -2508,14 +2648,18 @@ StreamGeom stream_geom(const GemvArgs& a, int wdtype, int adtype, int sms) {
   if (wdtype != MOE_BF16 || adtype != MOE_BF16 || a.T != 1 || a.n_shared != 0) return g;
   if (a.H % 256 != 0 || (a.H / 256 != 4 && a.H / 256 != 8) || a.I % 256 != 0 || (a.I / 256 != 3 && a.I / 256 != 4))
     return g;
+  if (a.max_g > kStreamWarps * 2) return g;   // finish_block reads at most 16 experts' rows per lane group
   const BulkGeom dg = down_geom(a, wdtype, sms);
-  if (dg.NS < 1 || !dg.h_smem || dg.R < 1) return g;
+  if (dg.NS < 1 || dg.R < 1 || dg.R > 16) return g;
   g.R = dg.R;
   g.nblk = dg.grid;
   const size_t row_h = wrow(MOE_BF16, (size_t)a.H), row_i = wrow(MOE_BF16, (size_t)a.I), hb = (size_t)a.I * 4;
-  g.SB = up128(std::max(2 * row_h, hb + 2 * row_i));
-  g.RS = (int)std::min<size_t>(std::min<size_t>((size_t)kStreamRows, (size_t)g.R), (g.SB - hb) / row_i);
+  // 4 rows per down item where they and h fit in about a gate/up row pair, else 2
+  g.RS = (4 * row_i + hb <= 2 * row_h + 1024) ? 4 : 2;
+  if (g.RS > g.R) g.RS = g.R >= 2 ? 2 : 1;
+  if (g.RS != 2 && g.RS != 4) return g;
   g.Q = (g.R + g.RS - 1) / g.RS;
+  g.SB = up128(std::max(2 * row_h, hb + (size_t)g.RS * row_i));
   const size_t plan = up128(staged_plan_bytes(a.max_g, a.max_p));
   const size_t xb = up128((size_t)a.H * 2);
   const size_t extra = up128((size_t)a.k * 8);
@@ -2536,23 +2680,20 @@ bool resident_stream_ok(const Shape& sh, int T, int sms) {
   return stream_geom(a, sh.wdtype, sh.adtype, sms).NS > 0;
 }
 
-int resident_stream_counters(const Shape& sh, int T, int sms) {
-  const GemvArgs a = make_args(sh, 0, T, nullptr, DecodeBufs{});
-  const StreamGeom g = stream_geom(a, sh.wdtype, sh.adtype, sms);
-  return g.NS > 0 ? a.max_g + g.nblk : 0;
-}
-
 cudaError_t launch_resident_stream(const Shape& sh, int T, const void* x, const float* w, const float* cpu_part,
                                    DecodeBufs b, float* out, uint32_t* err, int sms, cudaStream_t s) {
   const GemvArgs a = make_args(sh, 0, T, x, b);
   const StreamGeom g = stream_geom(a, sh.wdtype, sh.adtype, sms);
-  if (g.NS == 0 || b.scnt == nullptr || b.n_scnt < a.max_g + g.nblk) return cudaErrorInvalidValue;
+  if (g.NS == 0 || b.hs2 == nullptr || b.ys2 == nullptr || !b.stream) return cudaErrorInvalidValue;
   const dim3 grid(sms), block(kStreamWarps * 32);
   const int jx = a.H / 256, jn = a.I / 256;
-  if (jx == 8 && jn == 3) return launch_pdl(resident_stream_kernel<8, 3>, grid, block, g.smem, s, a, g, w, cpu_part, out, err);
-  if (jx == 8 && jn == 4) return launch_pdl(resident_stream_kernel<8, 4>, grid, block, g.smem, s, a, g, w, cpu_part, out, err);
-  if (jx == 4 && jn == 3) return launch_pdl(resident_stream_kernel<4, 3>, grid, block, g.smem, s, a, g, w, cpu_part, out, err);
-  return launch_pdl(resident_stream_kernel<4, 4>, grid, block, g.smem, s, a, g, w, cpu_part, out, err);
+#define MOE_STREAM_LAUNCH(JX, JN, ROWS)                                                                             \
+  if (jx == JX && jn == JN && g.RS == ROWS)                                                                         \
+    return launch_pdl(resident_stream_kernel<JX, JN, ROWS>, grid, block, g.smem, s, a, g, w, cpu_part, out, err);
+  MOE_STREAM_LAUNCH(8, 3, 4) MOE_STREAM_LAUNCH(8, 3, 2) MOE_STREAM_LAUNCH(8, 4, 4) MOE_STREAM_LAUNCH(8, 4, 2)
+  MOE_STREAM_LAUNCH(4, 3, 4) MOE_STREAM_LAUNCH(4, 3, 2) MOE_STREAM_LAUNCH(4, 4, 4) MOE_STREAM_LAUNCH(4, 4, 2)
+#undef MOE_STREAM_LAUNCH
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_down_combine(const Shape& sh, int T, const float* w, const float* cpu_part, DecodeBufs b,
@@ -2575,7 +2716,7 @@ cudaError_t launch_down_combine(const Shape& sh, int T, const float* w, const fl
   if (sh.wdtype == MOE_F32) e = launch_down_typed<MOE_F32>(a, sms, s);
   else if (sh.wdtype == MOE_BF16) e = launch_down_typed<MOE_BF16>(a, sms, s);
   else e = launch_down_typed<MOE_FP8E4M3_B128>(a, sms, s);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || b.defer_combine) return e;   // deferred: the combine follows the CPU branch
   return launch_combine(sh, T, w, cpu_part, b, out, err, s);
 }
 

@@ -779,10 +779,10 @@ moe_status prefill_init(moe_cache* c) {
   const int E = k.n_experts;
   ps->P_max = k.max_prefill_tokens * k.top_k;
   ps->max_mtiles = (ps->P_max + BM - 1) / BM + E;
-  CK(cudaMalloc(&ps->xs, (size_t)ps->P_max * k.hidden * 2));
-  CK(cudaMalloc(&ps->hs, (size_t)ps->P_max * k.inter * 2));
+  CK(moe_malloc(&ps->xs, (size_t)ps->P_max * k.hidden * 2));
+  CK(moe_malloc(&ps->hs, (size_t)ps->P_max * k.inter * 2));
   const size_t ints = (size_t)ps->P_max + E + (E + 1) + E + (size_t)ps->max_mtiles * 4 + 1 + E + E + 4 * E + 2;
-  CK(cudaMalloc(&ps->ibuf, ints * 4));
+  CK(moe_malloc(&ps->ibuf, ints * 4));
   CK(cudaMemset(ps->ibuf, 0, ints * 4));
   int32_t* p = ps->ibuf;
   ps->perm = p; p += ps->P_max;
@@ -798,8 +798,8 @@ moe_status prefill_init(moe_cache* c) {
   c->dev_bytes += (size_t)ps->P_max * (k.hidden + k.inter) * 2 + ints * 4;
   if (fp4_weights(c)) {
     const size_t wb = (size_t)E * 3 * k.inter * k.hidden * 2;
-    CK(cudaMalloc(&ps->wbf, wb));
-    CK(cudaMalloc(&ps->ident, (size_t)E * 4));
+    CK(moe_malloc(&ps->wbf, wb));
+    CK(moe_malloc(&ps->ident, (size_t)E * 4));
     std::vector<int32_t> id(E);
     for (int e = 0; e < E; ++e) id[e] = e;
     CK(cudaMemcpy(ps->ident, id.data(), (size_t)E * 4, cudaMemcpyHostToDevice));

@@ -52,14 +52,15 @@ def make_cache(cfg: Config, pool, offs, shared, bw, max_prefill_tokens=0, n_slot
 
 
 def run_decode_parity(cfg: Config, bw, n_phys=None, fp_every=1, fp_limit=None, check_plan=True,
-                      pinned=True, state_every=1) -> DecodeRun:
+                      pinned=True, state_every=1, fp_steps=(), memo=16) -> DecodeRun:
     """Replay cfg's decode trace on the GPU and in the oracle; compare control state bit for bit.
 
     Every call: slot map (bit-exact) and, with check_plan, q / victims / fills.
     Every `state_every` steps: slot table, stamps, flat-id table, counters, clock.
-    Every `fp_every`-th layer-step (up to fp_limit): the layer output within TOL,
-    with the CPU-assigned pairs' partial sums supplied from the oracle and NaN
-    planted in every entry the combine must not read.
+    Every `fp_every`-th layer-step (up to fp_limit), and every layer-step of the
+    steps in `fp_steps`: the layer output within TOL, with the CPU-assigned
+    pairs' partial sums supplied from the oracle and NaN planted in every entry
+    the combine must not read.  `memo`: parsed experts the oracle keeps.
     """
     import torch
     s = cfg.shape
@@ -68,7 +69,8 @@ def run_decode_parity(cfg: Config, bw, n_phys=None, fp_every=1, fp_limit=None, c
     shared = make_shared(s, cfg.seed) if s.n_shared else None
     cache, K = make_cache(cfg, pool, offs, shared, bw)
     ora = SlotCache(s.L, s.E, cfg.capacity, K, bw[0], bw[1])
-    store = ExpertStore(arena, offs, s.wdtype, s.H, s.I, s.blob_bytes)
+    store = ExpertStore(arena, offs, s.wdtype, s.H, s.I, s.blob_bytes, memo=memo)
+    fp_steps = set(fp_steps)
     ids, w = routing_trace(cfg)
     res = DecodeRun()
     out = torch.empty(cfg.T, s.H, device=dev)
@@ -82,7 +84,7 @@ def run_decode_parity(cfg: Config, bw, n_phys=None, fp_every=1, fp_limit=None, c
         for l in range(s.L):
             plan = ora.decode(l, ids[st, l])
             x = activations(cfg, st, l)
-            check_fp = (n % fp_every == 0) and (fp_limit is None or res.fp_checked < fp_limit)
+            check_fp = (st in fp_steps) or ((n % fp_every == 0) and (fp_limit is None or res.fp_checked < fp_limit))
             n += 1
             if check_fp:
                 y = pair_outputs(store, l, s.E, x, s.adtype, ids[st, l])

@@ -62,17 +62,21 @@ def test_qwen3_b1_full_trace():
 
 
 def test_qwen3_b16_with_resize():
+    # outputs on every layer-step of the 8 steps around the resize (1228 -> 737 slots before step 128)
     cfg = config("qwen3_decode_b16")
-    res = run_decode_parity(cfg, cfg.bw_mbps, n_phys=48, fp_every=1499, state_every=8, check_plan=True)
+    res = run_decode_parity(cfg, cfg.bw_mbps, n_phys=48, fp_every=1499, state_every=8, check_plan=True,
+                            fp_steps=range(124, 132), memo=48)
     _ok(res)
-    assert res.calls == 256 * 48 and res.cpu_pairs > 0
+    assert res.calls == 256 * 48 and res.cpu_pairs > 0 and res.fp_checked >= 8 * 48
 
 
 def test_dsv3_fp8_shared_expert():
+    # outputs on every layer-step of the first 16 steps (cold start: fills, hits, CPU pairs and the
+    # shared expert mixed), then every 97th
     cfg = config("dsv3_decode_slice")
-    res = run_decode_parity(cfg, (150000, 150000), n_phys=6, fp_every=97, fp_limit=6, state_every=4)
+    res = run_decode_parity(cfg, (150000, 150000), n_phys=6, fp_every=97, state_every=4, fp_steps=range(16))
     _ok(res)
-    assert res.fp_checked >= 5
+    assert res.fp_checked >= 16 * 4 and res.cpu_pairs > 0 and res.fills > 0
 
 
 def test_control_one_warp_path_at_its_limit():

@@ -125,6 +125,14 @@ def test_qwen3_shape_1k_tokens():
     _run_prefill(cfg, C=300, layers=[0, 1, 2], n_phys=64, sample=256)
 
 
+def test_qwen3_prefill_8k_every_token_of_two_layers():
+    # the whole 8192-token chunk's outputs, every token, for a layer loaded in full and
+    # the one prefetched beside its GEMMs
+    cfg = config("qwen3_prefill_8k")
+    worst, _ = _run_prefill(cfg, C=cfg.capacity, layers=[0, 1], n_phys=64, sample=None)
+    assert worst <= TOL
+
+
 def test_qwen3_prefill_8k_all_layers_state_and_sampled_outputs():
     import torch
     cfg = config("qwen3_prefill_8k")
@@ -257,6 +265,13 @@ def test_fp4_small_full_layer_on_demand_and_ragged(fmt):
 def test_fp4_qwen3_shape_1k_tokens(fmt):
     cfg = _fp4(config("qwen3_prefill_8k").with_(T=1024), fmt)
     _run_prefill(cfg, C=300, layers=[0, 1, 2], n_phys=64, sample=128)
+
+
+@pytest.mark.parametrize("fmt", FP4)
+def test_fp4_qwen3_prefill_8k_every_token(fmt):
+    # the bench's 4-bit chunk size: every token of two layers, full-layer double buffering
+    cfg = _fp4(config("qwen3_prefill_8k"), fmt)
+    _run_prefill(cfg, C=cfg.capacity, layers=[0, 1], n_phys=64, sample=None)
 
 
 def test_mxfp4_prefill_survivors_seed_decode():
