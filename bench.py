@@ -64,11 +64,7 @@ FUSED_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of the
                         "qwen3 b1 shape, 8 resident experts per layer); profiles/decode_fused_resident_qwen3_b1.md")
 
 
-# the same for the expert-major stream launch (the default): none captured yet
-STREAM_TRAFFIC_PER_LAYER_STEP = None
-STREAM_TRAFFIC_SOURCE = None
-RESIDENT_TRAFFIC = {0: (TRAFFIC_PER_LAYER_STEP, TRAFFIC_SOURCE), 1: (FUSED_TRAFFIC_PER_LAYER_STEP, FUSED_TRAFFIC_SOURCE),
-                    2: (STREAM_TRAFFIC_PER_LAYER_STEP, STREAM_TRAFFIC_SOURCE)}
+RESIDENT_TRAFFIC = {0: (TRAFFIC_PER_LAYER_STEP, TRAFFIC_SOURCE), 1: (FUSED_TRAFFIC_PER_LAYER_STEP, FUSED_TRAFFIC_SOURCE)}
 # DRAM bytes per launch of the other workloads' dominant kernel group, from ncu
 # captures (none yet: the roofline's traffic stays null).
 WORKLOAD_TRAFFIC: dict = {}
@@ -548,7 +544,7 @@ def main(args):
     # the resident experts' kernels (one launch, or a gate/up grid and a down +
     # combine grid), as the library reports
     launches_per_layer = int(run.cache.info()[6])
-    resident_path = int(run.cache.info()[7])   # 0: two grids, 1: one launch with a grid barrier, 2: one stream
+    resident_path = int(run.cache.info()[7])   # 0: two grids, 1: one launch with a grid barrier
 
     # ---- timed region: inputs resident in HBM; trace steps [prefix, prefix + steps) ----
     if world > 1:
@@ -679,12 +675,7 @@ def main(args):
                          1: "resident-expert SwiGLU per layer-step, one launch: the gate/up stream (with the L2 "
                             "fetch of W_down), a grid-wide barrier, then the down projection fused with the "
                             "combine; one step replayed with every routed expert resident, an event pair around "
-                            "the launch",
-                         2: "resident-expert SwiGLU per layer-step, one launch (resident_stream_kernel): gate/up "
-                            "rows and W_down row blocks as one expert-major stream of bulk copies, each expert's "
-                            "down rows computed once its h is counted complete, the combine by the warp that "
-                            "completes a row block; one step replayed with every routed expert resident, an event "
-                            "pair around the launch"}[resident_path],
+                            "the launch"}[resident_path],
                      "achieved": round(res_gbs, 1) if res_gbs else None, "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(res_gbs / hbm_peak, 3) if res_gbs else None, "peak_source": peak_src,
                      "traffic": RESIDENT_TRAFFIC[resident_path][0],
@@ -767,6 +758,7 @@ def cpu_branch_measure(args, dev, steps=32):
                 host["s"] += time.perf_counter() - t0
             run.cache.set_cpu_branch(fn)
         run.warm(PREFIX_STEPS)
+        run.sync()
         host.update(calls=0, s=0.0, pairs=0)
         ms, dcnt = run.timed(steps)
         out[mode] = {"value": round(steps * s.L / (ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(ms / steps, 4),

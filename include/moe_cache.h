@@ -104,9 +104,9 @@ typedef enum moe_dtype {
  * (fp8), 32 (nvfp4, mxfp4) or 8 (f32, bf16), and S a multiple of 16 bytes (for
  * fp8: the scale count (2I/128)(H/128) + (H/128)(I/128) a multiple of 4);
  * otherwise moe_cache_create and moe_layer_ffn_noalloc return MOE_EINVAL.
- * NVFP4 and MXFP4 experts serve decode calls of up to 2 tokens (max_tokens <=
- * 2); their prefill decodes each layer's routed experts to bf16 for the
- * grouped GEMM (see moe_layer_prefill).
+ * NVFP4 and MXFP4 experts stay 4-bit in the slots and are decoded chunk by
+ * chunk inside the decode GEMVs (any batch); their prefill decodes each
+ * layer's routed experts to bf16 for the grouped GEMM (see moe_layer_prefill).
  */
 typedef struct moe_config {
   int32_t n_layers;       /* L */
@@ -172,9 +172,7 @@ moe_status moe_cache_resize(moe_cache* cache, uint64_t n_slots);
  * MOE_DECODE_RESIDENT=fused (or MOE_DECODE_FUSED=1) in the environment when the
  * cache is created, one-token calls on bf16 caches with at most top-8 routed
  * experts and no shared expert run both in one launch with a grid-wide barrier
- * between them instead; with MOE_DECODE_RESIDENT=stream, one-token bf16 calls
- * without a shared expert run them as one launch streaming gate/up rows and
- * W_down row blocks as one expert-major item list (same outputs bit for bit).
+ * between them instead (same outputs bit for bit).
  * With a CPU branch registered (moe_cache_set_cpu_branch) cpu_part_dev is
  * ignored.
  */
@@ -246,8 +244,7 @@ moe_status moe_cache_get_plan(moe_cache* cache, int32_t* scalars_host, int32_t* 
  * max_tokens tokens (with a CPU branch registered: its combine kernel
  * included), and how such a call runs its resident experts: 0 = a gate/up grid
  * then a down + combine grid, 1 = one launch with a grid-wide barrier between
- * gate/up and down + combine, 2 = one launch streaming gate/up and down rows as
- * one expert-major item list.
+ * gate/up and down + combine.
  */
 moe_status moe_cache_info(moe_cache* cache, uint64_t* info_host);
 

@@ -158,10 +158,8 @@ extern "C" moe_status moe_cache_create(const moe_config* cfg, const void* host_p
     return fail(MOE_EINVAL, "H and I must be positive multiples of 8");
   if (k.wdtype == MOE_FP8E4M3_B128 && (k.hidden % 128 || k.inter % 128))
     return fail(MOE_EINVAL, "fp8 block-scaled weights need H and I multiples of 128");
-  if (k.wdtype == MOE_NVFP4 || k.wdtype == MOE_MXFP4) {
-    if (k.hidden % 32 || k.inter % 32) return fail(MOE_EINVAL, "fp4 weights need H and I multiples of 32");
-    if (k.max_tokens > 2) return fail(MOE_EINVAL, "fp4 weights serve decode calls of at most 2 tokens");
-  }
+  if ((k.wdtype == MOE_NVFP4 || k.wdtype == MOE_MXFP4) && (k.hidden % 32 || k.inter % 32))
+    return fail(MOE_EINVAL, "fp4 weights need H and I multiples of 32");
   // every slot and host blob starts on a 16-byte boundary (the kernels move 16-byte chunks)
   if (blob_bytes(k.wdtype, k.hidden, k.inter) % 16)
     return fail(MOE_EINVAL, "blob size S = %llu is not a multiple of 16 bytes (fp8: the scale count "
@@ -214,20 +212,16 @@ extern "C" moe_status moe_cache_create(const moe_config* cfg, const void* host_p
     // The resident experts of a decode call run as a gate/up grid then a down +
     // combine grid (the default, "grids"), or, for one-token calls, chosen by
     // MOE_DECODE_RESIDENT when the cache is created: "fused" = one launch with a
-    // grid-wide barrier between the two (also MOE_DECODE_FUSED=1), "stream" = one
-    // launch streaming gate/up and down rows as one expert-major item list.  All
-    // three give the same outputs bit for bit.
+    // grid-wide barrier between the two (also MOE_DECODE_FUSED=1).  Both give the
+    // same outputs bit for bit.
     const char* er = getenv("MOE_DECODE_RESIDENT");
     const char* ef = getenv("MOE_DECODE_FUSED");
     c->resident_mode = 0;
     if (ef && ef[0] == '1') c->resident_mode = 1;
     if (er && strcmp(er, "grids") == 0) c->resident_mode = 0;
     else if (er && strcmp(er, "fused") == 0) c->resident_mode = 1;
-    else if (er && strcmp(er, "stream") == 0) c->resident_mode = 2;
-    else if (er && er[0]) return bail(fail(MOE_EINVAL, "MOE_DECODE_RESIDENT must be grids, fused or stream"));
+    else if (er && er[0]) return bail(fail(MOE_EINVAL, "MOE_DECODE_RESIDENT must be grids or fused"));
   }
-  if ((k.wdtype == MOE_NVFP4 || k.wdtype == MOE_MXFP4) && !fp4_decode_fits(c->sh, k.max_tokens, c->sms))
-    return bail(fail(MOE_EINVAL, "fp4 weights: H / I too large for the bulk decode kernels"));
 
   // host pool: page-lock (mapped) unless it already is
   cudaPointerAttributes attr;
@@ -287,9 +281,7 @@ extern "C" moe_status moe_cache_create(const moe_config* cfg, const void* host_p
                  o_sm = take((size_t)k.max_tokens * k.top_k * 4), o_goff = take((size_t)(max_gpu + 1) * 4),
                  o_gp = take(max_pairs * 4), o_gw = take((size_t)max_gpu * 8),
                  o_h = take(max_pairs * k.inter * 4), o_y = take(max_pairs * k.hidden * 4),
-                 o_arr = take((size_t)k.hidden * 4), o_fb = take(8), o_seq = take(4),
-                 o_hs2 = take(2 * (size_t)max_gpu * k.inter * 4), o_ys2 = take(2 * (size_t)k.top_k * k.hidden * 4),
-                 o_ns = take(4);
+                 o_arr = take((size_t)k.hidden * 4), o_fb = take(8), o_ns = take(4);
     CKB(moe_malloc(&c->work, off));
     CKB(cudaMemset(c->work, 0, off));
     uint8_t* w = static_cast<uint8_t*>(c->work);
@@ -305,18 +297,10 @@ extern "C" moe_status moe_cache_create(const moe_config* cfg, const void* host_p
     c->b.y = reinterpret_cast<float*>(w + o_y);
     c->b.arrive = reinterpret_cast<uint32_t*>(w + o_arr);
     c->b.fused_bar = reinterpret_cast<unsigned long long*>(w + o_fb);
-    c->b.sseq = reinterpret_cast<uint32_t*>(w + o_seq);
-    c->b.hs2 = reinterpret_cast<float*>(w + o_hs2);
-    c->b.ys2 = reinterpret_cast<float*>(w + o_ys2);
-    // one-token calls are the only ones the stream kernel takes; its h and y
-    // buffers start empty
-    c->b.stream = resident_path(c, 1) == 2 ? 1 : 0;
-    CKB(cudaMemset(w + o_hs2, 0xff, 2 * (size_t)max_gpu * k.inter * 4));
-    CKB(cudaMemset(w + o_ys2, 0xff, 2 * (size_t)k.top_k * k.hidden * 4));
     // A test of the bounded waits (MOE_TEST_UNSET_WAIT=1 when the cache is created):
-    // the resident experts' down kernel (or the stream kernel's block-finishing
-    // warps) also waits for a word nothing writes, gives up after 20 ms, flags the
-    // timeout and returns; the next call reports MOE_EDEVICE.  Off unless set.
+    // the resident experts' down kernel also waits for a word nothing writes,
+    // gives up after 20 ms, flags the timeout and returns; the next call reports
+    // MOE_EDEVICE.  Off unless set.
     CKB(cudaMemset(w + o_ns, 0xff, 4));
     c->b.never_set = reinterpret_cast<const float*>(w + o_ns);
     {
@@ -460,10 +444,9 @@ extern "C" moe_status moe_layer_decode(moe_cache* c, int32_t layer, int32_t T, c
     CK(launch_fill_gate_up(c->sh, T, x, b, c->host_pool_dev, c->offsets, c->slots, c->fill_ctas, c->fill_stream));
   }
   if (split) {
-    // Beside a resident launch whose warps wait on one another (the fused launch's
-    // grid barrier, the stream's per-expert counts), the filled-expert grid is a
-    // plain launch: launched early, its CTAs would sit on SMs for the whole fill
-    // and could keep some of that launch's CTAs off the GPU.
+    // Beside the fused resident launch, whose CTAs wait on one another at its grid
+    // barrier, the filled-expert grid is a plain launch: launched early, its CTAs
+    // would sit on SMs for the whole fill and could keep some fused CTAs off the GPU.
     ProfScope p(c, c->fill_stream, PROF_DOWN_FILLED);
     CK(launch_down_split(c->sh, 1, T, w, cpu_part, b, out, c->err_dev, c->sms, c->fill_stream, path == 0));
   }
@@ -472,9 +455,7 @@ extern "C" moe_status moe_layer_decode(moe_cache* c, int32_t layer, int32_t T, c
     {
       // one timed group: the two grids run back to back under a programmatic dependency
       ProfScope p(c, s, PROF_GEMV_RESIDENT);
-      if (path == 2) {
-        CK(launch_resident_stream(c->sh, T, x, w, cpu_part, b, out, c->err_dev, c->sms, s));
-      } else if (path == 1) {
+      if (path == 1) {
         CK(launch_resident_fused(c->sh, T, x, w, cpu_part, b, out, c->err_dev, c->sms, s));
       } else {
         CK(launch_gate_up(c->sh, 0, T, x, b, c->sms, s, c->err_dev));

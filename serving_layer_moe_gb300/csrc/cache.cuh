@@ -57,7 +57,7 @@ struct moe_cache {
   int gemv_grid = 0;
   int fill_ctas = 0;
   // how one-token calls run their resident experts: 0 a gate/up grid then a down +
-  // combine grid, 1 one launch with a grid-wide barrier, 2 one expert-major stream
+  // combine grid, 1 one launch with a grid-wide barrier
   int resident_mode = 0;
   // host pool
   const uint8_t* host_pool = nullptr;
@@ -102,11 +102,10 @@ struct moe_cache {
   size_t prof_used = 0;
 };
 
-// The resident-expert path a call of T tokens takes (0, 1 or 2 as resident_mode;
-// only split-down shapes take 1 or 2, and only where that kernel applies).
+// The resident-expert path a call of T tokens takes (0 or 1 as resident_mode;
+// only split-down shapes take 1, and only where the fused launch applies).
 inline int resident_path(const moe_cache* c, int T) {
   if (!down_split_ok(c->sh, T, c->sms)) return 0;
-  if (c->resident_mode == 2 && resident_stream_ok(c->sh, T, c->sms)) return 2;
   if (c->resident_mode == 1 && resident_fused_ok(c->sh, T, c->sms)) return 1;
   return 0;
 }

@@ -95,16 +95,6 @@ __device__ __forceinline__ unsigned long long key_of_fast(const CtrlArgs& a, con
   return a.cache_keys ? rawkey[s] : (((unsigned long long)a.tab.stamp[s] << kSlotBits) | (unsigned long long)s);
 }
 
-// This call's launch number of the resident stream kernel (one thread; the
-// control kernels of a cache run one after another), or 0 when the call does not
-// run it.  Its parity picks the stream kernel's h / y buffers.
-__device__ __forceinline__ int32_t stream_seq(const CtrlArgs& a) {
-  if (!a.b.stream || a.T != 1) return 0;
-  const uint32_t n = *a.b.sseq + 1u;
-  *a.b.sseq = n;
-  return (int32_t)(n & 0x7fffffffu);
-}
-
 // shared scalars of the control CTA
 struct CtrlScalars {
   int bad, u, h, m, q, keff, ncand, digit, kth, read_hits, read_misses, pool_n, enough;
@@ -311,7 +301,6 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
         int32_t* pl = a.b.plan;
         pl[P_LAYER] = a.layer; pl[P_U] = u; pl[P_H] = h; pl[P_M] = m; pl[P_Q] = q;
         pl[P_NCPU] = m - q; pl[P_NGPU] = ngpu; pl[P_NFIRST] = nfirst;
-        pl[P_SEQ] = stream_seq(a);
         unsigned long long* cn = reinterpret_cast<unsigned long long*>(a.tab.counters);
         atomicAdd(cn + 0, (unsigned long long)h);
         atomicAdd(cn + 1, (unsigned long long)m);
@@ -681,7 +670,6 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
     int32_t* pl = a.b.plan;
     pl[P_LAYER] = a.layer; pl[P_U] = u; pl[P_H] = h; pl[P_M] = m; pl[P_Q] = q;
     pl[P_NCPU] = m - q; pl[P_NGPU] = ngpu; pl[P_NFIRST] = nfirst;
-    pl[P_SEQ] = stream_seq(a);
     // reductions, not read-modify-writes: nothing waits for the old values
     unsigned long long* c = reinterpret_cast<unsigned long long*>(a.tab.counters);
     atomicAdd(c + 0, (unsigned long long)h); atomicAdd(c + 1, (unsigned long long)m);

@@ -376,35 +376,53 @@ __global__ void __launch_bounds__(kGemvThreads, kTokGroup == 1 ? 2 : 1) gate_up_
         for (int j = 0; j < kChunksPerLane; ++j) {
           const int c = seg + j * 32 + lane;
           if (c < NCH) {
-            float fg[V], fu[V];
-            F::unpack(wg[j], fg);
-            F::unpack(wu[j], fu);
-            float scg = 1.f, scu = 1.f;
-            if (WT == MOE_FP8E4M3_B128) {
-              const int cb = (c * V) >> 7;
-              scg = __ldg(sgu + (size_t)(i >> 7) * HB + cb);
-              scu = __ldg(sgu + (size_t)((I + i) >> 7) * HB + cb);
-            }
+            if constexpr (kFp4<WT>) {   // the chunk dot product of every 4-bit path, with its block scales
+              const auto* srow = reinterpret_cast<const typename F::scale_t*>(wb + F::sgu_off(H, I));
+              const uint32_t s2g = __ldg(srow + (size_t)i * (H / 32) + c);
+              const uint32_t s2u = __ldg(srow + (size_t)(I + i) * (H / 32) + c);
 #pragma unroll
-            for (int n = 0; n < kTokGroup; ++n) {
-              if (n < nt) {
-                float xv[V];
-                load_x<AT, V>(xs, (size_t)tok[n] * H + (size_t)c * V, xv);
-                float dg = 0.f, du = 0.f;
+              for (int n = 0; n < kTokGroup; ++n) {
+                if (n < nt) {
+                  float xv[V];
+                  load_x<AT, V>(xs, (size_t)tok[n] * H + (size_t)c * V, xv);
+                  ag[n] += F::dot(wg[j], s2g, xv);
+                  au[n] += F::dot(wu[j], s2u, xv);
+                }
+              }
+            } else {
+              float fg[V], fu[V];
+              F::unpack(wg[j], fg);
+              F::unpack(wu[j], fu);
+              float scg = 1.f, scu = 1.f;
+              if (WT == MOE_FP8E4M3_B128) {
+                const int cb = (c * V) >> 7;
+                scg = __ldg(sgu + (size_t)(i >> 7) * HB + cb);
+                scu = __ldg(sgu + (size_t)((I + i) >> 7) * HB + cb);
+              }
 #pragma unroll
-                for (int v = 0; v < V; ++v) { dg = fmaf(fg[v], xv[v], dg); du = fmaf(fu[v], xv[v], du); }
-                ag[n] = fmaf(dg, scg, ag[n]);
-                au[n] = fmaf(du, scu, au[n]);
+              for (int n = 0; n < kTokGroup; ++n) {
+                if (n < nt) {
+                  float xv[V];
+                  load_x<AT, V>(xs, (size_t)tok[n] * H + (size_t)c * V, xv);
+                  float dg = 0.f, du = 0.f;
+#pragma unroll
+                  for (int v = 0; v < V; ++v) { dg = fmaf(fg[v], xv[v], dg); du = fmaf(fu[v], xv[v], du); }
+                  ag[n] = fmaf(dg, scg, ag[n]);
+                  au[n] = fmaf(du, scu, au[n]);
+                }
               }
             }
           }
         }
       }
+      float gg = 1.f;
+      if constexpr (WT == MOE_NVFP4) gg = __ldg(reinterpret_cast<const float*>(wb + F::g_off(H, I)));   // W_gu's scale
 #pragma unroll
       for (int n = 0; n < kTokGroup; ++n) {
         if (n < nt) {
-          const float sg = warp_sum(ag[n]);
-          const float su = warp_sum(au[n]);
+          float sg = warp_sum(ag[n]);
+          float su = warp_sum(au[n]);
+          if constexpr (WT == MOE_NVFP4) { sg *= gg; su *= gg; }
           if (lane == 0) a.b.h[(size_t)sp.pid[tp + n] * I + i] = silu(sg) * su;
         }
       }
@@ -608,28 +626,44 @@ __global__ void __launch_bounds__(kGemvThreads, kTokGroup == 1 ? 2 : 1) down_ker
         for (int j = 0; j < kChunksPerLane; ++j) {
           const int c = seg + j * 32 + lane;
           if (c < NCH) {
-            float fw[V];
-            F::unpack(w[j], fw);
-            float sc = 1.f;
-            if (WT == MOE_FP8E4M3_B128) sc = __ldg(sd + (size_t)(row >> 7) * IB + ((c * V) >> 7));
+            if constexpr (kFp4<WT>) {   // the chunk dot product of every 4-bit path, with its block scales
+              const auto* srow = reinterpret_cast<const typename F::scale_t*>(wb + sd_off);
+              const uint32_t s2 = __ldg(srow + (size_t)row * (I / 32) + c);
 #pragma unroll
-            for (int n = 0; n < kTokGroup; ++n) {
-              if (n < nt) {
-                float hv[V];
-                load_act_f32<V>(a.b.h + (size_t)pid[n] * I + (size_t)c * V, hv);
-                float d = 0.f;
+              for (int n = 0; n < kTokGroup; ++n) {
+                if (n < nt) {
+                  float hv[V];
+                  load_act_f32<V>(a.b.h + (size_t)pid[n] * I + (size_t)c * V, hv);
+                  acc[n] += F::dot(w[j], s2, hv);
+                }
+              }
+            } else {
+              float fw[V];
+              F::unpack(w[j], fw);
+              float sc = 1.f;
+              if (WT == MOE_FP8E4M3_B128) sc = __ldg(sd + (size_t)(row >> 7) * IB + ((c * V) >> 7));
 #pragma unroll
-                for (int v = 0; v < V; ++v) d = fmaf(fw[v], hv[v], d);
-                acc[n] = fmaf(d, sc, acc[n]);
+              for (int n = 0; n < kTokGroup; ++n) {
+                if (n < nt) {
+                  float hv[V];
+                  load_act_f32<V>(a.b.h + (size_t)pid[n] * I + (size_t)c * V, hv);
+                  float d = 0.f;
+#pragma unroll
+                  for (int v = 0; v < V; ++v) d = fmaf(fw[v], hv[v], d);
+                  acc[n] = fmaf(d, sc, acc[n]);
+                }
               }
             }
           }
         }
       }
+      float gd = 1.f;
+      if constexpr (WT == MOE_NVFP4) gd = __ldg(reinterpret_cast<const float*>(wb + F::g_off(H, I)) + 1);   // W_d's scale
 #pragma unroll
       for (int n = 0; n < kTokGroup; ++n) {
         if (n < nt) {
-          const float s = warp_sum(acc[n]);
+          float s = warp_sum(acc[n]);
+          if constexpr (WT == MOE_NVFP4) s *= gd;
           if (lane == 0) a.b.y[(size_t)pid[n] * H + row] = s;
         }
       }
@@ -889,40 +923,6 @@ __device__ __forceinline__ float reduce8(float (&v)[8], int lane) {
   v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
   return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
 }
-
-// The same for 4 values: afterwards lane l holds the full sum of value (l >> 3) & 3;
-// and for 2 values: value (l >> 4) & 1.  Same lane pairing as above.
-__device__ __forceinline__ float reduce4(float (&v)[4], int lane) {
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const bool hi = lane & 16;
-    const float send = hi ? v[j] : v[j + 2];
-    v[j] = (hi ? v[j + 2] : v[j]) + __shfl_xor_sync(0xffffffffu, send, 16);
-  }
-  {
-    const bool hi = lane & 8;
-    const float send = hi ? v[0] : v[1];
-    v[0] = (hi ? v[1] : v[0]) + __shfl_xor_sync(0xffffffffu, send, 8);
-  }
-  v[0] += __shfl_xor_sync(0xffffffffu, v[0], 4);
-  v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
-  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
-}
-__device__ __forceinline__ float reduce2(float (&v)[2], int lane) {
-  {
-    const bool hi = lane & 16;
-    const float send = hi ? v[0] : v[1];
-    v[0] = (hi ? v[1] : v[0]) + __shfl_xor_sync(0xffffffffu, send, 16);
-  }
-  v[0] += __shfl_xor_sync(0xffffffffu, v[0], 8);
-  v[0] += __shfl_xor_sync(0xffffffffu, v[0], 4);
-  v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
-  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
-}
-template <int N> __device__ __forceinline__ float reduce_rows(float (&v)[N], int lane);
-template <> __device__ __forceinline__ float reduce_rows<2>(float (&v)[2], int lane) { return reduce2(v, lane); }
-template <> __device__ __forceinline__ float reduce_rows<4>(float (&v)[4], int lane) { return reduce4(v, lane); }
-template <> __device__ __forceinline__ float reduce_rows<8>(float (&v)[8], int lane) { return reduce8(v, lane); }
 
 constexpr int kDownRows = 16;   // output rows per CTA of the bulk down kernel, at most
 constexpr size_t kPrefetchPiece = 32 * 1024;
@@ -1718,378 +1718,6 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 2) resident_fused_kernel(Gem
   if (missing) atomicOr_system(err, kErrMissingCpuPart);
 }
 
-// ---- resident experts, one token: gate/up and down rows as one expert-major stream --------
-// One bf16 token, bf16 weights, no shared expert.  Every byte the resident
-// experts need flows through the per-warp rings of one item list, and warp w of
-// the grid takes items w, w + warps, ...:
-//   items [0, ng*I): gate row i + up row i of expert g (n = g*I + i), so the
-//     experts' h complete one after another;
-//   then rounds of down items: in every round column c (the warp that owns it)
-//     takes RS rows of expert c mod ng's W_down, the next sub-block of that
-//     expert in each round.  A warp thus stays on one expert for all its down
-//     items and reads that expert's h once, into registers.
-// Weight copies do not depend on h, so lane 0 keeps NS items in flight whatever
-// they are; only the arithmetic of a down item waits, for its expert's h.
-// Every gate/up item precedes every down item and an item only waits for items
-// before it, so no wait can close a cycle.  The down projection runs inside
-// the weight stream instead of after a grid-wide barrier.
-//
-// No fences or counters order the items: h and y of the resident pairs live in
-// two buffers per cache, used by alternate launches (the parity of the launch
-// number the control kernel writes), and a launch sets the other buffers to the
-// empty mark for the next one.  A value is published by storing it; a reader
-// takes a value once it is not the empty mark (4-byte stores and loads are
-// single-copy atomic).  A warp's first down item copies its expert's h into the
-// stage with its rows; entries still empty then are re-read from L2, 8 at a
-// time, until written.  The warp holding the last sub-block of the last
-// expert's rows of row block b waits in the same way for every resident y of
-// that block, stores them to y for the caller and the filled-expert grid, and
-// forms the block's combine, or joins the split protocol with the filled-expert
-// down grid (both count themselves in arrive[b]; the second forms the combine).
-// Arithmetic order is that of gate_up_bulk_kernel and down_bulk_kernel
-// (per-lane chunk sums, the same shuffle tree), so h, y and the layer output
-// are bit-identical to the two grids'.  Every wait is bounded by the global timer.
-constexpr int kStreamWarps = 8;
-
-struct StreamGeom {
-  int NS;            // ring stages per warp
-  int R, nblk;       // row blocks of the split down protocol: rows per block, blocks
-  int RS, Q;         // rows per down item, down items per (expert, row block)
-  size_t SB;         // stage bytes: a gate/up row pair, or RS down rows + the expert's h
-  size_t ring_off, plan_off, x_off, extra_off, smem;
-};
-
-__device__ __forceinline__ bool stream_empty(float v) { return __float_as_uint(v) == kStreamEmpty; }
-
-__device__ __forceinline__ float ld_relaxed_f32(const float* p) {
-  float v;
-  asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ float4 ld_relaxed_f32x4(const float* p) {
-  float4 v;
-  asm volatile("ld.relaxed.gpu.global.v4.f32 {%0,%1,%2,%3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ bool any_empty8(const float* v) {
-  bool e = false;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) e |= stream_empty(v[i]);
-  return e;
-}
-
-template <int kJX, int kJN, int kRS>
-__global__ void __launch_bounds__(kStreamWarps * 32, 1) resident_stream_kernel(GemvArgs a, StreamGeom geo,
-                                                                              const float* __restrict__ w,
-                                                                              const float* __restrict__ cpu,
-                                                                              float* __restrict__ out, uint32_t* err) {
-  using F = WFmt<MOE_BF16>;
-  constexpr int V = 8;
-  extern __shared__ __align__(128) uint8_t sm[];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm) + warp * geo.NS;
-  uint8_t* ring = sm + geo.ring_off + (size_t)warp * geo.NS * geo.SB;
-  if (lane == 0) {
-    for (int i = 0; i < geo.NS; ++i) bar_init(&bars[i]);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  pdl_wait();
-  pdl_trigger();
-  const StagedPlan sp = stage_plan(sm + geo.plan_off, a);
-  const int H = a.H, I = a.I, k = a.k;
-  const int nfirst = a.b.plan[P_NFIRST], ngpu = a.b.plan[P_NGPU];
-  const int par = a.b.plan[P_SEQ] & 1;
-  const bool skip = nfirst == 0 && ngpu > 0;   // only filled experts: their grid combines alone
-  const bool alone = ngpu == nfirst;           // no filled expert: this kernel combines alone
-  const int ng = skip ? 0 : nfirst;
-  const size_t hn = (size_t)a.max_g * I, yn = (size_t)k * H;   // floats per h / y buffer
-  float* hb = a.b.hs2 + (size_t)par * hn;                      // this launch's h ...
-  float* yb = a.b.ys2 + (size_t)par * yn;                      // ... and y
-  const long nwarps = (long)gridDim.x * kStreamWarps;
-  const long w0 = (long)blockIdx.x * kStreamWarps + warp;
-  int* s_slot = reinterpret_cast<int*>(sm + geo.extra_off);
-  float* s_wt = reinterpret_cast<float*>(s_slot + k);
-  uint8_t* xsm = sm + geo.x_off;
-  for (int i = threadIdx.x; i < k; i += blockDim.x) { s_slot[i] = a.b.slot_map[i]; s_wt[i] = w[i]; }
-  __syncthreads();   // the staged plan
-  const size_t row_h = F::row(H), row_i = F::row(I);
-  const size_t down_off = 2ull * (size_t)I * row_h;
-  const size_t hbytes = (size_t)I * 4;
-  const int per_e = geo.nblk * geo.Q;                  // down items of one expert
-  const int cpe = ng > 0 ? (int)(nwarps / ng) : 0;     // down columns of one expert
-  const int drounds = cpe > 0 ? (per_e + cpe - 1) / cpe : 0;
-  const long n_gu = (long)ng * I;
-  const long items = n_gu + (long)drounds * nwarps;
-  const uint64_t pol = evict_first_policy();
-  bool missing = false;
-
-  struct DownItem { int g, b, q, r0, nr; };   // g < 0: no item in this slot
-  auto down_item = [&](long it) {
-    DownItem d{-1, 0, 0, 0, 0};
-    const long m = it - n_gu;
-    const int c = (int)(m % nwarps), r = (int)(m / nwarps);
-    if (c >= cpe * ng) return d;
-    const int j = r * cpe + c / ng;
-    if (j >= per_e) return d;
-    d.g = c % ng;
-    d.b = j / geo.Q;
-    d.q = j - d.b * geo.Q;
-    d.r0 = d.b * geo.R + d.q * geo.RS;
-    d.nr = min(geo.RS, min(geo.R, H - d.b * geo.R) - d.q * geo.RS);
-    return d;
-  };
-  long last_issued[4] = {-1, -1, -1, -1};
-  bool h_sent = false;   // lane 0: this warp's expert's h went out with an earlier down item
-  auto issue = [&](long it, int st) {   // lane 0 only
-    last_issued[st] = it;
-    uint8_t* dst = ring + (size_t)st * geo.SB;
-    if (it < n_gu) {
-      const int g = (int)(it / I), i = (int)(it % I);
-      bar_expect(&bars[st], (uint32_t)(2 * row_h));
-      bulk_copy(dst, sp.w[g] + (size_t)i * row_h, (uint32_t)row_h, &bars[st], pol);
-      bulk_copy(dst + row_h, sp.w[g] + (size_t)(I + i) * row_h, (uint32_t)row_h, &bars[st], pol);
-      return;
-    }
-    const DownItem d = down_item(it);
-    if (d.g < 0 || d.nr <= 0) {   // no rows here
-      bar_expect(&bars[st], 0u);
-      return;
-    }
-    const uint32_t wb = (uint32_t)(d.nr * row_i);
-    bar_expect(&bars[st], wb + (h_sent ? 0u : (uint32_t)hbytes));
-    bulk_copy(dst, sp.w[d.g] + down_off + (size_t)d.r0 * row_i, wb, &bars[st], pol);
-    if (!h_sent)   // the expert's h as it stands (checked entry by entry before use)
-      bulk_copy_keep(dst + (size_t)geo.RS * row_i, hb + (size_t)d.g * I, (uint32_t)hbytes, &bars[st]);
-    h_sent = true;
-  };
-  const long n_mine = items > w0 ? (items - w0 + nwarps - 1) / nwarps : 0;
-  if (lane == 0)
-    for (int kk = 0; kk < geo.NS && kk < n_mine; ++kk) issue(w0 + (long)kk * nwarps, kk);
-  {
-    // x while the first copies are in flight; and the other h / y buffers emptied
-    // for the next launch (the launch before this one, which used them, is complete)
-    uint4* dst = reinterpret_cast<uint4*>(xsm);
-    const uint4* src = reinterpret_cast<const uint4*>(a.x);
-    for (int i = threadIdx.x; i < H / 8; i += blockDim.x) dst[i] = src[i];
-    float* ho = a.b.hs2 + (size_t)(par ^ 1) * hn;
-    float* yo = a.b.ys2 + (size_t)(par ^ 1) * yn;
-    const float e = __uint_as_float(kStreamEmpty);
-    for (size_t i = (size_t)(w0 * 32 + lane); i < hn + yn; i += (size_t)nwarps * 32) {
-      if (i < hn) ho[i] = e;
-      else yo[i - hn] = e;
-    }
-  }
-  __syncthreads();
-
-  // Row block b: wait for every resident y of the block, store it to y, then form
-  // out[r] = sum_j w[j] * (slot >= 0 ? y : cpu) (or leave it to the filled-expert
-  // grid when that one arrives second).  false after the wait limit.
-  auto finish_block = [&](int b) -> bool {
-    if (a.b.test_wait) {   // a wait that runs out: the word is never written
-      bool set = false;
-      if (lane == 0) {
-        const unsigned long long t0 = gtime();
-        for (uint32_t n = 0; !set; ++n) {
-          set = !stream_empty(ld_relaxed_f32(a.b.never_set));
-          if ((n & 15u) == 15u && gtime() - t0 > kTestWaitNs) break;
-        }
-      }
-      if (!__shfl_sync(0xffffffffu, (int)set, 0)) return false;
-    }
-    const int rb = b * geo.R;
-    const int nrb = min(geo.R, H - rb);
-    constexpr int kPer = (kStreamWarps * 2 * 16 + 31) / 32;   // entries per lane: 8 experts x 16 rows at most
-    float v[kPer];
-    size_t o[kPer];
-    int pidv[kPer];
-#pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-      const int e = lane + 32 * u;
-      o[u] = 0;
-      pidv[u] = -1;
-      v[u] = 0.f;
-      if (e < ng * nrb) {
-        const int g = e / nrb, r = rb + e % nrb;
-        pidv[u] = sp.pid[sp.off[g]];
-        o[u] = (size_t)pidv[u] * H + r;
-        v[u] = ld_relaxed_f32(yb + o[u]);
-      }
-    }
-    bool done = true;
-    {
-      const unsigned long long t0 = gtime();
-      for (uint32_t n = 0;; ++n) {
-        bool again = false;
-#pragma unroll
-        for (int u = 0; u < kPer; ++u)
-          if (pidv[u] >= 0 && stream_empty(v[u])) { v[u] = ld_relaxed_f32(yb + o[u]); again = true; }
-        if (!again) break;
-        if ((n & 15u) == 15u && gtime() - t0 > kBulkWaitNs) { done = false; break; }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kPer; ++u)
-      if (pidv[u] >= 0) a.b.y[o[u]] = v[u];   // per-pair output stays readable (moe_cache_get_plan)
-    if (!__all_sync(0xffffffffu, done)) return false;
-    __syncwarp();   // the y stores above precede lane 0's release and the combine's loads
-    if (a.b.defer_combine) return true;   // the combine runs after the CPU branch
-    bool second = true;
-    if (!alone) {
-      uint32_t old = 0;
-      if (lane == 0)
-        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(a.b.arrive + b) : "memory");
-      second = (__shfl_sync(0xffffffffu, old, 0) & 1u) != 0u;
-    }
-    if (!second) return true;
-    if (lane < nrb) {
-      const int r = rb + lane;
-      float acc = 0.f;
-      for (int j = 0; j < k; ++j) {
-        float vv;
-        if (s_slot[j] >= 0) {
-          vv = __ldcg(a.b.y + (size_t)j * H + r);
-        } else if (cpu != nullptr) {
-          vv = __ldg(cpu + (size_t)j * H + r);
-        } else {
-          vv = 0.f;
-          missing = true;
-        }
-        acc = fmaf(s_wt[j], vv, acc);
-      }
-      out[r] = acc;
-    }
-    return true;
-  };
-
-  if (ng == 0) {   // every pair on the CPU (or only filled experts: their grid combines)
-    if (!skip)
-      for (long b = w0; b < geo.nblk; b += nwarps) finish_block((int)b);
-    if (missing) atomicOr_system(err, kErrMissingCpuPart);
-    return;
-  }
-
-  // the warp is done reading stage st (item it): lane 0 refills it with the item NS ahead
-  auto rearm = [&](long it, int st) {
-    __syncwarp();
-    if (lane == 0 && it + (long)geo.NS * nwarps < items) {
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      issue(it + (long)geo.NS * nwarps, st);
-    }
-  };
-  uint4 xr[kJX];
-#pragma unroll
-  for (int j = 0; j < kJX; ++j) xr[j] = reinterpret_cast<const uint4*>(xsm)[j * 32 + lane];
-  float hv[kJN][V];       // the h of this warp's down expert, once loaded
-  bool h_loaded = false;
-  bool ok = true;
-  int kk = 0;
-  for (long it = w0; it < items; it += nwarps, ++kk) {
-    const int st = kk % geo.NS;
-    if (!__all_sync(0xffffffffu, bar_wait(&bars[st], (uint32_t)((kk / geo.NS) & 1)))) { ok = false; break; }
-    const uint8_t* stage = ring + (size_t)st * geo.SB;
-    if (it < n_gu) {
-      const int g = (int)(it / I), i = (int)(it % I);
-      const uint4* gate = reinterpret_cast<const uint4*>(stage);
-      const uint4* up = reinterpret_cast<const uint4*>(stage + row_h);
-      float ag = 0.f, au = 0.f;   // the per-chunk partials and order of gate_up_bulk_kernel
-#pragma unroll
-      for (int j = 0; j < kJX; ++j) {
-        const uint4 wg = gate[j * 32 + lane], wu = up[j * 32 + lane];
-        float pg = 0.f, pu = 0.f;
-        pg = fma_bf16x2(wg.x, xr[j].x, pg); pu = fma_bf16x2(wu.x, xr[j].x, pu);
-        pg = fma_bf16x2(wg.y, xr[j].y, pg); pu = fma_bf16x2(wu.y, xr[j].y, pu);
-        pg = fma_bf16x2(wg.z, xr[j].z, pg); pu = fma_bf16x2(wu.z, xr[j].z, pu);
-        pg = fma_bf16x2(wg.w, xr[j].w, pg); pu = fma_bf16x2(wu.w, xr[j].w, pu);
-        ag += pg;
-        au += pu;
-      }
-      ag = warp_sum(ag);
-      au = warp_sum(au);
-      rearm(it, st);
-      if (lane == 0) {
-        const float h1 = silu(ag) * au;
-        asm volatile("st.relaxed.gpu.global.f32 [%0], %1;" ::"l"(hb + (size_t)g * I + i), "f"(h1) : "memory");
-      }
-      continue;
-    }
-    const DownItem d = down_item(it);
-    if (d.g >= 0 && d.nr > 0) {
-      const int pid = sp.pid[sp.off[d.g]];
-      if (!h_loaded) {
-        // the expert's h from the stage; entries still empty when it was copied
-        // are re-read from L2, 8 at a time, until written
-        const float* hsm = reinterpret_cast<const float*>(stage + (size_t)geo.RS * row_i);
-        const float* hg = hb + (size_t)d.g * I;
-#pragma unroll
-        for (int j = 0; j < kJN; ++j) {
-          const float4* hp = reinterpret_cast<const float4*>(hsm + (size_t)(j * 32 + lane) * V);
-          const float4 q0 = hp[0], q1 = hp[1];
-          hv[j][0] = q0.x; hv[j][1] = q0.y; hv[j][2] = q0.z; hv[j][3] = q0.w;
-          hv[j][4] = q1.x; hv[j][5] = q1.y; hv[j][6] = q1.z; hv[j][7] = q1.w;
-        }
-        bool hok = true;
-        const unsigned long long t0 = gtime();
-        for (uint32_t n = 0;; ++n) {
-          bool again = false;
-#pragma unroll
-          for (int j = 0; j < kJN; ++j) {
-            if (any_empty8(hv[j])) {
-              const float* src = hg + (size_t)(j * 32 + lane) * V;
-              const float4 q0 = ld_relaxed_f32x4(src), q1 = ld_relaxed_f32x4(src + 4);
-              hv[j][0] = q0.x; hv[j][1] = q0.y; hv[j][2] = q0.z; hv[j][3] = q0.w;
-              hv[j][4] = q1.x; hv[j][5] = q1.y; hv[j][6] = q1.z; hv[j][7] = q1.w;
-              again = true;
-            }
-          }
-          if (!again) break;
-          if ((n & 15u) == 15u && gtime() - t0 > kBulkWaitNs) { hok = false; break; }
-        }
-        if (!__all_sync(0xffffffffu, hok)) { ok = false; break; }
-        h_loaded = true;
-      }
-      // the straight-line rows of down_bulk_kernel: rows past nr repeat the last
-      // row (never stored), per-lane sums in the same order, the same shuffle tree
-      float acc[kRS];
-#pragma unroll
-      for (int r = 0; r < kRS; ++r) {
-        const int rr = r < d.nr ? r : d.nr - 1;
-        const uint4* wrow = reinterpret_cast<const uint4*>(stage + (size_t)rr * row_i);
-        float dsum = 0.f;
-#pragma unroll
-        for (int j = 0; j < kJN; ++j) {
-          float fw[V];
-          F::unpack(wrow[j * 32 + lane], fw);
-          float dj = 0.f;
-#pragma unroll
-          for (int v = 0; v < V; ++v) dj = fmaf(fw[v], hv[j][v], dj);
-          dsum += dj;
-        }
-        acc[r] = 0.f + dsum;
-      }
-      const float v = reduce_rows<kRS>(acc, lane);
-      const int r = (lane >> (5 - (kRS == 2 ? 1 : kRS == 4 ? 2 : 3))) & (kRS - 1);
-      if ((lane & (32 / kRS - 1)) == 0 && r < d.nr)
-        asm volatile("st.relaxed.gpu.global.f32 [%0], %1;" ::"l"(yb + (size_t)pid * H + d.r0 + r), "f"(v) : "memory");
-    }
-    rearm(it, st);
-    // the last sub-block of the last expert's rows of a block finishes the block
-    if (d.g == ng - 1 && d.q == geo.Q - 1 && !finish_block(d.b)) { ok = false; break; }
-  }
-  if (!ok && lane == 0) {   // flag the timeout; this warp's copies land before the CTA exits
-    atomicOr_system(err, kErrTimeout);
-    for (int s2 = 0; s2 < geo.NS; ++s2) {
-      if (last_issued[s2] < 0) continue;
-      const long k2 = (last_issued[s2] - w0) / nwarps;
-      const uint32_t par2 = (uint32_t)((k2 / geo.NS) & 1);
-      const unsigned long long t0 = gtime();
-      while (!bar_test(&bars[s2], par2) && gtime() - t0 < kBulkWaitNs) {
-      }
-    }
-  }
-  if (missing) atomicOr_system(err, kErrMissingCpuPart);
-}
-
 // ---- combine: out[t] = sum_j w[t,j] * (slot >= 0 ? y : cpu_part) in j order (+ shared) --
 __global__ void combine_kernel(int T, int H, int k, int n_shared, const float* __restrict__ w,
                                const int32_t* __restrict__ sm, const float* __restrict__ y,
@@ -2322,11 +1950,7 @@ cudaError_t setup_gemv_kernels() {
     if (e != cudaSuccess) return e;
   }
   for (const void* k : {(const void*)resident_fused_kernel<8, 3>, (const void*)resident_fused_kernel<8, 4>,
-                        (const void*)resident_fused_kernel<4, 3>, (const void*)resident_fused_kernel<4, 4>,
-                        (const void*)resident_stream_kernel<8, 3, 4>, (const void*)resident_stream_kernel<8, 3, 2>,
-                        (const void*)resident_stream_kernel<8, 4, 4>, (const void*)resident_stream_kernel<8, 4, 2>,
-                        (const void*)resident_stream_kernel<4, 3, 4>, (const void*)resident_stream_kernel<4, 3, 2>,
-                        (const void*)resident_stream_kernel<4, 4, 4>, (const void*)resident_stream_kernel<4, 4, 2>}) {
+                        (const void*)resident_fused_kernel<4, 3>, (const void*)resident_fused_kernel<4, 4>}) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFusedSmemMax);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, kDecodeCarveout);
     if (e != cudaSuccess) return e;
@@ -2344,6 +1968,10 @@ cudaError_t setup_gemv_kernels() {
   if (e == cudaSuccess) e = carveout_typed<MOE_BF16, MOE_BF16>();
   if (e == cudaSuccess) e = carveout_typed<MOE_FP8E4M3_B128, MOE_F32>();
   if (e == cudaSuccess) e = carveout_typed<MOE_FP8E4M3_B128, MOE_BF16>();
+  if (e == cudaSuccess) e = carveout_typed<MOE_NVFP4, MOE_F32>();
+  if (e == cudaSuccess) e = carveout_typed<MOE_NVFP4, MOE_BF16>();
+  if (e == cudaSuccess) e = carveout_typed<MOE_MXFP4, MOE_F32>();
+  if (e == cudaSuccess) e = carveout_typed<MOE_MXFP4, MOE_BF16>();
   return e;
 }
 
@@ -2490,7 +2118,11 @@ cudaError_t launch_gate_up(const Shape& sh, int pass, int T, const void* x, Deco
       }
     }
   }
-  switch (sh.wdtype * 2 + sh.adtype) {   // register-staged kernels (no NVFP4: the create call rules it out)
+  switch (sh.wdtype * 2 + sh.adtype) {   // register-staged kernels
+    case MOE_NVFP4 * 2 + MOE_F32: return launch_gate_up_typed<MOE_NVFP4, MOE_F32>(a, sms, s);
+    case MOE_NVFP4 * 2 + MOE_BF16: return launch_gate_up_typed<MOE_NVFP4, MOE_BF16>(a, sms, s);
+    case MOE_MXFP4 * 2 + MOE_F32: return launch_gate_up_typed<MOE_MXFP4, MOE_F32>(a, sms, s);
+    case MOE_MXFP4 * 2 + MOE_BF16: return launch_gate_up_typed<MOE_MXFP4, MOE_BF16>(a, sms, s);
     case MOE_F32 * 2 + MOE_F32: return launch_gate_up_typed<MOE_F32, MOE_F32>(a, sms, s);
     case MOE_F32 * 2 + MOE_BF16: return launch_gate_up_typed<MOE_F32, MOE_BF16>(a, sms, s);
     case MOE_BF16 * 2 + MOE_F32: return launch_gate_up_typed<MOE_BF16, MOE_F32>(a, sms, s);
@@ -2553,13 +2185,6 @@ cudaError_t launch_down_bulk_any(const Shape& sh, const GemvArgs& a, const BulkG
   return launch_down_bulk<MOE_FP8E4M3_B128>(a, geo, ring, pdl, w, cpu, out, err, s);
 }
 
-bool fp4_decode_fits(const Shape& sh, int max_tokens, int sms) {
-  for (int T = 1; T <= max_tokens; ++T) {
-    const GemvArgs a = make_args(sh, 0, T, nullptr, DecodeBufs{});
-    if (gate_up_geom(a, sh.wdtype, sh.adtype, sms).NS < 2 || !down_split_ok(sh, T, sms)) return false;
-  }
-  return true;
-}
 
 // The bulk down kernel runs when its ring fits and every pair's h fits in
 // shared memory, or, for one token, when only the ring fits: each warp then
@@ -2585,7 +2210,8 @@ cudaError_t launch_down_split(const Shape& sh, int pass, int T, const float* w, 
 int down_combine_launches(const Shape& sh, int T, int sms) {
   const GemvArgs a = make_args(sh, 2, T, nullptr, DecodeBufs{});
   const BulkGeom geo = down_geom(a, sh.wdtype, sms);
-  if ((geo.NS >= 1 && geo.h_smem) || down_combine_fits(sh, T)) return 1;
+  if (geo.NS >= 1 && geo.h_smem) return 1;
+  if (down_combine_fits(sh, T) && sh.wdtype != MOE_NVFP4 && sh.wdtype != MOE_MXFP4) return 1;
   return 2;
 }
 
@@ -2638,63 +2264,6 @@ cudaError_t launch_resident_fused(const Shape& sh, int T, const void* x, const f
 }
 
 
-// Geometry of resident_stream_kernel, or NS = 0 when the call does not take it:
-// bf16 weights and activations, one token, no shared expert, gate/up rows of 4 or
-// 8 16-byte chunks per lane, W_down rows of 3 or 4, and the row blocks of the
-// split down kernels (the filled-expert grid's combine protocol counts per block).
-// A stage holds a gate/up row pair, or RS down rows plus the expert's h.
-StreamGeom stream_geom(const GemvArgs& a, int wdtype, int adtype, int sms) {
-  StreamGeom g{};
-  if (wdtype != MOE_BF16 || adtype != MOE_BF16 || a.T != 1 || a.n_shared != 0) return g;
-  if (a.H % 256 != 0 || (a.H / 256 != 4 && a.H / 256 != 8) || a.I % 256 != 0 || (a.I / 256 != 3 && a.I / 256 != 4))
-    return g;
-  if (a.max_g > kStreamWarps * 2) return g;   // finish_block reads at most 16 experts' rows per lane group
-  const BulkGeom dg = down_geom(a, wdtype, sms);
-  if (dg.NS < 1 || dg.R < 1 || dg.R > 16) return g;
-  g.R = dg.R;
-  g.nblk = dg.grid;
-  const size_t row_h = wrow(MOE_BF16, (size_t)a.H), row_i = wrow(MOE_BF16, (size_t)a.I), hb = (size_t)a.I * 4;
-  // 4 rows per down item where they and h fit in about a gate/up row pair, else 2
-  g.RS = (4 * row_i + hb <= 2 * row_h + 1024) ? 4 : 2;
-  if (g.RS > g.R) g.RS = g.R >= 2 ? 2 : 1;
-  if (g.RS != 2 && g.RS != 4) return g;
-  g.Q = (g.R + g.RS - 1) / g.RS;
-  g.SB = up128(std::max(2 * row_h, hb + (size_t)g.RS * row_i));
-  const size_t plan = up128(staged_plan_bytes(a.max_g, a.max_p));
-  const size_t xb = up128((size_t)a.H * 2);
-  const size_t extra = up128((size_t)a.k * 8);
-  g.ring_off = 256;
-  for (g.NS = 3; g.NS >= 2; --g.NS) {
-    g.plan_off = g.ring_off + (size_t)kStreamWarps * g.NS * g.SB;
-    g.x_off = g.plan_off + plan;
-    g.extra_off = g.x_off + xb;
-    g.smem = g.extra_off + extra;
-    if (g.smem <= kFusedSmemMax) return g;
-  }
-  g.NS = 0;
-  return g;
-}
-
-bool resident_stream_ok(const Shape& sh, int T, int sms) {
-  const GemvArgs a = make_args(sh, 0, T, nullptr, DecodeBufs{});
-  return stream_geom(a, sh.wdtype, sh.adtype, sms).NS > 0;
-}
-
-cudaError_t launch_resident_stream(const Shape& sh, int T, const void* x, const float* w, const float* cpu_part,
-                                   DecodeBufs b, float* out, uint32_t* err, int sms, cudaStream_t s) {
-  const GemvArgs a = make_args(sh, 0, T, x, b);
-  const StreamGeom g = stream_geom(a, sh.wdtype, sh.adtype, sms);
-  if (g.NS == 0 || b.hs2 == nullptr || b.ys2 == nullptr || !b.stream) return cudaErrorInvalidValue;
-  const dim3 grid(sms), block(kStreamWarps * 32);
-  const int jx = a.H / 256, jn = a.I / 256;
-#define MOE_STREAM_LAUNCH(JX, JN, ROWS)                                                                             \
-  if (jx == JX && jn == JN && g.RS == ROWS)                                                                         \
-    return launch_pdl(resident_stream_kernel<JX, JN, ROWS>, grid, block, g.smem, s, a, g, w, cpu_part, out, err);
-  MOE_STREAM_LAUNCH(8, 3, 4) MOE_STREAM_LAUNCH(8, 3, 2) MOE_STREAM_LAUNCH(8, 4, 4) MOE_STREAM_LAUNCH(8, 4, 2)
-  MOE_STREAM_LAUNCH(4, 3, 4) MOE_STREAM_LAUNCH(4, 3, 2) MOE_STREAM_LAUNCH(4, 4, 4) MOE_STREAM_LAUNCH(4, 4, 2)
-#undef MOE_STREAM_LAUNCH
-  return cudaErrorInvalidValue;
-}
 
 cudaError_t launch_down_combine(const Shape& sh, int T, const float* w, const float* cpu_part, DecodeBufs b,
                                 float* out, uint32_t* err, int sms, cudaStream_t s) {
@@ -2703,8 +2272,7 @@ cudaError_t launch_down_combine(const Shape& sh, int T, const float* w, const fl
     const BulkGeom geo = down_geom(a, sh.wdtype, sms);
     if (geo.NS >= 1 && geo.h_smem) return launch_down_bulk_any(sh, a, geo, true, true, w, cpu_part, out, err, s);
   }
-  if (sh.wdtype == MOE_NVFP4 || sh.wdtype == MOE_MXFP4) return cudaErrorInvalidValue;   // bulk kernels only (checked at create)
-  if (down_combine_fits(sh, T)) {
+  if (down_combine_fits(sh, T) && sh.wdtype != MOE_NVFP4 && sh.wdtype != MOE_MXFP4) {
     const GemvArgs a = make_args(sh, 2, T, nullptr, b);
     if (sh.wdtype == MOE_F32) return launch_down_combine_typed<MOE_F32>(a, w, cpu_part, out, err, sms, s);
     if (sh.wdtype == MOE_BF16) return launch_down_combine_typed<MOE_BF16>(a, w, cpu_part, out, err, sms, s);
@@ -2715,6 +2283,8 @@ cudaError_t launch_down_combine(const Shape& sh, int T, const float* w, const fl
   cudaError_t e;
   if (sh.wdtype == MOE_F32) e = launch_down_typed<MOE_F32>(a, sms, s);
   else if (sh.wdtype == MOE_BF16) e = launch_down_typed<MOE_BF16>(a, sms, s);
+  else if (sh.wdtype == MOE_NVFP4) e = launch_down_typed<MOE_NVFP4>(a, sms, s);
+  else if (sh.wdtype == MOE_MXFP4) e = launch_down_typed<MOE_MXFP4>(a, sms, s);
   else e = launch_down_typed<MOE_FP8E4M3_B128>(a, sms, s);
   if (e != cudaSuccess || b.defer_combine) return e;   // deferred: the combine follows the CPU branch
   return launch_combine(sh, T, w, cpu_part, b, out, err, s);

@@ -38,8 +38,7 @@ enum : uint32_t {
 enum PlanIdx : int {
   P_LAYER = 0, P_U = 1, P_H = 2, P_M = 3, P_Q = 4, P_NCPU = 5, P_NGPU = 6,
   P_NFIRST = 7,     // GPU experts in the first (resident) pass: hits + shared
-  P_SEQ = 8,        // launches of the resident stream kernel so far, this call's included (0: not this call)
-  P_COUNT = 9,
+  P_COUNT = 8,
 };
 
 // kernel groups timed by moe_cache_profile
@@ -62,15 +61,8 @@ struct DecodeBufs {
   float* y;               // [max_pairs, H] expert outputs (unweighted)
   uint32_t* arrive;       // [H] arrivals of the two split down kernels per row block (parity = who combines)
   unsigned long long* fused_bar;   // grid-barrier arrivals of the fused resident kernel (only grows)
-  // resident stream kernel: h and y of the resident pairs in two buffers each, used
-  // by alternate launches; a launch sets the other pair to the empty mark for the next
-  float* hs2;             // [2][max_g][I]
-  float* ys2;             // [2][k][H]
-  uint32_t* sseq;         // launches of the stream kernel (written by the control kernel)
-  int stream;             // this cache runs one-token calls through the stream kernel
   // test of the bounded waits: with test_wait set, the resident down kernel (pass 0)
-  // and the stream kernel's block-finishing warps also wait (20 ms at most) for
-  // *never_set, which nothing writes
+  // also waits (20 ms at most) for *never_set, which nothing writes
   const float* never_set;
   int test_wait;
   // This call's combine runs later, as its own kernel (a registered CPU branch
@@ -78,9 +70,6 @@ struct DecodeBufs {
   int defer_combine;
 };
 
-// The empty mark of the stream kernel's h and y buffers: a NaN bit pattern the
-// SwiGLU does not produce from finite inputs (a byte pattern, so cudaMemset sets it).
-constexpr uint32_t kStreamEmpty = 0xFFFFFFFFu;
 
 struct CacheTables {
   int32_t* e2s;           // [L*E]
@@ -144,9 +133,6 @@ bool down_combine_fits(const Shape& sh, int T);
 // gate/up), pass 1 = filled experts (fill stream, after the fill); the second
 // of the two CTAs of each row block to finish forms that block's combine.
 bool down_split_ok(const Shape& sh, int T, int sms);
-// NVFP4 and MXFP4 experts run only on the bulk gate/up and split down kernels: true when
-// both fit every call of up to max_tokens tokens
-bool fp4_decode_fits(const Shape& sh, int max_tokens, int sms);
 // pdl = false: a plain launch, whose CTAs hold no SM while the predecessor runs.
 cudaError_t launch_down_split(const Shape& sh, int pass, int T, const float* w, const float* cpu_part, DecodeBufs b,
                               float* out, uint32_t* err, int sms, cudaStream_t s, bool pdl = true);
@@ -158,15 +144,6 @@ cudaError_t launch_combine(const Shape& sh, int T, const float* w, const float* 
 bool resident_fused_ok(const Shape& sh, int T, int sms);
 cudaError_t launch_resident_fused(const Shape& sh, int T, const void* x, const float* w, const float* cpu_part,
                                   DecodeBufs b, float* out, uint32_t* err, int sms, cudaStream_t s);
-// Gate/up + down + combine of the resident experts as one expert-major stream of
-// weight items (bf16, one token, no shared expert): down rows start while later
-// experts' gate/up rows still stream, counted per expert and per row block, no
-// grid-wide barrier.  Can replace launch_gate_up(pass 0) + launch_down_split(pass 0).
-// It needs b.hs2 / b.ys2 set to kStreamEmpty at create and b.plan[P_SEQ] counting
-// its launches (the control kernel does it when b.stream and T == 1).
-bool resident_stream_ok(const Shape& sh, int T, int sms);
-cudaError_t launch_resident_stream(const Shape& sh, int T, const void* x, const float* w, const float* cpu_part,
-                                   DecodeBufs b, float* out, uint32_t* err, int sms, cudaStream_t s);
 int down_combine_launches(const Shape& sh, int T, int sms);   // kernels of launch_down_combine
 int gemv_block_threads();
 

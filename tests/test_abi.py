@@ -91,9 +91,9 @@ def test_fp4_create_errors_without_a_device_call(lib):
     h = ctypes.c_void_p()
     pool = ctypes.create_string_buffer(16)
     for wd in (MOE_NVFP4, MOE_MXFP4):
-        # H not a multiple of 32; then more than 2 decode tokens
-        for hidden, max_tokens in ((264, 1), (256, 4)):
-            cfg = MoEConfigC(1, 8, hidden, 128, 2, max_tokens, -1, wd, 1, 0, 1000, 0, 0, 0)
+        # H or I not a multiple of 32
+        for hidden, inter in ((264, 128), (256, 136)):
+            cfg = MoEConfigC(1, 8, hidden, inter, 2, 4, -1, wd, 1, 0, 1000, 0, 0, 0)
             assert lib.moe_cache_create(ctypes.byref(cfg), pool, 16, None, None, 4, ctypes.byref(h)) == 1
             assert b"fp4" in lib.moe_last_error()
 

@@ -322,15 +322,38 @@ def test_fp4_split_merges_exactly(fmt):
     small.close()
 
 
+@pytest.mark.parametrize("fmt,adtype", [("nvfp4", "bf16"), ("mxfp4", "bf16"), ("mxfp4", "f32")])
+def test_fp4_small_decode_sixteen_tokens(fmt, adtype):
+    # batches above 2 tokens: the register-staged gate/up and down kernels with 4-bit
+    # chunks, then the separate combine; ragged batches from one cache
+    from workloads import Config, Shape
+    cfg = Config(f"{fmt}_t16", Shape(L=3, E=24, k=4, H=256, I=128, wdtype=fmt, adtype=adtype), T=16, steps=16,
+                 capacity=30, routing="softmax_bias", bias_std=0.5, seed=97)
+    res = run_decode_parity(cfg, (1000, 1000), fp_every=1)
+    _ok(res)
+    assert res.fills > 0 and res.cpu_pairs > 0 and res.fp_checked == 16 * 3
+
+
 @pytest.mark.parametrize("fmt", FP4)
-def test_fp4_rejects_larger_batches_and_misshaped_prefill(fmt):
+def test_fp4_qwen3_shape_batch16(fmt):
+    # the batch-16 decode shape (top-8 of 128 with per-expert bias, 1:1 bandwidths) with 4-bit experts
+    cfg = config("qwen3_decode_b16")
+    cfg = cfg.with_(shape=cfg.shape.__class__(**{**cfg.shape.__dict__, "wdtype": fmt, "L": 6}), steps=10,
+                    capacity=150, resize_step=None, resize_to=None)
+    res = run_decode_parity(cfg, cfg.bw_mbps, n_phys=32, fp_every=2, state_every=2, memo=32)
+    _ok(res)
+    assert res.calls == 10 * 6 and res.fp_checked >= 30 and res.cpu_pairs > 0
+
+
+@pytest.mark.parametrize("fmt", FP4)
+def test_fp4_rejects_misshaped_prefill(fmt):
     import torch
     from serving_layer_moe_gb300 import MoECache, MoEError
     from workloads import Shape
     s = Shape(L=1, E=8, k=2, H=256, I=128, wdtype=fmt, adtype="bf16")
     pool = torch.zeros(8 * s.blob_bytes, dtype=torch.uint8).pin_memory()
-    # decode batches above 2 tokens; prefill with fp32 activations or H not a multiple of 256
-    for kw in ({"max_tokens": 4}, {"max_tokens": 1, "max_prefill_tokens": 64, "adtype": "f32"},
+    # prefill with fp32 activations or H not a multiple of 256
+    for kw in ({"max_tokens": 1, "max_prefill_tokens": 64, "adtype": "f32"},
                {"max_tokens": 1, "max_prefill_tokens": 64, "H": 160}):
         args = dict(L=1, E=8, H=256, I=128, top_k=2, wdtype=fmt, adtype="bf16", host_pool=pool, n_slots=4,
                     bw_pcie_mbps=1000, bw_cpu_mbps=0)
@@ -338,7 +361,7 @@ def test_fp4_rejects_larger_batches_and_misshaped_prefill(fmt):
         with pytest.raises(MoEError) as ei:
             MoECache(**args)
         assert ei.value.status == 1
-    # a 2-token decode cache with prefill is fine
+    # a 16-token decode cache with prefill is fine
     c = MoECache(L=1, E=8, H=256, I=128, top_k=2, wdtype=fmt, adtype="bf16", host_pool=pool, n_slots=4,
-                 bw_pcie_mbps=1000, bw_cpu_mbps=0, max_tokens=2, max_prefill_tokens=64)
+                 bw_pcie_mbps=1000, bw_cpu_mbps=0, max_tokens=16, max_prefill_tokens=64)
     c.close()

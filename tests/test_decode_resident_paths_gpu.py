@@ -1,14 +1,14 @@
-"""The three ways a decode call can run its resident experts, against each other.
+"""The two ways a decode call can run its resident experts, against each other.
 
-One-token bf16 calls run by default as one expert-major stream of gate/up and
-down items (MOE_DECODE_RESIDENT=stream); "grids" runs a gate/up grid then a
-down + combine grid, "fused" one launch with a grid-wide barrier between them
-(also MOE_DECODE_FUSED=1).  All three compute each resident expert's gate/up
-rows, down rows and the combine in the same arithmetic order, so on the same
-trace they give bit-identical layer outputs; the stream and the fused launch
-are also held to the oracle (slot maps bit-exact, outputs within 2e-2).  The
-traces start cold, so they also cover calls with fills but no resident expert,
-and calls whose pairs all go to the CPU.
+By default a gate/up grid then a down + combine grid ("grids"); with
+MOE_DECODE_RESIDENT=fused (or MOE_DECODE_FUSED=1) set when the cache is
+created, one-token bf16 calls run both in one launch with a grid-wide barrier
+between them.  Both compute each resident expert's gate/up rows, down rows and
+the combine in the same arithmetic order, so on the same trace they give
+bit-identical layer outputs; the fused launch is also held to the oracle (slot
+maps bit-exact, outputs within 2e-2).  The traces start cold, so they also
+cover calls with fills but no resident expert, and calls whose pairs all go to
+the CPU.
 """
 import os
 from dataclasses import replace
@@ -36,7 +36,7 @@ def _qwen3_small(T, steps, layers=6, **kw):
                                            capacity=int(0.37 * layers * shape.E), **kw)
 
 
-MODE_PATH = {"grids": 0, "fused": 1, "stream": 2}
+MODE_PATH = {"grids": 0, "fused": 1}
 
 
 def _cache(cfg, pool, offs, bw, mode):
@@ -88,34 +88,26 @@ def _path_equals_two_grids(cfg, bw, mode):
     return n_cpu, n_fill_only
 
 
-@pytest.mark.parametrize("mode", ["stream", "fused"])
+@pytest.mark.parametrize("mode", ["fused"])
 def test_bit_identical_to_two_grids_offload(mode):
     n_cpu, n_fill_only = _path_equals_two_grids(_qwen3_small(T=1, steps=20), (100000, 0), mode)
     assert n_cpu == 0 and n_fill_only > 0
 
 
-@pytest.mark.parametrize("mode", ["stream", "fused"])
+@pytest.mark.parametrize("mode", ["fused"])
 def test_bit_identical_to_two_grids_hybrid(mode):
     n_cpu, _ = _path_equals_two_grids(_qwen3_small(T=1, steps=20), (100000, 900000), mode)
     assert n_cpu > 0
 
 
-@pytest.mark.parametrize("mode", ["stream", "fused"])
+@pytest.mark.parametrize("mode", ["fused"])
 def test_bit_identical_all_cpu_calls(mode):
     # K = 0: no fill ever; cold calls send every pair to the CPU
     n_cpu, _ = _path_equals_two_grids(_qwen3_small(T=1, steps=4, layers=3, max_fetch=0), (1000, 1000), mode)
     assert n_cpu > 0
 
 
-def test_stream_bit_identical_hidden_1024_inter_1024():
-    # the other geometry the stream kernel takes: 4 x-chunks and 4 h-chunks per lane
-    shape = replace(QWEN3, L=4, E=32, H=1024, I=1024)
-    cfg = config("qwen3_decode_b1").with_(shape=shape, T=1, steps=12, capacity=40)
-    n_cpu, _ = _path_equals_two_grids(cfg, (100000, 100000), "stream")
-    assert n_cpu > 0
-
-
-@pytest.mark.parametrize("mode", ["stream", "fused"])
+@pytest.mark.parametrize("mode", ["fused"])
 def test_oracle_parity_one_token(monkeypatch, mode):
     monkeypatch.delenv("MOE_DECODE_FUSED", raising=False)
     monkeypatch.setenv("MOE_DECODE_RESIDENT", mode)
@@ -126,9 +118,9 @@ def test_oracle_parity_one_token(monkeypatch, mode):
     assert res.fp_checked >= 40 and res.cpu_pairs > 0 and res.fills > 0
 
 
-@pytest.mark.parametrize("mode", ["stream", "fused"])
+@pytest.mark.parametrize("mode", ["fused"])
 def test_one_token_paths_fall_back_where_they_do_not_apply(monkeypatch, mode):
-    # two tokens per call: neither the stream nor the fused launch applies and the two grids run
+    # two tokens per call: the fused launch does not apply and the two grids run
     monkeypatch.delenv("MOE_DECODE_FUSED", raising=False)
     monkeypatch.setenv("MOE_DECODE_RESIDENT", mode)
     cfg = _qwen3_small(T=2, steps=6, layers=3)

@@ -7,9 +7,8 @@
   must return MOE_ENOMEM and keep the old pool, so decode goes on matching the
   oracle bit for bit.
 * A bounded device wait that runs out: with MOE_TEST_UNSET_WAIT=1 when the
-  cache is created, the resident experts' down kernel (or, on the opt-in
-  stream path, its block-finishing warps) also waits for a word nothing
-  writes.  It gives up after 20 ms, flags the timeout and returns; the next
+  cache is created, the resident experts' down kernel also waits for a word
+  nothing writes.  It gives up after 20 ms, flags the timeout and returns; the next
   call on the cache reports MOE_EDEVICE, and a fresh cache afterwards computes
   correctly.
 """
@@ -114,7 +113,7 @@ def test_failed_resize_keeps_the_old_pool(monkeypatch):
     cache.close()
 
 
-@pytest.mark.parametrize("mode,path", [("grids", 0), ("stream", 2)])
+@pytest.mark.parametrize("mode,path", [("grids", 0)])
 def test_bounded_wait_runs_out_and_is_reported(monkeypatch, mode, path):
     import torch
     from serving_layer_moe_gb300 import MoEError

@@ -144,3 +144,30 @@ def test_lru_beats_a_prefill_pinned_subset_when_routing_shifts():
         for l in range(s.L):
             c.decode(l, ids[st, l])
     assert lru_miss_rate(c.counters) < pinned
+
+
+def test_lru_beats_the_static_placements_at_eleven_percent_capacity():
+    # The pages' second capacity point (about 11%: the DeepSeek-V3-shaped slice,
+    # C = 112 of 4 x 256 slots).  The layer-granular split cannot hold even one
+    # whole layer (it misses every read), the prefill-pinned subset misses about
+    # 1 - capacity of the decode reads (its prefill's routing is independent of the
+    # decode's), and the global LRU misses far fewer.
+    from oracle.static_split import prefill_updated_miss_rate, static_split_miss_rate
+    from workloads import Config, prefill_routing
+    cfg = config("dsv3_decode_slice").with_(steps=32)
+    s = cfg.shape
+    cap = cfg.capacity / (s.L * s.E)
+    assert abs(cap - 0.11) < 0.005
+    ids, _ = routing_trace(cfg)
+    pre_cfg = Config("dsv3_prefill", s, T=2048, steps=1, capacity=cfg.capacity, routing="softmax",
+                     seed=cfg.seed + 100, prefill=True)
+    pre = [prefill_routing(pre_cfg, l)[0] for l in range(s.L)]
+    pinned = prefill_updated_miss_rate([(pre, ids)], cfg.capacity, s.E)
+    assert abs(pinned - (1 - cap)) < 0.06   # 1024 decode reads of a Zipf(1.0) trace: a few points of noise
+    assert static_split_miss_rate(ids, cfg.capacity, s.E) == 1.0
+    c = SlotCache(s.L, s.E, cfg.capacity, K=8, b_pcie=1, b_cpu=0)
+    for st in range(cfg.steps):
+        for l in range(s.L):
+            c.decode(l, ids[st, l])
+    lru = lru_miss_rate(c.counters)
+    assert lru < 0.5 * pinned

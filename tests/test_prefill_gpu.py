@@ -27,8 +27,8 @@ def _make(cfg, C, n_phys=None, max_tokens=None):
     s = cfg.shape
     arena, offs = make_pool(s, cfg.seed, n_phys=n_phys)
     pool = torch.from_numpy(arena).pin_memory()
-    if max_tokens is None:   # 4-bit caches take decode calls of at most 2 tokens
-        max_tokens = 2 if s.wdtype in ("nvfp4", "mxfp4") else 16
+    if max_tokens is None:
+        max_tokens = 16
     cache = MoECache(L=s.L, E=s.E, H=s.H, I=s.I, top_k=s.k, max_tokens=max_tokens, wdtype=s.wdtype,
                      adtype=s.adtype, host_pool=pool, blob_offsets=offs, n_slots=C, bw_pcie_mbps=1000,
                      bw_cpu_mbps=0, device=0, max_prefill_tokens=cfg.T)
