@@ -96,6 +96,7 @@ def parse_args(argv=None):
                    help="skip the prefill chunks without the second buffer (4k / 8k / 16k tokens)")
     p.add_argument("--capacity", type=int, default=0, help="override the slot count (small profiling runs)")
     p.add_argument("--profile-layers", type=int, default=16, help="profile-decode: MoE layers of the small case")
+    p.add_argument("--profile-workload", default=WORKLOAD, help="profile-decode: the workload whose shape to use")
     p.add_argument("--profile-allhit", action="store_true",
                    help="profile-decode: replay one step so every routed expert is resident after the first")
     p.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
@@ -852,29 +853,35 @@ def decode_workload_measure(name, args, dev, bw_measured, hbm_peak, peak_src, wi
 
 
 def profile_case(args, dev):
-    """A small decode case for ncu captures (a few GB on the device): the qwen3 b1
-    shape with --profile-layers layers and 256 slots (--capacity to change),
-    --steps eager steps of single decode calls, no graph, no timing."""
+    """A small decode case for ncu captures (a few GB on the device): the shape of
+    --profile-workload (default the qwen3 b1 one) with --profile-layers layers and
+    256 slots (--capacity to change), --steps eager steps of single decode calls,
+    no graph, no timing.  With --profile-allhit every step replays step 0, so all
+    routed experts are resident after the first."""
     import torch
     from serving_layer_moe_gb300 import MoECache
-    base = config(WORKLOAD)
-    cfg = base.with_(shape=base.shape.__class__(**{**base.shape.__dict__, "L": args.profile_layers}))
+    name = args.profile_workload
+    base = config(name)
+    cfg = base.with_(shape=base.shape.__class__(**{**base.shape.__dict__, "L": min(args.profile_layers, base.shape.L)}),
+                     resize_step=None, resize_to=None)
     s = cfg.shape
-    arena, offs = make_pool(s, cfg.seed, n_phys=16)
+    arena, offs = make_pool(s, cfg.seed, n_phys=min(16, s.n_flat))
     pool = torch.from_numpy(arena).pin_memory()
-    cache = MoECache(L=s.L, E=s.E, H=s.H, I=s.I, top_k=s.k, max_tokens=1, wdtype=s.wdtype, adtype=s.adtype,
-                     host_pool=pool, blob_offsets=offs, n_slots=args.capacity or 256, bw_pcie_mbps=192000,
-                     bw_cpu_mbps=0, device=dev.index or 0)
+    shared = make_shared(s, cfg.seed) if s.n_shared else None
+    cache = MoECache(L=s.L, E=s.E, H=s.H, I=s.I, top_k=s.k, max_tokens=cfg.T, wdtype=s.wdtype, adtype=s.adtype,
+                     host_pool=pool, blob_offsets=offs, shared=shared, n_slots=args.capacity or 256,
+                     bw_pcie_mbps=192000, bw_cpu_mbps=0, device=dev.index or 0)
     ids, w = routing_trace(cfg)
-    out = torch.empty(1, s.H, device=dev)
+    out = torch.empty(cfg.T, s.H, device=dev)
     for st0 in range(args.steps):
         st = 0 if args.profile_allhit else st0 % cfg.steps
         for l in range(s.L):
-            x = torch.from_numpy(activations(cfg, st, l).view(np.int16)).to(dev)
+            xa = activations(cfg, st, l)
+            x = torch.from_numpy(xa.view(np.int16) if xa.dtype == np.uint16 else xa).to(dev)
             cache.decode(l, x, torch.from_numpy(ids[st, l]).to(dev), torch.from_numpy(w[st, l]).to(dev), out)
     torch.cuda.synchronize(dev)
     c = cache.state()[3]
-    print(json.dumps({"profile_case": f"{WORKLOAD} shape, {s.L} layers, {int(cache.info()[1])} slots",
+    print(json.dumps({"profile_case": f"{name} shape, {s.L} layers, {int(cache.info()[1])} slots",
                       "hits": int(c[0]), "misses": int(c[1]), "fills": int(c[2])}))
     cache.close()
 
