@@ -527,7 +527,7 @@ def main(args):
             print(json.dumps({"cpu_branch": cpu_branch_measure(args, dev)}))
         return
     if args.mode == "workloads":
-        res = {n: decode_workload_measure(n, args, dev, (b_pcie, b_cpu), hbm_peak, peak_src, rank == 0)
+        res = {n: decode_workload_measure(n, args, dev, (b_pcie, b_cpu), hbm_peak, peak_src, rank == 0, bp_gbs)
                for n in EXTRA_WORKLOADS}
         if rank == 0:
             print(json.dumps({"workloads": res}))
@@ -706,7 +706,7 @@ def main(args):
     }
     if args.mode == "all" and not args.no_workloads:
         result["workloads"] = {n: decode_workload_measure(n, args, dev, (b_pcie, b_cpu), hbm_peak, peak_src,
-                                                          rank == 0 and not args.no_cpu_baseline)
+                                                          rank == 0 and not args.no_cpu_baseline, bp_gbs)
                                for n in EXTRA_WORKLOADS}
     if args.mode == "all" and not args.no_nvfp4:
         result["nvfp4_decode"] = fp4_measure(args, dev, local, b_pcie, b_cpu, "nvfp4")
@@ -797,7 +797,7 @@ WORKLOAD_DESC = {
 }
 
 
-def decode_workload_measure(name, args, dev, bw_measured, hbm_peak, peak_src, with_cpu):
+def decode_workload_measure(name, args, dev, bw_measured, hbm_peak, peak_src, with_cpu, bw_link_gbs=None):
     """One of the other decode workloads: graph-replayed steps after an untimed
     prefix, the kernel groups' event times over profiled replays after the
     window, and a bounded oracle sample of the same workload."""
@@ -828,6 +828,13 @@ def decode_workload_measure(name, args, dev, bw_measured, hbm_peak, peak_src, wi
                         f"{n_phys or s.n_flat}",
            "roofline": roofline_from_groups(groups, hbm_peak, peak_src, WORKLOAD_TRAFFIC.get(name),
                                             WORKLOAD_TRAFFIC_SOURCE.get(name)),
+           # the fills' bytes over the window's wall time, against the calibrated host link
+           "link": {"fill_bytes_per_step": round(int(dcnt[2]) * s.blob_bytes / steps),
+                    "achieved_gbs": round(int(dcnt[2]) * s.blob_bytes / (ms / 1e3) / 1e9, 1),
+                    "B_P_gbs": round(bw_link_gbs, 1),
+                    "frac": round(int(dcnt[2]) * s.blob_bytes / (ms / 1e3) / 1e9 / bw_link_gbs, 3) if bw_link_gbs else None,
+                    "note": "fill bytes of the timed window over its whole wall time (a lower bound of the fill "
+                            "rate), against bench_bw's B_P"},
            "roofline_note": "the kernel group with the most event time, over profiled replays of the "
                             f"{prof_steps} steps after the timed window (fills and CPU-assigned pairs as they occur)",
            "kernel_groups": {k: {"bytes_per_launch": round(b / max(1, n)), "us_per_launch": round(1e3 * m / max(1, n), 2),

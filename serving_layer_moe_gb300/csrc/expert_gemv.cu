@@ -934,6 +934,8 @@ struct BulkGeom {
   int NS;       // ring stages per warp (< 2: the shape does not fit)
   int NW;       // warps per CTA
   int h_smem;   // down: h of every pair staged in shared memory
+  int pf_down;  // gate/up: have L2 fetch the experts' W_down behind the rows (it fits there)
+  int RS, nsb;  // down: rows per ring stage, and sub-blocks of RS rows per CTA's R rows
   int grid;     // CTAs
   size_t SB;    // bytes per stage
   size_t ring_off, plan_off, extra_off, smem;
@@ -995,7 +997,7 @@ __global__ void __launch_bounds__(256) gate_up_bulk_kernel(GemvArgs a, BulkGeom 
       const long it = w0 + (long)k * nwarps;
       if (it < items) issue(it, k);
     }
-    if (n_mine <= geo.NS) prefetch_down();
+    if (geo.pf_down && n_mine <= geo.NS) prefetch_down();
   }
   {
     uint4* dst = reinterpret_cast<uint4*>(xsm);
@@ -1081,7 +1083,7 @@ __global__ void __launch_bounds__(256) gate_up_bulk_kernel(GemvArgs a, BulkGeom 
     if (lane == 0 && it + (long)geo.NS * nwarps < items) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       issue(it + (long)geo.NS * nwarps, st);
-      if (k == n_mine - geo.NS - 1) prefetch_down();   // that was this warp's last row copy
+      if (geo.pf_down && k == n_mine - geo.NS - 1) prefetch_down();   // that was this warp's last row copy
     }
   }
   if (!ok && lane == 0) {  // flag the timeout; this warp's copies land before it exits
@@ -1115,7 +1117,7 @@ __global__ void __launch_bounds__(256) gate_up_bulk_kernel(GemvArgs a, BulkGeom 
 // itself in arrive[block], and the second of the two (odd count before its
 // increment) forms the block's combine from y in global memory.
 template <int WT, bool kRing, int kJN, bool kPair = false>
-__global__ void __launch_bounds__((kRing && !kPair) ? 256 : 512) down_bulk_kernel(GemvArgs a, BulkGeom geo,
+__global__ void __launch_bounds__((kRing && !kPair) || (!kRing && kJN > 0) ? 256 : 512) down_bulk_kernel(GemvArgs a, BulkGeom geo,
                                                         const float* __restrict__ w,
                                                         const float* __restrict__ cpu, float* __restrict__ out,
                                                         uint32_t* err) {
@@ -1170,21 +1172,32 @@ __global__ void __launch_bounds__((kRing && !kPair) ? 256 : 512) down_bulk_kerne
   const size_t row_bytes = F::row(I);
   const size_t down_off = 2ull * (size_t)I * F::row(H);
   const size_t sd_off = F::sd_off(H, I);
-  const uint32_t bytes = (uint32_t)(nr * row_bytes);
   const uint64_t pol = evict_first_policy();
   const bool h_copy = geo.h_smem && g1 > g0;
   __syncthreads();
+  // Ring items: (expert g, sub-block sb of RS rows) of this pass's experts, expert
+  // major; this CTA's nr rows (fewer than R in the last CTA) take ceil(nr / RS)
+  // sub-blocks of 1..RS rows.  Each ring owner takes an even, contiguous share of
+  // the items, so consecutive items of a warp mostly keep the same expert (and its
+  // h in registers) and no warp has more than one item above another.
+  const int nsb = (nr + geo.RS - 1) / geo.RS;
+  const int n_all = (g1 - g0) * nsb;
+  const int k_base = n_all * rw / geo.NW;
+  const int n_wi = n_all * (rw + 1) / geo.NW - k_base;
+  auto item_g = [&](int k) { return g0 + (k_base + k) / nsb; };
+  auto item_sb = [&](int k) { return (k_base + k) % nsb; };
+  auto item_rows = [&](int sb) { return min(geo.RS, nr - sb * geo.RS); };
   int last_issued[2] = {-1, -1};
-  auto issue = [&](int g, int st) {   // lane 0 only
-    last_issued[st] = g;
+  auto issue = [&](int k, int st) {   // lane 0 only
+    last_issued[st] = k;
+    const int sb = item_sb(k);
+    const uint32_t bytes = (uint32_t)(item_rows(sb) * row_bytes);
     bar_expect(&bars[st], bytes);
-    bulk_copy(ring + (size_t)st * geo.SB, sp.w[g] + down_off + (size_t)r0 * row_bytes, bytes, &bars[st], pol);
+    bulk_copy(ring + (size_t)st * geo.SB, sp.w[item_g(k)] + down_off + (size_t)(r0 + sb * geo.RS) * row_bytes, bytes,
+              &bars[st], pol);
   };
   if (kRing && lane == 0 && owner)
-    for (int k = 0; k < geo.NS; ++k) {
-      const int g = g0 + rw + k * geo.NW;
-      if (g < g1) issue(g, k);
-    }
+    for (int k = 0; k < geo.NS && k < n_wi; ++k) issue(k, k);
   pdl_wait();   // h of the resident experts is complete from here on
   pdl_trigger();
   if (h_copy && threadIdx.x == 0) {   // the h rows (I floats, a 16-byte multiple) of this pass's pairs
@@ -1198,7 +1211,73 @@ __global__ void __launch_bounds__((kRing && !kPair) ? 256 : 512) down_bulk_kerne
   const int NCH = I / V;
   const int IB = I / 128;
   bool ok = true;
-  if (!kRing) {   // (expert, row) items over all warps; the per-lane sums and the butterfly match the ring path
+  if (!kRing && kJN > 0) {
+    // NCH = 32 kJN, no ring: items of (expert, kG rows) over all warps.  Every
+    // 16-byte chunk of the kG rows is loaded before the first is used, so a warp
+    // has kG x kJN loads in flight (the rows come from L2 right after their fill);
+    // rows past nr repeat the last one.  The per-lane chunk order, its grouping by
+    // J and the butterfly are those of the other paths, so y is the same bit for bit.
+    constexpr int kG = 4;
+    const int ngr = (nr + kG - 1) / kG;
+    const int n_items = (g1 - g0) * ngr;
+    float hn[kJN > 0 ? kJN : 1][V];
+    int hn_pid = -1;
+    for (int item = warp; item < n_items; item += geo.NW) {
+      const int g = g0 + item / ngr, rb = (item % ngr) * kG;
+      const int nrr = min(kG, nr - rb);
+      const uint8_t* base = sp.w[g] + down_off + (size_t)(r0 + rb) * row_bytes;
+      const float* sd = reinterpret_cast<const float*>(sp.w[g] + sd_off);
+      uint4 wv[kG][kJN > 0 ? kJN : 1];
+#pragma unroll
+      for (int r = 0; r < kG; ++r) {
+        const uint4* wrow = reinterpret_cast<const uint4*>(base + (size_t)(r < nrr ? r : nrr - 1) * row_bytes);
+#pragma unroll
+        for (int j = 0; j < kJN; ++j) wv[r][j] = wrow[j * 32 + lane];
+      }
+      for (int tp = sp.off[g]; tp < sp.off[g + 1]; ++tp) {
+        const int pid = sp.pid[tp];
+        if (pid != hn_pid) {
+#pragma unroll
+          for (int j = 0; j < kJN; ++j) {
+            const float4* hp = reinterpret_cast<const float4*>(hsrc + (size_t)pid * I + (size_t)(j * 32 + lane) * V);
+#pragma unroll
+            for (int v = 0; v < V; v += 4) {
+              const float4 q = hp[v / 4];
+              hn[j][v] = q.x; hn[j][v + 1] = q.y; hn[j][v + 2] = q.z; hn[j][v + 3] = q.w;
+            }
+          }
+          hn_pid = pid;
+        }
+#pragma unroll
+        for (int r = 0; r < kG; ++r) {
+          const int rr = r < nrr ? r : nrr - 1;
+          float s = 0.f, d = 0.f;
+#pragma unroll
+          for (int j = 0; j < kJN; ++j) {
+            float fw[V];
+            F::unpack(wv[r][j], fw);
+            float dj = 0.f;
+#pragma unroll
+            for (int v = 0; v < V; ++v) dj = fmaf(fw[v], hn[j][v], dj);
+            if (WT == MOE_FP8E4M3_B128) dj *= __ldg(sd + (size_t)((r0 + rb + rr) >> 7) * IB + (((j * 32 + lane) * V) >> 7));
+            d += dj;
+            if ((j + 1) % J == 0 || j + 1 == kJN) {
+              s += d;
+              d = 0.f;
+            }
+          }
+          float acc = 0.f;
+          acc += s;
+          acc = warp_sum(acc);
+          if (lane == 0 && r < nrr) {
+            ys[(size_t)(rb + r) * NP + pid] = acc;
+            a.b.y[(size_t)pid * H + r0 + rb + r] = acc;
+          }
+        }
+      }
+    }
+  }
+  if (!kRing && kJN == 0) {   // (expert, row) items over all warps; the per-lane sums and the butterfly match the ring path
     if (h_copy && !__all_sync(0xffffffffu, bar_wait(hbar, 0))) ok = false;
     const int n_items = (g1 - g0) * nr;
     for (int item = warp; ok && item < n_items; item += geo.NW) {
@@ -1257,12 +1336,16 @@ __global__ void __launch_bounds__((kRing && !kPair) ? 256 : 512) down_bulk_kerne
       }
     }
   }
-  int k = 0;
-  for (int g = g0 + rw; kRing && g < g1; g += geo.NW, ++k) {
+  float hv[kJN > 0 ? kJN : 1][V];   // the straight-line path's h of pair hv_pid
+  int hv_pid = -1;
+  for (int k = 0; kRing && k < n_wi; ++k) {
     const int st = k % geo.NS;
     if (k == 0 && h_copy && !__all_sync(0xffffffffu, bar_wait(hbar, 0))) { ok = false; break; }
     if (!__all_sync(0xffffffffu, bar_wait(&bars[st], (uint32_t)((k / geo.NS) & 1)))) { ok = false; break; }
     const uint8_t* blk = ring + (size_t)st * geo.SB;
+    const int g = item_g(k), sb = item_sb(k);
+    const int rsb = sb * geo.RS;             // this sub-block's first row within the CTA's R rows
+    const int nrs = item_rows(sb);           // and its rows
     const float* sd = reinterpret_cast<const float*>(sp.w[g] + sd_off);
     const int pb = sp.off[g], pe = sp.off[g + 1];
     constexpr int kRW = kPair ? 8 : kDownRows;   // rows this warp accumulates
@@ -1275,22 +1358,26 @@ __global__ void __launch_bounds__((kRing && !kPair) ? 256 : 512) down_bulk_kerne
       if (kJN > 0) {
         // NCH = 32 kJN: one column segment, no guards; rows past nr repeat the
         // last row (their sums are never stored), so the whole block is one
-        // straight run of independent chains
-        float hv[kJN > 0 ? kJN : 1][V];
+        // straight run of independent chains.  h stays in registers while the
+        // warp's items keep the same pair.
+        if (pid != hv_pid) {
 #pragma unroll
-        for (int j = 0; j < kJN; ++j) {
-          const float4* hp = reinterpret_cast<const float4*>(hsrc + (size_t)pid * I + (size_t)(j * 32 + lane) * V);
+          for (int j = 0; j < kJN; ++j) {
+            const float4* hp = reinterpret_cast<const float4*>(hsrc + (size_t)pid * I + (size_t)(j * 32 + lane) * V);
 #pragma unroll
-          for (int v = 0; v < V; v += 4) {
-            const float4 q = hp[v / 4];
-            hv[j][v] = q.x; hv[j][v + 1] = q.y; hv[j][v + 2] = q.z; hv[j][v + 3] = q.w;
+            for (int v = 0; v < V; v += 4) {
+              const float4 q = hp[v / 4];
+              hv[j][v] = q.x; hv[j][v + 1] = q.y; hv[j][v + 2] = q.z; hv[j][v + 3] = q.w;
+            }
           }
+          hv_pid = pid;
         }
 #pragma unroll
         for (int r = 0; r < kRW; ++r) {
-          const int rr = rbase + r < nr ? rbase + r : nr - 1;
+          const int rr = rbase + r < nrs ? rbase + r : nrs - 1;
           const uint4* wrow = reinterpret_cast<const uint4*>(blk + (size_t)rr * row_bytes);
-          float d = 0.f;
+          // chunk sums grouped J at a time, as the guarded path below adds them
+          float s = 0.f, d = 0.f;
 #pragma unroll
           for (int j = 0; j < kJN; ++j) {
             float fw[V];
@@ -1298,10 +1385,14 @@ __global__ void __launch_bounds__((kRing && !kPair) ? 256 : 512) down_bulk_kerne
             float dj = 0.f;
 #pragma unroll
             for (int v = 0; v < V; ++v) dj = fmaf(fw[v], hv[j][v], dj);
-            if (WT == MOE_FP8E4M3_B128) dj *= __ldg(sd + (size_t)((r0 + rr) >> 7) * IB + (((j * 32 + lane) * V) >> 7));
+            if (WT == MOE_FP8E4M3_B128) dj *= __ldg(sd + (size_t)((r0 + rsb + rr) >> 7) * IB + (((j * 32 + lane) * V) >> 7));
             d += dj;
+            if ((j + 1) % J == 0 || j + 1 == kJN) {
+              s += d;
+              d = 0.f;
+            }
           }
-          acc[r] += d;
+          acc[r] += s;
         }
       }
       for (int c0 = 0; kJN == 0 && c0 < NCH; c0 += 32 * J) {
@@ -1323,7 +1414,7 @@ __global__ void __launch_bounds__((kRing && !kPair) ? 256 : 512) down_bulk_kerne
         }
 #pragma unroll
         for (int r = 0; r < kDownRows; ++r) {
-          if (r < nr) {
+          if (r < nrs) {
             const uint4* wrow = reinterpret_cast<const uint4*>(blk + (size_t)r * row_bytes);
             float d = 0.f;
 #pragma unroll
@@ -1333,13 +1424,13 @@ __global__ void __launch_bounds__((kRing && !kPair) ? 256 : 512) down_bulk_kerne
                 float dj = 0.f;
                 if constexpr (kFp4<WT>) {
                   const auto* srow = reinterpret_cast<const typename F::scale_t*>(sp.w[g] + sd_off);
-                  dj = F::dot(wrow[c], __ldg(srow + (size_t)(r0 + r) * (I / 32) + c), hv[j]);
+                  dj = F::dot(wrow[c], __ldg(srow + (size_t)(r0 + rsb + r) * (I / 32) + c), hv[j]);
                 } else {
                   float fw[V];
                   F::unpack(wrow[c], fw);
 #pragma unroll
                   for (int v = 0; v < V; ++v) dj = fmaf(fw[v], hv[j][v], dj);
-                  if (WT == MOE_FP8E4M3_B128) dj *= __ldg(sd + (size_t)((r0 + r) >> 7) * IB + ((c * V) >> 7));
+                  if (WT == MOE_FP8E4M3_B128) dj *= __ldg(sd + (size_t)((r0 + rsb + r) >> 7) * IB + ((c * V) >> 7));
                 }
                 d += dj;
               }
@@ -1361,15 +1452,15 @@ __global__ void __launch_bounds__((kRing && !kPair) ? 256 : 512) down_bulk_kerne
         mine = (lane & 1) == 0;
       }
       if constexpr (WT == MOE_NVFP4) v *= __ldg(reinterpret_cast<const float*>(sp.w[g] + F::g_off(H, I)) + 1);
-      if (mine && r < nr) {
-        ys[(size_t)r * NP + pid] = v;
-        a.b.y[(size_t)pid * H + r0 + r] = v;   // per-pair output stays readable (moe_cache_get_plan)
+      if (mine && r < nrs) {
+        ys[(size_t)(rsb + r) * NP + pid] = v;
+        a.b.y[(size_t)pid * H + r0 + rsb + r] = v;   // per-pair output stays readable (moe_cache_get_plan)
       }
     }
     __syncwarp();
-    if (lane == 0 && owner && g + geo.NS * geo.NW < g1) {
+    if (lane == 0 && owner && k + geo.NS < n_wi) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      issue(g + geo.NS * geo.NW, st);
+      issue(k + geo.NS, st);
     }
   }
   if (!ok && lane == 0) {   // flag the timeout; this warp's copies land before the CTA exits
@@ -1377,7 +1468,7 @@ __global__ void __launch_bounds__((kRing && !kPair) ? 256 : 512) down_bulk_kerne
     if (kRing)
       for (int s2 = 0; s2 < geo.NS; ++s2) {
         if (last_issued[s2] < 0) continue;
-        const int kk = (last_issued[s2] - g0 - warp) / geo.NW;
+        const int kk = last_issued[s2];   // the item index of the copy that stage holds
         const uint32_t par = (uint32_t)((kk / geo.NS) & 1);
         const unsigned long long t0 = gtime();
         while (!bar_test(&bars[s2], par) && gtime() - t0 < kBulkWaitNs) {
@@ -1937,7 +2028,12 @@ cudaError_t setup_gemv_kernels() {
                         (const void*)down_bulk_kernel<MOE_BF16, true, 3, true>,
                         (const void*)down_bulk_kernel<MOE_BF16, true, 4, true>,
                         (const void*)down_bulk_kernel<MOE_FP8E4M3_B128, true, 0>,
+                        (const void*)down_bulk_kernel<MOE_FP8E4M3_B128, true, 3>,
+                        (const void*)down_bulk_kernel<MOE_FP8E4M3_B128, true, 4>,
                         (const void*)down_bulk_kernel<MOE_F32, false, 0>, (const void*)down_bulk_kernel<MOE_BF16, false, 0>,
+                        (const void*)down_bulk_kernel<MOE_BF16, false, 3>, (const void*)down_bulk_kernel<MOE_BF16, false, 4>,
+                        (const void*)down_bulk_kernel<MOE_FP8E4M3_B128, false, 3>,
+                        (const void*)down_bulk_kernel<MOE_FP8E4M3_B128, false, 4>,
                         (const void*)down_bulk_kernel<MOE_FP8E4M3_B128, false, 0>,
                         (const void*)down_bulk_kernel<MOE_NVFP4, true, 0>, (const void*)down_bulk_kernel<MOE_NVFP4, false, 0>,
                         (const void*)gate_up_bulk_kernel<MOE_NVFP4, MOE_F32, 0>,
@@ -2022,6 +2118,7 @@ size_t up128(size_t x) { return (x + 127) & ~size_t(127); }
 // (gate/up: NS < 2) means the shape does not fit and the register-staged
 // kernel runs instead.
 constexpr size_t kRingBudget = 220 * 1024;
+constexpr size_t kPrefetchDownMax = 40ull << 20;   // W_down bytes the gate/up grid has L2 fetch, at most
 
 // Gate/up: one CTA per SM, up to 8 warps with up to 3 stages of one row pair each
 // (about 200 KB for the Qwen3 shape: the stream is bound by the bytes each SM has
@@ -2045,12 +2142,22 @@ BulkGeom gate_up_geom(const GemvArgs& a, int wdtype, int adtype, int sms) {
   g.plan_off = g.ring_off + (size_t)g.NW * g.NS * g.SB;
   g.extra_off = g.plan_off + plan;
   g.smem = g.extra_off + up128(xbytes);
+  // W_down of the call's experts fetched into L2 behind the gate/up rows helps only
+  // if it stays there until the down grid reads it: beside a full-rate stream that
+  // holds for a few tens of MB (8 Qwen3-shaped experts: 25 MB), not for 132 MB
+  // (the DeepSeek-V3 slice) or 200 MB (16 tokens over ~66 experts), which L2 evicts
+  // first and the down grid reads from HBM again.
+  g.pf_down = (size_t)a.max_g * a.H * wrow(wdtype, (size_t)a.I) <= kPrefetchDownMax ? 1 : 0;
   return g;
 }
 
-// Down: min(ceil(H / sms), 16) output rows per CTA, with one stage for each of 8
-// warps when there are at most 8 GPU experts, else two-stage rings of at least
-// four warps; fewer rows per CTA when that does not fit.
+// Down: R = ceil(H / sms) output rows per CTA, so the grid is one wave; the ring
+// streams them in sub-blocks of RS <= 16 rows (one sub-block when R <= 16, as for
+// the Qwen3 shapes; 4 of up to 13 rows for the DeepSeek-V3 slice's R = 48), with
+// one stage for each of 8 warps when there are at most 8 GPU experts, else
+// two-stage rings of at least four warps; fewer rows per stage when that does not
+// fit.  (Shrinking R instead would take several waves of CTAs, each filling its
+// ring from cold.)
 BulkGeom down_geom(const GemvArgs& a, int wdtype, int sms) {
   BulkGeom g{};
   const size_t row = wrow(wdtype, (size_t)a.I);
@@ -2058,12 +2165,13 @@ BulkGeom down_geom(const GemvArgs& a, int wdtype, int sms) {
   const size_t hbytes = np * a.I * 4;
   const size_t plan = up128(staged_plan_bytes(a.max_g, a.max_p));
   g.h_smem = hbytes <= 64 * 1024 ? 1 : 0;
-  for (int R = std::min((a.H + sms - 1) / sms, kDownRows); R >= 1; --R) {
-    g.SB = up128((size_t)R * row);
-    const size_t extra = up128((size_t)a.P * 8) + up128((size_t)R * np * 4 + np) + (g.h_smem ? hbytes : 0);
-    const size_t fixed = 256 + plan + up128(extra);
-    if (fixed >= kRingBudget) continue;
-    const size_t room = kRingBudget - fixed;
+  const int R = (a.H + sms - 1) / sms;
+  const size_t extra = up128((size_t)a.P * 8) + up128((size_t)R * np * 4 + np) + (g.h_smem ? hbytes : 0);
+  const size_t fixed = 256 + plan + up128(extra);
+  if (fixed >= kRingBudget) { g.NS = 0; return g; }
+  const size_t room = kRingBudget - fixed;
+  for (int RS = std::min(R, kDownRows); RS >= 1; --RS) {
+    g.SB = up128((size_t)RS * row);
     if (a.max_g <= 8 && 8 * g.SB <= room) {
       g.NS = 1;
       g.NW = 8;
@@ -2073,6 +2181,8 @@ BulkGeom down_geom(const GemvArgs& a, int wdtype, int sms) {
     }
     if (g.NW >= 4) {
       g.R = R;
+      g.RS = RS;
+      g.nsb = (R + RS - 1) / RS;
       g.grid = (a.H + R - 1) / R;
       g.ring_off = 256;
       g.plan_off = g.ring_off + (size_t)g.NW * g.NS * g.SB;
@@ -2153,21 +2263,37 @@ cudaError_t launch_down_bulk(const GemvArgs& a, const BulkGeom& geo, bool ring, 
       d.smem -= (size_t)(a.P + a.T * a.n_shared) * a.I * 4;
       d.h_smem = 0;
     }
-    if (pdl)
-      return launch_pdl(down_bulk_kernel<WT, false, 0>, dim3(d.grid), dim3(d.NW * 32), d.smem, s, a, d, w, cpu, out,
-                        err);
-    down_bulk_kernel<WT, false, 0><<<d.grid, d.NW * 32, d.smem, s>>>(a, d, w, cpu, out, err);
-    return cudaGetLastError();
+    auto go1 = [&](auto kern) -> cudaError_t {
+      if (pdl) return launch_pdl(kern, dim3(d.grid), dim3(d.NW * 32), d.smem, s, a, d, w, cpu, out, err);
+      kern<<<d.grid, d.NW * 32, d.smem, s>>>(a, d, w, cpu, out, err);
+      return cudaGetLastError();
+    };
+    // bf16 or fp8 rows of 3 or 4 16-byte chunks per lane: the straight-line variant,
+    // 8 warps (measured against 4 warps, and against plain launches of both, on the
+    // DeepSeek-V3 slice: 3593 layer-steps/s against 3546-3576; the guarded path 3459)
+    if constexpr (WT == MOE_BF16 || WT == MOE_FP8E4M3_B128) {
+      const int nch = (int)(a.I / WFmt<WT>::V);
+      d.NW = 8;
+      if (nch == 96) return go1(down_bulk_kernel<WT, false, 3>);
+      if (nch == 128) return go1(down_bulk_kernel<WT, false, 4>);
+      d.NW = 16;
+    }
+    return go1(down_bulk_kernel<WT, false, 0>);
   }
   auto go = [&](auto kern, int threads) -> cudaError_t {
     if (pdl) return launch_pdl(kern, dim3(geo.grid), dim3(threads), geo.smem, s, a, geo, w, cpu, out, err);
     kern<<<geo.grid, threads, geo.smem, s>>>(a, geo, w, cpu, out, err);
     return cudaGetLastError();
   };
+  if constexpr (WT == MOE_FP8E4M3_B128) {   // the same for fp8 rows of 3 or 4 chunks per lane
+    const int nch = a.I / 16;
+    if (nch == 96) return go(down_bulk_kernel<WT, true, 3>, geo.NW * 32);
+    if (nch == 128) return go(down_bulk_kernel<WT, true, 4>, geo.NW * 32);
+  }
   if constexpr (WT == MOE_BF16) {   // rows of 3 or 4 chunks per lane: the unguarded straight-line path
     const int nch = a.I / 8;
     // one stage per expert for at most 8 experts: two warps per stage, 8 rows each
-    const bool pair = geo.NS == 1 && geo.NW == 8 && a.max_g <= 8 && geo.R <= 16;
+    const bool pair = geo.NS == 1 && geo.NW == 8 && a.max_g <= 8 && geo.R <= 16 && geo.nsb == 1;
     if (nch == 96)
       return pair ? go(down_bulk_kernel<WT, true, 3, true>, 512) : go(down_bulk_kernel<WT, true, 3>, geo.NW * 32);
     if (nch == 128)

@@ -365,3 +365,42 @@ def test_fp4_rejects_misshaped_prefill(fmt):
     c = MoECache(L=1, E=8, H=256, I=128, top_k=2, wdtype=fmt, adtype="bf16", host_pool=pool, n_slots=4,
                  bw_pcie_mbps=1000, bw_cpu_mbps=0, max_tokens=16, max_prefill_tokens=64)
     c.close()
+
+
+@pytest.mark.parametrize("name,fmt", [("qwen3_decode_b1", None), ("dsv3_decode_slice", None),
+                                      ("qwen3_decode_b1", "nvfp4"), ("qwen3_decode_b1", "mxfp4")])
+def test_a_pair_is_the_same_filled_or_resident(name, fmt):
+    # One layer twice on the same input: first every routed expert is filled (the
+    # fill computes gate/up on the way, the filled-expert grid the down rows), then
+    # every one is resident (the resident grids).  Both form each pair's y in the
+    # same per-lane order and butterfly, so y and the layer output match bit for bit.
+    import torch
+    from dataclasses import replace
+    from workloads import make_shared
+    base = config(name)
+    shape = replace(base.shape, L=1, **({"wdtype": fmt} if fmt else {}))
+    cfg = base.with_(shape=shape, steps=1, capacity=2 * shape.k, max_fetch=shape.k,
+                     resize_step=None, resize_to=None)
+    s = cfg.shape
+    dev = torch.device("cuda", 0)
+    arena, offs, pool = build_pool(cfg, n_phys=16)
+    shared = make_shared(s, cfg.seed) if s.n_shared else None
+    cache, _ = make_cache(cfg, pool, offs, shared, (100000, 0))
+    ids, w = routing_trace(cfg)
+    x = torch_act(activations(cfg, 0, 0), dev)
+    i_d, w_d = torch.from_numpy(ids[0, 0]).to(dev), torch.from_numpy(w[0, 0]).to(dev)
+    outs, ys = [], []
+    for call in range(2):
+        out = torch.empty(cfg.T, s.H, device=dev)
+        sm = torch.empty(cfg.T, s.k, dtype=torch.int32, device=dev)
+        cache.decode(0, x, i_d, w_d, out, slot_map=sm)
+        torch.cuda.synchronize()
+        p = cache.plan(T=cfg.T)
+        assert (p["q"], p["h"]) == ((s.k, 0) if call == 0 else (0, s.k)), p
+        assert bool((sm >= 0).all())
+        outs.append(out.cpu().numpy())
+        ys.append(p["y"])
+    cache.close()
+    assert np.all(np.isfinite(outs[0]))
+    assert np.array_equal(ys[0].view(np.uint32), ys[1].view(np.uint32))
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
