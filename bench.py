@@ -85,9 +85,9 @@ def parse_args(argv=None):
     p.add_argument("--no-nvfp4", action="store_true",
                    help="skip the 4-bit-expert variants (NVFP4, MXFP4) of the decode workload")
     p.add_argument("--mode", default="all", choices=["all", "decode", "prefill", "profile-decode", "workloads",
-                                                     "cpu-branch"],
+                                                     "cpu-branch", "fill-step"],
                    help="prefill: only the prefill measurement; workloads: only the tiny, batch-16 and "
-                        "DeepSeek-V3 decode workloads")
+                        "DeepSeek-V3 decode workloads; fill-step: a layer-step with one fill against its floor")
     p.add_argument("--no-workloads", action="store_true",
                    help="skip the tiny, batch-16 and DeepSeek-V3 decode workloads")
     p.add_argument("--cpu-workload", default=WORKLOAD, help=argparse.SUPPRESS)
@@ -526,6 +526,10 @@ def main(args):
         if rank == 0:
             print(json.dumps({"cpu_branch": cpu_branch_measure(args, dev)}))
         return
+    if args.mode == "fill-step":
+        if rank == 0:
+            print(json.dumps({"fill_step": fill_step_measure(args, dev, bp_gbs)}))
+        return
     if args.mode == "workloads":
         res = {n: decode_workload_measure(n, args, dev, (b_pcie, b_cpu), hbm_peak, peak_src, rank == 0, bp_gbs)
                for n in EXTRA_WORKLOADS}
@@ -773,6 +777,99 @@ def cpu_branch_measure(args, dev, steps=32):
         run.close()
     out["branch_cost_us_per_layer"] = round(1e3 * (out["branch"]["ms_per_step"] - out["supplied"]["ms_per_step"]) / s.L, 2)
     return out
+
+
+def fill_step_measure(args, dev, b_p, calls=96, reps=6):
+    """The link-bound layer-step against its floor.  One Qwen3-shaped layer with
+    C = 8 slots and B_cpu = 0: every call routes the same 7 hot experts (resident
+    after the first call) and one expert that no call of the last 96 routed, so
+    each call fills exactly one 9.44 MB blob over the host link while the 7
+    resident experts stream from HBM.  The calls are graph-replayed back to back;
+    the same calls with the 8th expert hot too give the all-resident layer-step.
+    A fill step cannot be shorter than its fill, which cannot start before the
+    control kernel has picked the victim: the line reports the fill kernel's own
+    event time beside one blob at bench_bw's B_P, and what the step spends
+    outside the fill (control, the filled expert's down grid, the combine)."""
+    import torch
+    from dataclasses import replace
+    from serving_layer_moe_gb300 import MoECache
+    base = config(WORKLOAD)
+    s = replace(base.shape, L=1)
+    arena, offs = make_pool(s, base.seed, n_phys=32)
+    pool = torch.from_numpy(arena).pin_memory()
+    del arena
+    rng = np.random.default_rng(base.seed)
+    x = torch.from_numpy(rng.standard_normal((1, s.H)).astype(np.float32)).to(dev).to(torch.bfloat16).view(torch.int16)
+    w_d = torch.full((calls, 1, s.k), 1.0 / s.k, dtype=torch.float32, device=dev)
+    cpu = torch.zeros(1, s.k, s.H, dtype=torch.float32, device=dev)
+    out_all = torch.empty(calls, 1, s.H, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    res = {"workload": f"{WORKLOAD} shape, one layer, C = {s.k} slots, B_cpu = 0: 7 hot experts + one expert "
+                       f"not routed in the last {calls} calls (exactly one fill per call)",
+           "calls_timed": calls * reps, "B_P_gbs": round(b_p, 1), "blob_bytes": s.blob_bytes}
+    for mode in ("one_fill", "all_resident"):
+        cache = MoECache(L=1, E=s.E, H=s.H, I=s.I, top_k=s.k, max_tokens=1, wdtype=s.wdtype, adtype=s.adtype,
+                         host_pool=pool, blob_offsets=offs, n_slots=s.k, max_fetch=s.k,
+                         bw_pcie_mbps=int(b_p * 1000), bw_cpu_mbps=0, device=dev.index or 0)
+        ids = np.empty((calls, 1, s.k), np.int32)
+        for c in range(calls):
+            ids[c, 0, :s.k - 1] = np.arange(s.k - 1)
+            ids[c, 0, s.k - 1] = s.k - 1 + (c % (s.E - s.k + 1) if mode == "one_fill" else 0)
+        i_d = torch.from_numpy(ids).to(dev)
+
+        def enqueue():
+            for c in range(calls):
+                cache.decode_ptrs(0, 1, x.data_ptr(), i_d[c].data_ptr(), w_d[c].data_ptr(), cpu.data_ptr(),
+                                  out_all[c].data_ptr(), None, stream.cuda_stream)
+
+        with torch.cuda.stream(stream):
+            enqueue()                       # eager: fills the hot experts
+        cache.plan()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            enqueue()
+        cache.plan()
+        with torch.cuda.stream(stream):
+            g.replay()
+        cache.plan()
+        cnt0 = cache.state()[3].copy()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        cache.plan()
+        ms = e0.elapsed_time(e1)
+        dcnt = cache.state()[3].copy() - cnt0
+        # kernel groups: event pairs in a second graph of the same calls
+        cache.profile_start()
+        pg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(pg, stream=stream):
+            enqueue()
+        cache.profile_pause()
+        cache.plan()
+        prof = {k: [0.0, 0] for k in cache.PROFILE_KINDS}
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                pg.replay()
+                for k, (ms_k, n_k) in cache.profile_read().items():
+                    prof[k][0] += ms_k
+                    prof[k][1] += n_k
+        cache.profile_stop()
+        cache.close()
+        r = {"us_per_call": round(1e3 * ms / (calls * reps), 2), "fills": int(dcnt[2]), "hits": int(dcnt[0]),
+             "cpu_assigned": int(dcnt[3]),
+             "group_us_per_call": {k: round(1e3 * v[0] / max(1, v[1]), 2) for k, v in prof.items() if v[1]}}
+        res[mode] = r
+    fill_ev = res["one_fill"]["group_us_per_call"].get("fill", 0.0)
+    res["blob_at_B_P_us"] = round(s.blob_bytes / (b_p * 1e9) * 1e6, 2)
+    res["fill_kernel_us"] = fill_ev
+    res["outside_fill_us"] = round(res["one_fill"]["us_per_call"] - fill_ev, 2)
+    res["note"] = ("fill_kernel_us: event pair around the fill kernel in a profiling graph of the same calls; "
+                   "B_P is a long-transfer rate, one blob alone takes longer (first-byte latency and ramp); "
+                   "outside_fill_us: control kernel + filled-expert down grid + combine + launch gaps")
+    return res
 
 
 # The other decode workloads, measured beside the headline: (untimed prefix, timed
