@@ -505,7 +505,10 @@ def main(args):
     dev = torch.device("cuda", local)
     if args.mode == "prefill":
         if rank == 0:
-            print(json.dumps({"prefill": prefill_measure(args, dev, local)}))
+            res = {"prefill": prefill_measure(args, dev, local)}
+            if not args.no_nvfp4:
+                res["prefill_mxfp4"] = prefill_fp4_measure(args, dev, local, "mxfp4")
+            print(json.dumps(res))
         return
     if args.mode == "profile-decode":
         return profile_case(args, dev)
