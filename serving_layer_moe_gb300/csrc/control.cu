@@ -97,17 +97,18 @@ __device__ __forceinline__ unsigned long long key_of_fast(const CtrlArgs& a, con
 
 // shared scalars of the control CTA
 struct CtrlScalars {
-  int bad, u, h, m, q, keff, ncand, digit, kth, read_hits, read_misses, pool_n, enough;
+  int bad, u, h, m, q, keff, ncand, read_hits, read_misses, pool_n, enough;
+  int rdigit[2], rkth[2], rstop[2];   // radix select: one result per pass, double-buffered
   unsigned long long clock0;
 };
 
-// kSel: 0 = K <= 32 by warp minima, 1 = radix select, 2 = K <= kPoolMaxK from the
-// kept candidate pool (rebuilt by radix select when it runs short)
+// kSel: 1 = radix select over all slots on every call (K > kPoolMaxK), 2 = K <=
+// kPoolMaxK from the kept candidate pool (rebuilt by radix select when it runs short)
 template <int kSel>
 __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ CtrlScalars sc;
-  __shared__ unsigned long long wcand[(kCtrlThreads / 32) * 32];   // per-warp sorted candidates (K <= 32)
+  __shared__ unsigned long long wcand[2 * (kCtrlThreads / 32)];   // per-warp key minimum and maximum
   const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
   const int E = a.E, NW = (E + 31) >> 5;
   const int P = a.T * a.k;
@@ -128,9 +129,9 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
   int32_t* miss_list = uniq_cls + U;                                               // [U]
   int32_t* gcnt = miss_list + U;                                                   // [U + 2]
   int32_t* vict = gcnt + U + 2;                                                    // [K]
-  uint32_t* hist = reinterpret_cast<uint32_t*>(vict + a.K);                        // [256]
+  uint32_t* hist = reinterpret_cast<uint32_t*>(vict + a.K);                        // [2][256]
   unsigned long long* cand = reinterpret_cast<unsigned long long*>(
-      (reinterpret_cast<uintptr_t>(hist + 256) + 7) & ~uintptr_t(7));               // [max(K, kPoolN)]
+      (reinterpret_cast<uintptr_t>(hist + 512) + 7) & ~uintptr_t(7));               // [max(K, kPoolN)]
   unsigned long long* s_pool = cand + (a.K > kPoolN ? a.K : kPoolN);               // [kPoolN]
 
   int32_t* s2e = a.tab.s2e;
@@ -192,7 +193,7 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
   }
   pdl_wait();       // the routed ids may come from the preceding kernel
   pdl_trigger();
-  if (kSel == 2 && P + a.n_shared <= 32 && NW <= 32) {
+  if (kSel == 2 && a.K <= kWarpPathMaxK && P + a.n_shared <= 32 && NW <= 32) {
     // ---- one warp for calls of at most 32 routed pairs ---------------------------
     // The steps below for a handful of pairs, in warp 0 with ballots and warp
     // barriers instead of block barriers.  Two block barriers remain: one makes
@@ -436,27 +437,91 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
     }
     return a.cache_keys ? rawkey[s] : (((unsigned long long)stamp[s] << kSlotBits) | (unsigned long long)s);
   };
-  // The n_want smallest keys (keyfn; keys unique, n_want <= number of keys),
-  // emitted ascending as emit(rank, key): MSB radix select with 8-bit digits,
-  // then a rank sort of the candidates.
+  // The n_want smallest keys (keyfn; keys unique among the finite ones, n_want <=
+  // number of finite keys), emitted ascending as emit(rank, key): MSB radix select
+  // with 8-bit digits, then a rank sort of the candidates.
+  //   * A thread keeps the keys of its slots in registers (C <= 8 threads' worth).
+  //   * Each pass has two block barriers: the histograms and the per-pass results
+  //     are double-buffered, and the next pass's histogram is cleared by warps
+  //     1.. while warp 0 scans this one.
+  //   * It stops as soon as the bucket holding the n_want-th key is needed whole:
+  //     stamps are unique (only empty slots share stamp 0), so after the stamp's
+  //     digits the buckets hold single keys.  The selected keys are then every key
+  //     <= prefix | (bits below the last digit).
   auto radix_smallest = [&](int n_want, auto keyfn, auto emit) {
+    constexpr int KPT = 8;
+    const bool in_regs = C <= KPT * nt;
+    unsigned long long mk[KPT];
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+      const int s = tid + j * nt;
+      mk[j] = (in_regs && s < C) ? keyfn(s) : ~0ull;
+    }
     const unsigned long long maxkey = (sc.clock0 << kSlotBits) | (kMaxSlots - 1);
     const int top = 63 - __clzll((long long)maxkey);
+    // The bits above the highest bit where the smallest and the largest finite key
+    // differ are the same for every finite key: the first digit is the 8 bits
+    // ending at that bit (so the first pass spreads the keys over 256 buckets
+    // instead of the few a byte-aligned top digit would use), the last digit may
+    // be narrower.  (Keys in registers only; otherwise the top byte.)
+    int hib = (top / 8) * 8 + 7;   // highest bit of the first digit
     unsigned long long prefix = 0ull, maskhi = 0ull;
-    int kth = n_want;  // 1-based rank still to find below the current prefix
-    for (int shift = (top / 8) * 8; shift >= 0; shift -= 8) {
-      for (int i = tid; i < 256; i += nt) hist[i] = 0u;
-      if (tid == 0) sc.ncand = 0;
-      __syncthreads();
-      for (int s = tid; s < C; s += nt) {
-        const unsigned long long key = keyfn(s);
-        if ((key & maskhi) == prefix) atomicAdd(&hist[(key >> shift) & 255ull], 1u);
+    if (in_regs) {
+      unsigned long long lo = ~0ull, hi = 0ull;
+#pragma unroll
+      for (int j = 0; j < KPT; ++j) {
+        const unsigned long long key = mk[j];
+        if (tid + j * nt < C && key != ~0ull) { lo = key < lo ? key : lo; hi = key > hi ? key : hi; }
       }
+      const unsigned lhi = __reduce_min_sync(0xffffffffu, (unsigned)(lo >> 32));
+      const unsigned llo = __reduce_min_sync(0xffffffffu, (unsigned)(lo >> 32) == lhi ? (unsigned)lo : ~0u);
+      const unsigned hhi = __reduce_max_sync(0xffffffffu, (unsigned)(hi >> 32));
+      const unsigned hlo = __reduce_max_sync(0xffffffffu, (unsigned)(hi >> 32) == hhi ? (unsigned)hi : 0u);
+      if (lane == 0) { wcand[2 * warp] = ((unsigned long long)lhi << 32) | llo; wcand[2 * warp + 1] = ((unsigned long long)hhi << 32) | hlo; }
+    }
+    for (int i = tid; i < 256; i += nt) hist[i] = 0u;
+    if (tid == 0) sc.ncand = 0;
+    __syncthreads();
+    if (in_regs) {
+      unsigned long long lo = ~0ull, hi = 0ull;
+      for (int w = 0; w < (nt >> 5); ++w) {
+        lo = wcand[2 * w] < lo ? wcand[2 * w] : lo;
+        hi = wcand[2 * w + 1] > hi ? wcand[2 * w + 1] : hi;
+      }
+      if (lo <= hi) {   // some finite key (always: n_want >= 1 finite keys)
+        const unsigned long long diff = lo ^ hi;
+        hib = diff ? 63 - __clzll((long long)diff) : 0;
+        maskhi = hib + 1 >= 64 ? 0ull : ~((1ull << (hib + 1)) - 1ull);
+        prefix = lo & maskhi;
+      }
+    }
+    int kth = n_want;  // 1-based rank still to find below the current prefix
+    int last_shift = 0;
+    int pass = 0;
+    for (int lo_bit = hib - 7;; lo_bit -= 8, ++pass) {
+      const int shift = lo_bit > 0 ? lo_bit : 0;
+      const unsigned long long dmask = (1ull << (lo_bit >= 0 ? 8 : 8 + lo_bit)) - 1ull;   // digit bits
+      uint32_t* hc = hist + (pass & 1) * 256;
+      uint32_t* hn = hist + ((pass + 1) & 1) * 256;
+      if (in_regs) {
+#pragma unroll
+        for (int j = 0; j < KPT; ++j) {
+          const unsigned long long key = mk[j];
+          if (tid + j * nt < C && (key & maskhi) == prefix) atomicAdd(&hc[(key >> shift) & dmask], 1u);
+        }
+      } else {
+        for (int s = tid; s < C; s += nt) {
+          const unsigned long long key = keyfn(s);
+          if ((key & maskhi) == prefix) atomicAdd(&hc[(key >> shift) & dmask], 1u);
+        }
+      }
+      if (warp != 0)
+        for (int i = tid - 32; i < 256; i += nt - 32) hn[i] = 0u;
       __syncthreads();
-      if (tid < 32) {
+      if (warp == 0) {
         int c = 0;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) c += (int)hist[lane * 8 + j];
+        for (int j = 0; j < 8; ++j) c += (int)hc[lane * 8 + j];
         int incl = c;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -467,34 +532,54 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
         if ((excl < kth) && (kth <= incl)) {
           int run = excl, d = lane * 8;
           for (int j = 0; j < 8; ++j) {
-            const int hj = (int)hist[lane * 8 + j];
+            const int hj = (int)hc[lane * 8 + j];
             if (run + hj >= kth) { d = lane * 8 + j; break; }
             run += hj;
           }
-          sc.digit = d;
-          sc.kth = kth - run;
+          sc.rdigit[pass & 1] = d;
+          sc.rkth[pass & 1] = kth - run;
+          sc.rstop[pass & 1] = (int)hc[d] == kth - run;
         }
       }
       __syncthreads();
-      prefix |= (unsigned long long)sc.digit << shift;
-      maskhi |= 255ull << shift;
-      kth = sc.kth;
-      __syncthreads();
+      prefix |= (unsigned long long)sc.rdigit[pass & 1] << shift;
+      maskhi |= dmask << shift;
+      kth = sc.rkth[pass & 1];
+      last_shift = shift;
+      if (sc.rstop[pass & 1] || shift == 0) break;
     }
-    // prefix is now the n_want-th smallest key; exactly n_want keys are <= it
-    for (int s = tid; s < C; s += nt) {
-      const unsigned long long key = keyfn(s);
-      if (key <= prefix) {
-        const int i = atomicAdd(&sc.ncand, 1);
-        if (i < n_want) cand[i] = key;
+    // exactly n_want keys are <= thr
+    const unsigned long long thr = prefix | ((1ull << last_shift) - 1ull);
+    auto collect = [&](bool valid, unsigned long long key) {   // warp-uniform call
+      const bool in = valid && key <= thr;
+      const uint32_t bal = __ballot_sync(0xffffffffu, in);
+      int base = 0;
+      if (bal && lane == 0) base = atomicAdd(&sc.ncand, __popc(bal));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      const int i = base + __popc(bal & lanemask_lt());
+      if (in && i < n_want) cand[i] = key;
+    };
+    if (in_regs) {
+#pragma unroll
+      for (int j = 0; j < KPT; ++j) collect(tid + j * nt < C, mk[j]);
+    } else {
+      for (int s0 = warp * 32; s0 < C; s0 += nt) {
+        const int s = s0 + lane;
+        collect(s < C, s < C ? keyfn(s) : ~0ull);
       }
     }
     __syncthreads();
-    for (int i = tid; i < n_want; i += nt) {
-      const unsigned long long ki = cand[i];
+    // ranks: four threads per candidate, each over a quarter of the list
+    const int sub = tid & 3;
+    for (int i0 = 0; i0 < n_want; i0 += nt >> 2) {   // uniform trip count
+      const int i = i0 + (tid >> 2);
+      const unsigned long long ki = i < n_want ? cand[i] : 0ull;
       int r = 0;
-      for (int j = 0; j < n_want; ++j) r += (cand[j] < ki);
-      emit(r, ki);
+#pragma unroll 8
+      for (int j = sub; j < n_want; j += 4) r += (cand[j] < ki);
+      r += __shfl_xor_sync(0xffffffffu, r, 1);
+      r += __shfl_xor_sync(0xffffffffu, r, 2);
+      if (i < n_want && sub == 0) emit(r, ki);
     }
     __syncthreads();
   };
@@ -507,29 +592,32 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
     // is larger still; so the valid entries (key unchanged) are exactly the slots
     // below that bound and the keff smallest evictable keys are the first keff
     // valid entries that are not this call's hits, whenever there are that many.
+    // One entry per thread (n <= kPoolN = the CTA's threads); its rank among the
+    // valid entries is a ballot prefix over the warps.
+    __shared__ int s_wcnt[kCtrlThreads / 32];
+    bool enough = false;
     for (int attempt = 0; attempt < 2; ++attempt) {
-      if (warp == 0) {
-        const int pn = sc.pool_n;
-        int taken = 0;
-        for (int i0 = 0; i0 < pn; i0 += 32) {
-          const int i = i0 + lane;
-          const unsigned long long k = i < pn ? s_pool[i] : ~0ull;
-          const bool ok = i < pn && key_of((int)(k & (kMaxSlots - 1))) == k;
-          const uint32_t bal = __ballot_sync(0xffffffffu, ok);
-          const int r = taken + __popc(bal & lanemask_lt());
-          if (ok && r < keff) vict[r] = (int)(k & (kMaxSlots - 1));
-          taken += __popc(bal);
-        }
-        if (lane == 0) sc.enough = taken >= keff;
-      }
+      const int pn = sc.pool_n;
+      const unsigned long long k = tid < pn ? s_pool[tid] : ~0ull;
+      const bool ok = tid < pn && key_of((int)(k & (kMaxSlots - 1))) == k;
+      const uint32_t bal = __ballot_sync(0xffffffffu, ok);
+      if (lane == 0) s_wcnt[warp] = __popc(bal);
       __syncthreads();
-      if (sc.enough || attempt == 1) break;
-      // rebuild: the kPoolN smallest keys over all slots (hits included); with
-      // C <= kPoolN every slot, so keff <= C - h entries are always evictable
-      const int n = C < kPoolN ? C : kPoolN;
-      radix_smallest(n, raw_key, [&](int r, unsigned long long key) {
-        s_pool[r] = key;
-        a.tab.pool[r] = key;
+      int before = 0, total = 0;
+      for (int w2 = 0; w2 < (nt >> 5); ++w2) {
+        const int c = s_wcnt[w2];
+        before += w2 < warp ? c : 0;
+        total += c;
+      }
+      const int r = before + __popc(bal & lanemask_lt());
+      if (ok && r < keff) vict[r] = (int)(k & (kMaxSlots - 1));
+      enough = total >= keff;   // the same in every thread
+      if (enough || attempt == 1) break;
+      // rebuild: the n smallest keys over all slots (hits included)
+      const int n = pool_size(a.K, C);
+      radix_smallest(n, raw_key, [&](int r2, unsigned long long key) {
+        s_pool[r2] = key;
+        a.tab.pool[r2] = key;
       });
       if (tid == 0) {
         sc.pool_n = n;
@@ -537,57 +625,11 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
       }
       __syncthreads();
     }
-  } else if (kSel == 0 && keff > 0) {
-    // each warp: its keff smallest keys, ascending, by repeated warp-minimum; a
-    // thread holds the effective keys of its slots in registers (C <= 8 * 512)
-    // and a 64-bit warp minimum is two 32-bit reductions (high word, then the
-    // low word among the lanes that hold the minimal high word)
-    constexpr int KPT = 8;
-    const bool in_regs = C <= KPT * nt;
-    unsigned long long mykeys[KPT];
-#pragma unroll
-    for (int j = 0; j < KPT; ++j) {
-      const int s = tid + j * nt;
-      mykeys[j] = (in_regs && s < C) ? key_of(s) : ~0ull;
-    }
-    unsigned long long last = 0ull;
-    bool first = true;
-    for (int r = 0; r < keff; ++r) {
-      unsigned long long mine = ~0ull;
-      if (in_regs) {
-#pragma unroll
-        for (int j = 0; j < KPT; ++j) {
-          const unsigned long long key = mykeys[j];
-          if ((first || key > last) && key < mine) mine = key;
-        }
-      } else {
-        for (int s = tid; s < C; s += nt) {
-          const unsigned long long key = key_of(s);
-          if ((first || key > last) && key < mine) mine = key;
-        }
-      }
-      const unsigned mhi = __reduce_min_sync(0xffffffffu, (unsigned)(mine >> 32));
-      const unsigned mlo = __reduce_min_sync(0xffffffffu, (unsigned)(mine >> 32) == mhi ? (unsigned)mine : ~0u);
-      const unsigned long long wmin = ((unsigned long long)mhi << 32) | mlo;
-      if (lane == 0) wcand[warp * 32 + r] = wmin;
-      last = wmin;
-      first = false;
-    }
-    __syncthreads();
-    if (warp == 0) {  // merge the sorted per-warp lists: lane l walks warp l's list
-      const int nwarps = nt >> 5;
-      int ptr = 0;
-      for (int r = 0; r < keff; ++r) {
-        const unsigned long long head = (lane < nwarps && ptr < keff) ? wcand[lane * 32 + ptr] : ~0ull;
-        const unsigned mhi = __reduce_min_sync(0xffffffffu, (unsigned)(head >> 32));
-        const unsigned mlo = __reduce_min_sync(0xffffffffu, (unsigned)(head >> 32) == mhi ? (unsigned)head : ~0u);
-        const unsigned long long mn = ((unsigned long long)mhi << 32) | mlo;
-        const uint32_t owner = __ballot_sync(0xffffffffu, head == mn);
-        if (lane == __ffs(owner) - 1) ++ptr;
-        if (lane == 0) vict[r] = (mn == ~0ull) ? -1 : (int)(mn & (kMaxSlots - 1));
-      }
-    }
-  } else if (kSel == 1 && keff > 0) {
+    // More of this call's hits among the n oldest slots than n - keff: the exact
+    // selection over all slots for this call
+    if (!enough)
+      radix_smallest(keff, key_of, [&](int r2, unsigned long long key) { vict[r2] = (int32_t)(key & (kMaxSlots - 1)); });
+  } else if (kSel == 1 && keff > 0) {   // K above the pool's reach: the exact selection every call
     radix_smallest(keff, key_of, [&](int r, unsigned long long key) { vict[r] = (int32_t)(key & (kMaxSlots - 1)); });
   }
   for (int i = keff + tid; i < a.K; i += nt) vict[i] = -1;
@@ -731,18 +773,17 @@ cudaError_t launch_decode_control(const Shape& sh, int layer, int T, int C, int 
   a.umax = min(sh.E, T * sh.k);
   const int NW = (sh.E + 31) / 32;
   const size_t base = (size_t)sh.E * 4 + (size_t)T * sh.k * 4 + (size_t)(2 * NW + 1) * 4 +
-                      (size_t)(6 * a.umax + 2) * 4 + (size_t)K * 4 + 256 * 4 + 8 +
+                      (size_t)(6 * a.umax + 2) * 4 + (size_t)K * 4 + 512 * 4 + 8 +
                       (size_t)(K > kPoolN ? K : kPoolN) * 8 + (size_t)kPoolN * 8 + 16;
   a.cache_keys = (C <= kSmemKeyCap && base + (size_t)C * 12 <= kCtrlSmemLimit) ? 1 : 0;
   const size_t smem = base + (a.cache_keys ? (size_t)C * 12 : 0);
   if (smem > kCtrlSmemLimit) return cudaErrorInvalidConfiguration;
   if (K <= kPoolMaxK) return launch_pdl(decode_control_kernel<2>, dim3(1), dim3(kCtrlThreads), smem, s, a);
-  if (K <= 32) return launch_pdl(decode_control_kernel<0>, dim3(1), dim3(kCtrlThreads), smem, s, a);
   return launch_pdl(decode_control_kernel<1>, dim3(1), dim3(kCtrlThreads), smem, s, a);
 }
 
 cudaError_t setup_control_kernels() {
-  for (auto k : {decode_control_kernel<0>, decode_control_kernel<1>, decode_control_kernel<2>}) {
+  for (auto k : {decode_control_kernel<1>, decode_control_kernel<2>}) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCtrlSmemLimit);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, kDecodeCarveout);
     if (e != cudaSuccess) return e;

@@ -80,10 +80,15 @@ struct CacheTables {
   uint64_t* pool;         // [kPoolN + 1]: oldest LRU keys at the last rebuild, ascending; [kPoolN] = count
 };
 
-// Decode victim candidates kept between calls (K <= kPoolMaxK): the kPoolN
-// smallest LRU keys as of the last full selection.
-constexpr int kPoolN = 64;
-constexpr int kPoolMaxK = 16;
+// Decode victim candidates kept between calls (K <= kPoolMaxK): the n smallest
+// LRU keys as of the last full selection, n = pool_size(K, C) <= kPoolN.
+constexpr int kPoolN = 512;
+constexpr int kPoolMaxK = 128;
+constexpr int kWarpPathMaxK = 16;   // the control kernel's one-warp path
+__host__ __device__ constexpr int pool_size(int K, int C) {
+  const int want = 4 * K < 64 ? 64 : (4 * K > kPoolN ? kPoolN : 4 * K);
+  return C < want ? C : want;
+}
 
 struct Shape {
   int L, E, H, I, k;

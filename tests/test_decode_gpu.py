@@ -194,12 +194,23 @@ def test_odd_expert_count_and_top3():
 
 
 def test_radix_victim_path_small():
-    # K = min(E, T*k) = 64 > 32 selects victims by radix select
+    # K = min(E, T*k) = 64: the block-wide path with the kept pool of 256 candidates,
+    # rebuilt by radix select whenever it runs short
     from workloads import Config
     cfg = Config("radix", _small_shape(64, 4), T=16, steps=12, capacity=40, routing="softmax_bias", bias_std=0.5,
                  seed=92)
     res = run_decode_parity(cfg, (1000, 1000), fp_every=5)
     _ok(res)
+
+
+def test_exact_select_path_above_the_pool():
+    # K = min(E, T*k) = 192 > 128: the radix select over all slots on every call
+    from workloads import Config
+    cfg = Config("radix_k192", _small_shape(256, 8), T=24, steps=10, capacity=150, routing="softmax_bias",
+                 bias_std=0.5, seed=93)
+    res = run_decode_parity(cfg, (1000, 1000), fp_every=7)
+    _ok(res)
+    assert res.fills > 0 and res.cpu_pairs > 0
 
 
 def test_random_resizes_grow_and_shrink():
