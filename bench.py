@@ -962,8 +962,9 @@ def decode_workload_measure(name, args, dev, bw_measured, hbm_peak, peak_src, wi
 def profile_case(args, dev):
     """A small decode case for ncu captures (a few GB on the device): the shape of
     --profile-workload (default the qwen3 b1 one) with --profile-layers layers and
-    256 slots (--capacity to change), --steps eager steps of single decode calls,
-    no graph, no timing.  With --profile-allhit every step replays step 0, so all
+    256 slots (--capacity to change), the workload's bandwidth split if it fixes
+    one (else every miss fills), --steps eager steps of single decode calls, no
+    graph, no timing.  With --profile-allhit every step replays step 0, so all
     routed experts are resident after the first."""
     import torch
     from serving_layer_moe_gb300 import MoECache
@@ -975,21 +976,24 @@ def profile_case(args, dev):
     arena, offs = make_pool(s, cfg.seed, n_phys=min(16, s.n_flat))
     pool = torch.from_numpy(arena).pin_memory()
     shared = make_shared(s, cfg.seed) if s.n_shared else None
+    bw = cfg.bw_mbps or (192000, 0)   # the workload's split where it fixes one, else every miss fills
     cache = MoECache(L=s.L, E=s.E, H=s.H, I=s.I, top_k=s.k, max_tokens=cfg.T, wdtype=s.wdtype, adtype=s.adtype,
                      host_pool=pool, blob_offsets=offs, shared=shared, n_slots=args.capacity or 256,
-                     bw_pcie_mbps=192000, bw_cpu_mbps=0, device=dev.index or 0)
+                     bw_pcie_mbps=bw[0], bw_cpu_mbps=bw[1], device=dev.index or 0)
     ids, w = routing_trace(cfg)
     out = torch.empty(cfg.T, s.H, device=dev)
+    cpu = torch.zeros(cfg.T, s.k, s.H, device=dev)   # the CPU-assigned pairs' partial sums (zeros)
     for st0 in range(args.steps):
         st = 0 if args.profile_allhit else st0 % cfg.steps
         for l in range(s.L):
             xa = activations(cfg, st, l)
             x = torch.from_numpy(xa.view(np.int16) if xa.dtype == np.uint16 else xa).to(dev)
-            cache.decode(l, x, torch.from_numpy(ids[st, l]).to(dev), torch.from_numpy(w[st, l]).to(dev), out)
+            cache.decode(l, x, torch.from_numpy(ids[st, l]).to(dev), torch.from_numpy(w[st, l]).to(dev), out,
+                         cpu_part=cpu)
     torch.cuda.synchronize(dev)
     c = cache.state()[3]
     print(json.dumps({"profile_case": f"{name} shape, {s.L} layers, {int(cache.info()[1])} slots",
-                      "hits": int(c[0]), "misses": int(c[1]), "fills": int(c[2])}))
+                      "hits": int(c[0]), "misses": int(c[1]), "fills": int(c[2]), "cpu_assigned": int(c[3])}))
     cache.close()
 
 

@@ -133,6 +133,7 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
   unsigned long long* cand = reinterpret_cast<unsigned long long*>(
       (reinterpret_cast<uintptr_t>(hist + 512) + 7) & ~uintptr_t(7));               // [max(K, kPoolN)]
   unsigned long long* s_pool = cand + (a.K > kPoolN ? a.K : kPoolN);               // [kPoolN]
+  const int cand_cap = a.K > kPoolN ? a.K : kPoolN;
 
   int32_t* s2e = a.tab.s2e;
   uint64_t* stamp = a.tab.stamp;
@@ -559,9 +560,25 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
       const int i = base + __popc(bal & lanemask_lt());
       if (in && i < n_want) cand[i] = key;
     };
-    if (in_regs) {
+    if (in_regs) {   // every ballot first, then one shared atomic per warp
+      uint32_t bals[KPT];
+      int tot = 0;
 #pragma unroll
-      for (int j = 0; j < KPT; ++j) collect(tid + j * nt < C, mk[j]);
+      for (int j = 0; j < KPT; ++j) {
+        bals[j] = __ballot_sync(0xffffffffu, tid + j * nt < C && mk[j] <= thr);
+        tot += __popc(bals[j]);
+      }
+      int base = 0;
+      if (lane == 0 && tot) base = atomicAdd(&sc.ncand, tot);
+      base = __shfl_sync(0xffffffffu, base, 0);
+#pragma unroll
+      for (int j = 0; j < KPT; ++j) {
+        if ((bals[j] >> lane) & 1u) {
+          const int i = base + __popc(bals[j] & lanemask_lt());
+          if (i < n_want) cand[i] = mk[j];
+        }
+        base += __popc(bals[j]);
+      }
     } else {
       for (int s0 = warp * 32; s0 < C; s0 += nt) {
         const int s = s0 + lane;
@@ -569,17 +586,40 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
       }
     }
     __syncthreads();
-    // ranks: four threads per candidate, each over a quarter of the list
-    const int sub = tid & 3;
-    for (int i0 = 0; i0 < n_want; i0 += nt >> 2) {   // uniform trip count
-      const int i = i0 + (tid >> 2);
-      const unsigned long long ki = i < n_want ? cand[i] : 0ull;
-      int r = 0;
+    if (n_want > 128 && n_want <= nt && nt <= cand_cap) {
+      // many candidates (a pool rebuild): bitonic sort of nt keys, one per thread,
+      // the tail padded with all-ones keys.  Exchanges between lanes of a warp go
+      // by shuffles; the 10 of 45 steps (for 512) between warps go through
+      // shared memory.
+      unsigned long long v = tid < n_want ? cand[tid] : ~0ull;
+      for (int kk = 2; kk <= nt; kk <<= 1)
+        for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+          unsigned long long pv;
+          if (jj < 32) {
+            pv = __shfl_xor_sync(0xffffffffu, v, jj);
+          } else {
+            __syncthreads();
+            cand[tid] = v;
+            __syncthreads();
+            pv = cand[tid ^ jj];
+          }
+          const bool keep_min = ((tid & jj) == 0) == ((tid & kk) == 0);
+          v = keep_min ? (v < pv ? v : pv) : (v > pv ? v : pv);
+        }
+      if (tid < n_want) emit(tid, v);
+    } else {
+      // ranks: four threads per candidate, each over a quarter of the list
+      const int sub = tid & 3;
+      for (int i0 = 0; i0 < n_want; i0 += nt >> 2) {   // uniform trip count
+        const int i = i0 + (tid >> 2);
+        const unsigned long long ki = i < n_want ? cand[i] : 0ull;
+        int r = 0;
 #pragma unroll 8
-      for (int j = sub; j < n_want; j += 4) r += (cand[j] < ki);
-      r += __shfl_xor_sync(0xffffffffu, r, 1);
-      r += __shfl_xor_sync(0xffffffffu, r, 2);
-      if (i < n_want && sub == 0) emit(r, ki);
+        for (int j = sub; j < n_want; j += 4) r += (cand[j] < ki);
+        r += __shfl_xor_sync(0xffffffffu, r, 1);
+        r += __shfl_xor_sync(0xffffffffu, r, 2);
+        if (i < n_want && sub == 0) emit(r, ki);
+      }
     }
     __syncthreads();
   };
