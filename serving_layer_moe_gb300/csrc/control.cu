@@ -128,7 +128,8 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
   int32_t* uniq_cls = uniq_rank + U;                                               // [U] 0 hit, 1 fill, 2 cpu
   int32_t* miss_list = uniq_cls + U;                                               // [U]
   int32_t* gcnt = miss_list + U;                                                   // [U + 2]
-  int32_t* vict = gcnt + U + 2;                                                    // [K]
+  int32_t* ecnt = gcnt + U + 2;                                                    // [E] routed pairs per expert
+  int32_t* vict = ecnt + E;                                                        // [K]
   uint32_t* hist = reinterpret_cast<uint32_t*>(vict + a.K);                        // [2][256]
   unsigned long long* cand = reinterpret_cast<unsigned long long*>(
       (reinterpret_cast<uintptr_t>(hist + 512) + 7) & ~uintptr_t(7));               // [max(K, kPoolN)]
@@ -171,6 +172,7 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
     }
     for (int i = tid; i < NW; i += nt) ebits[i] = 0u;
     for (int i = tid; i < U + 2; i += nt) gcnt[i] = 0;
+    for (int i = tid; i < E; i += nt) ecnt[i] = 0;
     if (tid < E) lslot[tid] = ls;
     for (int e = tid + nt; e < E; e += nt) lslot[e] = a.tab.e2s[fbase + e];   // E above the CTA's threads
     if (kSel == 2 && tid < kPoolN) s_pool[tid] = pv;
@@ -355,78 +357,131 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
   for (int p = tid; p < P; p += nt) pid[p] = a.ids[p];
   __syncthreads();
 
-  // ---- 1. dedup: routed-expert bitmap ------------------------------------
+  // ---- 1. dedup: routed-expert bitmap and routed pairs per expert ---------
   for (int p = tid; p < P; p += nt) {
     const int e = pid[p];
-    if ((unsigned)e >= (unsigned)E) atomicOr(&sc.bad, 1);
-    else atomicOr(&ebits[e >> 5], 1u << (e & 31));
+    if ((unsigned)e >= (unsigned)E) {
+      atomicOr(&sc.bad, 1);
+    } else {
+      atomicOr(&ebits[e >> 5], 1u << (e & 31));
+      atomicAdd(&ecnt[e], 1);
+    }
   }
   __syncthreads();
-  if (tid < 32) {  // exclusive popcount prefix over the bitmap words
-    int running = 0;
-    for (int w0 = 0; w0 < NW; w0 += 32) {
-      const int w = w0 + lane;
-      const int c = (w < NW) ? __popc(ebits[w]) : 0;
-      int incl = c;
+  int u, h, m, q, keff;
+  // One thread per expert of the layer when E fits the CTA: thread e holds
+  // whether e is routed, a hit or a miss, and its ranks among them in ascending
+  // flat id (a ballot prefix over the warps), and takes every later step of e.
+  const bool by_expert = E <= nt;
+  __shared__ int s_wc[3][kCtrlThreads / 32];
+  bool e_hit = false, e_miss = false, e_fill = false;
+  int e_slot = -1, e_hrank = 0, e_mrank = 0, e_g = -1;
+  if (by_expert) {
+    // ---- 2. classification and ranks, one thread per expert ---------------
+    const int e = tid;
+    const bool present = e < E && ((ebits[e >> 5] >> (e & 31)) & 1u);
+    e_slot = present ? lslot[e] : -1;
+    e_hit = present && e_slot >= 0;
+    e_miss = present && e_slot < 0;
+    const uint32_t bpr = __ballot_sync(0xffffffffu, present);
+    const uint32_t bht = __ballot_sync(0xffffffffu, e_hit);
+    const uint32_t bms = __ballot_sync(0xffffffffu, e_miss);
+    if (lane == 0) { s_wc[0][warp] = __popc(bpr); s_wc[1][warp] = __popc(bht); s_wc[2][warp] = __popc(bms); }
+    __syncthreads();
+    int pb = 0;
+    u = 0; h = 0; m = 0;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
+    for (int w2 = 0; w2 < kCtrlThreads / 32; ++w2) {
+      const int c0 = s_wc[0][w2], c1 = s_wc[1][w2], c2 = s_wc[2][w2];
+      if (w2 < warp) { pb += c0; e_hrank += c1; e_mrank += c2; }
+      u += c0; h += c1; m += c2;
+    }
+    const uint32_t lt = lanemask_lt();
+    const int uidx = pb + __popc(bpr & lt);
+    e_hrank += __popc(bht & lt);   // hits before e
+    e_mrank += __popc(bms & lt);   // misses before e
+    // ---- 3. the split q (every thread) -----------------------------------------
+    const int V = C - h;  // slots this call may evict
+    q = 0;
+    if (m > 0) {
+      q = (int)q_star((uint32_t)m, a.bp, a.bc);
+      q = max(1, min(q, m));
+      q = min(q, min(a.K, V));
+      q = max(q, 0);
+    }
+    keff = max(0, min(a.K, V));
+    if (present) {
+      uniq_e[uidx] = e;
+      if (e_miss) miss_list[e_mrank] = uidx;
+    }
+    if (e < E) lslot[e] = present ? uidx : -1;   // from here on: e -> its unique index
+  } else {   // more experts than threads: the unique list from the bitmap's word prefix
+    if (tid < 32) {  // exclusive popcount prefix over the bitmap words
+      int running = 0;
+      for (int w0 = 0; w0 < NW; w0 += 32) {
+        const int w = w0 + lane;
+        const int c = (w < NW) ? __popc(ebits[w]) : 0;
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        if (w < NW) ebase[w] = running + incl - c;
+        running += __shfl_sync(0xffffffffu, incl, 31);
       }
-      if (w < NW) ebase[w] = running + incl - c;
-      running += __shfl_sync(0xffffffffu, incl, 31);
+      if (lane == 0) { ebase[NW] = running; sc.u = running; }
     }
-    if (lane == 0) { ebase[NW] = running; sc.u = running; }
-  }
-  __syncthreads();
-  const int u = sc.u;
-  // ---- 2. unique list (ascending flat id) and classification --------------
-  for (int e = tid; e < E; e += nt) {
-    const uint32_t wbits = ebits[e >> 5];
-    if (wbits & (1u << (e & 31))) {
-      const int idx = ebase[e >> 5] + __popc(wbits & ((1u << (e & 31)) - 1u));
-      uniq_e[idx] = e;
-      uniq_slot[idx] = lslot[e];
-    }
-  }
-  __syncthreads();
-  if (tid < 32) {  // hit / miss ranks in ascending flat id
-    int hb = 0, mb = 0;
-    for (int c0 = 0; c0 < u; c0 += 32) {
-      const int i = c0 + lane;
-      const bool valid = i < u;
-      const bool hit = valid && uniq_slot[i] >= 0;
-      const bool miss = valid && !hit;
-      const uint32_t bh = __ballot_sync(0xffffffffu, hit);
-      const uint32_t bm = __ballot_sync(0xffffffffu, miss);
-      if (hit) { uniq_rank[i] = hb + __popc(bh & lanemask_lt()); uniq_cls[i] = 0; }
-      if (miss) {
-        const int r = mb + __popc(bm & lanemask_lt());
-        uniq_rank[i] = r;
-        miss_list[r] = i;
-        uniq_cls[i] = 2;
+    __syncthreads();
+    u = sc.u;
+    // ---- 2. unique list (ascending flat id) and classification --------------
+    for (int e = tid; e < E; e += nt) {
+      const uint32_t wbits = ebits[e >> 5];
+      if (wbits & (1u << (e & 31))) {
+        const int idx = ebase[e >> 5] + __popc(wbits & ((1u << (e & 31)) - 1u));
+        uniq_e[idx] = e;
+        uniq_slot[idx] = lslot[e];
       }
-      hb += __popc(bh);
-      mb += __popc(bm);
     }
-    if (lane == 0) {
-      sc.h = hb;
-      sc.m = mb;
-      // ---- 3. the split q ----------------------------------------------------
-      const int V = C - hb;  // slots this call may evict
-      int q = 0;
-      if (mb > 0) {
-        q = (int)q_star((uint32_t)mb, a.bp, a.bc);
-        q = max(1, min(q, mb));
-        q = min(q, min(a.K, V));
-        q = max(q, 0);
+    __syncthreads();
+    if (tid < 32) {  // hit / miss ranks in ascending flat id
+      int hb = 0, mb = 0;
+      for (int c0 = 0; c0 < u; c0 += 32) {
+        const int i = c0 + lane;
+        const bool valid = i < u;
+        const bool hit = valid && uniq_slot[i] >= 0;
+        const bool miss = valid && !hit;
+        const uint32_t bh = __ballot_sync(0xffffffffu, hit);
+        const uint32_t bm = __ballot_sync(0xffffffffu, miss);
+        if (hit) { uniq_rank[i] = hb + __popc(bh & lanemask_lt()); uniq_cls[i] = 0; }
+        if (miss) {
+          const int r = mb + __popc(bm & lanemask_lt());
+          uniq_rank[i] = r;
+          miss_list[r] = i;
+          uniq_cls[i] = 2;
+        }
+        hb += __popc(bh);
+        mb += __popc(bm);
       }
-      sc.q = q;
-      sc.keff = max(0, min(a.K, V));
+      if (lane == 0) {
+        sc.h = hb;
+        sc.m = mb;
+        // ---- 3. the split q ----------------------------------------------------
+        const int V = C - hb;  // slots this call may evict
+        int q = 0;
+        if (mb > 0) {
+          q = (int)q_star((uint32_t)mb, a.bp, a.bc);
+          q = max(1, min(q, mb));
+          q = min(q, min(a.K, V));
+          q = max(q, 0);
+        }
+        sc.q = q;
+        sc.keff = max(0, min(a.K, V));
+      }
     }
+    __syncthreads();
+    h = sc.h; m = sc.m; q = sc.q; keff = sc.keff;
   }
-  __syncthreads();
-  const int h = sc.h, m = sc.m, q = sc.q, keff = sc.keff;
 
   // ---- 4. the K least-recently-used evictable slots, one pass ----------------
   // key(s) = (stamp << 20) | s, or all-ones when s holds one of this call's hits
@@ -675,108 +730,205 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
   for (int i = keff + tid; i < a.K; i += nt) vict[i] = -1;
   __syncthreads();
 
-  // ---- 5. rewrite: fills take victims in order, the rest go to the CPU ------
+  // ---- 5.-6. rewrite, recency, GPU expert index -----------------------------
+  // fills take victims in order, the rest go to the CPU; hits and fills in
+  // ascending flat id take the next clock values; GPU expert index: hits
+  // 0..h-1, the shared expert h, fills after
+  const int ns = a.n_shared;
+  const int nfirst = h + ns;
   for (int i = tid; i < a.K; i += nt) a.b.victims[i] = vict[i];
-  for (int r = tid; r < m; r += nt) {
-    const int i = miss_list[r];
-    const int f = fbase + uniq_e[i];
-    if (r < q) {
-      const int v = vict[r];
+  if (by_expert) {
+    const int e = tid;
+    e_fill = e_miss && e_mrank < q;
+    int slot = e_slot;
+    if (e_fill) {
+      const int f = fbase + e;
+      const int v = vict[e_mrank];
       const int old = a.cache_keys ? slotf[v] : s2e[v];
       if (old >= 0) a.tab.e2s[old] = -1;
       s2e[v] = f;
       a.tab.e2s[f] = v;
-      uniq_slot[i] = v;
-      uniq_cls[i] = 1;
-      a.b.fills[2 * r] = f;
-      a.b.fills[2 * r + 1] = v;
-    } else {
-      a.b.cpu[r - q] = f;
+      a.b.fills[2 * e_mrank] = f;
+      a.b.fills[2 * e_mrank + 1] = v;
+      slot = v;
+    } else if (e_miss) {
+      a.b.cpu[e_mrank - q] = fbase + e;
     }
-  }
-  __syncthreads();
+    // e_hrank hits and min(e_mrank, q) fills come before e
+    if (e_hit || e_fill) stamp[slot] = sc.clock0 + (unsigned long long)(e_hrank + min(e_mrank, q)) + 1ull;
+    if (tid == 0) {
+      *a.tab.clock = sc.clock0 + (unsigned long long)(h + q);
+      if (((sc.clock0 + (unsigned long long)(h + q)) >> (64 - kSlotBits)) != 0ull) atomicOr(&sc.bad, 2);
+    }
+    e_g = e_hit ? e_hrank : e_fill ? nfirst + e_mrank : -1;
+    if (e_g >= 0) a.b.gpu_w[e_g] = a.slots_base + (size_t)slot * a.S;
+    const int ui = e < E ? lslot[e] : -1;
+    if (ui >= 0) {
+      uniq_cls[ui] = e_hit ? 0 : e_fill ? 1 : 2;
+      uniq_slot[ui] = slot;
+      uniq_rank[ui] = e_g;
+    }
+  } else {
+    // ---- 5. rewrite: fills take victims in order, the rest go to the CPU ------
+    for (int r = tid; r < m; r += nt) {
+      const int i = miss_list[r];
+      const int f = fbase + uniq_e[i];
+      if (r < q) {
+        const int v = vict[r];
+        const int old = a.cache_keys ? slotf[v] : s2e[v];
+        if (old >= 0) a.tab.e2s[old] = -1;
+        s2e[v] = f;
+        a.tab.e2s[f] = v;
+        uniq_slot[i] = v;
+        uniq_cls[i] = 1;
+        a.b.fills[2 * r] = f;
+        a.b.fills[2 * r + 1] = v;
+      } else {
+        a.b.cpu[r - q] = f;
+      }
+    }
+    __syncthreads();
 
-  // ---- 6. recency: stamp GPU-run experts in ascending flat id ---------------
-  if (tid < 32) {
-    int tb = 0;
-    for (int c0 = 0; c0 < u; c0 += 32) {
-      const int i = c0 + lane;
-      const bool touched = (i < u) && uniq_cls[i] < 2;
-      const uint32_t bt = __ballot_sync(0xffffffffu, touched);
-      if (touched) stamp[uniq_slot[i]] = sc.clock0 + (unsigned long long)(tb + __popc(bt & lanemask_lt())) + 1ull;
-      tb += __popc(bt);
+    // ---- 6. recency: stamp GPU-run experts in ascending flat id ---------------
+    if (tid < 32) {
+      int tb = 0;
+      for (int c0 = 0; c0 < u; c0 += 32) {
+        const int i = c0 + lane;
+        const bool touched = (i < u) && uniq_cls[i] < 2;
+        const uint32_t bt = __ballot_sync(0xffffffffu, touched);
+        if (touched) stamp[uniq_slot[i]] = sc.clock0 + (unsigned long long)(tb + __popc(bt & lanemask_lt())) + 1ull;
+        tb += __popc(bt);
+      }
+      if (lane == 0) {
+        *a.tab.clock = sc.clock0 + (unsigned long long)tb;
+        if (((sc.clock0 + tb) >> (64 - kSlotBits)) != 0ull) atomicOr(&sc.bad, 2);
+      }
     }
-    if (lane == 0) {
-      *a.tab.clock = sc.clock0 + (unsigned long long)tb;
-      if (((sc.clock0 + tb) >> (64 - kSlotBits)) != 0ull) atomicOr(&sc.bad, 2);
+    // GPU expert index of each unique: hits 0..h-1, shared expert h, fills after
+    for (int i = tid; i < u; i += nt) {
+      const int cls = uniq_cls[i];
+      int g = -1;
+      if (cls == 0) g = uniq_rank[i];
+      else if (cls == 1) g = nfirst + uniq_rank[i];
+      uniq_rank[i] = g;  // reuse: GPU expert index (or -1)
+      if (g >= 0) a.b.gpu_w[g] = a.slots_base + (size_t)uniq_slot[i] * a.S;
     }
-  }
-  // GPU expert index of each unique: hits 0..h-1, shared expert h, fills after
-  const int ns = a.n_shared;
-  const int nfirst = h + ns;
-  for (int i = tid; i < u; i += nt) {
-    const int cls = uniq_cls[i];
-    int g = -1;
-    if (cls == 0) g = uniq_rank[i];
-    else if (cls == 1) g = nfirst + uniq_rank[i];
-    uniq_rank[i] = g;  // reuse: GPU expert index (or -1)
-    if (g >= 0) a.b.gpu_w[g] = a.slots_base + (size_t)uniq_slot[i] * a.S;
   }
   if (ns && tid == 0) a.b.gpu_w[h] = a.shared_blob;
   __syncthreads();
 
   // ---- 7. slot map and pair lists ---------------------------------------------
-  int my_hits = 0, my_misses = 0;
-  for (int p = tid; p < P; p += nt) {
-    const int e = pid[p];
-    int slot = -1;
-    if ((unsigned)e < (unsigned)E) {
-      const uint32_t wbits = ebits[e >> 5];
-      const int i = ebase[e >> 5] + __popc(wbits & ((1u << (e & 31)) - 1u));
-      const int cls = uniq_cls[i];
-      if (cls == 0) ++my_hits; else ++my_misses;
-      if (cls < 2) {
-        slot = uniq_slot[i];
-        atomicAdd(&gcnt[uniq_rank[i]], 1);
-      }
-    } else {
-      ++my_misses;
-    }
-    a.b.slot_map[p] = slot;
-    if (a.slot_map_out) a.slot_map_out[p] = slot;
-  }
-  if (my_hits) atomicAdd(&sc.read_hits, my_hits);
-  if (my_misses) atomicAdd(&sc.read_misses, my_misses);
   const int ngpu = nfirst + q;
-  if (ns && tid == 0) gcnt[h] = a.T;
-  __syncthreads();
-  if (tid < 32) {  // exclusive scan of pair counts -> offsets (gcnt becomes write cursors)
-    int running = 0;
-    for (int c0 = 0; c0 < ngpu; c0 += 32) {
-      const int g = c0 + lane;
-      const int c = g < ngpu ? gcnt[g] : 0;
-      int incl = c;
+  if (by_expert) {
+    // Pair counts of the hits and fills, exclusive prefix in GPU-index order
+    // (hits in ascending flat id, the shared expert, fills in ascending flat id):
+    // a warp scan per count and one block barrier; thread e keeps its expert's
+    // offset as the write cursor of its pairs.  The order of an expert's pairs
+    // within its list is not fixed (as in the other block-wide form): each pair's
+    // values are formed on their own.
+    const int e = tid;
+    const int c = (e_hit || e_fill) ? ecnt[e] : 0;
+    const int vh = e_hit ? c : 0, vf = e_fill ? c : 0;
+    int ih = vh, iff = vf;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int x = __shfl_up_sync(0xffffffffu, ih, o);
+      const int y = __shfl_up_sync(0xffffffffu, iff, o);
+      if (lane >= o) { ih += x; iff += y; }
+    }
+    if (lane == 31) { s_wc[0][warp] = ih; s_wc[1][warp] = iff; }
+    __syncthreads();
+    int bh = 0, bf = 0, th = 0, tf = 0;
+#pragma unroll
+    for (int w2 = 0; w2 < kCtrlThreads / 32; ++w2) {
+      const int x = s_wc[0][w2], y = s_wc[1][w2];
+      if (w2 < warp) { bh += x; bf += y; }
+      th += x;
+      tf += y;
+    }
+    const int fill_base = th + ns * a.T;   // the shared expert's pairs follow the hits'
+    if (e_g >= 0) {
+      const int off = e_hit ? bh + ih - vh : fill_base + bf + iff - vf;
+      a.b.gpu_off[e_g] = off;
+      ecnt[e] = off;
+    }
+    if (ns && tid == 0) a.b.gpu_off[h] = th;
+    if (tid == 0) a.b.gpu_off[ngpu] = fill_base + tf;
+    __syncthreads();
+    int my_hits = 0, my_misses = 0;
+    for (int p = tid; p < P; p += nt) {
+      const int e2 = pid[p];
+      int slot = -1;
+      if ((unsigned)e2 < (unsigned)E) {
+        const int i = lslot[e2];
+        const int cls = uniq_cls[i];
+        if (cls == 0) ++my_hits; else ++my_misses;
+        if (cls < 2) {
+          slot = uniq_slot[i];
+          a.b.gpu_pairs[atomicAdd(&ecnt[e2], 1)] = p;
+        }
+      } else {
+        ++my_misses;
       }
-      if (g < ngpu) { a.b.gpu_off[g] = running + incl - c; gcnt[g] = running + incl - c; }
-      running += __shfl_sync(0xffffffffu, incl, 31);
+      a.b.slot_map[p] = slot;
+      if (a.slot_map_out) a.slot_map_out[p] = slot;
     }
-    if (lane == 0) a.b.gpu_off[ngpu] = running;
-  }
-  __syncthreads();
-  for (int p = tid; p < P; p += nt) {
-    const int e = pid[p];
-    if ((unsigned)e < (unsigned)E) {
-      const uint32_t wbits = ebits[e >> 5];
-      const int i = ebase[e >> 5] + __popc(wbits & ((1u << (e & 31)) - 1u));
-      if (uniq_cls[i] < 2) a.b.gpu_pairs[atomicAdd(&gcnt[uniq_rank[i]], 1)] = p;
+    if (my_hits) atomicAdd(&sc.read_hits, my_hits);
+    if (my_misses) atomicAdd(&sc.read_misses, my_misses);
+    if (ns)
+      for (int t = tid; t < a.T; t += nt) a.b.gpu_pairs[th + t] = P + t;   // shared pairs after routed hits
+  } else {
+    int my_hits = 0, my_misses = 0;
+    for (int p = tid; p < P; p += nt) {
+      const int e = pid[p];
+      int slot = -1;
+      if ((unsigned)e < (unsigned)E) {
+        const uint32_t wbits = ebits[e >> 5];
+        const int i = by_expert ? lslot[e] : ebase[e >> 5] + __popc(wbits & ((1u << (e & 31)) - 1u));
+        const int cls = uniq_cls[i];
+        if (cls == 0) ++my_hits; else ++my_misses;
+        if (cls < 2) {
+          slot = uniq_slot[i];
+          atomicAdd(&gcnt[uniq_rank[i]], 1);
+        }
+      } else {
+        ++my_misses;
+      }
+      a.b.slot_map[p] = slot;
+      if (a.slot_map_out) a.slot_map_out[p] = slot;
     }
-  }
-  if (ns) {
-    for (int t = tid; t < a.T; t += nt) a.b.gpu_pairs[gcnt[h] + t] = P + t;  // shared pairs after routed ones
+    if (my_hits) atomicAdd(&sc.read_hits, my_hits);
+    if (my_misses) atomicAdd(&sc.read_misses, my_misses);
+    if (ns && tid == 0) gcnt[h] = a.T;
+    __syncthreads();
+    if (tid < 32) {  // exclusive scan of pair counts -> offsets (gcnt becomes write cursors)
+      int running = 0;
+      for (int c0 = 0; c0 < ngpu; c0 += 32) {
+        const int g = c0 + lane;
+        const int c = g < ngpu ? gcnt[g] : 0;
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        if (g < ngpu) { a.b.gpu_off[g] = running + incl - c; gcnt[g] = running + incl - c; }
+        running += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) a.b.gpu_off[ngpu] = running;
+    }
+    __syncthreads();
+    for (int p = tid; p < P; p += nt) {
+      const int e = pid[p];
+      if ((unsigned)e < (unsigned)E) {
+        const uint32_t wbits = ebits[e >> 5];
+        const int i = by_expert ? lslot[e] : ebase[e >> 5] + __popc(wbits & ((1u << (e & 31)) - 1u));
+        if (uniq_cls[i] < 2) a.b.gpu_pairs[atomicAdd(&gcnt[uniq_rank[i]], 1)] = p;
+      }
+    }
+    if (ns) {
+      for (int t = tid; t < a.T; t += nt) a.b.gpu_pairs[gcnt[h] + t] = P + t;  // shared pairs after routed ones
+    }
   }
 
   // ---- 8. plan scalars, counters, error word ------------------------------------
@@ -813,7 +965,7 @@ cudaError_t launch_decode_control(const Shape& sh, int layer, int T, int C, int 
   a.umax = min(sh.E, T * sh.k);
   const int NW = (sh.E + 31) / 32;
   const size_t base = (size_t)sh.E * 4 + (size_t)T * sh.k * 4 + (size_t)(2 * NW + 1) * 4 +
-                      (size_t)(6 * a.umax + 2) * 4 + (size_t)K * 4 + 512 * 4 + 8 +
+                      (size_t)(6 * a.umax + 2) * 4 + (size_t)sh.E * 4 + (size_t)K * 4 + 512 * 4 + 8 +
                       (size_t)(K > kPoolN ? K : kPoolN) * 8 + (size_t)kPoolN * 8 + 16;
   a.cache_keys = (C <= kSmemKeyCap && base + (size_t)C * 12 <= kCtrlSmemLimit) ? 1 : 0;
   const size_t smem = base + (a.cache_keys ? (size_t)C * 12 : 0);
