@@ -155,7 +155,7 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
     unsigned long long pv = 0ull;
     int pn = 0;
     if (kSel == 2) {
-      if (tid < kPoolN) pv = a.tab.pool[tid];
+      if (tid < pool_size(a.K, C)) pv = a.tab.pool[tid];   // the cache's pool size, not the capacity
       if (tid == 0) pn = (int)a.tab.pool[kPoolN];
     }
     int sv[kB];
@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
     for (int i = tid; i < E; i += nt) ecnt[i] = 0;
     if (tid < E) lslot[tid] = ls;
     for (int e = tid + nt; e < E; e += nt) lslot[e] = a.tab.e2s[fbase + e];   // E above the CTA's threads
-    if (kSel == 2 && tid < kPoolN) s_pool[tid] = pv;
+    if (kSel == 2 && tid < pool_size(a.K, C)) s_pool[tid] = pv;
 #pragma unroll
     for (int u = 0; u < kB; ++u) {
       const int i = tid + u * nt;
