@@ -69,6 +69,16 @@ RESIDENT_TRAFFIC = {0: (TRAFFIC_PER_LAYER_STEP, TRAFFIC_SOURCE), 1: (FUSED_TRAFF
 # captures (none yet: the roofline's traffic stays null).
 WORKLOAD_TRAFFIC: dict = {}
 WORKLOAD_TRAFFIC_SOURCE: dict = {}
+# The all-resident replays' pair (every routed expert + the shared one resident): DRAM
+# bytes per layer-step from ncu; the windows' launches mix hits and fills, so their
+# per-launch bytes vary and carry no ncu figure.
+ALL_RESIDENT_TRAFFIC = {
+    "dsv3_decode_slice": (398_800_000,
+                          "ncu dram__bytes_read.sum + dram__bytes_write.sum of gate_up_bulk_kernel + down_bulk_kernel "
+                          "pass 0, mean of the three all-resident layer-steps (9 experts, 396.4 MB algorithmic) in "
+                          "bench.py --mode profile-decode --steps 4 --profile-workload dsv3_decode_slice "
+                          "--profile-layers 4 --capacity 64; profiles/decode_dsv3_fp8_slice.md"),
+}
 
 
 def parse_args(argv=None):
@@ -467,12 +477,15 @@ KERNEL_NAMES = {
 }
 
 
-def roofline_from_groups(groups, hbm_peak, peak_src, traffic=None, traffic_source=None):
-    """The roofline object of the group with the most event time (all are HBM-bound)."""
+def roofline_from_groups(groups, hbm_peak, peak_src, traffic=None, traffic_source=None, split=None):
+    """The roofline object of the group with the most event time (all are HBM-bound).
+    split: the call took the split down grids (the resident group is the whole pair);
+    by default read from the groups (a "down_filled" group exists)."""
     kind, (b, ms, n) = max(groups.items(), key=lambda kv: kv[1][1])
     if ms <= 0 or n == 0:
         return None
-    split = "down_filled" in groups
+    if split is None:
+        split = "down_filled" in groups
     achieved = b / (ms / 1e3) / 1e9
     return {"bound": "hbm",
             "kernel": KERNEL_NAMES["gemv_resident_split" if (split and kind == "gemv_resident") else kind],
@@ -950,7 +963,9 @@ def decode_workload_measure(name, args, dev, bw_measured, hbm_peak, peak_src, wi
         run.profiled(3, same_step=True)
         rp, dr = run.profiled(16, same_step=True)
         rg = kernel_groups(s, rp, dr)
-        res["roofline_all_resident"] = roofline_from_groups({"gemv_resident": rg["gemv_resident"]}, hbm_peak, peak_src)
+        tr, trs = ALL_RESIDENT_TRAFFIC.get(name, (None, None))
+        res["roofline_all_resident"] = roofline_from_groups({"gemv_resident": rg["gemv_resident"]}, hbm_peak, peak_src,
+                                                            tr, trs, split="down_filled" in rg)
         res["roofline_all_resident_note"] = "one step's inputs replayed until every routed expert is resident; " \
                                             f"{int(dr[2])} fills during the 16 replays"
     run.close()
