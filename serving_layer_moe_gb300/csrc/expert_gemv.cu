@@ -1046,6 +1046,9 @@ __global__ void __launch_bounds__(256) gate_up_bulk_kernel(GemvArgs a, BulkGeom 
     for (int tp = pb; kJX == 0 && tp < pe; ++tp) {
       const int t = sp.tok[tp];
       float ag = 0.f, au = 0.f;
+      // unrolled: four chunks' independent FMA chains in flight; the sums keep
+      // their order, so h is the same bit for bit as the fill's
+#pragma unroll 4
       for (int c = lane; c < NCH; c += 32) {
         float dg = 0.f, du = 0.f;
         if constexpr (kFp4<WT>) {
