@@ -74,8 +74,15 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
 __device__ __forceinline__ uint32_t q_star(uint32_t m, uint32_t bp, uint32_t bc) {
   const uint64_t num = (uint64_t)m * bp;
   const uint64_t den = (uint64_t)bp + bc;
-  uint64_t q = num / den;
-  const uint64_t r = num - q * den;
+  uint64_t q, r;
+  if ((num >> 32) == 0 && (den >> 32) == 0) {   // the 32-bit divide (the 64-bit one is a long routine)
+    const uint32_t n32 = (uint32_t)num, d32 = (uint32_t)den;
+    q = n32 / d32;
+    r = n32 - (uint32_t)q * d32;
+  } else {
+    q = num / den;
+    r = num - q * den;
+  }
   if (2 * r > den) q += 1;
   else if (2 * r == den) q += (q & 1);
   return (uint32_t)q;
@@ -699,7 +706,8 @@ __global__ void __launch_bounds__(kCtrlThreads, 1) decode_control_kernel(CtrlArg
       if (lane == 0) s_wcnt[warp] = __popc(bal);
       __syncthreads();
       int before = 0, total = 0;
-      for (int w2 = 0; w2 < (nt >> 5); ++w2) {
+#pragma unroll
+      for (int w2 = 0; w2 < kCtrlThreads / 32; ++w2) {
         const int c = s_wcnt[w2];
         before += w2 < warp ? c : 0;
         total += c;
