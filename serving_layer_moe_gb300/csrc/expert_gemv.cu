@@ -1119,13 +1119,15 @@ __global__ void __launch_bounds__(256) gate_up_bulk_kernel(GemvArgs a, BulkGeom 
 // and 1 are two grids over the same row blocks: each publishes its y, counts
 // itself in arrive[block], and the second of the two (odd count before its
 // increment) forms the block's combine from y in global memory.
-template <int WT, bool kRing, int kJN, bool kPair = false>
+template <int WT, bool kRing, int kJN, bool kPair = false, bool kR8 = false>
 __global__ void __launch_bounds__((kRing && !kPair) || (!kRing && kJN > 0) ? 256 : 512) down_bulk_kernel(GemvArgs a, BulkGeom geo,
                                                         const float* __restrict__ w,
                                                         const float* __restrict__ cpu, float* __restrict__ out,
                                                         uint32_t* err) {
-  // kPair: two warps per ring stage (one expert each pair), each taking 8 of its rows
+  // kPair: two warps per ring stage (one expert each pair), each taking 8 of its rows;
+  // kR8: ring items of at most 8 rows, each warp accumulating 8 rows
   static_assert(!kPair || (kRing && kJN > 0), "pair mode is the straight-line ring path");
+  static_assert(!kR8 || (kRing && !kPair), "8-row items are a ring form");
   using F = WFmt<WT>;
   constexpr int V = F::V;
   constexpr int J = 32 / V;   // 16-byte chunks per lane per column segment (32 h values in registers)
@@ -1351,7 +1353,7 @@ __global__ void __launch_bounds__((kRing && !kPair) || (!kRing && kJN > 0) ? 256
     const int nrs = item_rows(sb);           // and its rows
     const float* sd = reinterpret_cast<const float*>(sp.w[g] + sd_off);
     const int pb = sp.off[g], pe = sp.off[g + 1];
-    constexpr int kRW = kPair ? 8 : kDownRows;   // rows this warp accumulates
+    constexpr int kRW = (kPair || kR8) ? 8 : kDownRows;   // rows this warp accumulates
     const int rbase = kPair ? 8 * half : 0;
     for (int tp = pb; tp < pe; ++tp) {
       const int pid = sp.pid[tp];
@@ -1416,7 +1418,7 @@ __global__ void __launch_bounds__((kRing && !kPair) || (!kRing && kJN > 0) ? 256
           }
         }
 #pragma unroll
-        for (int r = 0; r < kDownRows; ++r) {
+        for (int r = 0; r < kRW; ++r) {
           if (r < nrs) {
             const uint4* wrow = reinterpret_cast<const uint4*>(blk + (size_t)r * row_bytes);
             float d = 0.f;
@@ -1445,7 +1447,7 @@ __global__ void __launch_bounds__((kRing && !kPair) || (!kRing && kJN > 0) ? 256
       float v;
       int r;
       bool mine;
-      if constexpr (kPair) {
+      if constexpr (kPair || kR8) {
         v = reduce8(acc, lane);
         r = rbase + ((lane >> 2) & 7);
         mine = (lane & 3) == 0;
@@ -2031,8 +2033,8 @@ cudaError_t setup_gemv_kernels() {
                         (const void*)down_bulk_kernel<MOE_BF16, true, 3, true>,
                         (const void*)down_bulk_kernel<MOE_BF16, true, 4, true>,
                         (const void*)down_bulk_kernel<MOE_FP8E4M3_B128, true, 0>,
-                        (const void*)down_bulk_kernel<MOE_FP8E4M3_B128, true, 3>,
-                        (const void*)down_bulk_kernel<MOE_FP8E4M3_B128, true, 4>,
+                        (const void*)down_bulk_kernel<MOE_FP8E4M3_B128, true, 3, false, true>,
+                        (const void*)down_bulk_kernel<MOE_FP8E4M3_B128, true, 4, false, true>,
                         (const void*)down_bulk_kernel<MOE_F32, false, 0>, (const void*)down_bulk_kernel<MOE_BF16, false, 0>,
                         (const void*)down_bulk_kernel<MOE_BF16, false, 3>, (const void*)down_bulk_kernel<MOE_BF16, false, 4>,
                         (const void*)down_bulk_kernel<MOE_FP8E4M3_B128, false, 3>,
@@ -2173,7 +2175,10 @@ BulkGeom down_geom(const GemvArgs& a, int wdtype, int sms) {
   const size_t fixed = 256 + plan + up128(extra);
   if (fixed >= kRingBudget) { g.NS = 0; return g; }
   const size_t room = kRingBudget - fixed;
-  for (int RS = std::min(R, kDownRows); RS >= 1; --RS) {
+  // fp8 rows stream in items of at most 8 rows (the straight-line 8-row form;
+  // with 16 the DeepSeek-V3 slice got sub-blocks of 12 rows on 4 warps)
+  const int rs_max = wdtype == MOE_FP8E4M3_B128 ? 8 : kDownRows;
+  for (int RS = std::min(R, rs_max); RS >= 1; --RS) {
     g.SB = up128((size_t)RS * row);
     if (a.max_g <= 8 && 8 * g.SB <= room) {
       g.NS = 1;
@@ -2290,8 +2295,8 @@ cudaError_t launch_down_bulk(const GemvArgs& a, const BulkGeom& geo, bool ring, 
   };
   if constexpr (WT == MOE_FP8E4M3_B128) {   // the same for fp8 rows of 3 or 4 chunks per lane
     const int nch = a.I / 16;
-    if (nch == 96) return go(down_bulk_kernel<WT, true, 3>, geo.NW * 32);
-    if (nch == 128) return go(down_bulk_kernel<WT, true, 4>, geo.NW * 32);
+    if (geo.RS <= 8 && nch == 96) return go(down_bulk_kernel<WT, true, 3, false, true>, geo.NW * 32);
+    if (geo.RS <= 8 && nch == 128) return go(down_bulk_kernel<WT, true, 4, false, true>, geo.NW * 32);
   }
   if constexpr (WT == MOE_BF16) {   // rows of 3 or 4 chunks per lane: the unguarded straight-line path
     const int nch = a.I / 8;
