@@ -73,7 +73,7 @@ WORKLOAD_TRAFFIC_SOURCE: dict = {}
 # bytes per layer-step from ncu; the windows' launches mix hits and fills, so their
 # per-launch bytes vary and carry no ncu figure.
 ALL_RESIDENT_TRAFFIC = {
-    "dsv3_decode_slice": (398_800_000,
+    "dsv3_decode_slice": (399_100_000,
                           "ncu dram__bytes_read.sum + dram__bytes_write.sum of gate_up_bulk_kernel + down_bulk_kernel "
                           "pass 0, mean of the three all-resident layer-steps (9 experts, 396.4 MB algorithmic) in "
                           "bench.py --mode profile-decode --steps 4 --profile-workload dsv3_decode_slice "
