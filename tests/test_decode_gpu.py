@@ -282,6 +282,20 @@ def test_varying_T_on_one_cache():
 # ---- 4-bit experts: NVFP4 (e2m1 codes, e4m3 scales per 16 row elements, fp32 per
 # matrix) and MXFP4 (e2m1 codes, e8m0 scales per 32 row elements) ----
 
+@pytest.mark.parametrize("I,T", [(1536, 1), (2048, 1), (1536, 2), (2048, 2)])
+def test_fp8_straight_line_shapes(I, T):
+    # fp8 rows of 96 and 128 16-byte chunks take the straight-line down paths (the
+    # 8-row ring items of the resident grid, the 4-row items of the filled-expert
+    # grid) and the unrolled gate/up loop; B_pcie = B_cpu gives fills, hits and
+    # CPU-assigned pairs in the same calls
+    from workloads import Config, Shape
+    cfg = Config(f"fp8_I{I}_T{T}", Shape(L=3, E=24, k=4, H=1024, I=I, wdtype="fp8", adtype="bf16"), T=T,
+                 steps=16, capacity=24, routing="softmax", seed=97)
+    res = run_decode_parity(cfg, (1000, 1000), n_phys=12, fp_every=1)
+    _ok(res)
+    assert res.fills > 0 and res.cpu_pairs > 0 and res.fp_checked == 16 * 3
+
+
 FP4 = ["nvfp4", "mxfp4"]
 
 @pytest.mark.parametrize("fmt,adtype", [("nvfp4", "bf16"), ("mxfp4", "bf16"), ("mxfp4", "f32")])
