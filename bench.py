@@ -473,7 +473,8 @@ KERNEL_NAMES = {
     "gemv_resident_split": "resident-expert GEMV pair: gate_up_bulk_kernel (with the L2 fetch of W_down) + "
                            "down_bulk_kernel pass 0 fused with the combine",
     "gemv_resident": "resident-expert gate/up grid (gate_up_bulk_kernel)",
-    "down_combine": "down projection of every GPU expert fused with the combine (down_combine_kernel)",
+    "down_combine": "down projection of every GPU expert fused with the combine, one grid after the fills "
+                    "(down_bulk_kernel over all GPU experts, each item's h read through L1)",
 }
 
 

@@ -2344,7 +2344,7 @@ cudaError_t launch_down_split(const Shape& sh, int pass, int T, const float* w, 
 int down_combine_launches(const Shape& sh, int T, int sms) {
   const GemvArgs a = make_args(sh, 2, T, nullptr, DecodeBufs{});
   const BulkGeom geo = down_geom(a, sh.wdtype, sms);
-  if (geo.NS >= 1 && geo.h_smem) return 1;
+  if (geo.NS >= 1) return 1;
   if (down_combine_fits(sh, T) && sh.wdtype != MOE_NVFP4 && sh.wdtype != MOE_MXFP4) return 1;
   return 2;
 }
@@ -2402,9 +2402,13 @@ cudaError_t launch_resident_fused(const Shape& sh, int T, const void* x, const f
 cudaError_t launch_down_combine(const Shape& sh, int T, const float* w, const float* cpu_part, DecodeBufs b,
                                 float* out, uint32_t* err, int sms, cudaStream_t s) {
   {
+    // The bulk down kernel whenever its ring fits.  When not every pair's h fits in
+    // shared memory (more than two tokens at the Qwen3 shape) each warp reads the
+    // h of its item's pairs through L1, once per item of up to kDownRows rows;
+    // down_combine_kernel reads it once per row.
     const GemvArgs a = make_args(sh, 2, T, nullptr, b);
     const BulkGeom geo = down_geom(a, sh.wdtype, sms);
-    if (geo.NS >= 1 && geo.h_smem) return launch_down_bulk_any(sh, a, geo, true, true, w, cpu_part, out, err, s);
+    if (geo.NS >= 1) return launch_down_bulk_any(sh, a, geo, true, true, w, cpu_part, out, err, s);
   }
   if (down_combine_fits(sh, T) && sh.wdtype != MOE_NVFP4 && sh.wdtype != MOE_MXFP4) {
     const GemvArgs a = make_args(sh, 2, T, nullptr, b);

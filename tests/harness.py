@@ -52,7 +52,7 @@ def make_cache(cfg: Config, pool, offs, shared, bw, max_prefill_tokens=0, n_slot
 
 
 def run_decode_parity(cfg: Config, bw, n_phys=None, fp_every=1, fp_limit=None, check_plan=True,
-                      pinned=True, state_every=1, fp_steps=(), memo=16) -> DecodeRun:
+                      pinned=True, state_every=1, fp_steps=(), memo=16, trace=None) -> DecodeRun:
     """Replay cfg's decode trace on the GPU and in the oracle; compare control state bit for bit.
 
     Every call: slot map (bit-exact) and, with check_plan, q / victims / fills.
@@ -61,6 +61,7 @@ def run_decode_parity(cfg: Config, bw, n_phys=None, fp_every=1, fp_limit=None, c
     steps in `fp_steps`: the layer output within TOL, with the CPU-assigned
     pairs' partial sums supplied from the oracle and NaN planted in every entry
     the combine must not read.  `memo`: parsed experts the oracle keeps.
+    `trace`: (ids, gates) replacing cfg's generated routing.
     """
     import torch
     s = cfg.shape
@@ -71,7 +72,7 @@ def run_decode_parity(cfg: Config, bw, n_phys=None, fp_every=1, fp_limit=None, c
     ora = SlotCache(s.L, s.E, cfg.capacity, K, bw[0], bw[1])
     store = ExpertStore(arena, offs, s.wdtype, s.H, s.I, s.blob_bytes, memo=memo)
     fp_steps = set(fp_steps)
-    ids, w = routing_trace(cfg)
+    ids, w = routing_trace(cfg) if trace is None else trace
     res = DecodeRun()
     out = torch.empty(cfg.T, s.H, device=dev)
     sm = torch.empty(cfg.T, s.k, dtype=torch.int32, device=dev)
@@ -130,3 +131,38 @@ def run_decode_parity(cfg: Config, bw, n_phys=None, fp_every=1, fp_limit=None, c
                 return res
     cache.close()
     return res
+
+
+POOL_SHORT_STEP = 7
+
+
+def pool_short_trace(tail_steps=8, seed=95):
+    """A one-layer trace on which the kept pool of the 64 least-recent slots holds
+    fewer evictable slots than the call needs, even after a rebuild.
+
+    100 slots, 128 experts, top-8 over 16 tokens (128 routed pairs), K = 16, so
+    the pool keeps min(C, max(64, 4K)) = 64 keys.  Steps 0-6 fill every slot
+    (experts 0-95 in groups of 16, then 84-99); step POOL_SHORT_STEP routes
+    experts 0-59 (60 hits, all among the 64 least recent) and 100-115 (16
+    misses): 4 evictable pool entries for 16 victims, so the victims come from
+    the selection over all slots.  `tail_steps` steps of random routing follow.
+    Returns (cfg, ids [steps, 1, 16, 8], gates).
+    """
+    from workloads import Shape
+    shape = Shape(L=1, E=128, k=8, H=256, I=128, wdtype="bf16", adtype="bf16")
+    T, k = 16, 8
+    groups = [list(range(b, b + 16)) for b in (0, 16, 32, 48, 64, 80, 84)]
+    groups.append(list(range(60)) + list(range(100, 116)))
+    steps = len(groups) + tail_steps
+    ids = np.empty((steps, 1, T, k), np.int32)
+    for st, grp in enumerate(groups):
+        for t in range(T):
+            ids[st, 0, t] = [grp[(k * t + i) % len(grp)] for i in range(k)]
+    g = np.random.default_rng(seed)
+    for st in range(len(groups), steps):
+        for t in range(T):
+            ids[st, 0, t] = g.choice(shape.E, size=k, replace=False)
+    w = g.dirichlet(np.ones(k), size=(steps, 1, T)).astype(np.float32)
+    cfg = Config("pool_short", shape, T=T, steps=steps, capacity=100, routing="softmax", seed=seed,
+                 max_fetch=16)
+    return cfg, ids, w

@@ -213,6 +213,17 @@ def test_exact_select_path_above_the_pool():
     assert res.fills > 0 and res.cpu_pairs > 0
 
 
+@pytest.mark.parametrize("bw", [(1000, 0), (1000, 1000)])
+def test_pool_short_falls_back_to_selection_over_all_slots(bw):
+    # 60 of the call's hits among the 64 least-recent slots, K = 16: the pool (also
+    # after its rebuild) holds 4 victims, the other 12 come from all slots
+    from tests.harness import pool_short_trace
+    cfg, ids, w = pool_short_trace()
+    res = run_decode_parity(cfg, bw, fp_every=1, trace=(ids, w))
+    _ok(res)
+    assert res.calls == cfg.steps and res.fp_checked == cfg.steps and res.fills > 100
+
+
 def test_random_resizes_grow_and_shrink():
     import torch
     from oracle.cache import SlotCache
@@ -294,6 +305,19 @@ def test_fp8_straight_line_shapes(I, T):
     res = run_decode_parity(cfg, (1000, 1000), n_phys=12, fp_every=1)
     _ok(res)
     assert res.fills > 0 and res.cpu_pairs > 0 and res.fp_checked == 16 * 3
+
+
+@pytest.mark.parametrize("wdtype", ["bf16", "fp8", "f32"])
+def test_h_through_l1_above_two_tokens(wdtype):
+    # 12 tokens x top-8 at I = 512: 96 pairs' h (196 KB in fp32) do not fit in shared
+    # memory, so the bulk down kernel reads each item's h through L1; CPU pairs mixed in
+    from workloads import Config, Shape
+    cfg = Config(f"hl1_{wdtype}", Shape(L=2, E=32, k=8, H=256, I=512, wdtype=wdtype,
+                                        adtype="f32" if wdtype == "f32" else "bf16"),
+                 T=12, steps=10, capacity=40, routing="softmax_bias", bias_std=0.5, seed=98)
+    res = run_decode_parity(cfg, (1000, 1000), fp_every=1)
+    _ok(res)
+    assert res.fills > 0 and res.cpu_pairs > 0 and res.fp_checked == 10 * 2
 
 
 FP4 = ["nvfp4", "mxfp4"]

@@ -221,3 +221,23 @@ def test_cpu_assigned_experts_do_not_enter_the_cache():
     assert p.q == 1 and p.fills == [(0, 0)] and p.cpu == [1, 2, 3]
     assert set(o.slot_of) == {0}
     assert p.slot_map.tolist() == [[0, -1], [-1, -1]]
+
+
+def test_pool_short_trace_needs_victims_beyond_the_pool():
+    # The scripted trace must put more of its hits among the 64 least-recent slots
+    # than 64 - K, so that the GPU test of it reaches the selection over all slots.
+    from tests.harness import POOL_SHORT_STEP, pool_short_trace
+    cfg, ids, _ = pool_short_trace()
+    ora = SlotCache(1, cfg.shape.E, cfg.capacity, cfg.max_fetch, 1000, 0)
+    for st in range(POOL_SHORT_STEP):
+        ora.decode(0, ids[st, 0])
+    assert len(ora.expert_in) == cfg.capacity
+    s2e, stamps, _, _, _ = ora.state()
+    n_pool = min(cfg.capacity, max(64, 4 * cfg.max_fetch))
+    oldest = sorted(range(cfg.capacity), key=lambda s: (int(stamps[s]), s))[:n_pool]
+    routed = set(ids[POOL_SHORT_STEP, 0].ravel().tolist())
+    hits_in_pool = sum(int(s2e[s]) in routed for s in oldest)
+    assert n_pool - hits_in_pool < cfg.max_fetch
+    plan = ora.decode(0, ids[POOL_SHORT_STEP, 0])
+    assert len(plan.hits) == 60 and len(plan.misses) == 16 and plan.q == 16
+    assert len(set(plan.victims) - set(oldest)) == cfg.max_fetch - (n_pool - hits_in_pool)
