@@ -479,10 +479,13 @@ KERNEL_NAMES = {
 
 
 def roofline_from_groups(groups, hbm_peak, peak_src, traffic=None, traffic_source=None, split=None):
-    """The roofline object of the group with the most event time (all are HBM-bound).
+    """The roofline object of the group with the most event time (all are HBM-bound)
+    among those that move bytes: a grid whose expert set is empty (the resident
+    gate/up grid when every read misses) only waits for SMs and has no roofline.
     split: the call took the split down grids (the resident group is the whole pair);
     by default read from the groups (a "down_filled" group exists)."""
-    kind, (b, ms, n) = max(groups.items(), key=lambda kv: kv[1][1])
+    moving = {k: v for k, v in groups.items() if v[0] > 0} or groups
+    kind, (b, ms, n) = max(moving.items(), key=lambda kv: kv[1][1])
     if ms <= 0 or n == 0:
         return None
     if split is None:

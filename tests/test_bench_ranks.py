@@ -37,3 +37,16 @@ def test_reference_arm_two_gloo_ranks_print_one_line():
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["steps"] == 1
     assert d["value"] is not None and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_roofline_skips_a_grid_that_moves_no_bytes():
+    # every read a miss: the resident gate/up grid runs with no experts and only waits
+    # for SMs behind the fill, so the roofline belongs to the down grid
+    sys.path.insert(0, ROOT)
+    import bench
+    groups = {"gemv_resident": (0, 49.0e-3 * 768, 768), "down_combine": (104_185_856 * 768, 45.4e-3 * 768, 768)}
+    r = bench.roofline_from_groups(groups, 6688.8, "of measured")
+    assert r["bytes_per_launch"] == 104_185_856 and r["us_per_launch"] == 45.4
+    assert abs(r["frac"] - 104_185_856 / 45.4e-6 / 1e9 / 6688.8) < 1e-3
+    # with no byte-moving group the largest one still gives the line
+    assert bench.roofline_from_groups({"gemv_resident": (0, 1.0, 4)}, 6688.8, "of measured")["frac"] == 0.0
