@@ -320,6 +320,20 @@ def test_h_through_l1_above_two_tokens(wdtype):
     assert res.fills > 0 and res.cpu_pairs > 0 and res.fp_checked == 10 * 2
 
 
+@pytest.mark.parametrize("T,wdtype", [(128, "bf16"), (160, "bf16"), (128, "nvfp4")])
+def test_down_fallbacks_when_the_ring_does_not_fit(T, wdtype):
+    # H = 8192 gives each down CTA 54 rows; with 1024 or more routed pairs their
+    # partial sums no longer fit in shared memory beside a ring, so the down
+    # projection takes the register-staged kernels: down_combine_kernel up to 1024
+    # pairs, down_kernel + combine_kernel above (and for 4-bit experts)
+    from workloads import Config, Shape
+    cfg = Config(f"fallback_{T}_{wdtype}", Shape(L=1, E=16, k=8, H=8192, I=256, wdtype=wdtype, adtype="bf16"),
+                 T=T, steps=2, capacity=16, routing="softmax", seed=99)
+    res = run_decode_parity(cfg, (1000, 1000), fp_every=1)
+    _ok(res)
+    assert res.fills > 0 and res.cpu_pairs > 0 and res.fp_checked == 2
+
+
 FP4 = ["nvfp4", "mxfp4"]
 
 @pytest.mark.parametrize("fmt,adtype", [("nvfp4", "bf16"), ("mxfp4", "bf16"), ("mxfp4", "f32")])
