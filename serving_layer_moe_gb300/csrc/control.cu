@@ -28,18 +28,19 @@
 // is loaded into shared memory in one parallel pass, so the critical path has
 // a single global-memory round trip; the rest runs out of shared memory.  The
 // routed set is a bitmap over E experts (dedup = atomicOr, order = popcount
-// prefix), hit/miss ranks come from warp ballots.  The K smallest keys (K <=
-// 32) come from one pass in which each warp extracts its own K smallest by
-// repeated warp-minimum (32-bit redux instructions over the high and low words
-// of register-resident keys) and warp 0 merges the sorted per-warp lists; for
-// larger K an MSB radix select with 8-bit digits over the shared keys.  For K <=
-// 16 the kernel keeps, between calls, the 64 smallest keys of its last full
-// selection: since keys only grow, the first valid entries of that pool are
-// the victims, and the full selection reruns only when the pool runs short.
-// Calls of at most 32 routed pairs (decode at small batch) take every step in
-// one warp with ballots, match and warp barriers, after one block barrier that
-// makes the loaded tables visible: 2.6 us less per call than the block-wide
-// steps with their dozen block barriers.
+// prefix), hit/miss ranks come from warp ballots (one thread per expert when
+// the layer's experts fit the CTA).  Victims: for K <= kPoolMaxK the kernel
+// keeps, between calls, the min(C, max(64, 4K)) smallest keys of its last full
+// selection.  Keys only grow, so the first valid entries of that pool that are
+// not this call's hits are the victims; the pool is rebuilt only when it runs
+// short, and if even the rebuilt pool is short (more of this call's hits among
+// its slots than it has room for) the call selects over all slots.  Above
+// kPoolMaxK every call selects over all slots.  Both selections are an MSB
+// radix select with 8-bit digits (keys held in registers up to 8 slots per
+// thread), then a sort of the selected keys.  Calls of at most 32 routed pairs with K <= 16 (decode at
+// small batch) take every step in one warp with ballots, match and warp
+// barriers, after one block barrier that makes the loaded tables visible:
+// 2.6 us less per call than the block-wide steps with their block barriers.
 #include "internal.cuh"
 
 namespace moe {
