@@ -14,15 +14,27 @@
 //
 // GB300 design: decode is a matrix-vector product per expert (a handful of
 // tokens per expert), so it is bound by HBM bandwidth, not by tensor cores.
-// Each warp streams whole weight rows with 16-byte loads (coalesced: lane l
-// reads chunks l, l+32, ...), keeps several rows' loads in flight, and reduces
-// with shuffles.  Work is the flat list of (GPU expert, row) pairs the control
-// kernel published through device-resident counts, spread over a fixed grid of
-// a few CTAs per SM (152 SMs), so launches have fixed shapes and can be graph
-// captured.  The fill copy is an SM copy kernel reading page-locked host memory
-// over the host link (NVLink-C2C on a Grace host), because the fill list is
-// decided on the device and a copy-engine memcpy would need host-known
-// addresses.
+//   * Resident experts: gate_up_bulk_kernel gives every warp a ring of
+//     shared-memory stages that cp.async.bulk fills with whole gate/up row
+//     pairs (mbarrier completion), so each SM keeps ~200 KB of weights in
+//     flight while the warp computes from the previous stage; it also has L2
+//     fetch the same experts' W_down.  down_bulk_kernel then streams W_down
+//     row blocks the same way, one wave of CTAs with R = ceil(H / SMs) rows
+//     each, and fuses the fixed-order combine.
+//   * Filled experts: fill_gate_up_kernel copies each blob from page-locked
+//     host memory (an SM copy over NVLink-C2C, since the fill list is decided
+//     on the device) and computes gate/up on the rows as they pass; a second
+//     down grid on the fill stream takes those experts.  The resident and
+//     filled-expert down grids count their arrivals per row block, and the
+//     second to arrive combines.
+//   * Each pair's y is formed in the same per-lane order and reduction tree on
+//     the ring, no-ring and fused paths, so it is the same bit for bit whichever
+//     of those grids computes it.
+//   * Register-staged gate_up_kernel / down_kernel / down_combine_kernel take
+//     the calls whose x (gate/up) or ring (down) does not fit in shared memory.
+//   * Launch shapes depend only on the cache's shape, never on the plan (the
+//     control kernel publishes it in device memory), so a decode step can be
+//     captured in a CUDA graph.
 #include <vector>
 
 #include "internal.cuh"
