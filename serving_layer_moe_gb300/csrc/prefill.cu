@@ -34,18 +34,25 @@
 // stored as bf16, y = h W_down^T in fp32, out[t] = sum_j w[t,j] y[t,j].
 //
 // GB300 design of the GEMM (one CTA per SM, persistent):
-//   rows of x are gathered per expert into a contiguous bf16 matrix; tiles of
-//   128 rows x 256 columns x 64-deep K slices are staged by TMA (128-byte
-//   swizzle) into a 4-stage shared-memory ring, multiplied by tcgen05.mma
-//   (kind::f16, bf16 in, fp32 accumulate, M=128 N=256 K=16) issued by one
-//   thread into a double-buffered TMEM accumulator (2 x 256 columns), and
-//   drained by four epilogue warps with tcgen05.ld while the next tile's MMAs
-//   run.  The expert's weights are read straight out of its pool slot through
-//   one tensor map over the whole pool (the slot picks the row coordinate).
+//   rows of x are gathered per expert into a contiguous bf16 matrix, and each
+//   expert's rows are cut into 128-row tiles (the last one partial: its
+//   epilogue keeps only the expert's own rows); tiles of 128 rows x 256
+//   columns x 64-deep K slices are staged by TMA (128-byte swizzle) into a
+//   shared-memory ring (4 stages for GEMM 1, 3 for GEMM 2), multiplied by
+//   tcgen05.mma (kind::f16, bf16 in, fp32 accumulate, M=128 N=256 K=16) issued
+//   by one thread into a double-buffered TMEM accumulator (2 x 256 columns),
+//   and drained with tcgen05.ld by 8 (GEMM 1) or 16 (GEMM 2) epilogue warps,
+//   several per 32-lane TMEM quarter, while the next tile's MMAs run.  The
+//   expert's weights are read straight out of its pool slot through one tensor
+//   map over the whole pool (the slot picks the row coordinate).
 //   GEMM 1 (gate|up, N = 128 gate + 128 up columns of the same rows) fuses
 //   SwiGLU into its epilogue and writes h as bf16; GEMM 2 (down) multiplies by
-//   the router gate in its epilogue and accumulates into out with fp32 vector
-//   atomics (the k contributions of a token arrive from k different experts).
+//   the router gate in its epilogue and adds its rows into out with bulk
+//   reductions (cp.reduce.async.bulk .add.f32 of 128-byte row pieces): the k
+//   contributions of a token arrive from k different experts, so their order
+//   varies from run to run.
+//   4-bit experts (NVFP4, MXFP4) are first decoded to a bf16 staging area by
+//   fp4_to_bf16_kernel and the GEMMs read that instead of the pool.
 //   Every wait on an mbarrier is bounded by the GPU global timer; on timeout
 //   the kernel flags the error word, drains its own copies and frees TMEM.
 #include "cache.cuh"
