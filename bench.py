@@ -551,7 +551,8 @@ def main(args):
             print(json.dumps({"fill_step": fill_step_measure(args, dev, bp_gbs)}))
         return
     if args.mode == "workloads":
-        res = {n: decode_workload_measure(n, args, dev, (b_pcie, b_cpu), hbm_peak, peak_src, rank == 0, bp_gbs)
+        res = {n: decode_workload_measure(n, args, dev, (b_pcie, b_cpu), hbm_peak, peak_src,
+                                          rank == 0 and not args.no_cpu_baseline, bp_gbs)
                for n in EXTRA_WORKLOADS}
         if rank == 0:
             print(json.dumps({"workloads": res}))
